@@ -1,0 +1,436 @@
+"""Pins of the CPU oracle against hand-worked values, closed forms, invariants, library routines and brute force.
+
+Each test is chosen so that a plausible slip in the oracle (a transposed operand, a wrong block or scale index, a
+dropped term, a wrong sign, eps outside the root, gate and up swapped, a wrong rotary pairing, an off-by-one expert
+base) fails at least one of them.  No expected value here comes from the CUDA path.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")))
+
+
+# ---- input generator -------------------------------------------------------------------------------------------------
+
+def test_synth_splitmix_reference_value():
+    # SplitMix64 from state 0: the published first output of the generator is 0xE220A8397B1DCDAF; our key for
+    # (seed=0) starts from mix64(0 + GAMMA), which is exactly that output.
+    lib = synth.lib()
+    import ctypes
+    gamma = 0x9E3779B97F4A7C15
+    # key(0, t) = mix64(mix64(GAMMA) + (t+1)*GAMMA); u64(0, t, i) = mix64(key + (i+1)*GAMMA).  With the public
+    # first output M0 = mix64(GAMMA), draw i of tensor t equals mix64(M0 + (t+1)*GAMMA) fed back once more; check the
+    # relation on the first draw through an independent Python mix64.
+    def mix64(z):
+        m = (1 << 64) - 1
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & m
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & m
+        return z ^ (z >> 31)
+    assert mix64(gamma) == 0xE220A8397B1DCDAF
+    assert mix64((2 * gamma) & ((1 << 64) - 1)) == 0x6E789E6AA1B965F4
+    key = mix64((mix64(gamma) + gamma) & ((1 << 64) - 1))
+    for i in range(4):
+        assert synth.u64(0, 0, i) == mix64((key + (i + 1) * gamma) & ((1 << 64) - 1))
+    del lib, ctypes
+
+
+def test_synth_distributions_and_thread_independence():
+    q = synth.int8(1 << 18, seed=0, tensor=3)
+    assert q.min() == -127 and q.max() == 127
+    assert abs(q.mean()) < 1.0
+    z = synth.normal(1 << 18, seed=0, tensor=4)
+    assert abs(z.mean()) < 0.01 and abs(z.std() - 1.0) < 0.01
+    s = synth.normal(1000, seed=0, tensor=5, mul=0.01, absval=True)
+    assert (s >= 0).all() and abs(s.mean() - 0.01 * math.sqrt(2 / math.pi)) < 5e-4
+    # an offset window reproduces the same elements
+    a = synth.normal(100, seed=1, tensor=9)
+    b = synth.normal(40, seed=1, tensor=9, offset=30)
+    np.testing.assert_array_equal(a[30:70], b)
+    old = synth.THREADS
+    try:
+        synth.THREADS = 1
+        one = synth.normal(1 << 17, seed=2, tensor=1)
+        synth.THREADS = 7
+        many = synth.normal(1 << 17, seed=2, tensor=1)
+    finally:
+        synth.THREADS = old
+    np.testing.assert_array_equal(one, many)
+
+
+# ---- Q8_0 dequant and the f32-activation product -------------------------------------------------------------------
+
+def test_q8_gemv_hand_example():
+    g = GOLD["q8_gemv_hand"]
+    q = np.array(g["q"], np.int8)
+    s = np.array(g["s"], np.float32)
+    x = np.array(g["x"], np.float32)
+    assert oracle.gemv_f32act(q, s, x).tolist() == g["y"]
+    assert oracle.weight(q, s, 1, 40) == 2.0 * 1  # q1[40] = (-1)^40 = 1, block 1 scale 2.0
+    assert oracle.weight(q, s, 0, 31) == 32 * 0.5
+
+
+def test_q8_gemv_closed_form_constant():
+    n, k = 3, 96
+    q = np.full((n, k), -7, np.int8)
+    s = np.full((n, k // 32), 0.125, np.float32)
+    x = np.full(k, 3.0, np.float32)
+    assert np.all(oracle.gemv_f32act(q, s, x) == k * -7 * 0.125 * 3.0)
+
+
+def test_q8_gemv_unit_scales_is_integer_matmul():
+    # special case: scales 1 and integer activations reduce the product to an exact integer matmul (numpy)
+    q = synth.int8((37, 160), seed=0, tensor=11)
+    x = (synth.int8(160, seed=0, tensor=12) // 4).astype(np.float32)
+    s = np.ones((37, 5), np.float32)
+    ref = q.astype(np.int64) @ x.astype(np.int64)
+    assert np.array_equal(oracle.gemv_f32act(q, s, x), ref.astype(np.float64))
+
+
+def test_q8_dequant_matches_numpy_expansion_and_matmul():
+    q, s = synth.q8_matrix(29, 128, seed=0, tensor=13)
+    x = synth.normal(128, seed=0, tensor=14)
+    w = oracle.dequant(q, s)
+    np.testing.assert_array_equal(w, q.astype(np.float64) * np.repeat(s.astype(np.float64), 32, axis=1))
+    y = oracle.gemv_f32act(q, s, x)
+    ref = w @ x.astype(np.float64)
+    assert np.max(np.abs(y - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_q8_gemv_exact_rational_brute_force():
+    q, s = synth.q8_matrix(3, 64, seed=5, tensor=15)
+    x = synth.normal(64, seed=5, tensor=16)
+    y = oracle.gemv_f32act(q, s, x)
+    for o in range(3):
+        exact = sum(Fraction(int(q[o, t])) * Fraction(float(s[o, t // 32])) * Fraction(float(x[t])) for t in range(64))
+        bound = 64 * 2.0 ** -52 * sum(abs(float(q[o, t]) * float(s[o, t // 32]) * float(x[t])) for t in range(64))
+        assert abs(Fraction(float(y[o])) - exact) <= Fraction(bound)
+
+
+# ---- activation quantisation ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["quantize_ties", "quantize_zero_block", "quantize_single"])
+def test_quantize_hand_blocks(name):
+    g = GOLD[name]
+    xq, xs = oracle.quantize(np.array(g["x"], np.float32))
+    assert xq.tolist() == g["q"]
+    if "d" in g:
+        assert xs[0] == np.float32(g["d"])
+
+
+def test_quantize_invariants():
+    x = synth.normal((64, 256), seed=0, tensor=17, mul=3.0)
+    xq, xs = oracle.quantize(x)
+    blocks = x.reshape(64, 8, 32)
+    qb = xq.reshape(64, 8, 32).astype(np.int32)
+    amax = np.abs(blocks).max(-1)
+    np.testing.assert_array_equal(xs, (amax / np.float32(127)).astype(np.float32))
+    assert np.abs(qb).max() <= 127
+    # the largest magnitude of every block maps to +-127 with its sign
+    idx = np.abs(blocks).argmax(-1)
+    top = np.take_along_axis(qb, idx[..., None], -1)[..., 0]
+    sign = np.sign(np.take_along_axis(blocks, idx[..., None], -1)[..., 0])
+    np.testing.assert_array_equal(top, (127 * sign).astype(np.int32))
+    # reconstruction within half a step (plus one f32 rounding of the quotient)
+    err = np.abs(blocks - qb * xs[..., None])
+    assert np.all(err <= xs[..., None] * (0.5 + 1e-6))
+
+
+# ---- int8-activation product ---------------------------------------------------------------------------------------
+
+def test_blockdots_library_and_bounds():
+    q = synth.int8((17, 192), seed=0, tensor=18)
+    xq = synth.int8(192, seed=0, tensor=19)
+    D = oracle.blockdots(q, xq)
+    ref = (q.reshape(17, 6, 32).astype(np.int64) * xq.reshape(6, 32).astype(np.int64)).sum(-1)
+    np.testing.assert_array_equal(D, ref)
+    full = np.full((1, 32), 127, np.int8)
+    assert oracle.blockdots(full, np.full(32, -127, np.int8))[0, 0] == -516128
+
+
+def test_gemv_int8act_unit_scales_and_scaled():
+    q = synth.int8((9, 64), seed=1, tensor=20)
+    xq = synth.int8(64, seed=1, tensor=21)
+    ones_w = np.ones((9, 2), np.float32)
+    ones_x = np.ones(2, np.float32)
+    ref = q.astype(np.int64) @ xq.astype(np.int64)
+    np.testing.assert_array_equal(oracle.gemv_int8act(q, ones_w, xq, ones_x), ref.astype(np.float64))
+    # per-block scales: block 0 x2 on the weights, block 1 x0.5 on the activation
+    sw = np.array([[2.0, 1.0]] * 9, np.float32)
+    sx = np.array([1.0, 0.5], np.float32)
+    D = oracle.blockdots(q, xq)
+    np.testing.assert_array_equal(oracle.gemv_int8act(q, sw, xq, sx), 2.0 * D[:, 0] + 0.5 * D[:, 1])
+
+
+def test_gemv_mode1_is_quantize_then_int8():
+    q, s = synth.q8_matrix(11, 96, seed=2, tensor=22)
+    x = synth.normal(96, seed=2, tensor=23)
+    xq, xs = oracle.quantize(x)
+    np.testing.assert_array_equal(oracle.gemv(1, q, s, x), oracle.gemv_int8act(q, s, xq, xs))
+    np.testing.assert_array_equal(oracle.gemv(0, q, s, x), oracle.gemv_f32act(q, s, x))
+    # the two modes differ by the activation quantisation error only (bounded by half a step per value)
+    y0, y1 = oracle.gemv(0, q, s, x), oracle.gemv(1, q, s, x)
+    w = np.abs(oracle.dequant(q, s))
+    bound = w @ np.repeat(xs, 32).astype(np.float64) * 0.5 * (1 + 1e-6)
+    assert np.all(np.abs(y0 - y1) <= bound)
+
+
+# ---- add + RMSNorm -------------------------------------------------------------------------------------------------
+
+def test_rmsnorm_hand_and_eps():
+    g = GOLD["rmsnorm_hand"]
+    s, y = oracle.add_rmsnorm(np.array(g["a"]), np.array(g["b"]), np.array(g["w"]), g["eps"])
+    assert s[0].tolist() == g["s"]
+    np.testing.assert_allclose(y[0], g["y"], rtol=1e-15)
+    g = GOLD["rmsnorm_eps_inside"]
+    _, y = oracle.add_rmsnorm(np.array(g["a"]), None, np.array(g["w"]), g["eps"])
+    assert y[0].tolist() == g["y"]
+
+
+def test_rmsnorm_sum_is_f32_add_and_unit_rms():
+    a = synth.normal((5, 2048), seed=0, tensor=24)
+    b = synth.normal((5, 2048), seed=0, tensor=25)
+    s, y = oracle.add_rmsnorm(a, b, np.ones(2048, np.float32), 0.0)
+    np.testing.assert_array_equal(s, a + b)  # numpy f32 addition, one rounding
+    np.testing.assert_allclose(np.sqrt((y ** 2).mean(-1)), 1.0, rtol=1e-13)
+    # constant rows: y = w * sign(c) / sqrt(1 + eps / c^2)
+    c = np.float32(-1.5)
+    _, y = oracle.add_rmsnorm(np.full((1, 64), c, np.float32), None, np.full(64, 2.0, np.float32), 0.25)
+    np.testing.assert_allclose(y, 2.0 * -1.0 / math.sqrt(1 + 0.25 / 2.25), rtol=1e-15)
+
+
+# ---- router ---------------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["route_hand", "route_ties"])
+def test_route_hand(name):
+    g = GOLD[name]
+    ids, gates = oracle.route(np.array(g["logits"]), g["k"])
+    assert ids.tolist() == g["ids"]
+    np.testing.assert_allclose(gates, g["gates"], rtol=1e-14)
+
+
+def test_route_brute_force_and_invariants():
+    rng_logits = synth.normal((50, 12), seed=3, tensor=26, mul=4.0).astype(np.float64)
+    for l in rng_logits:
+        for k in (1, 3, 12):
+            ids, g = oracle.route(l, k)
+            order = sorted(range(12), key=lambda i: (-l[i], i))[:k]
+            assert ids.tolist() == order
+            assert abs(g.sum() - 1.0) < 1e-14
+            p = np.exp(l - l.max())
+            np.testing.assert_allclose(g, p[order] / p[order].sum(), rtol=1e-13)
+    ids, g = oracle.route(np.zeros(8), 8)
+    assert ids.tolist() == list(range(8))
+    np.testing.assert_allclose(g, 1 / 8, rtol=1e-15)
+
+
+def test_silu_values():
+    g = GOLD["silu"]
+    for z, y in zip(g["z"], g["y"]):
+        assert oracle.silu(z) == pytest.approx(y, rel=1e-15, abs=0)
+    assert oracle.silu(-800.0) == 0.0 and math.copysign(1.0, oracle.silu(-800.0)) == -1.0
+
+
+# ---- the mixture ---------------------------------------------------------------------------------------------------
+
+def _zeros_q8(n, k):
+    return np.zeros((n, k), np.int8), np.zeros((n, k // 32), np.float32)
+
+
+def _ident_q8(n, val=1, scale=1.0):
+    q = np.zeros((n, n), np.int8)
+    np.fill_diagonal(q, val)
+    return q, np.full((n, n // 32), scale, np.float32)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_moe_identity_expert_closed_form(mode):
+    # E=3, K=1; the router row of expert 2 is the only non-zero one (x has a positive sum) so expert 2 is kept with
+    # gate 1.  Expert 2: gate = 127*0.01*I, up = I, down = I; experts 0 and 1 are zero.  Then
+    #   y = silu(1.27 x) * x     (mode 0),  and the same on the quantized x in mode 1.
+    d = dff = 32
+    E = 3
+    router_q = np.zeros((E, d), np.int8)
+    router_q[2] = 1
+    router = (router_q, np.ones((E, 1), np.float32))
+    gq, gs = np.zeros((E * dff, d), np.int8), np.zeros((E * dff, 1), np.float32)
+    uq, us = gq.copy(), gs.copy()
+    dq, ds = np.zeros((E * d, dff), np.int8), np.zeros((E * d, 1), np.float32)
+    gq[2 * dff:3 * dff], gs[2 * dff:3 * dff] = _ident_q8(32, 127, 0.01)
+    uq[2 * dff:3 * dff], us[2 * dff:3 * dff] = _ident_q8(32)
+    dq[2 * d:3 * d], ds[2 * d:3 * d] = _ident_q8(32)
+    w = oracle.MoeWeights(d, dff, E, 1, router, (gq, gs), (uq, us), (dq, ds))
+    x = np.abs(synth.normal(d, seed=0, tensor=27)) + 0.1
+    out = oracle.moe_rows(mode, w, x)
+    assert out["ids"][0].tolist() == [2] and out["gates"][0, 0] == 1.0
+    if mode == 0:
+        xv = x.astype(np.float64)
+        gv = np.float64(np.float32(0.01)) * 127 * xv
+        h = gv / (1 + np.exp(-gv)) * xv
+        np.testing.assert_allclose(out["hidden"][0, 0], h, rtol=1e-14)
+        np.testing.assert_allclose(out["y"][0], h.astype(np.float32).astype(np.float64), rtol=1e-14)
+    else:
+        xq, xs = oracle.quantize(x)
+        xv = xq.astype(np.float64) * np.float64(xs[0])
+        gv = np.float64(np.float32(0.01)) * 127 * xv
+        h = gv / (1 + np.exp(-gv)) * xv
+        np.testing.assert_allclose(out["hidden"][0, 0], h, rtol=1e-14)
+        hq, hs = oracle.quantize(h.astype(np.float32))
+        np.testing.assert_allclose(out["y"][0], hq.astype(np.float64) * np.float64(hs[0]), rtol=1e-14)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_moe_equal_gates_all_experts_is_mean_expert(mode):
+    # spec invariant: with K = E and equal router logits the mixture equals the mean of the experts' outputs
+    d, dff, E = 64, 32, 4
+    router = _zeros_q8(E, d)
+    gate = synth.q8_matrix(E * dff, d, seed=1, tensor=30)
+    up = synth.q8_matrix(E * dff, d, seed=1, tensor=31)
+    down = synth.q8_matrix(E * d, dff, seed=1, tensor=32)
+    w = oracle.MoeWeights(d, dff, E, E, router, gate, up, down)
+    x = synth.normal(d, seed=1, tensor=33)
+    res = synth.normal(d, seed=1, tensor=34)
+    out = oracle.moe_rows(mode, w, x, residual=res)
+    assert out["ids"][0].tolist() == list(range(E))
+    np.testing.assert_allclose(out["gates"][0], 0.25, rtol=1e-15)
+    mean = out["expert_out"][0].mean(0)
+    np.testing.assert_allclose(out["y"][0], res + mean, rtol=1e-12, atol=1e-12 * np.abs(mean).max())
+    # each expert's output is its own down . (silu(gate . x) * (up . x)) at the stacked base e*dff / e*d
+    for e in range(E):
+        gv = oracle.gemv(mode, gate[0][e * dff:(e + 1) * dff], gate[1][e * dff:(e + 1) * dff], x)
+        uv = oracle.gemv(mode, up[0][e * dff:(e + 1) * dff], up[1][e * dff:(e + 1) * dff], x)
+        h = gv / (1 + np.exp(-gv)) * uv
+        ye = oracle.gemv(mode, down[0][e * d:(e + 1) * d], down[1][e * d:(e + 1) * d], h.astype(np.float32))
+        np.testing.assert_allclose(out["expert_out"][0, e], ye, rtol=1e-13, atol=1e-13 * np.abs(ye).max())
+
+
+def test_group_brute_force():
+    ids = (synth.int8((13, 5), seed=4, tensor=35).astype(np.int32) + 127) % 9
+    counts, offsets, lists = oracle.group(ids, 9)
+    flat = ids.reshape(-1)
+    np.testing.assert_array_equal(counts, np.bincount(flat, minlength=9))
+    assert offsets[0] == 0 and offsets[-1] == flat.size
+    np.testing.assert_array_equal(lists, np.argsort(flat, kind="stable"))
+
+
+# ---- decode-step pieces --------------------------------------------------------------------------------------------
+
+def test_rope_pairs_and_norm():
+    g = GOLD["rope_pairs"]
+    y = oracle.rope(g["x"], g["pos"], g["theta"])
+    np.testing.assert_allclose(y, g["y"], rtol=1e-15, atol=1e-16)
+    x = synth.normal(128, seed=0, tensor=36).astype(np.float64)
+    y = oracle.rope(x, 4095, 1e6)
+    np.testing.assert_allclose(x[:64] ** 2 + x[64:] ** 2, y[:64] ** 2 + y[64:] ** 2, rtol=1e-12)
+    np.testing.assert_array_equal(oracle.rope(x, 0, 1e6), x)
+
+
+def test_attention_hand_and_invariants():
+    g = GOLD["attention_hand"]
+    out = oracle.attention(g["q"], np.array(g["k"], np.float32), np.array(g["v"], np.float32))
+    np.testing.assert_allclose(out, g["out"], rtol=1e-14)
+    q = synth.normal(128, seed=0, tensor=37).astype(np.float64)
+    v1 = synth.normal((1, 128), seed=0, tensor=38)
+    np.testing.assert_allclose(oracle.attention(q, synth.normal((1, 128), seed=0, tensor=39), v1), v1[0], rtol=1e-15)
+    v = synth.normal((7, 128), seed=0, tensor=40)
+    kc = np.repeat(synth.normal((1, 128), seed=0, tensor=41), 7, axis=0)
+    np.testing.assert_allclose(oracle.attention(q, kc, v), v.astype(np.float64).mean(0), rtol=1e-12, atol=1e-14)
+
+
+def test_rmsnorm_head_and_argmax():
+    y = oracle.rmsnorm_head(np.full(128, 3.0), np.full(128, 0.5, np.float32), 0.0)
+    np.testing.assert_allclose(y, 0.5, rtol=1e-15)
+    assert oracle.argmax(np.array([1.0, 7.0, 3.0, 7.0])) == 1
+
+
+def _tiny_model(seed, layers=2, d=64, heads=4, kv=2, hd=32, dff=32, E=4, K=2, vocab=96, ctx=8, zero_attn=False):
+    cfg = dict(layers=layers, d=d, heads=heads, kv_heads=kv, hd=hd, vocab=vocab, ctx=ctx, eps=1e-6, rope_theta=1e6,
+               dff=dff, experts=E, k=K)
+    t = iter(range(1000))
+
+    def m(n, k):
+        q, s = synth.q8_matrix(n, k, seed, next(t))
+        if zero_attn:
+            s = np.zeros_like(s)
+        return q, s
+
+    def nrm(n):
+        return synth.normal(n, seed, 2000 + next(t), mul=0.1, add=1.0)
+
+    arrays = dict(
+        embed=synth.normal((vocab, d), seed, 3000), attn_norm=[nrm(d) for _ in range(layers)],
+        ffn_norm=[nrm(d) for _ in range(layers)], q_norm=[nrm(hd) for _ in range(layers)],
+        k_norm=[nrm(hd) for _ in range(layers)], final_norm=nrm(d),
+        wq=[m(heads * hd, d) for _ in range(layers)], wk=[m(kv * hd, d) for _ in range(layers)],
+        wv=[m(kv * hd, d) for _ in range(layers)], wo=[m(d, heads * hd) for _ in range(layers)],
+        router=[m(E, d) for _ in range(layers)], gate=[m(E * dff, d) for _ in range(layers)],
+        up=[m(E * dff, d) for _ in range(layers)], down=[m(E * d, dff) for _ in range(layers)],
+        lm_head=synth.q8_matrix(vocab, d, seed, 999),
+        k_cache=[synth.normal((kv, ctx, hd), seed, 4000 + i) for i in range(layers)],
+        v_cache=[synth.normal((kv, ctx, hd), seed, 5000 + i) for i in range(layers)],
+    )
+    return cfg, arrays
+
+
+def test_decode_step_zero_blocks_reduce_to_lm_head_of_normed_embedding():
+    # all attention and mixture scales zero: every block adds zero, so the logits are the LM head of the final norm of
+    # the embedding row, and the new cache rows are zero (the per-head norm of a zero vector is zero)
+    cfg, arr = _tiny_model(7, zero_attn=True)
+    model = oracle.ModelArrays(cfg, **arr)
+    tok, pos = 5, 6
+    nxt, logits = oracle.decode_step(0, model, tok, pos)
+    _, n = oracle.add_rmsnorm(arr["embed"][tok], None, arr["final_norm"], cfg["eps"])
+    ref = oracle.gemv(0, *arr["lm_head"], n[0].astype(np.float32))
+    np.testing.assert_array_equal(logits, ref)
+    assert nxt == int(np.argmax(ref))
+    for l in range(cfg["layers"]):
+        assert not model.k_cache[l][:, pos].any() and not model.v_cache[l][:, pos].any()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_decode_step_matches_composition_of_pinned_pieces(mode):
+    # the step's wiring, recomposed in Python from the pieces pinned above, in the pages' order
+    cfg, arr = _tiny_model(11)
+    model = oracle.ModelArrays(cfg, **arr)
+    kc = [c.copy() for c in arr["k_cache"]]
+    vc = [c.copy() for c in arr["v_cache"]]
+    tok, pos = 17, 5
+    nxt, logits = oracle.decode_step(mode, model, tok, pos)
+    d, H, KV, hd, eps = cfg["d"], cfg["heads"], cfg["kv_heads"], cfg["hd"], cfg["eps"]
+    h = arr["embed"][tok].copy()
+    moe_out = None
+    for l in range(cfg["layers"]):
+        h, n = oracle.add_rmsnorm(h, moe_out, arr["attn_norm"][l], eps)
+        h, x = h[0], n[0].astype(np.float32)
+        q = oracle.gemv(mode, *arr["wq"][l], x).reshape(H, hd)
+        k = oracle.gemv(mode, *arr["wk"][l], x).reshape(KV, hd)
+        v = oracle.gemv(mode, *arr["wv"][l], x).reshape(KV, hd)
+        q = np.stack([oracle.rope(oracle.rmsnorm_head(qh, arr["q_norm"][l], eps), pos, 1e6) for qh in q])
+        k = np.stack([oracle.rope(oracle.rmsnorm_head(kh, arr["k_norm"][l], eps), pos, 1e6) for kh in k])
+        kc[l][:, pos] = k.astype(np.float32)
+        vc[l][:, pos] = v.astype(np.float32)
+        att = np.concatenate([oracle.attention(q[i], kc[l][i // (H // KV), :pos + 1], vc[l][i // (H // KV), :pos + 1])
+                              for i in range(H)])
+        o = oracle.gemv(mode, *arr["wo"][l], att.astype(np.float32)).astype(np.float32)
+        h, n2 = oracle.add_rmsnorm(h, o, arr["ffn_norm"][l], eps)
+        h = h[0]
+        w = oracle.MoeWeights(d, cfg["dff"], cfg["experts"], cfg["k"], arr["router"][l], arr["gate"][l],
+                              arr["up"][l], arr["down"][l])
+        moe_out = oracle.moe_rows(mode, w, n2[0].astype(np.float32))["y"][0].astype(np.float32)
+    h = h + moe_out
+    _, nf = oracle.add_rmsnorm(h, None, arr["final_norm"], eps)
+    ref = oracle.gemv(mode, *arr["lm_head"], nf[0].astype(np.float32))
+    np.testing.assert_array_equal(logits, ref)
+    assert nxt == oracle.argmax(ref)
+    for l in range(cfg["layers"]):
+        np.testing.assert_array_equal(model.k_cache[l], kc[l])
+        np.testing.assert_array_equal(model.v_cache[l], vc[l])
