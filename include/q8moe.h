@@ -1,0 +1,210 @@
+/*
+ * q8moe — C ABI of a GB300 (sm_103a) Q8_0 mixture-of-experts decode step.
+ *
+ * The calls compute the batch-1 (and small-chunk) decode step of a Q8_0-quantized transformer whose feed-forward block
+ * is a sparse mixture of experts.  They follow the pages of the "logicaffeine_compile/codegen_cuda" documentation:
+ *   - forward_shim.rs (module docs; kernel_refusal; ForwardShim::supports / numerics / activation),
+ *   - lane_link.rs (Link::prim: the Gemv, Norm, Moe, Rope, Attention, ArgMax launch records),
+ *   - lane/mod.rs (module docs: the three projection numerics),
+ *   - lane/arena.rs (scratch: arrival counters that are zero before and after a launch),
+ *   - qwen_emit module docs (Q8Ref, MoeWeights, Q8MatKind, emit_moe_forward, emit_qwen30b_generate).
+ *
+ * Conventions shared by every call:
+ *   - Pointers named as device pointers must be device memory of the current device (or managed memory); host
+ *     pointers are named as such.  Every buffer is owned by the caller; the library owns only the workspace and the
+ *     decode model's internal buffers and graphs.
+ *   - Layouts are dense and row-major.  A Q8_0 matrix of `rows` x `cols` is two arrays: int8 quants q[rows*cols]
+ *     (row o at q + o*cols) and f32 block scales s[rows*(cols/32)] (qwen_emit, Q8Ref:
+ *     W[o][t] = q[o*cols + t] * s[o*(cols/32) + t/32]).  cols must be a multiple of 32; q must be 32-byte aligned and s
+ *     4-byte aligned.
+ *   - A quantized activation (one int8 word per value plus one f32 scale per 32-value block; lane/mod.rs module docs,
+ *     "llama.cpp's one int8 word") of R rows x C values is q[R*C] int8 and s[R*(C/32)] f32, q 32-byte aligned.
+ *     Quantisation rule: d = max|x|/127 over the block; word = round-half-away-from-zero(x/d) clamped to +-127, both
+ *     divisions IEEE f32; a block of zeros has d = 0 and zero words.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream), allocates nothing,
+ *     never synchronizes and never reads device memory back to the host, so every call but the first decode_step can
+ *     be captured into a CUDA graph.
+ *   - Arguments are checked before any launch.  A bad argument returns Q8_EINVAL (Q8_EUNSUPPORTED for a shape the
+ *     kernels refuse, as kernel_refusal does in forward_shim.rs) and launches nothing; q8_last_error() names the
+ *     argument.  A CUDA launch error returns Q8_ECUDA.  Errors raised later on the device surface at the caller's next
+ *     synchronization as CUDA errors.
+ *   - Calls that take a workspace use its scratch and its arrival counters.  Calls sharing one workspace must be
+ *     ordered (one stream, or events); two calls that overlap on the device through one workspace race.
+ */
+#ifndef Q8MOE_H
+#define Q8MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define Q8_API __attribute__((visibility("default")))
+#else
+#define Q8_API
+#endif
+
+typedef struct CUstream_st *q8_stream; /* cudaStream_t */
+
+typedef enum {
+    Q8_OK = 0,
+    Q8_EINVAL = -1,       /* a null, misaligned or out-of-range argument */
+    Q8_EUNSUPPORTED = -2, /* a shape the kernels refuse (cols % 32, K outside [1,32], more than 8192 experts, ...) */
+    Q8_ECUDA = -3,        /* a CUDA runtime error (launch, capture, allocation at create time) */
+    Q8_ETIMEOUT = -4,     /* reserved: a bounded device-side wait gave up */
+    Q8_ENOSPACE = -5      /* the workspace is too small for the call */
+} q8_status;
+
+/* The projection numerics (lane/mod.rs module docs; forward_shim.rs, ForwardShim::numerics):
+ *   Q8_F32ACT_F64SUM — f32 activations times dequantized int8 weights, each 32-block's f32 partial sum added into an
+ *                      f64 accumulator (qwen_emit, emit_moe_forward: "f32 activation x int8 weight, f64 accumulate");
+ *   Q8_INT8ACT       — the activation quantized to one int8 word per value; each 32-block's exact int32 dot is
+ *                      scaled by both block scales and summed in f32. */
+typedef enum { Q8_F32ACT_F64SUM = 0, Q8_INT8ACT = 1 } q8_mode;
+
+/* A device Q8_0 matrix (see the layout above). */
+typedef struct {
+    const int8_t *q;
+    const float *s;
+    int64_t rows, cols;
+} q8_mat;
+
+/* A device quantized activation (see the layout above). */
+typedef struct {
+    int8_t *q;
+    float *s;
+} q8_act;
+
+/* ---- workspace ------------------------------------------------------------------------------------------------ */
+typedef struct q8_ws q8_ws;
+
+/* Allocates a workspace on the current device: `bytes` of scratch (0 picks 64 MiB) plus a zeroed array of arrival
+ * counters.  Counters are zero between calls: the last block of a launch to arrive resets them (lane/arena.rs,
+ * Scratch: "a counter ... is zero before the launch and left zero by it").  Returns Q8_ECUDA if allocation fails. */
+Q8_API int q8_workspace_create(size_t bytes, q8_ws **ws);
+Q8_API void q8_workspace_destroy(q8_ws *ws);
+Q8_API size_t q8_workspace_bytes(const q8_ws *ws);
+
+/* ---- a1 / K4: quantisation and the residual add + RMSNorm -------------------------------------------------------- */
+
+/* Quantizes x (device f32, rows x cols, cols % 32 == 0) to out (lane_link.rs, Link::prim: the standalone Quant
+ * launch). */
+Q8_API int q8_quantize(const float *x, int64_t rows, int64_t cols, const q8_act *out, q8_stream stream);
+
+/* Fused residual add + RMSNorm with an int8 epilogue (forward_shim.rs module docs: "a sum and the RMS norm of it ... as
+ * one row kernel writing the sum on"; "the activation a Q8_0 projection reads quantized in its producer's epilogue").
+ * For each of `rows` rows of d values (device f32):
+ *     s = a + b (one f32 add; b may be NULL: s = a)           -> sum_out (may be NULL; may alias a)
+ *     y = s / sqrt(mean(s^2) + eps) * w   (the norm in f64, y rounded once to f32)  -> y_out (may be NULL)
+ *     yq = quantize(y)                                         -> yq (may be NULL; needs d % 32 == 0)
+ * w is device f32 [d].  At least one output must be given.  eps >= 0. */
+Q8_API int add_rmsnorm_q8(const float *a, const float *b, const float *w, int64_t rows, int64_t d, float eps, float *sum_out,
+                   float *y_out, const q8_act *yq, q8_stream stream);
+
+/* ---- a2-a4: the Q8_0 projection ----------------------------------------------------------------------------------- */
+
+/* y[r][o] = sum_t W[o][t] * x[r][t] for r < rows (lane_link.rs, Link::prim: Gemv{x, w, y, k, n, m}; qwen_emit, Q8Ref).
+ * mode Q8_F32ACT_F64SUM reads x (device f32 [rows][W.cols]); mode Q8_INT8ACT reads xq ([rows][W.cols] words plus
+ * scales) or, when xq is NULL, quantizes x first into workspace scratch.  y is device f32 [rows][W.rows].  Matrices
+ * whose rows under-fill the GPU are cut along k; the partial sums meet in workspace scratch and the last slice to
+ * arrive adds them in slice order (lane_link.rs, Link::prim: gemm_blk_tail; lane/arena.rs: the tp/tc scratch). */
+Q8_API int q8_gemv(const q8_mat *W, q8_mode mode, const float *x, const q8_act *xq, int64_t rows, float *y, q8_ws *ws,
+            q8_stream stream);
+
+/* Debug export of the int8 path: the q8_gemv call in Q8_INT8ACT mode (y as above) that also writes
+ * dots[r][o][b] = the exact int32 dot of weight block (o, b) with activation block (r, b), from the same device code.
+ * dots is device int32 [rows][W.rows][W.cols/32]. */
+Q8_API int q8_gemv_blockdots(const q8_mat *W, const q8_act *xq, int64_t rows, int32_t *dots, float *y, q8_ws *ws,
+                      q8_stream stream);
+
+/* ---- a5-a8: the sparse mixture ------------------------------------------------------------------------------------ */
+
+/* Grouping of a chunk's choices by expert (lane_link.rs, Link::class_launch: MoeTokenSort; lane/arena.rs, scratch:
+ * ec/eo/el): counts[e] choices of expert e, offsets[e] = sum of counts before e (offsets[experts] = rows*k), and
+ * lists[offsets[e] .. offsets[e+1]) the choice indices r*k + j of expert e in ascending order.  Device int32 arrays. */
+typedef struct {
+    int32_t *counts;  /* [experts] */
+    int32_t *offsets; /* [experts + 1] */
+    int32_t *lists;   /* [rows * k] */
+    int32_t *active;  /* [experts + 1]: the number of experts with choices, then those experts ascending */
+} q8_moe_plan;
+
+/* Router and top-k (forward_shim.rs, kernel_refusal Moe arms; lane_link.rs, Link::prim Moe: k <= 32, experts <= 8192):
+ * l = router . x_r (the projection in `mode`), p = softmax(l), the k largest kept in descending order (equal logits:
+ * lower expert first), g_j = p_j / sum of the kept p.  ids: device int32 [rows][k]; gates: device f32 [rows][k];
+ * logits: device f32 [rows][experts] or NULL; plan: filled when not NULL.  experts = router->rows. */
+Q8_API int moe_route_topk(const q8_mat *router, q8_mode mode, const float *x, const q8_act *xq, int64_t rows, int k,
+                   int32_t *ids, float *gates, float *logits, const q8_moe_plan *plan, q8_ws *ws, q8_stream stream);
+
+/* Gate-up with SwiGLU (qwen_emit, MoeWeights: gate/up [E*dff, d] stacked, expert e's rows at e*dff; emit_moe_forward:
+ * each expert's SwiGLU at an expert-indexed base): h[r][j][i] = silu(Wg[e*dff+i] . x_r) * (Wu[e*dff+i] . x_r) with
+ * e = ids[r][j], silu(z) = z/(1+e^-z).  h: device f32 [rows][k][dff].  In Q8_INT8ACT mode hq (device, words
+ * [rows*k*dff] + scales [rows*k*dff/32]) receives quantize(h) (dff % 32 == 0); in the other mode hq may be NULL.
+ * plan (from moe_route_topk) is required when rows > 1: each expert's weights are then read once for all its rows. */
+Q8_API int moe_gate_up(const q8_mat *gate, const q8_mat *up, int64_t dff, q8_mode mode, const float *x, const q8_act *xq,
+                int64_t rows, int k, const int32_t *ids, const q8_moe_plan *plan, float *h, const q8_act *hq,
+                q8_ws *ws, q8_stream stream);
+
+/* Down-and-combine (qwen_emit, MoeWeights: down [E*d, dff] stacked, expert e's rows at e*d; emit_moe_forward: the
+ * weighted combine): y[r] = residual[r] + sum_j gates[r][j] * (Wd[e*d .. e*d+d) . h[r][j]), the sum over j in order.
+ * Mode Q8_F32ACT_F64SUM reads h; mode Q8_INT8ACT reads hq.  residual may be NULL (and may alias y); y is device f32
+ * [rows][d]; expert_out (device f32 [rows][k][d] or NULL) receives each expert's unweighted output. */
+Q8_API int moe_down_combine(const q8_mat *down, int64_t d, q8_mode mode, const float *h, const q8_act *hq, int64_t rows,
+                     int k, const int32_t *ids, const float *gates, const q8_moe_plan *plan, const float *residual,
+                     float *y, float *expert_out, q8_ws *ws, q8_stream stream);
+
+/* ---- a10-a11: the decode step ----------------------------------------------------------------------------------- */
+
+/* A model for decode_step (qwen_emit, emit_qwen30b_generate: RMSNorm -> Q/K/V -> per-head QK-norm + RoPE -> attention
+ * over the KV cache -> O-proj -> residual -> RMSNorm -> mixture -> residual, per layer; then the LM head and the greedy
+ * token).  Arrays named [layers] are HOST arrays of per-layer DEVICE pointers or matrices; q8_model_create copies
+ * them.  Every device buffer stays owned by the caller and must outlive the model. */
+typedef struct {
+    int64_t layers, d, heads, kv_heads, head_dim, experts, k, dff, vocab, ctx;
+    float eps;                  /* RMSNorm and QK-norm epsilon */
+    double rope_theta;          /* RoPE base; pairs (i, i + head_dim/2) */
+    q8_mode mode;
+    const float *embed;         /* device f32 [vocab][d] */
+    const float *const *attn_norm, *const *ffn_norm; /* [layers] -> device f32 [d] */
+    const float *const *q_norm, *const *k_norm;      /* [layers] -> device f32 [head_dim] */
+    const float *final_norm;    /* device f32 [d] */
+    const q8_mat *wq, *wk, *wv, *wo;           /* [layers]: [heads*hd, d], [kv*hd, d], [kv*hd, d], [d, heads*hd] */
+    const q8_mat *router, *gate, *up, *down;   /* [layers]: [E, d], [E*dff, d], [E*dff, d], [E*d, dff] */
+    q8_mat lm_head;                            /* [vocab, d] */
+    float *const *k_cache, *const *v_cache;    /* [layers] -> device f32 [kv_heads][ctx][head_dim] */
+    int32_t *tok;               /* device int32 [1]: the token the step reads; the step writes the next token here */
+    int32_t *pos;               /* device int32 [1]: the position the step writes; the step adds 1 */
+    float *logits;              /* device f32 [vocab] or NULL */
+} q8_model_desc;
+
+typedef struct q8_model q8_model;
+
+/* Checks the descriptor, allocates the model's activation buffers and workspace on the current device and builds the
+ * RoPE table.  Refuses shapes the kernels do not run (head_dim != 128, heads % kv_heads, d % 32, ...). */
+Q8_API int q8_model_create(const q8_model_desc *desc, q8_model **model);
+Q8_API void q8_model_destroy(q8_model *model);
+
+/* One token: reads *tok and *pos on the device, writes the new key/value rows at *pos, the logits (if requested) and the
+ * next token into *tok, and advances *pos.  The first call on a model captures the whole step as one CUDA graph on a
+ * private capture of `stream`; every call then replays it on `stream` (qwen_emit docs: one captured graph replayed per
+ * token, position and token in device memory).  The first call must not be made while `stream` is capturing.  A step
+ * whose *pos is outside [0, ctx) writes nothing and leaves *tok and *pos unchanged (the error is counted in the
+ * model's device error word). */
+Q8_API int decode_step(q8_model *model, q8_stream stream);
+/* The same step as plain launches, without a graph (for tests and graph-capture by the caller). */
+Q8_API int decode_step_launches(q8_model *model, q8_stream stream);
+/* Reads and clears the model's device error word (synchronizes `stream`): Q8_OK, or Q8_EINVAL when a step met an
+ * out-of-range position or token. */
+Q8_API int q8_model_check(q8_model *model, q8_stream stream);
+
+/* ---- errors --------------------------------------------------------------------------------------------------- */
+/* The text of the calling thread's last error (empty when none); valid until the thread's next call. */
+Q8_API const char *q8_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

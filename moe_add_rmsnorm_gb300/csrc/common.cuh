@@ -1,0 +1,118 @@
+// Device helpers shared by the q8moe kernels (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "q8moe.h"
+
+#define Q8_QBLOCK 32
+#define Q8_WARPS 8          // warps per CTA in the streaming kernels
+#define Q8_THREADS (Q8_WARPS * 32)
+
+namespace q8 {
+
+// ---- loads ------------------------------------------------------------------------------------------------------
+
+// One 32-byte Q8_0 block of weights in one 256-bit load (sm_100+), read once: not kept in L1.
+__device__ __forceinline__ void ld_block_stream(const int8_t* p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+
+// A 32-byte block read through L1 (activations that several warps of the CTA share).
+__device__ __forceinline__ void ld_block_shared_use(const int8_t* p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ float ld_scale_stream(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// ---- int8 -> f32 --------------------------------------------------------------------------------------------------
+// Byte i of w (a signed int8) as an exact f32: flip the sign bit to get b+128 in [0,255], place it in the low mantissa
+// byte of 2^23 (0x4B000000), and subtract 2^23 + 128.  Both steps are exact.
+template <int I>
+__device__ __forceinline__ float i8_to_f32(uint32_t w_flipped) {
+    return __uint_as_float(__byte_perm(w_flipped, 0x4B000000u, 0x7440u | I)) - 8388736.0f;
+}
+
+// ---- the per-block dot products --------------------------------------------------------------------------------
+
+// f32 partial sum of one 32-value block: sum_t q[t] * x[t] (x in registers), four independent FMA chains.
+__device__ __forceinline__ float block_dot_f32(const uint32_t (&w)[8], const float* __restrict__ x) {
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t u = w[i] ^ 0x80808080u;
+        p0 = fmaf(i8_to_f32<0>(u), x[4 * i + 0], p0);
+        p1 = fmaf(i8_to_f32<1>(u), x[4 * i + 1], p1);
+        p2 = fmaf(i8_to_f32<2>(u), x[4 * i + 2], p2);
+        p3 = fmaf(i8_to_f32<3>(u), x[4 * i + 3], p3);
+    }
+    return (p0 + p1) + (p2 + p3);
+}
+
+// Exact int32 dot of one weight block with one activation block (dp4a: four int8 products per instruction).
+__device__ __forceinline__ int block_dot_i8(const uint32_t (&w)[8], const uint32_t (&x)[8]) {
+    int d0 = 0, d1 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        d0 = __dp4a((int)w[i], (int)x[i], d0);
+        d1 = __dp4a((int)w[i + 1], (int)x[i + 1], d1);
+    }
+    return d0 + d1;
+}
+
+// ---- reductions -----------------------------------------------------------------------------------------------
+
+template <int LANES, typename T>
+__device__ __forceinline__ T group_sum(T v) {
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ---- the one-word activation quantizer ------------------------------------------------------------------------
+// A warp holds one 32-value block, value `v` in lane `lane`.  d = amax / 127 and q = round-half-away(v / d), both
+// divisions IEEE-rounded f32 (never the approximate divide), q clamped to [-127, 127]; amax = 0 gives d = 0, q = 0.
+__device__ __forceinline__ int8_t quantize_lane(float v, float& d_out) {
+    const float amax = warp_max(fabsf(v));
+    const float d = __fdiv_rn(amax, 127.0f);
+    d_out = d;
+    if (d == 0.0f) return 0;
+    float r = roundf(__fdiv_rn(v, d));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return (int8_t)(int)r;
+}
+
+// ---- SiLU -------------------------------------------------------------------------------------------------------
+// silu(z) = z / (1 + e^-z): for z << 0, e^-z overflows to +inf and the quotient is -0, the correct limit.
+__device__ __forceinline__ float silu_f32(float z) { return __fdiv_rn(z, 1.0f + expf(-z)); }
+
+// ---- grid-level arrival -----------------------------------------------------------------------------------------
+// Called by every lane of a warp after the lanes' partial results are stored.  Returns true in every lane of the one
+// warp that arrives last among `expected` arrivals on `counter`; that warp must reset the counter to 0 after reading
+// the others' partials (through L2: __ldcg).
+__device__ __forceinline__ bool warp_arrive_last(int* counter, int expected) {
+    __threadfence();
+    __syncwarp();
+    int old = 0;
+    if ((threadIdx.x & 31) == 0) old = atomicAdd(counter, 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    const bool last = (old == expected - 1);
+    if (last) __threadfence();
+    return last;
+}
+
+}  // namespace q8

@@ -1,0 +1,385 @@
+// The decode step's attention side and its last stage: per-head QK-norm + RoPE + KV append, single-query GQA
+// attention split over positions, and the greedy arg-max that advances token and position on the device.
+//
+// What it computes: qwen_emit docs, emit_qwen30b_generate (per-head QK-norm + RoPE, causal attention over a KV cache,
+// device-side position and token); forward_shim.rs, kernel_refusal (Rope: a full rotary; Attention: scores scaled by
+// 1/sqrt(HD), query heads grouped evenly over key/value heads, no mask, window, sink or soft cap) and
+// ForwardShim::supports (KvCacheQuant refused: the caches are f32); lane_link.rs, Link::prim (Rope, Attention with its
+// splits over positions, ArgMax) and Link::class_launch (FusedSampling: the arg-max advances token and position);
+// lane/arena.rs, scratch (ap partials and ac counters of a split attention; av/ai/ac of the arg-max).
+//
+// How (GB300 design): the f32 cache is the second-largest byte stream of the step (one key and one value row of 512 B
+// per position and key/value head), so the attention is a streaming kernel: every (key/value head, chunk of
+// positions) pair is one CTA that reads its rows once with coalesced 16-byte loads and serves all query heads of its
+// group from those registers; chunk partials (max, sum, weighted values) meet in scratch and the last CTA of a head
+// folds them in chunk order.  The 48 KiB static score row of the pages' design is not needed: a chunk's scores live in
+// shared memory and any cache length works.
+#include <float.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace q8 {
+namespace {
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// ==== QK-norm + RoPE + KV append =================================================================================
+
+// CTA h < heads: query head h (normed and turned in place).  CTA heads + g: key head g (normed, turned, written at
+// pos) and value head g (written at pos).  hd/2 threads; thread i holds the pair (i, i + hd/2).
+__global__ void __launch_bounds__(256) qk_rope_kv_kernel(const QkRopeCall c) {
+    __shared__ float red[8];
+    const int h = blockIdx.x;
+    const int i = threadIdx.x;
+    const int half = c.hd / 2;
+    griddep_wait();
+    const int pos = *c.pos;
+    if (pos < 0 || pos >= c.ctx) {
+        if (i == 0 && h == 0 && c.err) atomicOr(c.err, 2);
+        return;
+    }
+    const bool is_q = h < c.heads;
+    const int g = is_q ? h : h - c.heads;
+    const float* src = is_q ? c.q + (int64_t)g * c.hd : c.k + (int64_t)g * c.hd;
+    const float* w = is_q ? c.q_norm : c.k_norm;
+    float a = src[i], b = src[i + half];
+    float ss = a * a + b * b;
+    ss = group_sum<32>(ss);
+    if ((i & 31) == 0) red[i >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int j = 0; j < (half + 31) / 32; ++j) tot += red[j];
+    const float inv = 1.0f / sqrtf(tot / (float)c.hd + c.eps);
+    a = a * inv * w[i];
+    b = b * inv * w[i + half];
+    const float cs = c.cos_t[(int64_t)pos * half + i], sn = c.sin_t[(int64_t)pos * half + i];
+    const float ra = a * cs - b * sn;
+    const float rb = a * sn + b * cs;
+    if (is_q) {
+        __syncthreads();  // every thread has read its pair before any write
+        c.q[(int64_t)g * c.hd + i] = ra;
+        c.q[(int64_t)g * c.hd + i + half] = rb;
+    } else {
+        float* kr = c.k_cache + ((int64_t)g * c.ctx + pos) * c.hd;
+        float* vr = c.v_cache + ((int64_t)g * c.ctx + pos) * c.hd;
+        kr[i] = ra;
+        kr[i + half] = rb;
+        vr[i] = c.v[(int64_t)g * c.hd + i];
+        vr[i + half] = c.v[(int64_t)g * c.hd + i + half];
+    }
+    griddep_launch();
+}
+
+// ==== attention ===================================================================================================
+
+constexpr int ATT_THREADS = 256;
+constexpr int ATT_CHUNK = 64;   // positions per CTA
+constexpr int ATT_MAXG = 8;     // query heads per key/value head (static shared memory bound)
+constexpr int ATT_HD = 128;     // head width the kernel is built for
+
+struct AttnParams {
+    const float* q;
+    const float* k_cache;
+    const float* v_cache;
+    const int32_t* pos;
+    int heads, kv, ctx, G;
+    float scale;
+    float* out;
+    int8_t* outq;
+    float* outs;
+    float* part;   // [kv][nch_max][G][ATT_HD + 2]
+    int* cnt;      // [kv]
+    int nch_max;
+};
+
+// grid (kv, chunk).  Scores: 4 lanes per position (32 dims each), 8 positions per warp per pass.  Values: each warp
+// takes positions t = warp (mod 8), lane l the dims 4l..4l+3; the 8 warps' sums meet in shared memory.
+__global__ void __launch_bounds__(ATT_THREADS) attention_kernel(const AttnParams p) {
+    __shared__ float qs[ATT_MAXG][ATT_HD];
+    __shared__ float sc[ATT_MAXG][ATT_CHUNK];
+    __shared__ float red[ATT_THREADS / 32][ATT_MAXG][ATT_HD];  // [warp][g][dim]
+    __shared__ float stat[ATT_MAXG][2];
+    __shared__ int last;
+    const int g = blockIdx.x, chunk = blockIdx.y;
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int G = p.G;
+    griddep_wait();
+    const int len = *p.pos + 1;  // rows 0..pos
+    const int nch = (len + ATT_CHUNK - 1) / ATT_CHUNK;
+    if (len < 1 || len > p.ctx || chunk >= nch) return;
+    const int p0 = chunk * ATT_CHUNK;
+    const int np = min(ATT_CHUNK, len - p0);
+    for (int i = t; i < G * ATT_HD; i += ATT_THREADS) qs[i / ATT_HD][i % ATT_HD] = p.q[((int64_t)g * G) * ATT_HD + i];
+    __syncthreads();
+    const float* kb = p.k_cache + ((int64_t)g * p.ctx + p0) * ATT_HD;
+    const float* vb = p.v_cache + ((int64_t)g * p.ctx + p0) * ATT_HD;
+    // scores (every lane runs the same path; lanes past the chunk's end multiply zeros and store nothing)
+    {
+        const int sub = lane & 3;         // 32-dim quarter of the row
+        const int pl = wid * 8 + (lane >> 2);
+        const bool valid = pl < np;
+        float kr[32];
+        const float4* kp = reinterpret_cast<const float4*>(kb + (int64_t)(valid ? pl : 0) * ATT_HD + sub * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 v = valid ? __ldcs(kp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            kr[4 * i] = v.x;
+            kr[4 * i + 1] = v.y;
+            kr[4 * i + 2] = v.z;
+            kr[4 * i + 3] = v.w;
+        }
+        for (int hh = 0; hh < G; ++hh) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc = fmaf(qs[hh][sub * 32 + i], kr[i], acc);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (sub == 0 && valid) sc[hh][pl] = acc * p.scale;
+        }
+    }
+    __syncthreads();
+    // chunk softmax statistics per head (warp hh), scores replaced by exp(s - m)
+    for (int hh = wid; hh < G; hh += ATT_THREADS / 32) {
+        float m = -FLT_MAX;
+        for (int i = lane; i < np; i += 32) m = fmaxf(m, sc[hh][i]);
+        m = warp_max(m);
+        float l = 0.f;
+        for (int i = lane; i < np; i += 32) {
+            const float e = expf(sc[hh][i] - m);
+            sc[hh][i] = e;
+            l += e;
+        }
+        l = group_sum<32>(l);
+        if (lane == 0) {
+            stat[hh][0] = m;
+            stat[hh][1] = l;
+        }
+    }
+    __syncthreads();
+    // weighted values
+    {
+        float acc[ATT_MAXG][4];
+#pragma unroll
+        for (int hh = 0; hh < ATT_MAXG; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
+        for (int pl = wid; pl < np; pl += ATT_THREADS / 32) {
+            const float4 v = __ldcs(reinterpret_cast<const float4*>(vb + (int64_t)pl * ATT_HD) + lane);
+#pragma unroll
+            for (int hh = 0; hh < ATT_MAXG; ++hh) {
+                if (hh < G) {
+                    const float w = sc[hh][pl];
+                    acc[hh][0] = fmaf(w, v.x, acc[hh][0]);
+                    acc[hh][1] = fmaf(w, v.y, acc[hh][1]);
+                    acc[hh][2] = fmaf(w, v.z, acc[hh][2]);
+                    acc[hh][3] = fmaf(w, v.w, acc[hh][3]);
+                }
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < ATT_MAXG; ++hh)
+            if (hh < G)
+                *reinterpret_cast<float4*>(&red[wid][hh][4 * lane]) =
+                    make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+    }
+    __syncthreads();
+    float* part = p.part + ((int64_t)g * p.nch_max + chunk) * G * (ATT_HD + 2);
+    for (int i = t; i < G * ATT_HD; i += ATT_THREADS) {
+        const int hh = i / ATT_HD, dd = i % ATT_HD;
+        float s = 0.f;
+        for (int w = 0; w < ATT_THREADS / 32; ++w) s += red[w][hh][dd];
+        part[hh * (ATT_HD + 2) + dd] = s;
+    }
+    if (t < G) {
+        part[t * (ATT_HD + 2) + ATT_HD] = stat[t][0];
+        part[t * (ATT_HD + 2) + ATT_HD + 1] = stat[t][1];
+    }
+    // the last chunk of this key/value head folds all chunks in chunk order
+    __threadfence();
+    __syncthreads();
+    if (t == 0) last = (atomicAdd(p.cnt + g, 1) == nch - 1);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    for (int i = t; i < G * ATT_HD; i += ATT_THREADS) {
+        const int hh = i / ATT_HD, dd = i % ATT_HD;
+        const float* base = p.part + (int64_t)g * p.nch_max * G * (ATT_HD + 2) + hh * (ATT_HD + 2);
+        float M = -FLT_MAX;
+        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(base + (int64_t)cc * G * (ATT_HD + 2) + ATT_HD));
+        float num = 0.f, den = 0.f;
+        for (int cc = 0; cc < nch; ++cc) {
+            const float* b = base + (int64_t)cc * G * (ATT_HD + 2);
+            const float f = expf(__ldcg(b + ATT_HD) - M);
+            num = fmaf(f, __ldcg(b + dd), num);
+            den = fmaf(f, __ldcg(b + ATT_HD + 1), den);
+        }
+        const float o = num / den;
+        const int64_t oi = ((int64_t)g * G + hh) * ATT_HD + dd;
+        p.out[oi] = o;
+        if (p.outq) {  // i spans whole 32-value blocks per warp (ATT_HD and the stride are multiples of 32)
+            float d;
+            const int8_t qv = quantize_lane(o, d);
+            p.outq[oi] = qv;
+            if (lane == 0) p.outs[oi / 32] = d;
+        }
+    }
+    if (t == 0) p.cnt[g] = 0;
+    griddep_launch();
+}
+
+// ==== arg-max and advance ========================================================================================
+
+constexpr int AM_THREADS = 512;
+
+__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
+    return bi < 0 || v > bv || (v == bv && i < bi);
+}
+
+__global__ void __launch_bounds__(AM_THREADS) argmax_kernel(const float* __restrict__ x, int64_t n, float* bv_out,
+                                                            int* bi_out, int* cnt, int32_t* tok, int32_t* pos,
+                                                            const int* err, int ctx) {
+    __shared__ float sv[AM_THREADS / 32];
+    __shared__ int si[AM_THREADS / 32];
+    __shared__ int last;
+    griddep_wait();
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    float bv = -FLT_MAX;
+    int bi = -1;
+    for (int64_t i = (int64_t)blockIdx.x * AM_THREADS + t; i < n; i += (int64_t)gridDim.x * AM_THREADS) {
+        const float v = x[i];
+        if (am_better(v, (int)i, bv, bi)) {
+            bv = v;
+            bi = (int)i;
+        }
+    }
+    auto reduce = [&](float& v, int& i) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+            if (oi >= 0 && am_better(ov, oi, v, i)) {
+                v = ov;
+                i = oi;
+            }
+        }
+    };
+    reduce(bv, bi);
+    if (lane == 0) {
+        sv[wid] = bv;
+        si[wid] = bi;
+    }
+    __syncthreads();
+    if (wid == 0) {
+        bv = lane < AM_THREADS / 32 ? sv[lane] : -FLT_MAX;
+        bi = lane < AM_THREADS / 32 ? si[lane] : -1;
+        reduce(bv, bi);
+        if (lane == 0) {
+            bv_out[blockIdx.x] = bv;
+            bi_out[blockIdx.x] = bi;
+            __threadfence();
+            last = (atomicAdd(cnt, 1) == (int)gridDim.x - 1);
+        }
+    }
+    __syncthreads();
+    if (!last || wid != 0) return;
+    __threadfence();
+    bv = -FLT_MAX;
+    bi = -1;
+    for (int b = lane; b < (int)gridDim.x; b += 32) {
+        const float v = __ldcg(bv_out + b);
+        const int i = __ldcg(bi_out + b);
+        if (i >= 0 && am_better(v, i, bv, bi)) {
+            bv = v;
+            bi = i;
+        }
+    }
+    reduce(bv, bi);
+    if (lane == 0) {
+        const bool bad = (err && __ldcg(err) != 0) || (pos && (*pos < 0 || *pos >= ctx));
+        if (!bad) {
+            *tok = bi;
+            if (pos) *pos = *pos + 1;
+        }
+        *cnt = 0;
+    }
+}
+
+__global__ void rope_table_kernel(float* cos_t, float* sin_t, int ctx, int half, double theta) {
+    const int64_t n = (int64_t)ctx * half;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t pos = i / half;
+        const int j = (int)(i % half);
+        const double ang = (double)pos * pow(theta, -2.0 * (double)j / (double)(2 * half));
+        double s, c;
+        sincos(ang, &s, &c);
+        cos_t[i] = (float)c;
+        sin_t[i] = (float)s;
+    }
+}
+
+int attn_chunks(int ctx) { return (ctx + ATT_CHUNK - 1) / ATT_CHUNK; }
+
+int argmax_blocks(int64_t n) {
+    int64_t b = (n + AM_THREADS * 4 - 1) / (AM_THREADS * 4);
+    const int64_t cap = (int64_t)device_info().sms * 2;
+    if (b > cap) b = cap;
+    if (b < 1) b = 1;
+    return (int)b;
+}
+
+}  // namespace
+
+cudaError_t launch_qk_rope_kv(const QkRopeCall& c, cudaStream_t st) {
+    return launch(qk_rope_kv_kernel, dim3(c.heads + c.kv), dim3(c.hd / 2), 0, st, c.pdl, c);
+}
+
+void attention_scratch(const AttnCall& c, size_t* bytes, size_t* counters) {
+    const int G = c.heads / c.kv;
+    *bytes = (size_t)c.kv * attn_chunks(c.ctx) * G * (ATT_HD + 2) * sizeof(float);
+    *counters = (size_t)c.kv;
+}
+
+cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
+    AttnParams p = {};
+    p.q = c.q;
+    p.k_cache = c.k_cache;
+    p.v_cache = c.v_cache;
+    p.pos = c.pos;
+    p.heads = c.heads;
+    p.kv = c.kv;
+    p.ctx = c.ctx;
+    p.G = c.heads / c.kv;
+    p.scale = (float)(1.0 / sqrt((double)c.hd));
+    p.out = c.out;
+    p.outq = c.outq;
+    p.outs = c.outs;
+    p.nch_max = attn_chunks(c.ctx);
+    size_t bytes = 0, cnt = 0;
+    attention_scratch(c, &bytes, &cnt);
+    p.part = ws.take<float>(bytes / sizeof(float));
+    p.cnt = ws.take_counters(cnt);
+    if (ws.overflow) return cudaErrorMemoryAllocation;
+    return launch(attention_kernel, dim3(c.kv, p.nch_max), dim3(ATT_THREADS), 0, st, c.pdl, p);
+}
+
+void argmax_scratch(const ArgmaxCall& c, size_t* bytes, size_t* counters) {
+    *bytes = (size_t)argmax_blocks(c.n) * 8 + 256;
+    *counters = 1;
+}
+
+cudaError_t launch_argmax(const ArgmaxCall& c, Carve& ws, cudaStream_t st) {
+    const int blocks = argmax_blocks(c.n);
+    float* bv = ws.take<float>(blocks);
+    int* bi = ws.take<int>(blocks);
+    int* cnt = ws.take_counters(1);
+    if (ws.overflow) return cudaErrorMemoryAllocation;
+    return launch(argmax_kernel, dim3(blocks), dim3(AM_THREADS), 0, st, c.pdl, c.x, c.n, bv, bi, cnt, c.tok, c.pos,
+                  c.err, c.ctx);
+}
+
+cudaError_t launch_rope_table(float* cos_t, float* sin_t, int ctx, int half, double theta, cudaStream_t st) {
+    rope_table_kernel<<<256, 256, 0, st>>>(cos_t, sin_t, ctx, half, theta);
+    return cudaGetLastError();
+}
+
+}  // namespace q8

@@ -1,0 +1,206 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel files.  Host code only.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "q8moe.h"
+
+namespace q8 {
+
+// Device facts the launchers size grids by (cached per device).
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+const DeviceInfo& device_info();
+
+// A bump allocator over one workspace's scratch and counters, for the launches of one call.
+struct Carve {
+    char* base = nullptr;
+    size_t size = 0, used = 0;
+    int* counters = nullptr;
+    size_t n_counters = 0, used_counters = 0;
+    bool overflow = false;
+    template <typename T>
+    T* take(size_t n) {
+        size_t off = (used + 255) & ~size_t(255);
+        size_t bytes = n * sizeof(T);
+        if (off + bytes > size) {
+            overflow = true;
+            return nullptr;
+        }
+        used = off + bytes;
+        return reinterpret_cast<T*>(base + off);
+    }
+    int* take_counters(size_t n) {
+        if (used_counters + n > n_counters) {
+            overflow = true;
+            return nullptr;
+        }
+        int* p = counters + used_counters;
+        used_counters += n;
+        return p;
+    }
+};
+
+// ---- projections ------------------------------------------------------------------------------------------------
+// One matrix of a (possibly merged) projection: all segments share cols and the activation.
+struct GemvSeg {
+    const int8_t* q = nullptr;
+    const float* s = nullptr;
+    int64_t n = 0;
+    float* y = nullptr;                  // [R][n]
+    const float* residual = nullptr;     // optional: y = fl32(residual + fl32(acc))
+};
+
+struct GemvCall {
+    int mode = 0;
+    int64_t k = 0;
+    int nseg = 1;
+    GemvSeg seg[3];
+    const float* x = nullptr;            // [R][k] (mode 0)
+    const int8_t* xq = nullptr;          // [R][k] (mode 1)
+    const float* xs = nullptr;           // [R][k/32]
+    int64_t R = 1;
+    int32_t* dots = nullptr;             // mode 1 debug export [R][n][k/32] (single segment)
+    int pdl = 0;                         // launch with programmatic dependent launch allowed
+};
+
+// Scratch needed by a projection (bytes, counters).
+void gemv_scratch(const GemvCall& c, size_t* bytes, size_t* counters);
+cudaError_t launch_gemv(const GemvCall& c, Carve& ws, cudaStream_t st);
+
+// ---- norm and quantisation ------------------------------------------------------------------------------------
+struct NormCall {
+    const float* a = nullptr;
+    const int32_t* a_row = nullptr;      // optional: a's row for each row r is a + a_row[r]*d (an embedding gather)
+    int64_t a_rows = 0;                  // rows of the gathered table (bounds check)
+    const float* b = nullptr;
+    const float* w = nullptr;
+    int64_t rows = 0, d = 0;
+    float eps = 0.f;
+    float* sum = nullptr;
+    float* y = nullptr;
+    int8_t* yq = nullptr;
+    float* ys = nullptr;
+    int* err = nullptr;                  // device error word for a gathered row out of range
+    int pdl = 0;
+};
+cudaError_t launch_add_rmsnorm(const NormCall& c, cudaStream_t st);
+cudaError_t launch_quantize(const float* x, int64_t n, int8_t* q, float* s, cudaStream_t st);
+
+// ---- mixture ----------------------------------------------------------------------------------------------------
+struct PlanPtrs {
+    int32_t* counts = nullptr;    // [E]
+    int32_t* offsets = nullptr;   // [E+1]
+    int32_t* lists = nullptr;     // [R*K]
+    int32_t* active = nullptr;    // [E+1]: count then the active experts ascending
+};
+
+struct TopkCall {
+    const float* logits = nullptr;  // [R][E]
+    int64_t R = 1, E = 0;
+    int K = 0;
+    int32_t* ids = nullptr;
+    float* gates = nullptr;
+    PlanPtrs plan;                  // filled when plan.counts != nullptr
+    int pdl = 0;
+};
+cudaError_t launch_topk(const TopkCall& c, cudaStream_t st);
+
+struct ExpertCall {
+    int mode = 0;
+    // gate-up: w0 = gate, w1 = up (rows E*dff, cols d); down: w0 = down (rows E*d, cols dff)
+    const int8_t* q0 = nullptr;
+    const float* s0 = nullptr;
+    const int8_t* q1 = nullptr;
+    const float* s1 = nullptr;
+    int64_t E = 0, out_rows = 0, k = 0;  // out_rows per expert (dff for gate-up, d for down); k = input width
+    int64_t R = 1;
+    int K = 0;
+    const int32_t* ids = nullptr;
+    const float* gates = nullptr;
+    PlanPtrs plan;                       // used when plan.active != nullptr, else choice j is group j (R == 1)
+    const float* x = nullptr;            // [R][k] (gate-up, mode 0) or h [R*K][k] (down, mode 0)
+    const int8_t* xq = nullptr;          // mode 1
+    const float* xs = nullptr;
+    float* h = nullptr;                  // gate-up out [R*K][dff]
+    int8_t* hq = nullptr;                // gate-up out, mode 1
+    float* hs = nullptr;
+    const float* residual = nullptr;     // down
+    float* y = nullptr;                  // down out [R][d]
+    float* expert_out = nullptr;         // down out [R][K][d]
+    int pdl = 0;
+};
+void gate_up_scratch(const ExpertCall& c, size_t* bytes, size_t* counters);
+void down_scratch(const ExpertCall& c, size_t* bytes, size_t* counters);
+cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st);
+cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st);
+
+// ---- decode-step pieces -----------------------------------------------------------------------------------------
+struct QkRopeCall {
+    float* q = nullptr;          // [heads][hd], normed and turned in place
+    const float* k = nullptr;    // [kv][hd]
+    const float* v = nullptr;    // [kv][hd]
+    const float* q_norm = nullptr;
+    const float* k_norm = nullptr;
+    const float* cos_t = nullptr;   // [ctx][hd/2]
+    const float* sin_t = nullptr;
+    float* k_cache = nullptr;       // [kv][ctx][hd]
+    float* v_cache = nullptr;
+    const int32_t* pos = nullptr;
+    int heads = 0, kv = 0, hd = 0, ctx = 0;
+    float eps = 0.f;
+    int* err = nullptr;
+    int pdl = 0;
+};
+cudaError_t launch_qk_rope_kv(const QkRopeCall& c, cudaStream_t st);
+
+struct AttnCall {
+    const float* q = nullptr;       // [heads][hd]
+    const float* k_cache = nullptr; // [kv][ctx][hd]
+    const float* v_cache = nullptr;
+    const int32_t* pos = nullptr;   // attends rows 0..pos
+    int heads = 0, kv = 0, hd = 0, ctx = 0;
+    float* out = nullptr;           // [heads][hd]
+    int8_t* outq = nullptr;         // optional quantized output
+    float* outs = nullptr;
+    int pdl = 0;
+};
+void attention_scratch(const AttnCall& c, size_t* bytes, size_t* counters);
+cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st);
+
+struct ArgmaxCall {
+    const float* x = nullptr;
+    int64_t n = 0;
+    int32_t* tok = nullptr;     // written with the argmax
+    int32_t* pos = nullptr;     // incremented (when not null)
+    const int* err = nullptr;   // when set and non-zero, tok and pos are left unchanged
+    int ctx = 0;                // with pos: a position outside [0, ctx) leaves tok and pos unchanged
+    int pdl = 0;
+};
+void argmax_scratch(const ArgmaxCall& c, size_t* bytes, size_t* counters);
+cudaError_t launch_argmax(const ArgmaxCall& c, Carve& ws, cudaStream_t st);
+
+cudaError_t launch_rope_table(float* cos_t, float* sin_t, int ctx, int half, double theta, cudaStream_t st);
+
+// Launch helper: programmatic dependent launch when requested.
+template <typename Kern, typename... Args>
+cudaError_t launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, int pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace q8

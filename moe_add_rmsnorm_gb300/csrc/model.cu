@@ -1,0 +1,504 @@
+// The decode step of a whole model: its launches in order and the CUDA graph they are captured into.
+//
+// What it computes: qwen_emit docs, emit_qwen30b_generate (RMSNorm -> Q/K/V -> per-head QK-norm + RoPE -> attention
+// over the KV cache -> O-proj -> residual -> RMSNorm -> 8-of-128 mixture -> residual per layer; the LM head; a T=1
+// step captured as one CUDA graph and replayed per token with position and token on the device) and forward_shim.rs
+// (module docs: the whole forward captured as one CUDA graph; every stage reads and writes whole buffers).
+//
+// Launches per layer (the merges are GB300 choices, not the pages'): one add+RMSNorm with its int8 epilogue; one
+// projection for q, k and v together; one QK-norm + RoPE + KV append; one split attention (its fold quantizes the
+// result for the O projection); the O projection with the residual sum in its epilogue; one add+RMSNorm; the router
+// projection and its top-k; gate-up; down-and-combine with the residual sum in its epilogue.  Then the final norm, the
+// LM head and the arg-max that advances token and position.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <vector>
+
+#include "kernels.h"
+#include "q8moe.h"
+
+namespace q8 {
+extern int model_fail(int code, const char* fmt, ...);
+}
+
+using namespace q8;
+
+struct q8_model {
+    q8_model_desc d;
+    std::vector<const float*> attn_norm, ffn_norm, q_norm, k_norm;
+    std::vector<q8_mat> wq, wk, wv, wo, router, gate, up, down;
+    std::vector<float*> kc, vc;
+    char* arena = nullptr;
+    size_t arena_bytes = 0;
+    float *h = nullptr, *x = nullptr, *q = nullptr, *k = nullptr, *v = nullptr, *att = nullptr, *logits = nullptr;
+    float *cos_t = nullptr, *sin_t = nullptr, *hbuf = nullptr, *gates = nullptr, *rlog = nullptr;
+    int8_t *xq = nullptr, *attq = nullptr, *hq = nullptr;
+    float *xs = nullptr, *atts = nullptr, *hs = nullptr;
+    int32_t* ids = nullptr;
+    int* err = nullptr;
+    char* ws = nullptr;
+    size_t ws_bytes = 0;
+    int* counters = nullptr;
+    size_t n_counters = 0;
+    cudaStream_t cap = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int pdl = 0;
+};
+
+namespace {
+
+int check_mat_shape(const q8_mat& m, int64_t rows, int64_t cols, const char* name, int64_t layer) {
+    if (!m.q || !m.s) return model_fail(Q8_EINVAL, "%s[%lld]: null quants or scales", name, (long long)layer);
+    if (m.rows != rows || m.cols != cols)
+        return model_fail(Q8_EINVAL, "%s[%lld]: %lld x %lld, expected %lld x %lld", name, (long long)layer,
+                          (long long)m.rows, (long long)m.cols, (long long)rows, (long long)cols);
+    if ((uintptr_t)m.q % 32) return model_fail(Q8_EINVAL, "%s[%lld]: quants not 32-byte aligned", name, (long long)layer);
+    if ((uintptr_t)m.s % 4) return model_fail(Q8_EINVAL, "%s[%lld]: scales not 4-byte aligned", name, (long long)layer);
+    return Q8_OK;
+}
+
+template <typename T>
+T* carve_arena(char*& at, size_t n) {
+    uintptr_t p = ((uintptr_t)at + 255) & ~uintptr_t(255);
+    at = (char*)(p + n * sizeof(T));
+    return (T*)p;
+}
+
+Carve fresh_carve(q8_model* m) {
+    Carve c;
+    c.base = m->ws;
+    c.size = m->ws_bytes;
+    c.counters = m->counters;
+    c.n_counters = m->n_counters;
+    return c;
+}
+
+cudaError_t step_launches(q8_model* m, cudaStream_t st) {
+    const q8_model_desc& d = m->d;
+    const int mode = (int)d.mode;
+    const int64_t D = d.d, H = d.heads, KV = d.kv_heads, HD = d.head_dim;
+    const int pdl = m->pdl;
+    cudaError_t e = cudaSuccess;
+#define Q8_TRY(x)                    \
+    do {                             \
+        e = (x);                     \
+        if (e != cudaSuccess) return e; \
+    } while (0)
+    for (int64_t l = 0; l < d.layers; ++l) {
+        // attention half: norm (the first layer gathers the token's embedding row into the residual stream)
+        NormCall n;
+        if (l == 0) {
+            n.a = d.embed;
+            n.a_row = d.tok;
+            n.a_rows = d.vocab;
+            n.sum = m->h;
+        } else {
+            n.a = m->h;
+        }
+        n.w = m->attn_norm[l];
+        n.rows = 1;
+        n.d = D;
+        n.eps = d.eps;
+        if (mode == 0) n.y = m->x;
+        else {
+            n.yq = m->xq;
+            n.ys = m->xs;
+        }
+        n.err = m->err;
+        n.pdl = pdl;
+        Q8_TRY(launch_add_rmsnorm(n, st));
+        // q, k and v in one projection launch
+        {
+            Carve cv = fresh_carve(m);
+            GemvCall g;
+            g.mode = mode;
+            g.k = D;
+            g.nseg = 3;
+            g.seg[0] = GemvSeg{m->wq[l].q, m->wq[l].s, H * HD, m->q, nullptr};
+            g.seg[1] = GemvSeg{m->wk[l].q, m->wk[l].s, KV * HD, m->k, nullptr};
+            g.seg[2] = GemvSeg{m->wv[l].q, m->wv[l].s, KV * HD, m->v, nullptr};
+            g.x = m->x;
+            g.xq = m->xq;
+            g.xs = m->xs;
+            g.pdl = pdl;
+            Q8_TRY(launch_gemv(g, cv, st));
+        }
+        {
+            QkRopeCall r;
+            r.q = m->q;
+            r.k = m->k;
+            r.v = m->v;
+            r.q_norm = m->q_norm[l];
+            r.k_norm = m->k_norm[l];
+            r.cos_t = m->cos_t;
+            r.sin_t = m->sin_t;
+            r.k_cache = m->kc[l];
+            r.v_cache = m->vc[l];
+            r.pos = d.pos;
+            r.heads = (int)H;
+            r.kv = (int)KV;
+            r.hd = (int)HD;
+            r.ctx = (int)d.ctx;
+            r.eps = d.eps;
+            r.err = m->err;
+            r.pdl = pdl;
+            Q8_TRY(launch_qk_rope_kv(r, st));
+        }
+        {
+            Carve cv = fresh_carve(m);
+            AttnCall a;
+            a.q = m->q;
+            a.k_cache = m->kc[l];
+            a.v_cache = m->vc[l];
+            a.pos = d.pos;
+            a.heads = (int)H;
+            a.kv = (int)KV;
+            a.hd = (int)HD;
+            a.ctx = (int)d.ctx;
+            a.out = m->att;
+            if (mode == 1) {
+                a.outq = m->attq;
+                a.outs = m->atts;
+            }
+            a.pdl = pdl;
+            Q8_TRY(launch_attention(a, cv, st));
+        }
+        {
+            Carve cv = fresh_carve(m);
+            GemvCall g;
+            g.mode = mode;
+            g.k = H * HD;
+            g.seg[0] = GemvSeg{m->wo[l].q, m->wo[l].s, D, m->h, m->h};  // h = h + o
+            g.x = m->att;
+            g.xq = m->attq;
+            g.xs = m->atts;
+            g.pdl = pdl;
+            Q8_TRY(launch_gemv(g, cv, st));
+        }
+        // feed-forward half
+        NormCall n2;
+        n2.a = m->h;
+        n2.w = m->ffn_norm[l];
+        n2.rows = 1;
+        n2.d = D;
+        n2.eps = d.eps;
+        if (mode == 0) n2.y = m->x;
+        else {
+            n2.yq = m->xq;
+            n2.ys = m->xs;
+        }
+        n2.pdl = pdl;
+        Q8_TRY(launch_add_rmsnorm(n2, st));
+        {
+            Carve cv = fresh_carve(m);
+            GemvCall g;
+            g.mode = mode;
+            g.k = D;
+            g.seg[0] = GemvSeg{m->router[l].q, m->router[l].s, d.experts, m->rlog, nullptr};
+            g.x = m->x;
+            g.xq = m->xq;
+            g.xs = m->xs;
+            g.pdl = pdl;
+            Q8_TRY(launch_gemv(g, cv, st));
+            TopkCall t;
+            t.logits = m->rlog;
+            t.R = 1;
+            t.E = d.experts;
+            t.K = (int)d.k;
+            t.ids = m->ids;
+            t.gates = m->gates;
+            t.pdl = pdl;
+            Q8_TRY(launch_topk(t, st));
+        }
+        {
+            Carve cv = fresh_carve(m);
+            ExpertCall c;
+            c.mode = mode;
+            c.q0 = m->gate[l].q;
+            c.s0 = m->gate[l].s;
+            c.q1 = m->up[l].q;
+            c.s1 = m->up[l].s;
+            c.E = d.experts;
+            c.out_rows = d.dff;
+            c.k = D;
+            c.R = 1;
+            c.K = (int)d.k;
+            c.ids = m->ids;
+            c.x = m->x;
+            c.xq = m->xq;
+            c.xs = m->xs;
+            c.h = m->hbuf;
+            if (mode == 1) {
+                c.hq = m->hq;
+                c.hs = m->hs;
+            }
+            c.pdl = pdl;
+            Q8_TRY(launch_gate_up(c, cv, st));
+        }
+        {
+            Carve cv = fresh_carve(m);
+            ExpertCall c;
+            c.mode = mode;
+            c.q0 = m->down[l].q;
+            c.s0 = m->down[l].s;
+            c.E = d.experts;
+            c.out_rows = D;
+            c.k = d.dff;
+            c.R = 1;
+            c.K = (int)d.k;
+            c.ids = m->ids;
+            c.gates = m->gates;
+            c.x = m->hbuf;
+            c.xq = m->hq;
+            c.xs = m->hs;
+            c.residual = m->h;  // h = h + mixture
+            c.y = m->h;
+            c.pdl = pdl;
+            Q8_TRY(launch_down_combine(c, cv, st));
+        }
+    }
+    // final norm, LM head, greedy token
+    NormCall nf;
+    nf.a = m->h;
+    nf.w = d.final_norm;
+    nf.rows = 1;
+    nf.d = D;
+    nf.eps = d.eps;
+    if (mode == 0) nf.y = m->x;
+    else {
+        nf.yq = m->xq;
+        nf.ys = m->xs;
+    }
+    nf.pdl = pdl;
+    Q8_TRY(launch_add_rmsnorm(nf, st));
+    {
+        Carve cv = fresh_carve(m);
+        GemvCall g;
+        g.mode = mode;
+        g.k = D;
+        g.seg[0] = GemvSeg{d.lm_head.q, d.lm_head.s, d.vocab, m->logits, nullptr};
+        g.x = m->x;
+        g.xq = m->xq;
+        g.xs = m->xs;
+        g.pdl = pdl;
+        Q8_TRY(launch_gemv(g, cv, st));
+    }
+    {
+        Carve cv = fresh_carve(m);
+        ArgmaxCall a;
+        a.x = m->logits;
+        a.n = d.vocab;
+        a.tok = d.tok;
+        a.pos = d.pos;
+        a.err = m->err;
+        a.ctx = (int)d.ctx;
+        a.pdl = pdl;
+        Q8_TRY(launch_argmax(a, cv, st));
+    }
+#undef Q8_TRY
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+int q8_model_create(const q8_model_desc* desc, q8_model** out) {
+    if (!out) return model_fail(Q8_EINVAL, "model: null");
+    *out = nullptr;
+    if (!desc) return model_fail(Q8_EINVAL, "desc: null");
+    const q8_model_desc& d = *desc;
+    if (d.mode != Q8_F32ACT_F64SUM && d.mode != Q8_INT8ACT) return model_fail(Q8_EINVAL, "mode %d", (int)d.mode);
+    if (d.layers < 1 || d.d < 32 || d.heads < 1 || d.kv_heads < 1 || d.vocab < 1 || d.ctx < 1 || d.experts < 1 ||
+        d.dff < 32)
+        return model_fail(Q8_EINVAL, "a size below its minimum (layers, d, heads, kv_heads, vocab, ctx, experts, dff)");
+    if (d.head_dim != 128) return model_fail(Q8_EUNSUPPORTED, "head_dim %lld: the attention kernel is built for 128",
+                                             (long long)d.head_dim);
+    if (d.heads % d.kv_heads) return model_fail(Q8_EUNSUPPORTED, "query heads that do not group evenly over the key/value heads");
+    if (d.heads / d.kv_heads > 8) return model_fail(Q8_EUNSUPPORTED, "more than 8 query heads per key/value head");
+    if (d.d % 32 || d.dff % 32) return model_fail(Q8_EUNSUPPORTED, "d and dff must be whole 32-value blocks");
+    if (d.d > 8192) return model_fail(Q8_EUNSUPPORTED, "d %lld: a row kernel holds at most 8192 values", (long long)d.d);
+    if (d.k < 1 || d.k > 32 || d.k > d.experts) return model_fail(Q8_EUNSUPPORTED, "k %lld: 1 to 32 kept experts", (long long)d.k);
+    if (d.experts > 8192) return model_fail(Q8_EUNSUPPORTED, "%lld experts: at most 8192", (long long)d.experts);
+    if (d.ctx > (1 << 24) || d.vocab > (1 << 30)) return model_fail(Q8_EUNSUPPORTED, "ctx or vocab past the index range");
+    if (!(d.eps >= 0.f) || !(d.rope_theta > 0.0)) return model_fail(Q8_EINVAL, "eps or rope_theta out of range");
+    if (!d.embed || !d.final_norm || !d.tok || !d.pos) return model_fail(Q8_EINVAL, "embed, final_norm, tok or pos: null");
+    if (!d.attn_norm || !d.ffn_norm || !d.q_norm || !d.k_norm || !d.wq || !d.wk || !d.wv || !d.wo || !d.router ||
+        !d.gate || !d.up || !d.down || !d.k_cache || !d.v_cache)
+        return model_fail(Q8_EINVAL, "a per-layer array: null");
+    const int64_t D = d.d, QD = d.heads * d.head_dim, KD = d.kv_heads * d.head_dim;
+    for (int64_t l = 0; l < d.layers; ++l) {
+        if (!d.attn_norm[l] || !d.ffn_norm[l] || !d.q_norm[l] || !d.k_norm[l] || !d.k_cache[l] || !d.v_cache[l])
+            return model_fail(Q8_EINVAL, "layer %lld: a null norm weight or cache", (long long)l);
+        int r;
+        if ((r = check_mat_shape(d.wq[l], QD, D, "wq", l)) || (r = check_mat_shape(d.wk[l], KD, D, "wk", l)) ||
+            (r = check_mat_shape(d.wv[l], KD, D, "wv", l)) || (r = check_mat_shape(d.wo[l], D, QD, "wo", l)) ||
+            (r = check_mat_shape(d.router[l], d.experts, D, "router", l)) ||
+            (r = check_mat_shape(d.gate[l], d.experts * d.dff, D, "gate", l)) ||
+            (r = check_mat_shape(d.up[l], d.experts * d.dff, D, "up", l)) ||
+            (r = check_mat_shape(d.down[l], d.experts * D, d.dff, "down", l)))
+            return r;
+    }
+    if (int r = check_mat_shape(d.lm_head, d.vocab, D, "lm_head", 0)) return r;
+
+    q8_model* m = new q8_model();
+    m->d = d;
+    m->attn_norm.assign(d.attn_norm, d.attn_norm + d.layers);
+    m->ffn_norm.assign(d.ffn_norm, d.ffn_norm + d.layers);
+    m->q_norm.assign(d.q_norm, d.q_norm + d.layers);
+    m->k_norm.assign(d.k_norm, d.k_norm + d.layers);
+    m->wq.assign(d.wq, d.wq + d.layers);
+    m->wk.assign(d.wk, d.wk + d.layers);
+    m->wv.assign(d.wv, d.wv + d.layers);
+    m->wo.assign(d.wo, d.wo + d.layers);
+    m->router.assign(d.router, d.router + d.layers);
+    m->gate.assign(d.gate, d.gate + d.layers);
+    m->up.assign(d.up, d.up + d.layers);
+    m->down.assign(d.down, d.down + d.layers);
+    m->kc.assign(d.k_cache, d.k_cache + d.layers);
+    m->vc.assign(d.v_cache, d.v_cache + d.layers);
+    // pointers into the caller's arrays are not kept
+    m->d.attn_norm = m->d.ffn_norm = m->d.q_norm = m->d.k_norm = nullptr;
+    m->d.wq = m->d.wk = m->d.wv = m->d.wo = m->d.router = m->d.gate = m->d.up = m->d.down = nullptr;
+    m->d.k_cache = m->d.v_cache = nullptr;
+
+    // one arena for the step's activations (sizes rounded to 256 B each)
+    const int64_t KF = d.k * d.dff;
+    const size_t half = (size_t)d.head_dim / 2;
+    size_t need = 0;
+    auto add = [&](size_t bytes) { need += (bytes + 255) & ~size_t(255); };
+    add(D * 4);          // h
+    add(D * 4);          // x
+    add(QD * 4);         // q
+    add(KD * 4);         // k
+    add(KD * 4);         // v
+    add(QD * 4);         // att
+    add(d.logits ? 0 : d.vocab * 4);
+    add(d.ctx * half * 4);  // cos
+    add(d.ctx * half * 4);  // sin
+    add(KF * 4);         // hbuf
+    add(d.k * 4);        // gates
+    add(d.experts * 4);  // router logits
+    add(D);              // xq
+    add(D / 32 * 4);     // xs
+    add(QD);             // attq
+    add(QD / 32 * 4);    // atts
+    add(KF);             // hq
+    add(KF / 32 * 4);    // hs
+    add(d.k * 4);        // ids
+    add(256);            // err
+    need += 4096;
+    cudaError_t e = cudaMalloc(&m->arena, need);
+    if (e != cudaSuccess) {
+        delete m;
+        return model_fail(Q8_ECUDA, "q8_model_create: %s", cudaGetErrorString(e));
+    }
+    m->arena_bytes = need;
+    char* at = m->arena;
+    m->h = carve_arena<float>(at, D);
+    m->x = carve_arena<float>(at, D);
+    m->q = carve_arena<float>(at, QD);
+    m->k = carve_arena<float>(at, KD);
+    m->v = carve_arena<float>(at, KD);
+    m->att = carve_arena<float>(at, QD);
+    m->logits = d.logits ? d.logits : carve_arena<float>(at, d.vocab);
+    m->cos_t = carve_arena<float>(at, d.ctx * half);
+    m->sin_t = carve_arena<float>(at, d.ctx * half);
+    m->hbuf = carve_arena<float>(at, KF);
+    m->gates = carve_arena<float>(at, d.k);
+    m->rlog = carve_arena<float>(at, d.experts);
+    m->xq = carve_arena<int8_t>(at, D);
+    m->xs = carve_arena<float>(at, D / 32);
+    m->attq = carve_arena<int8_t>(at, QD);
+    m->atts = carve_arena<float>(at, QD / 32);
+    m->hq = carve_arena<int8_t>(at, KF);
+    m->hs = carve_arena<float>(at, KF / 32);
+    m->ids = carve_arena<int32_t>(at, d.k);
+    m->err = carve_arena<int>(at, 64);
+    if (d.mode == Q8_F32ACT_F64SUM) {
+        m->xq = nullptr;
+        m->xs = nullptr;
+        m->attq = nullptr;
+        m->atts = nullptr;
+        m->hq = nullptr;
+        m->hs = nullptr;
+    }
+    // workspace: the largest single launch's scratch (launches of a step run one after another)
+    m->ws_bytes = size_t(64) << 20;
+    m->n_counters = size_t(1) << 20;
+    e = cudaMalloc(&m->ws, m->ws_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&m->counters, m->n_counters * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(m->counters, 0, m->n_counters * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(m->err, 0, 256);
+    if (e == cudaSuccess) e = launch_rope_table(m->cos_t, m->sin_t, (int)d.ctx, (int)half, d.rope_theta, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        q8_model_destroy(m);
+        return model_fail(Q8_ECUDA, "q8_model_create: %s", cudaGetErrorString(e));
+    }
+    *out = m;
+    return Q8_OK;
+}
+
+void q8_model_destroy(q8_model* m) {
+    if (!m) return;
+    if (m->exec) cudaGraphExecDestroy(m->exec);
+    if (m->cap) cudaStreamDestroy(m->cap);
+    cudaFree(m->arena);
+    cudaFree(m->ws);
+    cudaFree(m->counters);
+    delete m;
+}
+
+int decode_step_launches(q8_model* m, q8_stream stream) {
+    if (!m) return model_fail(Q8_EINVAL, "model: null");
+    cudaError_t e = step_launches(m, (cudaStream_t)stream);
+    return e == cudaSuccess ? Q8_OK : model_fail(Q8_ECUDA, "decode_step_launches: %s", cudaGetErrorString(e));
+}
+
+int decode_step(q8_model* m, q8_stream stream) {
+    if (!m) return model_fail(Q8_EINVAL, "model: null");
+    cudaError_t e = cudaSuccess;
+    if (!m->exec) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing((cudaStream_t)stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone)
+            return model_fail(Q8_EINVAL, "decode_step: the first call captures the step and cannot run inside a capture");
+        if (!m->cap) {
+            e = cudaStreamCreateWithFlags(&m->cap, cudaStreamNonBlocking);
+            if (e != cudaSuccess) return model_fail(Q8_ECUDA, "decode_step: %s", cudaGetErrorString(e));
+        }
+        cudaGraph_t graph = nullptr;
+        e = cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal);
+        if (e == cudaSuccess) {
+            cudaError_t le = step_launches(m, m->cap);
+            e = cudaStreamEndCapture(m->cap, &graph);
+            if (le != cudaSuccess) e = le;
+        }
+        if (e == cudaSuccess) e = cudaGraphInstantiate(&m->exec, graph, 0);
+        if (graph) cudaGraphDestroy(graph);
+        if (e != cudaSuccess) {
+            m->exec = nullptr;
+            return model_fail(Q8_ECUDA, "decode_step capture: %s", cudaGetErrorString(e));
+        }
+    }
+    e = cudaGraphLaunch(m->exec, (cudaStream_t)stream);
+    return e == cudaSuccess ? Q8_OK : model_fail(Q8_ECUDA, "decode_step: %s", cudaGetErrorString(e));
+}
+
+int q8_model_check(q8_model* m, q8_stream stream) {
+    if (!m) return model_fail(Q8_EINVAL, "model: null");
+    int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, m->err, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->err, 0, sizeof(int), (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return model_fail(Q8_ECUDA, "q8_model_check: %s", cudaGetErrorString(e));
+    if (v & 1) return model_fail(Q8_EINVAL, "a step read a token outside [0, vocab)");
+    if (v & 2) return model_fail(Q8_EINVAL, "a step met a position outside [0, ctx)");
+    return Q8_OK;
+}
+
+}  // extern "C"

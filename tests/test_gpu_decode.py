@@ -1,0 +1,130 @@
+"""The decode step (embedding, 48-layer shape, LM head, greedy token) against the oracle, and graph replay."""
+import numpy as np
+import pytest
+
+import oracle
+from synth import recipes
+
+pytestmark = pytest.mark.gpu
+
+TOL = {0: 1e-4, 1: 2e-3}
+
+
+def rel_err(gpu, ora):
+    gpu = np.asarray(gpu, np.float64)
+    ora = np.asarray(ora, np.float64)
+    return float(np.max(np.abs(gpu - ora)) / max(np.max(np.abs(ora)), 1e-300))
+
+
+def build(q8, cfg, seed, mode):
+    import torch
+    arr = recipes.decode_model(cfg, seed)
+
+    def dv(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    t = {}
+    for key, v in arr.items():
+        if isinstance(v, list):
+            t[key] = [tuple(dv(x) for x in e) if isinstance(e, tuple) else dv(e) for e in v]
+        elif isinstance(v, tuple):
+            t[key] = tuple(dv(x) for x in v)
+        else:
+            t[key] = dv(v)
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pos = torch.zeros(1, dtype=torch.int32, device="cuda")
+    logits = torch.empty(cfg["vocab"], dtype=torch.float32, device="cuda")
+    m = q8.Model(cfg, t, mode, tok, pos, logits)
+    return m, arr, t, tok, pos, logits
+
+
+SMALL = dict(layers=2, d=256, heads=8, kv_heads=2, hd=128, experts=16, k=4, dff=64, vocab=1000, ctx=96, eps=1e-6,
+             rope_theta=1e6)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_decode_small_matches_oracle_over_steps(q8, mode):
+    import torch
+    cfg = SMALL
+    m, arr, t, tok, pos, logits = build(q8, cfg, 5, mode)
+    om = oracle.ModelArrays(cfg, **arr)
+    cur_tok, cur_pos = 7, 60
+    tok.fill_(cur_tok)
+    pos.fill_(cur_pos)
+    for step in range(4):
+        nxt, ora_logits = oracle.decode_step(mode, om, cur_tok, cur_pos)
+        if step % 2 == 0:
+            m.step()            # graph replay (captured on the first call)
+        else:
+            m.step_launches()   # plain launches
+        torch.cuda.synchronize()
+        gl = logits.cpu().numpy()
+        assert rel_err(gl, ora_logits) < TOL[mode], (step, rel_err(gl, ora_logits))
+        srt = np.sort(ora_logits)[::-1]
+        if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
+            assert int(tok.item()) == nxt
+        assert int(pos.item()) == cur_pos + 1
+        # the step wrote its key/value rows at cur_pos
+        for l in range(cfg["layers"]):
+            kc = t["k_cache"][l].cpu().numpy()
+            assert rel_err(kc[:, cur_pos], om.k_cache[l][:, cur_pos]) < 10 * TOL[mode]
+        cur_tok, cur_pos = int(tok.item()), cur_pos + 1
+    m.check()
+    m.close()
+
+
+def test_decode_graph_equals_launches_bitwise(q8):
+    import torch
+    cfg = SMALL
+    outs = []
+    for use_graph in (True, False):
+        m, arr, t, tok, pos, logits = build(q8, cfg, 6, 1)
+        tok.fill_(3)
+        pos.fill_(10)
+        for _ in range(3):
+            (m.step if use_graph else m.step_launches)()
+        torch.cuda.synchronize()
+        outs.append((logits.cpu().numpy().copy(), int(tok.item()), int(pos.item()),
+                     t["k_cache"][1].cpu().numpy().copy()))
+        m.close()
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    assert outs[0][1:3] == outs[1][1:3]
+    np.testing.assert_array_equal(outs[0][3], outs[1][3])
+
+
+def test_decode_bad_position_is_refused_on_device(q8):
+    import torch
+    m, arr, t, tok, pos, logits = build(q8, SMALL, 7, 0)
+    tok.fill_(1)
+    pos.fill_(SMALL["ctx"])  # one past the cache
+    before = [c.clone() for c in t["k_cache"]]
+    m.step()
+    torch.cuda.synchronize()
+    assert int(pos.item()) == SMALL["ctx"] and int(tok.item()) == 1
+    for a, b in zip(before, t["k_cache"]):
+        assert torch.equal(a, b)
+    with pytest.raises(q8.Q8Error, match="position"):
+        m.check()
+    m.close()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", [1, 0])
+def test_decode_full_config_one_step(q8, mode):
+    """The full 48-layer configuration at the last cache position (every cached row attended), one step."""
+    import torch
+    cfg = recipes.DECODE
+    m, arr, t, tok, pos, logits = build(q8, cfg, 0, mode)
+    om = oracle.ModelArrays(cfg, **arr)
+    tok.fill_(0)
+    pos.fill_(cfg["ctx"] - 1)
+    m.step()
+    torch.cuda.synchronize()
+    nxt, ora_logits = oracle.decode_step(mode, om, 0, cfg["ctx"] - 1)
+    gl = logits.cpu().numpy()
+    err = rel_err(gl, ora_logits)
+    assert err < TOL[mode], err
+    srt = np.sort(ora_logits)[::-1]
+    if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
+        assert int(tok.item()) == nxt
+    m.close()

@@ -1,0 +1,68 @@
+"""Host-side checks that need no GPU: the C-ABI library loads, exports every declared entry point, and refuses bad
+arguments by name before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def q8():
+    from moe_add_rmsnorm_gb300 import build
+    build.build()
+    import moe_add_rmsnorm_gb300 as m
+    return m
+
+
+def declared():
+    text = open(os.path.join(ROOT, "include", "q8moe.h")).read()
+    return re.findall(r"^Q8_API\s+[\w\s\*]*?\b(\w+)\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared())
+    for n in ("q8_gemv", "add_rmsnorm_q8", "moe_route_topk", "moe_gate_up", "moe_down_combine", "decode_step"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(q8):
+    lib = ctypes.CDLL(q8.LIB_PATH)
+    for name in declared():
+        assert hasattr(lib, name), name
+    assert set(declared()) == set(q8.EXPORTS)
+
+
+def test_refusals_before_any_launch(q8):
+    lib = q8.lib
+    W = q8.q8_mat(None, None, 4, 64)
+    assert lib.q8_gemv(ctypes.byref(W), 0, None, None, 1, None, None, None) == -1
+    assert "y: null" in q8.last_error()
+    assert lib.q8_gemv(ctypes.byref(W), 0, None, None, 1, ctypes.c_void_p(256), None, None) == -1
+    assert "W" in q8.last_error()
+    W = q8.q8_mat(64, 64, 4, 40)  # fake aligned addresses: refused on shape before any use
+    y = ctypes.c_void_p(256)
+    assert lib.q8_gemv(ctypes.byref(W), 0, ctypes.c_void_p(512), None, 1, y, None, None) == -2
+    assert "32-value" in q8.last_error()
+    R = q8.q8_mat(64, 64, 128, 2048)
+    ids = ctypes.c_void_p(1024)
+    assert lib.moe_route_topk(ctypes.byref(R), 0, ctypes.c_void_p(512), None, 1, 33, ids, ids, None, None,
+                              ctypes.c_void_p(8), None) == -2
+    assert "k 33" in q8.last_error()
+    assert lib.moe_route_topk(ctypes.byref(R), 0, ctypes.c_void_p(512), None, 1, 0, ids, ids, None, None,
+                              ctypes.c_void_p(8), None) == -2
+    Rbig = q8.q8_mat(64, 64, 8193, 2048)
+    assert lib.moe_route_topk(ctypes.byref(Rbig), 0, ctypes.c_void_p(512), None, 1, 8, ids, ids, None, None,
+                              ctypes.c_void_p(8), None) == -2
+    assert "8192" in q8.last_error()
+    assert lib.add_rmsnorm_q8(ctypes.c_void_p(512), None, ctypes.c_void_p(512), 1, 2048, ctypes.c_float(-1.0), None,
+                              ctypes.c_void_p(512), None, None) == -1
+    assert "eps" in q8.last_error()
+    d = q8.q8_model_desc()
+    d.layers, d.d, d.heads, d.kv_heads, d.head_dim = 1, 2048, 32, 4, 64
+    d.experts, d.k, d.dff, d.vocab, d.ctx = 128, 8, 768, 100, 16
+    h = ctypes.c_void_p()
+    assert lib.q8_model_create(ctypes.byref(d), ctypes.byref(h)) == -2
+    assert "head_dim" in q8.last_error()
