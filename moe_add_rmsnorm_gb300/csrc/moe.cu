@@ -138,7 +138,10 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
     const int n = p.R * p.K;
     for (int e = threadIdx.x; e < p.E; e += TOPK_THREADS) cnt[e] = 0;
     __syncthreads();
-    for (int c = threadIdx.x; c < n; c += TOPK_THREADS) atomicAdd(&cnt[p.ids[c]], 1);
+    for (int c = threadIdx.x; c < n; c += TOPK_THREADS) {
+        const int e = p.ids[c];
+        if (e >= 0 && e < p.E) atomicAdd(&cnt[e], 1);  // a row whose logits were all NaN chose no expert
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < p.E; e += TOPK_THREADS) {
         p.counts[e] = cnt[e];
@@ -152,11 +155,12 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
         if (p.counts[e] > 0) p.active[1 + flag[e]] = e;
     }
     if (threadIdx.x == 0) {
-        p.offsets[p.E] = n;
+        p.offsets[p.E] = cnt[p.E - 1] + p.counts[p.E - 1];
         p.active[0] = nactive;
     }
     for (int c = threadIdx.x; c < n; c += TOPK_THREADS) {
         const int e = p.ids[c];
+        if (e < 0 || e >= p.E) continue;
         int rank = 0;
         for (int c2 = 0; c2 < c; ++c2) rank += (p.ids[c2] == e);
         p.lists[cnt[e] + rank] = c;

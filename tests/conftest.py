@@ -37,7 +37,7 @@ def q8():
     """The CUDA library's Python binding, built for sm_103a on first use; GPU tests only."""
     if not gpu_available():
         pytest.skip("no CUDA device")
-    from moe_add_rmsnorm_gb300 import build as pkg_build
-    pkg_build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import moe_add_rmsnorm_gb300 as m
     return m

@@ -11,8 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def q8():
-    from moe_add_rmsnorm_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import moe_add_rmsnorm_gb300 as m
     return m
 
