@@ -1,0 +1,379 @@
+"""Decode-step throughput of the Q8_0 mixture-of-experts model on GB300.
+
+Workload: the full decode step of 48 layers (d=2048, 32 query / 4 key-value heads of 128, RoPE theta 1e6, f32 KV cache
+of 4096 positions, 128 experts keep 8 of dff 768, vocab 151936 Q8_0 LM head, greedy arg-max), random-init Q8_0 weights
+from the seeded generator.  One step = one token = one replay of the captured CUDA graph; the position advances each
+step (a growing cache, tg-style) and ends at the last cache position.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead (a bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--mode", default="int8", choices=["int8", "f32"])
+    ap.add_argument("--layers", type=int, default=48)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi samples of one GPU during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[4:8]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_model_tensors(cfg, seed=0):
+    """Host arrays in pinned memory (from the seeded generator) and their device copies."""
+    import numpy as np
+    import torch
+    from synth import recipes
+
+    dtypes = {np.dtype(np.int8): torch.int8, np.dtype(np.float32): torch.float32}
+    host = recipes.decode_model(cfg, seed, alloc=lambda shape, dt: torch.empty(shape, dtype=dtypes[np.dtype(dt)],
+                                                                               pin_memory=True),
+                                ptr=lambda t: t.data_ptr())
+
+    def up(v):
+        if isinstance(v, list):
+            return [up(e) for e in v]
+        if isinstance(v, tuple):
+            return tuple(up(e) for e in v)
+        return v.cuda(non_blocking=True)
+
+    dev = {k: up(v) for k, v in host.items()}
+    torch.cuda.synchronize()
+    return host, dev
+
+
+def time_dominant_kernel(q8, cfg, dev, mode, reps, stream):
+    """The mixture's gate-up kernel at the decode shape (8 experts x 768 gate and 768 up rows of 2048), launched over
+    the layers' own stacked matrices in turn (each launch reads weights no earlier launch brought into L2), timed with
+    CUDA events on its stream.  Returns (average seconds per launch, algorithmic bytes per launch)."""
+    import torch
+    L, d, dff, K, E = cfg["layers"], cfg["d"], cfg["dff"], cfg["k"], cfg["experts"]
+    ws = q8.Workspace(64 << 20)
+    s = torch.cuda.ExternalStream(stream)
+    with torch.cuda.stream(s):
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(0)
+        x = torch.randn(1, d, device="cuda", generator=gen)
+        xq = torch.empty(1, d, dtype=torch.int8, device="cuda")
+        xs = torch.empty(1, d // 32, dtype=torch.float32, device="cuda")
+        q8.q8_quantize(x, xq, xs, stream=stream)
+        ids = torch.stack([torch.randperm(E, device="cuda", generator=gen)[:K] for _ in range(L)]).to(torch.int32)
+        h = torch.empty(K, dff, device="cuda")
+
+        def one(l):
+            g, u = dev["gate"][l], dev["up"][l]
+            if mode == 1:
+                q8.moe_gate_up(*g, *u, dff, 1, K, ids[l], h, xq=xq, xs=xs, ws=ws, stream=stream)
+            else:
+                q8.moe_gate_up(*g, *u, dff, 0, K, ids[l], h, x=x, ws=ws, stream=stream)
+
+        for l in range(min(L, 4)):
+            one(l)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.synchronize()
+        start.record(s)
+        n = 0
+        for _ in range(reps):
+            for l in range(L):
+                one(l)
+                n += 1
+        end.record(s)
+        end.synchronize()
+    ws.close()
+    sec = start.elapsed_time(end) / 1e3 / n
+    return sec, K * 2 * dff * d * 9 // 8
+
+
+def cpu_baseline_oracle(cfg, host, mode, tok, pos):
+    """The oracle's whole decode step for one token on this host (single thread), from the same host arrays."""
+    import oracle
+
+    def np_(v):
+        if isinstance(v, list):
+            return [np_(e) for e in v]
+        if isinstance(v, tuple):
+            return tuple(np_(e) for e in v)
+        return v.numpy()
+
+    arr = {k: np_(v) for k, v in host.items()}
+    arr["k_cache"] = [c.copy() for c in arr["k_cache"]]
+    arr["v_cache"] = [c.copy() for c in arr["v_cache"]]
+    om = oracle.ModelArrays(cfg, **arr)
+    t0 = time.perf_counter()
+    oracle.decode_step(mode, om, tok, pos)
+    dt = time.perf_counter() - t0
+    return 1.0 / dt, dt
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle (the only other implementation of what the pages define), each step a bounded
+    sample of the decode step — one layer of the 48 (layer = step mod 48) plus 1/48 of the LM head — scaled to
+    tokens/s as 1 / (48 x sample time)."""
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import synth
+    from synth import recipes
+    cfg = dict(recipes.DECODE)
+    L = cfg["layers"]
+    one = dict(cfg, layers=1, vocab=cfg["vocab"] // L)
+    mode = 1 if args.mode == "int8" else 0
+    pos = cfg["ctx"] - 1
+    base = recipes.decode_model(one, seed=0)
+    times = []
+    for step in range(args.warmup + args.steps):
+        ids = recipes.layer_ids(step % L)
+        arr = dict(base)
+        for key in ("wq", "wk", "wv", "wo", "router", "gate", "up", "down"):
+            n, k = base[key][0][0].shape
+            arr[key] = [synth.q8_matrix(n, k, 0, ids[key])]  # this step's layer (generated outside the timing)
+        arr["k_cache"] = [c.copy() for c in base["k_cache"]]
+        arr["v_cache"] = [c.copy() for c in base["v_cache"]]
+        om = oracle.ModelArrays(one, **arr)
+        t0 = time.perf_counter()
+        oracle.decode_step(mode, om, 0, pos)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+    per_token = L * float(np.mean(times))
+    value = 1.0 / per_token
+    line = {
+        "impl": "reference", "metric": "decode tokens/s (Q8_0 MoE, 48 layers) and Q8_0 weight-stream GB/s",
+        "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_token * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "i8" if mode else "f32", "data": "synthetic",
+        "config": {"workload": "decode step, 48 layers d=2048 32q/4kv hd128 E=128 K=8 dff=768 vocab=151936 "
+                               "ctx=4096 (full decode configuration)", "mode": args.mode},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "per step: one decoder layer (layer = step mod 48) plus 1/48 of the LM head rows "
+                                   "at position 4095, single-threaded f64 C oracle, scaled x48 to one token"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import numpy as np
+    import torch
+    import moe_add_rmsnorm_gb300 as q8
+    from synth import recipes
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    cfg = dict(recipes.DECODE, layers=args.layers)
+    mode = q8.INT8ACT if args.mode == "int8" else q8.F32ACT_F64SUM
+    host, dev = make_model_tensors(cfg, seed=0)
+    total = args.warmup + args.steps
+    start_pos = cfg["ctx"] - total
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pos = torch.full((1,), start_pos, dtype=torch.int32, device="cuda")
+    logits = torch.empty(cfg["vocab"], device="cuda")
+    model = q8.Model(cfg, dev, mode, tok, pos, logits)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # device-timed region: inputs resident in HBM, one graph replay per token
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            model.step(sh)
+        stream.synchronize()
+        barrier()
+        clocks = Clocks(local)
+        clocks.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            model.step(sh)
+        e1.record(stream)
+        e1.synchronize()
+        clk = clocks.stop()
+        torch.cuda.synchronize()
+        barrier()
+    sec = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([sec], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        sec = float(t.item())
+    model.check(sh)
+    value = world * args.steps / sec
+    ms_per_step = sec / args.steps * 1e3
+
+    # end to end: each token's inputs (token, position) copied from pinned host memory, the next token read back
+    pin_in = torch.zeros(2, dtype=torch.int32).pin_memory()
+    pin_out = torch.zeros(1, dtype=torch.int32).pin_memory()
+    e2e_steps = min(args.steps, 64)
+    with torch.cuda.stream(stream):
+        stream.synchronize()
+        t0 = time.perf_counter()
+        cur = 0
+        for i in range(e2e_steps):
+            pin_in[0] = cur
+            pin_in[1] = cfg["ctx"] - e2e_steps + i
+            tok.copy_(pin_in[0:1], non_blocking=True)
+            pos.copy_(pin_in[1:2], non_blocking=True)
+            model.step(sh)
+            pin_out.copy_(tok, non_blocking=True)
+            stream.synchronize()
+            cur = int(pin_out[0])
+        e2e_sec = time.perf_counter() - t0
+    e2e = {"value": world * e2e_steps / e2e_sec, "unit": "tokens/s", "h2d_bytes_per_step": 8,
+           "d2h_bytes_per_step": 4, "steps": e2e_steps}
+
+    wbytes = recipes.weight_bytes_per_token(cfg)
+    kv_mean = float(np.mean([recipes.kv_bytes_per_token(cfg, start_pos + args.warmup + i) for i in range(args.steps)]))
+    peak, peak_kind = peaks()
+    weight_gbs = wbytes * args.steps / sec / 1e9
+    total_gbs = (wbytes + kv_mean) * args.steps / sec / 1e9
+
+    line = {
+        "metric": "decode tokens/s (Q8_0 MoE, 48 layers) and Q8_0 weight-stream GB/s", "value": value,
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "i8" if mode == q8.INT8ACT else "f32", "data": "synthetic",
+        "config": {"workload": f"decode step, {cfg['layers']} layers d=2048 32q/4kv hd128 E=128 K=8 dff=768 "
+                               "vocab=151936 ctx=4096 (full decode configuration), tg-style growing cache",
+                   "mode": "int8-activation" if mode == q8.INT8ACT else "f32-activation/f64-sum",
+                   "positions": [start_pos + args.warmup, cfg["ctx"] - 1],
+                   "l2": "inputs larger than L2: every step streams 3.42 GB of weights and ~0.8 GB of cache",
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "weight_stream": {"gbs": weight_gbs, "frac_of_peak": weight_gbs / peak, "bytes_per_token": wbytes,
+                          "peak_gbs": peak, "peak_kind": peak_kind},
+        "hbm_total_gbs": total_gbs,
+        "gpu_launches": model_launches(cfg) * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+
+    if rank == 0:
+        dom_sec, dom_bytes = time_dominant_kernel(q8, cfg, dev, mode, reps=4, stream=sh)
+        achieved = dom_bytes / dom_sec / 1e9
+        line["roofline"] = {"bound": "hbm", "kernel": "moe_gate_up (8 experts x 2 x 768 rows of 2048)",
+                            "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                            "traffic": None, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+                            "us_per_launch": dom_sec * 1e6, "algorithmic_bytes_per_launch": dom_bytes}
+        if not args.no_secondary:
+            other = q8.F32ACT_F64SUM if mode == q8.INT8ACT else q8.INT8ACT
+            m2 = q8.Model(cfg, dev, other, tok, pos, logits)
+            pos.fill_(cfg["ctx"] - total)
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    m2.step(sh)
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                for _ in range(args.steps):
+                    m2.step(sh)
+                a1.record(stream)
+                a1.synchronize()
+            s2 = a0.elapsed_time(a1) / 1e3
+            line["secondary"] = {"mode": "f32-activation/f64-sum" if other == q8.F32ACT_F64SUM else "int8-activation",
+                                 "tokens_per_s": args.steps / s2, "weight_stream_gbs": wbytes * args.steps / s2 / 1e9}
+            m2.close()
+        if not args.no_cpu_baseline:
+            v, dt = cpu_baseline_oracle(cfg, host, 1 if mode == q8.INT8ACT else 0, 0, cfg["ctx"] - 1)
+            line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"one whole decode step (all {cfg['layers']} layers and the LM head) at "
+                                              f"position 4095, single-threaded f64 C oracle, {dt:.1f} s"}
+        print(json.dumps(line), flush=True)
+    model.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def model_launches(cfg):
+    """Kernels one decode step launches: 10 per layer (norm, q/k/v, QK-norm+RoPE+KV, attention, O projection, norm,
+    router, top-k, gate-up, down-combine) plus the final norm, the LM head and the arg-max."""
+    return cfg["layers"] * 10 + 3
+
+
+if __name__ == "__main__":
+    main()
