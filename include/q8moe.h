@@ -120,6 +120,21 @@ Q8_API int q8_gemv(const q8_mat *W, q8_mode mode, const float *x, const q8_act *
 Q8_API int q8_gemv_blockdots(const q8_mat *W, const q8_act *xq, int64_t rows, int32_t *dots, float *y, q8_ws *ws,
                       q8_stream stream);
 
+/* q8_gemv without a workspace, for callers that cannot allocate device memory when they call it (code running inside
+ * an allocator's callbacks, loops that forbid allocation after start-up, hosts whose device memory another runtime
+ * has already handed out).  The pages have no counterpart: this is an addition for such callers.  Arguments and
+ * results are those of q8_gemv.  Scratch (the quantized activation when xq is NULL, and the partial sums of a matrix
+ * cut along k) comes from a fixed array of Q8_NOALLOC_SCRATCH_BYTES bytes and Q8_NOALLOC_COUNTERS counters that the
+ * library holds on every device that loads it, until the process exits; a call that would need more returns
+ * Q8_ENOSPACE and launches nothing.  The call allocates nothing and frees nothing.  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress); make that first call before any stream capture.  Every
+ * call on a device shares the one array: calls that overlap on the GPU (other streams, other threads) race and must
+ * be ordered by the caller. */
+#define Q8_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define Q8_NOALLOC_COUNTERS 65536u
+Q8_API int q8_gemv_noalloc(const q8_mat *W, q8_mode mode, const float *x, const q8_act *xq, int64_t rows, float *y,
+                           q8_stream stream);
+
 /* ---- a5-a8: the sparse mixture ------------------------------------------------------------------------------------ */
 
 /* Grouping of a chunk's choices by expert (lane_link.rs, Link::class_launch: MoeTokenSort; lane/arena.rs, scratch:

@@ -65,6 +65,7 @@ _SIGS = {
     "add_rmsnorm_q8": [_vp, _vp, _vp, _i64, _i64, _f32, _vp, _vp, _P(q8_act), _vp],
     "q8_gemv": [_P(q8_mat), _i32, _vp, _P(q8_act), _i64, _vp, _vp, _vp],
     "q8_gemv_blockdots": [_P(q8_mat), _P(q8_act), _i64, _vp, _vp, _vp, _vp],
+    "q8_gemv_noalloc": [_P(q8_mat), _i32, _vp, _P(q8_act), _i64, _vp, _vp],
     "moe_route_topk": [_P(q8_mat), _i32, _vp, _P(q8_act), _i64, _i32, _vp, _vp, _vp, _P(q8_moe_plan), _vp, _vp],
     "moe_gate_up": [_P(q8_mat), _P(q8_mat), _i64, _i32, _vp, _P(q8_act), _i64, _i32, _vp, _P(q8_moe_plan), _vp,
                     _P(q8_act), _vp, _vp],
@@ -158,6 +159,13 @@ def q8_gemv(q, s, mode, y, x=None, xq=None, xs=None, rows=1, ws=None, stream=Non
     qa = ctypes.byref(q8_act(xq.data_ptr(), xs.data_ptr())) if xq is not None else None
     _check(lib.q8_gemv(ctypes.byref(W), int(mode), _ptr(x), qa, rows, _ptr(y), ws.handle if ws else None,
                        _stream(stream)))
+
+
+def q8_gemv_noalloc(q, s, mode, y, x=None, xq=None, xs=None, rows=1, stream=None):
+    """q8_gemv without a workspace: scratch comes from the library's fixed per-device array (see q8moe.h)."""
+    W = mat(q, s)
+    qa = ctypes.byref(q8_act(xq.data_ptr(), xs.data_ptr())) if xq is not None else None
+    _check(lib.q8_gemv_noalloc(ctypes.byref(W), int(mode), _ptr(x), qa, rows, _ptr(y), _stream(stream)))
 
 
 def q8_gemv_blockdots(q, s, xq, xs, dots, y, rows=1, ws=None, stream=None):

@@ -396,3 +396,45 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
 }
 
 }  // extern "C"
+
+namespace q8 {
+
+// Scratch one q8_gemv call takes (bytes and arrival counters): the quantized activation when x is quantized inside
+// the call, then the partial sums of a projection cut along k; each region rounded up to 256 bytes as a workspace
+// carve rounds it.
+void gemv_call_scratch(const q8_mat* W, q8_mode mode, const q8_act* xq, int64_t rows, size_t* bytes,
+                       size_t* counters) {
+    GemvCall c;
+    c.mode = (int)mode;
+    c.k = W->cols;
+    c.nseg = 1;
+    c.seg[0].n = W->rows;
+    c.R = rows;
+    size_t b = 0;
+    auto region = [&](size_t n) { b = ((b + 255) & ~size_t(255)) + n; };
+    if (mode == Q8_INT8ACT && !xq) {
+        region((size_t)(rows * W->cols));
+        region((size_t)(rows * W->cols / 32) * sizeof(float));
+    }
+    size_t pb = 0, pc = 0;
+    gemv_scratch(c, &pb, &pc);
+    if (pb) region(pb);
+    *bytes = b;
+    *counters = pc;
+}
+
+// q8_gemv over scratch memory the caller already holds instead of a workspace.
+int gemv_over_scratch(const q8_mat* W, q8_mode mode, const float* x, const q8_act* xq, int64_t rows, float* y,
+                      char* scratch, size_t bytes, int* counters, size_t n_counters, cudaStream_t st,
+                      const char* who) {
+    g_err[0] = 0;
+    if (!y) return fail(Q8_EINVAL, "y: null");
+    q8_ws w;
+    w.scratch = scratch;
+    w.bytes = bytes;
+    w.counters = counters;
+    w.n_counters = n_counters;
+    return gemv_common(W, mode, x, xq, rows, y, nullptr, &w, st, who);
+}
+
+}  // namespace q8
