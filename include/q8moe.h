@@ -157,7 +157,8 @@ Q8_API int moe_route_topk(const q8_mat *router, q8_mode mode, const float *x, co
 /* Gate-up with SwiGLU (qwen_emit, MoeWeights: gate/up [E*dff, d] stacked, expert e's rows at e*dff; emit_moe_forward:
  * each expert's SwiGLU at an expert-indexed base): h[r][j][i] = silu(Wg[e*dff+i] . x_r) * (Wu[e*dff+i] . x_r) with
  * e = ids[r][j], silu(z) = z/(1+e^-z).  h: device f32 [rows][k][dff].  In Q8_INT8ACT mode hq (device, words
- * [rows*k*dff] + scales [rows*k*dff/32]) receives quantize(h) (dff % 32 == 0); in the other mode hq may be NULL.
+ * [rows*k*dff] + scales [rows*k*dff/32], or NULL) receives quantize(h) (dff % 32 == 0); in the other mode it is
+ * ignored.
  * plan (from moe_route_topk) is required when rows > 1: each expert's weights are then read once for all its rows. */
 Q8_API int moe_gate_up(const q8_mat *gate, const q8_mat *up, int64_t dff, q8_mode mode, const float *x, const q8_act *xq,
                 int64_t rows, int k, const int32_t *ids, const q8_moe_plan *plan, float *h, const q8_act *hq,
@@ -165,7 +166,8 @@ Q8_API int moe_gate_up(const q8_mat *gate, const q8_mat *up, int64_t dff, q8_mod
 
 /* Down-and-combine (qwen_emit, MoeWeights: down [E*d, dff] stacked, expert e's rows at e*d; emit_moe_forward: the
  * weighted combine): y[r] = residual[r] + sum_j gates[r][j] * (Wd[e*d .. e*d+d) . h[r][j]), the sum over j in order.
- * Mode Q8_F32ACT_F64SUM reads h; mode Q8_INT8ACT reads hq.  residual may be NULL (and may alias y); y is device f32
+ * Mode Q8_F32ACT_F64SUM reads h; mode Q8_INT8ACT reads hq, or quantizes h when hq is NULL.  residual may be NULL (and
+ * may alias y); y is device f32
  * [rows][d]; expert_out (device f32 [rows][k][d] or NULL) receives each expert's unweighted output. */
 Q8_API int moe_down_combine(const q8_mat *down, int64_t d, q8_mode mode, const float *h, const q8_act *hq, int64_t rows,
                      int k, const int32_t *ids, const float *gates, const q8_moe_plan *plan, const float *residual,

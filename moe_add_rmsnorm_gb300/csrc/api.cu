@@ -306,9 +306,12 @@ int moe_gate_up(const q8_mat* gate, const q8_mat* up, int64_t dff, q8_mode mode,
     if (mode == Q8_F32ACT_F64SUM && (!x || !aligned(x, 16))) return fail(Q8_EINVAL, "x: null or not 16-byte aligned");
     if (mode == Q8_INT8ACT) {
         if (int r = check_act(xq, "xq")) return r;
-        if (int r = check_act(hq, "hq")) return r;
+        if (hq)
+            if (int r = check_act(hq, "hq")) return r;
         if (dff % 32) return fail(Q8_EUNSUPPORTED, "dff %lld: the int8 epilogue needs whole 32-row blocks", (long long)dff);
     }
+    if (!experts_supported((int)mode, gate->cols))
+        return fail(Q8_EUNSUPPORTED, "d %lld: an expert row wider than one pass of the kernel", (long long)gate->cols);
     if (plan)
         if (int r = check_plan(plan)) return r;
     if (rows == 0) return Q8_OK;
@@ -329,8 +332,6 @@ int moe_gate_up(const q8_mat* gate, const q8_mat* up, int64_t dff, q8_mode mode,
     c.xq = mode == Q8_INT8ACT ? xq->q : nullptr;
     c.xs = mode == Q8_INT8ACT ? xq->s : nullptr;
     c.h = h;
-    c.hq = mode == Q8_INT8ACT ? hq->q : nullptr;
-    c.hs = mode == Q8_INT8ACT ? hq->s : nullptr;
     if (plan) {
         c.plan.counts = plan->counts;
         c.plan.offsets = plan->offsets;
@@ -338,10 +339,8 @@ int moe_gate_up(const q8_mat* gate, const q8_mat* up, int64_t dff, q8_mode mode,
         c.plan.active = plan->active;
     }
     Carve cv = ws->carve();
-    size_t need = 0, cnt = 0;
-    gate_up_scratch(c, &need, &cnt);
     cudaError_t e = launch_gate_up(c, cv, st);
-    if (cv.overflow) return fail(Q8_ENOSPACE, "moe_gate_up: workspace too small (%zu bytes, %zu counters)", need, cnt);
+    if (e == cudaSuccess && mode == Q8_INT8ACT && hq) e = launch_quantize(h, rows * k * dff, hq->q, hq->s, st);
     return e == cudaSuccess ? Q8_OK : cuda_fail(e, "moe_gate_up");
 }
 
@@ -358,8 +357,15 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
     if (rows < 0) return fail(Q8_EINVAL, "rows negative");
     if (rows > 1 && !plan) return fail(Q8_EINVAL, "plan: null (a chunk of %lld rows is grouped by expert)", (long long)rows);
     if (mode == Q8_F32ACT_F64SUM && (!h || !aligned(h, 16))) return fail(Q8_EINVAL, "h: null or not 16-byte aligned");
-    if (mode == Q8_INT8ACT)
-        if (int r = check_act(hq, "hq")) return r;
+    if (mode == Q8_INT8ACT) {
+        if (hq) {
+            if (int r = check_act(hq, "hq")) return r;
+        } else if (!h || !aligned(h, 16)) {
+            return fail(Q8_EINVAL, "hq and h: both null (or h not 16-byte aligned)");
+        }
+    }
+    if (!experts_supported((int)mode, down->cols))
+        return fail(Q8_EUNSUPPORTED, "dff %lld: an expert row wider than one pass of the kernel", (long long)down->cols);
     if (plan)
         if (int r = check_plan(plan)) return r;
     if (rows == 0) return Q8_OK;
@@ -376,8 +382,11 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
     c.ids = ids;
     c.gates = gates;
     c.x = h;
-    c.xq = mode == Q8_INT8ACT ? hq->q : nullptr;
-    c.xs = mode == Q8_INT8ACT ? hq->s : nullptr;
+    if (mode == Q8_INT8ACT && hq) {
+        c.x = nullptr;
+        c.xq = hq->q;
+        c.xs = hq->s;
+    }
     c.residual = residual;
     c.y = y;
     c.expert_out = expert_out;
@@ -388,6 +397,16 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
         c.plan.active = plan->active;
     }
     Carve cv = ws->carve();
+    if (mode == Q8_INT8ACT && !hq && (rows > 1 || plan)) {  // a chunk reads its hidden rows quantized
+        int8_t* q = cv.take<int8_t>((size_t)(rows * k * down->cols));
+        float* s = cv.take<float>((size_t)(rows * k * down->cols / 32));
+        if (cv.overflow) return fail(Q8_ENOSPACE, "moe_down_combine: workspace too small for the quantized rows");
+        cudaError_t qe = launch_quantize(h, rows * k * down->cols, q, s, st);
+        if (qe != cudaSuccess) return cuda_fail(qe, "moe_down_combine");
+        c.x = nullptr;
+        c.xq = q;
+        c.xs = s;
+    }
     size_t need = 0, cnt = 0;
     down_scratch(c, &need, &cnt);
     cudaError_t e = launch_down_combine(c, cv, st);

@@ -68,6 +68,105 @@ __device__ __forceinline__ int block_dot_i8(const uint32_t (&w)[8], const uint32
     return d0 + d1;
 }
 
+// ---- a lane's tile of weights and activation blocks -------------------------------------------------------------
+// A lane owns BPL blocks (block indices bidx[j]) of RT consecutive rows.  The weights and scales of the whole tile are
+// loaded before any of them is used, so RT*BPL 32-byte loads are in flight per lane.
+template <int BPL, int RT>
+struct WTile {
+    uint32_t w[RT][BPL][8];
+    float s[RT][BPL];
+};
+
+template <int BPL, int RT>
+__device__ __forceinline__ void load_tile(WTile<BPL, RT>& t, const int8_t* __restrict__ q, const float* __restrict__ s,
+                                          int64_t row0, int nvalid, int64_t k, int nb, const int (&bidx)[BPL],
+                                          const bool (&bval)[BPL]) {
+#pragma unroll
+    for (int i = 0; i < RT; ++i)
+#pragma unroll
+        for (int j = 0; j < BPL; ++j) {
+            if (i < nvalid && bval[j]) {
+                ld_block_stream(q + (row0 + i) * k + bidx[j] * 32, t.w[i][j]);
+                t.s[i][j] = ld_scale_stream(s + (row0 + i) * nb + bidx[j]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t.w[i][j][e] = 0u;
+                t.s[i][j] = 0.f;
+            }
+        }
+}
+
+// The activation blocks a lane multiplies: f32 values (mode 0) or int8 words and their scales (mode 1).  The pointers
+// may be global or shared memory.
+template <int MODE, int BPL>
+struct XTile {
+    float f[MODE == 0 ? BPL : 1][MODE == 0 ? 32 : 1];
+    uint32_t w[MODE == 1 ? BPL : 1][8];
+    float s[BPL];
+};
+
+template <int MODE, int BPL>
+__device__ __forceinline__ void load_x(XTile<MODE, BPL>& x, const float* xf, const int8_t* xq, const float* xs,
+                                       const int (&bidx)[BPL], const bool (&bval)[BPL]) {
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+        if (MODE == 0) {
+            const float4* p = reinterpret_cast<const float4*>(xf + bidx[j] * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = bval[j] ? p[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                x.f[j][4 * i + 0] = v.x;
+                x.f[j][4 * i + 1] = v.y;
+                x.f[j][4 * i + 2] = v.z;
+                x.f[j][4 * i + 3] = v.w;
+            }
+            x.s[j] = 0.f;
+        } else {
+            if (bval[j]) {
+                const uint4* p = reinterpret_cast<const uint4*>(xq + bidx[j] * 32);
+                const uint4 a = p[0], b = p[1];
+                x.w[j][0] = a.x; x.w[j][1] = a.y; x.w[j][2] = a.z; x.w[j][3] = a.w;
+                x.w[j][4] = b.x; x.w[j][5] = b.y; x.w[j][6] = b.z; x.w[j][7] = b.w;
+                x.s[j] = xs[bidx[j]];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x.w[j][e] = 0u;
+                x.s[j] = 0.f;
+            }
+        }
+    }
+}
+
+template <int MODE>
+struct AccType;
+template <>
+struct AccType<0> {
+    using T = double;
+};
+template <>
+struct AccType<1> {
+    using T = float;
+};
+
+// This lane's share of row i of the tile: mode 0 adds each block's f32 partial, scaled, into f64; mode 1 scales each
+// block's exact int32 dot by both block scales and adds in f32.
+template <int MODE, int BPL, int RT>
+__device__ __forceinline__ typename AccType<MODE>::T tile_row_dot(const WTile<BPL, RT>& t, int i,
+                                                                  const XTile<MODE, BPL>& x) {
+    typename AccType<MODE>::T acc = 0;
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+        if (MODE == 0) {
+            const float ps = block_dot_f32(t.w[i][j], x.f[j]);
+            acc = fma((double)t.s[i][j], (double)ps, (double)acc);
+        } else {
+            const int D = block_dot_i8(t.w[i][j], x.w[j]);
+            acc = fmaf(t.s[i][j] * x.s[j], (float)D, (float)acc);
+        }
+    }
+    return acc;
+}
+
 // ---- reductions -----------------------------------------------------------------------------------------------
 
 template <int LANES, typename T>
@@ -114,5 +213,8 @@ __device__ __forceinline__ bool warp_arrive_last(int* counter, int expected) {
     if (last) __threadfence();
     return last;
 }
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 }  // namespace q8

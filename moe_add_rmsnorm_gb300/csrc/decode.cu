@@ -11,19 +11,22 @@
 // How (GB300 design): the f32 cache is the second-largest byte stream of the step (one key and one value row of 512 B
 // per position and key/value head), so the attention is a streaming kernel: every (key/value head, chunk of
 // positions) pair is one CTA that reads its rows once with coalesced 16-byte loads and serves all query heads of its
-// group from those registers; chunk partials (max, sum, weighted values) meet in scratch and the last CTA of a head
-// folds them in chunk order.  The 48 KiB static score row of the pages' design is not needed: a chunk's scores live in
-// shared memory and any cache length works.
+// group from those registers; chunk partials (max, sum, weighted values) are folded in chunk order, first inside a
+// thread-block cluster of 8 chunks through distributed shared memory, then across clusters by the last to arrive.  The
+// 48 KiB static score row of the pages' design is not needed: a chunk's scores live in shared memory and any cache
+// length works.
 #include <float.h>
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "kernels.h"
 
+namespace cg = cooperative_groups;
+
 namespace q8 {
 namespace {
 
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 // ==== QK-norm + RoPE + KV append =================================================================================
 
@@ -75,9 +78,11 @@ __global__ void __launch_bounds__(256) qk_rope_kv_kernel(const QkRopeCall c) {
 // ==== attention ===================================================================================================
 
 constexpr int ATT_THREADS = 256;
-constexpr int ATT_CHUNK = 64;   // positions per CTA
-constexpr int ATT_MAXG = 8;     // query heads per key/value head (static shared memory bound)
+constexpr int ATT_CHUNK = 128;  // positions per CTA
+constexpr int ATT_MAXG = 8;     // query heads per key/value head
 constexpr int ATT_HD = 128;     // head width the kernel is built for
+constexpr int ATT_QP = 33;      // padded 32-dim quarter of a query row in shared memory (no bank conflicts)
+constexpr int ATT_CLUSTER = 8;  // chunks per thread-block cluster
 
 struct AttnParams {
     const float* q;
@@ -89,54 +94,146 @@ struct AttnParams {
     float* out;
     int8_t* outq;
     float* outs;
-    float* part;   // [kv][nch_max][G][ATT_HD + 2]
-    int* cnt;      // [kv]
+    float* part;   // [kv][G][ncl_max][ATT_HD + 2]: each cluster's fold
+    int* cnt;      // [kv * G]
     int nch_max;
+    int ncl_max;
 };
 
-// grid (kv, chunk).  Scores: 4 lanes per position (32 dims each), 8 positions per warp per pass.  Values: each warp
-// takes positions t = warp (mod 8), lane l the dims 4l..4l+3; the 8 warps' sums meet in shared memory.
+// A chunk's partial: per query head its weighted values (ATT_HD), its max score and its sum of exponentials.
+__shared__ float att_partial[ATT_MAXG][ATT_HD + 2];
+
+// The cluster's 8 chunks are folded by rank: CTA rank r takes query head r of the group and reads that head's partial
+// from all 8 CTAs through distributed shared memory, in rank order.  The cluster's result goes to global scratch; the
+// last cluster of the key/value head to arrive (per query head) folds the clusters' results in cluster order, writes
+// the head's output and quantizes it.  Fold: M = max m_c, out = sum exp(m_c - M) acc_c / sum exp(m_c - M) l_c.
+__device__ void fold_cluster(const AttnParams& p, int g, int chunk, int G, int t) {
+    cg::cluster_group cluster = cg::this_cluster();
+    __shared__ int last;
+    __shared__ float fm[ATT_CLUSTER];
+    cluster.sync();  // every chunk's partial is in its CTA's shared memory
+    const int hh = (int)cluster.block_rank();
+    const int cl = chunk / ATT_CLUSTER;
+    const int ncl = p.ncl_max;
+    if (hh < G) {
+        float* out_part = p.part + (((int64_t)g * G + hh) * ncl + cl) * (ATT_HD + 2);
+        if (t < ATT_CLUSTER) fm[t] = cluster.map_shared_rank(&att_partial[0][0], t)[hh * (ATT_HD + 2) + ATT_HD];
+        __syncthreads();
+        float M = -FLT_MAX;
+#pragma unroll
+        for (int c = 0; c < ATT_CLUSTER; ++c) M = fmaxf(M, fm[c]);
+        if (t < ATT_HD + 2) {
+            const int col = (t == ATT_HD) ? ATT_HD + 1 : t;  // thread ATT_HD folds the sums; ATT_HD+1 writes M
+            float acc = 0.f;
+            if (t != ATT_HD + 1)
+                for (int c = 0; c < ATT_CLUSTER; ++c) {
+                    const float* src = cluster.map_shared_rank(&att_partial[0][0], c) + hh * (ATT_HD + 2);
+                    const float f = fm[c] == -FLT_MAX ? 0.f : expf(fm[c] - M);
+                    acc = fmaf(f, src[col], acc);
+                }
+            if (t < ATT_HD) out_part[t] = acc;
+            else if (t == ATT_HD) out_part[ATT_HD + 1] = acc;
+            else out_part[ATT_HD] = M;
+        }
+    }
+    cluster.sync();  // no CTA leaves while another reads its shared memory
+    if (hh >= G) return;
+    __threadfence();
+    __syncthreads();
+    const int ncl_used = (((*p.pos + 1) + ATT_CHUNK - 1) / ATT_CHUNK + ATT_CLUSTER - 1) / ATT_CLUSTER;
+    if (t == 0) last = (atomicAdd(p.cnt + g * G + hh, 1) == ncl_used - 1);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const float* base = p.part + ((int64_t)g * G + hh) * ncl * (ATT_HD + 2);
+    if (t < 32) {
+        float M = -FLT_MAX;
+        for (int c = t; c < ncl_used; c += 32) M = fmaxf(M, __ldcg(base + (int64_t)c * (ATT_HD + 2) + ATT_HD));
+        M = warp_max(M);
+        if (t == 0) fm[0] = M;
+    }
+    __syncthreads();
+    const float M = fm[0];
+    if (t < ATT_HD) {
+        float num = 0.f, den = 0.f;
+        for (int c = 0; c < ncl_used; ++c) {
+            const float* b = base + (int64_t)c * (ATT_HD + 2);
+            const float mc = __ldcg(b + ATT_HD);
+            const float f = mc == -FLT_MAX ? 0.f : expf(mc - M);
+            num = fmaf(f, __ldcg(b + t), num);
+            den = fmaf(f, __ldcg(b + ATT_HD + 1), den);
+        }
+        const float o = num / den;
+        const int64_t oi = ((int64_t)g * G + hh) * ATT_HD + t;
+        p.out[oi] = o;
+        if (p.outq) {  // warps 0..3 hold the head's four 32-value blocks
+            float d;
+            const int8_t qv = quantize_lane(o, d);
+            p.outq[oi] = qv;
+            if ((t & 31) == 0) p.outs[oi / 32] = d;
+        }
+    }
+    if (t == 0) p.cnt[g * G + hh] = 0;
+}
+
+// grid (kv, chunk) in clusters of 8 chunks, 8 warps.  Scores: 4 lanes per position (a 32-dim quarter each), each warp
+// 16 positions in two passes, all of a pass's key loads issued first.  Values: warp w takes positions w, w+8, ...
+// (16 rows, loaded before use), lane l the dims 4l..4l+3; the 8 warps' sums meet in shared memory.  A chunk's partial
+// is then folded with the rest of its cluster and across clusters (fold_cluster), always in chunk order.
 __global__ void __launch_bounds__(ATT_THREADS) attention_kernel(const AttnParams p) {
-    __shared__ float qs[ATT_MAXG][ATT_HD];
+    __shared__ float qs[ATT_MAXG][4 * ATT_QP];
     __shared__ float sc[ATT_MAXG][ATT_CHUNK];
     __shared__ float red[ATT_THREADS / 32][ATT_MAXG][ATT_HD];  // [warp][g][dim]
     __shared__ float stat[ATT_MAXG][2];
-    __shared__ int last;
     const int g = blockIdx.x, chunk = blockIdx.y;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int G = p.G;
     griddep_wait();
+    griddep_launch();
     const int len = *p.pos + 1;  // rows 0..pos
     const int nch = (len + ATT_CHUNK - 1) / ATT_CHUNK;
-    if (len < 1 || len > p.ctx || chunk >= nch) return;
+    // a whole cluster past the cache end (or a bad position) leaves together; a chunk past the end inside a working
+    // cluster contributes an empty partial
+    if (len < 1 || len > p.ctx || (chunk / ATT_CLUSTER) * ATT_CLUSTER >= nch) return;
     const int p0 = chunk * ATT_CHUNK;
-    const int np = min(ATT_CHUNK, len - p0);
-    for (int i = t; i < G * ATT_HD; i += ATT_THREADS) qs[i / ATT_HD][i % ATT_HD] = p.q[((int64_t)g * G) * ATT_HD + i];
+    const int np = max(0, min(ATT_CHUNK, len - p0));
+    for (int i = t; i < G * ATT_HD; i += ATT_THREADS) {
+        const int hh = i / ATT_HD, dd = i % ATT_HD;
+        qs[hh][(dd >> 5) * ATT_QP + (dd & 31)] = p.q[((int64_t)g * G) * ATT_HD + i];
+    }
     __syncthreads();
     const float* kb = p.k_cache + ((int64_t)g * p.ctx + p0) * ATT_HD;
     const float* vb = p.v_cache + ((int64_t)g * p.ctx + p0) * ATT_HD;
     // scores (every lane runs the same path; lanes past the chunk's end multiply zeros and store nothing)
     {
-        const int sub = lane & 3;         // 32-dim quarter of the row
-        const int pl = wid * 8 + (lane >> 2);
-        const bool valid = pl < np;
-        float kr[32];
-        const float4* kp = reinterpret_cast<const float4*>(kb + (int64_t)(valid ? pl : 0) * ATT_HD + sub * 32);
+        const int sub = lane & 3;
+        float kr[2][32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 v = valid ? __ldcs(kp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            kr[4 * i] = v.x;
-            kr[4 * i + 1] = v.y;
-            kr[4 * i + 2] = v.z;
-            kr[4 * i + 3] = v.w;
+        for (int pass = 0; pass < 2; ++pass) {
+            const int pl = pass * 64 + wid * 8 + (lane >> 2);
+            const bool valid = pl < np;
+            const float4* kp = reinterpret_cast<const float4*>(kb + (int64_t)(valid ? pl : 0) * ATT_HD + sub * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = valid ? __ldcs(kp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                kr[pass][4 * i] = v.x;
+                kr[pass][4 * i + 1] = v.y;
+                kr[pass][4 * i + 2] = v.z;
+                kr[pass][4 * i + 3] = v.w;
+            }
         }
-        for (int hh = 0; hh < G; ++hh) {
-            float acc = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc = fmaf(qs[hh][sub * 32 + i], kr[i], acc);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            if (sub == 0 && valid) sc[hh][pl] = acc * p.scale;
+        for (int pass = 0; pass < 2; ++pass) {
+            const int pl = pass * 64 + wid * 8 + (lane >> 2);
+            const bool valid = pl < np;
+            for (int hh = 0; hh < G; ++hh) {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc = fmaf(qs[hh][sub * ATT_QP + i], kr[pass][i], acc);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                if (sub == 0 && valid) sc[hh][pl] = acc * p.scale;
+            }
         }
     }
     __syncthreads();
@@ -153,78 +250,51 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_kernel(const AttnParams
         }
         l = group_sum<32>(l);
         if (lane == 0) {
-            stat[hh][0] = m;
+            stat[hh][0] = np > 0 ? m : -FLT_MAX;
             stat[hh][1] = l;
         }
     }
     __syncthreads();
-    // weighted values
+    // weighted values: 16 rows per warp, loaded before use
     {
-        float acc[ATT_MAXG][4];
+        float4 vr[ATT_CHUNK / 8];
 #pragma unroll
-        for (int hh = 0; hh < ATT_MAXG; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
-        for (int pl = wid; pl < np; pl += ATT_THREADS / 32) {
-            const float4 v = __ldcs(reinterpret_cast<const float4*>(vb + (int64_t)pl * ATT_HD) + lane);
-#pragma unroll
-            for (int hh = 0; hh < ATT_MAXG; ++hh) {
-                if (hh < G) {
-                    const float w = sc[hh][pl];
-                    acc[hh][0] = fmaf(w, v.x, acc[hh][0]);
-                    acc[hh][1] = fmaf(w, v.y, acc[hh][1]);
-                    acc[hh][2] = fmaf(w, v.z, acc[hh][2]);
-                    acc[hh][3] = fmaf(w, v.w, acc[hh][3]);
-                }
-            }
+        for (int u = 0; u < ATT_CHUNK / 8; ++u) {
+            const int pl = wid + 8 * u;
+            vr[u] = pl < np ? __ldcs(reinterpret_cast<const float4*>(vb + (int64_t)pl * ATT_HD) + lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int hh = 0; hh < ATT_MAXG; ++hh)
-            if (hh < G)
-                *reinterpret_cast<float4*>(&red[wid][hh][4 * lane]) =
-                    make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+        for (int hh = 0; hh < ATT_MAXG; ++hh) {
+            if (hh < G) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int u = 0; u < ATT_CHUNK / 8; ++u) {
+                    const int pl = wid + 8 * u;
+                    const float w = pl < np ? sc[hh][pl] : 0.f;
+                    acc.x = fmaf(w, vr[u].x, acc.x);
+                    acc.y = fmaf(w, vr[u].y, acc.y);
+                    acc.z = fmaf(w, vr[u].z, acc.z);
+                    acc.w = fmaf(w, vr[u].w, acc.w);
+                }
+                *reinterpret_cast<float4*>(&red[wid][hh][4 * lane]) = acc;
+            }
+        }
     }
     __syncthreads();
-    float* part = p.part + ((int64_t)g * p.nch_max + chunk) * G * (ATT_HD + 2);
+    // this chunk's partial stays in shared memory for the cluster's fold
     for (int i = t; i < G * ATT_HD; i += ATT_THREADS) {
         const int hh = i / ATT_HD, dd = i % ATT_HD;
         float s = 0.f;
+#pragma unroll
         for (int w = 0; w < ATT_THREADS / 32; ++w) s += red[w][hh][dd];
-        part[hh * (ATT_HD + 2) + dd] = s;
+        att_partial[hh][dd] = s;
     }
     if (t < G) {
-        part[t * (ATT_HD + 2) + ATT_HD] = stat[t][0];
-        part[t * (ATT_HD + 2) + ATT_HD + 1] = stat[t][1];
+        att_partial[t][ATT_HD] = stat[t][0];
+        att_partial[t][ATT_HD + 1] = stat[t][1];
     }
-    // the last chunk of this key/value head folds all chunks in chunk order
-    __threadfence();
-    __syncthreads();
-    if (t == 0) last = (atomicAdd(p.cnt + g, 1) == nch - 1);
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    for (int i = t; i < G * ATT_HD; i += ATT_THREADS) {
-        const int hh = i / ATT_HD, dd = i % ATT_HD;
-        const float* base = p.part + (int64_t)g * p.nch_max * G * (ATT_HD + 2) + hh * (ATT_HD + 2);
-        float M = -FLT_MAX;
-        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(base + (int64_t)cc * G * (ATT_HD + 2) + ATT_HD));
-        float num = 0.f, den = 0.f;
-        for (int cc = 0; cc < nch; ++cc) {
-            const float* b = base + (int64_t)cc * G * (ATT_HD + 2);
-            const float f = expf(__ldcg(b + ATT_HD) - M);
-            num = fmaf(f, __ldcg(b + dd), num);
-            den = fmaf(f, __ldcg(b + ATT_HD + 1), den);
-        }
-        const float o = num / den;
-        const int64_t oi = ((int64_t)g * G + hh) * ATT_HD + dd;
-        p.out[oi] = o;
-        if (p.outq) {  // i spans whole 32-value blocks per warp (ATT_HD and the stride are multiples of 32)
-            float d;
-            const int8_t qv = quantize_lane(o, d);
-            p.outq[oi] = qv;
-            if (lane == 0) p.outs[oi / 32] = d;
-        }
-    }
-    if (t == 0) p.cnt[g] = 0;
-    griddep_launch();
+    fold_cluster(p, g, chunk, G, t);
 }
 
 // ==== arg-max and advance ========================================================================================
@@ -317,7 +387,10 @@ __global__ void rope_table_kernel(float* cos_t, float* sin_t, int ctx, int half,
     }
 }
 
-int attn_chunks(int ctx) { return (ctx + ATT_CHUNK - 1) / ATT_CHUNK; }
+int attn_chunks(int ctx) {
+    const int n = (ctx + ATT_CHUNK - 1) / ATT_CHUNK;
+    return (n + ATT_CLUSTER - 1) / ATT_CLUSTER * ATT_CLUSTER;
+}
 
 int argmax_blocks(int64_t n) {
     int64_t b = (n + AM_THREADS * 4 - 1) / (AM_THREADS * 4);
@@ -335,8 +408,8 @@ cudaError_t launch_qk_rope_kv(const QkRopeCall& c, cudaStream_t st) {
 
 void attention_scratch(const AttnCall& c, size_t* bytes, size_t* counters) {
     const int G = c.heads / c.kv;
-    *bytes = (size_t)c.kv * attn_chunks(c.ctx) * G * (ATT_HD + 2) * sizeof(float);
-    *counters = (size_t)c.kv;
+    *bytes = (size_t)c.kv * G * (attn_chunks(c.ctx) / ATT_CLUSTER) * (ATT_HD + 2) * sizeof(float);
+    *counters = (size_t)c.kv * G;
 }
 
 cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
@@ -354,12 +427,30 @@ cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
     p.outq = c.outq;
     p.outs = c.outs;
     p.nch_max = attn_chunks(c.ctx);
+    p.ncl_max = p.nch_max / ATT_CLUSTER;
     size_t bytes = 0, cnt = 0;
     attention_scratch(c, &bytes, &cnt);
     p.part = ws.take<float>(bytes / sizeof(float));
     p.cnt = ws.take_counters(cnt);
     if (ws.overflow) return cudaErrorMemoryAllocation;
-    return launch(attention_kernel, dim3(c.kv, p.nch_max), dim3(ATT_THREADS), 0, st, c.pdl, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c.kv, p.nch_max);
+    cfg.blockDim = dim3(ATT_THREADS);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = ATT_CLUSTER;
+    attr[0].val.clusterDim.z = 1;
+    int na = 1;
+    if (c.pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        na = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, attention_kernel, p);
 }
 
 void argmax_scratch(const ArgmaxCall& c, size_t* bytes, size_t* counters) {

@@ -6,10 +6,11 @@
 //
 // How (GB300 design): the projection is bound by the weight bytes, so every byte is read once with a 256-bit load —
 // one whole Q8_0 block per lane per load — and its scale with a coalesced 32-bit load beside it.  A row is spread over
-// LPR lanes (LPR consecutive blocks per load, contiguous in memory); the activation blocks a lane multiplies stay in
-// its registers for every row it visits.  Rows are dealt to warps round-robin over a persistent grid sized to the SMs.
-// When a row is wider than LPR*BPL blocks it is cut into slices; each slice's partial goes to scratch and the last warp
-// to arrive on the row-set's counter adds the slices in slice order (deterministic) and resets the counter.
+// LPR lanes (LPR consecutive blocks per load, contiguous in memory); each lane group takes RT consecutive rows per item
+// and issues all RT*BPL block loads of the item before multiplying any of them; the activation blocks a lane
+// multiplies stay in its registers for every row it visits.  Items are dealt to warps round-robin over a persistent
+// grid sized to the SMs.  Only a matrix too short to fill the GPU is cut along k: each slice's partial goes to scratch
+// and the last warp to arrive on the item's counter adds the slices in slice order (deterministic) and resets it.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -23,7 +24,7 @@ struct GemvParams {
     float* y[3];
     const float* res[3];
     int n[3];
-    int rs0[4];      // first row-set of each segment (rs0[nseg] = total row-sets)
+    int it0[4];      // first item of each segment (it0[nseg] = total items)
     int row0[3];     // first row of each segment in the concatenated row space
     int nseg;
     int ntot;        // rows of all segments
@@ -34,31 +35,16 @@ struct GemvParams {
     int R;
     int S;           // slices along k
     void* partial;   // [R][S][ntot] (f64 in mode 0, f32 in mode 1)
-    int* counters;   // [R][row-sets]
+    int* counters;   // [R][items]
     int32_t* dots;
 };
 
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
-
-template <int MODE>
-struct Acc;
-template <>
-struct Acc<0> {
-    using T = double;
-};
-template <>
-struct Acc<1> {
-    using T = float;
-};
-
-// MODE: 0 = f32 activations / f64 sums, 1 = int8 activations.  LPR lanes per row, BPL blocks per lane per slice, U
-// row-sets in flight per warp.
-template <int MODE, int LPR, int BPL, int U, bool DOTS>
-__global__ void __launch_bounds__(Q8_THREADS) gemv_kernel(const GemvParams p) {
-    using T = typename Acc<MODE>::T;
+template <int MODE, int LPR, int BPL, int RT, bool DOTS>
+__global__ void __launch_bounds__(Q8_THREADS, 1) gemv_kernel(const GemvParams p) {
+    using T = typename AccType<MODE>::T;
     constexpr int RPW = 32 / LPR;
-    constexpr int SB = LPR * BPL;
+    constexpr int ROWS = RPW * RT;  // rows per item
+    constexpr int SB = LPR * BPL;   // blocks per slice
     const int lane = threadIdx.x & 31;
     const int lg = lane % LPR;
     const int grp = lane / LPR;
@@ -67,7 +53,7 @@ __global__ void __launch_bounds__(Q8_THREADS) gemv_kernel(const GemvParams p) {
     const int S = p.S;
     const int slice = warp % S;
     const int wstride = (W - slice + S - 1) / S;  // warps serving this slice
-    const int nrs = p.rs0[p.nseg];
+    const int nit = p.it0[p.nseg];
 
     int bidx[BPL];
     bool bval[BPL];
@@ -76,181 +62,144 @@ __global__ void __launch_bounds__(Q8_THREADS) gemv_kernel(const GemvParams p) {
         bidx[j] = slice * SB + lg + j * LPR;
         bval[j] = bidx[j] < p.nb;
     }
-
-    // The weights do not depend on earlier kernels: warm L2 with this warp's first rows before waiting.
-    {
-        const int rs = warp / S;
-        if (rs < nrs) {
-            int sg = 0;
-            while (sg + 1 < p.nseg && rs >= p.rs0[sg + 1]) ++sg;
-            const int row = (rs - p.rs0[sg]) * RPW + grp;
-            if (row < p.n[sg] && bval[0])
-                asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p.q[sg] + (int64_t)row * p.k + bidx[0] * 32));
-        }
-    }
     griddep_wait();
+    griddep_launch();
 
     for (int r = 0; r < p.R; ++r) {
-        // this lane's activation blocks
-        float xf[MODE == 0 ? BPL * 32 : 1];
-        uint32_t xw[MODE == 1 ? BPL : 1][8];
-        float xsc[BPL];
+        XTile<MODE, BPL> x;
+        load_x<MODE, BPL>(x, p.x + (int64_t)r * p.k, p.xq + (int64_t)r * p.k, p.xs + (int64_t)r * p.nb, bidx, bval);
+        for (int it = warp / S; it < nit; it += wstride) {
+            int sg = 0;
+            while (sg + 1 < p.nseg && it >= p.it0[sg + 1]) ++sg;
+            const int row0 = (it - p.it0[sg]) * ROWS + grp * RT;
+            const int nvalid = min(RT, p.n[sg] - row0);
+            WTile<BPL, RT> t;
+            load_tile<BPL, RT>(t, p.q[sg], p.s[sg], row0, nvalid, p.k, p.nb, bidx, bval);
+            T acc[RT];
 #pragma unroll
-        for (int j = 0; j < BPL; ++j) {
-            if (MODE == 0) {
-                const float4* xp = reinterpret_cast<const float4*>(p.x + (int64_t)r * p.k + bidx[j] * 32);
+            for (int i = 0; i < RT; ++i) {
+                if (DOTS) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float4 v = bval[j] ? __ldg(xp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    xf[j * 32 + 4 * i + 0] = v.x;
-                    xf[j * 32 + 4 * i + 1] = v.y;
-                    xf[j * 32 + 4 * i + 2] = v.z;
-                    xf[j * 32 + 4 * i + 3] = v.w;
+                    for (int j = 0; j < BPL; ++j)
+                        if (i < nvalid && bval[j])
+                            p.dots[((int64_t)r * p.ntot + row0 + i) * p.nb + bidx[j]] = block_dot_i8(t.w[i][j], x.w[j]);
                 }
-                xsc[j] = 0.f;
-            } else {
-                if (bval[j]) {
-                    ld_block_shared_use(p.xq + (int64_t)r * p.k + bidx[j] * 32, xw[j]);
-                    xsc[j] = __ldg(p.xs + (int64_t)r * p.nb + bidx[j]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) xw[j][i] = 0u;
-                    xsc[j] = 0.f;
-                }
+                acc[i] = group_sum<LPR>(tile_row_dot<MODE, BPL, RT>(t, i, x));
             }
-        }
-
-        for (int rs_base = warp / S; rs_base < nrs; rs_base += U * wstride) {
-            uint32_t w[U][BPL][8];
-            float sc[U][BPL];
-            int seg[U], row[U];
-            bool rv[U];
+            if (S == 1) {
+                if (lg == 0)
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int rs = rs_base + u * wstride;
-                int sg = 0;
-                while (sg + 1 < p.nseg && rs >= p.rs0[sg + 1]) ++sg;
-                seg[u] = sg;
-                row[u] = (rs - p.rs0[sg]) * RPW + grp;
-                rv[u] = rs < nrs && row[u] < p.n[sg];
-#pragma unroll
-                for (int j = 0; j < BPL; ++j) {
-                    if (rv[u] && bval[j]) {
-                        ld_block_stream(p.q[sg] + (int64_t)row[u] * p.k + bidx[j] * 32, w[u][j]);
-                        sc[u][j] = ld_scale_stream(p.s[sg] + (int64_t)row[u] * p.nb + bidx[j]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) w[u][j][i] = 0u;
-                        sc[u][j] = 0.f;
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int rs = rs_base + u * wstride;
-                if (rs >= nrs) break;  // warp-uniform
-                T acc = 0;
-#pragma unroll
-                for (int j = 0; j < BPL; ++j) {
-                    if (MODE == 0) {
-                        const float ps = block_dot_f32(w[u][j], &xf[j * 32]);
-                        acc = fma((double)sc[u][j], (double)ps, (double)acc);
-                    } else {
-                        const int D = block_dot_i8(w[u][j], xw[j]);
-                        if (DOTS && rv[u] && bval[j])
-                            p.dots[((int64_t)r * p.ntot + row[u]) * p.nb + bidx[j]] = D;
-                        acc = fmaf(sc[u][j] * xsc[j], (float)D, (float)acc);
-                    }
-                }
-                acc = group_sum<LPR>(acc);
-                const int sg = seg[u];
-                if (S == 1) {
-                    if (lg == 0 && rv[u]) {
-                        float v = (float)acc;
-                        if (p.res[sg]) v = p.res[sg][(int64_t)r * p.n[sg] + row[u]] + v;
-                        p.y[sg][(int64_t)r * p.n[sg] + row[u]] = v;
-                    }
-                } else {
-                    T* part = reinterpret_cast<T*>(p.partial);
-                    const int grow = p.row0[sg] + row[u];
-                    if (lg == 0 && rv[u]) part[((int64_t)r * S + slice) * p.ntot + grow] = acc;
-                    int* cnt = p.counters + (int64_t)r * nrs + rs;
-                    if (warp_arrive_last(cnt, S)) {
-                        if (lg == 0 && rv[u]) {
-                            T sum = 0;
-                            for (int sl = 0; sl < S; ++sl) sum += __ldcg(part + ((int64_t)r * S + sl) * p.ntot + grow);
-                            float v = (float)sum;
-                            if (p.res[sg]) v = p.res[sg][(int64_t)r * p.n[sg] + row[u]] + v;
-                            p.y[sg][(int64_t)r * p.n[sg] + row[u]] = v;
+                    for (int i = 0; i < RT; ++i)
+                        if (i < nvalid) {
+                            float v = (float)acc[i];
+                            if (p.res[sg]) v = p.res[sg][(int64_t)r * p.n[sg] + row0 + i] + v;
+                            p.y[sg][(int64_t)r * p.n[sg] + row0 + i] = v;
                         }
-                        if (lane == 0) *cnt = 0;
-                    }
+            } else {
+                T* part = reinterpret_cast<T*>(p.partial);
+                const int grow = p.row0[sg] + row0;
+                if (lg == 0)
+#pragma unroll
+                    for (int i = 0; i < RT; ++i)
+                        if (i < nvalid) part[((int64_t)r * S + slice) * p.ntot + grow + i] = acc[i];
+                int* cnt = p.counters + (int64_t)r * nit + it;
+                if (warp_arrive_last(cnt, S)) {
+                    if (lg == 0)
+                        for (int i = 0; i < nvalid; ++i) {
+                            T sum = 0;
+                            for (int sl = 0; sl < S; ++sl)
+                                sum += __ldcg(part + ((int64_t)r * S + sl) * p.ntot + grow + i);
+                            float v = (float)sum;
+                            if (p.res[sg]) v = p.res[sg][(int64_t)r * p.n[sg] + row0 + i] + v;
+                            p.y[sg][(int64_t)r * p.n[sg] + row0 + i] = v;
+                        }
+                    if (lane == 0) *cnt = 0;
                 }
             }
         }
     }
-    griddep_launch();
 }
 
 struct Plan {
-    int lpr, bpl, S, U, rpw;
+    int lpr, bpl, rt, S;
+    int rpw() const { return 32 / lpr; }
+    int rows() const { return rpw() * rt; }
 };
 
-Plan plan_for(int mode, int nb) {
-    // lanes per row and blocks per lane: use every lane (no idle block slots), then the fewest slices
-    const int bpl_max = (mode == 0) ? 1 : 2;
-    Plan best{32, 1, 1, 2, 1};
+int items_of(const GemvCall& c, const Plan& pl) {
+    int total = 0;
+    for (int i = 0; i < c.nseg; ++i) total += (int)((c.seg[i].n + pl.rows() - 1) / pl.rows());
+    return total;
+}
+
+Plan plan_for(const GemvCall& c) {
+    const int nb = (int)(c.k / 32);
+    const int bpl_max = (c.mode == 0) ? 3 : 4;
+    // lanes per row and blocks per lane: the fewest slices, then every lane busy
+    Plan best{32, 1, 1, 1 << 30};
     double best_util = -1.0;
     for (int lpr : {32, 16, 8}) {
         for (int bpl = 1; bpl <= bpl_max; ++bpl) {
             const int sb = lpr * bpl;
             const int S = (nb + sb - 1) / sb;
             const double util = (double)nb / (double)(S * sb);
-            if (util > best_util + 1e-9 || (util > best_util - 1e-9 && S < best.S)) {
+            if (S < best.S || (S == best.S && util > best_util + 1e-9)) {
                 best_util = util;
-                best = Plan{lpr, bpl, S, 2, 32 / lpr};
+                best = Plan{lpr, bpl, 1, S};
             }
         }
+    }
+    // rows per item: about eight (int8) or four (f32) 32-byte loads in flight per lane
+    const int target = (c.mode == 0) ? 4 : 8;
+    const int rt = target / best.bpl;
+    best.rt = rt >= 4 ? 4 : (rt >= 2 ? 2 : 1);
+    // a matrix too short to fill the GPU: fewer rows per item, then more slices
+    const int sms = device_info().sms;
+    while (best.rt > 1 && items_of(c, best) * best.S < 4 * sms) best.rt /= 2;
+    while (best.bpl > 1 && items_of(c, best) * best.S < 2 * sms) {
+        best.bpl = (best.bpl + 1) / 2;
+        best.S = (nb + best.lpr * best.bpl - 1) / (best.lpr * best.bpl);
     }
     return best;
 }
 
-template <int MODE, int LPR, int BPL, int U, bool DOTS>
-cudaError_t run(const GemvParams& p, int grid, cudaStream_t st, int pdl) {
-    return launch(gemv_kernel<MODE, LPR, BPL, U, DOTS>, dim3(grid), dim3(Q8_THREADS), 0, st, pdl, p);
+template <int MODE, int LPR, int BPL, int RT, bool DOTS>
+cudaError_t run(const GemvParams& p, int64_t warps, cudaStream_t st, int pdl) {
+    auto kern = gemv_kernel<MODE, LPR, BPL, RT, DOTS>;
+    return launch(kern, dim3(persistent_grid(kern, 0, warps)), dim3(Q8_THREADS), 0, st, pdl, p);
 }
 
-template <int MODE, bool DOTS>
-cudaError_t dispatch(const Plan& pl, const GemvParams& p, int grid, cudaStream_t st, int pdl) {
-#define Q8_CASE(L, B)                                                            \
-    if (pl.lpr == L && pl.bpl == B) return run<MODE, L, B, 2, DOTS>(p, grid, st, pdl);
-    Q8_CASE(32, 1)
-    Q8_CASE(16, 1)
-    Q8_CASE(8, 1)
-    if (MODE == 1) {
-        Q8_CASE(32, 2)
-        Q8_CASE(16, 2)
-        Q8_CASE(8, 2)
-    }
-#undef Q8_CASE
+template <int MODE, bool DOTS, int LPR>
+cudaError_t dispatch_lpr(const Plan& pl, const GemvParams& p, int64_t grid, cudaStream_t st, int pdl) {
+    if (pl.bpl == 1 && pl.rt == 1) return run<MODE, LPR, 1, 1, DOTS>(p, grid, st, pdl);
+    if (pl.bpl == 1 && pl.rt == 2) return run<MODE, LPR, 1, 2, DOTS>(p, grid, st, pdl);
+    if (pl.bpl == 1 && pl.rt == 4) return run<MODE, LPR, 1, 4, DOTS>(p, grid, st, pdl);
+    if (pl.bpl == 2 && pl.rt == 1) return run<MODE, LPR, 2, 1, DOTS>(p, grid, st, pdl);
+    if (pl.bpl == 2 && pl.rt == 2) return run<MODE, LPR, 2, 2, DOTS>(p, grid, st, pdl);
+    if (pl.bpl == 2 && pl.rt == 4) return run<MODE, LPR, 2, 4, DOTS>(p, grid, st, pdl);
+    if (pl.bpl == 3 && pl.rt == 1) return run<MODE, LPR, 3, 1, DOTS>(p, grid, st, pdl);
+    if (pl.bpl == 3 && pl.rt == 2) return run<MODE, LPR, 3, 2, DOTS>(p, grid, st, pdl);
+    if (MODE == 1 && pl.bpl == 4 && pl.rt == 1) return run<MODE, LPR, 4, 1, DOTS>(p, grid, st, pdl);
+    if (MODE == 1 && pl.bpl == 4 && pl.rt == 2) return run<MODE, LPR, 4, 2, DOTS>(p, grid, st, pdl);
     return cudaErrorInvalidConfiguration;
 }
 
-int rowsets(const GemvCall& c, const Plan& pl) {
-    int total = 0;
-    for (int i = 0; i < c.nseg; ++i) total += (int)((c.seg[i].n + pl.rpw - 1) / pl.rpw);
-    return total;
+template <int MODE, bool DOTS>
+cudaError_t dispatch(const Plan& pl, const GemvParams& p, int64_t grid, cudaStream_t st, int pdl) {
+    if (pl.lpr == 32) return dispatch_lpr<MODE, DOTS, 32>(pl, p, grid, st, pdl);
+    if (pl.lpr == 16) return dispatch_lpr<MODE, DOTS, 16>(pl, p, grid, st, pdl);
+    return dispatch_lpr<MODE, DOTS, 8>(pl, p, grid, st, pdl);
 }
 
 }  // namespace
 
 void gemv_scratch(const GemvCall& c, size_t* bytes, size_t* counters) {
-    const Plan pl = plan_for(c.mode, (int)(c.k / 32));
+    const Plan pl = plan_for(c);
     int64_t ntot = 0;
     for (int i = 0; i < c.nseg; ++i) ntot += c.seg[i].n;
     if (pl.S > 1) {
         *bytes = (size_t)c.R * pl.S * ntot * (c.mode == 0 ? 8 : 4);
-        *counters = (size_t)c.R * rowsets(c, pl);
+        *counters = (size_t)c.R * items_of(c, pl);
     } else {
         *bytes = 0;
         *counters = 0;
@@ -259,22 +208,22 @@ void gemv_scratch(const GemvCall& c, size_t* bytes, size_t* counters) {
 
 cudaError_t launch_gemv(const GemvCall& c, Carve& ws, cudaStream_t st) {
     const int nb = (int)(c.k / 32);
-    const Plan pl = plan_for(c.mode, nb);
+    const Plan pl = plan_for(c);
     GemvParams p = {};
     p.nseg = c.nseg;
-    int rs = 0, row = 0;
+    int it = 0, row = 0;
     for (int i = 0; i < c.nseg; ++i) {
         p.q[i] = c.seg[i].q;
         p.s[i] = c.seg[i].s;
         p.y[i] = c.seg[i].y;
         p.res[i] = c.seg[i].residual;
         p.n[i] = (int)c.seg[i].n;
-        p.rs0[i] = rs;
+        p.it0[i] = it;
         p.row0[i] = row;
-        rs += (int)((c.seg[i].n + pl.rpw - 1) / pl.rpw);
+        it += (int)((c.seg[i].n + pl.rows() - 1) / pl.rows());
         row += (int)c.seg[i].n;
     }
-    p.rs0[c.nseg] = rs;
+    p.it0[c.nseg] = it;
     p.ntot = row;
     p.k = (int)c.k;
     p.nb = nb;
@@ -291,12 +240,8 @@ cudaError_t launch_gemv(const GemvCall& c, Carve& ws, cudaStream_t st) {
         p.counters = ws.take_counters(cnt);
         if (ws.overflow) return cudaErrorMemoryAllocation;
     }
-    // persistent grid: enough warps for every (row-set, slice) item, at most 4 CTAs per SM
-    const int64_t items = (int64_t)rs * pl.S;
-    const int64_t max_warps = (int64_t)device_info().sms * 4 * Q8_WARPS;
-    int64_t warps = items < max_warps ? items : max_warps;
-    if (warps < 1) warps = 1;
-    const int grid = (int)((warps + Q8_WARPS - 1) / Q8_WARPS);
+    // persistent grid: one warp per (item, slice), at most the CTAs resident at once
+    const int64_t grid = (int64_t)it * pl.S;
     if (c.mode == 0) return dispatch<0, false>(pl, p, grid, st, c.pdl);
     if (c.dots) return dispatch<1, true>(pl, p, grid, st, c.pdl);
     return dispatch<1, false>(pl, p, grid, st, c.pdl);

@@ -122,12 +122,11 @@ struct ExpertCall {
     const int32_t* ids = nullptr;
     const float* gates = nullptr;
     PlanPtrs plan;                       // used when plan.active != nullptr, else choice j is group j (R == 1)
-    const float* x = nullptr;            // [R][k] (gate-up, mode 0) or h [R*K][k] (down, mode 0)
-    const int8_t* xq = nullptr;          // mode 1
+    const float* x = nullptr;            // gate-up: x [R][k]; down: h [R*K][k] (f32; for one row in mode 1 the kernel
+                                         // quantizes it as it stages it)
+    const int8_t* xq = nullptr;          // mode 1: gate-up xq [R][k]; down hq [R*K][k]
     const float* xs = nullptr;
     float* h = nullptr;                  // gate-up out [R*K][dff]
-    int8_t* hq = nullptr;                // gate-up out, mode 1
-    float* hs = nullptr;
     const float* residual = nullptr;     // down
     float* y = nullptr;                  // down out [R][d]
     float* expert_out = nullptr;         // down out [R][K][d]
@@ -135,6 +134,8 @@ struct ExpertCall {
 };
 void gate_up_scratch(const ExpertCall& c, size_t* bytes, size_t* counters);
 void down_scratch(const ExpertCall& c, size_t* bytes, size_t* counters);
+// The expert kernels read a whole row of k in one pass: k <= 4096 (int8 mode) or 3072 (f32 mode).
+bool experts_supported(int mode, int64_t k);
 cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st);
 cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st);
 
@@ -184,6 +185,19 @@ void argmax_scratch(const ArgmaxCall& c, size_t* bytes, size_t* counters);
 cudaError_t launch_argmax(const ArgmaxCall& c, Carve& ws, cudaStream_t st);
 
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int ctx, int half, double theta, cudaStream_t st);
+
+// A persistent grid for `kernel`: enough CTAs of Q8_THREADS threads for `warps` warps, at most the CTAs that fit on
+// the device at once (occupancy times SMs).
+template <typename Kern>
+int persistent_grid(Kern kernel, size_t smem, int64_t warps) {
+    int occ = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, 256, smem) != cudaSuccess || occ < 1) occ = 1;
+    int64_t ctas = (warps + 7) / 8;
+    const int64_t cap = (int64_t)device_info().sms * occ;
+    if (ctas > cap) ctas = cap;
+    if (ctas < 1) ctas = 1;
+    return (int)ctas;
+}
 
 // Launch helper: programmatic dependent launch when requested.
 template <typename Kern, typename... Args>

@@ -231,10 +231,6 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             c.xq = m->xq;
             c.xs = m->xs;
             c.h = m->hbuf;
-            if (mode == 1) {
-                c.hq = m->hq;
-                c.hs = m->hs;
-            }
             c.pdl = pdl;
             Q8_TRY(launch_gate_up(c, cv, st));
         }
@@ -251,9 +247,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             c.K = (int)d.k;
             c.ids = m->ids;
             c.gates = m->gates;
-            c.x = m->hbuf;
-            c.xq = m->hq;
-            c.xs = m->hs;
+            c.x = m->hbuf;  // f32 hidden rows; the int8 mode quantizes them as the kernel stages them
             c.residual = m->h;  // h = h + mixture
             c.y = m->h;
             c.pdl = pdl;

@@ -21,8 +21,6 @@
 namespace q8 {
 namespace {
 
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 // ==== top-k and grouping ==========================================================================================
 
@@ -89,6 +87,16 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
     griddep_wait();
     for (int r = wid; r < p.R; r += NW) {
         const float* l = p.logits + (int64_t)r * p.E;
+        // the row's logits in registers (up to 512 experts), else read from global memory each round
+        constexpr int EPL = 16;
+        float lr[EPL];
+        const bool in_regs = p.E <= 32 * EPL;
+        if (in_regs)
+#pragma unroll
+            for (int u = 0; u < EPL; ++u) {
+                const int e = lane + 32 * u;
+                lr[u] = e < p.E ? l[e] : -FLT_MAX;
+            }
         float pv = FLT_MAX;
         int pi = -1;
         float kept = 0.f;  // lane j holds the j-th kept logit
@@ -96,12 +104,25 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
         for (int j = 0; j < p.K; ++j) {
             float bv = -FLT_MAX;
             int bi = -1;
-            for (int e = lane; e < p.E; e += 32) {
-                const float v = l[e];
-                const bool eligible = pi < 0 || v < pv || (v == pv && e > pi);
-                if (eligible && better(v, e, bv, bi)) {
-                    bv = v;
-                    bi = e;
+            if (in_regs) {
+#pragma unroll
+                for (int u = 0; u < EPL; ++u) {
+                    const int e = lane + 32 * u;
+                    const float v = lr[u];
+                    const bool eligible = e < p.E && (pi < 0 || v < pv || (v == pv && e > pi));
+                    if (eligible && better(v, e, bv, bi)) {
+                        bv = v;
+                        bi = e;
+                    }
+                }
+            } else {
+                for (int e = lane; e < p.E; e += 32) {
+                    const float v = l[e];
+                    const bool eligible = pi < 0 || v < pv || (v == pv && e > pi);
+                    if (eligible && better(v, e, bv, bi)) {
+                        bv = v;
+                        bi = e;
+                    }
                 }
             }
 #pragma unroll
@@ -170,17 +191,6 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
 
 // ==== expert products =============================================================================================
 
-template <int MODE>
-struct AccT;
-template <>
-struct AccT<0> {
-    using T = double;
-};
-template <>
-struct AccT<1> {
-    using T = float;
-};
-
 struct ExpertParams {
     int mode;
     const int8_t* q0;
@@ -194,20 +204,15 @@ struct ExpertParams {
     const int32_t* offsets;
     const int32_t* lists;
     const int32_t* active;
-    const float* x;
-    const int8_t* xq;
+    const float* x;         // gate-up: [R][k]; down: h [R*K][k] f32
+    const int8_t* xq;       // gate-up: [R][k]; down: hq [R*K][k]
     const float* xs;
-    float* h;
-    int8_t* hq;
-    float* hs;
-    const float* residual;
-    float* y;
-    float* expert_out;
-    int S, nrs;
-    void* partial;
-    int* cnt_slice;   // gate-up: [R*K][nrs]
-    int* cnt_quant;   // gate-up: [R*K][out_rows/32]
-    int* cnt_row;     // down: [R][nrs]
+    float* h;               // gate-up out [R*K][out_rows]
+    const float* residual;  // down
+    float* y;               // down out [R][out_rows]
+    float* expert_out;      // down out [R*K][out_rows]
+    void* partial;          // down over a chunk: [R*K][out_rows] (f64 in mode 0, f32 in mode 1)
+    int nrs;                // items per group (row tiles of out_rows)
 };
 
 struct Group {
@@ -228,271 +233,237 @@ __device__ __forceinline__ int choice_of(const ExpertParams& p, const Group& g, 
     return p.active ? p.lists[g.c0 + i] : g.c0 + i;
 }
 
-// Loads one activation row's blocks for this lane.
-template <int MODE, int BPL>
-__device__ __forceinline__ void load_x(const float* x, const int8_t* xq, const float* xs, int64_t row, int k, int nb,
-                                       const int (&bidx)[BPL], const bool (&bval)[BPL], float* xf,
-                                       uint32_t (&xw)[MODE == 1 ? BPL : 1][8], float (&xsc)[BPL]) {
-#pragma unroll
-    for (int j = 0; j < BPL; ++j) {
-        if (MODE == 0) {
-            const float4* xp = reinterpret_cast<const float4*>(x + row * k + bidx[j] * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = bval[j] ? __ldcg(xp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-                xf[j * 32 + 4 * i + 0] = v.x;
-                xf[j * 32 + 4 * i + 1] = v.y;
-                xf[j * 32 + 4 * i + 2] = v.z;
-                xf[j * 32 + 4 * i + 3] = v.w;
-            }
-            xsc[j] = 0.f;
-        } else {
-            if (bval[j]) {
-                const uint4* xp = reinterpret_cast<const uint4*>(xq + row * k + bidx[j] * 32);
-                const uint4 a = __ldcg(xp), b = __ldcg(xp + 1);
-                xw[j][0] = a.x; xw[j][1] = a.y; xw[j][2] = a.z; xw[j][3] = a.w;
-                xw[j][4] = b.x; xw[j][5] = b.y; xw[j][6] = b.z; xw[j][7] = b.w;
-                xsc[j] = __ldcg(xs + row * nb + bidx[j]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) xw[j][i] = 0u;
-                xsc[j] = 0.f;
-            }
-        }
-    }
-}
-
-template <int MODE, int BPL>
-__device__ __forceinline__ void load_w(const int8_t* q, const float* s, int64_t row, bool rv, int k, int nb,
-                                       const int (&bidx)[BPL], const bool (&bval)[BPL], uint32_t (&w)[BPL][8],
-                                       float (&sc)[BPL]) {
-#pragma unroll
-    for (int j = 0; j < BPL; ++j) {
-        if (rv && bval[j]) {
-            ld_block_stream(q + row * k + bidx[j] * 32, w[j]);
-            sc[j] = ld_scale_stream(s + row * nb + bidx[j]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) w[j][i] = 0u;
-            sc[j] = 0.f;
-        }
-    }
-}
-
-template <int MODE, int BPL>
-__device__ __forceinline__ typename AccT<MODE>::T dot(const uint32_t (&w)[BPL][8], const float (&sc)[BPL],
-                                                      const float* xf, const uint32_t (&xw)[MODE == 1 ? BPL : 1][8],
-                                                      const float (&xsc)[BPL]) {
-    typename AccT<MODE>::T acc = 0;
-#pragma unroll
-    for (int j = 0; j < BPL; ++j) {
-        if (MODE == 0) {
-            const float ps = block_dot_f32(w[j], xf + j * 32);
-            acc = fma((double)sc[j], (double)ps, (double)acc);
-        } else {
-            const int D = block_dot_i8(w[j], xw[j]);
-            acc = fmaf(sc[j] * xsc[j], (float)D, (float)acc);
-        }
-    }
-    return acc;
-}
-
-// After h[c][i0 .. i0+rows) is stored: count those rows into their 32-row block; the warp completing a block
-// quantizes it (the int8 epilogue of the gate-up kernel).
-template <int RPW>
-__device__ __forceinline__ void quant_arrive(const ExpertParams& p, int c, int i0, int rows) {
-    const int lane = threadIdx.x & 31;
-    const int qb = i0 / 32;
-    int* cnt = p.cnt_quant + (int64_t)c * (p.out_rows / 32) + qb;
-    __threadfence();
-    __syncwarp();
-    int old = 0;
-    if (lane == 0) old = atomicAdd(cnt, rows);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old + rows == 32) {
-        __threadfence();
-        const int64_t base = (int64_t)c * p.out_rows + qb * 32;
-        const float v = __ldcg(p.h + base + lane);
-        float d;
-        const int8_t qv = quantize_lane(v, d);
-        p.hq[base + lane] = qv;
-        if (lane == 0) {
-            p.hs[base / 32] = d;
-            *cnt = 0;
-        }
-    }
-}
-
-// Gate-up: item (group a, row-set rs) on slice `slice`; rows i of expert e: h = silu(g . x) * (u . x).
-template <int MODE, int LPR, int BPL>
-__global__ void __launch_bounds__(Q8_THREADS, 2) gate_up_kernel(const ExpertParams p) {
-    using T = typename AccT<MODE>::T;
+// Gate-up: item (group a, row tile) — the tile's gate and up rows of expert e are loaded once into registers and
+// multiplied by every choice routed to e: h[c][i] = silu(g . x_r) * (u . x_r), r the choice's token row.
+template <int MODE, int LPR, int BPL, int RT>
+__global__ void __launch_bounds__(Q8_THREADS, 1) gate_up_kernel(const ExpertParams p) {
+    using T = typename AccType<MODE>::T;
     constexpr int RPW = 32 / LPR;
-    constexpr int SB = LPR * BPL;
+    constexpr int ROWS = RPW * RT;
     const int lane = threadIdx.x & 31, lg = lane % LPR, grp = lane / LPR;
     const int warp = blockIdx.x * Q8_WARPS + (threadIdx.x >> 5);
     const int W = gridDim.x * Q8_WARPS;
-    const int S = p.S;
-    const int slice = warp % S;
-    const int wstride = (W - slice + S - 1) / S;
     int bidx[BPL];
     bool bval[BPL];
 #pragma unroll
     for (int j = 0; j < BPL; ++j) {
-        bidx[j] = slice * SB + lg + j * LPR;
+        bidx[j] = lg + j * LPR;
         bval[j] = bidx[j] < p.nb;
     }
     griddep_wait();
-    const int ng = n_groups(p);
-    const int items = ng * p.nrs;
-    float xf[MODE == 0 ? BPL * 32 : 1];
-    uint32_t xw[MODE == 1 ? BPL : 1][8];
-    float xsc[BPL];
-    int64_t loaded = -1;
-    for (int it = warp / S; it < items; it += wstride) {
+    griddep_launch();
+    const int items = n_groups(p) * p.nrs;
+    XTile<MODE, BPL> x;
+    int loaded = -1;
+    for (int it = warp; it < items; it += W) {
         const int a = it / p.nrs, rs = it % p.nrs;
         const Group g = group_of(p, a);
         // an expert id outside [0, E) reads no weights and counts as an expert of zero weights
         const bool ev = g.expert >= 0 && g.expert < p.E;
-        const int i = rs * RPW + grp;
-        const bool rv = i < p.out_rows;
-        const int64_t wrow = (int64_t)(ev ? g.expert : 0) * p.out_rows + i;
-        uint32_t wg[BPL][8], wu[BPL][8];
-        float sg[BPL], su[BPL];
-        load_w<MODE, BPL>(p.q0, p.s0, wrow, rv && ev, p.k, p.nb, bidx, bval, wg, sg);
-        load_w<MODE, BPL>(p.q1, p.s1, wrow, rv && ev, p.k, p.nb, bidx, bval, wu, su);
+        const int i0 = rs * ROWS + grp * RT;
+        const int nvalid = min(RT, p.out_rows - i0);
+        const int64_t wrow = (int64_t)(ev ? g.expert : 0) * p.out_rows + i0;
+        WTile<BPL, RT> tg, tu;
+        load_tile<BPL, RT>(tg, p.q0, p.s0, wrow, ev ? nvalid : 0, p.k, p.nb, bidx, bval);
+        load_tile<BPL, RT>(tu, p.q1, p.s1, wrow, ev ? nvalid : 0, p.k, p.nb, bidx, bval);
         for (int ci = 0; ci < g.nc; ++ci) {
             const int c = choice_of(p, g, ci);
-            const int64_t xrow = c / p.K;  // the token row of choice c
+            const int xrow = c / p.K;
             if (xrow != loaded) {
-                load_x<MODE, BPL>(p.x, p.xq, p.xs, xrow, p.k, p.nb, bidx, bval, xf, xw, xsc);
+                load_x<MODE, BPL>(x, p.x + (int64_t)xrow * p.k, p.xq + (int64_t)xrow * p.k,
+                                  p.xs + (int64_t)xrow * p.nb, bidx, bval);
                 loaded = xrow;
             }
-            T gv = group_sum<LPR>(dot<MODE, BPL>(wg, sg, xf, xw, xsc));
-            T uv = group_sum<LPR>(dot<MODE, BPL>(wu, su, xf, xw, xsc));
-            bool done = true;
-            if (S > 1) {
-                T* part = reinterpret_cast<T*>(p.partial);  // [R*K][S][2][out_rows]
-                if (lg == 0 && rv) {
-                    part[(((int64_t)c * S + slice) * 2 + 0) * p.out_rows + i] = gv;
-                    part[(((int64_t)c * S + slice) * 2 + 1) * p.out_rows + i] = uv;
-                }
-                int* cnt = p.cnt_slice + (int64_t)c * p.nrs + rs;
-                done = warp_arrive_last(cnt, S);
-                if (done) {
-                    gv = 0;
-                    uv = 0;
-                    if (lg == 0 && rv)
-                        for (int sl = 0; sl < S; ++sl) {
-                            gv += __ldcg(part + (((int64_t)c * S + sl) * 2 + 0) * p.out_rows + i);
-                            uv += __ldcg(part + (((int64_t)c * S + sl) * 2 + 1) * p.out_rows + i);
-                        }
-                    if (lane == 0) *cnt = 0;
-                }
-            }
-            if (done) {
-                if (lg == 0 && rv) p.h[(int64_t)c * p.out_rows + i] = silu_f32((float)gv) * (float)uv;
-                if (p.hq) {
-                    const int i0 = rs * RPW;
-                    const int rows = min(RPW, p.out_rows - i0);
-                    quant_arrive<RPW>(p, c, i0, rows);
-                }
+#pragma unroll
+            for (int i = 0; i < RT; ++i) {
+                const T gv = group_sum<LPR>(tile_row_dot<MODE, BPL, RT>(tg, i, x));
+                const T uv = group_sum<LPR>(tile_row_dot<MODE, BPL, RT>(tu, i, x));
+                if (lg == 0 && i < nvalid) p.h[(int64_t)c * p.out_rows + i0 + i] = silu_f32((float)gv) * (float)uv;
             }
         }
     }
-    griddep_launch();
 }
 
-// Down-and-combine: item (group a, row-set rs over the d outputs) on slice `slice` of dff; the last of the K*S
-// arrivals for (token row r, rs) combines y[r] = residual + sum_j g_j * (sum over slices), j and slices in order.
-template <int MODE, int LPR, int BPL>
-__global__ void __launch_bounds__(Q8_THREADS, 2) down_kernel(const ExpertParams p) {
-    using T = typename AccT<MODE>::T;
+constexpr int DOWN_SMEM_MAX = 96 * 1024;
+
+// Down-and-combine for one token row: the CTA first stages the k hidden rows in shared memory (quantized there in the
+// int8 mode when given f32); item = a row tile of the d outputs, and the warp runs the kept experts in choice order,
+// EU experts' tiles loaded at a time, so y = residual + sum_j g_j * (Wd[e_j] . h_j) is formed in one place, in order.
+template <int MODE, int LPR, int BPL, int RT, int EU>
+__global__ void __launch_bounds__(Q8_THREADS, 1) down_one_kernel(const ExpertParams p) {
+    using T = typename AccType<MODE>::T;
+    extern __shared__ __align__(16) unsigned char dsm[];
     constexpr int RPW = 32 / LPR;
-    constexpr int SB = LPR * BPL;
-    const int lane = threadIdx.x & 31, lg = lane % LPR, grp = lane / LPR;
-    const int warp = blockIdx.x * Q8_WARPS + (threadIdx.x >> 5);
+    constexpr int ROWS = RPW * RT;
+    const int lane = threadIdx.x & 31, lg = lane % LPR, grp = lane / LPR, wid = threadIdx.x >> 5;
+    const int warp = blockIdx.x * Q8_WARPS + wid;
     const int W = gridDim.x * Q8_WARPS;
-    const int S = p.S;
-    const int slice = warp % S;
-    const int wstride = (W - slice + S - 1) / S;
+    const int K = p.K, kk = p.k;
     int bidx[BPL];
     bool bval[BPL];
 #pragma unroll
     for (int j = 0; j < BPL; ++j) {
-        bidx[j] = slice * SB + lg + j * LPR;
+        bidx[j] = lg + j * LPR;
         bval[j] = bidx[j] < p.nb;
     }
     griddep_wait();
-    const int ng = n_groups(p);
-    const int items = ng * p.nrs;
-    T* part = reinterpret_cast<T*>(p.partial);  // [R*K][S][out_rows]
-    float xf[MODE == 0 ? BPL * 32 : 1];
-    uint32_t xw[MODE == 1 ? BPL : 1][8];
-    float xsc[BPL];
-    for (int it = warp / S; it < items; it += wstride) {
+    griddep_launch();
+    float* hf = reinterpret_cast<float*>(dsm);
+    int8_t* hq = reinterpret_cast<int8_t*>(dsm);
+    float* hs = reinterpret_cast<float*>(dsm + ((size_t)K * kk + 15) / 16 * 16);
+    if (MODE == 0) {
+        for (int i = threadIdx.x; i < K * kk / 4; i += Q8_THREADS)
+            reinterpret_cast<float4*>(hf)[i] = __ldcg(reinterpret_cast<const float4*>(p.x) + i);
+    } else if (p.x) {
+        for (int b = wid; b < K * kk / 32; b += Q8_WARPS) {
+            float dsc;
+            const int8_t v = quantize_lane(__ldcg(p.x + (int64_t)b * 32 + lane), dsc);
+            hq[b * 32 + lane] = v;
+            if (lane == 0) hs[b] = dsc;
+        }
+    } else {
+        for (int i = threadIdx.x; i < K * kk / 16; i += Q8_THREADS)
+            reinterpret_cast<uint4*>(hq)[i] = __ldcg(reinterpret_cast<const uint4*>(p.xq) + i);
+        for (int i = threadIdx.x; i < K * kk / 32; i += Q8_THREADS) hs[i] = __ldcg(p.xs + i);
+    }
+    __syncthreads();
+    for (int it = warp; it < p.nrs; it += W) {
+        const int o0 = it * ROWS + grp * RT;
+        const int nvalid = min(RT, p.out_rows - o0);
+        T acc[RT];
+#pragma unroll
+        for (int i = 0; i < RT; ++i) acc[i] = 0;
+        for (int j0 = 0; j0 < K; j0 += EU) {
+            WTile<BPL, RT> t[EU];
+#pragma unroll
+            for (int u = 0; u < EU; ++u) {
+                const int j = j0 + u;
+                const int e = j < K ? __ldg(p.ids + j) : -1;
+                const bool ev = e >= 0 && e < p.E;
+                load_tile<BPL, RT>(t[u], p.q0, p.s0, (int64_t)(ev ? e : 0) * p.out_rows + o0, ev ? nvalid : 0, kk,
+                                   p.nb, bidx, bval);
+            }
+#pragma unroll
+            for (int u = 0; u < EU; ++u) {
+                const int j = j0 + u;
+                if (j >= K) break;
+                XTile<MODE, BPL> x;
+                load_x<MODE, BPL>(x, hf + (int64_t)j * kk, hq + (int64_t)j * kk, hs + (int64_t)j * p.nb, bidx, bval);
+                const float gj = __ldg(p.gates + j);
+#pragma unroll
+                for (int i = 0; i < RT; ++i) {
+                    const T e = group_sum<LPR>(tile_row_dot<MODE, BPL, RT>(t[u], i, x));
+                    if (p.expert_out && lg == 0 && i < nvalid) p.expert_out[(int64_t)j * p.out_rows + o0 + i] = (float)e;
+                    acc[i] = (MODE == 0) ? (T)fma((double)gj, (double)e, (double)acc[i])
+                                         : (T)fmaf(gj, (float)e, (float)acc[i]);
+                }
+            }
+        }
+        if (lg == 0)
+#pragma unroll
+            for (int i = 0; i < RT; ++i)
+                if (i < nvalid) {
+                    float v = (float)acc[i];
+                    if (p.residual) v = p.residual[o0 + i] + v;
+                    p.y[o0 + i] = v;
+                }
+    }
+}
+
+// Down over a chunk: item (group a, row tile) — expert e's tile is loaded once and multiplied by every choice routed
+// to it; each choice's unweighted output goes to scratch for the combine.
+template <int MODE, int LPR, int BPL, int RT>
+__global__ void __launch_bounds__(Q8_THREADS, 1) down_group_kernel(const ExpertParams p) {
+    using T = typename AccType<MODE>::T;
+    constexpr int RPW = 32 / LPR;
+    constexpr int ROWS = RPW * RT;
+    const int lane = threadIdx.x & 31, lg = lane % LPR, grp = lane / LPR;
+    const int warp = blockIdx.x * Q8_WARPS + (threadIdx.x >> 5);
+    const int W = gridDim.x * Q8_WARPS;
+    int bidx[BPL];
+    bool bval[BPL];
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+        bidx[j] = lg + j * LPR;
+        bval[j] = bidx[j] < p.nb;
+    }
+    griddep_wait();
+    griddep_launch();
+    const int items = n_groups(p) * p.nrs;
+    T* part = reinterpret_cast<T*>(p.partial);
+    for (int it = warp; it < items; it += W) {
         const int a = it / p.nrs, rs = it % p.nrs;
         const Group g = group_of(p, a);
-        const bool ev = g.expert >= 0 && g.expert < p.E;  // see gate_up_kernel
-        const int o = rs * RPW + grp;
-        const bool rv = o < p.out_rows;
-        uint32_t w[BPL][8];
-        float sc[BPL];
-        load_w<MODE, BPL>(p.q0, p.s0, (int64_t)(ev ? g.expert : 0) * p.out_rows + o, rv && ev, p.k, p.nb, bidx, bval,
-                          w, sc);
+        const bool ev = g.expert >= 0 && g.expert < p.E;
+        const int o0 = rs * ROWS + grp * RT;
+        const int nvalid = min(RT, p.out_rows - o0);
+        WTile<BPL, RT> t;
+        load_tile<BPL, RT>(t, p.q0, p.s0, (int64_t)(ev ? g.expert : 0) * p.out_rows + o0, ev ? nvalid : 0, p.k, p.nb,
+                           bidx, bval);
         for (int ci = 0; ci < g.nc; ++ci) {
             const int c = choice_of(p, g, ci);
-            load_x<MODE, BPL>(p.x, p.xq, p.xs, c, p.k, p.nb, bidx, bval, xf, xw, xsc);
-            const T acc = group_sum<LPR>(dot<MODE, BPL>(w, sc, xf, xw, xsc));
-            if (lg == 0 && rv) part[((int64_t)c * S + slice) * p.out_rows + o] = acc;
-            const int r = c / p.K;
-            int* cnt = p.cnt_row + (int64_t)r * p.nrs + rs;
-            if (warp_arrive_last(cnt, p.K * S)) {
-                if (lg == 0 && rv) {
-                    T comb = 0;
-                    for (int j = 0; j < p.K; ++j) {
-                        const int cj = r * p.K + j;
-                        T e = 0;
-                        for (int sl = 0; sl < S; ++sl) e += __ldcg(part + ((int64_t)cj * S + sl) * p.out_rows + o);
-                        if (p.expert_out) p.expert_out[(int64_t)cj * p.out_rows + o] = (float)e;
-                        comb += (T)__ldcg(p.gates + cj) * e;
-                    }
-                    float v = (float)comb;
-                    if (p.residual) v = p.residual[(int64_t)r * p.out_rows + o] + v;
-                    p.y[(int64_t)r * p.out_rows + o] = v;
-                }
-                if (lane == 0) *cnt = 0;
+            XTile<MODE, BPL> x;
+            load_x<MODE, BPL>(x, p.x + (int64_t)c * p.k, p.xq + (int64_t)c * p.k, p.xs + (int64_t)c * p.nb, bidx, bval);
+#pragma unroll
+            for (int i = 0; i < RT; ++i) {
+                const T e = group_sum<LPR>(tile_row_dot<MODE, BPL, RT>(t, i, x));
+                if (lg == 0 && i < nvalid) part[(int64_t)c * p.out_rows + o0 + i] = e;
             }
         }
     }
+}
+
+// y[r][o] = residual[r][o] + sum_j g[r][j] * part[r*K + j][o], the experts in choice order.
+template <int MODE>
+__global__ void __launch_bounds__(256) combine_kernel(const ExpertParams p) {
+    using T = typename AccType<MODE>::T;
+    griddep_wait();
     griddep_launch();
+    const T* part = reinterpret_cast<const T*>(p.partial);
+    const int64_t n = (int64_t)p.R * p.out_rows;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / p.out_rows, o = i % p.out_rows;
+        T acc = 0;
+        for (int j = 0; j < p.K; ++j) {
+            const int64_t c = r * p.K + j;
+            const T e = part[c * p.out_rows + o];
+            if (p.expert_out) p.expert_out[c * p.out_rows + o] = (float)e;
+            acc = (MODE == 0) ? (T)fma((double)p.gates[c], (double)e, (double)acc)
+                              : (T)fmaf(p.gates[c], (float)e, (float)acc);
+        }
+        float v = (float)acc;
+        if (p.residual) v = p.residual[i] + v;
+        p.y[i] = v;
+    }
 }
 
 struct EPlan {
-    int lpr, bpl, S;
+    int lpr, bpl, rt;
+    int rows() const { return 32 / lpr * rt; }
 };
 
-EPlan eplan(int mode, int nb) {
-    const int bpl_max = (mode == 0) ? 1 : 2;
+// One slice over k, every lane busy; about target_loads 32-byte loads in flight per lane.
+EPlan eplan(int mode, int nb, int target_loads) {
+    const int bpl_max = (mode == 0) ? 3 : 4;
     EPlan best{32, 1, 1};
+    int bestS = 1 << 30;
     double best_util = -1.0;
     for (int lpr : {32, 16, 8}) {
         for (int bpl = 1; bpl <= bpl_max; ++bpl) {
             const int sb = lpr * bpl;
             const int S = (nb + sb - 1) / sb;
             const double util = (double)nb / (double)(S * sb);
-            if (util > best_util + 1e-9 || (util > best_util - 1e-9 && S < best.S)) {
+            if (S < bestS || (S == bestS && util > best_util + 1e-9)) {
+                bestS = S;
                 best_util = util;
-                best = EPlan{lpr, bpl, S};
+                best = EPlan{lpr, bpl, 1};
             }
         }
     }
+    const int rt = target_loads / best.bpl;
+    best.rt = rt >= 4 ? 4 : (rt >= 2 ? 2 : 1);
+    if (best.bpl > 2 && best.rt > 2) best.rt = 2;
     return best;
-}
-
-int max_groups(const ExpertCall& c) {
-    const int64_t choices = c.R * c.K;
-    return (int)(choices < c.E ? choices : c.E);
 }
 
 ExpertParams make_params(const ExpertCall& c, const EPlan& pl) {
@@ -517,22 +488,77 @@ ExpertParams make_params(const ExpertCall& c, const EPlan& pl) {
     p.xq = c.xq;
     p.xs = c.xs;
     p.h = c.h;
-    p.hq = c.hq;
-    p.hs = c.hs;
     p.residual = c.residual;
     p.y = c.y;
     p.expert_out = c.expert_out;
-    p.S = pl.S;
-    p.nrs = (int)((c.out_rows + (32 / pl.lpr) - 1) / (32 / pl.lpr));
+    p.nrs = (int)((c.out_rows + pl.rows() - 1) / pl.rows());
     return p;
 }
 
-int grid_for(int64_t items, int S) {
-    const int64_t max_warps = (int64_t)device_info().sms * 2 * Q8_WARPS;
-    int64_t warps = items * S;
-    if (warps > max_warps) warps = max_warps;
-    if (warps < 1) warps = 1;
-    return (int)((warps + Q8_WARPS - 1) / Q8_WARPS);
+
+int max_groups(const ExpertCall& c) {
+    const int64_t choices = c.R * c.K;
+    return (int)(choices < c.E ? choices : c.E);
+}
+
+size_t down_one_smem(const ExpertCall& c) {
+    return c.mode == 0 ? (size_t)c.K * c.k * 4 : ((size_t)c.K * c.k + 15) / 16 * 16 + (size_t)c.K * c.k / 32 * 4;
+}
+
+#define Q8_EXPERT_ONE(KERNEL, MODE, L, B, R)                                                               \
+    if (pl.lpr == L && pl.bpl == B && pl.rt == R) {                                                        \
+        auto kern = KERNEL<MODE, L, B, R>;                                                                 \
+        return launch(kern, dim3(persistent_grid(kern, 0, warps)), dim3(Q8_THREADS), 0, st, c.pdl, p);     \
+    }
+#define Q8_EXPERT_LPR(KERNEL, MODE, L)                                                                     \
+    Q8_EXPERT_ONE(KERNEL, MODE, L, 1, 1) Q8_EXPERT_ONE(KERNEL, MODE, L, 1, 2) Q8_EXPERT_ONE(KERNEL, MODE, L, 1, 4) \
+    Q8_EXPERT_ONE(KERNEL, MODE, L, 2, 1) Q8_EXPERT_ONE(KERNEL, MODE, L, 2, 2) Q8_EXPERT_ONE(KERNEL, MODE, L, 3, 1) \
+    if (MODE == 1) {                                                                                       \
+        Q8_EXPERT_ONE(KERNEL, 1, L, 2, 4) Q8_EXPERT_ONE(KERNEL, 1, L, 3, 2) Q8_EXPERT_ONE(KERNEL, 1, L, 4, 1) \
+        Q8_EXPERT_ONE(KERNEL, 1, L, 4, 2)                                                                  \
+    }
+#define Q8_EXPERT_DISPATCH(KERNEL, MODE)                                                                   \
+    do {                                                                                                   \
+        Q8_EXPERT_LPR(KERNEL, MODE, 32) Q8_EXPERT_LPR(KERNEL, MODE, 16) Q8_EXPERT_LPR(KERNEL, MODE, 8)     \
+    } while (0)
+
+template <int MODE>
+cudaError_t run_gate_up(const ExpertCall& c, const EPlan& pl, const ExpertParams& p, int64_t warps, cudaStream_t st) {
+    Q8_EXPERT_DISPATCH(gate_up_kernel, MODE);
+    return cudaErrorInvalidConfiguration;
+}
+
+template <int MODE>
+cudaError_t run_down_group(const ExpertCall& c, const EPlan& pl, const ExpertParams& p, int64_t warps, cudaStream_t st) {
+    Q8_EXPERT_DISPATCH(down_group_kernel, MODE);
+    return cudaErrorInvalidConfiguration;
+}
+
+template <int MODE, int L, int B>
+cudaError_t run_down_one(const ExpertParams& p, int64_t warps, size_t smem, cudaStream_t st, int pdl) {
+    auto kern = down_one_kernel<MODE, L, B, 1, (MODE == 0 ? 2 : 4)>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DOWN_SMEM_MAX);
+    if (e != cudaSuccess) return e;
+    return launch(kern, dim3(persistent_grid(kern, smem, warps)), dim3(Q8_THREADS), smem, st, pdl, p);
+}
+
+template <int MODE>
+cudaError_t dispatch_down_one(const EPlan& pl, const ExpertParams& p, int64_t grid, size_t smem, cudaStream_t st, int pdl) {
+    if (pl.lpr == 32 && pl.bpl == 1) return run_down_one<MODE, 32, 1>(p, grid, smem, st, pdl);
+    if (pl.lpr == 32 && pl.bpl == 2) return run_down_one<MODE, 32, 2>(p, grid, smem, st, pdl);
+    if (pl.lpr == 32 && pl.bpl == 3) return run_down_one<MODE, 32, 3>(p, grid, smem, st, pdl);
+    if (pl.lpr == 16 && pl.bpl == 1) return run_down_one<MODE, 16, 1>(p, grid, smem, st, pdl);
+    if (pl.lpr == 16 && pl.bpl == 2) return run_down_one<MODE, 16, 2>(p, grid, smem, st, pdl);
+    if (pl.lpr == 16 && pl.bpl == 3) return run_down_one<MODE, 16, 3>(p, grid, smem, st, pdl);
+    if (pl.lpr == 8 && pl.bpl == 1) return run_down_one<MODE, 8, 1>(p, grid, smem, st, pdl);
+    if (pl.lpr == 8 && pl.bpl == 2) return run_down_one<MODE, 8, 2>(p, grid, smem, st, pdl);
+    if (pl.lpr == 8 && pl.bpl == 3) return run_down_one<MODE, 8, 3>(p, grid, smem, st, pdl);
+    if (MODE == 1) {
+        if (pl.lpr == 32 && pl.bpl == 4) return run_down_one<1, 32, 4>(p, grid, smem, st, pdl);
+        if (pl.lpr == 16 && pl.bpl == 4) return run_down_one<1, 16, 4>(p, grid, smem, st, pdl);
+        if (pl.lpr == 8 && pl.bpl == 4) return run_down_one<1, 8, 4>(p, grid, smem, st, pdl);
+    }
+    return cudaErrorInvalidConfiguration;
 }
 
 }  // namespace
@@ -548,63 +574,54 @@ cudaError_t launch_topk(const TopkCall& c, cudaStream_t st) {
     return launch(topk_kernel, dim3(1), dim3(TOPK_THREADS), smem, st, c.pdl, p);
 }
 
+bool experts_supported(int mode, int64_t k) { return k / 32 <= 32 * ((mode == 0) ? 3 : 4); }
+
 void gate_up_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
-    const EPlan pl = eplan(c.mode, (int)(c.k / 32));
-    const int64_t nrs = (c.out_rows + (32 / pl.lpr) - 1) / (32 / pl.lpr);
-    const int64_t choices = c.R * c.K;
-    *bytes = pl.S > 1 ? (size_t)choices * pl.S * 2 * c.out_rows * (c.mode == 0 ? 8 : 4) : 0;
-    *counters = (size_t)(pl.S > 1 ? choices * nrs : 0) + (size_t)(c.hq ? choices * (c.out_rows / 32) : 0);
+    (void)c;
+    *bytes = 0;
+    *counters = 0;
 }
 
 void down_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
-    const EPlan pl = eplan(c.mode, (int)(c.k / 32));
-    const int64_t nrs = (c.out_rows + (32 / pl.lpr) - 1) / (32 / pl.lpr);
-    *bytes = (size_t)c.R * c.K * pl.S * c.out_rows * (c.mode == 0 ? 8 : 4);
-    *counters = (size_t)(c.R * nrs);
+    const bool one = c.R == 1 && !c.plan.active && down_one_smem(c) <= (size_t)DOWN_SMEM_MAX;
+    *bytes = one ? 0 : (size_t)c.R * c.K * c.out_rows * (c.mode == 0 ? 8 : 4);
+    *counters = 0;
 }
 
-#define Q8_EXPERT_DISPATCH(KERNEL, MODE)                                                                   \
-    if (pl.lpr == 32 && pl.bpl == 1) return launch(KERNEL<MODE, 32, 1>, grid, blk, 0, st, c.pdl, p);     \
-    if (pl.lpr == 16 && pl.bpl == 1) return launch(KERNEL<MODE, 16, 1>, grid, blk, 0, st, c.pdl, p);     \
-    if (pl.lpr == 8 && pl.bpl == 1) return launch(KERNEL<MODE, 8, 1>, grid, blk, 0, st, c.pdl, p);       \
-    if (MODE == 1 && pl.lpr == 32 && pl.bpl == 2) return launch(KERNEL<1, 32, 2>, grid, blk, 0, st, c.pdl, p); \
-    if (MODE == 1 && pl.lpr == 16 && pl.bpl == 2) return launch(KERNEL<1, 16, 2>, grid, blk, 0, st, c.pdl, p); \
-    if (MODE == 1 && pl.lpr == 8 && pl.bpl == 2) return launch(KERNEL<1, 8, 2>, grid, blk, 0, st, c.pdl, p);
-
 cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
-    const EPlan pl = eplan(c.mode, (int)(c.k / 32));
+    (void)ws;
+    // gate and up tiles are both in flight: about four (f32) or eight (int8) 32-byte loads per lane in all
+    const EPlan pl = eplan(c.mode, (int)(c.k / 32), c.mode == 0 ? 2 : 4);
     ExpertParams p = make_params(c, pl);
-    const int64_t choices = c.R * c.K;
-    if (pl.S > 1) {
-        p.partial = ws.take<char>((size_t)choices * pl.S * 2 * c.out_rows * (c.mode == 0 ? 8 : 4));
-        p.cnt_slice = ws.take_counters((size_t)(choices * p.nrs));
-    }
-    if (c.hq) p.cnt_quant = ws.take_counters((size_t)(choices * (c.out_rows / 32)));
-    if (ws.overflow) return cudaErrorMemoryAllocation;
-    const int grid = grid_for((int64_t)max_groups(c) * p.nrs, pl.S);
-    const dim3 blk(Q8_THREADS);
-    if (c.mode == 0) {
-        Q8_EXPERT_DISPATCH(gate_up_kernel, 0)
-    } else {
-        Q8_EXPERT_DISPATCH(gate_up_kernel, 1)
-    }
-    return cudaErrorInvalidConfiguration;
+    const int64_t warps = (int64_t)max_groups(c) * p.nrs;
+    return c.mode == 0 ? run_gate_up<0>(c, pl, p, warps, st) : run_gate_up<1>(c, pl, p, warps, st);
 }
 
 cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st) {
-    const EPlan pl = eplan(c.mode, (int)(c.k / 32));
-    ExpertParams p = make_params(c, pl);
-    p.partial = ws.take<char>((size_t)c.R * c.K * pl.S * c.out_rows * (c.mode == 0 ? 8 : 4));
-    p.cnt_row = ws.take_counters((size_t)(c.R * p.nrs));
-    if (ws.overflow) return cudaErrorMemoryAllocation;
-    const int grid = grid_for((int64_t)max_groups(c) * p.nrs, pl.S);
-    const dim3 blk(Q8_THREADS);
-    if (c.mode == 0) {
-        Q8_EXPERT_DISPATCH(down_kernel, 0)
-    } else {
-        Q8_EXPERT_DISPATCH(down_kernel, 1)
+    const int nb = (int)(c.k / 32);
+    if (c.R == 1 && !c.plan.active && down_one_smem(c) <= (size_t)DOWN_SMEM_MAX) {
+        // one token: the experts combined in-warp; a row tile of 1 keeps several experts' loads in flight
+        EPlan pl = eplan(c.mode, nb, 4);
+        pl.rt = 1;
+        ExpertParams p = make_params(c, pl);
+        const int64_t grid = p.nrs;
+        const size_t smem = down_one_smem(c);
+        return c.mode == 0 ? dispatch_down_one<0>(pl, p, grid, smem, st, c.pdl)
+                           : dispatch_down_one<1>(pl, p, grid, smem, st, c.pdl);
     }
-    return cudaErrorInvalidConfiguration;
+    // a chunk (or one row through a plan): grouped product into scratch, then the ordered combine
+    const EPlan pl = eplan(c.mode, nb, c.mode == 0 ? 4 : 8);
+    ExpertParams p = make_params(c, pl);
+    p.partial = ws.take<char>((size_t)c.R * c.K * c.out_rows * (c.mode == 0 ? 8 : 4));
+    if (ws.overflow) return cudaErrorMemoryAllocation;
+    const int64_t warps = (int64_t)max_groups(c) * p.nrs;
+    cudaError_t e = c.mode == 0 ? run_down_group<0>(c, pl, p, warps, st) : run_down_group<1>(c, pl, p, warps, st);
+    if (e != cudaSuccess) return e;
+    const int64_t n = c.R * c.out_rows;
+    int cg = (int)((n + 255) / 256);
+    if (cg > device_info().sms * 4) cg = device_info().sms * 4;
+    return c.mode == 0 ? launch(combine_kernel<0>, dim3(cg), dim3(256), 0, st, c.pdl, p)
+                       : launch(combine_kernel<1>, dim3(cg), dim3(256), 0, st, c.pdl, p);
 }
 
 }  // namespace q8

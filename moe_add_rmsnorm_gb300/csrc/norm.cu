@@ -5,17 +5,20 @@
 // ForwardShim::supports (the residual summed in f32, uncompensated); lane_link.rs, Link::prim (Norm{x, add, w, rows,
 // cols, eps}; the standalone Quant launch).
 //
-// How: one CTA per row (rows are at most a few thousand values and the kernel is latency-bound).  A warp holds 32
-// consecutive values per step, so each 32-value quantisation block is one warp's registers and its maximum one warp
-// reduction.  The mean of squares is summed in f64 and the norm factor taken in f64, so y is rounded to f32 once.
+// How: one row per thread-block cluster of up to 8 CTAs (the kernel is latency-bound; its f64 work is spread over 8
+// SMs).  A warp holds 32 consecutive values per step, so each 32-value quantisation block is one warp's registers and
+// its maximum one warp reduction.  The mean of squares is summed in f64 and the norm factor taken in f64, so y is
+// rounded to f32 once.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace q8 {
 namespace {
 
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 constexpr int NORM_THREADS = 256;
 constexpr int NORM_MAX_D = 8192;
@@ -35,22 +38,31 @@ struct NormParams {
     int* err;
 };
 
-// PER values per thread (d <= PER * 256), kept in registers between the two passes.
-template <int PER>
+// One row per cluster of CL CTAs (distributed shared memory, sm_90+): CTA c of the cluster owns the contiguous slice
+// [c*d/CL, (c+1)*d/CL) of the row, PER values per thread.  Each CTA sums its squares in f64; the CL partial sums are read
+// through distributed shared memory after a cluster barrier and added in rank order by every CTA, so every CTA holds
+// the same f64 norm factor and the row's f64 arithmetic is spread over CL SMs.
+template <int PER, int CL>
 __global__ void __launch_bounds__(NORM_THREADS) add_rmsnorm_kernel(const NormParams p) {
     __shared__ double red[NORM_THREADS / 32];
-    const int r = blockIdx.x;
+    __shared__ double part;
+    __shared__ double inv_s;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int crank = (int)cluster.block_rank();
+    const int r = blockIdx.x / CL;
     const int t = threadIdx.x;
     const int lane = t & 31, wid = t >> 5;
+    const int dl = p.d / CL;  // this CTA's slice
+    const int base = crank * dl;
     griddep_wait();
+    griddep_launch();
     const float* a = p.a + (int64_t)r * p.d;
+    bool bad = false;
     if (p.a_row) {
         const int32_t idx = p.a_row[r];
-        if (idx < 0 || idx >= p.a_rows) {  // an out-of-range token: flag it and write nothing
-            if (t == 0 && p.err) atomicOr(p.err, 1);
-            return;
-        }
-        a = p.a + (int64_t)idx * p.d;
+        bad = idx < 0 || idx >= p.a_rows;  // an out-of-range token: flag it and write nothing
+        a = p.a + (int64_t)(bad ? 0 : idx) * p.d;
+        if (bad && t == 0 && crank == 0 && p.err) atomicOr(p.err, 1);
     }
     float s[PER];
     double ss = 0.0;
@@ -58,43 +70,49 @@ __global__ void __launch_bounds__(NORM_THREADS) add_rmsnorm_kernel(const NormPar
     for (int j = 0; j < PER; ++j) {
         const int i = j * NORM_THREADS + t;
         float v = 0.f;
-        if (i < p.d) {
-            v = a[i];
-            if (p.b) v = v + p.b[(int64_t)r * p.d + i];
+        if (i < dl) {
+            v = a[base + i];
+            if (p.b) v = v + p.b[(int64_t)r * p.d + base + i];
             ss = fma((double)v, (double)v, ss);
         }
         s[j] = v;
     }
-    // f64 sum of squares over the row
     ss = group_sum<32>(ss);
     if (lane == 0) red[wid] = ss;
     __syncthreads();
-    if (wid == 0) {
-        double v = lane < NORM_THREADS / 32 ? red[lane] : 0.0;
-        v = group_sum<32>(v);
-        if (lane == 0) red[0] = v;
+    if (t == 0) {
+        double v = 0.0;
+        for (int w = 0; w < NORM_THREADS / 32; ++w) v += red[w];
+        part = v;
     }
-    __syncthreads();
-    const double inv = 1.0 / sqrt(red[0] / (double)p.d + (double)p.eps);
+    cluster.sync();
+    if (t == 0) {
+        double tot = 0.0;
+        for (int c = 0; c < CL; ++c) tot += *cluster.map_shared_rank(&part, c);
+        inv_s = 1.0 / sqrt(tot / (double)p.d + (double)p.eps);
+    }
+    cluster.sync();  // every CTA has read the others' partial sums before any CTA moves on or exits
+    if (bad) return;
+    const double inv = inv_s;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
         const int i = j * NORM_THREADS + t;
-        const bool in = i < p.d;
+        const bool in = i < dl;
+        const int64_t gi = (int64_t)r * p.d + base + i;
         float y = 0.f;
         if (in) {
-            if (p.sum) p.sum[(int64_t)r * p.d + i] = s[j];
-            y = (float)((double)s[j] * inv * (double)p.w[i]);
-            if (p.y) p.y[(int64_t)r * p.d + i] = y;
+            if (p.sum) p.sum[gi] = s[j];
+            y = (float)((double)s[j] * inv * (double)p.w[base + i]);
+            if (p.y) p.y[gi] = y;
         }
-        // The block of 32 values i0..i0+31 lies in this warp's lanes (d % 32 == 0 when quantizing).
-        if (p.yq && (j * NORM_THREADS + wid * 32) < p.d) {
+        // The block of 32 values lies in this warp's lanes (the slice is whole 32-value blocks when quantizing).
+        if (p.yq && (j * NORM_THREADS + wid * 32) < dl) {
             float dsc;
             const int8_t qv = quantize_lane(y, dsc);
-            if (in) p.yq[(int64_t)r * p.d + i] = qv;
-            if (lane == 0) p.ys[((int64_t)r * p.d + i) / 32] = dsc;
+            if (in) p.yq[gi] = qv;
+            if (lane == 0) p.ys[gi / 32] = dsc;
         }
     }
-    griddep_launch();
 }
 
 __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ x, int64_t nblocks,
@@ -114,16 +132,49 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__
 
 }  // namespace
 
+template <int PER, int CL>
+cudaError_t launch_norm(const NormParams& p, int64_t rows, cudaStream_t st, int pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows * CL));
+    cfg.blockDim = dim3(NORM_THREADS);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int na = 1;
+    if (pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        na = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, add_rmsnorm_kernel<PER, CL>, p);
+}
+
 cudaError_t launch_add_rmsnorm(const NormCall& c, cudaStream_t st) {
     NormParams p = {c.a, c.a_row, c.a_rows, c.b, c.w, (int)c.d, c.eps, c.sum, c.y, c.yq, c.ys, c.err};
-    const dim3 grid((unsigned)c.rows), block(NORM_THREADS);
-    const int per = (int)((c.d + NORM_THREADS - 1) / NORM_THREADS);
-    if (per <= 1) return launch(add_rmsnorm_kernel<1>, grid, block, 0, st, c.pdl, p);
-    if (per <= 2) return launch(add_rmsnorm_kernel<2>, grid, block, 0, st, c.pdl, p);
-    if (per <= 4) return launch(add_rmsnorm_kernel<4>, grid, block, 0, st, c.pdl, p);
-    if (per <= 8) return launch(add_rmsnorm_kernel<8>, grid, block, 0, st, c.pdl, p);
-    if (per <= 16) return launch(add_rmsnorm_kernel<16>, grid, block, 0, st, c.pdl, p);
-    if (per <= NORM_MAX_D / NORM_THREADS) return launch(add_rmsnorm_kernel<32>, grid, block, 0, st, c.pdl, p);
+    // cluster size: up to 8 CTAs of at least 256 values each, each slice whole 32-value blocks
+    int cl = 1;
+    while (cl < 8 && c.d % (cl * 2 * 32) == 0 && c.d / (cl * 2) >= NORM_THREADS) cl *= 2;
+    const int dl = (int)(c.d / cl);
+    const int per = (dl + NORM_THREADS - 1) / NORM_THREADS;
+#define Q8_NORM(CL)                                                                            \
+    if (cl == CL) {                                                                            \
+        if (per <= 1) return launch_norm<1, CL>(p, c.rows, st, c.pdl);                         \
+        if (per <= 2) return launch_norm<2, CL>(p, c.rows, st, c.pdl);                         \
+        if (per <= 4) return launch_norm<4, CL>(p, c.rows, st, c.pdl);                         \
+        if (per <= 8) return launch_norm<8, CL>(p, c.rows, st, c.pdl);                         \
+        if (per <= 16) return launch_norm<16, CL>(p, c.rows, st, c.pdl);                       \
+        if (per <= NORM_MAX_D / NORM_THREADS) return launch_norm<32, CL>(p, c.rows, st, c.pdl); \
+    }
+    Q8_NORM(1)
+    Q8_NORM(2)
+    Q8_NORM(4)
+    Q8_NORM(8)
+#undef Q8_NORM
     return cudaErrorInvalidValue;
 }
 
