@@ -101,7 +101,7 @@ struct AttnParams {
 };
 
 // A chunk's partial: per query head its weighted values (ATT_HD), its max score and its sum of exponentials.
-__shared__ float att_partial[ATT_MAXG][ATT_HD + 2];
+__shared__ __align__(16) float att_partial[ATT_MAXG][ATT_HD + 2];
 
 // The cluster's 8 chunks are folded by rank: CTA rank r takes query head r of the group and reads that head's partial
 // from all 8 CTAs through distributed shared memory, in rank order.  The cluster's result goes to global scratch; the
@@ -181,9 +181,9 @@ __device__ void fold_cluster(const AttnParams& p, int g, int chunk, int G, int t
 // (16 rows, loaded before use), lane l the dims 4l..4l+3; the 8 warps' sums meet in shared memory.  A chunk's partial
 // is then folded with the rest of its cluster and across clusters (fold_cluster), always in chunk order.
 __global__ void __launch_bounds__(ATT_THREADS) attention_kernel(const AttnParams p) {
-    __shared__ float qs[ATT_MAXG][4 * ATT_QP];
-    __shared__ float sc[ATT_MAXG][ATT_CHUNK];
-    __shared__ float red[ATT_THREADS / 32][ATT_MAXG][ATT_HD];  // [warp][g][dim]
+    __shared__ __align__(16) float qs[ATT_MAXG][4 * ATT_QP];
+    __shared__ __align__(16) float sc[ATT_MAXG][ATT_CHUNK];
+    __shared__ __align__(16) float red[ATT_THREADS / 32][ATT_MAXG][ATT_HD];  // [warp][g][dim]; float4 stores
     __shared__ float stat[ATT_MAXG][2];
     const int g = blockIdx.x, chunk = blockIdx.y;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
