@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(256) qk_rope_kv_kernel(const QkRopeCall c) {
     const int i = threadIdx.x;
     const int half = c.hd / 2;
     griddep_wait();
+    griddep_launch();
     const int pos = *c.pos;
     if (pos < 0 || pos >= c.ctx) {
         if (i == 0 && h == 0 && c.err) atomicOr(c.err, 2);
@@ -72,7 +73,6 @@ __global__ void __launch_bounds__(256) qk_rope_kv_kernel(const QkRopeCall c) {
         vr[i] = c.v[(int64_t)g * c.hd + i];
         vr[i + half] = c.v[(int64_t)g * c.hd + i + half];
     }
-    griddep_launch();
 }
 
 // ==== attention ===================================================================================================
@@ -81,7 +81,7 @@ constexpr int ATT_THREADS = 256;
 constexpr int ATT_CHUNK = 128;  // positions per CTA
 constexpr int ATT_MAXG = 8;     // query heads per key/value head
 constexpr int ATT_HD = 128;     // head width the kernel is built for
-constexpr int ATT_QP = 33;      // padded 32-dim quarter of a query row in shared memory (no bank conflicts)
+constexpr int ATT_QP = 36;      // padded 32-dim quarter of a query row in shared memory: 16-byte reads, no conflicts
 constexpr int ATT_CLUSTER = 8;  // chunks per thread-block cluster
 
 struct AttnParams {
@@ -188,52 +188,91 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_kernel(const AttnParams
     const int g = blockIdx.x, chunk = blockIdx.y;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int G = p.G;
-    griddep_wait();
-    griddep_launch();
+    // The position is fixed for the whole step (the previous step's last kernel wrote it), and every cached row but
+    // the new one at `pos` was written by earlier steps: those rows are read before waiting for the kernels of this
+    // step; the new row and the queries after.
     const int len = *p.pos + 1;  // rows 0..pos
     const int nch = (len + ATT_CHUNK - 1) / ATT_CHUNK;
     // a whole cluster past the cache end (or a bad position) leaves together; a chunk past the end inside a working
     // cluster contributes an empty partial
-    if (len < 1 || len > p.ctx || (chunk / ATT_CLUSTER) * ATT_CLUSTER >= nch) return;
+    if (len < 1 || len > p.ctx || (chunk / ATT_CLUSTER) * ATT_CLUSTER >= nch) {
+        griddep_wait();
+        griddep_launch();
+        return;
+    }
     const int p0 = chunk * ATT_CHUNK;
     const int np = max(0, min(ATT_CHUNK, len - p0));
-    for (int i = t; i < G * ATT_HD; i += ATT_THREADS) {
-        const int hh = i / ATT_HD, dd = i % ATT_HD;
-        qs[hh][(dd >> 5) * ATT_QP + (dd & 31)] = p.q[((int64_t)g * G) * ATT_HD + i];
-    }
-    __syncthreads();
+    const int newrow = len - 1 - p0;  // the row this step writes, if it falls in this chunk
     const float* kb = p.k_cache + ((int64_t)g * p.ctx + p0) * ATT_HD;
     const float* vb = p.v_cache + ((int64_t)g * p.ctx + p0) * ATT_HD;
-    // scores (every lane runs the same path; lanes past the chunk's end multiply zeros and store nothing)
-    {
-        const int sub = lane & 3;
-        float kr[2][32];
+    const int sub = lane & 3;
+    float kr[2][32];
+    float4 vr[ATT_CHUNK / 8];
 #pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            const int pl = pass * 64 + wid * 8 + (lane >> 2);
-            const bool valid = pl < np;
-            const float4* kp = reinterpret_cast<const float4*>(kb + (int64_t)(valid ? pl : 0) * ATT_HD + sub * 32);
+    for (int pass = 0; pass < 2; ++pass) {
+        const int pl = pass * 64 + wid * 8 + (lane >> 2);
+        const bool pre = pl < np && pl != newrow;
+        const float4* kp = reinterpret_cast<const float4*>(kb + (int64_t)(pre ? pl : 0) * ATT_HD + sub * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 v = pre ? __ldcs(kp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            kr[pass][4 * i] = v.x;
+            kr[pass][4 * i + 1] = v.y;
+            kr[pass][4 * i + 2] = v.z;
+            kr[pass][4 * i + 3] = v.w;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < ATT_CHUNK / 8; ++u) {
+        const int pl = wid + 8 * u;
+        vr[u] = (pl < np && pl != newrow) ? __ldcs(reinterpret_cast<const float4*>(vb + (int64_t)pl * ATT_HD) + lane)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    griddep_wait();
+    griddep_launch();
+    // the new row and the queries, written by this step's earlier kernels
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int pl = pass * 64 + wid * 8 + (lane >> 2);
+        if (pl == newrow) {
+            const float4* kp = reinterpret_cast<const float4*>(kb + (int64_t)pl * ATT_HD + sub * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float4 v = valid ? __ldcs(kp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 v = __ldcg(kp + i);
                 kr[pass][4 * i] = v.x;
                 kr[pass][4 * i + 1] = v.y;
                 kr[pass][4 * i + 2] = v.z;
                 kr[pass][4 * i + 3] = v.w;
             }
         }
+    }
 #pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            const int pl = pass * 64 + wid * 8 + (lane >> 2);
-            const bool valid = pl < np;
-            for (int hh = 0; hh < G; ++hh) {
-                float acc = 0.f;
+    for (int u = 0; u < ATT_CHUNK / 8; ++u)
+        if (wid + 8 * u == newrow) vr[u] = __ldcg(reinterpret_cast<const float4*>(vb + (int64_t)newrow * ATT_HD) + lane);
+    for (int i = t; i < G * ATT_HD; i += ATT_THREADS) {
+        const int hh = i / ATT_HD, dd = i % ATT_HD;
+        qs[hh][(dd >> 5) * ATT_QP + (dd & 31)] = p.q[((int64_t)g * G) * ATT_HD + i];
+    }
+    __syncthreads();
+    // scores (every lane runs the same path; lanes past the chunk's end multiply zeros and store nothing)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc = fmaf(qs[hh][sub * ATT_QP + i], kr[pass][i], acc);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                if (sub == 0 && valid) sc[hh][pl] = acc * p.scale;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int pl = pass * 64 + wid * 8 + (lane >> 2);
+        const bool valid = pl < np;
+        for (int hh = 0; hh < G; ++hh) {
+            const float4* qv = reinterpret_cast<const float4*>(&qs[hh][sub * ATT_QP]);
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 q4 = qv[i];
+                acc = fmaf(q4.x, kr[pass][4 * i], acc);
+                acc = fmaf(q4.y, kr[pass][4 * i + 1], acc);
+                acc = fmaf(q4.z, kr[pass][4 * i + 2], acc);
+                acc = fmaf(q4.w, kr[pass][4 * i + 3], acc);
             }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (sub == 0 && valid) sc[hh][pl] = acc * p.scale;
         }
     }
     __syncthreads();
@@ -255,15 +294,8 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_kernel(const AttnParams
         }
     }
     __syncthreads();
-    // weighted values: 16 rows per warp, loaded before use
+    // weighted values: the warp's 16 rows, already in registers
     {
-        float4 vr[ATT_CHUNK / 8];
-#pragma unroll
-        for (int u = 0; u < ATT_CHUNK / 8; ++u) {
-            const int pl = wid + 8 * u;
-            vr[u] = pl < np ? __ldcs(reinterpret_cast<const float4*>(vb + (int64_t)pl * ATT_HD) + lane)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
 #pragma unroll
         for (int hh = 0; hh < ATT_MAXG; ++hh) {
             if (hh < G) {

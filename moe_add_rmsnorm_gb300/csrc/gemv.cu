@@ -62,19 +62,27 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gemv_kernel(const GemvParams p)
         bidx[j] = slice * SB + lg + j * LPR;
         bval[j] = bidx[j] < p.nb;
     }
+    // the weights do not depend on earlier kernels: the warp's first tile is read before waiting for them
+    const int first = warp / S;
+    WTile<BPL, RT> t;
+    if (first < nit) {
+        int sg = 0;
+        while (sg + 1 < p.nseg && first >= p.it0[sg + 1]) ++sg;
+        const int row0 = (first - p.it0[sg]) * ROWS + grp * RT;
+        load_tile<BPL, RT>(t, p.q[sg], p.s[sg], row0, min(RT, p.n[sg] - row0), p.k, p.nb, bidx, bval);
+    }
     griddep_wait();
     griddep_launch();
 
     for (int r = 0; r < p.R; ++r) {
         XTile<MODE, BPL> x;
         load_x<MODE, BPL>(x, p.x + (int64_t)r * p.k, p.xq + (int64_t)r * p.k, p.xs + (int64_t)r * p.nb, bidx, bval);
-        for (int it = warp / S; it < nit; it += wstride) {
+        for (int it = first; it < nit; it += wstride) {
             int sg = 0;
             while (sg + 1 < p.nseg && it >= p.it0[sg + 1]) ++sg;
             const int row0 = (it - p.it0[sg]) * ROWS + grp * RT;
             const int nvalid = min(RT, p.n[sg] - row0);
-            WTile<BPL, RT> t;
-            load_tile<BPL, RT>(t, p.q[sg], p.s[sg], row0, nvalid, p.k, p.nb, bidx, bval);
+            if (r > 0 || it != first) load_tile<BPL, RT>(t, p.q[sg], p.s[sg], row0, nvalid, p.k, p.nb, bidx, bval);
             T acc[RT];
 #pragma unroll
             for (int i = 0; i < RT; ++i) {

@@ -45,7 +45,7 @@ struct q8_model {
     size_t n_counters = 0;
     cudaStream_t cap = nullptr;
     cudaGraphExec_t exec = nullptr;
-    int pdl = 0;
+    int pdl = 1;  // programmatic dependent launch between the step's kernels
 };
 
 namespace {

@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     constexpr int NW = TOPK_THREADS / 32;
     griddep_wait();
+    griddep_launch();
     for (int r = wid; r < p.R; r += NW) {
         const float* l = p.logits + (int64_t)r * p.E;
         // the row's logits in registers (up to 512 experts), else read from global memory each round
@@ -186,7 +187,6 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
         for (int c2 = 0; c2 < c; ++c2) rank += (p.ids[c2] == e);
         p.lists[cnt[e] + rank] = c;
     }
-    griddep_launch();
 }
 
 // ==== expert products =============================================================================================
@@ -287,15 +287,15 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gate_up_kernel(const ExpertPara
 constexpr int DOWN_SMEM_MAX = 96 * 1024;
 
 // Down-and-combine for one token row: the CTA first stages the k hidden rows in shared memory (quantized there in the
-// int8 mode when given f32); item = a row tile of the d outputs, and the warp runs the kept experts in choice order,
-// EU experts' tiles loaded at a time, so y = residual + sum_j g_j * (Wd[e_j] . h_j) is formed in one place, in order.
-template <int MODE, int LPR, int BPL, int RT, int EU>
+// int8 mode when given f32).  A warp owns one output row o; its 32/LPR lane groups take the kept experts round-robin
+// (group gi: experts gi, gi + 32/LPR, ...), so every expert's row o is loaded at once across the warp, and lane 0
+// gathers the k dot products and forms y = residual + sum_j g_j * (Wd[e_j] . h_j) in choice order.
+template <int MODE, int LPR, int BPL>
 __global__ void __launch_bounds__(Q8_THREADS, 1) down_one_kernel(const ExpertParams p) {
     using T = typename AccType<MODE>::T;
     extern __shared__ __align__(16) unsigned char dsm[];
-    constexpr int RPW = 32 / LPR;
-    constexpr int ROWS = RPW * RT;
-    const int lane = threadIdx.x & 31, lg = lane % LPR, grp = lane / LPR, wid = threadIdx.x >> 5;
+    constexpr int NG = 32 / LPR;   // lane groups = experts in flight per pass
+    const int lane = threadIdx.x & 31, lg = lane % LPR, gi = lane / LPR, wid = threadIdx.x >> 5;
     const int warp = blockIdx.x * Q8_WARPS + wid;
     const int W = gridDim.x * Q8_WARPS;
     const int K = p.K, kk = p.k;
@@ -306,67 +306,70 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) down_one_kernel(const ExpertPar
         bidx[j] = lg + j * LPR;
         bval[j] = bidx[j] < p.nb;
     }
+    // the routing (ids, gates) was written two launches back, before the previous kernel passed its own wait
+    const int npass = (K + NG - 1) / NG;
     griddep_wait();
     griddep_launch();
-    float* hf = reinterpret_cast<float*>(dsm);
-    int8_t* hq = reinterpret_cast<int8_t*>(dsm);
-    float* hs = reinterpret_cast<float*>(dsm + ((size_t)K * kk + 15) / 16 * 16);
-    if (MODE == 0) {
+    float* hf = reinterpret_cast<float*>(dsm);                              // [K][kk] f32 staging
+    int8_t* hq = reinterpret_cast<int8_t*>(dsm + (size_t)K * kk * 4);       // [K][kk] words (int8 mode)
+    float* hs = reinterpret_cast<float*>(dsm + (size_t)K * kk * 5);         // [K][kk/32] scales
+    if (MODE == 0 || p.x) {
         for (int i = threadIdx.x; i < K * kk / 4; i += Q8_THREADS)
             reinterpret_cast<float4*>(hf)[i] = __ldcg(reinterpret_cast<const float4*>(p.x) + i);
-    } else if (p.x) {
-        for (int b = wid; b < K * kk / 32; b += Q8_WARPS) {
-            float dsc;
-            const int8_t v = quantize_lane(__ldcg(p.x + (int64_t)b * 32 + lane), dsc);
-            hq[b * 32 + lane] = v;
-            if (lane == 0) hs[b] = dsc;
-        }
+        __syncthreads();
+        if (MODE == 1)
+            for (int b = wid; b < K * kk / 32; b += Q8_WARPS) {
+                float dsc;
+                const int8_t v = quantize_lane(hf[b * 32 + lane], dsc);
+                hq[b * 32 + lane] = v;
+                if (lane == 0) hs[b] = dsc;
+            }
     } else {
         for (int i = threadIdx.x; i < K * kk / 16; i += Q8_THREADS)
             reinterpret_cast<uint4*>(hq)[i] = __ldcg(reinterpret_cast<const uint4*>(p.xq) + i);
         for (int i = threadIdx.x; i < K * kk / 32; i += Q8_THREADS) hs[i] = __ldcg(p.xs + i);
     }
     __syncthreads();
-    for (int it = warp; it < p.nrs; it += W) {
-        const int o0 = it * ROWS + grp * RT;
-        const int nvalid = min(RT, p.out_rows - o0);
-        T acc[RT];
+    for (int o = warp; o < p.out_rows; o += W) {
+        T acc = 0;
+        // passes of NG experts (expert j = m*NG + gi), two passes' loads in flight at a time
+        for (int m0 = 0; m0 < npass; m0 += 2) {
+            WTile<BPL, 1> t[2];
 #pragma unroll
-        for (int i = 0; i < RT; ++i) acc[i] = 0;
-        for (int j0 = 0; j0 < K; j0 += EU) {
-            WTile<BPL, RT> t[EU];
-#pragma unroll
-            for (int u = 0; u < EU; ++u) {
-                const int j = j0 + u;
+            for (int u = 0; u < 2; ++u) {
+                const int j = (m0 + u) * NG + gi;
                 const int e = j < K ? __ldg(p.ids + j) : -1;
                 const bool ev = e >= 0 && e < p.E;
-                load_tile<BPL, RT>(t[u], p.q0, p.s0, (int64_t)(ev ? e : 0) * p.out_rows + o0, ev ? nvalid : 0, kk,
-                                   p.nb, bidx, bval);
+                load_tile<BPL, 1>(t[u], p.q0, p.s0, (int64_t)(ev ? e : 0) * p.out_rows + o, ev ? 1 : 0, kk, p.nb,
+                                  bidx, bval);
             }
 #pragma unroll
-            for (int u = 0; u < EU; ++u) {
-                const int j = j0 + u;
-                if (j >= K) break;
+            for (int u = 0; u < 2; ++u) {
+                const int m = m0 + u;
+                if (m >= npass) break;
+                const int j = m * NG + gi;
+                const int jj = j < K ? j : 0;
                 XTile<MODE, BPL> x;
-                load_x<MODE, BPL>(x, hf + (int64_t)j * kk, hq + (int64_t)j * kk, hs + (int64_t)j * p.nb, bidx, bval);
-                const float gj = __ldg(p.gates + j);
-#pragma unroll
-                for (int i = 0; i < RT; ++i) {
-                    const T e = group_sum<LPR>(tile_row_dot<MODE, BPL, RT>(t[u], i, x));
-                    if (p.expert_out && lg == 0 && i < nvalid) p.expert_out[(int64_t)j * p.out_rows + o0 + i] = (float)e;
-                    acc[i] = (MODE == 0) ? (T)fma((double)gj, (double)e, (double)acc[i])
-                                         : (T)fmaf(gj, (float)e, (float)acc[i]);
+                load_x<MODE, BPL>(x, hf + (int64_t)jj * kk, hq + (int64_t)jj * kk, hs + (int64_t)jj * p.nb, bidx, bval);
+                const T mine = group_sum<LPR>(tile_row_dot<MODE, BPL, 1>(t[u], 0, x));
+                // lane 0 adds this pass's experts in choice order
+                for (int g = 0; g < NG; ++g) {
+                    const T ej = __shfl_sync(0xffffffffu, mine, g * LPR);
+                    const int jg = m * NG + g;
+                    if (lane == 0 && jg < K) {
+                        if (p.expert_out) p.expert_out[(int64_t)jg * p.out_rows + o] = (float)ej;
+                        const float gj = __ldg(p.gates + jg);
+                        acc = (MODE == 0) ? (T)fma((double)gj, (double)ej, (double)acc)
+                                          : (T)fmaf(gj, (float)ej, (float)acc);
+                    }
                 }
             }
         }
-        if (lg == 0)
-#pragma unroll
-            for (int i = 0; i < RT; ++i)
-                if (i < nvalid) {
-                    float v = (float)acc[i];
-                    if (p.residual) v = p.residual[o0 + i] + v;
-                    p.y[o0 + i] = v;
-                }
+        if (lane == 0) {
+            float v = (float)acc;
+            if (p.residual) v = p.residual[o] + v;
+            p.y[o] = v;
+        }
     }
 }
 
@@ -502,7 +505,7 @@ int max_groups(const ExpertCall& c) {
 }
 
 size_t down_one_smem(const ExpertCall& c) {
-    return c.mode == 0 ? (size_t)c.K * c.k * 4 : ((size_t)c.K * c.k + 15) / 16 * 16 + (size_t)c.K * c.k / 32 * 4;
+    return (size_t)c.K * c.k * 4 + (c.mode == 1 ? (size_t)c.K * c.k + (size_t)c.K * c.k / 32 * 4 : 0);
 }
 
 #define Q8_EXPERT_ONE(KERNEL, MODE, L, B, R)                                                               \
@@ -536,7 +539,7 @@ cudaError_t run_down_group(const ExpertCall& c, const EPlan& pl, const ExpertPar
 
 template <int MODE, int L, int B>
 cudaError_t run_down_one(const ExpertParams& p, int64_t warps, size_t smem, cudaStream_t st, int pdl) {
-    auto kern = down_one_kernel<MODE, L, B, 1, (MODE == 0 ? 2 : 4)>;
+    auto kern = down_one_kernel<MODE, L, B>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DOWN_SMEM_MAX);
     if (e != cudaSuccess) return e;
     return launch(kern, dim3(persistent_grid(kern, smem, warps)), dim3(Q8_THREADS), smem, st, pdl, p);
@@ -583,7 +586,7 @@ void gate_up_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
 }
 
 void down_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
-    const bool one = c.R == 1 && !c.plan.active && down_one_smem(c) <= (size_t)DOWN_SMEM_MAX;
+    const bool one = c.R == 1 && !c.plan.active && c.K <= 32 && down_one_smem(c) <= (size_t)DOWN_SMEM_MAX;
     *bytes = one ? 0 : (size_t)c.R * c.K * c.out_rows * (c.mode == 0 ? 8 : 4);
     *counters = 0;
 }
@@ -599,12 +602,12 @@ cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
 
 cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     const int nb = (int)(c.k / 32);
-    if (c.R == 1 && !c.plan.active && down_one_smem(c) <= (size_t)DOWN_SMEM_MAX) {
-        // one token: the experts combined in-warp; a row tile of 1 keeps several experts' loads in flight
+    if (c.R == 1 && !c.plan.active && c.K <= 32 && down_one_smem(c) <= (size_t)DOWN_SMEM_MAX) {
+        // one token: a warp per output row, its lane groups over the kept experts
         EPlan pl = eplan(c.mode, nb, 4);
         pl.rt = 1;
         ExpertParams p = make_params(c, pl);
-        const int64_t grid = p.nrs;
+        const int64_t grid = c.out_rows;
         const size_t smem = down_one_smem(c);
         return c.mode == 0 ? dispatch_down_one<0>(pl, p, grid, smem, st, c.pdl)
                            : dispatch_down_one<1>(pl, p, grid, smem, st, c.pdl);

@@ -54,6 +54,12 @@ __global__ void __launch_bounds__(NORM_THREADS) add_rmsnorm_kernel(const NormPar
     const int lane = t & 31, wid = t >> 5;
     const int dl = p.d / CL;  // this CTA's slice
     const int base = crank * dl;
+    float wv[PER];  // the norm weight does not depend on earlier kernels: read it before waiting for them
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int i = j * NORM_THREADS + t;
+        wv[j] = i < dl ? p.w[base + i] : 0.f;
+    }
     griddep_wait();
     griddep_launch();
     const float* a = p.a + (int64_t)r * p.d;
@@ -102,7 +108,7 @@ __global__ void __launch_bounds__(NORM_THREADS) add_rmsnorm_kernel(const NormPar
         float y = 0.f;
         if (in) {
             if (p.sum) p.sum[gi] = s[j];
-            y = (float)((double)s[j] * inv * (double)p.w[base + i]);
+            y = (float)((double)s[j] * inv * (double)wv[j]);
             if (p.y) p.y[gi] = y;
         }
         // The block of 32 values lies in this warp's lanes (the slice is whole 32-value blocks when quantizing).
