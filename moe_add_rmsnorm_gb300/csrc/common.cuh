@@ -4,6 +4,7 @@
 #include <stdint.h>
 
 #include "q8moe.h"
+#include "prefetch.h"
 
 #define Q8_QBLOCK 32
 #define Q8_WARPS 8          // warps per CTA in the streaming kernels
@@ -212,6 +213,39 @@ __device__ __forceinline__ bool warp_arrive_last(int* counter, int expected) {
     const bool last = (old == expected - 1);
     if (last) __threadfence();
     return last;
+}
+
+// ---- L2 prefetch of weights the step reads later ----------------------------------------------------------------
+// Bulk prefetch (TMA unit) of [p, p + n) into L2, in 64 KB pieces.  Only the 16-byte-aligned interior of a region is
+// prefetched, so no piece reaches outside it.
+constexpr unsigned long long kPrefetchPiece = 64ull << 10;
+
+__device__ __forceinline__ void l2_prefetch_piece(const char* p, unsigned n) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+}
+
+// Each (CTA, lane of warp 0) takes the pieces g = lane_index + m * (CTAs * 32) of the regions' concatenated pieces.
+__device__ __forceinline__ void issue_l2_prefetch(const L2Prefetch& pf) {
+    if (pf.n == 0 || threadIdx.x >= 32) return;
+    const unsigned long long cta = blockIdx.x + (unsigned long long)gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const unsigned long long step = (unsigned long long)gridDim.x * gridDim.y * gridDim.z * 32;
+    const unsigned long long mine = cta * 32 + threadIdx.x;
+    unsigned long long base = 0;  // global index of the region's first piece
+    for (int r = 0; r < pf.n && r < L2Prefetch::kMax; ++r) {
+        const uintptr_t a = ((uintptr_t)pf.ptr[r] + 15) & ~uintptr_t(15);
+        const uintptr_t e = ((uintptr_t)pf.ptr[r] + pf.bytes[r]) & ~uintptr_t(15);
+        if (e <= a) continue;
+        const unsigned long long len = e - a;
+        const unsigned long long np = (len + kPrefetchPiece - 1) / kPrefetchPiece;
+        unsigned long long g = mine;
+        if (g < base) g += (base - g + step - 1) / step * step;
+        for (; g < base + np; g += step) {
+            const unsigned long long off = (g - base) * kPrefetchPiece;
+            const unsigned long long n = len - off < kPrefetchPiece ? len - off : kPrefetchPiece;
+            l2_prefetch_piece((const char*)a + off, (unsigned)n);
+        }
+        base += np;
+    }
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

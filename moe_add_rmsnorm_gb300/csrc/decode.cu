@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(256) qk_rope_kv_kernel(const QkRopeCall c) {
     const int h = blockIdx.x;
     const int i = threadIdx.x;
     const int half = c.hd / 2;
+    issue_l2_prefetch(c.pf);
     griddep_wait();
     griddep_launch();
     const int pos = *c.pos;
@@ -98,6 +99,7 @@ struct AttnParams {
     int* cnt;      // [kv * G]
     int nch_max;
     int ncl_max;
+    L2Prefetch pf;
 };
 
 // A chunk's partial: per query head its weighted values (ATT_HD), its max score and its sum of exponentials.
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_kernel(const AttnParams
     const int g = blockIdx.x, chunk = blockIdx.y;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int G = p.G;
+    issue_l2_prefetch(p.pf);
     // The position is fixed for the whole step (the previous step's last kernel wrote it), and every cached row but
     // the new one at `pos` was written by earlier steps: those rows are read before waiting for the kernels of this
     // step; the new row and the queries after.
@@ -339,10 +342,11 @@ __device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
 
 __global__ void __launch_bounds__(AM_THREADS) argmax_kernel(const float* __restrict__ x, int64_t n, float* bv_out,
                                                             int* bi_out, int* cnt, int32_t* tok, int32_t* pos,
-                                                            const int* err, int ctx) {
+                                                            const int* err, int ctx, L2Prefetch pf) {
     __shared__ float sv[AM_THREADS / 32];
     __shared__ int si[AM_THREADS / 32];
     __shared__ int last;
+    issue_l2_prefetch(pf);
     griddep_wait();
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     float bv = -FLT_MAX;
@@ -460,6 +464,7 @@ cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
     p.outs = c.outs;
     p.nch_max = attn_chunks(c.ctx);
     p.ncl_max = p.nch_max / ATT_CLUSTER;
+    p.pf = c.pf;
     size_t bytes = 0, cnt = 0;
     attention_scratch(c, &bytes, &cnt);
     p.part = ws.take<float>(bytes / sizeof(float));
@@ -497,7 +502,7 @@ cudaError_t launch_argmax(const ArgmaxCall& c, Carve& ws, cudaStream_t st) {
     int* cnt = ws.take_counters(1);
     if (ws.overflow) return cudaErrorMemoryAllocation;
     return launch(argmax_kernel, dim3(blocks), dim3(AM_THREADS), 0, st, c.pdl, c.x, c.n, bv, bi, cnt, c.tok, c.pos,
-                  c.err, c.ctx);
+                  c.err, c.ctx, c.pf);
 }
 
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int ctx, int half, double theta, cudaStream_t st) {

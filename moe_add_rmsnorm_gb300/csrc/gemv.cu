@@ -37,6 +37,7 @@ struct GemvParams {
     void* partial;   // [R][S][ntot] (f64 in mode 0, f32 in mode 1)
     int* counters;   // [R][items]
     int32_t* dots;
+    L2Prefetch pf;
 };
 
 template <int MODE, int LPR, int BPL, int RT, bool DOTS>
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gemv_kernel(const GemvParams p)
         bidx[j] = slice * SB + lg + j * LPR;
         bval[j] = bidx[j] < p.nb;
     }
+    issue_l2_prefetch(p.pf);
     // the weights do not depend on earlier kernels: the warp's first tile is read before waiting for them
     const int first = warp / S;
     WTile<BPL, RT> t;
@@ -241,6 +243,7 @@ cudaError_t launch_gemv(const GemvCall& c, Carve& ws, cudaStream_t st) {
     p.R = (int)c.R;
     p.S = pl.S;
     p.dots = c.dots;
+    p.pf = c.pf;
     if (pl.S > 1) {
         size_t bytes = 0, cnt = 0;
         gemv_scratch(c, &bytes, &cnt);

@@ -4,6 +4,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "prefetch.h"
 #include "q8moe.h"
 
 namespace q8 {
@@ -64,6 +65,7 @@ struct GemvCall {
     const float* xs = nullptr;           // [R][k/32]
     int64_t R = 1;
     int32_t* dots = nullptr;             // mode 1 debug export [R][n][k/32] (single segment)
+    L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;                         // launch with programmatic dependent launch allowed
 };
 
@@ -85,6 +87,7 @@ struct NormCall {
     int8_t* yq = nullptr;
     float* ys = nullptr;
     int* err = nullptr;                  // device error word for a gathered row out of range
+    L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };
 cudaError_t launch_add_rmsnorm(const NormCall& c, cudaStream_t st);
@@ -98,13 +101,26 @@ struct PlanPtrs {
     int32_t* active = nullptr;    // [E+1]: count then the active experts ascending
 };
 
+// The stacked expert matrices whose chosen rows the top-k kernel prefetches into L2 once it has chosen (one row).
+struct ExpertPrefetch {
+    const int8_t* gq = nullptr;
+    const float* gs = nullptr;
+    const int8_t* uq = nullptr;
+    const float* us = nullptr;
+    const int8_t* dq = nullptr;
+    const float* ds = nullptr;
+    int64_t dff = 0, d = 0;
+};
+
 struct TopkCall {
+    ExpertPrefetch xp;
     const float* logits = nullptr;  // [R][E]
     int64_t R = 1, E = 0;
     int K = 0;
     int32_t* ids = nullptr;
     float* gates = nullptr;
     PlanPtrs plan;                  // filled when plan.counts != nullptr
+    L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };
 cudaError_t launch_topk(const TopkCall& c, cudaStream_t st);
@@ -130,6 +146,7 @@ struct ExpertCall {
     const float* residual = nullptr;     // down
     float* y = nullptr;                  // down out [R][d]
     float* expert_out = nullptr;         // down out [R][K][d]
+    L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };
 void gate_up_scratch(const ExpertCall& c, size_t* bytes, size_t* counters);
@@ -154,6 +171,7 @@ struct QkRopeCall {
     int heads = 0, kv = 0, hd = 0, ctx = 0;
     float eps = 0.f;
     int* err = nullptr;
+    L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };
 cudaError_t launch_qk_rope_kv(const QkRopeCall& c, cudaStream_t st);
@@ -167,6 +185,7 @@ struct AttnCall {
     float* out = nullptr;           // [heads][hd]
     int8_t* outq = nullptr;         // optional quantized output
     float* outs = nullptr;
+    L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };
 void attention_scratch(const AttnCall& c, size_t* bytes, size_t* counters);
@@ -179,6 +198,7 @@ struct ArgmaxCall {
     int32_t* pos = nullptr;     // incremented (when not null)
     const int* err = nullptr;   // when set and non-zero, tok and pos are left unchanged
     int ctx = 0;                // with pos: a position outside [0, ctx) leaves tok and pos unchanged
+    L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };
 void argmax_scratch(const ArgmaxCall& c, size_t* bytes, size_t* counters);

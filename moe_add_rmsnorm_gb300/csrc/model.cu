@@ -45,7 +45,8 @@ struct q8_model {
     size_t n_counters = 0;
     cudaStream_t cap = nullptr;
     cudaGraphExec_t exec = nullptr;
-    int pdl = 1;  // programmatic dependent launch between the step's kernels
+    int pdl = 1;       // programmatic dependent launch between the step's kernels
+    int prefetch = 1;  // weights fetched into L2 ahead of the launches that read them
 };
 
 namespace {
@@ -65,6 +66,11 @@ T* carve_arena(char*& at, size_t n) {
     uintptr_t p = ((uintptr_t)at + 255) & ~uintptr_t(255);
     at = (char*)(p + n * sizeof(T));
     return (T*)p;
+}
+
+void add_mat(L2Prefetch& pf, const q8_mat& w) {
+    pf.add(w.q, (size_t)(w.rows * w.cols));
+    pf.add(w.s, (size_t)(w.rows * (w.cols / 32)) * sizeof(float));
 }
 
 Carve fresh_carve(q8_model* m) {
@@ -109,6 +115,10 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
         }
         n.err = m->err;
         n.pdl = pdl;
+        if (m->prefetch) {  // this layer's O projection and router, read after the attention
+            add_mat(n.pf, m->wo[l]);
+            add_mat(n.pf, m->router[l]);
+        }
         Q8_TRY(launch_add_rmsnorm(n, st));
         // q, k and v in one projection launch
         {
@@ -211,6 +221,16 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             t.ids = m->ids;
             t.gates = m->gates;
             t.pdl = pdl;
+            if (m->prefetch) {  // the chosen experts' rows, as soon as they are chosen
+                t.xp.gq = m->gate[l].q;
+                t.xp.gs = m->gate[l].s;
+                t.xp.uq = m->up[l].q;
+                t.xp.us = m->up[l].s;
+                t.xp.dq = m->down[l].q;
+                t.xp.ds = m->down[l].s;
+                t.xp.dff = d.dff;
+                t.xp.d = D;
+            }
             Q8_TRY(launch_topk(t, st));
         }
         {
@@ -232,6 +252,11 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             c.xs = m->xs;
             c.h = m->hbuf;
             c.pdl = pdl;
+            if (m->prefetch && l + 1 < d.layers) {  // the next layer's q, k and v projections
+                add_mat(c.pf, m->wq[l + 1]);
+                add_mat(c.pf, m->wk[l + 1]);
+                add_mat(c.pf, m->wv[l + 1]);
+            }
             Q8_TRY(launch_gate_up(c, cv, st));
         }
         {
@@ -290,6 +315,11 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
         a.err = m->err;
         a.ctx = (int)d.ctx;
         a.pdl = pdl;
+        if (m->prefetch) {  // the first layer's q, k and v projections, for the next step
+            add_mat(a.pf, m->wq[0]);
+            add_mat(a.pf, m->wk[0]);
+            add_mat(a.pf, m->wv[0]);
+        }
         Q8_TRY(launch_argmax(a, cv, st));
     }
 #undef Q8_TRY

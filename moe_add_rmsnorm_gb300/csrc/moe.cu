@@ -27,6 +27,8 @@ namespace {
 constexpr int TOPK_THREADS = 512;
 
 struct TopkParams {
+    ExpertPrefetch xp;
+    L2Prefetch pf;
     const float* logits;
     int R, E, K;
     int32_t* ids;
@@ -36,6 +38,16 @@ struct TopkParams {
     int32_t* lists;
     int32_t* active;
 };
+
+// One thread's prefetch of [p, p + n) into L2 (16-byte-aligned interior, 64 KB pieces).
+__device__ __forceinline__ void prefetch_range(const void* p, size_t n) {
+    const uintptr_t a = ((uintptr_t)p + 15) & ~uintptr_t(15);
+    const uintptr_t e = ((uintptr_t)p + n) & ~uintptr_t(15);
+    for (uintptr_t o = a; o < e; o += kPrefetchPiece) {
+        const uintptr_t m = e - o < kPrefetchPiece ? e - o : kPrefetchPiece;
+        l2_prefetch_piece((const char*)o, (unsigned)m);
+    }
+}
 
 __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
     return be < 0 || v > bv || (v == bv && e < be);
@@ -84,6 +96,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
     extern __shared__ int sm[];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     constexpr int NW = TOPK_THREADS / 32;
+    issue_l2_prefetch(p.pf);
     griddep_wait();
     griddep_launch();
     for (int r = wid; r < p.R; r += NW) {
@@ -150,6 +163,16 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
             p.ids[(int64_t)r * p.K + lane] = kept_id;
             p.gates[(int64_t)r * p.K + lane] = __fdiv_rn(pe, z);
         }
+        // one row: the chosen experts' gate, up and down rows are fetched into L2 now, ahead of their kernels
+        if (p.xp.gq && p.R == 1 && lane < p.K && kept_id >= 0 && kept_id < p.E) {
+            const int64_t e = kept_id, dff = p.xp.dff, d = p.xp.d;
+            prefetch_range(p.xp.gq + e * dff * d, (size_t)(dff * d));
+            prefetch_range(p.xp.uq + e * dff * d, (size_t)(dff * d));
+            prefetch_range(p.xp.dq + e * d * dff, (size_t)(d * dff));
+            prefetch_range(p.xp.gs + e * dff * (d / 32), (size_t)(dff * (d / 32)) * 4);
+            prefetch_range(p.xp.us + e * dff * (d / 32), (size_t)(dff * (d / 32)) * 4);
+            prefetch_range(p.xp.ds + e * d * (dff / 32), (size_t)(d * (dff / 32)) * 4);
+        }
     }
     if (!p.counts) return;
     __syncthreads();
@@ -213,6 +236,7 @@ struct ExpertParams {
     float* expert_out;      // down out [R*K][out_rows]
     void* partial;          // down over a chunk: [R*K][out_rows] (f64 in mode 0, f32 in mode 1)
     int nrs;                // items per group (row tiles of out_rows)
+    L2Prefetch pf;
 };
 
 struct Group {
@@ -250,6 +274,7 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gate_up_kernel(const ExpertPara
         bidx[j] = lg + j * LPR;
         bval[j] = bidx[j] < p.nb;
     }
+    issue_l2_prefetch(p.pf);
     griddep_wait();
     griddep_launch();
     const int items = n_groups(p) * p.nrs;
@@ -308,6 +333,7 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) down_one_kernel(const ExpertPar
     }
     // the routing (ids, gates) was written two launches back, before the previous kernel passed its own wait
     const int npass = (K + NG - 1) / NG;
+    issue_l2_prefetch(p.pf);
     griddep_wait();
     griddep_launch();
     float* hf = reinterpret_cast<float*>(dsm);                              // [K][kk] f32 staging
@@ -495,6 +521,7 @@ ExpertParams make_params(const ExpertCall& c, const EPlan& pl) {
     p.y = c.y;
     p.expert_out = c.expert_out;
     p.nrs = (int)((c.out_rows + pl.rows() - 1) / pl.rows());
+    p.pf = c.pf;
     return p;
 }
 
@@ -567,7 +594,7 @@ cudaError_t dispatch_down_one(const EPlan& pl, const ExpertParams& p, int64_t gr
 }  // namespace
 
 cudaError_t launch_topk(const TopkCall& c, cudaStream_t st) {
-    TopkParams p = {c.logits, (int)c.R, (int)c.E, c.K, c.ids, c.gates,
+    TopkParams p = {c.xp, c.pf, c.logits, (int)c.R, (int)c.E, c.K, c.ids, c.gates,
                     c.plan.counts, c.plan.offsets, c.plan.lists, c.plan.active};
     const size_t smem = c.plan.counts ? (size_t)(2 * c.E + 32) * sizeof(int) : 0;
     if (smem > 48 * 1024) {

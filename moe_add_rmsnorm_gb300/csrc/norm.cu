@@ -36,6 +36,7 @@ struct NormParams {
     int8_t* yq;
     float* ys;
     int* err;
+    L2Prefetch pf;
 };
 
 // One row per cluster of CL CTAs (distributed shared memory, sm_90+): CTA c of the cluster owns the contiguous slice
@@ -54,6 +55,7 @@ __global__ void __launch_bounds__(NORM_THREADS) add_rmsnorm_kernel(const NormPar
     const int lane = t & 31, wid = t >> 5;
     const int dl = p.d / CL;  // this CTA's slice
     const int base = crank * dl;
+    issue_l2_prefetch(p.pf);
     float wv[PER];  // the norm weight does not depend on earlier kernels: read it before waiting for them
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
@@ -161,7 +163,7 @@ cudaError_t launch_norm(const NormParams& p, int64_t rows, cudaStream_t st, int 
 }
 
 cudaError_t launch_add_rmsnorm(const NormCall& c, cudaStream_t st) {
-    NormParams p = {c.a, c.a_row, c.a_rows, c.b, c.w, (int)c.d, c.eps, c.sum, c.y, c.yq, c.ys, c.err};
+    NormParams p = {c.a, c.a_row, c.a_rows, c.b, c.w, (int)c.d, c.eps, c.sum, c.y, c.yq, c.ys, c.err, c.pf};
     // cluster size: up to 8 CTAs of at least 256 values each, each slice whole 32-value blocks
     int cl = 1;
     while (cl < 8 && c.d % (cl * 2 * 32) == 0 && c.d / (cl * 2) >= NORM_THREADS) cl *= 2;
