@@ -79,11 +79,11 @@ __global__ void __launch_bounds__(256) qk_rope_kv_kernel(const QkRopeCall c) {
 // ==== attention ===================================================================================================
 
 constexpr int ATT_THREADS = 256;
-constexpr int ATT_CHUNK = 128;  // positions per CTA
+constexpr int ATT_CHUNK = 64;   // positions per CTA (8 per warp)
 constexpr int ATT_MAXG = 8;     // query heads per key/value head
 constexpr int ATT_HD = 128;     // head width the kernel is built for
 constexpr int ATT_QP = 36;      // padded 32-dim quarter of a query row in shared memory: 16-byte reads, no conflicts
-constexpr int ATT_CLUSTER = 8;  // chunks per thread-block cluster
+constexpr int ATT_CLUSTER = 4;  // chunks per thread-block cluster
 
 struct AttnParams {
     const float* q;
@@ -105,32 +105,36 @@ struct AttnParams {
 // A chunk's partial: per query head its weighted values (ATT_HD), its max score and its sum of exponentials.
 __shared__ __align__(16) float att_partial[ATT_MAXG][ATT_HD + 2];
 
-// The cluster's 8 chunks are folded by rank: CTA rank r takes query head r of the group and reads that head's partial
-// from all 8 CTAs through distributed shared memory, in rank order.  The cluster's result goes to global scratch; the
+// The cluster's chunks are folded by rank: CTA rank r takes query heads r, r + 4, ... of the group and reads each
+// head's partial from every CTA of the cluster through distributed shared memory, in rank order.  The cluster's result goes to global scratch; the
 // last cluster of the key/value head to arrive (per query head) folds the clusters' results in cluster order, writes
 // the head's output and quantizes it.  Fold: M = max m_c, out = sum exp(m_c - M) acc_c / sum exp(m_c - M) l_c.
 __device__ void fold_cluster(const AttnParams& p, int g, int chunk, int G, int t) {
     cg::cluster_group cluster = cg::this_cluster();
-    __shared__ int last;
-    __shared__ float fm[ATT_CLUSTER];
+    __shared__ int last[ATT_MAXG];
+    __shared__ float fm[ATT_MAXG][ATT_CLUSTER];
+    __shared__ float fM[ATT_MAXG];
     cluster.sync();  // every chunk's partial is in its CTA's shared memory
-    const int hh = (int)cluster.block_rank();
+    const int rank = (int)cluster.block_rank();
     const int cl = chunk / ATT_CLUSTER;
     const int ncl = p.ncl_max;
-    if (hh < G) {
+    // this rank's query heads: rank, rank + ATT_CLUSTER, ...
+    for (int hh = rank; hh < G; hh += ATT_CLUSTER)
+        if (t < ATT_CLUSTER) fm[hh][t] = cluster.map_shared_rank(&att_partial[0][0], t)[hh * (ATT_HD + 2) + ATT_HD];
+    __syncthreads();
+    for (int hh = rank; hh < G; hh += ATT_CLUSTER) {
         float* out_part = p.part + (((int64_t)g * G + hh) * ncl + cl) * (ATT_HD + 2);
-        if (t < ATT_CLUSTER) fm[t] = cluster.map_shared_rank(&att_partial[0][0], t)[hh * (ATT_HD + 2) + ATT_HD];
-        __syncthreads();
         float M = -FLT_MAX;
 #pragma unroll
-        for (int c = 0; c < ATT_CLUSTER; ++c) M = fmaxf(M, fm[c]);
+        for (int c = 0; c < ATT_CLUSTER; ++c) M = fmaxf(M, fm[hh][c]);
         if (t < ATT_HD + 2) {
             const int col = (t == ATT_HD) ? ATT_HD + 1 : t;  // thread ATT_HD folds the sums; ATT_HD+1 writes M
             float acc = 0.f;
             if (t != ATT_HD + 1)
+#pragma unroll
                 for (int c = 0; c < ATT_CLUSTER; ++c) {
                     const float* src = cluster.map_shared_rank(&att_partial[0][0], c) + hh * (ATT_HD + 2);
-                    const float f = fm[c] == -FLT_MAX ? 0.f : expf(fm[c] - M);
+                    const float f = fm[hh][c] == -FLT_MAX ? 0.f : expf(fm[hh][c] - M);
                     acc = fmaf(f, src[col], acc);
                 }
             if (t < ATT_HD) out_part[t] = acc;
@@ -139,50 +143,55 @@ __device__ void fold_cluster(const AttnParams& p, int g, int chunk, int G, int t
         }
     }
     cluster.sync();  // no CTA leaves while another reads its shared memory
-    if (hh >= G) return;
+    if (rank >= G) return;
     __threadfence();
     __syncthreads();
     const int ncl_used = (((*p.pos + 1) + ATT_CHUNK - 1) / ATT_CHUNK + ATT_CLUSTER - 1) / ATT_CLUSTER;
-    if (t == 0) last = (atomicAdd(p.cnt + g * G + hh, 1) == ncl_used - 1);
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    const float* base = p.part + ((int64_t)g * G + hh) * ncl * (ATT_HD + 2);
-    if (t < 32) {
-        float M = -FLT_MAX;
-        for (int c = t; c < ncl_used; c += 32) M = fmaxf(M, __ldcg(base + (int64_t)c * (ATT_HD + 2) + ATT_HD));
-        M = warp_max(M);
-        if (t == 0) fm[0] = M;
+    if (t < ATT_MAXG) {
+        const int hh = rank + t * ATT_CLUSTER;
+        last[t] = hh < G ? (atomicAdd(p.cnt + g * G + hh, 1) == ncl_used - 1) : 0;
     }
     __syncthreads();
-    const float M = fm[0];
-    if (t < ATT_HD) {
-        float num = 0.f, den = 0.f;
-        for (int c = 0; c < ncl_used; ++c) {
-            const float* b = base + (int64_t)c * (ATT_HD + 2);
-            const float mc = __ldcg(b + ATT_HD);
-            const float f = mc == -FLT_MAX ? 0.f : expf(mc - M);
-            num = fmaf(f, __ldcg(b + t), num);
-            den = fmaf(f, __ldcg(b + ATT_HD + 1), den);
+    for (int u = 0, hh = rank; hh < G; ++u, hh += ATT_CLUSTER) {
+        if (!last[u]) continue;  // CTA-uniform
+        __threadfence();
+        const float* base = p.part + ((int64_t)g * G + hh) * ncl * (ATT_HD + 2);
+        if (t < 32) {
+            float M = -FLT_MAX;
+            for (int c = t; c < ncl_used; c += 32) M = fmaxf(M, __ldcg(base + (int64_t)c * (ATT_HD + 2) + ATT_HD));
+            M = warp_max(M);
+            if (t == 0) fM[u] = M;
         }
-        const float o = num / den;
-        const int64_t oi = ((int64_t)g * G + hh) * ATT_HD + t;
-        p.out[oi] = o;
-        if (p.outq) {  // warps 0..3 hold the head's four 32-value blocks
-            float d;
-            const int8_t qv = quantize_lane(o, d);
-            p.outq[oi] = qv;
-            if ((t & 31) == 0) p.outs[oi / 32] = d;
+        __syncthreads();
+        const float M = fM[u];
+        if (t < ATT_HD) {
+            float num = 0.f, den = 0.f;
+            for (int c = 0; c < ncl_used; ++c) {
+                const float* b = base + (int64_t)c * (ATT_HD + 2);
+                const float mc = __ldcg(b + ATT_HD);
+                const float f = mc == -FLT_MAX ? 0.f : expf(mc - M);
+                num = fmaf(f, __ldcg(b + t), num);
+                den = fmaf(f, __ldcg(b + ATT_HD + 1), den);
+            }
+            const float o = num / den;
+            const int64_t oi = ((int64_t)g * G + hh) * ATT_HD + t;
+            p.out[oi] = o;
+            if (p.outq) {  // warps 0..3 hold the head's four 32-value blocks
+                float d;
+                const int8_t qv = quantize_lane(o, d);
+                p.outq[oi] = qv;
+                if ((t & 31) == 0) p.outs[oi / 32] = d;
+            }
         }
+        if (t == 0) p.cnt[g * G + hh] = 0;
     }
-    if (t == 0) p.cnt[g * G + hh] = 0;
 }
 
-// grid (kv, chunk) in clusters of 8 chunks, 8 warps.  Scores: 4 lanes per position (a 32-dim quarter each), each warp
-// 16 positions in two passes, all of a pass's key loads issued first.  Values: warp w takes positions w, w+8, ...
-// (16 rows, loaded before use), lane l the dims 4l..4l+3; the 8 warps' sums meet in shared memory.  A chunk's partial
+// grid (kv, chunk) in clusters of 4 chunks, 8 warps, two CTAs per SM.  Scores: 4 lanes per position (a 32-dim quarter
+// each), each warp 8 positions.  Values: warp w takes positions w, w+8, ... (8 rows), lane l the dims 4l..4l+3; every
+// key and value row is loaded before any is used; the 8 warps' sums meet in shared memory.  A chunk's partial
 // is then folded with the rest of its cluster and across clusters (fold_cluster), always in chunk order.
-__global__ void __launch_bounds__(ATT_THREADS) attention_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(ATT_THREADS, 2) attention_kernel(const AttnParams p) {
     __shared__ __align__(16) float qs[ATT_MAXG][4 * ATT_QP];
     __shared__ __align__(16) float sc[ATT_MAXG][ATT_CHUNK];
     __shared__ __align__(16) float red[ATT_THREADS / 32][ATT_MAXG][ATT_HD];  // [warp][g][dim]; float4 stores
@@ -209,10 +218,11 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_kernel(const AttnParams
     const float* kb = p.k_cache + ((int64_t)g * p.ctx + p0) * ATT_HD;
     const float* vb = p.v_cache + ((int64_t)g * p.ctx + p0) * ATT_HD;
     const int sub = lane & 3;
-    float kr[2][32];
+    constexpr int PASSES = ATT_CHUNK / 64;
+    float kr[PASSES][32];
     float4 vr[ATT_CHUNK / 8];
 #pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
+    for (int pass = 0; pass < PASSES; ++pass) {
         const int pl = pass * 64 + wid * 8 + (lane >> 2);
         const bool pre = pl < np && pl != newrow;
         const float4* kp = reinterpret_cast<const float4*>(kb + (int64_t)(pre ? pl : 0) * ATT_HD + sub * 32);
@@ -235,7 +245,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_kernel(const AttnParams
     griddep_launch();
     // the new row and the queries, written by this step's earlier kernels
 #pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
+    for (int pass = 0; pass < PASSES; ++pass) {
         const int pl = pass * 64 + wid * 8 + (lane >> 2);
         if (pl == newrow) {
             const float4* kp = reinterpret_cast<const float4*>(kb + (int64_t)pl * ATT_HD + sub * 32);
@@ -259,7 +269,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_kernel(const AttnParams
     __syncthreads();
     // scores (every lane runs the same path; lanes past the chunk's end multiply zeros and store nothing)
 #pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
+    for (int pass = 0; pass < PASSES; ++pass) {
         const int pl = pass * 64 + wid * 8 + (lane >> 2);
         const bool valid = pl < np;
         for (int hh = 0; hh < G; ++hh) {

@@ -115,10 +115,6 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
         }
         n.err = m->err;
         n.pdl = pdl;
-        if (m->prefetch) {  // this layer's O projection and router, read after the attention
-            add_mat(n.pf, m->wo[l]);
-            add_mat(n.pf, m->router[l]);
-        }
         Q8_TRY(launch_add_rmsnorm(n, st));
         // q, k and v in one projection launch
         {
@@ -221,16 +217,6 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             t.ids = m->ids;
             t.gates = m->gates;
             t.pdl = pdl;
-            if (m->prefetch) {  // the chosen experts' rows, as soon as they are chosen
-                t.xp.gq = m->gate[l].q;
-                t.xp.gs = m->gate[l].s;
-                t.xp.uq = m->up[l].q;
-                t.xp.us = m->up[l].s;
-                t.xp.dq = m->down[l].q;
-                t.xp.ds = m->down[l].s;
-                t.xp.dff = d.dff;
-                t.xp.d = D;
-            }
             Q8_TRY(launch_topk(t, st));
         }
         {
@@ -315,11 +301,6 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
         a.err = m->err;
         a.ctx = (int)d.ctx;
         a.pdl = pdl;
-        if (m->prefetch) {  // the first layer's q, k and v projections, for the next step
-            add_mat(a.pf, m->wq[0]);
-            add_mat(a.pf, m->wk[0]);
-            add_mat(a.pf, m->wv[0]);
-        }
         Q8_TRY(launch_argmax(a, cv, st));
     }
 #undef Q8_TRY
