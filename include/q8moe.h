@@ -54,7 +54,7 @@ typedef enum {
     Q8_EINVAL = -1,       /* a null, misaligned or out-of-range argument */
     Q8_EUNSUPPORTED = -2, /* a shape the kernels refuse (cols % 32, K outside [1,32], more than 8192 experts, ...) */
     Q8_ECUDA = -3,        /* a CUDA runtime error (launch, capture, allocation at create time) */
-    Q8_ETIMEOUT = -4,     /* reserved: a bounded device-side wait gave up */
+    Q8_ETIMEOUT = -4,     /* a bounded device-side wait gave up (reported by q8_model_check) */
     Q8_ENOSPACE = -5      /* the workspace is too small for the call */
 } q8_status;
 

@@ -13,6 +13,7 @@
 // and the last warp to arrive on the item's counter adds the slices in slice order (deterministic) and resets it.
 #include "common.cuh"
 #include "kernels.h"
+#include "stream.cuh"
 
 namespace q8 {
 
@@ -130,6 +131,161 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gemv_kernel(const GemvParams p)
     }
 }
 
+// ---- the TMA-fed projection (one activation row) -------------------------------------------------------------------
+// A CTA owns tiles t = blockIdx.x + i*gridDim.x of TR consecutive rows (never across segments).  Warp 8 lane 0 copies
+// each tile's quant rows and scale rows into a ring of NS shared-memory stages with cp.async.bulk; the first NS tiles
+// are issued before waiting for earlier kernels, since weights never depend on them.  Warps 0..7 take rows w, w+8, ...
+// of a stage: lane l reads the 16 bytes at 16l + 512j of the row (conflict-free), lanes 2m and 2m+1 hold the two halves
+// of block m + 16j and add their partial dots with one shuffle before the block is scaled.
+constexpr int TMA_CONSUMERS = 8;
+constexpr int TMA_THREADS = (TMA_CONSUMERS + 1) * 32;
+constexpr int TMA_MAX_TR = 16;
+constexpr int TMA_SMEM = 100 * 1024;
+
+struct TmaParams {
+    GemvParams g;
+    int tr;        // rows per tile
+    int tiles;     // total tiles over all segments
+    int t0[4];     // first tile of each segment
+    int ns;        // stages
+    int stage;     // bytes per stage (quants then scales, 16-byte aligned)
+    int* err;
+};
+
+template <int MODE, int KCH>
+__global__ void __launch_bounds__(TMA_THREADS, 1) gemv_tma_kernel(const TmaParams tp) {
+    using T = typename AccType<MODE>::T;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const GemvParams& p = tp.g;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + 8;
+    unsigned char* ring = smem + 128;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int k = p.k, nb = p.nb;
+    const int nmine = tp.tiles > (int)blockIdx.x ? (tp.tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < tp.ns; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], TMA_CONSUMERS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    issue_l2_prefetch(p.pf);
+
+    auto tile_of = [&](int i, int& sg, int& row0, int& rows) {
+        const int t = blockIdx.x + i * gridDim.x;
+        sg = 0;
+        while (sg + 1 < p.nseg && t >= tp.t0[sg + 1]) ++sg;
+        row0 = (t - tp.t0[sg]) * tp.tr;
+        rows = min(tp.tr, p.n[sg] - row0);
+    };
+
+    if (wid == TMA_CONSUMERS) {
+        // producer: weights only, so it never waits for earlier kernels
+        if (lane == 0) {
+            for (int i = 0; i < nmine; ++i) {
+                const int s = i % tp.ns;
+                if (i >= tp.ns && !mbar_wait(&empty[s], ((i / tp.ns) - 1) & 1, tp.err)) break;
+                int sg, row0, rows;
+                tile_of(i, sg, row0, rows);
+                unsigned char* st = ring + (size_t)s * tp.stage;
+                const unsigned qb = (unsigned)rows * (unsigned)k, sb = (unsigned)rows * (unsigned)nb * 4u;
+                mbar_arrive_expect_tx(&full[s], qb + sb);
+                bulk_g2s(st, p.q[sg] + (int64_t)row0 * k, qb, &full[s]);
+                bulk_g2s(st + (size_t)tp.tr * k, p.s[sg] + (int64_t)row0 * nb, sb, &full[s]);
+            }
+        }
+        return;
+    }
+
+    griddep_wait();
+    griddep_launch();
+    // this lane's activation values: columns 16*lane + 512*j
+    uint32_t xw[MODE == 1 ? KCH : 1][4];
+    float xsc[KCH];
+    float xf[MODE == 0 ? KCH : 1][MODE == 0 ? 16 : 1];
+#pragma unroll
+    for (int j = 0; j < KCH; ++j) {
+        const int col = 16 * lane + 512 * j;
+        const bool ok = col < k;
+        if (MODE == 1) {
+            const uint4 v = ok ? *reinterpret_cast<const uint4*>(p.xq + col) : make_uint4(0, 0, 0, 0);
+            xw[j][0] = v.x; xw[j][1] = v.y; xw[j][2] = v.z; xw[j][3] = v.w;
+            xsc[j] = ok ? p.xs[col / 32] : 0.f;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 v = ok ? *reinterpret_cast<const float4*>(p.x + col + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xf[j][4 * e] = v.x; xf[j][4 * e + 1] = v.y; xf[j][4 * e + 2] = v.z; xf[j][4 * e + 3] = v.w;
+            }
+            xsc[j] = 0.f;
+        }
+    }
+    bool ok_all = true;
+    for (int i = 0; i < nmine; ++i) {
+        const int s = i % tp.ns;
+        if (!mbar_wait(&full[s], (i / tp.ns) & 1, tp.err)) {
+            ok_all = false;
+            break;
+        }
+        int sg, row0, rows;
+        tile_of(i, sg, row0, rows);
+        const int8_t* sq = reinterpret_cast<const int8_t*>(ring + (size_t)s * tp.stage);
+        const float* ss = reinterpret_cast<const float*>(ring + (size_t)s * tp.stage + (size_t)tp.tr * k);
+        for (int r = wid; r < rows; r += TMA_CONSUMERS) {
+            T acc = 0;
+#pragma unroll
+            for (int j = 0; j < KCH; ++j) {
+                const int col = 16 * lane + 512 * j;
+                const bool ok = col < k;
+                const uint4 w = ok ? *reinterpret_cast<const uint4*>(sq + (size_t)r * k + col) : make_uint4(0, 0, 0, 0);
+                const float sc = ok ? ss[(size_t)r * nb + col / 32] : 0.f;
+                if (MODE == 1) {
+                    int d = __dp4a((int)w.x, (int)xw[j][0], 0);
+                    d = __dp4a((int)w.y, (int)xw[j][1], d);
+                    d = __dp4a((int)w.z, (int)xw[j][2], d);
+                    d = __dp4a((int)w.w, (int)xw[j][3], d);
+                    d += __shfl_xor_sync(0xffffffffu, d, 1);  // the block's exact dot: both halves
+                    if (!(lane & 1)) acc = fmaf(sc * xsc[j], (float)d, (float)acc);
+                } else {
+                    const uint32_t wv[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u,
+                                            w.w ^ 0x80808080u};
+                    float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        p0 = fmaf(i8_to_f32<0>(wv[e]), xf[j][4 * e + 0], p0);
+                        p1 = fmaf(i8_to_f32<1>(wv[e]), xf[j][4 * e + 1], p1);
+                        p0 = fmaf(i8_to_f32<2>(wv[e]), xf[j][4 * e + 2], p0);
+                        p1 = fmaf(i8_to_f32<3>(wv[e]), xf[j][4 * e + 3], p1);
+                    }
+                    float ps = p0 + p1;
+                    ps += __shfl_xor_sync(0xffffffffu, ps, 1);  // the block's f32 partial: both halves
+                    if (!(lane & 1)) acc = fma((double)sc, (double)ps, (double)acc);
+                }
+            }
+            acc = group_sum<32>(acc);
+            if (lane == 0) {
+                float v = (float)acc;
+                const int row = row0 + r;
+                if (p.res[sg]) v = p.res[sg][row] + v;
+                p.y[sg][row] = v;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (!ok_all)  // a wait gave up: let this CTA's copies in flight land before it exits (again bounded)
+        for (int i = 0; i < nmine && i < tp.ns; ++i) mbar_wait(&full[i], 0, nullptr);
+}
+
+bool tma_eligible(const GemvCall& c) {
+    if (c.R != 1 || c.dots || c.k % 128 != 0 || c.k > 4096) return false;
+    for (int i = 0; i < c.nseg; ++i)
+        if ((uintptr_t)c.seg[i].s % 16 != 0 || (uintptr_t)c.seg[i].q % 16 != 0) return false;
+    return true;
+}
+
 struct Plan {
     int lpr, bpl, rt, S;
     int rpw() const { return 32 / lpr; }
@@ -204,6 +360,11 @@ cudaError_t dispatch(const Plan& pl, const GemvParams& p, int64_t grid, cudaStre
 }  // namespace
 
 void gemv_scratch(const GemvCall& c, size_t* bytes, size_t* counters) {
+    if (tma_eligible(c)) {  // whole rows through the TMA ring: no scratch
+        *bytes = 0;
+        *counters = 0;
+        return;
+    }
     const Plan pl = plan_for(c);
     int64_t ntot = 0;
     for (int i = 0; i < c.nseg; ++i) ntot += c.seg[i].n;
@@ -216,7 +377,75 @@ void gemv_scratch(const GemvCall& c, size_t* bytes, size_t* counters) {
     }
 }
 
+namespace {
+
+template <int MODE, int KCH>
+cudaError_t run_tma(const TmaParams& tp, int grid, size_t smem, cudaStream_t st, int pdl) {
+    auto kern = gemv_tma_kernel<MODE, KCH>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch(kern, dim3(grid), dim3(TMA_THREADS), smem, st, pdl, tp);
+}
+
+cudaError_t launch_gemv_tma(const GemvCall& c, int* err, cudaStream_t st) {
+    TmaParams tp = {};
+    GemvParams& p = tp.g;
+    p.nseg = c.nseg;
+    p.k = (int)c.k;
+    p.nb = (int)(c.k / 32);
+    p.x = c.x;
+    p.xq = c.xq;
+    p.xs = c.xs;
+    p.R = 1;
+    p.S = 1;
+    p.pf = c.pf;
+    int64_t rows_total = 0;
+    for (int i = 0; i < c.nseg; ++i) rows_total += c.seg[i].n;
+    // rows per tile: about 16 KB of quants per stage; smaller tiles when there are few
+    int tr = (int)(16384 / c.k);
+    if (tr < 4) tr = 4;
+    if (tr > TMA_MAX_TR) tr = TMA_MAX_TR;
+    const int sms = device_info().sms;
+    while (tr > 2 && rows_total / tr < 2 * sms) tr /= 2;
+    int tiles = 0;
+    for (int i = 0; i < c.nseg; ++i) {
+        p.q[i] = c.seg[i].q;
+        p.s[i] = c.seg[i].s;
+        p.y[i] = c.seg[i].y;
+        p.res[i] = c.seg[i].residual;
+        p.n[i] = (int)c.seg[i].n;
+        tp.t0[i] = tiles;
+        tiles += (int)((c.seg[i].n + tr - 1) / tr);
+    }
+    tp.t0[c.nseg] = tiles;
+    tp.tr = tr;
+    tp.tiles = tiles;
+    tp.stage = (int)(((size_t)tr * c.k + (size_t)tr * (c.k / 32) * 4 + 127) / 128 * 128);
+    int ns = (TMA_SMEM - 128) / tp.stage;
+    if (ns > 8) ns = 8;
+    if (ns < 2) return cudaErrorInvalidConfiguration;
+    tp.ns = ns;
+    tp.err = err;
+    const size_t smem = 128 + (size_t)ns * tp.stage;
+    const int grid = tiles < sms ? tiles : sms;
+    const int kch = (int)((c.k + 511) / 512);
+    if (c.mode == 1) {
+        if (kch <= 1) return run_tma<1, 1>(tp, grid, smem, st, c.pdl);
+        if (kch <= 2) return run_tma<1, 2>(tp, grid, smem, st, c.pdl);
+        if (kch <= 4) return run_tma<1, 4>(tp, grid, smem, st, c.pdl);
+        return run_tma<1, 8>(tp, grid, smem, st, c.pdl);
+    }
+    if (kch <= 1) return run_tma<0, 1>(tp, grid, smem, st, c.pdl);
+    if (kch <= 2) return run_tma<0, 2>(tp, grid, smem, st, c.pdl);
+    if (kch <= 4) return run_tma<0, 4>(tp, grid, smem, st, c.pdl);
+    return run_tma<0, 8>(tp, grid, smem, st, c.pdl);
+}
+
+}  // namespace
+
 cudaError_t launch_gemv(const GemvCall& c, Carve& ws, cudaStream_t st) {
+    if (tma_eligible(c))
+        return launch_gemv_tma(c, c.err ? c.err : (ws.counters ? ws.counters + ws.n_counters - 1 : nullptr), st);
     const int nb = (int)(c.k / 32);
     const Plan pl = plan_for(c);
     GemvParams p = {};

@@ -65,6 +65,7 @@ struct GemvCall {
     const float* xs = nullptr;           // [R][k/32]
     int64_t R = 1;
     int32_t* dots = nullptr;             // mode 1 debug export [R][n][k/32] (single segment)
+    int* err = nullptr;                  // device error word for a pipeline wait that gave up
     L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;                         // launch with programmatic dependent launch allowed
 };

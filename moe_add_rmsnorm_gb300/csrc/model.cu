@@ -130,6 +130,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             g.xq = m->xq;
             g.xs = m->xs;
             g.pdl = pdl;
+            g.err = m->err;
             Q8_TRY(launch_gemv(g, cv, st));
         }
         {
@@ -182,6 +183,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             g.xq = m->attq;
             g.xs = m->atts;
             g.pdl = pdl;
+            g.err = m->err;
             Q8_TRY(launch_gemv(g, cv, st));
         }
         // feed-forward half
@@ -208,6 +210,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             g.xq = m->xq;
             g.xs = m->xs;
             g.pdl = pdl;
+            g.err = m->err;
             Q8_TRY(launch_gemv(g, cv, st));
             TopkCall t;
             t.logits = m->rlog;
@@ -289,6 +292,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
         g.xq = m->xq;
         g.xs = m->xs;
         g.pdl = pdl;
+        g.err = m->err;
         Q8_TRY(launch_gemv(g, cv, st));
     }
     {
@@ -503,6 +507,7 @@ int q8_model_check(q8_model* m, q8_stream stream) {
     if (e != cudaSuccess) return model_fail(Q8_ECUDA, "q8_model_check: %s", cudaGetErrorString(e));
     if (v & 1) return model_fail(Q8_EINVAL, "a step read a token outside [0, vocab)");
     if (v & 2) return model_fail(Q8_EINVAL, "a step met a position outside [0, ctx)");
+    if (v & 4) return model_fail(Q8_ETIMEOUT, "a weight pipeline wait gave up (the step's results are not valid)");
     return Q8_OK;
 }
 
