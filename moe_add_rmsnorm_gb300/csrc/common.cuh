@@ -168,6 +168,76 @@ __device__ __forceinline__ typename AccType<MODE>::T tile_row_dot(const WTile<BP
     return acc;
 }
 
+// ---- a lane's half-block view of a row held in shared memory -----------------------------------------------------
+// Lane l reads the 16 bytes at columns 16l + 512j (j < KCH) of a row: conflict-free 128-bit shared loads.  Lanes 2m and
+// 2m+1 hold the two halves of block m + 16j, so a block's dot is the sum of the pair's halves (one shuffle).
+template <int MODE, int KCH>
+struct XHalf {
+    uint32_t w[MODE == 1 ? KCH : 1][4];
+    float f[MODE == 0 ? KCH : 1][MODE == 0 ? 16 : 1];
+    float s[KCH];
+};
+
+// Loads this lane's columns of an activation row (global or shared): f32 values, or words and their block scales.
+template <int MODE, int KCH>
+__device__ __forceinline__ void load_xhalf(XHalf<MODE, KCH>& x, const float* xf, const int8_t* xq, const float* xs,
+                                           int k, int lane) {
+#pragma unroll
+    for (int j = 0; j < KCH; ++j) {
+        const int col = 16 * lane + 512 * j;
+        const bool ok = col < k;
+        if (MODE == 1) {
+            const uint4 v = ok ? *reinterpret_cast<const uint4*>(xq + col) : make_uint4(0, 0, 0, 0);
+            x.w[j][0] = v.x; x.w[j][1] = v.y; x.w[j][2] = v.z; x.w[j][3] = v.w;
+            x.s[j] = ok ? xs[col / 32] : 0.f;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 v = ok ? *reinterpret_cast<const float4*>(xf + col + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                x.f[j][4 * e] = v.x; x.f[j][4 * e + 1] = v.y; x.f[j][4 * e + 2] = v.z; x.f[j][4 * e + 3] = v.w;
+            }
+            x.s[j] = 0.f;
+        }
+    }
+}
+
+// This lane's share of (row . x) for a Q8_0 row in shared memory (quants q_row[k], scales s_row[k/32]); summed over the
+// warp it is the row's dot (blocks scaled, f64 sums in mode 0, f32 in mode 1).  Every lane must call it.
+template <int MODE, int KCH>
+__device__ __forceinline__ typename AccType<MODE>::T smem_row_dot(const int8_t* q_row, const float* s_row, int k,
+                                                                  const XHalf<MODE, KCH>& x, int lane) {
+    typename AccType<MODE>::T acc = 0;
+#pragma unroll
+    for (int j = 0; j < KCH; ++j) {
+        const int col = 16 * lane + 512 * j;
+        const bool ok = col < k;
+        const uint4 w = ok ? *reinterpret_cast<const uint4*>(q_row + col) : make_uint4(0, 0, 0, 0);
+        const float sc = ok ? s_row[col / 32] : 0.f;
+        if (MODE == 1) {
+            int d = __dp4a((int)w.x, (int)x.w[j][0], 0);
+            d = __dp4a((int)w.y, (int)x.w[j][1], d);
+            d = __dp4a((int)w.z, (int)x.w[j][2], d);
+            d = __dp4a((int)w.w, (int)x.w[j][3], d);
+            d += __shfl_xor_sync(0xffffffffu, d, 1);
+            if (!(lane & 1)) acc = fmaf(sc * x.s[j], (float)d, (float)acc);
+        } else {
+            const uint32_t wv[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+            float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                p0 = fmaf(i8_to_f32<0>(wv[e]), x.f[j][4 * e + 0], p0);
+                p1 = fmaf(i8_to_f32<1>(wv[e]), x.f[j][4 * e + 1], p1);
+                p0 = fmaf(i8_to_f32<2>(wv[e]), x.f[j][4 * e + 2], p0);
+                p1 = fmaf(i8_to_f32<3>(wv[e]), x.f[j][4 * e + 3], p1);
+            }
+            float ps = p0 + p1;
+            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+            if (!(lane & 1)) acc = fma((double)sc, (double)ps, (double)acc);
+        }
+    }
+    return acc;
+}
+
 // ---- reductions -----------------------------------------------------------------------------------------------
 
 template <int LANES, typename T>

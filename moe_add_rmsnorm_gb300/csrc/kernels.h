@@ -147,6 +147,7 @@ struct ExpertCall {
     const float* residual = nullptr;     // down
     float* y = nullptr;                  // down out [R][d]
     float* expert_out = nullptr;         // down out [R][K][d]
+    int* err = nullptr;                  // device error word for a pipeline wait that gave up
     L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };

@@ -241,6 +241,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             c.xs = m->xs;
             c.h = m->hbuf;
             c.pdl = pdl;
+            c.err = m->err;
             if (m->prefetch && l + 1 < d.layers) {  // the next layer's q, k and v projections
                 add_mat(c.pf, m->wq[l + 1]);
                 add_mat(c.pf, m->wk[l + 1]);
@@ -265,6 +266,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             c.residual = m->h;  // h = h + mixture
             c.y = m->h;
             c.pdl = pdl;
+            c.err = m->err;
             Q8_TRY(launch_down_combine(c, cv, st));
         }
     }
