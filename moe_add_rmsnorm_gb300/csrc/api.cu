@@ -257,6 +257,25 @@ int moe_route_topk(const q8_mat* router, q8_mode mode, const float* x, const q8_
         if (int r = check_plan(plan)) return r;
     if (rows == 0) return Q8_OK;
     cudaStream_t st = (cudaStream_t)stream;
+    const bool act = mode == Q8_INT8ACT ? (xq && !check_act(xq, "xq")) : (x && aligned(x, 16));
+    if (rows == 1 && !plan && act && route_row_supported((int)mode, E, router->cols, k)) {
+        // one row: the projection and the top-k in one cluster launch
+        RouteRowCall c;
+        c.mode = (int)mode;
+        c.q = router->q;
+        c.s = router->s;
+        c.E = E;
+        c.d = router->cols;
+        c.K = k;
+        c.x = x;
+        c.xq = mode == Q8_INT8ACT ? xq->q : nullptr;
+        c.xs = mode == Q8_INT8ACT ? xq->s : nullptr;
+        c.logits = logits;
+        c.ids = ids;
+        c.gates = gates;
+        cudaError_t e = launch_route_row(c, st);
+        return e == cudaSuccess ? Q8_OK : cuda_fail(e, "moe_route_topk");
+    }
     q8_ws tmp = *ws;
     float* l = logits;
     Carve cv = ws->carve();

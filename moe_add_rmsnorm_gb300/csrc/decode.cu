@@ -1,5 +1,6 @@
-// The decode step's attention side and its last stage: per-head QK-norm + RoPE + KV append, single-query GQA
-// attention split over positions, and the greedy arg-max that advances token and position on the device.
+// The decode step's attention side and its last stage: single-query GQA attention split over positions, with the
+// per-head QK-norm + RoPE and the KV append done inside it, and the greedy arg-max that advances token and position on
+// the device.
 //
 // What it computes: qwen_emit docs, emit_qwen30b_generate (per-head QK-norm + RoPE, causal attention over a KV cache,
 // device-side position and token); forward_shim.rs, kernel_refusal (Rope: a full rotary; Attention: scores scaled by
@@ -12,9 +13,11 @@
 // per position and key/value head), so the attention is a streaming kernel: every (key/value head, chunk of
 // positions) pair is one CTA that reads its rows once with coalesced 16-byte loads and serves all query heads of its
 // group from those registers; chunk partials (max, sum, weighted values) are folded in chunk order, first inside a
-// thread-block cluster of 8 chunks through distributed shared memory, then across clusters by the last to arrive.  The
+// thread-block cluster of 4 chunks through distributed shared memory, then across clusters by the last to arrive.  The
 // 48 KiB static score row of the pages' design is not needed: a chunk's scores live in shared memory and any cache
-// length works.
+// length works.  Every CTA norms and turns its group's query heads itself (a few hundred values), so no launch sits
+// between the projection and the attention; the CTA whose chunk holds the new position also norms and turns the new
+// key row and writes it and the value row to the caches.
 #include <float.h>
 
 #include <cooperative_groups.h>
@@ -28,54 +31,6 @@ namespace q8 {
 namespace {
 
 
-// ==== QK-norm + RoPE + KV append =================================================================================
-
-// CTA h < heads: query head h (normed and turned in place).  CTA heads + g: key head g (normed, turned, written at
-// pos) and value head g (written at pos).  hd/2 threads; thread i holds the pair (i, i + hd/2).
-__global__ void __launch_bounds__(256) qk_rope_kv_kernel(const QkRopeCall c) {
-    __shared__ float red[8];
-    const int h = blockIdx.x;
-    const int i = threadIdx.x;
-    const int half = c.hd / 2;
-    issue_l2_prefetch(c.pf);
-    griddep_wait();
-    griddep_launch();
-    const int pos = *c.pos;
-    if (pos < 0 || pos >= c.ctx) {
-        if (i == 0 && h == 0 && c.err) atomicOr(c.err, 2);
-        return;
-    }
-    const bool is_q = h < c.heads;
-    const int g = is_q ? h : h - c.heads;
-    const float* src = is_q ? c.q + (int64_t)g * c.hd : c.k + (int64_t)g * c.hd;
-    const float* w = is_q ? c.q_norm : c.k_norm;
-    float a = src[i], b = src[i + half];
-    float ss = a * a + b * b;
-    ss = group_sum<32>(ss);
-    if ((i & 31) == 0) red[i >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-    for (int j = 0; j < (half + 31) / 32; ++j) tot += red[j];
-    const float inv = 1.0f / sqrtf(tot / (float)c.hd + c.eps);
-    a = a * inv * w[i];
-    b = b * inv * w[i + half];
-    const float cs = c.cos_t[(int64_t)pos * half + i], sn = c.sin_t[(int64_t)pos * half + i];
-    const float ra = a * cs - b * sn;
-    const float rb = a * sn + b * cs;
-    if (is_q) {
-        __syncthreads();  // every thread has read its pair before any write
-        c.q[(int64_t)g * c.hd + i] = ra;
-        c.q[(int64_t)g * c.hd + i + half] = rb;
-    } else {
-        float* kr = c.k_cache + ((int64_t)g * c.ctx + pos) * c.hd;
-        float* vr = c.v_cache + ((int64_t)g * c.ctx + pos) * c.hd;
-        kr[i] = ra;
-        kr[i + half] = rb;
-        vr[i] = c.v[(int64_t)g * c.hd + i];
-        vr[i + half] = c.v[(int64_t)g * c.hd + i + half];
-    }
-}
-
 // ==== attention ===================================================================================================
 
 constexpr int ATT_THREADS = 256;
@@ -86,9 +41,17 @@ constexpr int ATT_QP = 36;      // padded 32-dim quarter of a query row in share
 constexpr int ATT_CLUSTER = 4;  // chunks per thread-block cluster
 
 struct AttnParams {
-    const float* q;
-    const float* k_cache;
-    const float* v_cache;
+    const float* q;        // the projection's q, k and v rows, before QK-norm and RoPE
+    const float* k;
+    const float* v;
+    const float* q_norm;
+    const float* k_norm;
+    const float* cos_t;    // [ctx][ATT_HD / 2]
+    const float* sin_t;
+    float eps;
+    int* err;
+    float* k_cache;
+    float* v_cache;
     const int32_t* pos;
     int heads, kv, ctx, G;
     float scale;
@@ -113,7 +76,6 @@ __device__ void fold_cluster(const AttnParams& p, int g, int chunk, int G, int t
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ int last[ATT_MAXG];
     __shared__ float fm[ATT_MAXG][ATT_CLUSTER];
-    __shared__ float fM[ATT_MAXG];
     cluster.sync();  // every chunk's partial is in its CTA's shared memory
     const int rank = (int)cluster.block_rank();
     const int cl = chunk / ATT_CLUSTER;
@@ -152,38 +114,62 @@ __device__ void fold_cluster(const AttnParams& p, int g, int chunk, int G, int t
         last[t] = hh < G ? (atomicAdd(p.cnt + g * G + hh, 1) == ncl_used - 1) : 0;
     }
     __syncthreads();
+    // the heads this CTA arrived last for: all 256 threads fold the clusters' partials, every load of a batch of 8
+    // clusters in flight at once; the CTA's two halves take the first and the second half of the clusters
+    __shared__ float redm[ATT_THREADS / 32];
+    __shared__ float fnum[ATT_HD];
+    __shared__ float fden;
+    const int lane = t & 31, wid = t >> 5;
+    const int half = t / ATT_HD, d = t % ATT_HD;
+    const int hsplit = (ncl_used + 1) / 2;
+    const int c0 = half ? hsplit : 0, c1 = half ? ncl_used : hsplit;
     for (int u = 0, hh = rank; hh < G; ++u, hh += ATT_CLUSTER) {
         if (!last[u]) continue;  // CTA-uniform
         __threadfence();
         const float* base = p.part + ((int64_t)g * G + hh) * ncl * (ATT_HD + 2);
-        if (t < 32) {
-            float M = -FLT_MAX;
-            for (int c = t; c < ncl_used; c += 32) M = fmaxf(M, __ldcg(base + (int64_t)c * (ATT_HD + 2) + ATT_HD));
-            M = warp_max(M);
-            if (t == 0) fM[u] = M;
+        float M = -FLT_MAX;
+        for (int c = t; c < ncl_used; c += ATT_THREADS) M = fmaxf(M, __ldcg(base + (int64_t)c * (ATT_HD + 2) + ATT_HD));
+        M = warp_max(M);
+        if (lane == 0) redm[wid] = M;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < ATT_THREADS / 32; ++w) M = fmaxf(M, redm[w]);
+        float num = 0.f, den = 0.f;
+        for (int cb = c0; cb < c1; cb += 8) {
+            float mc[8], vc[8], lc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int c = cb + i;
+                const float* b = base + (int64_t)(c < c1 ? c : c1 - 1) * (ATT_HD + 2);
+                mc[i] = c < c1 ? __ldcg(b + ATT_HD) : -FLT_MAX;
+                vc[i] = c < c1 ? __ldcg(b + d) : 0.f;
+                lc[i] = c < c1 ? __ldcg(b + ATT_HD + 1) : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float f = mc[i] == -FLT_MAX ? 0.f : expf(mc[i] - M);
+                num = fmaf(f, vc[i], num);
+                den = fmaf(f, lc[i], den);
+            }
+        }
+        if (half) {
+            fnum[d] = num;
+            if (d == 0) fden = den;
         }
         __syncthreads();
-        const float M = fM[u];
-        if (t < ATT_HD) {
-            float num = 0.f, den = 0.f;
-            for (int c = 0; c < ncl_used; ++c) {
-                const float* b = base + (int64_t)c * (ATT_HD + 2);
-                const float mc = __ldcg(b + ATT_HD);
-                const float f = mc == -FLT_MAX ? 0.f : expf(mc - M);
-                num = fmaf(f, __ldcg(b + t), num);
-                den = fmaf(f, __ldcg(b + ATT_HD + 1), den);
-            }
-            const float o = num / den;
-            const int64_t oi = ((int64_t)g * G + hh) * ATT_HD + t;
+        if (!half) {
+            const float o = (num + fnum[d]) / (den + fden);
+            const int64_t oi = ((int64_t)g * G + hh) * ATT_HD + d;
             p.out[oi] = o;
             if (p.outq) {  // warps 0..3 hold the head's four 32-value blocks
-                float d;
-                const int8_t qv = quantize_lane(o, d);
+                float dsc;
+                const int8_t qv = quantize_lane(o, dsc);
                 p.outq[oi] = qv;
-                if ((t & 31) == 0) p.outs[oi / 32] = d;
+                if (lane == 0) p.outs[oi / 32] = dsc;
             }
         }
         if (t == 0) p.cnt[g * G + hh] = 0;
+        __syncthreads();  // fnum and redm are reused by the next head
     }
 }
 
@@ -196,6 +182,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attention_kernel(const AttnPar
     __shared__ __align__(16) float sc[ATT_MAXG][ATT_CHUNK];
     __shared__ __align__(16) float red[ATT_THREADS / 32][ATT_MAXG][ATT_HD];  // [warp][g][dim]; float4 stores
     __shared__ float stat[ATT_MAXG][2];
+    __shared__ __align__(16) float knew[ATT_HD];
+    __shared__ __align__(16) float vnew[ATT_HD];
+    __shared__ float nred[ATT_MAXG + 1][2];
     const int g = blockIdx.x, chunk = blockIdx.y;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int G = p.G;
@@ -210,6 +199,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attention_kernel(const AttnPar
     if (len < 1 || len > p.ctx || (chunk / ATT_CLUSTER) * ATT_CLUSTER >= nch) {
         griddep_wait();
         griddep_launch();
+        if ((len < 1 || len > p.ctx) && g == 0 && chunk == 0 && t == 0 && p.err) atomicOr(p.err, 2);
         return;
     }
     const int p0 = chunk * ATT_CHUNK;
@@ -241,32 +231,96 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attention_kernel(const AttnPar
         vr[u] = (pl < np && pl != newrow) ? __ldcs(reinterpret_cast<const float4*>(vb + (int64_t)pl * ATT_HD) + lane)
                                           : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    // QK-norm and RoPE constants for this position: thread t takes the pair (i, i + 64) of query heads t/64 and
+    // t/64 + 4 (and of the key head when t < 64)
+    const int hsub = t >> 6, pi = t & 63;
+    const int pos = len - 1;
+    const float cs = p.cos_t[(int64_t)pos * (ATT_HD / 2) + pi], sn = p.sin_t[(int64_t)pos * (ATT_HD / 2) + pi];
+    const float qw0 = p.q_norm[pi], qw1 = p.q_norm[pi + ATT_HD / 2];
+    const float kw0 = p.k_norm[pi], kw1 = p.k_norm[pi + ATT_HD / 2];
+    const bool has_new = newrow >= 0 && newrow < np;  // CTA-uniform
     griddep_wait();
     griddep_launch();
-    // the new row and the queries, written by this step's earlier kernels
+    // the projection's rows of this step: the group's queries, and the key and value rows the new position appends
+    float qa[2], qb[2], ka = 0.f, kb2 = 0.f, va = 0.f, vb2 = 0.f;
 #pragma unroll
-    for (int pass = 0; pass < PASSES; ++pass) {
-        const int pl = pass * 64 + wid * 8 + (lane >> 2);
-        if (pl == newrow) {
-            const float4* kp = reinterpret_cast<const float4*>(kb + (int64_t)pl * ATT_HD + sub * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = __ldcg(kp + i);
-                kr[pass][4 * i] = v.x;
-                kr[pass][4 * i + 1] = v.y;
-                kr[pass][4 * i + 2] = v.z;
-                kr[pass][4 * i + 3] = v.w;
-            }
-        }
+    for (int u = 0; u < 2; ++u) {
+        const int hh = hsub + 4 * u;
+        const float* src = p.q + ((int64_t)g * G + (hh < G ? hh : 0)) * ATT_HD;
+        qa[u] = hh < G ? __ldcg(src + pi) : 0.f;
+        qb[u] = hh < G ? __ldcg(src + pi + ATT_HD / 2) : 0.f;
     }
+    if (has_new && t < 64) {
+        ka = __ldcg(p.k + (int64_t)g * ATT_HD + pi);
+        kb2 = __ldcg(p.k + (int64_t)g * ATT_HD + pi + ATT_HD / 2);
+    } else if (has_new && t < 128) {
+        va = __ldcg(p.v + (int64_t)g * ATT_HD + pi);
+        vb2 = __ldcg(p.v + (int64_t)g * ATT_HD + pi + ATT_HD / 2);
+    }
+    // per-head sum of squares: a head's 64 threads are two warps
 #pragma unroll
-    for (int u = 0; u < ATT_CHUNK / 8; ++u)
-        if (wid + 8 * u == newrow) vr[u] = __ldcg(reinterpret_cast<const float4*>(vb + (int64_t)newrow * ATT_HD) + lane);
-    for (int i = t; i < G * ATT_HD; i += ATT_THREADS) {
-        const int hh = i / ATT_HD, dd = i % ATT_HD;
-        qs[hh][(dd >> 5) * ATT_QP + (dd & 31)] = p.q[((int64_t)g * G) * ATT_HD + i];
+    for (int u = 0; u < 2; ++u) {
+        const float ss = group_sum<32>(qa[u] * qa[u] + qb[u] * qb[u]);
+        if (lane == 0) nred[hsub + 4 * u][wid & 1] = ss;
+    }
+    {
+        const float ss = group_sum<32>(ka * ka + kb2 * kb2);
+        if (lane == 0 && t < 64) nred[ATT_MAXG][wid & 1] = ss;
     }
     __syncthreads();
+    // per-head RMSNorm (eps inside the root, the head weight multiplies), then the NeoX rotation of (i, i + 64)
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int hh = hsub + 4 * u;
+        if (hh < G) {
+            const float tot = (0.f + nred[hh][0]) + nred[hh][1];
+            const float inv = 1.0f / sqrtf(tot / (float)ATT_HD + p.eps);
+            const float a = qa[u] * inv * qw0, b = qb[u] * inv * qw1;
+            const float ra = a * cs - b * sn, rb = a * sn + b * cs;
+            qs[hh][(pi >> 5) * ATT_QP + (pi & 31)] = ra;
+            qs[hh][((pi + 64) >> 5) * ATT_QP + (pi & 31)] = rb;
+        }
+    }
+    if (has_new) {
+        if (t < 64) {
+            const float tot = (0.f + nred[ATT_MAXG][0]) + nred[ATT_MAXG][1];
+            const float inv = 1.0f / sqrtf(tot / (float)ATT_HD + p.eps);
+            const float a = ka * inv * kw0, b = kb2 * inv * kw1;
+            const float ra = a * cs - b * sn, rb = a * sn + b * cs;
+            knew[pi] = ra;
+            knew[pi + ATT_HD / 2] = rb;
+            float* kr_out = p.k_cache + ((int64_t)g * p.ctx + pos) * ATT_HD;
+            kr_out[pi] = ra;
+            kr_out[pi + ATT_HD / 2] = rb;
+        } else if (t < 128) {
+            vnew[pi] = va;
+            vnew[pi + ATT_HD / 2] = vb2;
+            float* vr_out = p.v_cache + ((int64_t)g * p.ctx + pos) * ATT_HD;
+            vr_out[pi] = va;
+            vr_out[pi + ATT_HD / 2] = vb2;
+        }
+    }
+    __syncthreads();
+    if (has_new) {  // the lanes that hold the new row take it from shared memory
+#pragma unroll
+        for (int pass = 0; pass < PASSES; ++pass) {
+            const int pl = pass * 64 + wid * 8 + (lane >> 2);
+            if (pl == newrow) {
+                const float4* kp = reinterpret_cast<const float4*>(knew + sub * 32);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 v = kp[i];
+                    kr[pass][4 * i] = v.x;
+                    kr[pass][4 * i + 1] = v.y;
+                    kr[pass][4 * i + 2] = v.z;
+                    kr[pass][4 * i + 3] = v.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < ATT_CHUNK / 8; ++u)
+            if (wid + 8 * u == newrow) vr[u] = reinterpret_cast<const float4*>(vnew)[lane];
+    }
     // scores (every lane runs the same path; lanes past the chunk's end multiply zeros and store nothing)
 #pragma unroll
     for (int pass = 0; pass < PASSES; ++pass) {
@@ -448,10 +502,6 @@ int argmax_blocks(int64_t n) {
 
 }  // namespace
 
-cudaError_t launch_qk_rope_kv(const QkRopeCall& c, cudaStream_t st) {
-    return launch(qk_rope_kv_kernel, dim3(c.heads + c.kv), dim3(c.hd / 2), 0, st, c.pdl, c);
-}
-
 void attention_scratch(const AttnCall& c, size_t* bytes, size_t* counters) {
     const int G = c.heads / c.kv;
     *bytes = (size_t)c.kv * G * (attn_chunks(c.ctx) / ATT_CLUSTER) * (ATT_HD + 2) * sizeof(float);
@@ -461,6 +511,14 @@ void attention_scratch(const AttnCall& c, size_t* bytes, size_t* counters) {
 cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
     AttnParams p = {};
     p.q = c.q;
+    p.k = c.k;
+    p.v = c.v;
+    p.q_norm = c.q_norm;
+    p.k_norm = c.k_norm;
+    p.cos_t = c.cos_t;
+    p.sin_t = c.sin_t;
+    p.eps = c.eps;
+    p.err = c.err;
     p.k_cache = c.k_cache;
     p.v_cache = c.v_cache;
     p.pos = c.pos;

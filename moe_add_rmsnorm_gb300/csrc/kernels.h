@@ -158,35 +158,48 @@ bool experts_supported(int mode, int64_t k);
 cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st);
 cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st);
 
+// One token row (moe_row.cu): the router projection and its top-k in one cluster launch, and a down-and-combine that
+// requests its weights before the dependency wait.
+struct RouteRowCall {
+    int mode = 0;
+    const int8_t* q = nullptr;  // router [E][d]
+    const float* s = nullptr;
+    int64_t E = 0, d = 0;
+    int K = 0;
+    const float* x = nullptr;   // f32 mode
+    const int8_t* xq = nullptr; // int8 mode
+    const float* xs = nullptr;
+    float* logits = nullptr;    // optional [E]
+    int32_t* ids = nullptr;
+    float* gates = nullptr;
+    L2Prefetch pf;
+    int pdl = 0;
+};
+bool route_row_supported(int mode, int64_t E, int64_t d, int K);
+cudaError_t launch_route_row(const RouteRowCall& c, cudaStream_t st);
+bool down_row_supported(const ExpertCall& c);
+cudaError_t launch_down_row(const ExpertCall& c, cudaStream_t st);
+
 // ---- decode-step pieces -----------------------------------------------------------------------------------------
-struct QkRopeCall {
-    float* q = nullptr;          // [heads][hd], normed and turned in place
-    const float* k = nullptr;    // [kv][hd]
-    const float* v = nullptr;    // [kv][hd]
-    const float* q_norm = nullptr;
+struct AttnCall {
+    // the projection's rows of this step, before QK-norm and RoPE: the kernel norms and turns them, appends k and v
+    // at `pos` to the caches and attends rows 0..pos
+    const float* q = nullptr;       // [heads][hd]
+    const float* k = nullptr;       // [kv][hd]
+    const float* v = nullptr;       // [kv][hd]
+    const float* q_norm = nullptr;  // [hd], shared by the heads
     const float* k_norm = nullptr;
     const float* cos_t = nullptr;   // [ctx][hd/2]
     const float* sin_t = nullptr;
+    float eps = 0.f;
     float* k_cache = nullptr;       // [kv][ctx][hd]
     float* v_cache = nullptr;
     const int32_t* pos = nullptr;
     int heads = 0, kv = 0, hd = 0, ctx = 0;
-    float eps = 0.f;
-    int* err = nullptr;
-    L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
-    int pdl = 0;
-};
-cudaError_t launch_qk_rope_kv(const QkRopeCall& c, cudaStream_t st);
-
-struct AttnCall {
-    const float* q = nullptr;       // [heads][hd]
-    const float* k_cache = nullptr; // [kv][ctx][hd]
-    const float* v_cache = nullptr;
-    const int32_t* pos = nullptr;   // attends rows 0..pos
-    int heads = 0, kv = 0, hd = 0, ctx = 0;
     float* out = nullptr;           // [heads][hd]
     int8_t* outq = nullptr;         // optional quantized output
     float* outs = nullptr;
+    int* err = nullptr;             // bit 2 set for a position outside [0, ctx)
     L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };

@@ -6,10 +6,11 @@
 // (module docs: the whole forward captured as one CUDA graph; every stage reads and writes whole buffers).
 //
 // Launches per layer (the merges are GB300 choices, not the pages'): one add+RMSNorm with its int8 epilogue; one
-// projection for q, k and v together; one QK-norm + RoPE + KV append; one split attention (its fold quantizes the
-// result for the O projection); the O projection with the residual sum in its epilogue; one add+RMSNorm; the router
-// projection and its top-k; gate-up; down-and-combine with the residual sum in its epilogue.  Then the final norm, the
-// LM head and the arg-max that advances token and position.
+// projection for q, k and v together; one split attention that first applies QK-norm and RoPE and appends the new key
+// and value rows (its fold quantizes the result for the O projection); the O projection with the residual sum in its
+// epilogue; one add+RMSNorm; the router projection with its top-k in one cluster launch; gate-up with its int8
+// epilogue; down-and-combine with the residual sum in its epilogue.  Then the final norm, the LM head and the arg-max
+// that advances token and position.
 #include <cuda_runtime.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -134,30 +135,17 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             Q8_TRY(launch_gemv(g, cv, st));
         }
         {
-            QkRopeCall r;
-            r.q = m->q;
-            r.k = m->k;
-            r.v = m->v;
-            r.q_norm = m->q_norm[l];
-            r.k_norm = m->k_norm[l];
-            r.cos_t = m->cos_t;
-            r.sin_t = m->sin_t;
-            r.k_cache = m->kc[l];
-            r.v_cache = m->vc[l];
-            r.pos = d.pos;
-            r.heads = (int)H;
-            r.kv = (int)KV;
-            r.hd = (int)HD;
-            r.ctx = (int)d.ctx;
-            r.eps = d.eps;
-            r.err = m->err;
-            r.pdl = pdl;
-            Q8_TRY(launch_qk_rope_kv(r, st));
-        }
-        {
             Carve cv = fresh_carve(m);
-            AttnCall a;
+            AttnCall a;  // QK-norm, RoPE and the cache append happen inside the attention launch
             a.q = m->q;
+            a.k = m->k;
+            a.v = m->v;
+            a.q_norm = m->q_norm[l];
+            a.k_norm = m->k_norm[l];
+            a.cos_t = m->cos_t;
+            a.sin_t = m->sin_t;
+            a.eps = d.eps;
+            a.err = m->err;
             a.k_cache = m->kc[l];
             a.v_cache = m->vc[l];
             a.pos = d.pos;
@@ -200,7 +188,23 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
         }
         n2.pdl = pdl;
         Q8_TRY(launch_add_rmsnorm(n2, st));
-        {
+        if (route_row_supported(mode, d.experts, D, (int)d.k)) {
+            // the router projection and its top-k in one cluster launch
+            RouteRowCall r;
+            r.mode = mode;
+            r.q = m->router[l].q;
+            r.s = m->router[l].s;
+            r.E = d.experts;
+            r.d = D;
+            r.K = (int)d.k;
+            r.x = m->x;
+            r.xq = m->xq;
+            r.xs = m->xs;
+            r.ids = m->ids;
+            r.gates = m->gates;
+            r.pdl = pdl;
+            Q8_TRY(launch_route_row(r, st));
+        } else {
             Carve cv = fresh_carve(m);
             GemvCall g;
             g.mode = mode;
@@ -262,7 +266,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             c.K = (int)d.k;
             c.ids = m->ids;
             c.gates = m->gates;
-            c.x = m->hbuf;  // f32 hidden rows; the int8 mode quantizes them as the kernel stages them
+            c.x = m->hbuf;  // f32 hidden rows; the int8 mode quantizes them as each CTA stages them
             c.residual = m->h;  // h = h + mixture
             c.y = m->h;
             c.pdl = pdl;

@@ -17,7 +17,6 @@
 
 #include "common.cuh"
 #include "kernels.h"
-#include "stream.cuh"
 
 namespace q8 {
 namespace {
@@ -400,207 +399,6 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) down_one_kernel(const ExpertPar
     }
 }
 
-// ---- TMA-fed expert kernels for one token row --------------------------------------------------------------------
-// Both take tiles of 8 rows; warp 8 lane 0 copies each tile's rows into a ring of shared-memory stages with
-// cp.async.bulk, consumer warp w takes row w of the stage.
-constexpr int XT_CONSUMERS = 8;
-constexpr int XT_THREADS = (XT_CONSUMERS + 1) * 32;
-constexpr int XT_TR = 8;
-constexpr int XT_SMEM = 100 * 1024;
-constexpr int DN_TR = 4;  // down-and-combine rows per tile: K experts' rows per stage
-
-struct XtParams {
-    ExpertParams e;
-    int ns, stage;  // stages and bytes per stage
-    int tiles;
-    int* err;
-};
-
-// Gate-up: tile = (kept expert j, rows i0 .. i0+8) — the gate rows, then the up rows, then their scale rows.
-template <int MODE, int KCH>
-__global__ void __launch_bounds__(XT_THREADS, 1) gate_up_tma_kernel(const XtParams xp) {
-    using T = typename AccType<MODE>::T;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const ExpertParams& p = xp.e;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + 8;
-    unsigned char* ring = smem + 128;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int k = p.k, nb = p.nb;
-    const int nt = (p.out_rows + XT_TR - 1) / XT_TR;  // tiles per expert
-    const int nmine = xp.tiles > (int)blockIdx.x ? (xp.tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < xp.ns; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], XT_CONSUMERS);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-    issue_l2_prefetch(p.pf);
-    griddep_wait();  // the expert ids come from the previous launch
-    griddep_launch();
-    const size_t qrows = (size_t)XT_TR * k, srows = (size_t)XT_TR * nb * 4;
-    if (wid == XT_CONSUMERS) {
-        if (lane == 0) {
-            for (int i = 0; i < nmine; ++i) {
-                const int s = i % xp.ns;
-                if (i >= xp.ns && !mbar_wait(&empty[s], ((i / xp.ns) - 1) & 1, xp.err)) break;
-                const int t = blockIdx.x + i * gridDim.x;
-                const int j = t / nt, i0 = (t % nt) * XT_TR;
-                const int rows = min(XT_TR, p.out_rows - i0);
-                const int e = p.ids[j];
-                const bool ev = e >= 0 && e < p.E;
-                const int64_t row0 = (int64_t)(ev ? e : 0) * p.out_rows + i0;
-                unsigned char* st = ring + (size_t)s * xp.stage;
-                const unsigned qb = (unsigned)rows * (unsigned)k, sb = (unsigned)rows * (unsigned)nb * 4u;
-                mbar_arrive_expect_tx(&full[s], 2 * (qb + sb));
-                bulk_g2s(st, p.q0 + row0 * k, qb, &full[s]);
-                bulk_g2s(st + qrows, p.q1 + row0 * k, qb, &full[s]);
-                bulk_g2s(st + 2 * qrows, p.s0 + row0 * nb, sb, &full[s]);
-                bulk_g2s(st + 2 * qrows + srows, p.s1 + row0 * nb, sb, &full[s]);
-            }
-        }
-        return;
-    }
-    XHalf<MODE, KCH> x;
-    load_xhalf<MODE, KCH>(x, p.x, p.xq, p.xs, k, lane);
-    bool ok_all = true;
-    for (int i = 0; i < nmine; ++i) {
-        const int s = i % xp.ns;
-        if (!mbar_wait(&full[s], (i / xp.ns) & 1, xp.err)) {
-            ok_all = false;
-            break;
-        }
-        const int t = blockIdx.x + i * gridDim.x;
-        const int j = t / nt, i0 = (t % nt) * XT_TR;
-        const int rows = min(XT_TR, p.out_rows - i0);
-        const int e = p.ids[j];
-        const bool ev = e >= 0 && e < p.E;
-        const unsigned char* st = ring + (size_t)s * xp.stage;
-        if (wid < rows) {
-            const int r = wid;
-            const int8_t* gq = reinterpret_cast<const int8_t*>(st) + (size_t)r * k;
-            const int8_t* uq = reinterpret_cast<const int8_t*>(st + qrows) + (size_t)r * k;
-            const float* gs = reinterpret_cast<const float*>(st + 2 * qrows) + (size_t)r * nb;
-            const float* us = reinterpret_cast<const float*>(st + 2 * qrows + srows) + (size_t)r * nb;
-            T gv = group_sum<32>(smem_row_dot<MODE, KCH>(gq, gs, k, x, lane));
-            T uv = group_sum<32>(smem_row_dot<MODE, KCH>(uq, us, k, x, lane));
-            if (!ev) gv = uv = 0;  // an id outside [0, E) counts as an expert of zero weights
-            if (lane == 0) p.h[(int64_t)j * p.out_rows + i0 + r] = silu_f32((float)gv) * (float)uv;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-    }
-    if (!ok_all)
-        for (int i = 0; i < nmine && i < xp.ns; ++i) mbar_wait(&full[i], 0, nullptr);
-}
-
-// Down-and-combine: tile = output rows o0 .. o0+4 of every kept expert (expert j's rows, then the scale rows).  The
-// routing was written two launches back, so the producer fills its first stages before waiting for earlier kernels;
-// the consumers stage the hidden rows (quantized in the int8 mode) after waiting.  Warp w < 4 forms row o0 + w:
-// y = residual + sum_j g_j * (Wd[e_j] row . h_j), j in choice order.
-template <int MODE, int KCH>
-__global__ void __launch_bounds__(XT_THREADS, 1) down_tma_kernel(const XtParams xp) {
-    using T = typename AccType<MODE>::T;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const ExpertParams& p = xp.e;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + 8;
-    const int K = p.K, kk = p.k, nb = p.nb;
-    // hidden rows: f32 [K][kk], words [K][kk], scales [K][nb]
-    float* hf = reinterpret_cast<float*>(smem + 128);
-    int8_t* hq = reinterpret_cast<int8_t*>(smem + 128 + (size_t)K * kk * 4);
-    float* hs = reinterpret_cast<float*>(smem + 128 + (size_t)K * kk * 5);
-    const size_t hbytes = ((size_t)K * kk * 5 + (size_t)K * nb * 4 + 127) / 128 * 128;
-    unsigned char* ring = smem + 128 + hbytes;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int nmine = xp.tiles > (int)blockIdx.x ? (xp.tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < xp.ns; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], XT_CONSUMERS);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-    issue_l2_prefetch(p.pf);
-    const size_t qrows = (size_t)DN_TR * kk, srows = (size_t)DN_TR * nb * 4;
-    if (wid == XT_CONSUMERS) {
-        if (lane == 0) {
-            for (int i = 0; i < nmine; ++i) {
-                const int s = i % xp.ns;
-                if (i >= xp.ns && !mbar_wait(&empty[s], ((i / xp.ns) - 1) & 1, xp.err)) break;
-                const int o0 = (blockIdx.x + i * gridDim.x) * DN_TR;
-                const int rows = min(DN_TR, p.out_rows - o0);
-                unsigned char* st = ring + (size_t)s * xp.stage;
-                const unsigned qb = (unsigned)rows * (unsigned)kk, sb = (unsigned)rows * (unsigned)nb * 4u;
-                mbar_arrive_expect_tx(&full[s], (unsigned)K * (qb + sb));
-                for (int j = 0; j < K; ++j) {
-                    const int e = p.ids[j];
-                    const int64_t row0 = (int64_t)((e >= 0 && e < p.E) ? e : 0) * p.out_rows + o0;
-                    bulk_g2s(st + (size_t)j * qrows, p.q0 + row0 * kk, qb, &full[s]);
-                    bulk_g2s(st + (size_t)K * qrows + (size_t)j * srows, p.s0 + row0 * nb, sb, &full[s]);
-                }
-            }
-        }
-        return;
-    }
-    griddep_wait();  // the hidden rows come from the previous launch
-    griddep_launch();
-    const int ct = threadIdx.x;  // consumer thread 0 .. 255
-    for (int i = ct; i < K * kk / 4; i += XT_CONSUMERS * 32)
-        reinterpret_cast<float4*>(hf)[i] = __ldcg(reinterpret_cast<const float4*>(p.x) + i);
-    asm volatile("bar.sync 1, %0;" ::"n"(XT_CONSUMERS * 32));
-    if (MODE == 1) {
-        for (int b = wid; b < K * kk / 32; b += XT_CONSUMERS) {
-            float dsc;
-            const int8_t v = quantize_lane(hf[b * 32 + lane], dsc);
-            hq[b * 32 + lane] = v;
-            if (lane == 0) hs[b] = dsc;
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(XT_CONSUMERS * 32));
-    }
-    bool ok_all = true;
-    for (int i = 0; i < nmine; ++i) {
-        const int s = i % xp.ns;
-        if (!mbar_wait(&full[s], (i / xp.ns) & 1, xp.err)) {
-            ok_all = false;
-            break;
-        }
-        const int o0 = (blockIdx.x + i * gridDim.x) * DN_TR;
-        const int rows = min(DN_TR, p.out_rows - o0);
-        const unsigned char* st = ring + (size_t)s * xp.stage;
-        if (wid < rows) {
-            const int r = wid;
-            T acc = 0;
-            for (int j = 0; j < K; ++j) {
-                XHalf<MODE, KCH> x;
-                load_xhalf<MODE, KCH>(x, hf + (size_t)j * kk, hq + (size_t)j * kk, hs + (size_t)j * nb, kk, lane);
-                const int8_t* q = reinterpret_cast<const int8_t*>(st + (size_t)j * qrows) + (size_t)r * kk;
-                const float* sc = reinterpret_cast<const float*>(st + (size_t)K * qrows + (size_t)j * srows) + (size_t)r * nb;
-                T ej = group_sum<32>(smem_row_dot<MODE, KCH>(q, sc, kk, x, lane));
-                const int e = p.ids[j];
-                if (!(e >= 0 && e < p.E)) ej = 0;
-                if (lane == 0) {
-                    if (p.expert_out) p.expert_out[(int64_t)j * p.out_rows + o0 + r] = (float)ej;
-                    const float gj = p.gates[j];
-                    acc = (MODE == 0) ? (T)fma((double)gj, (double)ej, (double)acc) : (T)fmaf(gj, (float)ej, (float)acc);
-                }
-            }
-            if (lane == 0) {
-                float v = (float)acc;
-                if (p.residual) v = p.residual[o0 + r] + v;
-                p.y[o0 + r] = v;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-    }
-    if (!ok_all)
-        for (int i = 0; i < nmine && i < xp.ns; ++i) mbar_wait(&full[i], 0, nullptr);
-}
-
 // Down over a chunk: item (group a, row tile) — expert e's tile is loaded once and multiplied by every choice routed
 // to it; each choice's unweighted output goes to scratch for the combine.
 template <int MODE, int LPR, int BPL, int RT>
@@ -815,71 +613,24 @@ void gate_up_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
 }
 
 void down_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
-    const bool one = c.R == 1 && !c.plan.active && c.K <= 32 && down_one_smem(c) <= (size_t)DOWN_SMEM_MAX;
+    const bool one = down_row_supported(c) ||
+                     (c.R == 1 && !c.plan.active && c.K <= 32 && down_one_smem(c) <= (size_t)DOWN_SMEM_MAX);
     *bytes = one ? 0 : (size_t)c.R * c.K * c.out_rows * (c.mode == 0 ? 8 : 4);
     *counters = 0;
 }
 
-bool xt_eligible(const ExpertCall& c) {
-    const bool mats = (uintptr_t)c.q0 % 16 == 0 && (uintptr_t)c.s0 % 16 == 0 &&
-                      (!c.q1 || ((uintptr_t)c.q1 % 16 == 0 && (uintptr_t)c.s1 % 16 == 0));
-    return c.R == 1 && !c.plan.active && c.k % 128 == 0 && c.k <= 4096 && c.K <= 32 && mats;
-}
-
-template <typename Kern>
-cudaError_t run_xt(Kern kern, const XtParams& xp, size_t smem, cudaStream_t st, int pdl) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    const int grid = xp.tiles < device_info().sms ? xp.tiles : device_info().sms;
-    return launch(kern, dim3(grid), dim3(XT_THREADS), smem, st, pdl, xp);
-}
-
 cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
-    if (xt_eligible(c)) {
-        XtParams xp = {};
-        EPlan pl{32, 1, 1};
-        xp.e = make_params(c, pl);
-        xp.err = c.err ? c.err : (ws.counters ? ws.counters + ws.n_counters - 1 : nullptr);
-        xp.stage = (int)((2 * ((size_t)XT_TR * c.k + (size_t)XT_TR * (c.k / 32) * 4) + 127) / 128 * 128);
-        xp.ns = (XT_SMEM - 128) / xp.stage;
-        if (xp.ns > 8) xp.ns = 8;
-        xp.tiles = c.K * (int)((c.out_rows + XT_TR - 1) / XT_TR);
-        if (xp.ns >= 2) {
-            const size_t smem = 128 + (size_t)xp.ns * xp.stage;
-            const int kch = (int)((c.k + 511) / 512);
-#define Q8_GU(MODE, KCH) if (c.mode == MODE && kch <= KCH) return run_xt(gate_up_tma_kernel<MODE, KCH>, xp, smem, st, c.pdl);
-            Q8_GU(0, 2) Q8_GU(0, 4) Q8_GU(0, 8) Q8_GU(1, 2) Q8_GU(1, 4) Q8_GU(1, 8)
-#undef Q8_GU
-        }
-    }
     // gate and up tiles are both in flight: about four (f32) or eight (int8) 32-byte loads per lane in all
     const EPlan pl = eplan(c.mode, (int)(c.k / 32), c.mode == 0 ? 2 : 4);
     ExpertParams p = make_params(c, pl);
+    (void)ws;
     const int64_t warps = (int64_t)max_groups(c) * p.nrs;
     return c.mode == 0 ? run_gate_up<0>(c, pl, p, warps, st) : run_gate_up<1>(c, pl, p, warps, st);
 }
 
 cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     const int nb = (int)(c.k / 32);
-    if (xt_eligible(c) && (c.x || c.mode == 1) && (c.mode == 0 || c.x)) {
-        XtParams xp = {};
-        EPlan pl{32, 1, 1};
-        xp.e = make_params(c, pl);
-        xp.err = c.err ? c.err : (ws.counters ? ws.counters + ws.n_counters - 1 : nullptr);
-        const size_t hbytes = ((size_t)c.K * c.k * 5 + (size_t)c.K * nb * 4 + 127) / 128 * 128;
-        xp.stage = (int)(((size_t)c.K * ((size_t)DN_TR * c.k + (size_t)DN_TR * nb * 4) + 127) / 128 * 128);
-        const int room = XT_SMEM - 128 - (int)hbytes;
-        xp.ns = room > 0 ? room / xp.stage : 0;
-        if (xp.ns > 8) xp.ns = 8;
-        xp.tiles = (int)((c.out_rows + DN_TR - 1) / DN_TR);
-        if (xp.ns >= 2) {
-            const size_t smem = 128 + hbytes + (size_t)xp.ns * xp.stage;
-            const int kch = (int)((c.k + 511) / 512);
-#define Q8_DN(MODE, KCH) if (c.mode == MODE && kch <= KCH) return run_xt(down_tma_kernel<MODE, KCH>, xp, smem, st, c.pdl);
-            Q8_DN(0, 2) Q8_DN(0, 4) Q8_DN(0, 8) Q8_DN(1, 2) Q8_DN(1, 4) Q8_DN(1, 8)
-#undef Q8_DN
-        }
-    }
+    if (down_row_supported(c)) return launch_down_row(c, st);
     if (c.R == 1 && !c.plan.active && c.K <= 32 && down_one_smem(c) <= (size_t)DOWN_SMEM_MAX) {
         // one token: a warp per output row, its lane groups over the kept experts
         EPlan pl = eplan(c.mode, nb, 4);

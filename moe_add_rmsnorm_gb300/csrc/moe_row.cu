@@ -1,0 +1,369 @@
+// The mixture for one token row, as a decode step runs it: the router projection and its top-k in one cluster
+// kernel, and the down-and-combine with every weight row requested before waiting for the kernel that writes the
+// hidden rows.
+//
+// What it computes: forward_shim.rs module docs (a sparse mixture as a top-k router, a gate-up kernel and a
+// down-and-combine kernel, its Q8_0 matrices dequantized inside the kernels that read them) and kernel_refusal (Moe
+// arms: a softmax router whose kept weights are renormalized, SwiGLU experts, no biases); qwen_emit docs,
+// emit_moe_forward (router product, softmax top-K renormalized, weighted combine of the kept experts) and MoeWeights
+// (stacked experts: down [E*d, dff] with expert e at row e*d).
+//
+// How (GB300 design): at batch 1 these launches are latency-bound, so the work is arranged around the dependency wait
+// of programmatic dependent launch.  The router rows do not depend on earlier kernels and are loaded before the wait;
+// one cluster of 8 CTAs forms all logits, gathers them in CTA 0 through distributed shared memory and ranks them
+// there (each expert counts the experts ahead of it), which replaces a second launch and K rounds of warp arg-max.
+// The down-and-combine reads the routing written two launches back, so a warp requests its output row's K*dff/32
+// weight blocks (one 256-bit load each) before the wait and only the hidden rows after it.
+#include <float.h>
+
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace cg = cooperative_groups;
+
+namespace q8 {
+namespace {
+
+// ==== router projection + top-k ===================================================================================
+
+constexpr int RR_CL = 8;         // CTAs in the cluster
+constexpr int RR_THREADS = 256;
+constexpr int RR_WARPS = RR_THREADS / 32;
+constexpr int RR_MAXE = 1024;    // experts one cluster ranks
+constexpr int RR_RW = 2;         // router rows per warp loaded before the wait
+
+struct RouteRowParams {
+    const int8_t* q;
+    const float* s;
+    int E, d, nb, K;
+    const float* x;
+    const int8_t* xq;
+    const float* xs;
+    float* logits;
+    int32_t* ids;
+    float* gates;
+    L2Prefetch pf;
+};
+
+// Ranking key: a NaN logit ranks below every number (and ties with -inf, broken by index).
+__device__ __forceinline__ float rank_key(float v) { return v != v ? -INFINITY : v; }
+
+// CTA c of the cluster owns router rows [c*rpc, (c+1)*rpc); warp w the rows w, w+8, ... of that slice; lane l the
+// 32-value blocks l, l+32, ... of a row (the projection's own lane layout, so the logits equal the projection's).
+template <int MODE, int BPL>
+__global__ void __launch_bounds__(RR_THREADS) route_row_kernel(const RouteRowParams p) {
+    __shared__ float own[RR_MAXE / RR_CL];
+    __shared__ float all[RR_MAXE];
+    __shared__ float key[RR_MAXE];
+    __shared__ int kid[32];
+    __shared__ float kv[32];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int rpc = (p.E + RR_CL - 1) / RR_CL;
+    const int r0 = rank * rpc;
+    int bidx[BPL];
+    bool bval[BPL];
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+        bidx[j] = lane + 32 * j;
+        bval[j] = bidx[j] < p.nb;
+    }
+    issue_l2_prefetch(p.pf);
+    WTile<BPL, 1> t[RR_RW];
+#pragma unroll
+    for (int u = 0; u < RR_RW; ++u) {
+        const int lr = wid + RR_WARPS * u;
+        const bool v = lr < rpc && r0 + lr < p.E;
+        load_tile<BPL, 1>(t[u], p.q, p.s, v ? r0 + lr : 0, v ? 1 : 0, p.d, p.nb, bidx, bval);
+    }
+    griddep_wait();  // the activation comes from the previous launch
+    griddep_launch();
+    XTile<MODE, BPL> x;
+    load_x<MODE, BPL>(x, p.x, p.xq, p.xs, bidx, bval);
+#pragma unroll
+    for (int u = 0; u < RR_RW; ++u) {
+        const int lr = wid + RR_WARPS * u;
+        const float v = (float)group_sum<32>(tile_row_dot<MODE, BPL, 1>(t[u], 0, x));
+        if (lane == 0 && lr < rpc && r0 + lr < p.E) {
+            own[lr] = v;
+            if (p.logits) p.logits[r0 + lr] = v;
+        }
+    }
+    for (int lr = wid + RR_WARPS * RR_RW; lr < rpc && r0 + lr < p.E; lr += RR_WARPS) {  // past the preloaded rows
+        WTile<BPL, 1> w;
+        load_tile<BPL, 1>(w, p.q, p.s, r0 + lr, 1, p.d, p.nb, bidx, bval);
+        const float v = (float)group_sum<32>(tile_row_dot<MODE, BPL, 1>(w, 0, x));
+        if (lane == 0) {
+            own[lr] = v;
+            if (p.logits) p.logits[r0 + lr] = v;
+        }
+    }
+    cluster.sync();  // every CTA's logits are in its shared memory
+    if (rank == 0)
+        for (int e = threadIdx.x; e < p.E; e += RR_THREADS) {
+            const float v = cluster.map_shared_rank(own, e / rpc)[e % rpc];
+            all[e] = v;
+            key[e] = rank_key(v);
+        }
+    cluster.sync();  // CTA 0 has read every slice: the others may leave
+    if (rank != 0) return;
+    // expert e's place among the kept = the number of experts with a larger key, or an equal key and a lower index
+    for (int e = threadIdx.x; e < p.E; e += RR_THREADS) {
+        const float ke = key[e];
+        int r = 0;
+#pragma unroll 8
+        for (int f = 0; f < p.E; ++f) {
+            const float kf = key[f];
+            r += (kf > ke) || (kf == ke && f < e);
+        }
+        if (r < p.K) {
+            kid[r] = e;
+            kv[r] = all[e];
+        }
+    }
+    __syncthreads();
+    if (wid == 0) {
+        // gates: softmax over all experts renormalized over the kept ones = softmax over the kept logits
+        const float kept = lane < p.K ? kv[lane] : 0.f;
+        const float m = kv[0];
+        const float pe = lane < p.K ? expf(kept - m) : 0.f;
+        const float z = group_sum<32>(pe);
+        if (lane < p.K) {
+            p.ids[lane] = kid[lane];
+            p.gates[lane] = __fdiv_rn(pe, z);
+        }
+    }
+}
+
+template <int MODE, int BPL>
+cudaError_t run_route_row(const RouteRowParams& p, cudaStream_t st, int pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(RR_CL);
+    cfg.blockDim = dim3(RR_THREADS);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = RR_CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int na = 1;
+    if (pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        na = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, route_row_kernel<MODE, BPL>, p);
+}
+
+// ==== down-and-combine ==============================================================================================
+
+constexpr int DR_MAXW = 16;  // warps per CTA at most
+constexpr int DR_MAXP = 8;   // (expert, block) pairs per lane at most: K * dff/32 <= 256
+
+struct DownRowParams {
+    const int8_t* q;  // down [E*rows][k]
+    const float* s;
+    int E, rows, k, nb, K;
+    const int32_t* ids;
+    const float* gates;
+    const float* h;    // the K hidden rows [K][k], f32
+    const int8_t* hq;  // int8 mode: their words [K][k] and scales [K][nb]; when null the CTA quantizes h itself
+    const float* hs;
+    const float* residual;
+    float* y;
+    L2Prefetch pf;
+};
+
+// Warp o owns output row o: y[o] = residual[o] + sum_j g_j * (Wd[e_j] row o . h_j).  The row's K*nb (expert, block)
+// pairs are dealt to the lanes, pair p = lane + 32 i being block p % nb of kept expert p / nb; the lanes add
+// g_j * (block product) for their pairs (f64 in the f32 mode) and the warp sums them.
+template <int MODE, int PPL>
+__global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRowParams p) {
+    extern __shared__ __align__(16) float hsm[];  // f32 mode: the hidden rows
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int o = blockIdx.x * (blockDim.x >> 5) + wid;
+    const bool orow = o < p.rows;
+    const int P = p.K * p.nb;
+    uint32_t w[PPL][8];
+    float sw[PPL], g[PPL];
+    int xo[PPL];  // the pair's first value in the hidden rows: j*k + 32*b
+    issue_l2_prefetch(p.pf);
+    // the routing was written two launches back, before the previous kernel passed its own wait
+#pragma unroll
+    for (int i = 0; i < PPL; ++i) {
+        const int pi = lane + 32 * i;
+        const bool in = orow && pi < P;
+        const int j = in ? pi / p.nb : 0;
+        const int b = in ? pi - j * p.nb : 0;
+        const int e = in ? __ldg(p.ids + j) : -1;
+        xo[i] = j * p.k + 32 * b;
+        g[i] = in ? __ldg(p.gates + j) : 0.f;
+        if (e >= 0 && e < p.E) {  // an id outside [0, E) counts as an expert of zero weights
+            const int64_t row = (int64_t)e * p.rows + o;
+            ld_block_stream(p.q + row * p.k + 32 * b, w[i]);
+            sw[i] = ld_scale_stream(p.s + row * p.nb + b);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) w[i][c] = 0u;
+            sw[i] = 0.f;
+        }
+    }
+    griddep_wait();  // the hidden rows come from the previous launch
+    griddep_launch();
+    const int8_t* hq = p.hq;
+    const float* hs = p.hs;
+    if (MODE == 0) {
+        for (int i = threadIdx.x; i < p.K * p.k / 4; i += blockDim.x)
+            reinterpret_cast<float4*>(hsm)[i] = __ldcg(reinterpret_cast<const float4*>(p.h) + i);
+        __syncthreads();
+    } else if (!hq) {
+        // the CTA quantizes the f32 hidden rows into shared memory: warp w takes blocks w, w + W, ..., four at a time
+        // (all four blocks' values loaded before any is quantized)
+        int8_t* sq = reinterpret_cast<int8_t*>(hsm);
+        float* ss = hsm + P * 8;  // after the P * 32 words
+        const int W = blockDim.x >> 5;
+        for (int b0 = wid; b0 < P; b0 += 4 * W) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * W;
+                v[u] = b < P ? __ldcg(p.h + (int64_t)b * 32 + lane) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * W;
+                float dsc;
+                const int8_t qv = quantize_lane(v[u], dsc);
+                if (b < P) {
+                    sq[b * 32 + lane] = qv;
+                    if (lane == 0) ss[b] = dsc;
+                }
+            }
+        }
+        __syncthreads();
+        hq = sq;
+        hs = ss;
+    }
+    typename AccType<MODE>::T acc = 0;
+#pragma unroll
+    for (int i = 0; i < PPL; ++i) {
+        const bool in = orow && lane + 32 * i < P;
+        if (MODE == 1) {
+            uint32_t xw[8];
+            float xs = 0.f;
+            if (in) {  // global (written by the previous launch) or this CTA's shared memory
+                const uint4 a = reinterpret_cast<const uint4*>(hq + xo[i])[0];
+                const uint4 b = reinterpret_cast<const uint4*>(hq + xo[i])[1];
+                xw[0] = a.x; xw[1] = a.y; xw[2] = a.z; xw[3] = a.w;
+                xw[4] = b.x; xw[5] = b.y; xw[6] = b.z; xw[7] = b.w;
+                xs = hs[xo[i] / 32];
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) xw[c] = 0u;
+            }
+            const int D = block_dot_i8(w[i], xw);
+            acc = fmaf(g[i] * (sw[i] * xs), (float)D, (float)acc);
+        } else {
+            float xf[32];
+            const float4* src = reinterpret_cast<const float4*>(hsm + xo[i]);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 v = src[c];
+                xf[4 * c] = v.x;
+                xf[4 * c + 1] = v.y;
+                xf[4 * c + 2] = v.z;
+                xf[4 * c + 3] = v.w;
+            }
+            const float ps = block_dot_f32(w[i], xf);
+            acc = fma((double)g[i] * (double)sw[i], (double)ps, (double)acc);
+        }
+    }
+    acc = group_sum<32>(acc);
+    if (lane == 0 && orow) {
+        float v = (float)acc;
+        if (p.residual) v = p.residual[o] + v;
+        p.y[o] = v;
+    }
+}
+
+template <int MODE, int PPL>
+cudaError_t run_down_row(const DownRowParams& p, int wpc, cudaStream_t st, int pdl) {
+    auto kern = down_row_kernel<MODE, PPL>;
+    const size_t smem = MODE == 0 ? (size_t)p.K * p.k * sizeof(float) : p.hq ? 0 : (size_t)p.K * p.k * 5 / 4 + 16;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    const int grid = (p.rows + wpc - 1) / wpc;
+    return launch(kern, dim3(grid), dim3(wpc * 32), smem, st, pdl, p);
+}
+
+template <int MODE>
+cudaError_t dispatch_down_row(const DownRowParams& p, int ppl, int wpc, cudaStream_t st, int pdl) {
+    switch (ppl) {
+        case 1: return run_down_row<MODE, 1>(p, wpc, st, pdl);
+        case 2: return run_down_row<MODE, 2>(p, wpc, st, pdl);
+        case 3: return run_down_row<MODE, 3>(p, wpc, st, pdl);
+        case 4: return run_down_row<MODE, 4>(p, wpc, st, pdl);
+        case 5: return run_down_row<MODE, 5>(p, wpc, st, pdl);
+        case 6: return run_down_row<MODE, 6>(p, wpc, st, pdl);
+        case 7: return run_down_row<MODE, 7>(p, wpc, st, pdl);
+        case 8: return run_down_row<MODE, 8>(p, wpc, st, pdl);
+    }
+    return cudaErrorInvalidConfiguration;
+}
+
+int route_bpl(int mode, int64_t d) {
+    const int64_t nb = d / 32;
+    const int bpl = nb <= 32 ? 1 : nb <= 64 ? 2 : nb <= 128 ? 4 : 0;
+    return (mode == 0 && bpl > 2) ? 0 : bpl;
+}
+
+}  // namespace
+
+bool route_row_supported(int mode, int64_t E, int64_t d, int K) {
+    return E >= 1 && E <= RR_MAXE && K >= 1 && K <= 32 && K <= E && d % 32 == 0 && route_bpl(mode, d) > 0;
+}
+
+cudaError_t launch_route_row(const RouteRowCall& c, cudaStream_t st) {
+    if (!route_row_supported(c.mode, c.E, c.d, c.K)) return cudaErrorInvalidConfiguration;
+    RouteRowParams p = {c.q, c.s, (int)c.E, (int)c.d, (int)(c.d / 32), c.K, c.x, c.xq, c.xs, c.logits, c.ids, c.gates,
+                        c.pf};
+    const int bpl = route_bpl(c.mode, c.d);
+    if (c.mode == 0) {
+        if (bpl == 1) return run_route_row<0, 1>(p, st, c.pdl);
+        if (bpl == 2) return run_route_row<0, 2>(p, st, c.pdl);
+    } else {
+        if (bpl == 1) return run_route_row<1, 1>(p, st, c.pdl);
+        if (bpl == 2) return run_route_row<1, 2>(p, st, c.pdl);
+        if (bpl == 4) return run_route_row<1, 4>(p, st, c.pdl);
+    }
+    return cudaErrorInvalidConfiguration;
+}
+
+bool down_row_supported(const ExpertCall& c) {
+    const bool act = c.mode == 0 ? (c.x != nullptr && (size_t)c.K * c.k * 4 <= 96 * 1024)
+                                 : (c.xq != nullptr || c.x != nullptr);
+    return c.R == 1 && !c.plan.active && !c.expert_out && act && c.k % 32 == 0 && c.K >= 1 &&
+           (int64_t)c.K * (c.k / 32) <= 32 * DR_MAXP;
+}
+
+cudaError_t launch_down_row(const ExpertCall& c, cudaStream_t st) {
+    if (!down_row_supported(c)) return cudaErrorInvalidConfiguration;
+    DownRowParams p = {c.q0, c.s0, (int)c.E, (int)c.out_rows, (int)c.k, (int)(c.k / 32), c.K, c.ids, c.gates,
+                       c.x, c.xq, c.xs, c.residual, c.y, c.pf};
+    const int ppl = (int)((c.K * (c.k / 32) + 31) / 32);
+    // one output row per warp, the rows spread over every SM
+    const int sms = device_info().sms;
+    int wpc = (int)((c.out_rows + sms - 1) / sms);
+    if (wpc < 4) wpc = 4;
+    if (wpc > DR_MAXW) wpc = DR_MAXW;
+    return c.mode == 0 ? dispatch_down_row<0>(p, ppl, wpc, st, c.pdl) : dispatch_down_row<1>(p, ppl, wpc, st, c.pdl);
+}
+
+}  // namespace q8

@@ -246,7 +246,7 @@ def test_route_topk(q8, ws, mode, R, router_scale):
     np.testing.assert_array_equal(act[1:1 + len(active)], active)
 
 
-def _run_moe_gpu(q8, ws, md, mode, x, K, residual=None, expert_out=True):
+def _run_moe_gpu(q8, ws, md, mode, x, K, residual=None, expert_out=True, route_plan=True):
     import torch
     R, d = x.shape
     dff = md["gate"][0].shape[0] // md["router"][0].shape[0]
@@ -267,13 +267,14 @@ def _run_moe_gpu(q8, ws, md, mode, x, K, residual=None, expert_out=True):
         oq, os_ = oracle.quantize(x)
         xq, xs = dev(oq), dev(os_)
     q8.moe_route_topk(*md["router"], mode, K, ids, gates, x=tx, xq=xq, xs=xs, rows=R, logits=logits,
-                      plan=q8.plan_struct(*pt), ws=ws)
+                      plan=q8.plan_struct(*pt) if route_plan else None, ws=ws)
     q8.moe_gate_up(*md["gate"], *md["up"], dff, mode, K, ids, h, x=tx, xq=xq, xs=xs, hq=hq, hs=hs, rows=R, plan=plan,
                    ws=ws)
     q8.moe_down_combine(*md["down"], d, mode, K, ids, gates, y, h=h, hq=hq, hs=hs, rows=R, plan=plan,
                         residual=dev(residual) if residual is not None else None, expert_out=eo, ws=ws)
     return dict(ids=host(ids), gates=host(gates), logits=host(logits), h=host(h).reshape(R, K, dff),
-                y=host(y), expert_out=host(eo) if expert_out else None, hq=host(hq) if hq is not None else None)
+                y=host(y), expert_out=host(eo) if expert_out else None, hq=host(hq) if hq is not None else None,
+                hs=host(hs) if hs is not None else None)
 
 
 def _compare_moe(out, ref, mode, K):
@@ -285,8 +286,14 @@ def _compare_moe(out, ref, mode, K):
         assert rel_err(out["gates"][r], ref["gates"][r]) < TOL[mode]
         for j in range(K):  # each expert separately: the gates are nearly one-hot at these router scales
             assert rel_err(out["h"][r, j], ref["hidden"][r, j]) < TOL[mode]
-            assert rel_err(out["expert_out"][r, j], ref["expert_out"][r, j]) < TOL[mode]
+            if out["expert_out"] is not None:
+                assert rel_err(out["expert_out"][r, j], ref["expert_out"][r, j]) < TOL[mode]
         assert rel_err(out["y"][r], ref["y"][r]) < TOL[mode]
+    if out["hq"] is not None:  # gate-up's int8 epilogue = the quantizer applied to its own f32 rows, bit for bit
+        h = out["h"].reshape(-1, out["h"].shape[-1])
+        oq, os_ = oracle.quantize(h)
+        np.testing.assert_array_equal(out["hq"], oq)
+        np.testing.assert_array_equal(out["hs"].reshape(os_.shape), os_)
 
 
 @pytest.mark.parametrize("mode", [0, 1])
@@ -297,6 +304,55 @@ def test_moe_block_batch1(q8, ws, moe_host, moe_dev, mode):
     ref = oracle.moe_rows(mode, w, x, residual=res)
     out = _run_moe_gpu(q8, ws, moe_dev, mode, x, 8, residual=res)
     _compare_moe(out, ref, mode, 8)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("spread", [False, True])
+def test_moe_one_row_fused_path(q8, ws, moe_host, moe_dev, mode, spread):
+    # one row, no plan, no per-expert outputs: the router and its top-k in one cluster launch, gate-up quantizing its
+    # own rows, and the down-and-combine that loads its weights before waiting
+    mh, md = moe_host, moe_dev
+    if spread:
+        mh = dict(moe_host)
+        mh["router"] = synth.q8_matrix(128, 2048, 0, recipes.layer_ids(0)["router"], scale_mul=1e-5)
+        md = dict(moe_dev)
+        md["router"] = (dev(mh["router"][0]), dev(mh["router"][1]))
+    for seed in range(3):
+        x = synth.normal((1, 2048), seed, recipes.VEC + 74)
+        res = synth.normal((1, 2048), seed, recipes.VEC + 75)
+        ref = oracle.moe_rows(mode, oracle.MoeWeights(2048, 768, 128, 8, **mh), x, residual=res)
+        out = _run_moe_gpu(q8, ws, md, mode, x, 8, residual=res, expert_out=False, route_plan=False)
+        assert rel_err(out["logits"][0], ref["logits"][0]) < TOL[mode]
+        _compare_moe(out, ref, mode, 8)
+        assert abs(out["gates"][0].sum() - 1.0) < 1e-5
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("E,K,d", [(4, 4, 64), (16, 3, 1024), (64, 32, 2048), (1000, 8, 4096), (1024, 1, 32)])
+def test_route_one_row_shapes(q8, ws, mode, E, K, d):
+    # the one-cluster router: experts not a multiple of the cluster, K = E, K = 32, the widest rows, one block
+    import torch
+    if mode == 0 and d > 2048:
+        pytest.skip("the f32 one-row router holds at most 2048 values a row; wider rows take the two-launch path")
+    rq, rs = synth.q8_matrix(E, d, 5, 95)
+    x = synth.normal((1, d), 5, recipes.VEC + 96)
+    ids = empty((1, K), torch.int32)
+    gates = empty((1, K), torch.float32)
+    logits = empty((1, E), torch.float32)
+    if mode == 0:
+        q8.moe_route_topk(dev(rq), dev(rs), 0, K, ids, gates, x=dev(x), rows=1, logits=logits, ws=ws)
+    else:
+        xq, xs = oracle.quantize(x)
+        q8.moe_route_topk(dev(rq), dev(rs), 1, K, ids, gates, xq=dev(xq), xs=dev(xs), rows=1, logits=logits, ws=ws)
+    l = oracle.gemv(mode, rq, rs, x[0])
+    gl = host(logits)[0]
+    assert rel_err(gl, l) < TOL[mode]
+    # ids: the top K of the GPU's own logits, descending, ties to the lower index
+    order = sorted(range(E), key=lambda e: (-gl[e], e))[:K]
+    np.testing.assert_array_equal(host(ids)[0], order)
+    kept = gl[order].astype(np.float64)
+    g = np.exp(kept - kept.max())
+    np.testing.assert_allclose(host(gates)[0], g / g.sum(), rtol=1e-5, atol=1e-7)
 
 
 @pytest.mark.parametrize("mode", [0, 1])
