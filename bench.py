@@ -32,6 +32,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="only the warm-up and timed decode steps (for profiler launch lists); prints tokens/s")
     return ap.parse_args()
 
 
@@ -287,6 +289,12 @@ def main():
     model.check(sh)
     value = world * args.steps / sec
     ms_per_step = sec / args.steps * 1e3
+    if args.decode_only:
+        if rank == 0:
+            print(json.dumps({"decode_only": True, "tokens_per_s": value, "ms_per_step": ms_per_step,
+                              "launches_per_step": model.launches_per_step(), "layers": cfg["layers"]}), flush=True)
+        model.close()
+        return
 
     # end to end: each token's inputs (token, position) copied from pinned host memory, the next token read back
     pin_in = torch.zeros(2, dtype=torch.int32).pin_memory()
@@ -329,7 +337,7 @@ def main():
         "weight_stream": {"gbs": weight_gbs, "frac_of_peak": weight_gbs / peak, "bytes_per_token": wbytes,
                           "peak_gbs": peak, "peak_kind": peak_kind},
         "hbm_total_gbs": total_gbs,
-        "gpu_launches": model_launches(cfg) * args.steps,
+        "gpu_launches": model.launches_per_step() * args.steps,
         "clocks": clk,
         "e2e": e2e,
     }
@@ -367,12 +375,6 @@ def main():
     model.close()
     if world > 1:
         torch.distributed.destroy_process_group()
-
-
-def model_launches(cfg):
-    """Kernels one decode step launches: 10 per layer (norm, q/k/v, QK-norm+RoPE+KV, attention, O projection, norm,
-    router, top-k, gate-up, down-combine) plus the final norm, the LM head and the arg-max."""
-    return cfg["layers"] * 10 + 3
 
 
 if __name__ == "__main__":

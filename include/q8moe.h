@@ -191,7 +191,7 @@ typedef struct {
     const q8_mat *wq, *wk, *wv, *wo;           /* [layers]: [heads*hd, d], [kv*hd, d], [kv*hd, d], [d, heads*hd] */
     const q8_mat *router, *gate, *up, *down;   /* [layers]: [E, d], [E*dff, d], [E*dff, d], [E*d, dff] */
     q8_mat lm_head;                            /* [vocab, d] */
-    float *const *k_cache, *const *v_cache;    /* [layers] -> device f32 [kv_heads][ctx][head_dim] */
+    float *const *k_cache, *const *v_cache;    /* [layers] -> device f32 [kv_heads][ctx][head_dim], 32-byte aligned */
     int32_t *tok;               /* device int32 [1]: the token the step reads; the step writes the next token here */
     int32_t *pos;               /* device int32 [1]: the position the step writes; the step adds 1 */
     float *logits;              /* device f32 [vocab] or NULL */
@@ -213,6 +213,8 @@ Q8_API void q8_model_destroy(q8_model *model);
 Q8_API int decode_step(q8_model *model, q8_stream stream);
 /* The same step as plain launches, without a graph (for tests and graph-capture by the caller). */
 Q8_API int decode_step_launches(q8_model *model, q8_stream stream);
+/* Kernels one step launches: the kernel nodes of the graph the first decode_step captured (0 before it). */
+Q8_API int64_t q8_model_launches_per_step(const q8_model *model);
 /* Reads and clears the model's device error word (synchronizes `stream`): Q8_OK, or Q8_EINVAL when a step met an
  * out-of-range position or token. */
 Q8_API int q8_model_check(q8_model *model, q8_stream stream);

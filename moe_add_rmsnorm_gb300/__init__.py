@@ -76,6 +76,7 @@ _SIGS = {
     "decode_step": [_vp, _vp],
     "decode_step_launches": [_vp, _vp],
     "q8_model_check": [_vp, _vp],
+    "q8_model_launches_per_step": [_vp],
     "q8_last_error": [],
 }
 for _name, _args in _SIGS.items():
@@ -86,6 +87,7 @@ lib.q8_workspace_destroy.restype = None
 lib.q8_model_destroy.restype = None
 lib.q8_workspace_bytes.restype = ctypes.c_size_t
 lib.q8_last_error.restype = ctypes.c_char_p
+lib.q8_model_launches_per_step.restype = ctypes.c_int64
 
 EXPORTS = tuple(_SIGS)
 
@@ -259,6 +261,10 @@ class Model:
 
     def check(self, stream=None):
         _check(lib.q8_model_check(self.handle, _stream(stream)))
+
+    def launches_per_step(self):
+        """Kernels one step launches (the captured graph's kernel nodes; 0 before the first step)."""
+        return int(lib.q8_model_launches_per_step(self.handle))
 
     def close(self):
         if self.handle:

@@ -357,9 +357,15 @@ int moe_gate_up(const q8_mat* gate, const q8_mat* up, int64_t dff, q8_mode mode,
         c.plan.lists = plan->lists;
         c.plan.active = plan->active;
     }
+    if (mode == Q8_INT8ACT && hq && gate_row_supported(c)) {  // one row: the kernel quantizes each 32-row block
+        c.hq_out = hq->q;
+        c.hs_out = hq->s;
+    }
     Carve cv = ws->carve();
     cudaError_t e = launch_gate_up(c, cv, st);
-    if (e == cudaSuccess && mode == Q8_INT8ACT && hq) e = launch_quantize(h, rows * k * dff, hq->q, hq->s, st);
+    if (cv.overflow) return fail(Q8_ENOSPACE, "moe_gate_up: workspace too small for the int8 epilogue's counters");
+    if (e == cudaSuccess && mode == Q8_INT8ACT && hq && !c.hq_out)
+        e = launch_quantize(h, rows * k * dff, hq->q, hq->s, st);
     return e == cudaSuccess ? Q8_OK : cuda_fail(e, "moe_gate_up");
 }
 

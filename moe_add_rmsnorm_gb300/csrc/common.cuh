@@ -21,6 +21,13 @@ __device__ __forceinline__ void ld_block_stream(const int8_t* p, uint32_t (&w)[8
                  : "l"(p));
 }
 
+// Eight consecutive floats (32 bytes, 32-byte aligned) in one 256-bit load, read once: not kept in L1.
+__device__ __forceinline__ void ld_f8_stream(const float* p, float* v) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+                 : "l"(p));
+}
+
 // A 32-byte block read through L1 (activations that several warps of the CTA share).
 __device__ __forceinline__ void ld_block_shared_use(const int8_t* p, uint32_t (&w)[8]) {
     asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -266,22 +273,102 @@ __device__ __forceinline__ int8_t quantize_lane(float v, float& d_out) {
     return (int8_t)(int)r;
 }
 
+// ---- pairs of f32 carrying about 44 significant bits ------------------------------------------------------------
+// FP64 issues at a small fraction of the f32 rate on this part, so the few quantities that want more than 24 bits
+// (a row's sum of squares, its norm factor, the product s * inv * w before its single rounding) are held as unevaluated
+// sums hi + lo of two floats: Knuth's two-sum and the FMA two-product are exact, Dekker's normalisation keeps
+// |lo| <= ulp(hi) / 2.
+struct F2 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ F2 f2_quick(float a, float b) {  // |a| >= |b|
+    const float s = a + b;
+    return F2{s, b - (s - a)};
+}
+
+__device__ __forceinline__ F2 f2_two_sum(float a, float b) {
+    const float s = a + b;
+    const float bb = s - a;
+    return F2{s, (a - (s - bb)) + (b - bb)};
+}
+
+__device__ __forceinline__ F2 f2_two_prod(float a, float b) {
+    const float p = a * b;
+    return F2{p, fmaf(a, b, -p)};
+}
+
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+    const F2 s = f2_two_sum(a.hi, b.hi);
+    return f2_quick(s.hi, s.lo + (a.lo + b.lo));
+}
+
+// 1 / sqrt(m) for m > 0 given as a pair: the f32 reciprocal root refined by one Newton step whose residual
+// 1 - m r^2 is formed with exact products (relative error of the pair about 2^-44).
+__device__ __forceinline__ F2 f2_rsqrt(F2 m) {
+    const float r = rsqrtf(m.hi);
+    const F2 r2 = f2_two_prod(r, r);
+    const F2 t = f2_two_prod(m.hi, r2.hi);
+    // 1 - m r^2 = (1 - t.hi) - t.lo - m.hi r2.lo - m.lo r2.hi; 1 - t.hi is exact (t.hi is within a few ulp of 1)
+    const float e = (((1.0f - t.hi) - t.lo) - m.hi * r2.lo) - m.lo * r2.hi;
+    return f2_quick(r, r * (0.5f * e));
+}
+
+// f32(a * b * inv) with one rounding: a * b is an exact pair, multiplied by the pair inv to about 2^-44.
+__device__ __forceinline__ float f2_mul3_round(float a, float b, F2 inv) {
+    const F2 p = f2_two_prod(a, b);
+    const F2 y = f2_two_prod(p.hi, inv.hi);
+    const float lo = y.lo + fmaf(p.hi, inv.lo, p.lo * inv.hi);
+    return y.hi + lo;
+}
+
+// N independent blocks at once (block i's value of this lane in v[i]): the same arithmetic as quantize_lane, with the N
+// warp reductions interleaved so their shuffles overlap.
+template <int N>
+__device__ __forceinline__ void quantize_lanes(const float (&v)[N], int8_t (&q)[N], float (&d)[N]) {
+    float m[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) m[i] = fabsf(v[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < N; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        d[i] = __fdiv_rn(m[i], 127.0f);
+        float r = d[i] == 0.0f ? 0.0f : roundf(__fdiv_rn(v[i], d[i]));
+        r = fminf(fmaxf(r, -127.0f), 127.0f);
+        q[i] = (int8_t)(int)r;
+    }
+}
+
 // ---- SiLU -------------------------------------------------------------------------------------------------------
 // silu(z) = z / (1 + e^-z): for z << 0, e^-z overflows to +inf and the quotient is -0, the correct limit.
 __device__ __forceinline__ float silu_f32(float z) { return __fdiv_rn(z, 1.0f + expf(-z)); }
 
 // ---- grid-level arrival -----------------------------------------------------------------------------------------
+// Release / acquire at GPU scope: orders this thread's earlier writes before its later ones as seen by other CTAs (and
+// its later reads after what those CTAs released), without the sequentially consistent fence's cost.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// atomicAdd with acquire-release semantics at GPU scope: releases what this thread (and, through a preceding barrier,
+// its CTA) wrote and acquires what earlier arrivals released, in one round trip.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Called by every lane of a warp after the lanes' partial results are stored.  Returns true in every lane of the one
 // warp that arrives last among `expected` arrivals on `counter`; that warp must reset the counter to 0 after reading
 // the others' partials (through L2: __ldcg).
 __device__ __forceinline__ bool warp_arrive_last(int* counter, int expected) {
-    __threadfence();
-    __syncwarp();
+    __syncwarp();  // orders the lanes' stores before lane 0's release (cumulative)
     int old = 0;
-    if ((threadIdx.x & 31) == 0) old = atomicAdd(counter, 1);
+    if ((threadIdx.x & 31) == 0) old = atomic_add_acq_rel_gpu(counter, 1);
     old = __shfl_sync(0xffffffffu, old, 0);
     const bool last = (old == expected - 1);
-    if (last) __threadfence();
+    __syncwarp();  // the other lanes read after lane 0's acquire
     return last;
 }
 
@@ -317,6 +404,11 @@ __device__ __forceinline__ void issue_l2_prefetch(const L2Prefetch& pf) {
         base += np;
     }
 }
+
+// A cluster barrier split in two: arrive (releasing this thread's writes) now, wait (acquiring the others') later.
+// Every thread of the CTA executes both, at warp-uniform points.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }

@@ -39,6 +39,7 @@ constexpr int ATT_MAXG = 8;     // query heads per key/value head
 constexpr int ATT_HD = 128;     // head width the kernel is built for
 constexpr int ATT_QP = 36;      // padded 32-dim quarter of a query row in shared memory: 16-byte reads, no conflicts
 constexpr int ATT_CLUSTER = 4;  // chunks per thread-block cluster
+constexpr int ATT_FOLD_B = 16;  // cluster partials a thread loads at once in the final fold
 
 struct AttnParams {
     const float* q;        // the projection's q, k and v rows, before QK-norm and RoPE
@@ -104,73 +105,72 @@ __device__ void fold_cluster(const AttnParams& p, int g, int chunk, int G, int t
             else out_part[ATT_HD] = M;
         }
     }
-    cluster.sync();  // no CTA leaves while another reads its shared memory
-    if (rank >= G) return;
-    __threadfence();
-    __syncthreads();
+    cluster_arrive();  // this CTA has read the others' partials; it waits for theirs only before it exits
+    if (rank >= G) {
+        cluster_wait();
+        return;
+    }
+    __syncthreads();  // the CTA's cluster results are written
     const int ncl_used = (((*p.pos + 1) + ATT_CHUNK - 1) / ATT_CHUNK + ATT_CLUSTER - 1) / ATT_CLUSTER;
-    if (t < ATT_MAXG) {
+    if (t < ATT_MAXG) {  // the arrival releases them (cumulative over the barrier) and acquires the others'
         const int hh = rank + t * ATT_CLUSTER;
-        last[t] = hh < G ? (atomicAdd(p.cnt + g * G + hh, 1) == ncl_used - 1) : 0;
+        last[t] = hh < G ? (atomic_add_acq_rel_gpu(p.cnt + g * G + hh, 1) == ncl_used - 1) : 0;
     }
-    __syncthreads();
-    // the heads this CTA arrived last for: all 256 threads fold the clusters' partials, every load of a batch of 8
-    // clusters in flight at once; the CTA's two halves take the first and the second half of the clusters
-    __shared__ float redm[ATT_THREADS / 32];
-    __shared__ float fnum[ATT_HD];
-    __shared__ float fden;
-    const int lane = t & 31, wid = t >> 5;
-    const int half = t / ATT_HD, d = t % ATT_HD;
-    const int hsplit = (ncl_used + 1) / 2;
-    const int c0 = half ? hsplit : 0, c1 = half ? ncl_used : hsplit;
-    for (int u = 0, hh = rank; hh < G; ++u, hh += ATT_CLUSTER) {
-        if (!last[u]) continue;  // CTA-uniform
-        __threadfence();
-        const float* base = p.part + ((int64_t)g * G + hh) * ncl * (ATT_HD + 2);
-        float M = -FLT_MAX;
-        for (int c = t; c < ncl_used; c += ATT_THREADS) M = fmaxf(M, __ldcg(base + (int64_t)c * (ATT_HD + 2) + ATT_HD));
-        M = warp_max(M);
-        if (lane == 0) redm[wid] = M;
-        __syncthreads();
+    __syncthreads();  // the other threads read after the arriving thread's acquire
+    // the heads this CTA arrived last for (at most two: rank and rank + 4) are folded at once, 128 threads a head,
+    // thread d summing dimension d over the clusters
+    const int lane = t & 31;
+    const int u = t / ATT_HD, d = t % ATT_HD;  // head slot, dimension
+    const int hh = rank + u * ATT_CLUSTER;
+    const bool mine = hh < G && last[u];       // uniform over the slot's four warps
+    const bool any = last[0] || (ATT_CLUSTER < G && last[1]);
+    if (!any) {
+        cluster_wait();
+        return;
+    }
+    const float* base = p.part + ((int64_t)g * G + (mine ? hh : 0)) * ncl * (ATT_HD + 2);
+    if (mine) {
+        // batches of 16 clusters, all loads of a batch in flight; the running maximum rescales the sums (online
+        // softmax), so no separate pass finds the maximum first
+        float M = -FLT_MAX, num = 0.f, den = 0.f;
+        for (int cb = 0; cb < ncl_used; cb += ATT_FOLD_B) {
+            float mc[ATT_FOLD_B], vc[ATT_FOLD_B], lc[ATT_FOLD_B];
 #pragma unroll
-        for (int w = 0; w < ATT_THREADS / 32; ++w) M = fmaxf(M, redm[w]);
-        float num = 0.f, den = 0.f;
-        for (int cb = c0; cb < c1; cb += 8) {
-            float mc[8], vc[8], lc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < ATT_FOLD_B; ++i) {
                 const int c = cb + i;
-                const float* b = base + (int64_t)(c < c1 ? c : c1 - 1) * (ATT_HD + 2);
-                mc[i] = c < c1 ? __ldcg(b + ATT_HD) : -FLT_MAX;
-                vc[i] = c < c1 ? __ldcg(b + d) : 0.f;
-                lc[i] = c < c1 ? __ldcg(b + ATT_HD + 1) : 0.f;
+                const float* b = base + (int64_t)(c < ncl_used ? c : ncl_used - 1) * (ATT_HD + 2);
+                mc[i] = c < ncl_used ? __ldcg(b + ATT_HD) : -FLT_MAX;
+                vc[i] = c < ncl_used ? __ldcg(b + d) : 0.f;
+                lc[i] = c < ncl_used ? __ldcg(b + ATT_HD + 1) : 0.f;
             }
+            float Mb = M;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float f = mc[i] == -FLT_MAX ? 0.f : expf(mc[i] - M);
-                num = fmaf(f, vc[i], num);
-                den = fmaf(f, lc[i], den);
+            for (int i = 0; i < ATT_FOLD_B; ++i) Mb = fmaxf(Mb, mc[i]);
+            if (Mb != -FLT_MAX) {
+                const float r = M == -FLT_MAX ? 0.f : expf(M - Mb);
+                num *= r;
+                den *= r;
+#pragma unroll
+                for (int i = 0; i < ATT_FOLD_B; ++i) {
+                    const float f = mc[i] == -FLT_MAX ? 0.f : expf(mc[i] - Mb);
+                    num = fmaf(f, vc[i], num);
+                    den = fmaf(f, lc[i], den);
+                }
+                M = Mb;
             }
         }
-        if (half) {
-            fnum[d] = num;
-            if (d == 0) fden = den;
+        const float o = num / den;
+        const int64_t oi = ((int64_t)g * G + hh) * ATT_HD + d;
+        p.out[oi] = o;
+        if (p.outq) {  // the slot's four warps hold the head's four 32-value blocks
+            float dsc;
+            const int8_t qv = quantize_lane(o, dsc);
+            p.outq[oi] = qv;
+            if (lane == 0) p.outs[oi / 32] = dsc;
         }
-        __syncthreads();
-        if (!half) {
-            const float o = (num + fnum[d]) / (den + fden);
-            const int64_t oi = ((int64_t)g * G + hh) * ATT_HD + d;
-            p.out[oi] = o;
-            if (p.outq) {  // warps 0..3 hold the head's four 32-value blocks
-                float dsc;
-                const int8_t qv = quantize_lane(o, dsc);
-                p.outq[oi] = qv;
-                if (lane == 0) p.outs[oi / 32] = dsc;
-            }
-        }
-        if (t == 0) p.cnt[g * G + hh] = 0;
-        __syncthreads();  // fnum and redm are reused by the next head
+        if (d == 0) p.cnt[g * G + hh] = 0;
     }
+    cluster_wait();  // no CTA leaves while another may still read its shared memory
 }
 
 // grid (kv, chunk) in clusters of 4 chunks, 8 warps, two CTAs per SM.  Scores: 4 lanes per position (a 32-dim quarter
@@ -215,14 +215,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attention_kernel(const AttnPar
     for (int pass = 0; pass < PASSES; ++pass) {
         const int pl = pass * 64 + wid * 8 + (lane >> 2);
         const bool pre = pl < np && pl != newrow;
-        const float4* kp = reinterpret_cast<const float4*>(kb + (int64_t)(pre ? pl : 0) * ATT_HD + sub * 32);
+        const float* kp = kb + (int64_t)(pre ? pl : 0) * ATT_HD + sub * 32;
+        // four 32-byte loads: each instruction reads whole sectors (lane quarter = 128 contiguous bytes)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 v = pre ? __ldcs(kp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            kr[pass][4 * i] = v.x;
-            kr[pass][4 * i + 1] = v.y;
-            kr[pass][4 * i + 2] = v.z;
-            kr[pass][4 * i + 3] = v.w;
+        for (int i = 0; i < 4; ++i) {
+            if (pre) {
+                ld_f8_stream(kp + 8 * i, &kr[pass][8 * i]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) kr[pass][8 * i + e] = 0.f;
+            }
         }
     }
 #pragma unroll

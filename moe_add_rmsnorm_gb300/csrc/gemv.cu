@@ -140,9 +140,26 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gemv_kernel(const GemvParams p)
 constexpr int TMA_CONSUMERS = 8;
 constexpr int TMA_THREADS = (TMA_CONSUMERS + 1) * 32;
 constexpr int TMA_MAX_TR = 16;
-constexpr int TMA_SMEM = 100 * 1024;
+constexpr int TMA_SMEM = 100 * 1024;      // ring of a projection that shares its SMs with the kernel before it
+constexpr int TMA_SMEM_BIG = 200 * 1024;  // ring of a matrix of more than 64 MB (the LM head): twice the bytes in flight
+constexpr int TMA_MAX_STAGES = 16;
+constexpr int TMA_HDR = 2 * TMA_MAX_STAGES * 8;  // the full and empty barriers
+
+
+// Optional RMSNorm prologue of the TMA projection: x = RMSNorm(a) * w formed by every CTA from the f32 row a (or the
+// row a_row of the table a, an embedding gather), kept in shared memory.  CTA 0 writes the gathered row to sum_out.
+struct NormIn {
+    const float* a;
+    const int32_t* a_row;
+    int64_t a_rows;
+    const float* w;
+    float eps;
+    float* sum_out;
+    int* err;
+};
 
 struct TmaParams {
+    NormIn ni;
     GemvParams g;
     int tr;        // rows per tile
     int tiles;     // total tiles over all segments
@@ -158,8 +175,8 @@ __global__ void __launch_bounds__(TMA_THREADS, 1) gemv_tma_kernel(const TmaParam
     extern __shared__ __align__(128) unsigned char smem[];
     const GemvParams& p = tp.g;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + 8;
-    unsigned char* ring = smem + 128;
+    uint64_t* empty = full + TMA_MAX_STAGES;
+    unsigned char* ring = smem + TMA_HDR;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int k = p.k, nb = p.nb;
     const int nmine = tp.tiles > (int)blockIdx.x ? (tp.tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -199,8 +216,88 @@ __global__ void __launch_bounds__(TMA_THREADS, 1) gemv_tma_kernel(const TmaParam
         return;
     }
 
+    const NormIn& ni = tp.ni;
+    const bool norm = ni.a != nullptr;  // grid-uniform
+    constexpr int NP = 2 * KCH;         // 256-value rounds of the row: k <= 512 * KCH
+    float nw[NP];
+    if (norm)
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const int i = threadIdx.x + TMA_CONSUMERS * 32 * j;
+            nw[j] = i < k ? ni.w[i] : 0.f;
+        }
     griddep_wait();
     griddep_launch();
+    const float* xfp = p.x;
+    const int8_t* xqp = p.xq;
+    const float* xsp = p.xs;
+    if (norm) {
+        // RMSNorm prologue, the same order in every CTA: squares summed as f32 pairs, each y rounded once
+        float* xbuf = reinterpret_cast<float*>(ring + (size_t)tp.ns * tp.stage);  // k floats (or k words), then scales
+        float* xsbuf = xbuf + k;
+        F2* nred = reinterpret_cast<F2*>(xsbuf + k / 32);
+        const float* a = ni.a;
+        if (ni.a_row) {
+            const int32_t idx = *ni.a_row;
+            const bool bad = idx < 0 || idx >= ni.a_rows;  // an out-of-range token: flagged, row 0 read instead
+            a = ni.a + (int64_t)(bad ? 0 : idx) * k;
+            if (bad && blockIdx.x == 0 && threadIdx.x == 0 && ni.err) atomicOr(ni.err, 1);
+        }
+        float av[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const int i = threadIdx.x + TMA_CONSUMERS * 32 * j;
+            av[j] = i < k ? __ldcg(a + i) : 0.f;
+        }
+        F2 ss = f2_two_prod(av[0], av[0]);
+#pragma unroll
+        for (int j = 1; j < NP; ++j) ss = f2_add(ss, f2_two_prod(av[j], av[j]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            ss = f2_add(ss, F2{__shfl_xor_sync(0xffffffffu, ss.hi, o), __shfl_xor_sync(0xffffffffu, ss.lo, o)});
+        if (lane == 0) nred[wid] = ss;
+        asm volatile("bar.sync 1, %0;" ::"n"(TMA_CONSUMERS * 32));
+        if (threadIdx.x == 0) {
+            F2 tot = nred[0];
+            for (int w = 1; w < TMA_CONSUMERS; ++w) tot = f2_add(tot, nred[w]);
+            const float df = (float)k;
+            const float qh = tot.hi / df;
+            const float ql = (fmaf(-qh, df, tot.hi) + tot.lo) / df;
+            nred[TMA_CONSUMERS] = f2_rsqrt(f2_add(f2_quick(qh, ql), F2{ni.eps, 0.f}));
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(TMA_CONSUMERS * 32));
+        const F2 inv = nred[TMA_CONSUMERS];
+        float y[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const int i = threadIdx.x + TMA_CONSUMERS * 32 * j;
+            y[j] = f2_mul3_round(av[j], nw[j], inv);
+            if (i < k && ni.sum_out && blockIdx.x == 0) ni.sum_out[i] = av[j];
+        }
+        if (MODE == 0) {
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int i = threadIdx.x + TMA_CONSUMERS * 32 * j;
+                if (i < k) xbuf[i] = y[j];
+            }
+        } else {
+            int8_t qv[NP];
+            float dsc[NP];
+            quantize_lanes<NP>(y, qv, dsc);  // round j: warp w holds block w + 8 j
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int i = threadIdx.x + TMA_CONSUMERS * 32 * j;
+                if (i < k) {
+                    reinterpret_cast<int8_t*>(xbuf)[i] = qv[j];
+                    if (lane == 0) xsbuf[i / 32] = dsc[j];
+                }
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(TMA_CONSUMERS * 32));
+        xfp = xbuf;
+        xqp = reinterpret_cast<const int8_t*>(xbuf);
+        xsp = xsbuf;
+    }
     // this lane's activation values: columns 16*lane + 512*j
     uint32_t xw[MODE == 1 ? KCH : 1][4];
     float xsc[KCH];
@@ -210,13 +307,13 @@ __global__ void __launch_bounds__(TMA_THREADS, 1) gemv_tma_kernel(const TmaParam
         const int col = 16 * lane + 512 * j;
         const bool ok = col < k;
         if (MODE == 1) {
-            const uint4 v = ok ? *reinterpret_cast<const uint4*>(p.xq + col) : make_uint4(0, 0, 0, 0);
+            const uint4 v = ok ? *reinterpret_cast<const uint4*>(xqp + col) : make_uint4(0, 0, 0, 0);
             xw[j][0] = v.x; xw[j][1] = v.y; xw[j][2] = v.z; xw[j][3] = v.w;
-            xsc[j] = ok ? p.xs[col / 32] : 0.f;
+            xsc[j] = ok ? xsp[col / 32] : 0.f;
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float4 v = ok ? *reinterpret_cast<const float4*>(p.x + col + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 v = ok ? *reinterpret_cast<const float4*>(xfp + col + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
                 xf[j][4 * e] = v.x; xf[j][4 * e + 1] = v.y; xf[j][4 * e + 2] = v.z; xf[j][4 * e + 3] = v.w;
             }
             xsc[j] = 0.f;
@@ -281,6 +378,7 @@ __global__ void __launch_bounds__(TMA_THREADS, 1) gemv_tma_kernel(const TmaParam
 
 bool tma_eligible(const GemvCall& c) {
     if (c.R != 1 || c.dots || c.k % 128 != 0 || c.k > 4096) return false;
+    if (c.norm_a && c.k % (TMA_CONSUMERS * 32)) return false;
     for (int i = 0; i < c.nseg; ++i)
         if ((uintptr_t)c.seg[i].s % 16 != 0 || (uintptr_t)c.seg[i].q % 16 != 0) return false;
     return true;
@@ -389,6 +487,7 @@ cudaError_t run_tma(const TmaParams& tp, int grid, size_t smem, cudaStream_t st,
 
 cudaError_t launch_gemv_tma(const GemvCall& c, int* err, cudaStream_t st) {
     TmaParams tp = {};
+    tp.ni = NormIn{c.norm_a, c.norm_a_row, c.norm_a_rows, c.norm_w, c.eps, c.norm_sum_out, c.err};
     GemvParams& p = tp.g;
     p.nseg = c.nseg;
     p.k = (int)c.k;
@@ -421,12 +520,15 @@ cudaError_t launch_gemv_tma(const GemvCall& c, int* err, cudaStream_t st) {
     tp.tr = tr;
     tp.tiles = tiles;
     tp.stage = (int)(((size_t)tr * c.k + (size_t)tr * (c.k / 32) * 4 + 127) / 128 * 128);
-    int ns = (TMA_SMEM - 128) / tp.stage;
-    if (ns > 8) ns = 8;
+    const int budget = (double)rows_total * c.k > 64.0 * (1 << 20) ? TMA_SMEM_BIG : TMA_SMEM;
+    int ns = (budget - TMA_HDR) / tp.stage;
+    if (ns > TMA_MAX_STAGES) ns = TMA_MAX_STAGES;
     if (ns < 2) return cudaErrorInvalidConfiguration;
     tp.ns = ns;
     tp.err = err;
-    const size_t smem = 128 + (size_t)ns * tp.stage;
+    // the normed activation after the ring: k values (f32) or words, k/32 scales, the reduction's pairs
+    const size_t nbytes = c.norm_a ? (size_t)c.k * 4 + (size_t)(c.k / 32) * 4 + (TMA_CONSUMERS + 1) * sizeof(F2) : 0;
+    const size_t smem = TMA_HDR + (size_t)ns * tp.stage + nbytes;
     const int grid = tiles < sms ? tiles : sms;
     const int kch = (int)((c.k + 511) / 512);
     if (c.mode == 1) {
@@ -443,9 +545,12 @@ cudaError_t launch_gemv_tma(const GemvCall& c, int* err, cudaStream_t st) {
 
 }  // namespace
 
+bool gemv_norm_supported(const GemvCall& c) { return tma_eligible(c); }
+
 cudaError_t launch_gemv(const GemvCall& c, Carve& ws, cudaStream_t st) {
     if (tma_eligible(c))
         return launch_gemv_tma(c, c.err ? c.err : (ws.counters ? ws.counters + ws.n_counters - 1 : nullptr), st);
+    if (c.norm_a) return cudaErrorInvalidConfiguration;  // the norm prologue exists in the TMA projection only
     const int nb = (int)(c.k / 32);
     const Plan pl = plan_for(c);
     GemvParams p = {};

@@ -68,7 +68,17 @@ struct GemvCall {
     int* err = nullptr;                  // device error word for a pipeline wait that gave up
     L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;                         // launch with programmatic dependent launch allowed
+    // optional RMSNorm prologue (one row, k a multiple of 256 and at most 4096): x = RMSNorm(norm_a) * norm_w formed
+    // inside the launch; with norm_a_row the row is norm_a + (*norm_a_row) * k (an embedding gather; bit 1 of err
+    // for an index outside [0, norm_a_rows)) and the gathered row is written to norm_sum_out
+    const float* norm_a = nullptr;
+    const int32_t* norm_a_row = nullptr;
+    int64_t norm_a_rows = 0;
+    const float* norm_w = nullptr;
+    float eps = 0.f;
+    float* norm_sum_out = nullptr;
 };
+bool gemv_norm_supported(const GemvCall& c);
 
 // Scratch needed by a projection (bytes, counters).
 void gemv_scratch(const GemvCall& c, size_t* bytes, size_t* counters);
@@ -144,6 +154,8 @@ struct ExpertCall {
     const int8_t* xq = nullptr;          // mode 1: gate-up xq [R][k]; down hq [R*K][k]
     const float* xs = nullptr;
     float* h = nullptr;                  // gate-up out [R*K][dff]
+    int8_t* hq_out = nullptr;            // gate-up, one row, int8 mode: h quantized per 32 rows (dff % 32 == 0)
+    float* hs_out = nullptr;             //   and its scales [K][dff/32]
     const float* residual = nullptr;     // down
     float* y = nullptr;                  // down out [R][d]
     float* expert_out = nullptr;         // down out [R][K][d]
@@ -172,11 +184,21 @@ struct RouteRowCall {
     float* logits = nullptr;    // optional [E]
     int32_t* ids = nullptr;
     float* gates = nullptr;
+    // optional: the kernel forms x = RMSNorm(norm_a) * norm_w itself (d a multiple of 256, at most 4096) and writes it
+    // to x_out (f32 mode) or xq_out / xs_out (int8 mode); x, xq and xs are then not read
+    const float* norm_a = nullptr;
+    const float* norm_w = nullptr;
+    float eps = 0.f;
+    float* x_out = nullptr;
+    int8_t* xq_out = nullptr;
+    float* xs_out = nullptr;
     L2Prefetch pf;
     int pdl = 0;
 };
 bool route_row_supported(int mode, int64_t E, int64_t d, int K);
 cudaError_t launch_route_row(const RouteRowCall& c, cudaStream_t st);
+bool gate_row_supported(const ExpertCall& c);
+cudaError_t launch_gate_row(const ExpertCall& c, Carve& ws, cudaStream_t st);
 bool down_row_supported(const ExpertCall& c);
 cudaError_t launch_down_row(const ExpertCall& c, cudaStream_t st);
 

@@ -5,12 +5,13 @@
 // step captured as one CUDA graph and replayed per token with position and token on the device) and forward_shim.rs
 // (module docs: the whole forward captured as one CUDA graph; every stage reads and writes whole buffers).
 //
-// Launches per layer (the merges are GB300 choices, not the pages'): one add+RMSNorm with its int8 epilogue; one
-// projection for q, k and v together; one split attention that first applies QK-norm and RoPE and appends the new key
-// and value rows (its fold quantizes the result for the O projection); the O projection with the residual sum in its
-// epilogue; one add+RMSNorm; the router projection with its top-k in one cluster launch; gate-up with its int8
-// epilogue; down-and-combine with the residual sum in its epilogue.  Then the final norm, the LM head and the arg-max
-// that advances token and position.
+// Launches per layer (the merges are GB300 choices, not the pages'): one projection for q, k and v together that first
+// forms RMSNorm of the residual row itself (the first layer gathers the token's embedding row into the residual
+// stream); one split attention that first applies QK-norm and RoPE and appends the new key and value rows (its fold
+// quantizes the result for the O projection); the O projection with the residual sum in its epilogue; the router
+// projection with its RMSNorm and its top-k in one cluster launch; gate-up; down-and-combine with the residual sum in
+// its epilogue.  Then the LM head with the final norm, and the arg-max that advances token and position.  Shapes the
+// fused forms do not take fall back to a separate add+RMSNorm launch.
 #include <cuda_runtime.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -46,6 +47,7 @@ struct q8_model {
     size_t n_counters = 0;
     cudaStream_t cap = nullptr;
     cudaGraphExec_t exec = nullptr;
+    int64_t kernels_per_step = 0;  // kernel nodes of the captured step
     int pdl = 1;       // programmatic dependent launch between the step's kernels
     int prefetch = 1;  // weights fetched into L2 ahead of the launches that read them
 };
@@ -95,43 +97,54 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
         if (e != cudaSuccess) return e; \
     } while (0)
     for (int64_t l = 0; l < d.layers; ++l) {
-        // attention half: norm (the first layer gathers the token's embedding row into the residual stream)
-        NormCall n;
-        if (l == 0) {
-            n.a = d.embed;
-            n.a_row = d.tok;
-            n.a_rows = d.vocab;
-            n.sum = m->h;
-        } else {
-            n.a = m->h;
+        // attention half: norm (the first layer gathers the token's embedding row into the residual stream), then q,
+        // k and v in one projection launch; the norm runs inside the projection launch when the shapes allow it
+        GemvCall g;
+        g.mode = mode;
+        g.k = D;
+        g.nseg = 3;
+        g.seg[0] = GemvSeg{m->wq[l].q, m->wq[l].s, H * HD, m->q, nullptr};
+        g.seg[1] = GemvSeg{m->wk[l].q, m->wk[l].s, KV * HD, m->k, nullptr};
+        g.seg[2] = GemvSeg{m->wv[l].q, m->wv[l].s, KV * HD, m->v, nullptr};
+        g.x = m->x;
+        g.xq = m->xq;
+        g.xs = m->xs;
+        g.pdl = pdl;
+        g.err = m->err;
+        g.norm_a = l == 0 ? d.embed : m->h;
+        g.norm_a_row = l == 0 ? d.tok : nullptr;
+        g.norm_a_rows = d.vocab;
+        g.norm_w = m->attn_norm[l];
+        g.eps = d.eps;
+        g.norm_sum_out = l == 0 ? m->h : nullptr;
+        if (!gemv_norm_supported(g)) {
+            g.norm_a = nullptr;
+            g.norm_a_row = nullptr;
+            g.norm_sum_out = nullptr;
+            NormCall n;
+            if (l == 0) {
+                n.a = d.embed;
+                n.a_row = d.tok;
+                n.a_rows = d.vocab;
+                n.sum = m->h;
+            } else {
+                n.a = m->h;
+            }
+            n.w = m->attn_norm[l];
+            n.rows = 1;
+            n.d = D;
+            n.eps = d.eps;
+            if (mode == 0) n.y = m->x;
+            else {
+                n.yq = m->xq;
+                n.ys = m->xs;
+            }
+            n.err = m->err;
+            n.pdl = pdl;
+            Q8_TRY(launch_add_rmsnorm(n, st));
         }
-        n.w = m->attn_norm[l];
-        n.rows = 1;
-        n.d = D;
-        n.eps = d.eps;
-        if (mode == 0) n.y = m->x;
-        else {
-            n.yq = m->xq;
-            n.ys = m->xs;
-        }
-        n.err = m->err;
-        n.pdl = pdl;
-        Q8_TRY(launch_add_rmsnorm(n, st));
-        // q, k and v in one projection launch
         {
             Carve cv = fresh_carve(m);
-            GemvCall g;
-            g.mode = mode;
-            g.k = D;
-            g.nseg = 3;
-            g.seg[0] = GemvSeg{m->wq[l].q, m->wq[l].s, H * HD, m->q, nullptr};
-            g.seg[1] = GemvSeg{m->wk[l].q, m->wk[l].s, KV * HD, m->k, nullptr};
-            g.seg[2] = GemvSeg{m->wv[l].q, m->wv[l].s, KV * HD, m->v, nullptr};
-            g.x = m->x;
-            g.xq = m->xq;
-            g.xs = m->xs;
-            g.pdl = pdl;
-            g.err = m->err;
             Q8_TRY(launch_gemv(g, cv, st));
         }
         {
@@ -174,20 +187,23 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             g.err = m->err;
             Q8_TRY(launch_gemv(g, cv, st));
         }
-        // feed-forward half
-        NormCall n2;
-        n2.a = m->h;
-        n2.w = m->ffn_norm[l];
-        n2.rows = 1;
-        n2.d = D;
-        n2.eps = d.eps;
-        if (mode == 0) n2.y = m->x;
-        else {
-            n2.yq = m->xq;
-            n2.ys = m->xs;
+        // feed-forward half: the norm happens inside the router launch when the shapes allow it
+        const bool fused_norm2 = route_row_supported(mode, d.experts, D, (int)d.k) && D % 256 == 0 && D <= 4096;
+        if (!fused_norm2) {
+            NormCall n2;
+            n2.a = m->h;
+            n2.w = m->ffn_norm[l];
+            n2.rows = 1;
+            n2.d = D;
+            n2.eps = d.eps;
+            if (mode == 0) n2.y = m->x;
+            else {
+                n2.yq = m->xq;
+                n2.ys = m->xs;
+            }
+            n2.pdl = pdl;
+            Q8_TRY(launch_add_rmsnorm(n2, st));
         }
-        n2.pdl = pdl;
-        Q8_TRY(launch_add_rmsnorm(n2, st));
         if (route_row_supported(mode, d.experts, D, (int)d.k)) {
             // the router projection and its top-k in one cluster launch
             RouteRowCall r;
@@ -202,6 +218,14 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             r.xs = m->xs;
             r.ids = m->ids;
             r.gates = m->gates;
+            if (fused_norm2) {
+                r.norm_a = m->h;
+                r.norm_w = m->ffn_norm[l];
+                r.eps = d.eps;
+                r.x_out = mode == 0 ? m->x : nullptr;
+                r.xq_out = m->xq;
+                r.xs_out = m->xs;
+            }
             r.pdl = pdl;
             Q8_TRY(launch_route_row(r, st));
         } else {
@@ -226,6 +250,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             t.pdl = pdl;
             Q8_TRY(launch_topk(t, st));
         }
+        bool hq_by_gate = false;
         {
             Carve cv = fresh_carve(m);
             ExpertCall c;
@@ -244,6 +269,11 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             c.xq = m->xq;
             c.xs = m->xs;
             c.h = m->hbuf;
+            if (mode == 1 && gate_row_supported(c)) {  // the hidden rows quantized once, by the kernel that forms them
+                c.hq_out = m->hq;
+                c.hs_out = m->hs;
+                hq_by_gate = true;
+            }
             c.pdl = pdl;
             c.err = m->err;
             if (m->prefetch && l + 1 < d.layers) {  // the next layer's q, k and v projections
@@ -266,7 +296,11 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             c.K = (int)d.k;
             c.ids = m->ids;
             c.gates = m->gates;
-            c.x = m->hbuf;  // f32 hidden rows; the int8 mode quantizes them as each CTA stages them
+            c.x = m->hbuf;  // f32 hidden rows
+            if (hq_by_gate) {  // and their int8 form, written by gate-up
+                c.xq = m->hq;
+                c.xs = m->hs;
+            }
             c.residual = m->h;  // h = h + mixture
             c.y = m->h;
             c.pdl = pdl;
@@ -274,22 +308,8 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             Q8_TRY(launch_down_combine(c, cv, st));
         }
     }
-    // final norm, LM head, greedy token
-    NormCall nf;
-    nf.a = m->h;
-    nf.w = d.final_norm;
-    nf.rows = 1;
-    nf.d = D;
-    nf.eps = d.eps;
-    if (mode == 0) nf.y = m->x;
-    else {
-        nf.yq = m->xq;
-        nf.ys = m->xs;
-    }
-    nf.pdl = pdl;
-    Q8_TRY(launch_add_rmsnorm(nf, st));
+    // final norm (inside the LM head launch when the shapes allow it), LM head, greedy token
     {
-        Carve cv = fresh_carve(m);
         GemvCall g;
         g.mode = mode;
         g.k = D;
@@ -299,6 +319,26 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
         g.xs = m->xs;
         g.pdl = pdl;
         g.err = m->err;
+        g.norm_a = m->h;
+        g.norm_w = d.final_norm;
+        g.eps = d.eps;
+        if (!gemv_norm_supported(g)) {
+            g.norm_a = nullptr;
+            NormCall nf;
+            nf.a = m->h;
+            nf.w = d.final_norm;
+            nf.rows = 1;
+            nf.d = D;
+            nf.eps = d.eps;
+            if (mode == 0) nf.y = m->x;
+            else {
+                nf.yq = m->xq;
+                nf.ys = m->xs;
+            }
+            nf.pdl = pdl;
+            Q8_TRY(launch_add_rmsnorm(nf, st));
+        }
+        Carve cv = fresh_carve(m);
         Q8_TRY(launch_gemv(g, cv, st));
     }
     {
@@ -348,6 +388,8 @@ int q8_model_create(const q8_model_desc* desc, q8_model** out) {
     for (int64_t l = 0; l < d.layers; ++l) {
         if (!d.attn_norm[l] || !d.ffn_norm[l] || !d.q_norm[l] || !d.k_norm[l] || !d.k_cache[l] || !d.v_cache[l])
             return model_fail(Q8_EINVAL, "layer %lld: a null norm weight or cache", (long long)l);
+        if ((uintptr_t)d.k_cache[l] % 32 || (uintptr_t)d.v_cache[l] % 32)
+            return model_fail(Q8_EINVAL, "layer %lld: a cache not 32-byte aligned", (long long)l);
         int r;
         if ((r = check_mat_shape(d.wq[l], QD, D, "wq", l)) || (r = check_mat_shape(d.wk[l], KD, D, "wk", l)) ||
             (r = check_mat_shape(d.wv[l], KD, D, "wv", l)) || (r = check_mat_shape(d.wo[l], D, QD, "wo", l)) ||
@@ -492,6 +534,19 @@ int decode_step(q8_model* m, q8_stream stream) {
             e = cudaStreamEndCapture(m->cap, &graph);
             if (le != cudaSuccess) e = le;
         }
+        if (e == cudaSuccess) {  // the step's kernel count, for callers that report launches
+            size_t n = 0;
+            e = cudaGraphGetNodes(graph, nullptr, &n);
+            std::vector<cudaGraphNode_t> nodes(n);
+            if (e == cudaSuccess && n) e = cudaGraphGetNodes(graph, nodes.data(), &n);
+            int64_t kernels = 0;
+            for (size_t i = 0; e == cudaSuccess && i < n; ++i) {
+                cudaGraphNodeType ty;
+                e = cudaGraphNodeGetType(nodes[i], &ty);
+                if (e == cudaSuccess && ty == cudaGraphNodeTypeKernel) ++kernels;
+            }
+            m->kernels_per_step = kernels;
+        }
         if (e == cudaSuccess) e = cudaGraphInstantiate(&m->exec, graph, 0);
         if (graph) cudaGraphDestroy(graph);
         if (e != cudaSuccess) {
@@ -502,6 +557,8 @@ int decode_step(q8_model* m, q8_stream stream) {
     e = cudaGraphLaunch(m->exec, (cudaStream_t)stream);
     return e == cudaSuccess ? Q8_OK : model_fail(Q8_ECUDA, "decode_step: %s", cudaGetErrorString(e));
 }
+
+int64_t q8_model_launches_per_step(const q8_model* m) { return m ? m->kernels_per_step : 0; }
 
 int q8_model_check(q8_model* m, q8_stream stream) {
     if (!m) return model_fail(Q8_EINVAL, "model: null");

@@ -607,9 +607,8 @@ cudaError_t launch_topk(const TopkCall& c, cudaStream_t st) {
 bool experts_supported(int mode, int64_t k) { return k / 32 <= 32 * ((mode == 0) ? 3 : 4); }
 
 void gate_up_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
-    (void)c;
     *bytes = 0;
-    *counters = 0;
+    *counters = c.hq_out ? (size_t)(c.R * c.K * (c.out_rows / 32)) : 0;
 }
 
 void down_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
@@ -620,6 +619,8 @@ void down_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
 }
 
 cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
+    if (gate_row_supported(c)) return launch_gate_row(c, ws, st);
+    if (c.hq_out) return cudaErrorInvalidConfiguration;  // the int8 epilogue exists in the one-row kernel only
     // gate and up tiles are both in flight: about four (f32) or eight (int8) 32-byte loads per lane in all
     const EPlan pl = eplan(c.mode, (int)(c.k / 32), c.mode == 0 ? 2 : 4);
     ExpertParams p = make_params(c, pl);

@@ -12,7 +12,8 @@
 // of programmatic dependent launch.  The router rows do not depend on earlier kernels and are loaded before the wait;
 // one cluster of 8 CTAs forms all logits, gathers them in CTA 0 through distributed shared memory and ranks them
 // there (each expert counts the experts ahead of it), which replaces a second launch and K rounds of warp arg-max.
-// The down-and-combine reads the routing written two launches back, so a warp requests its output row's K*dff/32
+// Gate-up deals each warp a few consecutive hidden rows and issues all of their weight loads at once.  The
+// down-and-combine reads the routing written two launches back, so a warp requests its output row's K*dff/32
 // weight blocks (one 256-bit load each) before the wait and only the hidden rows after it.
 #include <float.h>
 
@@ -34,6 +35,8 @@ constexpr int RR_WARPS = RR_THREADS / 32;
 constexpr int RR_MAXE = 1024;    // experts one cluster ranks
 constexpr int RR_RW = 2;         // router rows per warp loaded before the wait
 
+constexpr int RR_NPER = 16;      // 256-value rounds of a row the kernel norms itself, at most (d <= 4096)
+
 struct RouteRowParams {
     const int8_t* q;
     const float* s;
@@ -44,6 +47,14 @@ struct RouteRowParams {
     float* logits;
     int32_t* ids;
     float* gates;
+    // when norm_a is set the kernel forms the activation itself: x = RMSNorm(norm_a) * norm_w (int8 form in the int8
+    // mode), keeps it in shared memory and writes it to x_out (or xq_out / xs_out) for the launches after it
+    const float* norm_a;
+    const float* norm_w;
+    float eps;
+    float* x_out;
+    int8_t* xq_out;
+    float* xs_out;
     L2Prefetch pf;
 };
 
@@ -56,9 +67,15 @@ template <int MODE, int BPL>
 __global__ void __launch_bounds__(RR_THREADS) route_row_kernel(const RouteRowParams p) {
     __shared__ float own[RR_MAXE / RR_CL];
     __shared__ float all[RR_MAXE];
-    __shared__ float key[RR_MAXE];
+    __shared__ __align__(16) float key[RR_MAXE];
+    __shared__ int cnt0[RR_MAXE];
+    __shared__ int cnt1[RR_MAXE];
     __shared__ int kid[32];
     __shared__ float kv[32];
+    __shared__ __align__(16) float xbuf[RR_THREADS * RR_NPER];  // the normed activation (f32, or its int8 words)
+    __shared__ float xsbuf[RR_THREADS * RR_NPER / 32];
+    __shared__ F2 nred[RR_WARPS];
+    __shared__ F2 ninv;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -79,10 +96,83 @@ __global__ void __launch_bounds__(RR_THREADS) route_row_kernel(const RouteRowPar
         const bool v = lr < rpc && r0 + lr < p.E;
         load_tile<BPL, 1>(t[u], p.q, p.s, v ? r0 + lr : 0, v ? 1 : 0, p.d, p.nb, bidx, bval);
     }
-    griddep_wait();  // the activation comes from the previous launch
+    const bool norm = p.norm_a != nullptr;  // grid-uniform
+    constexpr int NP = 4 * BPL;             // 256-value rounds of the row: d <= 1024 * BPL
+    float nw[NP];
+    if (norm)
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const int i = threadIdx.x + RR_THREADS * j;
+            nw[j] = i < p.d ? p.norm_w[i] : 0.f;
+        }
+    griddep_wait();  // the activation (or the row it is normed from) comes from the previous launch
     griddep_launch();
+    const float* xf = p.x;
+    const int8_t* xq = p.xq;
+    const float* xsc = p.xs;
+    if (norm) {
+        // RMSNorm of the residual row, every CTA of the cluster in the same order (so all hold the same x): the sum
+        // of squares and the norm factor in f32 pairs, each y rounded once
+        float a[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const int i = threadIdx.x + RR_THREADS * j;
+            a[j] = i < p.d ? __ldcg(p.norm_a + i) : 0.f;
+        }
+        F2 ss = f2_two_prod(a[0], a[0]);
+#pragma unroll
+        for (int j = 1; j < NP; ++j) ss = f2_add(ss, f2_two_prod(a[j], a[j]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            ss = f2_add(ss, F2{__shfl_xor_sync(0xffffffffu, ss.hi, o), __shfl_xor_sync(0xffffffffu, ss.lo, o)});
+        if (lane == 0) nred[wid] = ss;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            F2 tot = nred[0];
+            for (int w = 1; w < RR_WARPS; ++w) tot = f2_add(tot, nred[w]);
+            const float df = (float)p.d;
+            const float qh = tot.hi / df;
+            const float ql = (fmaf(-qh, df, tot.hi) + tot.lo) / df;
+            ninv = f2_rsqrt(f2_add(f2_quick(qh, ql), F2{p.eps, 0.f}));
+        }
+        __syncthreads();
+        const F2 inv = ninv;
+        float y[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) y[j] = f2_mul3_round(a[j], nw[j], inv);
+        if (MODE == 0) {
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int i = threadIdx.x + RR_THREADS * j;
+                if (i < p.d) {
+                    xbuf[i] = y[j];
+                    if (j % RR_CL == rank) p.x_out[i] = y[j];  // CTA r writes rounds j = r, r + 8, ...
+                }
+            }
+        } else {
+            int8_t qv[NP];
+            float dsc[NP];
+            quantize_lanes<NP>(y, qv, dsc);  // round j: warp w holds block w + 8 j
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int i = threadIdx.x + RR_THREADS * j;
+                if (i < p.d) {
+                    reinterpret_cast<int8_t*>(xbuf)[i] = qv[j];
+                    if (lane == 0) xsbuf[i / 32] = dsc[j];
+                    if (j % RR_CL == rank) {  // CTA r writes rounds j = r, r + 8, ...
+                        p.xq_out[i] = qv[j];
+                        if (lane == 0) p.xs_out[i / 32] = dsc[j];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        xf = xbuf;
+        xq = reinterpret_cast<const int8_t*>(xbuf);
+        xsc = xsbuf;
+    }
     XTile<MODE, BPL> x;
-    load_x<MODE, BPL>(x, p.x, p.xq, p.xs, bidx, bval);
+    load_x<MODE, BPL>(x, xf, xq, xsc, bidx, bval);
 #pragma unroll
     for (int u = 0; u < RR_RW; ++u) {
         const int lr = wid + RR_WARPS * u;
@@ -110,15 +200,30 @@ __global__ void __launch_bounds__(RR_THREADS) route_row_kernel(const RouteRowPar
         }
     cluster.sync();  // CTA 0 has read every slice: the others may leave
     if (rank != 0) return;
-    // expert e's place among the kept = the number of experts with a larger key, or an equal key and a lower index
-    for (int e = threadIdx.x; e < p.E; e += RR_THREADS) {
+    // expert e's place among the kept = the number of experts with a larger key, or an equal key and a lower index;
+    // the two halves of the CTA count over the two halves of the experts (keys padded to a multiple of 8 with -inf
+    // entries that never count: they sit past every real index)
+    const int E8 = (p.E + 7) & ~7;
+    for (int e = p.E + threadIdx.x; e < E8; e += RR_THREADS) key[e] = -INFINITY;
+    __syncthreads();
+    const int half = threadIdx.x / (RR_THREADS / 2), hl = threadIdx.x % (RR_THREADS / 2);
+    const int f0 = half ? (E8 / 16) * 8 : 0, f1 = half ? E8 : (E8 / 16) * 8;
+    for (int e = hl; e < p.E; e += RR_THREADS / 2) {
         const float ke = key[e];
         int r = 0;
-#pragma unroll 8
-        for (int f = 0; f < p.E; ++f) {
-            const float kf = key[f];
-            r += (kf > ke) || (kf == ke && f < e);
+        for (int f = f0; f < f1; f += 8) {
+            const float4 a = *reinterpret_cast<const float4*>(key + f);
+            const float4 b = *reinterpret_cast<const float4*>(key + f + 4);
+            const float kf[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r += (kf[i] > ke) || (kf[i] == ke && f + i < e);
         }
+        if (half) cnt1[e] = r;
+        else cnt0[e] = r;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.E; e += RR_THREADS) {
+        const int r = cnt0[e] + cnt1[e];
         if (r < p.K) {
             kid[r] = e;
             kv[r] = all[e];
@@ -160,10 +265,109 @@ cudaError_t run_route_row(const RouteRowParams& p, cudaStream_t st, int pdl) {
     return cudaLaunchKernelEx(&cfg, route_row_kernel<MODE, BPL>, p);
 }
 
+// ==== gate-up ========================================================================================================
+
+constexpr int GR_WPC = 14;  // warps per CTA
+
+struct GateRowParams {
+    const int8_t* gq;  // gate and up [E*dff][d]
+    const float* gs;
+    const int8_t* uq;
+    const float* us;
+    int E, dff, d, nb, K;
+    const int32_t* ids;
+    const int8_t* xq;  // int8 mode: the normed activation [d] and its scales
+    const float* xs;
+    float* h;          // [K][dff]
+    int8_t* hq;        // optional: h quantized per 32 rows [K][dff] and its scales [K][dff/32] (dff % 32 == 0)
+    float* hs;
+    int* qcnt;         // [K*dff/32] arrivals per 32-row block (left zero)
+    L2Prefetch pf;
+};
+
+// Int8 mode, one row: item it = (kept expert it / dff, hidden row it % dff) is that row of the expert's gate and up
+// matrices; warp w takes items w*IPW .. w*IPW + IPW - 1 (consecutive rows, so each warp reads contiguous weights) and
+// issues all of their loads before it multiplies any, so a whole launch's weights are in flight at once.  The expert
+// ids and the activation are read after the wait.
+template <int BPL, int IPW>
+__global__ void __launch_bounds__(GR_WPC * 32, 1) gate_row_kernel(const GateRowParams p) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int warp = blockIdx.x * GR_WPC + wid;
+    const int W = gridDim.x * GR_WPC;
+    const int n = p.K * p.dff;
+    int bidx[BPL];
+    bool bval[BPL];
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+        bidx[j] = lane + 32 * j;
+        bval[j] = bidx[j] < p.nb;
+    }
+    issue_l2_prefetch(p.pf);
+    griddep_wait();  // the expert ids (and, when the router launch norms it, the activation) come from the previous launch
+    griddep_launch();
+    XTile<1, BPL> x;
+    load_x<1, BPL>(x, nullptr, p.xq, p.xs, bidx, bval);
+    for (int it0 = warp * IPW; it0 < n; it0 += W * IPW) {
+        WTile<BPL, 1> tg[IPW], tu[IPW];
+        int eid[IPW];  // every item's expert id read before any weight address depends on one
+#pragma unroll
+        for (int u = 0; u < IPW; ++u) eid[u] = it0 + u < n ? __ldcg(p.ids + (it0 + u) / p.dff) : -1;
+#pragma unroll
+        for (int u = 0; u < IPW; ++u) {
+            const int it = it0 + u;
+            const int j = it / p.dff, i = it - j * p.dff;
+            const int e = eid[u];
+            const bool ev = e >= 0 && e < p.E;  // an id outside [0, E) counts as an expert of zero weights
+            const int64_t wrow = (int64_t)(ev ? e : 0) * p.dff + i;
+            load_tile<BPL, 1>(tg[u], p.gq, p.gs, wrow, ev ? 1 : 0, p.d, p.nb, bidx, bval);
+            load_tile<BPL, 1>(tu[u], p.uq, p.us, wrow, ev ? 1 : 0, p.d, p.nb, bidx, bval);
+        }
+#pragma unroll
+        for (int u = 0; u < IPW; ++u) {
+            const float gv = group_sum<32>(tile_row_dot<1, BPL, 1>(tg[u], 0, x));
+            const float uv = group_sum<32>(tile_row_dot<1, BPL, 1>(tu[u], 0, x));
+            if (lane == 0 && it0 + u < n) p.h[it0 + u] = silu_f32(gv) * uv;
+        }
+        if (p.hq) {
+            // the int8 epilogue: every warp arrives on the 32-row blocks its rows belong to (item it is row it % 32 of
+            // block it / 32), releasing its rows; the warp that completes a block quantizes it, lane = row
+            const int b0 = it0 / 32;
+            const int last_it = min(it0 + IPW, n) - 1;
+            for (int b = b0; b <= last_it / 32; ++b) {  // at most two blocks
+                const int lo = max(it0, b * 32), hi = min(last_it, b * 32 + 31);
+                int old = 0;
+                __syncwarp();
+                if (lane == 0) old = atomic_add_acq_rel_gpu(p.qcnt + b, hi - lo + 1);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old + (hi - lo + 1) == 32) {  // warp-uniform
+                    __syncwarp();
+                    float dsc;
+                    const int8_t qv = quantize_lane(__ldcg(p.h + (int64_t)b * 32 + lane), dsc);
+                    p.hq[(int64_t)b * 32 + lane] = qv;
+                    if (lane == 0) {
+                        p.hs[b] = dsc;
+                        p.qcnt[b] = 0;
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int BPL, int IPW>
+cudaError_t run_gate_row(const GateRowParams& p, cudaStream_t st, int pdl) {
+    const int n = p.K * p.dff;
+    int grid = (n + GR_WPC * IPW - 1) / (GR_WPC * IPW);
+    const int cap = device_info().sms;
+    if (grid > cap) grid = cap;
+    return launch(gate_row_kernel<BPL, IPW>, dim3(grid), dim3(GR_WPC * 32), 0, st, pdl, p);
+}
+
 // ==== down-and-combine ==============================================================================================
 
-constexpr int DR_MAXW = 16;  // warps per CTA at most
+constexpr int DR_MAXW = 14;  // warps per CTA at most (146 registers a thread)
 constexpr int DR_MAXP = 8;   // (expert, block) pairs per lane at most: K * dff/32 <= 256
+constexpr int DR_QB = 16;    // hidden-row blocks a warp loads at once when it quantizes them
 
 struct DownRowParams {
     const int8_t* q;  // down [E*rows][k]
@@ -213,6 +417,8 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
             sw[i] = 0.f;
         }
     }
+    // the residual row was written three launches back, before the launch before this one passed its wait
+    const float res = (p.residual && orow && lane == 0) ? __ldcg(p.residual + o) : 0.f;
     griddep_wait();  // the hidden rows come from the previous launch
     griddep_launch();
     const int8_t* hq = p.hq;
@@ -222,26 +428,27 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
             reinterpret_cast<float4*>(hsm)[i] = __ldcg(reinterpret_cast<const float4*>(p.h) + i);
         __syncthreads();
     } else if (!hq) {
-        // the CTA quantizes the f32 hidden rows into shared memory: warp w takes blocks w, w + W, ..., four at a time
-        // (all four blocks' values loaded before any is quantized)
+        // the CTA quantizes the f32 hidden rows into shared memory: warp w takes blocks w, w + W, ..., up to
+        // DR_QB of them with every load in flight before the first is quantized
         int8_t* sq = reinterpret_cast<int8_t*>(hsm);
         float* ss = hsm + P * 8;  // after the P * 32 words
         const int W = blockDim.x >> 5;
-        for (int b0 = wid; b0 < P; b0 += 4 * W) {
-            float v[4];
+        for (int b0 = wid; b0 < P; b0 += DR_QB * W) {
+            float v[DR_QB];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < DR_QB; ++u) {
                 const int b = b0 + u * W;
                 v[u] = b < P ? __ldcg(p.h + (int64_t)b * 32 + lane) : 0.f;
             }
+            int8_t qv[DR_QB];
+            float dsc[DR_QB];
+            quantize_lanes<DR_QB>(v, qv, dsc);  // the blocks' warp reductions interleaved
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < DR_QB; ++u) {
                 const int b = b0 + u * W;
-                float dsc;
-                const int8_t qv = quantize_lane(v[u], dsc);
                 if (b < P) {
-                    sq[b * 32 + lane] = qv;
-                    if (lane == 0) ss[b] = dsc;
+                    sq[b * 32 + lane] = qv[u];
+                    if (lane == 0) ss[b] = dsc[u];
                 }
             }
         }
@@ -286,7 +493,7 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
     acc = group_sum<32>(acc);
     if (lane == 0 && orow) {
         float v = (float)acc;
-        if (p.residual) v = p.residual[o] + v;
+        if (p.residual) v = res + v;
         p.y[o] = v;
     }
 }
@@ -332,8 +539,11 @@ bool route_row_supported(int mode, int64_t E, int64_t d, int K) {
 
 cudaError_t launch_route_row(const RouteRowCall& c, cudaStream_t st) {
     if (!route_row_supported(c.mode, c.E, c.d, c.K)) return cudaErrorInvalidConfiguration;
+    if (c.norm_a && (c.d % RR_THREADS || c.d > RR_THREADS * RR_NPER || !c.norm_w ||
+                     (c.mode == 0 ? !c.x_out : (!c.xq_out || !c.xs_out))))
+        return cudaErrorInvalidValue;
     RouteRowParams p = {c.q, c.s, (int)c.E, (int)c.d, (int)(c.d / 32), c.K, c.x, c.xq, c.xs, c.logits, c.ids, c.gates,
-                        c.pf};
+                        c.norm_a, c.norm_w, c.eps, c.x_out, c.xq_out, c.xs_out, c.pf};
     const int bpl = route_bpl(c.mode, c.d);
     if (c.mode == 0) {
         if (bpl == 1) return run_route_row<0, 1>(p, st, c.pdl);
@@ -344,6 +554,37 @@ cudaError_t launch_route_row(const RouteRowCall& c, cudaStream_t st) {
         if (bpl == 4) return run_route_row<1, 4>(p, st, c.pdl);
     }
     return cudaErrorInvalidConfiguration;
+}
+
+bool gate_row_supported(const ExpertCall& c) {
+    return c.mode == 1 && c.R == 1 && !c.plan.active && c.xq && c.xs && c.k % 32 == 0 && c.k / 32 <= 128 &&
+           c.K >= 1 && c.out_rows >= 1 && c.E * c.out_rows < (int64_t(1) << 31);
+}
+
+cudaError_t launch_gate_row(const ExpertCall& c, Carve& ws, cudaStream_t st) {
+    if (!gate_row_supported(c)) return cudaErrorInvalidConfiguration;
+    GateRowParams p = {c.q0, c.s0, c.q1, c.s1, (int)c.E, (int)c.out_rows, (int)c.k, (int)(c.k / 32), c.K, c.ids,
+                       c.xq, c.xs, c.h, nullptr, nullptr, nullptr, c.pf};
+    if (c.hq_out) {
+        if (c.out_rows % 32) return cudaErrorInvalidValue;
+        p.hq = c.hq_out;
+        p.hs = c.hs_out;
+        p.qcnt = ws.take_counters((size_t)(c.K * c.out_rows / 32));
+        if (ws.overflow) return cudaErrorMemoryAllocation;
+    }
+    const int nb = (int)(c.k / 32);
+    const int bpl = nb <= 32 ? 1 : nb <= 64 ? 2 : 4;
+    // items per warp: enough that one pass covers every item on a grid of one CTA per SM, at most 6 blocks per lane
+    const int64_t n = (int64_t)c.K * c.out_rows;
+    const int64_t slots = (int64_t)device_info().sms * GR_WPC;
+    int ipw = (int)((n + slots - 1) / slots);
+    const int ipw_max = bpl == 4 ? 1 : 3;
+    if (ipw > ipw_max) ipw = ipw_max;
+    if (bpl == 1) return ipw == 1 ? run_gate_row<1, 1>(p, st, c.pdl) : ipw == 2 ? run_gate_row<1, 2>(p, st, c.pdl)
+                                                                            : run_gate_row<1, 3>(p, st, c.pdl);
+    if (bpl == 2) return ipw == 1 ? run_gate_row<2, 1>(p, st, c.pdl) : ipw == 2 ? run_gate_row<2, 2>(p, st, c.pdl)
+                                                                            : run_gate_row<2, 3>(p, st, c.pdl);
+    return run_gate_row<4, 1>(p, st, c.pdl);
 }
 
 bool down_row_supported(const ExpertCall& c) {

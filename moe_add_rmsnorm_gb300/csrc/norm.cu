@@ -5,10 +5,10 @@
 // ForwardShim::supports (the residual summed in f32, uncompensated); lane_link.rs, Link::prim (Norm{x, add, w, rows,
 // cols, eps}; the standalone Quant launch).
 //
-// How: one row per thread-block cluster of up to 8 CTAs (the kernel is latency-bound; its f64 work is spread over 8
+// How: one row per thread-block cluster of up to 8 CTAs (the kernel is latency-bound; its pair arithmetic is spread over 8
 // SMs).  A warp holds 32 consecutive values per step, so each 32-value quantisation block is one warp's registers and
-// its maximum one warp reduction.  The mean of squares is summed in f64 and the norm factor taken in f64, so y is
-// rounded to f32 once.
+// its maximum one warp reduction.  The mean of squares and the norm factor are carried to about 44 bits in pairs of
+// f32 (FP64 is slow on this part), so y is rounded to f32 once.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -40,14 +40,16 @@ struct NormParams {
 };
 
 // One row per cluster of CL CTAs (distributed shared memory, sm_90+): CTA c of the cluster owns the contiguous slice
-// [c*d/CL, (c+1)*d/CL) of the row, PER values per thread.  Each CTA sums its squares in f64; the CL partial sums are read
-// through distributed shared memory after a cluster barrier and added in rank order by every CTA, so every CTA holds
-// the same f64 norm factor and the row's f64 arithmetic is spread over CL SMs.
+// [c*d/CL, (c+1)*d/CL) of the row, PER values per thread.  Each CTA sums its squares exactly as products into a pair of
+// f32 (about 44 significant bits); the CL partial sums are read through distributed shared memory after a cluster
+// barrier and added in rank order by every CTA, so every CTA holds the same norm factor (also a pair) and rounds each
+// y = s * inv * w once.  The cluster's second barrier is split: a CTA arrives once it has read the others' sums and
+// waits only before it exits.
 template <int PER, int CL>
 __global__ void __launch_bounds__(NORM_THREADS) add_rmsnorm_kernel(const NormParams p) {
-    __shared__ double red[NORM_THREADS / 32];
-    __shared__ double part;
-    __shared__ double inv_s;
+    __shared__ F2 red[NORM_THREADS / 32];
+    __shared__ F2 part;
+    __shared__ F2 inv_s;
     cg::cluster_group cluster = cg::this_cluster();
     const int crank = (int)cluster.block_rank();
     const int r = blockIdx.x / CL;
@@ -73,7 +75,6 @@ __global__ void __launch_bounds__(NORM_THREADS) add_rmsnorm_kernel(const NormPar
         if (bad && t == 0 && crank == 0 && p.err) atomicOr(p.err, 1);
     }
     float s[PER];
-    double ss = 0.0;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
         const int i = j * NORM_THREADS + t;
@@ -81,46 +82,57 @@ __global__ void __launch_bounds__(NORM_THREADS) add_rmsnorm_kernel(const NormPar
         if (i < dl) {
             v = a[base + i];
             if (p.b) v = v + p.b[(int64_t)r * p.d + base + i];
-            ss = fma((double)v, (double)v, ss);
         }
         s[j] = v;
     }
-    ss = group_sum<32>(ss);
+    F2 ss = f2_two_prod(s[0], s[0]);
+#pragma unroll
+    for (int j = 1; j < PER; ++j) ss = f2_add(ss, f2_two_prod(s[j], s[j]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        ss = f2_add(ss, F2{__shfl_xor_sync(0xffffffffu, ss.hi, o), __shfl_xor_sync(0xffffffffu, ss.lo, o)});
     if (lane == 0) red[wid] = ss;
     __syncthreads();
     if (t == 0) {
-        double v = 0.0;
-        for (int w = 0; w < NORM_THREADS / 32; ++w) v += red[w];
+        F2 v = red[0];
+        for (int w = 1; w < NORM_THREADS / 32; ++w) v = f2_add(v, red[w]);
         part = v;
     }
     cluster.sync();
     if (t == 0) {
-        double tot = 0.0;
-        for (int c = 0; c < CL; ++c) tot += *cluster.map_shared_rank(&part, c);
-        inv_s = 1.0 / sqrt(tot / (double)p.d + (double)p.eps);
+        F2 tot = *cluster.map_shared_rank(&part, 0);
+        for (int c = 1; c < CL; ++c) tot = f2_add(tot, *cluster.map_shared_rank(&part, c));
+        // mean of squares + eps: the pair divided by d (exact remainder by FMA), then eps added
+        const float df = (float)p.d;
+        const float qh = tot.hi / df;
+        const float ql = (fmaf(-qh, df, tot.hi) + tot.lo) / df;
+        inv_s = f2_rsqrt(f2_add(f2_quick(qh, ql), F2{p.eps, 0.f}));
     }
-    cluster.sync();  // every CTA has read the others' partial sums before any CTA moves on or exits
-    if (bad) return;
-    const double inv = inv_s;
+    cluster_arrive();  // this CTA is done reading the others' shared memory
+    __syncthreads();
+    const F2 inv = inv_s;
+    if (!bad) {
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-        const int i = j * NORM_THREADS + t;
-        const bool in = i < dl;
-        const int64_t gi = (int64_t)r * p.d + base + i;
-        float y = 0.f;
-        if (in) {
-            if (p.sum) p.sum[gi] = s[j];
-            y = (float)((double)s[j] * inv * (double)wv[j]);
-            if (p.y) p.y[gi] = y;
-        }
-        // The block of 32 values lies in this warp's lanes (the slice is whole 32-value blocks when quantizing).
-        if (p.yq && (j * NORM_THREADS + wid * 32) < dl) {
-            float dsc;
-            const int8_t qv = quantize_lane(y, dsc);
-            if (in) p.yq[gi] = qv;
-            if (lane == 0) p.ys[gi / 32] = dsc;
+        for (int j = 0; j < PER; ++j) {
+            const int i = j * NORM_THREADS + t;
+            const bool in = i < dl;
+            const int64_t gi = (int64_t)r * p.d + base + i;
+            float y = 0.f;
+            if (in) {
+                if (p.sum) p.sum[gi] = s[j];
+                y = f2_mul3_round(s[j], wv[j], inv);
+                if (p.y) p.y[gi] = y;
+            }
+            // The block of 32 values lies in this warp's lanes (the slice is whole 32-value blocks when quantizing).
+            if (p.yq && (j * NORM_THREADS + wid * 32) < dl) {
+                float dsc;
+                const int8_t qv = quantize_lane(y, dsc);
+                if (in) p.yq[gi] = qv;
+                if (lane == 0) p.ys[gi / 32] = dsc;
+            }
         }
     }
+    cluster_wait();  // no CTA leaves while another may still read its shared memory
 }
 
 __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ x, int64_t nblocks,

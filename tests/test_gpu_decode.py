@@ -42,13 +42,19 @@ SMALL = dict(layers=2, d=256, heads=8, kv_heads=2, hd=128, experts=16, k=4, dff=
              rope_theta=1e6)
 
 
+# d = 160: no projection takes the TMA path or a norm prologue, so every norm is a launch of its own
+UNFUSED = dict(layers=2, d=160, heads=4, kv_heads=2, hd=128, experts=8, k=2, dff=32, vocab=300, ctx=70, eps=1e-6,
+               rope_theta=1e6)
+
+
 @pytest.mark.parametrize("mode", [0, 1])
-def test_decode_small_matches_oracle_over_steps(q8, mode):
+@pytest.mark.parametrize("cfg,launches", [(SMALL, lambda L: 6 * L + 2), (UNFUSED, lambda L: 8 * L + 3)],
+                         ids=["fused", "unfused"])
+def test_decode_small_matches_oracle_over_steps(q8, mode, cfg, launches):
     import torch
-    cfg = SMALL
     m, arr, t, tok, pos, logits = build(q8, cfg, 5, mode)
     om = oracle.ModelArrays(cfg, **arr)
-    cur_tok, cur_pos = 7, 60
+    cur_tok, cur_pos = 7, min(60, cfg["ctx"] - 5)
     tok.fill_(cur_tok)
     pos.fill_(cur_pos)
     for step in range(4):
@@ -69,6 +75,9 @@ def test_decode_small_matches_oracle_over_steps(q8, mode):
             kc = t["k_cache"][l].cpu().numpy()
             assert rel_err(kc[:, cur_pos], om.k_cache[l][:, cur_pos]) < 10 * TOL[mode]
         cur_tok, cur_pos = int(tok.item()), cur_pos + 1
+    # fused: per layer q/k/v (+norm), attention (+QK-norm, RoPE, append), O, router (+norm, top-k), gate-up, down;
+    # then LM head (+final norm) and arg-max.  Unfused adds the two norms per layer and the final norm.
+    assert m.launches_per_step() == launches(cfg["layers"])
     m.check()
     m.close()
 

@@ -246,7 +246,7 @@ def test_route_topk(q8, ws, mode, R, router_scale):
     np.testing.assert_array_equal(act[1:1 + len(active)], active)
 
 
-def _run_moe_gpu(q8, ws, md, mode, x, K, residual=None, expert_out=True, route_plan=True):
+def _run_moe_gpu(q8, ws, md, mode, x, K, residual=None, expert_out=True, route_plan=True, down_reads_h=True):
     import torch
     R, d = x.shape
     dff = md["gate"][0].shape[0] // md["router"][0].shape[0]
@@ -270,7 +270,8 @@ def _run_moe_gpu(q8, ws, md, mode, x, K, residual=None, expert_out=True, route_p
                       plan=q8.plan_struct(*pt) if route_plan else None, ws=ws)
     q8.moe_gate_up(*md["gate"], *md["up"], dff, mode, K, ids, h, x=tx, xq=xq, xs=xs, hq=hq, hs=hs, rows=R, plan=plan,
                    ws=ws)
-    q8.moe_down_combine(*md["down"], d, mode, K, ids, gates, y, h=h, hq=hq, hs=hs, rows=R, plan=plan,
+    q8.moe_down_combine(*md["down"], d, mode, K, ids, gates, y, h=h if (down_reads_h or mode == 0) else None,
+                        hq=hq, hs=hs, rows=R, plan=plan,
                         residual=dev(residual) if residual is not None else None, expert_out=eo, ws=ws)
     return dict(ids=host(ids), gates=host(gates), logits=host(logits), h=host(h).reshape(R, K, dff),
                 y=host(y), expert_out=host(eo) if expert_out else None, hq=host(hq) if hq is not None else None,
@@ -306,9 +307,9 @@ def test_moe_block_batch1(q8, ws, moe_host, moe_dev, mode):
     _compare_moe(out, ref, mode, 8)
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode,down_reads_h", [(0, True), (1, True), (1, False)])
 @pytest.mark.parametrize("spread", [False, True])
-def test_moe_one_row_fused_path(q8, ws, moe_host, moe_dev, mode, spread):
+def test_moe_one_row_fused_path(q8, ws, moe_host, moe_dev, mode, down_reads_h, spread):
     # one row, no plan, no per-expert outputs: the router and its top-k in one cluster launch, gate-up quantizing its
     # own rows, and the down-and-combine that loads its weights before waiting
     mh, md = moe_host, moe_dev
@@ -321,7 +322,9 @@ def test_moe_one_row_fused_path(q8, ws, moe_host, moe_dev, mode, spread):
         x = synth.normal((1, 2048), seed, recipes.VEC + 74)
         res = synth.normal((1, 2048), seed, recipes.VEC + 75)
         ref = oracle.moe_rows(mode, oracle.MoeWeights(2048, 768, 128, 8, **mh), x, residual=res)
-        out = _run_moe_gpu(q8, ws, md, mode, x, 8, residual=res, expert_out=False, route_plan=False)
+        # down_reads_h: f32 hidden rows staged in shared memory with the weights; else the int8 rows read directly
+        out = _run_moe_gpu(q8, ws, md, mode, x, 8, residual=res, expert_out=False, route_plan=False,
+                           down_reads_h=down_reads_h)
         assert rel_err(out["logits"][0], ref["logits"][0]) < TOL[mode]
         _compare_moe(out, ref, mode, 8)
         assert abs(out["gates"][0].sum() - 1.0) < 1e-5
