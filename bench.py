@@ -32,6 +32,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--roofline-only", action="store_true",
+                    help="only the dominant kernel's timing loop (for a profiler capture of that kernel)")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the warm-up and timed decode steps (for profiler launch lists); prints tokens/s")
     return ap.parse_args()
@@ -119,6 +121,24 @@ def make_model_tensors(cfg, seed=0):
     dev = {k: up(v) for k, v in host.items()}
     torch.cuda.synchronize()
     return host, dev
+
+
+# DRAM traffic per launch of the roofline kernel (gate_row_kernel through moe_gate_up, int8 mode), from the ncu capture
+# summarised in profiles/moe_gate_up_roofline_kernel_int8.md; valid only while the kernel's sources are the captured ones.
+ROOFLINE_TRAFFIC = {"bytes": 28345856, "sources": ["moe_add_rmsnorm_gb300/csrc/moe_row.cu",
+                                                   "moe_add_rmsnorm_gb300/csrc/common.cuh"],
+                    "sha256_16": "ec8a42926c24f74b", "profile": "profiles/moe_gate_up_roofline_kernel_int8.md"}
+
+
+def roofline_traffic(mode_int8):
+    """The captured traffic per launch, or None when the kernel changed since the capture (or in the f32 mode)."""
+    import hashlib
+    if not mode_int8:
+        return None
+    h = hashlib.sha256()
+    for f in ROOFLINE_TRAFFIC["sources"]:
+        h.update(open(os.path.join(os.path.dirname(os.path.abspath(__file__)), f), "rb").read())
+    return ROOFLINE_TRAFFIC["bytes"] if h.hexdigest()[:16] == ROOFLINE_TRAFFIC["sha256_16"] else None
 
 
 def time_dominant_kernel(q8, cfg, dev, mode, reps, stream):
@@ -255,9 +275,14 @@ def main():
     tok = torch.zeros(1, dtype=torch.int32, device="cuda")
     pos = torch.full((1,), start_pos, dtype=torch.int32, device="cuda")
     logits = torch.empty(cfg["vocab"], device="cuda")
-    model = q8.Model(cfg, dev, mode, tok, pos, logits)
     stream = torch.cuda.Stream()
     sh = stream.cuda_stream
+    if args.roofline_only:
+        dom_sec, dom_bytes = time_dominant_kernel(q8, cfg, dev, mode, reps=args.steps, stream=sh)
+        print(json.dumps({"roofline_only": True, "us_per_launch": dom_sec * 1e6, "algorithmic_bytes": dom_bytes,
+                          "gbs": dom_bytes / dom_sec / 1e9}), flush=True)
+        return
+    model = q8.Model(cfg, dev, mode, tok, pos, logits)
 
     def barrier():
         if world > 1:
@@ -347,7 +372,9 @@ def main():
         achieved = dom_bytes / dom_sec / 1e9
         line["roofline"] = {"bound": "hbm", "kernel": "moe_gate_up (8 experts x 2 x 768 rows of 2048)",
                             "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                            "traffic": None, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+                            "traffic": roofline_traffic(mode == q8.INT8ACT),
+                            "traffic_source": ROOFLINE_TRAFFIC["profile"],
+                            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
                             "us_per_launch": dom_sec * 1e6, "algorithmic_bytes_per_launch": dom_bytes}
         if not args.no_secondary:
             other = q8.F32ACT_F64SUM if mode == q8.INT8ACT else q8.INT8ACT

@@ -262,15 +262,24 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // ---- the one-word activation quantizer ------------------------------------------------------------------------
 // A warp holds one 32-value block, value `v` in lane `lane`.  d = amax / 127 and q = round-half-away(v / d), both
-// divisions IEEE-rounded f32 (never the approximate divide), q clamped to [-127, 127]; amax = 0 gives d = 0, q = 0.
+// divisions IEEE-rounded f32, q clamped to [-127, 127]; amax = 0 gives d = 0, q = 0.
+//
+// The word needs only the integer the correctly rounded quotient rounds to.  The approximate quotient (__fdividef:
+// within 2 ulp for a normal d, so within 2e-5 of v/d here, |v/d| <= 128) rounds to the same integer unless it lies
+// within 1e-4 of a half-integer; there, and for a subnormal-range d, the IEEE quotient decides.
+__device__ __forceinline__ float quant_word(float v, float d) {
+    float t = __fdividef(v, d);
+    const float a = fabsf(t);
+    if (!(d >= 1e-30f) || fabsf((a - floorf(a)) - 0.5f) <= 1e-4f) t = __fdiv_rn(v, d);
+    return fminf(fmaxf(roundf(t), -127.0f), 127.0f);
+}
+
 __device__ __forceinline__ int8_t quantize_lane(float v, float& d_out) {
     const float amax = warp_max(fabsf(v));
     const float d = __fdiv_rn(amax, 127.0f);
     d_out = d;
     if (d == 0.0f) return 0;
-    float r = roundf(__fdiv_rn(v, d));
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return (int8_t)(int)r;
+    return (int8_t)(int)quant_word(v, d);
 }
 
 // ---- pairs of f32 carrying about 44 significant bits ------------------------------------------------------------
@@ -336,9 +345,7 @@ __device__ __forceinline__ void quantize_lanes(const float (&v)[N], int8_t (&q)[
 #pragma unroll
     for (int i = 0; i < N; ++i) {
         d[i] = __fdiv_rn(m[i], 127.0f);
-        float r = d[i] == 0.0f ? 0.0f : roundf(__fdiv_rn(v[i], d[i]));
-        r = fminf(fmaxf(r, -127.0f), 127.0f);
-        q[i] = (int8_t)(int)r;
+        q[i] = d[i] == 0.0f ? (int8_t)0 : (int8_t)(int)quant_word(v[i], d[i]);
     }
 }
 

@@ -63,6 +63,30 @@ def test_quantize_bitexact(q8, rows, cols):
     np.testing.assert_array_equal(host(s), os_)
 
 
+def test_quantize_near_half_integers_bitexact(q8):
+    # blocks whose values sit exactly on, or one ulp either side of, (k + 1/2) * d for the block's own d = amax / 127:
+    # the quotients the round-half-away rule turns on
+    import torch
+    rng = np.random.default_rng(7)
+    nblk = 4096
+    amax = (10.0 ** rng.uniform(-44, 20, nblk)).astype(np.float32)  # down to subnormal scales
+    d = (amax / np.float32(127)).astype(np.float32)
+    k = rng.integers(-127, 127, (nblk, 31)).astype(np.float32)
+    base = ((k + np.float32(0.5)) * d[:, None]).astype(np.float32)
+    nudge = rng.integers(-1, 2, (nblk, 31))
+    vals = np.where(nudge < 0, np.nextafter(base, np.float32(-np.inf)),
+                    np.where(nudge > 0, np.nextafter(base, np.float32(np.inf)), base)).astype(np.float32)
+    vals = np.clip(vals, -amax[:, None], amax[:, None])
+    x = np.concatenate([amax[:, None] * np.where(rng.random((nblk, 1)) < 0.5, 1, -1).astype(np.float32), vals], 1)
+    x = x.astype(np.float32).reshape(1, nblk * 32)
+    q = empty((1, nblk * 32), torch.int8)
+    sc = empty((1, nblk), torch.float32)
+    q8.q8_quantize(dev(x), q, sc)
+    oq, os_ = oracle.quantize(x)
+    np.testing.assert_array_equal(host(sc), os_)
+    np.testing.assert_array_equal(host(q), oq)
+
+
 def oracle_golden_ties():
     import json
     import os
