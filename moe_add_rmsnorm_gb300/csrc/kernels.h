@@ -197,6 +197,12 @@ struct RouteRowCall {
 };
 bool route_row_supported(int mode, int64_t E, int64_t d, int K);
 cudaError_t launch_route_row(const RouteRowCall& c, cudaStream_t st);
+// Tensor-core products (moe_mma.cu) for a chunk's expert groups of moe_mma_min_rows()..moe_mma_max_rows() choices,
+// int8 mode: gate-up (q1 set) writes h, down writes the per-choice outputs to `out`; other groups are left alone.
+bool moe_mma_supported(const ExpertCall& c);
+int moe_mma_min_rows();
+int moe_mma_max_rows();
+cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, cudaStream_t st);
 bool gate_row_supported(const ExpertCall& c);
 cudaError_t launch_gate_row(const ExpertCall& c, Carve& ws, cudaStream_t st);
 bool down_row_supported(const ExpertCall& c);

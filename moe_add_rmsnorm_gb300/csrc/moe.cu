@@ -236,6 +236,7 @@ struct ExpertParams {
     float* expert_out;      // down out [R*K][out_rows]
     void* partial;          // down over a chunk: [R*K][out_rows] (f64 in mode 0, f32 in mode 1)
     int nrs;                // items per group (row tiles of out_rows)
+    int mma_lo, mma_hi;     // groups of mma_lo..mma_hi choices are left to the tensor-core kernel (0: none)
     L2Prefetch pf;
 };
 
@@ -285,6 +286,7 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gate_up_kernel(const ExpertPara
         const Group g = group_of(p, a);
         // an expert id outside [0, E) reads no weights and counts as an expert of zero weights
         const bool ev = g.expert >= 0 && g.expert < p.E;
+        if (p.mma_lo && ev && g.nc >= p.mma_lo && g.nc <= p.mma_hi) continue;  // on the tensor cores
         const int i0 = rs * ROWS + grp * RT;
         const int nvalid = min(RT, p.out_rows - i0);
         const int64_t wrow = (int64_t)(ev ? g.expert : 0) * p.out_rows + i0;
@@ -424,6 +426,7 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) down_group_kernel(const ExpertP
         const int a = it / p.nrs, rs = it % p.nrs;
         const Group g = group_of(p, a);
         const bool ev = g.expert >= 0 && g.expert < p.E;
+        if (p.mma_lo && ev && g.nc >= p.mma_lo && g.nc <= p.mma_hi) continue;  // on the tensor cores
         const int o0 = rs * ROWS + grp * RT;
         const int nvalid = min(RT, p.out_rows - o0);
         WTile<BPL, RT> t;
@@ -625,8 +628,15 @@ cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     const EPlan pl = eplan(c.mode, (int)(c.k / 32), c.mode == 0 ? 2 : 4);
     ExpertParams p = make_params(c, pl);
     (void)ws;
+    const bool mma = moe_mma_supported(c);
+    if (mma) {
+        p.mma_lo = moe_mma_min_rows();
+        p.mma_hi = moe_mma_max_rows();
+    }
     const int64_t warps = (int64_t)max_groups(c) * p.nrs;
-    return c.mode == 0 ? run_gate_up<0>(c, pl, p, warps, st) : run_gate_up<1>(c, pl, p, warps, st);
+    cudaError_t e = c.mode == 0 ? run_gate_up<0>(c, pl, p, warps, st) : run_gate_up<1>(c, pl, p, warps, st);
+    if (e == cudaSuccess && mma) e = launch_moe_mma(c, c.h, max_groups(c), st);  // the groups of >= 16 choices
+    return e;
 }
 
 cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st) {
@@ -647,8 +657,14 @@ cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st)
     ExpertParams p = make_params(c, pl);
     p.partial = ws.take<char>((size_t)c.R * c.K * c.out_rows * (c.mode == 0 ? 8 : 4));
     if (ws.overflow) return cudaErrorMemoryAllocation;
+    const bool mma = moe_mma_supported(c);
+    if (mma) {
+        p.mma_lo = moe_mma_min_rows();
+        p.mma_hi = moe_mma_max_rows();
+    }
     const int64_t warps = (int64_t)max_groups(c) * p.nrs;
     cudaError_t e = c.mode == 0 ? run_down_group<0>(c, pl, p, warps, st) : run_down_group<1>(c, pl, p, warps, st);
+    if (e == cudaSuccess && mma) e = launch_moe_mma(c, reinterpret_cast<float*>(p.partial), max_groups(c), st);
     if (e != cudaSuccess) return e;
     const int64_t n = c.R * c.out_rows;
     int cg = (int)((n + 255) / 256);

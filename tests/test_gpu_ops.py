@@ -406,16 +406,29 @@ def test_moe_chunk(q8, ws, moe_host, moe_dev, mode, R):
     _compare_moe(out, ref, mode, 8)
 
 
-@pytest.mark.parametrize("mode", [0, 1])
-def test_moe_chunk_correlated_rows(q8, ws, moe_host, moe_dev, mode):
-    # every row near one x0: the rows share their experts, so each expert's group holds all 32 rows
-    R = 32
+@pytest.mark.parametrize("mode,R", [(0, 32), (1, 16), (1, 32), (1, 64)])
+def test_moe_chunk_correlated_rows(q8, ws, moe_host, moe_dev, mode, R):
+    # every row near one x0: the rows share their experts, so each expert's group holds all R rows (int8 mode: the
+    # tensor-core products, groups of 16 to 64 rows)
     x0 = synth.normal((1, 2048), 2, recipes.VEC + 81)
     x = (x0 + 0.01 * synth.normal((R, 2048), 2, recipes.VEC + 82)).astype(np.float32)
     w = oracle.MoeWeights(2048, 768, 128, 8, **moe_host)
     ref = oracle.moe_rows(mode, w, x)
     out = _run_moe_gpu(q8, ws, moe_dev, mode, x, 8)
     _compare_moe(out, ref, mode, 8)
+
+
+def test_moe_chunk_two_clusters_mixed_groups(q8, ws, moe_host, moe_dev):
+    # 40 rows near x0 and 8 near x1: x0's experts get groups of 40 (tensor cores), x1's groups of 8 (CUDA cores),
+    # experts both clusters choose get 48
+    x0 = synth.normal((1, 2048), 5, recipes.VEC + 84)
+    x1 = synth.normal((1, 2048), 5, recipes.VEC + 85)
+    x = np.concatenate([x0 + 0.01 * synth.normal((40, 2048), 5, recipes.VEC + 86),
+                        x1 + 0.01 * synth.normal((8, 2048), 5, recipes.VEC + 87)]).astype(np.float32)
+    w = oracle.MoeWeights(2048, 768, 128, 8, **moe_host)
+    ref = oracle.moe_rows(1, w, x)
+    out = _run_moe_gpu(q8, ws, moe_dev, 1, x, 8)
+    _compare_moe(out, ref, 1, 8)
 
 
 def test_moe_chunk_equals_rows_one_by_one(q8, ws, moe_dev):
