@@ -35,6 +35,14 @@ __device__ __forceinline__ void ld_block_shared_use(const int8_t* p, uint32_t (&
                  : "l"(p));
 }
 
+// A read-only f32 load whose issue order the compiler keeps relative to the other volatile loads: used for the few
+// small values a kernel needs early, issued before its bulk weight loads so they do not queue behind them.
+__device__ __forceinline__ float ld_f32_early(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ float ld_scale_stream(const float* p) {
     float v;
     asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
@@ -264,22 +272,56 @@ __device__ __forceinline__ float warp_max(float v) {
 // A warp holds one 32-value block, value `v` in lane `lane`.  d = amax / 127 and q = round-half-away(v / d), both
 // divisions IEEE-rounded f32, q clamped to [-127, 127]; amax = 0 gives d = 0, q = 0.
 //
+// d: the product by fl32(1/127) corrected by one FMA residual step, which equals the IEEE quotient for every
+// non-negative finite float (checked exhaustively on the host over all 2,139,095,040 of them).
+__device__ __forceinline__ float div127(float a) {
+    const float c = 1.0f / 127.0f;
+    const float q = __fmul_rn(a, c);
+    return fmaf(fmaf(-q, 127.0f, a), c, q);
+}
+
 // The word needs only the integer the correctly rounded quotient rounds to.  The approximate quotient (__fdividef:
 // within 2 ulp for a normal d, so within 2e-5 of v/d here, |v/d| <= 128) rounds to the same integer unless it lies
 // within 1e-4 of a half-integer; there, and for a subnormal-range d, the IEEE quotient decides.
-__device__ __forceinline__ float quant_word(float v, float d) {
-    float t = __fdividef(v, d);
+__device__ __forceinline__ bool quotient_near_tie(float t, float d) {
     const float a = fabsf(t);
-    if (!(d >= 1e-30f) || fabsf((a - floorf(a)) - 0.5f) <= 1e-4f) t = __fdiv_rn(v, d);
-    return fminf(fmaxf(roundf(t), -127.0f), 127.0f);
+    return d != 0.0f && (!(d >= 1e-30f) || fabsf((a - floorf(a)) - 0.5f) <= 1e-4f);
+}
+
+// N independent blocks at once (block i's value of this lane in v[i]): the N warp reductions interleaved, the
+// quotients from reciprocals, and the IEEE division only on the rare warp that has a quotient near a half-integer.
+template <int N>
+__device__ __forceinline__ void quantize_lanes(const float (&v)[N], int8_t (&q)[N], float (&d)[N]) {
+    float m[N], t[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) m[i] = fabsf(v[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < N; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
+    bool near = false;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        d[i] = div127(m[i]);
+        t[i] = __fdividef(v[i], d[i]);
+        near |= quotient_near_tie(t[i], d[i]);
+    }
+    if (__any_sync(0xffffffffu, near)) {  // warp-uniform, rare
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (quotient_near_tie(t[i], d[i])) t[i] = __fdiv_rn(v[i], d[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) q[i] = d[i] == 0.0f ? (int8_t)0 : (int8_t)(int)fminf(fmaxf(roundf(t[i]), -127.0f), 127.0f);
 }
 
 __device__ __forceinline__ int8_t quantize_lane(float v, float& d_out) {
-    const float amax = warp_max(fabsf(v));
-    const float d = __fdiv_rn(amax, 127.0f);
-    d_out = d;
-    if (d == 0.0f) return 0;
-    return (int8_t)(int)quant_word(v, d);
+    const float vv[1] = {v};
+    int8_t q[1];
+    float d[1];
+    quantize_lanes<1>(vv, q, d);
+    d_out = d[0];
+    return q[0];
 }
 
 // ---- pairs of f32 carrying about 44 significant bits ------------------------------------------------------------
@@ -329,24 +371,6 @@ __device__ __forceinline__ float f2_mul3_round(float a, float b, F2 inv) {
     const F2 y = f2_two_prod(p.hi, inv.hi);
     const float lo = y.lo + fmaf(p.hi, inv.lo, p.lo * inv.hi);
     return y.hi + lo;
-}
-
-// N independent blocks at once (block i's value of this lane in v[i]): the same arithmetic as quantize_lane, with the N
-// warp reductions interleaved so their shuffles overlap.
-template <int N>
-__device__ __forceinline__ void quantize_lanes(const float (&v)[N], int8_t (&q)[N], float (&d)[N]) {
-    float m[N];
-#pragma unroll
-    for (int i = 0; i < N; ++i) m[i] = fabsf(v[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int i = 0; i < N; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        d[i] = __fdiv_rn(m[i], 127.0f);
-        q[i] = d[i] == 0.0f ? (int8_t)0 : (int8_t)(int)quant_word(v[i], d[i]);
-    }
 }
 
 // ---- SiLU -------------------------------------------------------------------------------------------------------

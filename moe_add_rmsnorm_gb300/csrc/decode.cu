@@ -202,6 +202,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attention_kernel(const AttnPar
         if ((len < 1 || len > p.ctx) && g == 0 && chunk == 0 && t == 0 && p.err) atomicOr(p.err, 2);
         return;
     }
+    // QK-norm and RoPE constants for this position, read first (before the bulk of the cache rows): thread t takes
+    // the pair (i, i + 64) of query heads t/64 and t/64 + 4 (and of the key head when t < 64)
+    const int hsub = t >> 6, pi = t & 63;
+    const int pos = len - 1;
+    const float cs = ld_f32_early(p.cos_t + (int64_t)pos * (ATT_HD / 2) + pi);
+    const float sn = ld_f32_early(p.sin_t + (int64_t)pos * (ATT_HD / 2) + pi);
+    const float qw0 = ld_f32_early(p.q_norm + pi), qw1 = ld_f32_early(p.q_norm + pi + ATT_HD / 2);
+    const float kw0 = ld_f32_early(p.k_norm + pi), kw1 = ld_f32_early(p.k_norm + pi + ATT_HD / 2);
     const int p0 = chunk * ATT_CHUNK;
     const int np = max(0, min(ATT_CHUNK, len - p0));
     const int newrow = len - 1 - p0;  // the row this step writes, if it falls in this chunk
@@ -233,13 +241,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attention_kernel(const AttnPar
         vr[u] = (pl < np && pl != newrow) ? __ldcs(reinterpret_cast<const float4*>(vb + (int64_t)pl * ATT_HD) + lane)
                                           : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    // QK-norm and RoPE constants for this position: thread t takes the pair (i, i + 64) of query heads t/64 and
-    // t/64 + 4 (and of the key head when t < 64)
-    const int hsub = t >> 6, pi = t & 63;
-    const int pos = len - 1;
-    const float cs = p.cos_t[(int64_t)pos * (ATT_HD / 2) + pi], sn = p.sin_t[(int64_t)pos * (ATT_HD / 2) + pi];
-    const float qw0 = p.q_norm[pi], qw1 = p.q_norm[pi + ATT_HD / 2];
-    const float kw0 = p.k_norm[pi], kw1 = p.k_norm[pi + ATT_HD / 2];
     const bool has_new = newrow >= 0 && newrow < np;  // CTA-uniform
     griddep_wait();
     griddep_launch();

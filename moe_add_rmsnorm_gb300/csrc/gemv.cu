@@ -198,8 +198,14 @@ __global__ void __launch_bounds__(TMA_THREADS, 1) gemv_tma_kernel(const TmaParam
         rows = min(tp.tr, p.n[sg] - row0);
     };
 
+    const NormIn& ni = tp.ni;
+    const bool norm = ni.a != nullptr;  // grid-uniform
+    constexpr int NP = 2 * KCH;         // 256-value rounds of the row: k <= 512 * KCH
+    float nw[NP];
     if (wid == TMA_CONSUMERS) {
-        // producer: weights only, so it never waits for earlier kernels
+        // producer: weights only, so it never waits for earlier kernels; with a norm prologue it first lets the
+        // consumers issue their norm-weight loads, so those do not queue behind the bulk copies
+        if (norm) asm volatile("bar.sync 2, %0;" ::"n"(TMA_THREADS));
         if (lane == 0) {
             for (int i = 0; i < nmine; ++i) {
                 const int s = i % tp.ns;
@@ -216,16 +222,14 @@ __global__ void __launch_bounds__(TMA_THREADS, 1) gemv_tma_kernel(const TmaParam
         return;
     }
 
-    const NormIn& ni = tp.ni;
-    const bool norm = ni.a != nullptr;  // grid-uniform
-    constexpr int NP = 2 * KCH;         // 256-value rounds of the row: k <= 512 * KCH
-    float nw[NP];
-    if (norm)
+    if (norm) {
 #pragma unroll
         for (int j = 0; j < NP; ++j) {
             const int i = threadIdx.x + TMA_CONSUMERS * 32 * j;
-            nw[j] = i < k ? ni.w[i] : 0.f;
+            nw[j] = i < k ? ld_f32_early(ni.w + i) : 0.f;
         }
+        asm volatile("bar.arrive 2, %0;" ::"n"(TMA_THREADS));
+    }
     griddep_wait();
     griddep_launch();
     const float* xfp = p.x;

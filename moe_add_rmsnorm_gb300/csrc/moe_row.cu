@@ -89,6 +89,15 @@ __global__ void __launch_bounds__(RR_THREADS) route_row_kernel(const RouteRowPar
         bval[j] = bidx[j] < p.nb;
     }
     issue_l2_prefetch(p.pf);
+    const bool norm = p.norm_a != nullptr;  // grid-uniform
+    constexpr int NP = 4 * BPL;             // 256-value rounds of the row: d <= 1024 * BPL
+    float nw[NP];                           // the norm weight, read before the router rows
+    if (norm)
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const int i = threadIdx.x + RR_THREADS * j;
+            nw[j] = i < p.d ? ld_f32_early(p.norm_w + i) : 0.f;
+        }
     WTile<BPL, 1> t[RR_RW];
 #pragma unroll
     for (int u = 0; u < RR_RW; ++u) {
@@ -96,15 +105,6 @@ __global__ void __launch_bounds__(RR_THREADS) route_row_kernel(const RouteRowPar
         const bool v = lr < rpc && r0 + lr < p.E;
         load_tile<BPL, 1>(t[u], p.q, p.s, v ? r0 + lr : 0, v ? 1 : 0, p.d, p.nb, bidx, bval);
     }
-    const bool norm = p.norm_a != nullptr;  // grid-uniform
-    constexpr int NP = 4 * BPL;             // 256-value rounds of the row: d <= 1024 * BPL
-    float nw[NP];
-    if (norm)
-#pragma unroll
-        for (int j = 0; j < NP; ++j) {
-            const int i = threadIdx.x + RR_THREADS * j;
-            nw[j] = i < p.d ? p.norm_w[i] : 0.f;
-        }
     griddep_wait();  // the activation (or the row it is normed from) comes from the previous launch
     griddep_launch();
     const float* xf = p.x;
@@ -397,6 +397,9 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
     float sw[PPL], g[PPL];
     int xo[PPL];  // the pair's first value in the hidden rows: j*k + 32*b
     issue_l2_prefetch(p.pf);
+    // the residual row was written three launches back, before the launch before this one passed its wait: read
+    // first, ahead of the weight rows
+    const float res = (p.residual && orow && lane == 0) ? ld_f32_early(p.residual + o) : 0.f;
     // the routing was written two launches back, before the previous kernel passed its own wait
 #pragma unroll
     for (int i = 0; i < PPL; ++i) {
@@ -417,8 +420,6 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
             sw[i] = 0.f;
         }
     }
-    // the residual row was written three launches back, before the launch before this one passed its wait
-    const float res = (p.residual && orow && lane == 0) ? __ldcg(p.residual + o) : 0.f;
     griddep_wait();  // the hidden rows come from the previous launch
     griddep_launch();
     const int8_t* hq = p.hq;
