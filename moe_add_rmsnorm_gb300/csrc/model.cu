@@ -49,7 +49,6 @@ struct q8_model {
     cudaGraphExec_t exec = nullptr;
     int64_t kernels_per_step = 0;  // kernel nodes of the captured step
     int pdl = 1;       // programmatic dependent launch between the step's kernels
-    int prefetch = 1;  // weights fetched into L2 ahead of the launches that read them
 };
 
 namespace {
@@ -69,11 +68,6 @@ T* carve_arena(char*& at, size_t n) {
     uintptr_t p = ((uintptr_t)at + 255) & ~uintptr_t(255);
     at = (char*)(p + n * sizeof(T));
     return (T*)p;
-}
-
-void add_mat(L2Prefetch& pf, const q8_mat& w) {
-    pf.add(w.q, (size_t)(w.rows * w.cols));
-    pf.add(w.s, (size_t)(w.rows * (w.cols / 32)) * sizeof(float));
 }
 
 Carve fresh_carve(q8_model* m) {
@@ -276,11 +270,6 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             }
             c.pdl = pdl;
             c.err = m->err;
-            if (m->prefetch && l + 1 < d.layers) {  // the next layer's q, k and v projections
-                add_mat(c.pf, m->wq[l + 1]);
-                add_mat(c.pf, m->wk[l + 1]);
-                add_mat(c.pf, m->wv[l + 1]);
-            }
             Q8_TRY(launch_gate_up(c, cv, st));
         }
         {
