@@ -202,7 +202,7 @@ cudaError_t launch_route_row(const RouteRowCall& c, cudaStream_t st);
 bool moe_mma_supported(const ExpertCall& c);
 int moe_mma_min_rows();
 int moe_mma_max_rows();
-cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, cudaStream_t st);
+cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carve& ws, cudaStream_t st);
 bool gate_row_supported(const ExpertCall& c);
 cudaError_t launch_gate_row(const ExpertCall& c, Carve& ws, cudaStream_t st);
 bool down_row_supported(const ExpertCall& c);

@@ -627,7 +627,6 @@ cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     // gate and up tiles are both in flight: about four (f32) or eight (int8) 32-byte loads per lane in all
     const EPlan pl = eplan(c.mode, (int)(c.k / 32), c.mode == 0 ? 2 : 4);
     ExpertParams p = make_params(c, pl);
-    (void)ws;
     const bool mma = moe_mma_supported(c);
     if (mma) {
         p.mma_lo = moe_mma_min_rows();
@@ -635,7 +634,7 @@ cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     }
     const int64_t warps = (int64_t)max_groups(c) * p.nrs;
     cudaError_t e = c.mode == 0 ? run_gate_up<0>(c, pl, p, warps, st) : run_gate_up<1>(c, pl, p, warps, st);
-    if (e == cudaSuccess && mma) e = launch_moe_mma(c, c.h, max_groups(c), st);  // the groups of >= 16 choices
+    if (e == cudaSuccess && mma) e = launch_moe_mma(c, c.h, max_groups(c), ws, st);  // the groups of >= 16 choices
     return e;
 }
 
@@ -664,7 +663,7 @@ cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st)
     }
     const int64_t warps = (int64_t)max_groups(c) * p.nrs;
     cudaError_t e = c.mode == 0 ? run_down_group<0>(c, pl, p, warps, st) : run_down_group<1>(c, pl, p, warps, st);
-    if (e == cudaSuccess && mma) e = launch_moe_mma(c, reinterpret_cast<float*>(p.partial), max_groups(c), st);
+    if (e == cudaSuccess && mma) e = launch_moe_mma(c, reinterpret_cast<float*>(p.partial), max_groups(c), ws, st);
     if (e != cudaSuccess) return e;
     const int64_t n = c.R * c.out_rows;
     int cg = (int)((n + 255) / 256);

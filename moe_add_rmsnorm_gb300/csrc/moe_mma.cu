@@ -11,12 +11,16 @@
 // converted to f16 in shared memory — exactly: every |v| <= 127 is an f16 integer, every product is exact in the f32
 // accumulator and so is every 32-value block sum (|D| <= 516,128 < 2^24).  For each 32-value block the tile's D
 // (128 weight rows x N group rows) is formed by two tcgen05.mma kind::f16 (K = 16) into a tensor-memory accumulator of
-// its own; the warpgroup reads it back with tcgen05.ld and adds s_w * s_x * D into registers, the block order and the
-// f32 arithmetic of the int8 mode.  Raw int8 tiles stream into a ring of shared-memory stages by cp.async three
-// stages ahead; each stage (two blocks) is converted to f16 by a byte permute (exact) into one of two operand buffers,
-// and its MMAs run while the previous stage's accumulators (two TMEM buffers) are read back.  Operands use the
-// no-swizzle K-major layout of 8-row x 16-byte core matrices.
+// its own; four warps per TMEM lane quarter read it back with tcgen05.ld (each a quarter of the columns) and add
+// s_w * s_x * D into registers, the block order and the f32 arithmetic of the int8 mode.  Raw int8 tiles stream into a
+// ring of shared-memory stages by cp.async four stages ahead; each stage (two blocks) is converted to f16 by a byte
+// permute (exact) into one of two operand buffers, and its MMAs run while the previous stage's accumulators (two TMEM
+// buffers) are read back.  Operands use the no-swizzle K-major layout of 8-row x 16-byte core matrices.  One CTA per
+// SM walks the items (group, 128-row tile, k slice) of the groups it takes; the k split is chosen per call from the
+// number of such groups, and the last slice of a tile to finish adds the slices' partial sums in slice order.
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -26,12 +30,15 @@ namespace q8 {
 namespace {
 
 constexpr int MM_M = 128;        // weight rows per tile: the MMA's M, one TMEM lane per thread
-constexpr int MM_THREADS = 128;
+constexpr int MM_THREADS = 512;  // 16 warps: warp w reads TMEM lanes 32*(w%4).., column chunks w/4, w/4+4, ...
+constexpr int MM_CG = MM_THREADS / MM_M;  // column groups
 constexpr int MM_NMAX = 64;      // group rows the kernel takes
 constexpr int MM_MIN = 16;       // smaller groups stay on the CUDA cores
 constexpr int MM_CORE = 128;     // bytes of one core matrix (8 rows x 16 bytes)
 constexpr int MM_BPS = 2;        // 32-value blocks per pipeline stage (K = 64)
-constexpr int MM_RING = 4;       // raw stages in flight (cp.async)
+constexpr int MM_RING = 5;       // raw stages in the ring (cp.async, MM_RING - 1 in flight)
+constexpr int MM_SMAX = 4;       // k slices per (group, tile) at most
+constexpr int MM_GCAP = 256;     // eligible groups listed in shared memory (beyond: found by a scan)
 constexpr int MM_ROWB = MM_BPS * 32;                 // bytes of one raw row of a stage (int8)
 constexpr int MM_KG = MM_BPS * 4;                    // f16 k-groups (core matrices) along K per stage
 constexpr int MM_SBO = MM_KG * MM_CORE;              // bytes between row groups of an operand tile
@@ -39,7 +46,7 @@ constexpr int MM_SBO = MM_KG * MM_CORE;              // bytes between row groups
 constexpr int MM_RAW_W = 2 * MM_M * MM_ROWB;
 constexpr int MM_RAW_X = MM_NMAX * MM_ROWB;
 constexpr int MM_RAW_SW = 2 * MM_M * MM_BPS * 4;
-constexpr int MM_RAW_SX = MM_NMAX * MM_BPS * 4;
+constexpr int MM_RAW_SX = MM_BPS * MM_NMAX * 4;  // block-major: [block][row]
 constexpr int MM_RAW = MM_RAW_W + MM_RAW_X + MM_RAW_SW + MM_RAW_SX;
 // operand buffer (f16, core-matrix layout): A per matrix [128 x 64], B [64 x 64]
 constexpr int MM_OPA = MM_M * MM_ROWB * 2;
@@ -62,6 +69,9 @@ struct MmaParams {
     const float* xs;
     float* out;          // gate-up: h [R*K][out_rows]; down: part [R*K][out_rows]
     int tiles;           // out_rows / 128
+    int S;               // k slices per (group, tile) at most (scratch holds that many); 1: no split
+    float* part;         // S > 1: [slots][tiles][S][2][64][128] scaled partial sums
+    int* cnt;            // S > 1: [slots][tiles] arrivals (left zero)
     int* err;
 };
 
@@ -87,15 +97,17 @@ __device__ __forceinline__ void mm_commit(uint64_t* bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(taddr));
 }
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp8(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
@@ -114,55 +126,99 @@ __device__ __forceinline__ void i8x4_to_h(uint32_t w, uint32_t& lo, uint32_t& hi
     hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
-// One raw row of a stage (64 int8 = MM_BPS blocks) into f16 operand row r: row r lives in core row-group r/8, row
-// r%8; its k-group g (values 8g..8g+7) at ((r/8) * MM_KG + g) * 128 + (r%8) * 16.
-__device__ __forceinline__ void convert_row(unsigned char* op, int r, const unsigned char* raw) {
-    unsigned char* base = op + (size_t)(r >> 3) * MM_SBO + (r & 7) * 16;
+// 16 int8 (quarter q of a raw row of a stage) into f16 operand row r, k-groups 2q and 2q+1: row r lives in core
+// row-group r/8, row r%8; its k-group g (values 8g..8g+7) at (r/8) * MM_SBO + g * 128 + (r%8) * 16.
+__device__ __forceinline__ void convert_quarter(unsigned char* op, int r, int q, const unsigned char* raw) {
+    unsigned char* base = op + (size_t)(r >> 3) * MM_SBO + (r & 7) * 16 + 2 * q * MM_CORE;
+    const uint4 v = *reinterpret_cast<const uint4*>(raw);
+    uint4 o0, o1;
+    i8x4_to_h(v.x, o0.x, o0.y);
+    i8x4_to_h(v.y, o0.z, o0.w);
+    i8x4_to_h(v.z, o1.x, o1.y);
+    i8x4_to_h(v.w, o1.z, o1.w);
+    *reinterpret_cast<uint4*>(base) = o0;
+    *reinterpret_cast<uint4*>(base + MM_CORE) = o1;
+}
+
+__device__ __forceinline__ void zero_quarter(unsigned char* op, int r, int q) {
+    unsigned char* base = op + (size_t)(r >> 3) * MM_SBO + (r & 7) * 16 + 2 * q * MM_CORE;
+    *reinterpret_cast<uint4*>(base) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(base + MM_CORE) = make_uint4(0, 0, 0, 0);
+}
+
+// Whether active group a is one this kernel takes (its expert id valid, MM_MIN..MM_NMAX rows).
+__device__ __forceinline__ bool mm_eligible(const MmaParams& p, int a) {
+    const int e = __ldg(p.active + 1 + a);
+    if (e < 0 || e >= p.E) return false;
+    const int n = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+    return n >= MM_MIN && n <= MM_NMAX;
+}
+
+// Warp-wide scan of the active groups in order: returns how many are eligible; the first MM_GCAP go to list (when
+// given) and the index of the target-th (0-based) to *found (when target >= 0 and it exists).
+__device__ int mm_scan(const MmaParams& p, int nact, int* list, int target, int* found) {
+    const int lane = threadIdx.x & 31;
+    int count = 0;
+    for (int a0 = 0; a0 < nact; a0 += 128) {
+        bool el[4];
 #pragma unroll
-    for (int q = 0; q < MM_ROWB / 16; ++q) {  // 16 int8 = two k-groups
-        const uint4 v = *reinterpret_cast<const uint4*>(raw + 16 * q);
-        uint4 o0, o1;
-        i8x4_to_h(v.x, o0.x, o0.y);
-        i8x4_to_h(v.y, o0.z, o0.w);
-        i8x4_to_h(v.z, o1.x, o1.y);
-        i8x4_to_h(v.w, o1.z, o1.w);
-        *reinterpret_cast<uint4*>(base + (2 * q) * MM_CORE) = o0;
-        *reinterpret_cast<uint4*>(base + (2 * q + 1) * MM_CORE) = o1;
+        for (int u = 0; u < 4; ++u) {  // four chunks' loads in flight
+            const int a = a0 + 32 * u + lane;
+            el[u] = a < nact && mm_eligible(p, a);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const unsigned bal = __ballot_sync(0xffffffffu, el[u]);
+            const int pos = count + __popc(bal & ((1u << lane) - 1u));
+            if (el[u] && list && pos < MM_GCAP) list[pos] = a0 + 32 * u + lane;
+            if (el[u] && pos == target) *found = a0 + 32 * u + lane;
+            count += __popc(bal);
+        }
     }
+    return count;
 }
 
-__device__ __forceinline__ void zero_row(unsigned char* op, int r) {
-    unsigned char* base = op + (size_t)(r >> 3) * MM_SBO + (r & 7) * 16;
-#pragma unroll
-    for (int g = 0; g < MM_KG; ++g) *reinterpret_cast<uint4*>(base + g * MM_CORE) = make_uint4(0, 0, 0, 0);
-}
-
-// CTA (group a, tile t): weight rows t*128 .. t*128+127 of the group's expert against the group's n rows (16 <= n <= 64).
+// Persistent: the work is the items (eligible group g, tile, k slice) in that order, CTA b taking items b,
+// b + gridDim.x, ...; an item covers weight rows tile*128 .. tile*128+127 of group g's expert against the group's n rows
+// (16 <= n <= 64), k stages [slice*nst/S, (slice+1)*nst/S), S chosen per call from the number of eligible groups.
 // Stage i covers blocks 2i, 2i+1: its raw bytes arrive by cp.async up to MM_RING - 1 stages ahead (a ring slot is
-// refilled once the stage it held has been read back, its scales included); the threads convert them
-// to f16 operands (two buffers), thread 0 issues four MMAs per matrix (two per block, K = 16 each) into the stage's
-// TMEM buffer, and stage i-1's accumulators are read back and scaled while stage i's MMAs run.
+// refilled once the stage it held has been read back, its scales included); the threads convert them to f16 operands
+// (two buffers), thread 0 issues two MMAs per block and matrix (K = 16 each) into the stage's TMEM buffer, and the
+// previous stage's accumulators are read back and scaled while these MMAs run.  TMEM, operand buffers and the two MMA
+// barriers carry on from item to item (a running stage count gives buffers and phases).
 __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams p) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t bar[2];
     __shared__ uint32_t tmem_base;
     __shared__ int rows_s[MM_NMAX];  // each group row's activation row
     __shared__ int choice_s[MM_NMAX];
-    const int t = threadIdx.x, w = t >> 5;
-    const int a = blockIdx.x / p.tiles, tile = blockIdx.x % p.tiles;
+    __shared__ int glist[MM_GCAP];   // the first eligible groups' indices in the active list
+    __shared__ int nelig_s, a_s, last_s;
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    const int r = 32 * (w & 3) + lane;  // this thread's tile row (its TMEM lane)
+    const int cg = w >> 2;              // its column group
     griddep_wait();
     griddep_launch();
-    if (a >= __ldg(p.active)) return;
-    const int e = __ldg(p.active + 1 + a);
-    if (e < 0 || e >= p.E) return;
-    const int c0 = __ldg(p.offsets + e), n = __ldg(p.offsets + e + 1) - c0;
-    if (n < MM_MIN || n > MM_NMAX) return;  // CTA-uniform: the CUDA-core kernel takes the group
-    const int N = (n + 15) & ~15;
-    if (t < n) {
-        const int c = __ldg(p.lists + c0 + t);
-        choice_s[t] = c;
-        rows_s[t] = p.gate_up ? c / p.K : c;
+    const int nact = __ldg(p.active);
+    if (w == 0) {
+        const int c = mm_scan(p, nact, glist, -1, nullptr);
+        if (lane == 0) nelig_s = c;
     }
+    __syncthreads();
+    const int nelig = nelig_s;
+    const int nst_all = p.nb / MM_BPS;
+    // k slices: the fewest rounds of items over the grid times the stages per item (plus two for fill and epilogue)
+    int S = 1;
+    {
+        int64_t best = -1;
+        for (int s = 1; s <= p.S; ++s) {
+            const int64_t its = (int64_t)nelig * p.tiles * s;
+            const int64_t cost = ((its + gridDim.x - 1) / gridDim.x) * ((nst_all + s - 1) / s + 2);
+            if (best < 0 || cost < best) best = cost, S = s;
+        }
+    }
+    const int items = nelig * p.tiles * S;
+    if ((int)blockIdx.x >= items) return;
     if (t == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
@@ -178,130 +234,218 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams 
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base;
     const int mats = p.gate_up ? 2 : 1;
-    const int64_t wrow = (int64_t)e * p.out_rows + (int64_t)tile * MM_M + t;  // this thread's weight row
-    const int xrow = t < n ? rows_s[t] : 0;
-    const uint32_t idesc = mm_idesc(N);
-    const int nst = p.nb / MM_BPS;
     unsigned char* raw = smem;
     unsigned char* ops = smem + (size_t)MM_RING * MM_RAW;
+    uint32_t gs = 0;  // stages this CTA has run
+    bool ok = true;
 
-    // this thread's share of raw stage i: its weight row(s) and scales, its group row and scales
-    auto fetch = [&](int i) {
-        unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
-        const int b0 = i * MM_BPS;
-        for (int m = 0; m < mats; ++m) {
-            const int8_t* q = (m == 0 ? p.q0 : p.q1) + wrow * p.k + 32 * b0;
-            unsigned char* d = st + (size_t)(m * MM_M + t) * MM_ROWB;
-#pragma unroll
-            for (int u = 0; u < MM_ROWB / 16; ++u) cp16(d + 16 * u, q + 16 * u);
-            cp8(st + MM_RAW_W + MM_RAW_X + (size_t)(m * MM_M + t) * MM_BPS * 4, (m == 0 ? p.s0 : p.s1) + wrow * p.nb + b0);
+    for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+        const int g = item / (p.tiles * S), tile = (item / S) % p.tiles, slice = item % S;
+        if (g >= MM_GCAP && w == 0) {  // beyond the listed groups: scan for it
+            int found = 0;
+            mm_scan(p, nact, nullptr, g, &found);
+            found = __reduce_max_sync(0xffffffffu, found);
+            if (lane == 0) a_s = found;
         }
+        __syncthreads();
+        const int a = g < MM_GCAP ? glist[g] : a_s;
+        const int e = __ldg(p.active + 1 + a);
+        const int c0 = __ldg(p.offsets + e), n = __ldg(p.offsets + e + 1) - c0;
         if (t < n) {
-            const int8_t* x = p.xq + (int64_t)xrow * p.k + 32 * b0;
-            unsigned char* d = st + MM_RAW_W + (size_t)t * MM_ROWB;
-#pragma unroll
-            for (int u = 0; u < MM_ROWB / 16; ++u) cp16(d + 16 * u, x + 16 * u);
-            cp8(st + MM_RAW_W + MM_RAW_X + MM_RAW_SW + (size_t)t * MM_BPS * 4, p.xs + (int64_t)xrow * p.nb + b0);
+            const int c = __ldg(p.lists + c0 + t);
+            choice_s[t] = c;
+            rows_s[t] = p.gate_up ? c / p.K : c;
         }
-    };
+        __syncthreads();
+        const int N = (n + 15) & ~15;
+        const int64_t wbase = (int64_t)e * p.out_rows + (int64_t)tile * MM_M;  // the tile's first weight row
+        const uint32_t idesc = mm_idesc(N);
+        const int st0 = slice * nst_all / S, nst = (slice + 1) * nst_all / S - st0;  // this item's stages
 
-    float acc0[MM_NMAX], acc1[MM_NMAX];
-#pragma unroll
-    for (int j = 0; j < MM_NMAX; ++j) acc0[j] = acc1[j] = 0.f;
+        // raw stage i (block-major scales for the rows, so a read-back loads four rows' scales at once)
+        auto fetch = [&](int i) {
+            unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
+            const int b0 = (st0 + i) * MM_BPS;
+            for (int task = t; task < mats * MM_M * 4; task += MM_THREADS) {  // weight row quarters
+                const int m = task / (MM_M * 4), wr = (task >> 2) & (MM_M - 1), q = task & 3;
+                const int8_t* src = (m == 0 ? p.q0 : p.q1) + (wbase + wr) * p.k + 32 * b0 + 16 * q;
+                cp16(st + (size_t)(m * MM_M + wr) * MM_ROWB + 16 * q, src);
+            }
+            if (t < mats * MM_M) {  // weight scales
+                const int m = t / MM_M, wr = t & (MM_M - 1);
+                cp8(st + MM_RAW_W + MM_RAW_X + (size_t)(m * MM_M + wr) * MM_BPS * 4,
+                    (m == 0 ? p.s0 : p.s1) + (wbase + wr) * p.nb + b0);
+            }
+            if (t < 4 * n) {  // group row quarters
+                const int xr = t >> 2, q = t & 3;
+                cp16(st + MM_RAW_W + (size_t)xr * MM_ROWB + 16 * q, p.xq + (int64_t)rows_s[xr] * p.k + 32 * b0 + 16 * q);
+            }
+            if (t < MM_BPS * n) {  // group row scales, [block][row]
+                const int j = t / n, xr = t - j * n;
+                float* sxr = reinterpret_cast<float*>(st + MM_RAW_W + MM_RAW_X + MM_RAW_SW);
+                cp4(sxr + j * MM_NMAX + xr, p.xs + (int64_t)rows_s[xr] * p.nb + b0 + j);
+            }
+        };
 
-    // stage i's accumulators (TMEM buffer i % 2: block j, matrix m at column (i%2)*256 + j*128 + m*64), scaled by the
-    // raw stage's scales and added into acc in block order
-    auto drain = [&](int i) {
-        const unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
-        const float* sw = reinterpret_cast<const float*>(st + MM_RAW_W + MM_RAW_X);
-        const float* sx = reinterpret_cast<const float*>(st + MM_RAW_W + MM_RAW_X + MM_RAW_SW);
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * w) << 16) + (uint32_t)((i & 1) * 256);
+        // this thread's outputs: row r, columns 4c..4c+3 for its chunks c = cg, cg + 4, ... (c < N/4)
+        float acc0[4][4], acc1[4][4];
 #pragma unroll
-        for (int j = 0; j < MM_BPS; ++j)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                if (m == 1 && !p.gate_up) break;
-                const float swm = sw[(m * MM_M + t) * MM_BPS + j];
-                // every 16-column load of the (block, matrix) accumulator issued, then one wait
-                uint32_t r[MM_NMAX / 16][16];
+            for (int u = 0; u < 4; ++u) acc0[c][u] = acc1[c][u] = 0.f;
+
+        // raw stage i's scales and TMEM buffer tb's accumulators (block j, matrix m at column tb*256 + j*128 + m*64),
+        // added into acc in block order
+        auto drain = [&](int i, int tb) {
+            const unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
+            const float* sw = reinterpret_cast<const float*>(st + MM_RAW_W + MM_RAW_X);
+            const float* sx = reinterpret_cast<const float*>(st + MM_RAW_W + MM_RAW_X + MM_RAW_SW);
+            const uint32_t lane_base = tmem + ((uint32_t)(32 * (w & 3)) << 16) + (uint32_t)(tb * 256);
 #pragma unroll
-                for (int c = 0; c < MM_NMAX / 16; ++c)
-                    if (c * 16 < N) tmem_ld16(lane_base + j * 128 + m * 64 + c * 16, r[c]);  // CTA-uniform
+            for (int j = 0; j < MM_BPS; ++j) {
+                uint32_t v[4][2][4];
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) {
+                    const int c = cg + MM_CG * ci;
+                    if (4 * c < N) {  // warp-uniform
+                        tmem_ld4(lane_base + j * 128 + 4 * c, v[ci][0]);
+                        if (p.gate_up) tmem_ld4(lane_base + j * 128 + 64 + 4 * c, v[ci][1]);
+                    }
+                }
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                const float sw0 = sw[r * MM_BPS + j];
+                const float sw1 = p.gate_up ? sw[(MM_M + r) * MM_BPS + j] : 0.f;
 #pragma unroll
-                for (int c = 0; c < MM_NMAX / 16; ++c) {
-                    if (c * 16 >= N) break;
+                for (int ci = 0; ci < 4; ++ci) {
+                    const int c = cg + MM_CG * ci;
+                    if (4 * c >= N) break;
+                    const float4 x4 = *reinterpret_cast<const float4*>(sx + j * MM_NMAX + 4 * c);
+                    const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const float sc = swm * sx[(c * 16 + q) * MM_BPS + j];
-                        if (m == 0) acc0[c * 16 + q] = fmaf(sc, __uint_as_float(r[c][q]), acc0[c * 16 + q]);
-                        else acc1[c * 16 + q] = fmaf(sc, __uint_as_float(r[c][q]), acc1[c * 16 + q]);
+                    for (int u = 0; u < 4; ++u) {
+                        acc0[ci][u] = fmaf(sw0 * xv[u], __uint_as_float(v[ci][0][u]), acc0[ci][u]);
+                        if (p.gate_up) acc1[ci][u] = fmaf(sw1 * xv[u], __uint_as_float(v[ci][1][u]), acc1[ci][u]);
                     }
                 }
             }
-    };
+        };
 
-    for (int i = 0; i < MM_RING - 1; ++i) {  // the ring's first stages
-        if (i < nst) fetch(i);
-        cp_commit();
-    }
-    bool ok = true;
-    for (int i = 0; i < nst; ++i) {
-        cp_wait<MM_RING - 2>();  // raw stage i has landed (this thread's copies)
-        __syncthreads();         // ... and every thread's
-        // f16 operands of stage i in buffer i % 2 (its previous MMAs, stage i-2, completed before stage i-1 drained)
-        {
-            const unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
-            unsigned char* op = ops + (size_t)(i & 1) * MM_OP;
-            for (int m = 0; m < mats; ++m) convert_row(op + m * MM_OPA, t, st + (size_t)(m * MM_M + t) * MM_ROWB);
-            if (t < n) convert_row(op + 2 * MM_OPA, t, st + MM_RAW_W + (size_t)t * MM_ROWB);
-            else if (t < N) zero_row(op + 2 * MM_OPA, t);
+        for (int i = 0; i < MM_RING - 1; ++i) {  // the ring's first stages
+            if (i < nst) fetch(i);
+            cp_commit();
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the operands, to the tensor cores
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncthreads();
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (t == 0) {
-            const unsigned char* op = ops + (size_t)(i & 1) * MM_OP;
-            const uint32_t dbase = tmem + (uint32_t)((i & 1) * 256);
-            for (int j = 0; j < MM_BPS; ++j)
-                for (int m = 0; m < mats; ++m) {
-                    const uint32_t d = dbase + j * 128 + m * 64;
-                    const unsigned char* A = op + m * MM_OPA + j * 4 * MM_CORE;
-                    const unsigned char* B = op + 2 * MM_OPA + j * 4 * MM_CORE;
-                    mm_issue(d, mm_desc(A), mm_desc(B), idesc, 0u);  // k 0..15 of block j
-                    mm_issue(d, mm_desc(A + 2 * MM_CORE), mm_desc(B + 2 * MM_CORE), idesc, 1u);  // k 16..31
+        for (int i = 0; i < nst; ++i) {
+            const uint32_t gi = gs + i;  // running stage: buffers gi & 1, barrier phase (gi >> 1) & 1
+            cp_wait<MM_RING - 2>();      // raw stage i has landed (this thread's copies)
+            __syncthreads();             // ... and every thread's
+            {  // f16 operands of stage i in buffer gi & 1 (its previous MMAs, stage gi-2, completed before gi-1 drained)
+                const unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
+                unsigned char* op = ops + (size_t)(gi & 1) * MM_OP;
+                for (int task = t; task < (mats * MM_M + N) * 4; task += MM_THREADS) {
+                    const int row = task >> 2, q = task & 3;
+                    if (row < mats * MM_M) {
+                        const int m = row / MM_M;
+                        convert_quarter(op + m * MM_OPA, row - m * MM_M, q, st + (size_t)row * MM_ROWB + 16 * q);
+                    } else {
+                        const int xr = row - mats * MM_M;
+                        if (xr < n) convert_quarter(op + 2 * MM_OPA, xr, q, st + MM_RAW_W + (size_t)xr * MM_ROWB + 16 * q);
+                        else zero_quarter(op + 2 * MM_OPA, xr, q);
+                    }
                 }
-            mm_commit(&bar[i & 1]);
-        }
-        if (i > 0) {  // stage i-1 while stage i's MMAs run
-            ok = mbar_wait(&bar[(i - 1) & 1], ((i - 1) >> 1) & 1, p.err) && ok;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the operands, to the tensor cores
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncthreads();
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            if (ok) drain(i - 1);
+            if (t == 0) {
+                const unsigned char* op = ops + (size_t)(gi & 1) * MM_OP;
+                const uint32_t dbase = tmem + (uint32_t)((gi & 1) * 256);
+                for (int j = 0; j < MM_BPS; ++j)
+                    for (int m = 0; m < mats; ++m) {
+                        const uint32_t d = dbase + j * 128 + m * 64;
+                        const unsigned char* A = op + m * MM_OPA + j * 4 * MM_CORE;
+                        const unsigned char* B = op + 2 * MM_OPA + j * 4 * MM_CORE;
+                        mm_issue(d, mm_desc(A), mm_desc(B), idesc, 0u);                             // k 0..15
+                        mm_issue(d, mm_desc(A + 2 * MM_CORE), mm_desc(B + 2 * MM_CORE), idesc, 1u);  // k 16..31
+                    }
+                mm_commit(&bar[gi & 1]);
+            }
+            if (i > 0) {  // stage i-1 while stage i's MMAs run
+                const uint32_t gp = gi - 1;
+                ok = mbar_wait(&bar[gp & 1], (gp >> 1) & 1, p.err) && ok;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (ok) drain(i - 1, gp & 1);
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncthreads();
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            // the ring slot of stage i-1 (its scales were read by the drain above) takes stage i + MM_RING - 1
+            if (ok && i + MM_RING - 1 < nst) fetch(i + MM_RING - 1);
+            cp_commit();
+            if (!ok) break;
         }
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncthreads();
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        // the ring slot of stage i-1 (its scales were read by the drain above) takes stage i + MM_RING - 1
-        if (ok && i + MM_RING - 1 < nst) fetch(i + MM_RING - 1);
-        cp_commit();
-        if (!ok) break;
+        cp_wait<0>();
+        if (ok && nst > 0) {
+            const uint32_t gl = gs + nst - 1;
+            ok = mbar_wait(&bar[gl & 1], (gl >> 1) & 1, p.err);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (ok) drain(nst - 1, gl & 1);
+        }
+        gs += nst;
+        const int orow = tile * MM_M + r;
+        if (ok && S == 1) {
+#pragma unroll
+            for (int ci = 0; ci < 4; ++ci) {
+                const int c = cg + MM_CG * ci;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int col = 4 * c + u;
+                    if (col >= n) break;
+                    const float v = p.gate_up ? silu_f32(acc0[ci][u]) * acc1[ci][u] : acc0[ci][u];
+                    p.out[(int64_t)choice_s[col] * p.out_rows + orow] = v;
+                }
+            }
+        } else if (ok) {
+            // K split: this slice's scaled sums to scratch; the last slice to arrive adds the slices in order
+            const int64_t pt = (int64_t)g * p.tiles + tile;
+            const size_t slab = (size_t)2 * MM_NMAX * MM_M;
+            float* mine = p.part + (size_t)(pt * S + slice) * slab;
+#pragma unroll
+            for (int ci = 0; ci < 4; ++ci) {
+                const int c = cg + MM_CG * ci;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int col = 4 * c + u;
+                    if (col >= n) break;
+                    mine[(size_t)col * MM_M + r] = acc0[ci][u];
+                    if (p.gate_up) mine[(size_t)(MM_NMAX + col) * MM_M + r] = acc1[ci][u];
+                }
+            }
+            __threadfence();
+            __syncthreads();
+            if (t == 0) last_s = atomic_add_acq_rel_gpu(p.cnt + pt, 1) == S - 1;
+            __syncthreads();
+            if (last_s) {
+                const float* base = p.part + (size_t)(pt * S) * slab;
+                for (int ci = 0; ci < 4; ++ci) {
+                    const int c = cg + MM_CG * ci;
+                    for (int u = 0; u < 4; ++u) {
+                        const int col = 4 * c + u;
+                        if (col >= n) break;
+                        float gsum = 0.f, usum = 0.f;
+                        for (int sl = 0; sl < S; ++sl) {
+                            gsum += __ldcg(base + (size_t)sl * slab + (size_t)col * MM_M + r);
+                            if (p.gate_up) usum += __ldcg(base + (size_t)sl * slab + (size_t)(MM_NMAX + col) * MM_M + r);
+                        }
+                        p.out[(int64_t)choice_s[col] * p.out_rows + orow] = p.gate_up ? silu_f32(gsum) * usum : gsum;
+                    }
+                }
+                if (t == 0) p.cnt[pt] = 0;
+            }
+        }
+        __syncthreads();  // the item's shared arrays are free for the next item
     }
     cp_wait<0>();
-    if (ok && nst > 0) {
-        ok = mbar_wait(&bar[(nst - 1) & 1], ((nst - 1) >> 1) & 1, p.err);
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (ok) drain(nst - 1);
-    }
-    if (ok) {
-        const int orow = tile * MM_M + t;
-#pragma unroll
-        for (int j = 0; j < MM_NMAX; ++j) {
-            if (j >= n) break;
-            const float v = p.gate_up ? silu_f32(acc0[j]) * acc1[j] : acc0[j];
-            p.out[(int64_t)choice_s[j] * p.out_rows + orow] = v;
-        }
-    }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (w == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(MM_TCOLS));
@@ -319,9 +463,27 @@ bool moe_mma_supported(const ExpertCall& c) {
 int moe_mma_min_rows() { return MM_MIN; }
 int moe_mma_max_rows() { return MM_NMAX; }
 
-cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, cudaStream_t st) {
+cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carve& ws, cudaStream_t st) {
     if (!moe_mma_supported(c)) return cudaErrorInvalidConfiguration;
     MmaParams p = {};
+    // K split: up to MM_SMAX slices of at least 4 stages, when the workspace holds their partial sums (the kernel picks
+    // the number per call from the groups it finds)
+    const int nst_all = (int)(c.k / 32) / MM_BPS;
+    int S = nst_all / 4;
+    S = S < 1 ? 1 : (S > MM_SMAX ? MM_SMAX : S);
+    const int tiles = (int)(c.out_rows / MM_M);
+    const int64_t slots = std::min<int64_t>(max_groups, c.R * c.K / MM_MIN);  // eligible groups at most
+    if (S > 1) {
+        const size_t bytes = (size_t)slots * tiles * S * 2 * MM_NMAX * MM_M * sizeof(float);
+        const size_t at = (ws.used + 255) & ~size_t(255);
+        if (at + bytes <= ws.size && ws.used_counters + (size_t)slots * tiles <= ws.n_counters) {
+            p.part = ws.take<float>(bytes / sizeof(float));
+            p.cnt = ws.take_counters((size_t)slots * tiles);
+        } else {
+            S = 1;
+        }
+    }
+    p.S = S;
     p.gate_up = c.q1 != nullptr;
     p.q0 = c.q0;
     p.s0 = c.s0;
@@ -342,7 +504,10 @@ cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, cuda
     p.err = c.err;
     cudaError_t e = cudaFuncSetAttribute(moe_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MM_SMEM);
     if (e != cudaSuccess) return e;
-    return launch(moe_mma_kernel, dim3((unsigned)(max_groups * p.tiles)), dim3(MM_THREADS), MM_SMEM, st, c.pdl, p);
+    int64_t grid = slots * p.tiles * p.S;  // persistent: one CTA per SM at most
+    if (grid > device_info().sms) grid = device_info().sms;
+    if (grid < 1) grid = 1;
+    return launch(moe_mma_kernel, dim3((unsigned)grid), dim3(MM_THREADS), MM_SMEM, st, c.pdl, p);
 }
 
 }  // namespace q8
