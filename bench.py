@@ -253,6 +253,79 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def time_chunks(q8, cfg, dev, stream, reps=4, correlated=False, rows=(2, 4, 8, 16, 32, 64)):
+    """Chunks of R token rows through the mixture block in the int8 mode: quantize the rows, route them with the
+    expert grouping, gate-up, down-and-combine onto a residual; each chunk uses another layer's router and experts (8
+    layers in turn, so the experts come from HBM), one CUDA graph of 8 chunks per R, replayed `reps` times and timed
+    with CUDA events.  tokens/s = R / time per chunk; the Q8_0 bytes counted per chunk are the router's plus those of
+    the experts the routing touched (unique experts read from the grouping).  `correlated`: rows x0 + 0.01 N(0,1),
+    so all rows share their experts (the groups the tensor-core products take)."""
+    import torch
+    L, d, dff, K, E = cfg["layers"], cfg["d"], cfg["dff"], cfg["k"], cfg["experts"]
+    G = min(L, 8)
+    ws = q8.Workspace(256 << 20)
+    s = torch.cuda.ExternalStream(stream)
+    expert_bytes = 3 * dff * d * 9 // 8
+    router_bytes = E * d * 9 // 8
+    out = []
+    for R in rows:
+        with torch.cuda.stream(s):
+            gen = torch.Generator(device="cuda")
+            gen.manual_seed(1000 + R)
+            if correlated:
+                x = torch.randn(1, d, device="cuda", generator=gen) + 0.01 * torch.randn(R, d, device="cuda",
+                                                                                        generator=gen)
+            else:
+                x = torch.randn(R, d, device="cuda", generator=gen)
+            res = torch.randn(R, d, device="cuda", generator=gen)
+            xq = torch.empty(R, d, dtype=torch.int8, device="cuda")
+            xs = torch.empty(R, d // 32, dtype=torch.float32, device="cuda")
+            ids = torch.empty(R, K, dtype=torch.int32, device="cuda")
+            gates = torch.empty(R, K, dtype=torch.float32, device="cuda")
+            logits = torch.empty(R, E, dtype=torch.float32, device="cuda")
+            pt = [torch.empty(E, dtype=torch.int32, device="cuda"), torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+                  torch.empty(R * K, dtype=torch.int32, device="cuda"), torch.empty(E + 1, dtype=torch.int32, device="cuda")]
+            plan = q8.plan_struct(*pt) if R > 1 else None
+            h = torch.empty(R * K, dff, device="cuda")
+            hq = torch.empty(R * K, dff, dtype=torch.int8, device="cuda")
+            hs = torch.empty(R * K, dff // 32, dtype=torch.float32, device="cuda")
+            y = torch.empty(R, d, device="cuda")
+
+            def step(l):
+                q8.q8_quantize(x, xq, xs, stream=stream)
+                q8.moe_route_topk(*dev["router"][l], 1, K, ids, gates, xq=xq, xs=xs, rows=R, logits=logits, plan=plan,
+                                  ws=ws, stream=stream)
+                q8.moe_gate_up(*dev["gate"][l], *dev["up"][l], dff, 1, K, ids, h, xq=xq, xs=xs, hq=hq, hs=hs, rows=R,
+                               plan=plan, ws=ws, stream=stream)
+                q8.moe_down_combine(*dev["down"][l], d, 1, K, ids, gates, y, h=h, hq=hq, hs=hs, rows=R, plan=plan,
+                                    residual=res, ws=ws, stream=stream)
+
+            uniq = []
+            for l in range(G):
+                step(l)
+                s.synchronize()
+                uniq.append(len(set(ids.cpu().flatten().tolist())))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for l in range(G):
+                    step(l)
+            g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.synchronize()
+            e0.record(s)
+            for _ in range(reps):
+                g.replay()
+            e1.record(s)
+            e1.synchronize()
+            t = e0.elapsed_time(e1) / 1e3 / (reps * G)
+            u = sum(uniq) / len(uniq)
+            out.append({"rows": R, "tokens_per_s": R / t, "us_per_chunk": t * 1e6, "unique_experts": u,
+                        "weight_gbs": (router_bytes + u * expert_bytes) / t / 1e9})
+            del g
+    ws.close()
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -393,6 +466,12 @@ def main():
             line["secondary"] = {"mode": "f32-activation/f64-sum" if other == q8.F32ACT_F64SUM else "int8-activation",
                                  "tokens_per_s": args.steps / s2, "weight_stream_gbs": wbytes * args.steps / s2 / 1e9}
             m2.close()
+            line["chunks"] = {
+                "what": "R-row chunks through the mixture block (int8: quantize, route + grouping, gate-up, "
+                        "down-and-combine), another layer's experts per chunk, one CUDA graph of 8 chunks per R",
+                "uncorrelated": time_chunks(q8, cfg, dev, sh, reps=max(2, min(args.steps, 8))),
+                "correlated": time_chunks(q8, cfg, dev, sh, reps=max(2, min(args.steps, 8)), correlated=True,
+                                          rows=(16, 32, 64))}
         if not args.no_cpu_baseline:
             v, dt = cpu_baseline_oracle(cfg, host, 1 if mode == q8.INT8ACT else 0, 0, cfg["ctx"] - 1)
             line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",

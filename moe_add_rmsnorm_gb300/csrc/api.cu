@@ -285,9 +285,15 @@ int moe_route_topk(const q8_mat* router, q8_mode mode, const float* x, const q8_
         tmp.scratch = ws->scratch + cv.used;
         tmp.bytes = ws->bytes - cv.used;
     }
+    int* done = nullptr;  // the top-k's arrival counter: the workspace's last one, kept from the projection
+    if (plan && tmp.n_counters > 0) {
+        done = tmp.counters + tmp.n_counters - 1;
+        tmp.n_counters -= 1;
+    }
     int r = gemv_common(router, mode, x, xq, rows, l, nullptr, &tmp, st, "moe_route_topk");
     if (r) return r;
     TopkCall t;
+    t.done = done;
     t.logits = l;
     t.R = rows;
     t.E = E;

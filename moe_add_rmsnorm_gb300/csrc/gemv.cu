@@ -34,6 +34,7 @@ struct GemvParams {
     const int8_t* xq;
     const float* xs;
     int R;
+    int RG;          // activation row groups: warp w takes rows w % RG, w % RG + RG, ... (RG <= warps)
     int S;           // slices along k
     void* partial;   // [R][S][ntot] (f64 in mode 0, f32 in mode 1)
     int* counters;   // [R][items]
@@ -51,10 +52,13 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gemv_kernel(const GemvParams p)
     const int lg = lane % LPR;
     const int grp = lane / LPR;
     const int warp = blockIdx.x * Q8_WARPS + (threadIdx.x >> 5);
-    const int W = gridDim.x * Q8_WARPS;
+    const int RG = p.RG;
+    const int rg = warp % RG;                     // this warp's activation rows: rg, rg + RG, ...
+    const int wq = warp / RG, WQ = (gridDim.x * Q8_WARPS) / RG;
+    if (wq >= WQ) return;                         // the last warps when RG does not divide the grid's warps
     const int S = p.S;
-    const int slice = warp % S;
-    const int wstride = (W - slice + S - 1) / S;  // warps serving this slice
+    const int slice = wq % S;
+    const int wstride = (WQ - slice + S - 1) / S;  // warps of this row group serving this slice
     const int nit = p.it0[p.nseg];
 
     int bidx[BPL];
@@ -66,7 +70,7 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gemv_kernel(const GemvParams p)
     }
     issue_l2_prefetch(p.pf);
     // the weights do not depend on earlier kernels: the warp's first tile is read before waiting for them
-    const int first = warp / S;
+    const int first = wq / S;
     WTile<BPL, RT> t;
     if (first < nit) {
         int sg = 0;
@@ -77,15 +81,16 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gemv_kernel(const GemvParams p)
     griddep_wait();
     griddep_launch();
 
-    for (int r = 0; r < p.R; ++r) {
-        XTile<MODE, BPL> x;
-        load_x<MODE, BPL>(x, p.x + (int64_t)r * p.k, p.xq + (int64_t)r * p.k, p.xs + (int64_t)r * p.nb, bidx, bval);
-        for (int it = first; it < nit; it += wstride) {
-            int sg = 0;
-            while (sg + 1 < p.nseg && it >= p.it0[sg + 1]) ++sg;
-            const int row0 = (it - p.it0[sg]) * ROWS + grp * RT;
-            const int nvalid = min(RT, p.n[sg] - row0);
-            if (r > 0 || it != first) load_tile<BPL, RT>(t, p.q[sg], p.s[sg], row0, nvalid, p.k, p.nb, bidx, bval);
+    // each weight tile is read once and multiplied by the warp's activation rows
+    for (int it = first; it < nit; it += wstride) {
+        int sg = 0;
+        while (sg + 1 < p.nseg && it >= p.it0[sg + 1]) ++sg;
+        const int row0 = (it - p.it0[sg]) * ROWS + grp * RT;
+        const int nvalid = min(RT, p.n[sg] - row0);
+        if (it != first) load_tile<BPL, RT>(t, p.q[sg], p.s[sg], row0, nvalid, p.k, p.nb, bidx, bval);
+        for (int r = rg; r < p.R; r += RG) {
+            XTile<MODE, BPL> x;
+            load_x<MODE, BPL>(x, p.x + (int64_t)r * p.k, p.xq + (int64_t)r * p.k, p.xs + (int64_t)r * p.nb, bidx, bval);
             T acc[RT];
 #pragma unroll
             for (int i = 0; i < RT; ++i) {
@@ -390,6 +395,7 @@ bool tma_eligible(const GemvCall& c) {
 
 struct Plan {
     int lpr, bpl, rt, S;
+    int RG = 1;  // activation row groups
     int rpw() const { return 32 / lpr; }
     int rows() const { return rpw() * rt; }
 };
@@ -421,10 +427,15 @@ Plan plan_for(const GemvCall& c) {
     const int target = (c.mode == 0) ? 4 : 8;
     const int rt = target / best.bpl;
     best.rt = rt >= 4 ? 4 : (rt >= 2 ? 2 : 1);
-    // a matrix too short to fill the GPU: fewer rows per item, then more slices
+    // several activation rows: warps split them (each weight tile is then read once per row group)
     const int sms = device_info().sms;
-    while (best.rt > 1 && items_of(c, best) * best.S < 4 * sms) best.rt /= 2;
-    while (best.bpl > 1 && items_of(c, best) * best.S < 2 * sms) {
+    best.RG = (int)std::min<int64_t>(c.R, 64);
+    int64_t wbytes = 0;
+    for (int i = 0; i < c.nseg; ++i) wbytes += c.seg[i].n * c.k;
+    while (best.RG > 1 && wbytes * best.RG > (int64_t)256 << 20) best.RG /= 2;  // re-reads stay mostly in L2
+    // a matrix too short to fill the GPU: fewer rows per item, then more slices
+    while (best.rt > 1 && items_of(c, best) * best.S * best.RG < 4 * sms) best.rt /= 2;
+    while (best.bpl > 1 && items_of(c, best) * best.S * best.RG < 2 * sms) {
         best.bpl = (best.bpl + 1) / 2;
         best.S = (nb + best.lpr * best.bpl - 1) / (best.lpr * best.bpl);
     }
@@ -434,7 +445,10 @@ Plan plan_for(const GemvCall& c) {
 template <int MODE, int LPR, int BPL, int RT, bool DOTS>
 cudaError_t run(const GemvParams& p, int64_t warps, cudaStream_t st, int pdl) {
     auto kern = gemv_kernel<MODE, LPR, BPL, RT, DOTS>;
-    return launch(kern, dim3(persistent_grid(kern, 0, warps)), dim3(Q8_THREADS), 0, st, pdl, p);
+    const int grid = persistent_grid(kern, 0, warps);
+    GemvParams q = p;
+    if (q.RG > grid * Q8_WARPS) q.RG = grid * Q8_WARPS;
+    return launch(kern, dim3(grid), dim3(Q8_THREADS), 0, st, pdl, q);
 }
 
 template <int MODE, bool DOTS, int LPR>
@@ -589,8 +603,9 @@ cudaError_t launch_gemv(const GemvCall& c, Carve& ws, cudaStream_t st) {
         p.counters = ws.take_counters(cnt);
         if (ws.overflow) return cudaErrorMemoryAllocation;
     }
-    // persistent grid: one warp per (item, slice), at most the CTAs resident at once
-    const int64_t grid = (int64_t)it * pl.S;
+    // persistent grid: one warp per (row group, item, slice), at most the CTAs resident at once
+    p.RG = pl.RG;
+    const int64_t grid = (int64_t)it * pl.S * pl.RG;
     if (c.mode == 0) return dispatch<0, false>(pl, p, grid, st, c.pdl);
     if (c.dots) return dispatch<1, true>(pl, p, grid, st, c.pdl);
     return dispatch<1, false>(pl, p, grid, st, c.pdl);

@@ -131,6 +131,7 @@ struct TopkCall {
     int32_t* ids = nullptr;
     float* gates = nullptr;
     PlanPtrs plan;                  // filled when plan.counts != nullptr
+    int* done = nullptr;            // with a plan: one zero-at-rest counter, so that several CTAs can take the rows
     L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };

@@ -24,7 +24,8 @@ namespace {
 
 // ==== top-k and grouping ==========================================================================================
 
-constexpr int TOPK_THREADS = 512;
+constexpr int TOPK_THREADS = 256;  // a warp per row; the grid covers the rows
+constexpr int TOPK_IDS_SMEM = 16384;  // choices staged in shared memory for the grouping (more: read from L2)
 
 struct TopkParams {
     ExpertPrefetch xp;
@@ -37,6 +38,7 @@ struct TopkParams {
     int32_t* offsets;
     int32_t* lists;
     int32_t* active;
+    int* done;  // grid > 1 with a plan: arrivals of the CTAs (left zero); the last one groups
 };
 
 // One thread's prefetch of [p, p + n) into L2 (16-byte-aligned interior, 64 KB pieces).
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
     issue_l2_prefetch(p.pf);
     griddep_wait();
     griddep_launch();
-    for (int r = wid; r < p.R; r += NW) {
+    for (int r = blockIdx.x * NW + wid; r < p.R; r += gridDim.x * NW) {
         const float* l = p.logits + (int64_t)r * p.E;
         // the row's logits in registers (up to 512 experts), else read from global memory each round
         constexpr int EPL = 16;
@@ -175,16 +177,29 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
         }
     }
     if (!p.counts) return;
+    if (gridDim.x > 1) {  // the last CTA to finish its rows groups them all
+        __shared__ int last_s;
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) last_s = atomic_add_acq_rel_gpu(p.done, 1) == (int)gridDim.x - 1;
+        __syncthreads();
+        if (!last_s) return;
+        if (threadIdx.x == 0) *p.done = 0;
+    }
     __syncthreads();
     // grouping: counts, offsets, stable lists, active experts
+    const int n = p.R * p.K;
     int* cnt = sm;                 // [E]
     int* flag = sm + p.E;          // [E]
     int* tmp = sm + 2 * p.E;       // [32]
-    const int n = p.R * p.K;
+    int* sid = sm + 2 * p.E + 32;  // [n] when n <= TOPK_IDS_SMEM
+    const bool staged = n <= TOPK_IDS_SMEM;
     for (int e = threadIdx.x; e < p.E; e += TOPK_THREADS) cnt[e] = 0;
+    if (staged)
+        for (int c = threadIdx.x; c < n; c += TOPK_THREADS) sid[c] = __ldcg(p.ids + c);
     __syncthreads();
     for (int c = threadIdx.x; c < n; c += TOPK_THREADS) {
-        const int e = p.ids[c];
+        const int e = staged ? sid[c] : __ldcg(p.ids + c);
         if (e >= 0 && e < p.E) atomicAdd(&cnt[e], 1);  // a row whose logits were all NaN chose no expert
     }
     __syncthreads();
@@ -203,12 +218,23 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
         p.offsets[p.E] = cnt[p.E - 1] + p.counts[p.E - 1];
         p.active[0] = nactive;
     }
-    for (int c = threadIdx.x; c < n; c += TOPK_THREADS) {
-        const int e = p.ids[c];
-        if (e < 0 || e >= p.E) continue;
-        int rank = 0;
-        for (int c2 = 0; c2 < c; ++c2) rank += (p.ids[c2] == e);
-        p.lists[cnt[e] + rank] = c;
+    __syncthreads();
+    // stable scatter, choices in order: warp 0 takes 32 at a time; the lanes holding the same expert find each other
+    // (match), the lowest of them advances the expert's cursor (cnt, now the offsets) past all of them
+    if (wid == 0) {
+        for (int c0 = 0; c0 < n; c0 += 32) {
+            const int c = c0 + lane;
+            int e = c < n ? (staged ? sid[c] : __ldcg(p.ids + c)) : -1;
+            if (e < 0 || e >= p.E) e = -1;
+            const unsigned same = __match_any_sync(0xffffffffu, e);
+            if (e >= 0) {
+                const int rank = __popc(same & ((1u << lane) - 1u));
+                p.lists[cnt[e] + rank] = c;
+            }
+            __syncwarp();
+            if (e >= 0 && (same & ((1u << lane) - 1u)) == 0) cnt[e] += __popc(same);
+            __syncwarp();
+        }
     }
 }
 
@@ -598,13 +624,19 @@ cudaError_t dispatch_down_one(const EPlan& pl, const ExpertParams& p, int64_t gr
 
 cudaError_t launch_topk(const TopkCall& c, cudaStream_t st) {
     TopkParams p = {c.xp, c.pf, c.logits, (int)c.R, (int)c.E, c.K, c.ids, c.gates,
-                    c.plan.counts, c.plan.offsets, c.plan.lists, c.plan.active};
-    const size_t smem = c.plan.counts ? (size_t)(2 * c.E + 32) * sizeof(int) : 0;
+                    c.plan.counts, c.plan.offsets, c.plan.lists, c.plan.active, c.done};
+    constexpr int NW = TOPK_THREADS / 32;
+    int64_t grid = (c.R + NW - 1) / NW;
+    if (grid > device_info().sms) grid = device_info().sms;
+    if (grid < 1) grid = 1;
+    if (c.plan.counts && grid > 1 && !c.done) grid = 1;  // no arrival counter: one CTA takes every row
+    const int64_t n = c.R * c.K;
+    const size_t smem = c.plan.counts ? (size_t)(2 * c.E + 32 + (n <= TOPK_IDS_SMEM ? n : 0)) * sizeof(int) : 0;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    return launch(topk_kernel, dim3(1), dim3(TOPK_THREADS), smem, st, c.pdl, p);
+    return launch(topk_kernel, dim3((unsigned)grid), dim3(TOPK_THREADS), smem, st, c.pdl, p);
 }
 
 bool experts_supported(int mode, int64_t k) { return k / 32 <= 32 * ((mode == 0) ? 3 : 4); }

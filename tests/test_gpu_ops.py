@@ -270,6 +270,31 @@ def test_route_topk(q8, ws, mode, R, router_scale):
     np.testing.assert_array_equal(act[1:1 + len(active)], active)
 
 
+def test_route_topk_grouping_many_rows(q8, ws):
+    """2100 rows x 8 choices: more choices than the grouping stages in shared memory (it reads them from L2), and
+    the rows spread over many CTAs whose last arrival groups them; the grouping is checked exactly."""
+    import torch
+    E, K, d, R = 128, 8, 2048, 2100
+    rq, rs = synth.q8_matrix(E, d, 0, recipes.layer_ids(0)["router"])
+    x = synth.normal((R, d), 0, recipes.VEC + 61)
+    xq, xs = oracle.quantize(x)
+    ids = empty((R, K), torch.int32)
+    gates = empty((R, K), torch.float32)
+    logits = empty((R, E), torch.float32)
+    pt = _plan_tensors(E, R * K)
+    q8.moe_route_topk(dev(rq), dev(rs), 1, K, ids, gates, xq=dev(xq), xs=dev(xs), rows=R, logits=logits,
+                      plan=q8.plan_struct(*pt), ws=ws)
+    gi = host(ids)
+    for r in range(0, R, 97):  # sampled rows against the oracle
+        l = oracle.gemv(1, rq, rs, x[r])
+        if not _near_tie(l, K):
+            np.testing.assert_array_equal(gi[r], oracle.route(l, K)[0])
+    counts, offsets, lists = oracle.group(gi, E)
+    np.testing.assert_array_equal(host(pt[0]), counts)
+    np.testing.assert_array_equal(host(pt[1]), offsets)
+    np.testing.assert_array_equal(host(pt[2]), lists)
+
+
 def _run_moe_gpu(q8, ws, md, mode, x, K, residual=None, expert_out=True, route_plan=True, down_reads_h=True):
     import torch
     R, d = x.shape
