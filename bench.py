@@ -36,6 +36,9 @@ def parse():
                     help="only the dominant kernel's timing loop (for a profiler capture of that kernel)")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the warm-up and timed decode steps (for profiler launch lists); prints tokens/s")
+    ap.add_argument("--chunk-only", type=int, default=0, metavar="R",
+                    help="only the R-row chunk timing through the mixture block (for a profiler capture of its kernels)")
+    ap.add_argument("--correlated", action="store_true", help="with --chunk-only: rows that share their experts")
     return ap.parse_args()
 
 
@@ -143,8 +146,8 @@ def roofline_traffic(mode_int8):
 
 def time_dominant_kernel(q8, cfg, dev, mode, reps, stream):
     """The mixture's gate-up kernel at the decode shape (8 experts x 768 gate and 768 up rows of 2048), launched over
-    the layers' own stacked matrices in turn (each launch reads weights no earlier launch brought into L2), timed with
-    CUDA events on its stream.  Returns (average seconds per launch, algorithmic bytes per launch)."""
+    the layers' own stacked matrices in turn (each launch reads weights no earlier launch brought into L2), the L
+    launches captured in one CUDA graph, timed with CUDA events on its stream.  Returns (average seconds per launch, algorithmic bytes per launch)."""
     import torch
     L, d, dff, K, E = cfg["layers"], cfg["d"], cfg["dff"], cfg["k"], cfg["experts"]
     ws = q8.Workspace(64 << 20)
@@ -168,16 +171,21 @@ def time_dominant_kernel(q8, cfg, dev, mode, reps, stream):
 
         for l in range(min(L, 4)):
             one(l)
+        # the L launches captured in one graph, so that host calls put no gaps between them
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for l in range(L):
+                one(l)
+        g.replay()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.synchronize()
         start.record(s)
-        n = 0
         for _ in range(reps):
-            for l in range(L):
-                one(l)
-                n += 1
+            g.replay()
         end.record(s)
         end.synchronize()
+        n = reps * L
+        del g
     ws.close()
     sec = start.elapsed_time(end) / 1e3 / n
     return sec, K * 2 * dff * d * 9 // 8
@@ -350,6 +358,11 @@ def main():
     logits = torch.empty(cfg["vocab"], device="cuda")
     stream = torch.cuda.Stream()
     sh = stream.cuda_stream
+    if args.chunk_only:
+        res = time_chunks(q8, cfg, dev, sh, reps=max(1, args.steps), correlated=args.correlated,
+                          rows=(args.chunk_only,))
+        print(json.dumps({"chunk_only": True, "correlated": args.correlated, **res[0]}), flush=True)
+        return
     if args.roofline_only:
         dom_sec, dom_bytes = time_dominant_kernel(q8, cfg, dev, mode, reps=args.steps, stream=sh)
         print(json.dumps({"roofline_only": True, "us_per_launch": dom_sec * 1e6, "algorithmic_bytes": dom_bytes,
