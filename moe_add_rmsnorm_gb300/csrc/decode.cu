@@ -13,7 +13,7 @@
 // per position and key/value head), so the attention is a streaming kernel: every (key/value head, chunk of
 // positions) pair is one CTA that reads its rows once with coalesced 16-byte loads and serves all query heads of its
 // group from those registers; chunk partials (max, sum, weighted values) are folded in chunk order, first inside a
-// thread-block cluster of 4 chunks through distributed shared memory, then across clusters by the last to arrive.  The
+// thread-block cluster of 8 chunks through distributed shared memory, then across clusters by the last to arrive.  The
 // 48 KiB static score row of the pages' design is not needed: a chunk's scores live in shared memory and any cache
 // length works.  Every CTA norms and turns its group's query heads itself (a few hundred values), so no launch sits
 // between the projection and the attention; the CTA whose chunk holds the new position also norms and turns the new
@@ -38,7 +38,7 @@ constexpr int ATT_CHUNK = 64;   // positions per CTA (8 per warp)
 constexpr int ATT_MAXG = 8;     // query heads per key/value head
 constexpr int ATT_HD = 128;     // head width the kernel is built for
 constexpr int ATT_QP = 36;      // padded 32-dim quarter of a query row in shared memory: 16-byte reads, no conflicts
-constexpr int ATT_CLUSTER = 4;  // chunks per thread-block cluster
+constexpr int ATT_CLUSTER = 8;  // chunks per thread-block cluster
 constexpr int ATT_FOLD_B = 16;  // cluster partials a thread loads at once in the final fold
 
 struct AttnParams {
@@ -117,7 +117,8 @@ __device__ void fold_cluster(const AttnParams& p, int g, int chunk, int G, int t
         last[t] = hh < G ? (atomic_add_acq_rel_gpu(p.cnt + g * G + hh, 1) == ncl_used - 1) : 0;
     }
     __syncthreads();  // the other threads read after the arriving thread's acquire
-    // the heads this CTA arrived last for (at most two: rank and rank + 4) are folded at once, 128 threads a head,
+    // the heads this CTA arrived last for (rank, and rank + ATT_CLUSTER when a group has more heads than the cluster
+    // has CTAs) are folded at once, 128 threads a head,
     // thread d summing dimension d over the clusters
     const int lane = t & 31;
     const int u = t / ATT_HD, d = t % ATT_HD;  // head slot, dimension
@@ -173,7 +174,7 @@ __device__ void fold_cluster(const AttnParams& p, int g, int chunk, int G, int t
     cluster_wait();  // no CTA leaves while another may still read its shared memory
 }
 
-// grid (kv, chunk) in clusters of 4 chunks, 8 warps, two CTAs per SM.  Scores: 4 lanes per position (a 32-dim quarter
+// grid (kv, chunk) in clusters of 8 chunks, 8 warps, two CTAs per SM.  Scores: 4 lanes per position (a 32-dim quarter
 // each), each warp 8 positions.  Values: warp w takes positions w, w+8, ... (8 rows), lane l the dims 4l..4l+3; every
 // key and value row is loaded before any is used; the 8 warps' sums meet in shared memory.  A chunk's partial
 // is then folded with the rest of its cluster and across clusters (fold_cluster), always in chunk order.
