@@ -11,13 +11,14 @@
 // converted to f16 in shared memory — exactly: every |v| <= 127 is an f16 integer, every product is exact in the f32
 // accumulator and so is every 32-value block sum (|D| <= 516,128 < 2^24).  For each 32-value block the tile's D
 // (128 weight rows x N group rows) is formed by two tcgen05.mma kind::f16 (K = 16) into a tensor-memory accumulator of
-// its own; four warps per TMEM lane quarter read it back with tcgen05.ld (each a quarter of the columns) and add
-// s_w * s_x * D into registers, the block order and the f32 arithmetic of the int8 mode.  Raw int8 tiles stream into a
-// ring of shared-memory stages by cp.async four stages ahead; each stage (two blocks) is converted to f16 by a byte
-// permute (exact) into one of two operand buffers, and its MMAs run while the previous stage's accumulators (two TMEM
-// buffers) are read back.  Operands use the no-swizzle K-major layout of 8-row x 16-byte core matrices.  One CTA per
-// SM walks the items (group, 128-row tile, k slice) of the groups it takes; the k split is chosen per call from the
-// number of such groups, and the last slice of a tile to finish adds the slices' partial sums in slice order.
+// its own; read-back warps take it with tcgen05.ld and add s_w * s_x * D into registers, the block order and the f32
+// arithmetic of the int8 mode.  The CTA's warps split into three roles joined by mbarriers: fetch-and-convert (raw
+// int8 tiles by cp.async four stages ahead, converted to f16 by a byte permute, exact, into one of two operand
+// buffers), MMA issue (one thread, tcgen05.commit), and read-back (two TMEM buffers) — so conversion, tensor-core work
+// and read-back of different stages overlap.  Operands use the no-swizzle K-major layout of 8-row x 16-byte core
+// matrices.  One CTA per SM walks the items (group, 128-row tile, k slice) of the groups it takes; the k split is
+// chosen per call from the number of such groups, and the last slice of a tile to finish adds the slices' partial sums
+// in slice order.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -30,13 +31,12 @@ namespace q8 {
 namespace {
 
 constexpr int MM_M = 128;        // weight rows per tile: the MMA's M, one TMEM lane per thread
-constexpr int MM_THREADS = 512;  // 16 warps: warp w reads TMEM lanes 32*(w%4).., column chunks w/4, w/4+4, ...
-constexpr int MM_CG = MM_THREADS / MM_M;  // column groups
+constexpr int MM_THREADS = 896;  // 28 warps in three roles (below)
 constexpr int MM_NMAX = 64;      // group rows the kernel takes
 constexpr int MM_MIN = 16;       // smaller groups stay on the CUDA cores
 constexpr int MM_CORE = 128;     // bytes of one core matrix (8 rows x 16 bytes)
 constexpr int MM_BPS = 2;        // 32-value blocks per pipeline stage (K = 64)
-constexpr int MM_RING = 5;       // raw stages in the ring (cp.async, MM_RING - 1 in flight)
+constexpr int MM_RING = 5;       // raw stages in the ring (cp.async, MM_RING - 1 ahead)
 constexpr int MM_SMAX = 4;       // k slices per (group, tile) at most
 constexpr int MM_GCAP = 256;     // eligible groups listed in shared memory (beyond: found by a scan)
 constexpr int MM_ROWB = MM_BPS * 32;                 // bytes of one raw row of a stage (int8)
@@ -53,7 +53,18 @@ constexpr int MM_OPA = MM_M * MM_ROWB * 2;
 constexpr int MM_OPB = MM_NMAX * MM_ROWB * 2;
 constexpr int MM_OP = 2 * MM_OPA + MM_OPB;
 constexpr int MM_TCOLS = 512;    // TMEM: 2 buffers x 2 blocks x 2 matrices x 64 columns
-constexpr size_t MM_SMEM = (size_t)MM_RING * MM_RAW + 2 * MM_OP;
+constexpr int MM_SQ = 4;         // scale slots between the converters and the read-back
+constexpr int MM_SCL = 2 * 2 * MM_M + MM_BPS * MM_NMAX;  // floats of a slot: sw [2][128][2], sx [2][64]
+constexpr size_t MM_SMEM = (size_t)MM_RING * MM_RAW + 2 * MM_OP + (size_t)MM_SQ * MM_SCL * sizeof(float);
+constexpr int MM_CONV_WARPS = 11;                  // warps 0..10 fetch and convert
+constexpr int MM_CONV_T = MM_CONV_WARPS * 32;
+constexpr int MM_ISSUE_WARP = 11;                  // lane 0 issues the MMAs
+constexpr int MM_DRAIN_W0 = 12;                    // warps 12..27 read back: lanes 32*(w%4).., 16 columns each
+constexpr int MM_DRAIN_WARPS = 16;
+constexpr int MM_DCOLS = 16;                       // columns a read-back warp takes
+constexpr int MM_DRAIN_T = MM_DRAIN_WARPS * 32;
+static_assert(MM_DRAIN_W0 + MM_DRAIN_WARPS == MM_THREADS / 32, "roles cover the CTA");
+static_assert(MM_DRAIN_W0 % 4 == 0 && MM_DRAIN_WARPS * MM_DCOLS == 4 * MM_NMAX, "read-back warps cover lanes and columns");
 
 struct MmaParams {
     int gate_up;         // 1: gate and up (SiLU product to h); 0: down (per-choice outputs to part)
@@ -97,9 +108,10 @@ __device__ __forceinline__ void mm_commit(uint64_t* bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
                  : "r"(taddr));
 }
 
@@ -178,25 +190,37 @@ __device__ int mm_scan(const MmaParams& p, int nact, int* list, int target, int*
     return count;
 }
 
+// The eligible group at position g of the order (warp-wide; the first MM_GCAP come from the list).
+__device__ __forceinline__ int mm_group_at(const MmaParams& p, int nact, const int* glist, int g) {
+    if (g < MM_GCAP) return glist[g];
+    int found = 0;
+    mm_scan(p, nact, nullptr, g, &found);
+    return __reduce_max_sync(0xffffffffu, found);
+}
+
 // Persistent: the work is the items (eligible group g, tile, k slice) in that order, CTA b taking items b,
 // b + gridDim.x, ...; an item covers weight rows tile*128 .. tile*128+127 of group g's expert against the group's n rows
 // (16 <= n <= 64), k stages [slice*nst/S, (slice+1)*nst/S), S chosen per call from the number of eligible groups.
-// Stage i covers blocks 2i, 2i+1: its raw bytes arrive by cp.async up to MM_RING - 1 stages ahead (a ring slot is
-// refilled once the stage it held has been read back, its scales included); the threads convert them to f16 operands
-// (two buffers), thread 0 issues two MMAs per block and matrix (K = 16 each) into the stage's TMEM buffer, and the
-// previous stage's accumulators are read back and scaled while these MMAs run.  TMEM, operand buffers and the two MMA
-// barriers carry on from item to item (a running stage count gives buffers and phases).
+// Stage i covers blocks 2i, 2i+1.  The warps have three roles, handing stages on through mbarriers:
+//  - warps 0..6 fetch raw stages by cp.async up to MM_RING - 1 ahead, convert each to f16 operands (two buffers, each
+//    reused once the MMAs that read it completed) and copy its scales into one of MM_SQ scale slots (reused once the
+//    read-back released it);
+//  - warp 7 (one lane) issues the stage's MMAs, two per block and matrix (K = 16 each), into one of two TMEM buffers
+//    (reused once the read-back released it) and commits them to the operand buffer's and the TMEM buffer's barriers;
+//  - warps 8..15 read the TMEM buffer back (warp w: lanes 32*(w%4).., columns 32*((w-8)/4)..+31), add
+//    s_w * s_x * D into registers in block order, and after an item's last stage store its outputs (or its k slice's
+//    partial sums, the last slice of a tile adding them in slice order).
+// TMEM, buffers and barriers carry on from item to item: a running stage count gives buffers and phases, so the
+// three roles run several stages apart.
 __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams p) {
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) uint64_t bar[2];
+    __shared__ __align__(8) uint64_t op_full[2], op_empty[2], tm_full[2], tm_empty[2], sc_full[MM_SQ], sc_empty[MM_SQ];
     __shared__ uint32_t tmem_base;
-    __shared__ int rows_s[MM_NMAX];  // each group row's activation row
-    __shared__ int choice_s[MM_NMAX];
-    __shared__ int glist[MM_GCAP];   // the first eligible groups' indices in the active list
-    __shared__ int nelig_s, a_s, last_s;
+    __shared__ int rows_c[MM_NMAX];    // converters: each group row's activation row
+    __shared__ int choice_d[MM_NMAX];  // read-back: each group row's choice
+    __shared__ int glist[MM_GCAP];     // the first eligible groups' indices in the active list
+    __shared__ int nelig_s, a_c, a_d, last_d;
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
-    const int r = 32 * (w & 3) + lane;  // this thread's tile row (its TMEM lane)
-    const int cg = w >> 2;              // its column group
     griddep_wait();
     griddep_launch();
     const int nact = __ldg(p.active);
@@ -220,8 +244,16 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams 
     const int items = nelig * p.tiles * S;
     if ((int)blockIdx.x >= items) return;
     if (t == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&op_full[i], MM_CONV_WARPS);
+            mbar_init(&op_empty[i], 1);
+            mbar_init(&tm_full[i], 1);
+            mbar_init(&tm_empty[i], MM_DRAIN_WARPS);
+        }
+        for (int i = 0; i < MM_SQ; ++i) {
+            mbar_init(&sc_full[i], MM_CONV_WARPS);
+            mbar_init(&sc_empty[i], MM_DRAIN_WARPS);
+        }
         fence_barrier_init();
     }
     if (w == 0) {
@@ -236,216 +268,241 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams 
     const int mats = p.gate_up ? 2 : 1;
     unsigned char* raw = smem;
     unsigned char* ops = smem + (size_t)MM_RING * MM_RAW;
-    uint32_t gs = 0;  // stages this CTA has run
+    float* scl = reinterpret_cast<float*>(ops + 2 * (size_t)MM_OP);  // [MM_SQ] slots: sw [2][128][2], sx [2][64]
+    uint32_t gs = 0;  // stages this CTA has run (every role counts the same)
     bool ok = true;
 
-    for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
-        const int g = item / (p.tiles * S), tile = (item / S) % p.tiles, slice = item % S;
-        if (g >= MM_GCAP && w == 0) {  // beyond the listed groups: scan for it
-            int found = 0;
-            mm_scan(p, nact, nullptr, g, &found);
-            found = __reduce_max_sync(0xffffffffu, found);
-            if (lane == 0) a_s = found;
-        }
-        __syncthreads();
-        const int a = g < MM_GCAP ? glist[g] : a_s;
-        const int e = __ldg(p.active + 1 + a);
-        const int c0 = __ldg(p.offsets + e), n = __ldg(p.offsets + e + 1) - c0;
-        if (t < n) {
-            const int c = __ldg(p.lists + c0 + t);
-            choice_s[t] = c;
-            rows_s[t] = p.gate_up ? c / p.K : c;
-        }
-        __syncthreads();
-        const int N = (n + 15) & ~15;
-        const int64_t wbase = (int64_t)e * p.out_rows + (int64_t)tile * MM_M;  // the tile's first weight row
-        const uint32_t idesc = mm_idesc(N);
-        const int st0 = slice * nst_all / S, nst = (slice + 1) * nst_all / S - st0;  // this item's stages
-
-        // raw stage i (block-major scales for the rows, so a read-back loads four rows' scales at once)
-        auto fetch = [&](int i) {
-            unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
-            const int b0 = (st0 + i) * MM_BPS;
-            for (int task = t; task < mats * MM_M * 4; task += MM_THREADS) {  // weight row quarters
-                const int m = task / (MM_M * 4), wr = (task >> 2) & (MM_M - 1), q = task & 3;
-                const int8_t* src = (m == 0 ? p.q0 : p.q1) + (wbase + wr) * p.k + 32 * b0 + 16 * q;
-                cp16(st + (size_t)(m * MM_M + wr) * MM_ROWB + 16 * q, src);
+    if (w < MM_CONV_WARPS) {
+        // ---- fetch and convert ------------------------------------------------------------------------------------
+        const int ct = t;  // 0 .. MM_CONV_T - 1
+        for (int item = blockIdx.x; item < items; item += gridDim.x) {  // (no early exit: named barriers below)
+            const int g = item / (p.tiles * S), tile = (item / S) % p.tiles, slice = item % S;
+            if (w == 0) {
+                const int a = mm_group_at(p, nact, glist, g);
+                if (lane == 0) a_c = a;
             }
-            if (t < mats * MM_M) {  // weight scales
-                const int m = t / MM_M, wr = t & (MM_M - 1);
-                cp8(st + MM_RAW_W + MM_RAW_X + (size_t)(m * MM_M + wr) * MM_BPS * 4,
-                    (m == 0 ? p.s0 : p.s1) + (wbase + wr) * p.nb + b0);
+            asm volatile("bar.sync 1, %0;" ::"n"(MM_CONV_T));
+            const int e = __ldg(p.active + 1 + a_c);
+            const int c0 = __ldg(p.offsets + e), n = __ldg(p.offsets + e + 1) - c0;
+            if (ct < n) {
+                const int c = __ldg(p.lists + c0 + ct);
+                rows_c[ct] = p.gate_up ? c / p.K : c;
             }
-            if (t < 4 * n) {  // group row quarters
-                const int xr = t >> 2, q = t & 3;
-                cp16(st + MM_RAW_W + (size_t)xr * MM_ROWB + 16 * q, p.xq + (int64_t)rows_s[xr] * p.k + 32 * b0 + 16 * q);
-            }
-            if (t < MM_BPS * n) {  // group row scales, [block][row]
-                const int j = t / n, xr = t - j * n;
-                float* sxr = reinterpret_cast<float*>(st + MM_RAW_W + MM_RAW_X + MM_RAW_SW);
-                cp4(sxr + j * MM_NMAX + xr, p.xs + (int64_t)rows_s[xr] * p.nb + b0 + j);
-            }
-        };
-
-        // this thread's outputs: row r, columns 4c..4c+3 for its chunks c = cg, cg + 4, ... (c < N/4)
-        float acc0[4][4], acc1[4][4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) acc0[c][u] = acc1[c][u] = 0.f;
-
-        // raw stage i's scales and TMEM buffer tb's accumulators (block j, matrix m at column tb*256 + j*128 + m*64),
-        // added into acc in block order
-        auto drain = [&](int i, int tb) {
-            const unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
-            const float* sw = reinterpret_cast<const float*>(st + MM_RAW_W + MM_RAW_X);
-            const float* sx = reinterpret_cast<const float*>(st + MM_RAW_W + MM_RAW_X + MM_RAW_SW);
-            const uint32_t lane_base = tmem + ((uint32_t)(32 * (w & 3)) << 16) + (uint32_t)(tb * 256);
-#pragma unroll
-            for (int j = 0; j < MM_BPS; ++j) {
-                uint32_t v[4][2][4];
-#pragma unroll
-                for (int ci = 0; ci < 4; ++ci) {
-                    const int c = cg + MM_CG * ci;
-                    if (4 * c < N) {  // warp-uniform
-                        tmem_ld4(lane_base + j * 128 + 4 * c, v[ci][0]);
-                        if (p.gate_up) tmem_ld4(lane_base + j * 128 + 64 + 4 * c, v[ci][1]);
-                    }
+            asm volatile("bar.sync 1, %0;" ::"n"(MM_CONV_T));
+            const int N = (n + 15) & ~15;
+            const int64_t wbase = (int64_t)e * p.out_rows + (int64_t)tile * MM_M;
+            const int st0 = slice * nst_all / S, nst = (slice + 1) * nst_all / S - st0;
+            auto fetch = [&](int i) {
+                unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
+                const int b0 = (st0 + i) * MM_BPS;
+                for (int task = ct; task < mats * MM_M * 4; task += MM_CONV_T) {  // weight row quarters
+                    const int m = task / (MM_M * 4), wr = (task >> 2) & (MM_M - 1), q = task & 3;
+                    cp16(st + (size_t)(m * MM_M + wr) * MM_ROWB + 16 * q,
+                         (m == 0 ? p.q0 : p.q1) + (wbase + wr) * p.k + 32 * b0 + 16 * q);
                 }
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                const float sw0 = sw[r * MM_BPS + j];
-                const float sw1 = p.gate_up ? sw[(MM_M + r) * MM_BPS + j] : 0.f;
-#pragma unroll
-                for (int ci = 0; ci < 4; ++ci) {
-                    const int c = cg + MM_CG * ci;
-                    if (4 * c >= N) break;
-                    const float4 x4 = *reinterpret_cast<const float4*>(sx + j * MM_NMAX + 4 * c);
-                    const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        acc0[ci][u] = fmaf(sw0 * xv[u], __uint_as_float(v[ci][0][u]), acc0[ci][u]);
-                        if (p.gate_up) acc1[ci][u] = fmaf(sw1 * xv[u], __uint_as_float(v[ci][1][u]), acc1[ci][u]);
-                    }
+                for (int task = ct; task < mats * MM_M; task += MM_CONV_T) {  // weight scales
+                    const int m = task / MM_M, wr = task & (MM_M - 1);
+                    cp8(st + MM_RAW_W + MM_RAW_X + (size_t)(m * MM_M + wr) * MM_BPS * 4,
+                        (m == 0 ? p.s0 : p.s1) + (wbase + wr) * p.nb + b0);
                 }
+                for (int task = ct; task < 4 * n; task += MM_CONV_T) {  // group row quarters
+                    const int xr = task >> 2, q = task & 3;
+                    cp16(st + MM_RAW_W + (size_t)xr * MM_ROWB + 16 * q,
+                         p.xq + (int64_t)rows_c[xr] * p.k + 32 * b0 + 16 * q);
+                }
+                for (int task = ct; task < MM_BPS * n; task += MM_CONV_T) {  // group row scales, [block][row]
+                    const int j = task / n, xr = task - j * n;
+                    float* sxr = reinterpret_cast<float*>(st + MM_RAW_W + MM_RAW_X + MM_RAW_SW);
+                    cp4(sxr + j * MM_NMAX + xr, p.xs + (int64_t)rows_c[xr] * p.nb + b0 + j);
+                }
+            };
+            for (int i = 0; i < MM_RING - 1; ++i) {
+                if (i < nst) fetch(i);
+                cp_commit();
             }
-        };
-
-        for (int i = 0; i < MM_RING - 1; ++i) {  // the ring's first stages
-            if (i < nst) fetch(i);
-            cp_commit();
-        }
-        for (int i = 0; i < nst; ++i) {
-            const uint32_t gi = gs + i;  // running stage: buffers gi & 1, barrier phase (gi >> 1) & 1
-            cp_wait<MM_RING - 2>();      // raw stage i has landed (this thread's copies)
-            __syncthreads();             // ... and every thread's
-            {  // f16 operands of stage i in buffer gi & 1 (its previous MMAs, stage gi-2, completed before gi-1 drained)
+            for (int i = 0; i < nst; ++i) {
+                const uint32_t gi = gs + i;
+                const int b = gi & 1, q = gi % MM_SQ;
+                cp_wait<MM_RING - 2>();
+                asm volatile("bar.sync 1, %0;" ::"n"(MM_CONV_T));  // raw stage i landed (every converter's copies)
+                // the ring slot of stage i-1 (converted, its scales copied) takes stage i + MM_RING - 1
+                if (i + MM_RING - 1 < nst) fetch(i + MM_RING - 1);
+                cp_commit();
                 const unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
-                unsigned char* op = ops + (size_t)(gi & 1) * MM_OP;
-                for (int task = t; task < (mats * MM_M + N) * 4; task += MM_THREADS) {
-                    const int row = task >> 2, q = task & 3;
+                if (ok && gi >= 2) ok = mbar_wait(&op_empty[b], ((gi >> 1) - 1) & 1, p.err);
+                unsigned char* op = ops + (size_t)b * MM_OP;
+                for (int task = ct; task < (mats * MM_M + N) * 4; task += MM_CONV_T) {
+                    const int row = task >> 2, qq = task & 3;
                     if (row < mats * MM_M) {
                         const int m = row / MM_M;
-                        convert_quarter(op + m * MM_OPA, row - m * MM_M, q, st + (size_t)row * MM_ROWB + 16 * q);
+                        convert_quarter(op + m * MM_OPA, row - m * MM_M, qq, st + (size_t)row * MM_ROWB + 16 * qq);
                     } else {
                         const int xr = row - mats * MM_M;
-                        if (xr < n) convert_quarter(op + 2 * MM_OPA, xr, q, st + MM_RAW_W + (size_t)xr * MM_ROWB + 16 * q);
-                        else zero_quarter(op + 2 * MM_OPA, xr, q);
+                        if (xr < n) convert_quarter(op + 2 * MM_OPA, xr, qq, st + MM_RAW_W + (size_t)xr * MM_ROWB + 16 * qq);
+                        else zero_quarter(op + 2 * MM_OPA, xr, qq);
                     }
                 }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the operands, to the tensor cores
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&op_full[b]);
+                if (ok && gi >= MM_SQ) ok = mbar_wait(&sc_empty[q], ((gi / MM_SQ) - 1) & 1, p.err);
+                {  // the stage's scales into slot q
+                    float* sl = scl + (size_t)q * MM_SCL;
+                    const float2* sw = reinterpret_cast<const float2*>(st + MM_RAW_W + MM_RAW_X);
+                    const float* sx = reinterpret_cast<const float*>(st + MM_RAW_W + MM_RAW_X + MM_RAW_SW);
+                    for (int task = ct; task < mats * MM_M; task += MM_CONV_T) reinterpret_cast<float2*>(sl)[task] = sw[task];
+                    for (int task = ct; task < MM_BPS * MM_NMAX; task += MM_CONV_T) sl[2 * 2 * MM_M + task] = sx[task];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sc_full[q]);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the operands, to the tensor cores
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncthreads();
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            if (t == 0) {
-                const unsigned char* op = ops + (size_t)(gi & 1) * MM_OP;
-                const uint32_t dbase = tmem + (uint32_t)((gi & 1) * 256);
-                for (int j = 0; j < MM_BPS; ++j)
-                    for (int m = 0; m < mats; ++m) {
-                        const uint32_t d = dbase + j * 128 + m * 64;
-                        const unsigned char* A = op + m * MM_OPA + j * 4 * MM_CORE;
-                        const unsigned char* B = op + 2 * MM_OPA + j * 4 * MM_CORE;
-                        mm_issue(d, mm_desc(A), mm_desc(B), idesc, 0u);                             // k 0..15
-                        mm_issue(d, mm_desc(A + 2 * MM_CORE), mm_desc(B + 2 * MM_CORE), idesc, 1u);  // k 16..31
-                    }
-                mm_commit(&bar[gi & 1]);
-            }
-            if (i > 0) {  // stage i-1 while stage i's MMAs run
-                const uint32_t gp = gi - 1;
-                ok = mbar_wait(&bar[gp & 1], (gp >> 1) & 1, p.err) && ok;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                if (ok) drain(i - 1, gp & 1);
-            }
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncthreads();
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            // the ring slot of stage i-1 (its scales were read by the drain above) takes stage i + MM_RING - 1
-            if (ok && i + MM_RING - 1 < nst) fetch(i + MM_RING - 1);
-            cp_commit();
-            if (!ok) break;
+            cp_wait<0>();
+            gs += nst;
         }
         cp_wait<0>();
-        if (ok && nst > 0) {
-            const uint32_t gl = gs + nst - 1;
-            ok = mbar_wait(&bar[gl & 1], (gl >> 1) & 1, p.err);
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            if (ok) drain(nst - 1, gl & 1);
-        }
-        gs += nst;
-        const int orow = tile * MM_M + r;
-        if (ok && S == 1) {
-#pragma unroll
-            for (int ci = 0; ci < 4; ++ci) {
-                const int c = cg + MM_CG * ci;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int col = 4 * c + u;
-                    if (col >= n) break;
-                    const float v = p.gate_up ? silu_f32(acc0[ci][u]) * acc1[ci][u] : acc0[ci][u];
-                    p.out[(int64_t)choice_s[col] * p.out_rows + orow] = v;
-                }
-            }
-        } else if (ok) {
-            // K split: this slice's scaled sums to scratch; the last slice to arrive adds the slices in order
-            const int64_t pt = (int64_t)g * p.tiles + tile;
-            const size_t slab = (size_t)2 * MM_NMAX * MM_M;
-            float* mine = p.part + (size_t)(pt * S + slice) * slab;
-#pragma unroll
-            for (int ci = 0; ci < 4; ++ci) {
-                const int c = cg + MM_CG * ci;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int col = 4 * c + u;
-                    if (col >= n) break;
-                    mine[(size_t)col * MM_M + r] = acc0[ci][u];
-                    if (p.gate_up) mine[(size_t)(MM_NMAX + col) * MM_M + r] = acc1[ci][u];
-                }
-            }
-            __threadfence();
-            __syncthreads();
-            if (t == 0) last_s = atomic_add_acq_rel_gpu(p.cnt + pt, 1) == S - 1;
-            __syncthreads();
-            if (last_s) {
-                const float* base = p.part + (size_t)(pt * S) * slab;
-                for (int ci = 0; ci < 4; ++ci) {
-                    const int c = cg + MM_CG * ci;
-                    for (int u = 0; u < 4; ++u) {
-                        const int col = 4 * c + u;
-                        if (col >= n) break;
-                        float gsum = 0.f, usum = 0.f;
-                        for (int sl = 0; sl < S; ++sl) {
-                            gsum += __ldcg(base + (size_t)sl * slab + (size_t)col * MM_M + r);
-                            if (p.gate_up) usum += __ldcg(base + (size_t)sl * slab + (size_t)(MM_NMAX + col) * MM_M + r);
-                        }
-                        p.out[(int64_t)choice_s[col] * p.out_rows + orow] = p.gate_up ? silu_f32(gsum) * usum : gsum;
+    } else if (w == MM_ISSUE_WARP) {
+        // ---- MMA issue --------------------------------------------------------------------------------------------
+        for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+            const int g = item / (p.tiles * S), slice = item % S;
+            const int a = mm_group_at(p, nact, glist, g);
+            const int e = __ldg(p.active + 1 + a);
+            const int n = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+            const int N = (n + 15) & ~15;
+            const uint32_t idesc = mm_idesc(N);
+            const int nst = (slice + 1) * nst_all / S - slice * nst_all / S;
+            for (int i = 0; i < nst && ok; ++i) {
+                const uint32_t gi = gs + i;
+                const int b = gi & 1;
+                if (lane == 0) {
+                    if (ok) ok = mbar_wait(&op_full[b], (gi >> 1) & 1, p.err);
+                    if (ok && gi >= 2) ok = mbar_wait(&tm_empty[b], ((gi >> 1) - 1) & 1, p.err);
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    if (ok) {
+                        const unsigned char* op = ops + (size_t)b * MM_OP;
+                        const uint32_t dbase = tmem + (uint32_t)(b * 256);
+                        for (int j = 0; j < MM_BPS; ++j)
+                            for (int m = 0; m < mats; ++m) {
+                                const uint32_t d = dbase + j * 128 + m * 64;
+                                const unsigned char* A = op + m * MM_OPA + j * 4 * MM_CORE;
+                                const unsigned char* B = op + 2 * MM_OPA + j * 4 * MM_CORE;
+                                mm_issue(d, mm_desc(A), mm_desc(B), idesc, 0u);                             // k 0..15
+                                mm_issue(d, mm_desc(A + 2 * MM_CORE), mm_desc(B + 2 * MM_CORE), idesc, 1u);  // k 16..31
+                            }
+                        mm_commit(&op_empty[b]);
+                        mm_commit(&tm_full[b]);
                     }
                 }
-                if (t == 0) p.cnt[pt] = 0;
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             }
+            gs += nst;
         }
-        __syncthreads();  // the item's shared arrays are free for the next item
+    } else {
+        // ---- read-back, scaling and epilogue ----------------------------------------------------------------------
+        const int dw = w - MM_DRAIN_W0;                 // 0 .. MM_DRAIN_WARPS - 1
+        const int r = 32 * (w & 3) + lane;              // tile row = TMEM lane
+        const int col0 = MM_DCOLS * (dw >> 2);          // this warp's columns
+        const int dt = t - MM_DRAIN_W0 * 32;            // 0 .. MM_DRAIN_T - 1
+        for (int item = blockIdx.x; item < items; item += gridDim.x) {  // (no early exit: named barriers below)
+            const int g = item / (p.tiles * S), tile = (item / S) % p.tiles, slice = item % S;
+            if (dw == 0) {
+                const int a = mm_group_at(p, nact, glist, g);
+                if (lane == 0) a_d = a;
+            }
+            asm volatile("bar.sync 2, %0;" ::"n"(MM_DRAIN_T));
+            const int e = __ldg(p.active + 1 + a_d);
+            const int c0 = __ldg(p.offsets + e), n = __ldg(p.offsets + e + 1) - c0;
+            if (dt < n) choice_d[dt] = __ldg(p.lists + c0 + dt);
+            asm volatile("bar.sync 2, %0;" ::"n"(MM_DRAIN_T));
+            const int N = (n + 15) & ~15;
+            const int nst = (slice + 1) * nst_all / S - slice * nst_all / S;
+            float acc0[MM_DCOLS], acc1[MM_DCOLS];
+#pragma unroll
+            for (int c = 0; c < MM_DCOLS; ++c) acc0[c] = acc1[c] = 0.f;
+            const uint32_t lane_base = tmem + ((uint32_t)(32 * (w & 3)) << 16);
+            for (int i = 0; i < nst; ++i) {
+                const uint32_t gi = gs + i;
+                const int b = gi & 1, q = gi % MM_SQ;
+                if (ok) ok = mbar_wait(&tm_full[b], (gi >> 1) & 1, p.err);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (ok) ok = mbar_wait(&sc_full[q], (gi / MM_SQ) & 1, p.err);
+                const float* sl = scl + (size_t)q * MM_SCL;
+                if (ok && col0 < N) {  // warp-uniform
+#pragma unroll
+                    for (int j = 0; j < MM_BPS; ++j)
+#pragma unroll
+                        for (int m = 0; m < 2; ++m) {
+                            if (m == 1 && !p.gate_up) break;
+                            uint32_t v[16];
+                            tmem_ld16(lane_base + (uint32_t)(b * 256 + j * 128 + m * 64 + col0), v);
+                            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                            const float swv = sl[(m * MM_M + r) * MM_BPS + j];
+                            const float* sxj = sl + 2 * 2 * MM_M + j * MM_NMAX + col0;
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const float4 x4 = *reinterpret_cast<const float4*>(sxj + 4 * q4);
+                                const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const int c = 4 * q4 + u;
+                                    if (m == 0) acc0[c] = fmaf(swv * xv[u], __uint_as_float(v[c]), acc0[c]);
+                                    else acc1[c] = fmaf(swv * xv[u], __uint_as_float(v[c]), acc1[c]);
+                                }
+                            }
+                        }
+                }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&tm_empty[b]);
+                    mbar_arrive(&sc_empty[q]);
+                }
+            }
+            gs += nst;
+            const int orow = tile * MM_M + r;
+            if (ok && S == 1) {
+#pragma unroll
+                for (int c = 0; c < MM_DCOLS; ++c) {
+                    const int col = col0 + c;
+                    if (col >= n) break;
+                    const float v = p.gate_up ? silu_f32(acc0[c]) * acc1[c] : acc0[c];
+                    p.out[(int64_t)choice_d[col] * p.out_rows + orow] = v;
+                }
+            } else if (S > 1) {
+                // K split: this slice's scaled sums to scratch; the last slice to arrive adds the slices in order
+                // (every read-back thread passes the barriers, whatever its wait status)
+                const int64_t pt = (int64_t)g * p.tiles + tile;
+                const size_t slab = (size_t)2 * MM_NMAX * MM_M;
+                float* mine = p.part + (size_t)(pt * S + slice) * slab;
+                if (ok)
+#pragma unroll
+                    for (int c = 0; c < MM_DCOLS; ++c) {
+                        const int col = col0 + c;
+                        if (col >= n) break;
+                        mine[(size_t)col * MM_M + r] = acc0[c];
+                        if (p.gate_up) mine[(size_t)(MM_NMAX + col) * MM_M + r] = acc1[c];
+                    }
+                __threadfence();
+                asm volatile("bar.sync 2, %0;" ::"n"(MM_DRAIN_T));
+                if (dt == 0) last_d = atomic_add_acq_rel_gpu(p.cnt + pt, 1) == S - 1;
+                asm volatile("bar.sync 2, %0;" ::"n"(MM_DRAIN_T));
+                if (last_d && ok) {
+                    const float* base = p.part + (size_t)(pt * S) * slab;
+                    for (int c = 0; c < MM_DCOLS; ++c) {
+                        const int col = col0 + c;
+                        if (col >= n) break;
+                        float gsum = 0.f, usum = 0.f;
+                        for (int sl2 = 0; sl2 < S; ++sl2) {
+                            gsum += __ldcg(base + (size_t)sl2 * slab + (size_t)col * MM_M + r);
+                            if (p.gate_up) usum += __ldcg(base + (size_t)sl2 * slab + (size_t)(MM_NMAX + col) * MM_M + r);
+                        }
+                        p.out[(int64_t)choice_d[col] * p.out_rows + orow] = p.gate_up ? silu_f32(gsum) * usum : gsum;
+                    }
+                    if (dt == 0) p.cnt[pt] = 0;
+                }
+            }
+            asm volatile("bar.sync 2, %0;" ::"n"(MM_DRAIN_T));  // choice_d and the flag are free for the next item
+        }
     }
-    cp_wait<0>();
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (w == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(MM_TCOLS));
