@@ -150,7 +150,9 @@ typedef struct {
 /* Router and top-k (forward_shim.rs, kernel_refusal Moe arms; lane_link.rs, Link::prim Moe: k <= 32, experts <= 8192):
  * l = router . x_r (the projection in `mode`), p = softmax(l), the k largest kept in descending order (equal logits:
  * lower expert first), g_j = p_j / sum of the kept p.  ids: device int32 [rows][k]; gates: device f32 [rows][k];
- * logits: device f32 [rows][experts] or NULL; plan: filled when not NULL.  experts = router->rows. */
+ * logits: device f32 [rows][experts] or NULL; plan: filled when not NULL.  experts = router->rows.  Several rows
+ * spread over several CTAs; with a plan the last one to finish groups the choices, counted on one of the workspace's
+ * arrival counters (left zero). */
 Q8_API int moe_route_topk(const q8_mat *router, q8_mode mode, const float *x, const q8_act *xq, int64_t rows, int k,
                    int32_t *ids, float *gates, float *logits, const q8_moe_plan *plan, q8_ws *ws, q8_stream stream);
 
