@@ -215,6 +215,16 @@ Q8_API void q8_model_destroy(q8_model *model);
 Q8_API int decode_step(q8_model *model, q8_stream stream);
 /* The same step as plain launches, without a graph (for tests and graph-capture by the caller). */
 Q8_API int decode_step_launches(q8_model *model, q8_stream stream);
+/* A chunk of `rows` token rows through every layer (the prefill of a prompt chunk): tokens is device int32 [rows]; row
+ * r takes position *pos + r.  Each layer: RMSNorm of the rows, the q/k/v projection of all rows, then for each row in
+ * turn QK-norm, RoPE, the key/value append at its position and attention over rows 0 .. its position (causal), the O
+ * projection onto the residual, RMSNorm, routing with the expert grouping, gate-up and down-and-combine of the chunk
+ * (each chosen expert's weights read once for all its rows).  Then the last row's final norm, LM head and greedy token
+ * into *tok; *pos advances by `rows`.  The result equals `rows` decode steps fed these tokens (up to the summation
+ * order of the multi-row kernels).  The chunk's activations and every launch's scratch come from `ws` (Q8_ENOSPACE if
+ * too small); plain launches on `stream`, no graph.  An id outside [0, vocab) or a row past the cache end sets the
+ * model's device error word (q8_model_check). */
+Q8_API int prefill_chunk(q8_model *model, const int32_t *tokens, int64_t rows, q8_ws *ws, q8_stream stream);
 /* Kernels one step launches: the kernel nodes of the graph the first decode_step captured (0 before it). */
 Q8_API int64_t q8_model_launches_per_step(const q8_model *model);
 /* Reads and clears the model's device error word (synchronizes `stream`): Q8_OK, or Q8_EINVAL when a step met an

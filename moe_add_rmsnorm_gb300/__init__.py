@@ -75,6 +75,7 @@ _SIGS = {
     "q8_model_destroy": [_vp],
     "decode_step": [_vp, _vp],
     "decode_step_launches": [_vp, _vp],
+    "prefill_chunk": [_vp, _vp, _i64, _vp, _vp],
     "q8_model_check": [_vp, _vp],
     "q8_model_launches_per_step": [_vp],
     "q8_last_error": [],
@@ -258,6 +259,10 @@ class Model:
 
     def step_launches(self, stream=None):
         _check(lib.decode_step_launches(self.handle, _stream(stream)))
+
+    def prefill(self, tokens, ws, stream=None):
+        """tokens: device int32 [rows]; the chunk through every layer (plain launches), last row's token into tok."""
+        _check(lib.prefill_chunk(self.handle, tokens.data_ptr(), tokens.numel(), ws.handle, _stream(stream)))
 
     def check(self, stream=None):
         _check(lib.q8_model_check(self.handle, _stream(stream)))

@@ -449,6 +449,8 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
 
 namespace q8 {
 
+Carve workspace_carve(const q8_ws* ws) { return ws->carve(); }
+
 // Scratch one q8_gemv call takes (bytes and arrival counters): the quantized activation when x is quantized inside
 // the call, then the partial sums of a projection cut along k; each region rounded up to 256 bytes as a workspace
 // carve rounds it.

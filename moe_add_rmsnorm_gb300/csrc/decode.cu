@@ -504,6 +504,33 @@ int argmax_blocks(int64_t n) {
     return (int)b;
 }
 
+// ==== a chunk of token rows ======================================================================================
+
+// Row r of the residual stream is the embedding row of tokens[r] (an id outside [0, vocab) reads row 0 and sets
+// error bit 1); posr[r] = *pos + r, the position row r takes (a row past the cache end sets bit 2, and its attention
+// launch then writes and attends nothing).
+__global__ void __launch_bounds__(256) chunk_setup_kernel(const int32_t* tokens, const float* embed, int64_t D,
+                                                          int64_t vocab, const int32_t* pos, int ctx, int32_t* posr,
+                                                          float* h, int* err) {
+    const int r = blockIdx.x;
+    const int32_t tk = tokens[r];
+    const bool bad = tk < 0 || tk >= vocab;
+    const float* src = embed + (bad ? 0 : (int64_t)tk) * D;
+    float* dst = h + (int64_t)r * D;
+    for (int64_t i = threadIdx.x; i < D; i += blockDim.x) dst[i] = __ldg(src + i);
+    if (threadIdx.x == 0) {
+        const int p = *pos + r;
+        posr[r] = p;
+        if (bad && err) atomicOr(err, 1);
+        if ((p < 0 || p >= ctx) && err) atomicOr(err, 2);
+    }
+}
+
+// *pos += add, unless the step's error word is set.
+__global__ void pos_add_kernel(int32_t* pos, int add, const int* err) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && !(err && *err)) *pos += add;
+}
+
 }  // namespace
 
 void attention_scratch(const AttnCall& c, size_t* bytes, size_t* counters) {
@@ -579,6 +606,18 @@ cudaError_t launch_argmax(const ArgmaxCall& c, Carve& ws, cudaStream_t st) {
 
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int ctx, int half, double theta, cudaStream_t st) {
     rope_table_kernel<<<256, 256, 0, st>>>(cos_t, sin_t, ctx, half, theta);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_setup(const int32_t* tokens, int64_t rows, const float* embed, int64_t D, int64_t vocab,
+                               const int32_t* pos, int ctx, int32_t* posr, float* h, int* err, cudaStream_t st) {
+    if (rows < 1) return cudaSuccess;
+    chunk_setup_kernel<<<(unsigned)rows, 256, 0, st>>>(tokens, embed, D, vocab, pos, ctx, posr, h, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pos_add(int32_t* pos, int add, const int* err, cudaStream_t st) {
+    pos_add_kernel<<<1, 32, 0, st>>>(pos, add, err);
     return cudaGetLastError();
 }
 

@@ -250,6 +250,15 @@ cudaError_t launch_argmax(const ArgmaxCall& c, Carve& ws, cudaStream_t st);
 
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int ctx, int half, double theta, cudaStream_t st);
 
+// A chunk of token rows: the residual rows gathered from the embedding and each row's position (*pos + r).
+cudaError_t launch_chunk_setup(const int32_t* tokens, int64_t rows, const float* embed, int64_t D, int64_t vocab,
+                               const int32_t* pos, int ctx, int32_t* posr, float* h, int* err, cudaStream_t st);
+// *pos += add on the device, unless *err is set.
+cudaError_t launch_pos_add(int32_t* pos, int add, const int* err, cudaStream_t st);
+
+// The scratch and counters of a caller's workspace, for the launches of one call (the C ABI's q8_ws).
+Carve workspace_carve(const q8_ws* ws);
+
 // A persistent grid for `kernel`: enough CTAs of Q8_THREADS threads for `warps` warps, at most the CTAs that fit on
 // the device at once (occupancy times SMs).
 template <typename Kern>

@@ -547,6 +547,239 @@ int decode_step(q8_model* m, q8_stream stream) {
     return e == cudaSuccess ? Q8_OK : model_fail(Q8_ECUDA, "decode_step: %s", cudaGetErrorString(e));
 }
 
+int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_stream stream) {
+    if (!m) return model_fail(Q8_EINVAL, "model: null");
+    if (!tokens || !ws) return model_fail(Q8_EINVAL, "prefill_chunk: tokens or ws null");
+    if (R < 1 || R > (1 << 20)) return model_fail(Q8_EINVAL, "prefill_chunk: %lld rows", (long long)R);
+    const q8_model_desc& d = m->d;
+    const int mode = (int)d.mode;
+    const int64_t D = d.d, H = d.heads, KV = d.kv_heads, HD = d.head_dim, E = d.experts, K = d.k, F = d.dff;
+    cudaStream_t st = (cudaStream_t)stream;
+    // the chunk's rows, carved from the caller's workspace; every launch's own scratch comes after them
+    Carve cb = workspace_carve(ws);
+    float* h = cb.take<float>((size_t)(R * D));
+    float* x = mode == 0 ? cb.take<float>((size_t)(R * D)) : nullptr;
+    int8_t* xq = mode == 1 ? cb.take<int8_t>((size_t)(R * D)) : nullptr;
+    float* xs = mode == 1 ? cb.take<float>((size_t)(R * D / 32)) : nullptr;
+    float* q = cb.take<float>((size_t)(R * H * HD));
+    float* k = cb.take<float>((size_t)(R * KV * HD));
+    float* v = cb.take<float>((size_t)(R * KV * HD));
+    float* att = cb.take<float>((size_t)(R * H * HD));
+    int8_t* attq = mode == 1 ? cb.take<int8_t>((size_t)(R * H * HD)) : nullptr;
+    float* atts = mode == 1 ? cb.take<float>((size_t)(R * H * HD / 32)) : nullptr;
+    float* rlog = cb.take<float>((size_t)(R * E));
+    int32_t* ids = cb.take<int32_t>((size_t)(R * K));
+    float* gates = cb.take<float>((size_t)(R * K));
+    PlanPtrs plan;
+    plan.counts = cb.take<int32_t>((size_t)E);
+    plan.offsets = cb.take<int32_t>((size_t)E + 1);
+    plan.lists = cb.take<int32_t>((size_t)(R * K));
+    plan.active = cb.take<int32_t>((size_t)E + 1);
+    float* hm = cb.take<float>((size_t)(R * K * F));
+    int8_t* hmq = mode == 1 ? cb.take<int8_t>((size_t)(R * K * F)) : nullptr;
+    float* hms = mode == 1 ? cb.take<float>((size_t)(R * K * F / 32)) : nullptr;
+    int32_t* posr = cb.take<int32_t>((size_t)R);
+    int* done = cb.take_counters(1);
+    if (cb.overflow) return model_fail(Q8_ENOSPACE, "prefill_chunk: workspace too small for %lld rows", (long long)R);
+    cudaError_t e = cudaSuccess;
+#define Q8_TRY(x)                                                                                                   \
+    do {                                                                                                            \
+        e = (x);                                                                                                    \
+        if (e != cudaSuccess) return model_fail(Q8_ECUDA, "prefill_chunk: %s", cudaGetErrorString(e));             \
+    } while (0)
+#define Q8_TRY_WS(x, cv)                                                                                            \
+    do {                                                                                                            \
+        e = (x);                                                                                                    \
+        if ((cv).overflow) return model_fail(Q8_ENOSPACE, "prefill_chunk: workspace too small for %lld rows",       \
+                                            (long long)R);                                                          \
+        if (e != cudaSuccess) return model_fail(Q8_ECUDA, "prefill_chunk: %s", cudaGetErrorString(e));             \
+    } while (0)
+    auto norm = [&](const float* a, const float* w, int64_t rows) {
+        NormCall n;
+        n.a = a;
+        n.w = w;
+        n.rows = rows;
+        n.d = D;
+        n.eps = d.eps;
+        if (mode == 0) n.y = x;
+        else {
+            n.yq = xq;
+            n.ys = xs;
+        }
+        n.err = m->err;
+        return launch_add_rmsnorm(n, st);
+    };
+    // Plain launches in order, no programmatic overlap: row r's attention reads the cache row that row r - 1's wrote.
+    Q8_TRY(launch_chunk_setup(tokens, R, d.embed, D, d.vocab, d.pos, (int)d.ctx, posr, h, m->err, st));
+    for (int64_t l = 0; l < d.layers; ++l) {
+        Q8_TRY(norm(h, m->attn_norm[l], R));
+        {
+            GemvCall g;
+            g.mode = mode;
+            g.k = D;
+            g.R = R;
+            g.nseg = 3;
+            g.seg[0] = GemvSeg{m->wq[l].q, m->wq[l].s, H * HD, q, nullptr};
+            g.seg[1] = GemvSeg{m->wk[l].q, m->wk[l].s, KV * HD, k, nullptr};
+            g.seg[2] = GemvSeg{m->wv[l].q, m->wv[l].s, KV * HD, v, nullptr};
+            g.x = x;
+            g.xq = xq;
+            g.xs = xs;
+            g.err = m->err;
+            Carve cv = cb;
+            Q8_TRY_WS(launch_gemv(g, cv, st), cv);
+        }
+        for (int64_t r = 0; r < R; ++r) {  // causal: row r attends rows 0 .. *pos + r after appending its own
+            AttnCall a;
+            a.q = q + r * H * HD;
+            a.k = k + r * KV * HD;
+            a.v = v + r * KV * HD;
+            a.q_norm = m->q_norm[l];
+            a.k_norm = m->k_norm[l];
+            a.cos_t = m->cos_t;
+            a.sin_t = m->sin_t;
+            a.eps = d.eps;
+            a.err = m->err;
+            a.k_cache = m->kc[l];
+            a.v_cache = m->vc[l];
+            a.pos = posr + r;
+            a.heads = (int)H;
+            a.kv = (int)KV;
+            a.hd = (int)HD;
+            a.ctx = (int)d.ctx;
+            a.out = att + r * H * HD;
+            if (mode == 1) {
+                a.outq = attq + r * H * HD;
+                a.outs = atts + r * H * HD / 32;
+            }
+            Carve cv = cb;
+            Q8_TRY_WS(launch_attention(a, cv, st), cv);
+        }
+        {
+            GemvCall g;
+            g.mode = mode;
+            g.k = H * HD;
+            g.R = R;
+            g.seg[0] = GemvSeg{m->wo[l].q, m->wo[l].s, D, h, h};  // h = h + o
+            g.x = att;
+            g.xq = attq;
+            g.xs = atts;
+            g.err = m->err;
+            Carve cv = cb;
+            Q8_TRY_WS(launch_gemv(g, cv, st), cv);
+        }
+        Q8_TRY(norm(h, m->ffn_norm[l], R));
+        {
+            GemvCall g;
+            g.mode = mode;
+            g.k = D;
+            g.R = R;
+            g.seg[0] = GemvSeg{m->router[l].q, m->router[l].s, E, rlog, nullptr};
+            g.x = x;
+            g.xq = xq;
+            g.xs = xs;
+            g.err = m->err;
+            Carve cv = cb;
+            Q8_TRY_WS(launch_gemv(g, cv, st), cv);
+            TopkCall t;
+            t.logits = rlog;
+            t.R = R;
+            t.E = E;
+            t.K = (int)K;
+            t.ids = ids;
+            t.gates = gates;
+            t.plan = plan;
+            t.done = done;
+            Q8_TRY(launch_topk(t, st));
+        }
+        {
+            ExpertCall c;
+            c.mode = mode;
+            c.q0 = m->gate[l].q;
+            c.s0 = m->gate[l].s;
+            c.q1 = m->up[l].q;
+            c.s1 = m->up[l].s;
+            c.E = E;
+            c.out_rows = F;
+            c.k = D;
+            c.R = R;
+            c.K = (int)K;
+            c.ids = ids;
+            c.x = x;
+            c.xq = xq;
+            c.xs = xs;
+            c.h = hm;
+            c.plan = plan;
+            c.err = m->err;
+            Carve cv = cb;
+            Q8_TRY_WS(launch_gate_up(c, cv, st), cv);
+            if (mode == 1) Q8_TRY(launch_quantize(hm, R * K * F, hmq, hms, st));
+        }
+        {
+            ExpertCall c;
+            c.mode = mode;
+            c.q0 = m->down[l].q;
+            c.s0 = m->down[l].s;
+            c.E = E;
+            c.out_rows = D;
+            c.k = F;
+            c.R = R;
+            c.K = (int)K;
+            c.ids = ids;
+            c.gates = gates;
+            c.x = mode == 1 ? nullptr : hm;
+            c.xq = hmq;
+            c.xs = hms;
+            c.plan = plan;
+            c.residual = h;  // h = h + mixture
+            c.y = h;
+            c.err = m->err;
+            Carve cv = cb;
+            Q8_TRY_WS(launch_down_combine(c, cv, st), cv);
+        }
+    }
+    // the last row's logits and greedy token; the position ends R rows on
+    Q8_TRY(launch_pos_add(d.pos, (int)(R - 1), m->err, st));
+    {
+        NormCall nf;
+        nf.a = h + (R - 1) * D;
+        nf.w = d.final_norm;
+        nf.rows = 1;
+        nf.d = D;
+        nf.eps = d.eps;
+        if (mode == 0) nf.y = m->x;
+        else {
+            nf.yq = m->xq;
+            nf.ys = m->xs;
+        }
+        Q8_TRY(launch_add_rmsnorm(nf, st));
+        GemvCall g;
+        g.mode = mode;
+        g.k = D;
+        g.seg[0] = GemvSeg{d.lm_head.q, d.lm_head.s, d.vocab, m->logits, nullptr};
+        g.x = m->x;
+        g.xq = m->xq;
+        g.xs = m->xs;
+        g.err = m->err;
+        Carve cv = cb;
+        Q8_TRY_WS(launch_gemv(g, cv, st), cv);
+    }
+    {
+        ArgmaxCall a;
+        a.x = m->logits;
+        a.n = d.vocab;
+        a.tok = d.tok;
+        a.pos = d.pos;
+        a.err = m->err;
+        a.ctx = (int)d.ctx;
+        Carve cv = cb;
+        Q8_TRY_WS(launch_argmax(a, cv, st), cv);
+    }
+#undef Q8_TRY
+#undef Q8_TRY_WS
+    return Q8_OK;
+}
+
 int64_t q8_model_launches_per_step(const q8_model* m) { return m ? m->kernels_per_step : 0; }
 
 int q8_model_check(q8_model* m, q8_stream stream) {

@@ -164,3 +164,98 @@ def test_decode_full_config_one_step(q8, mode):
         assert rel_err(t["k_cache"][l].cpu().numpy()[:, -1], om.k_cache[l][:, -1]) < 10 * TOL[mode]
         assert rel_err(t["v_cache"][l].cpu().numpy()[:, -1], om.v_cache[l][:, -1]) < 10 * TOL[mode]
     m.close()
+
+
+# ---- prefill chunks: R token rows through every layer ---------------------------------------------------------------
+
+def _prefill_vs_oracle(q8, cfg, mode, R, pos0, tokens, seed):
+    import torch
+    m, arr, t, tok, pos, logits = build(q8, cfg, seed, mode)
+    om = oracle.ModelArrays(cfg, **arr)
+    ws = q8.Workspace(128 << 20)
+    pos.fill_(pos0)
+    tok.fill_(0)
+    toks = torch.tensor(tokens, dtype=torch.int32, device="cuda")
+    m.prefill(toks, ws)
+    torch.cuda.synchronize()
+    for r, tk in enumerate(tokens):  # the oracle: R decode steps fed the same tokens
+        nxt, ora_logits = oracle.decode_step(mode, om, tk, pos0 + r)
+    gl = logits.cpu().numpy()
+    assert rel_err(gl, ora_logits) < TOL[mode], rel_err(gl, ora_logits)
+    srt = np.sort(ora_logits)[::-1]
+    if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
+        assert int(tok.item()) == nxt
+    assert int(pos.item()) == pos0 + R
+    for l in range(cfg["layers"]):  # every row's key and value at its position
+        kc, vc = t["k_cache"][l].cpu().numpy(), t["v_cache"][l].cpu().numpy()
+        rows = slice(pos0, pos0 + R)
+        assert rel_err(kc[:, rows], om.k_cache[l][:, rows]) < 10 * TOL[mode]
+        assert rel_err(vc[:, rows], om.v_cache[l][:, rows]) < 10 * TOL[mode]
+    m.check()
+    ws.close()
+    return m, tok, pos, logits
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("cfg,R", [(SMALL, 1), (SMALL, 5), (SMALL, 17), (UNFUSED, 6)], ids=["s1", "s5", "s17", "u6"])
+def test_prefill_chunk_matches_oracle(q8, mode, cfg, R):
+    rng = np.random.default_rng(R)
+    tokens = [int(v) for v in rng.integers(0, cfg["vocab"], R)]
+    m, tok, pos, logits = _prefill_vs_oracle(q8, cfg, mode, R, 40 if cfg is SMALL else 30, tokens, 11)
+    m.close()
+
+
+def test_prefill_chunk_same_token_rows_group_experts(q8):
+    """Eight copies of one token: every row routes alike at the first layer, so the chunk's expert groups hold all
+    rows (the grouped products with their largest groups)."""
+    m, tok, pos, logits = _prefill_vs_oracle(q8, SMALL, 1, 8, 20, [5] * 8, 12)
+    m.close()
+
+
+def test_prefill_then_decode_continues(q8):
+    """A prefill leaves token and position where the next decode step starts: prefill(tokens[:-1]) then one decode
+    step of tokens[-1] gives the oracle's logits after all of them."""
+    import torch
+    cfg, mode = SMALL, 1
+    tokens = [3, 141, 59, 26, 535, 897]
+    m, arr, t, tok, pos, logits = build(q8, cfg, 13, mode)
+    om = oracle.ModelArrays(cfg, **arr)
+    ws = q8.Workspace(64 << 20)
+    pos.fill_(50)
+    m.prefill(torch.tensor(tokens[:-1], dtype=torch.int32, device="cuda"), ws)
+    torch.cuda.synchronize()
+    assert int(pos.item()) == 50 + len(tokens) - 1
+    tok.fill_(tokens[-1])
+    m.step()
+    torch.cuda.synchronize()
+    for r, tk in enumerate(tokens):
+        _, ora_logits = oracle.decode_step(mode, om, tk, 50 + r)
+    assert rel_err(logits.cpu().numpy(), ora_logits) < TOL[mode]
+    m.check()
+    ws.close()
+    m.close()
+
+
+def test_prefill_past_the_cache_is_flagged(q8):
+    import torch
+    m, arr, t, tok, pos, logits = build(q8, SMALL, 14, 0)
+    ws = q8.Workspace(64 << 20)
+    pos.fill_(SMALL["ctx"] - 2)  # rows 2 and 3 of 4 fall past the cache
+    m.prefill(torch.tensor([1, 2, 3, 4], dtype=torch.int32, device="cuda"), ws)
+    torch.cuda.synchronize()
+    assert int(pos.item()) == SMALL["ctx"] - 2  # an error leaves the position where it was
+    with pytest.raises(q8.Q8Error, match="position"):
+        m.check()
+    ws.close()
+    m.close()
+
+
+def test_prefill_full_width_two_layers(q8):
+    """The full layer width (d 2048, 32 q / 4 kv heads, 128 experts, top-8, dff 768) on two layers, a chunk of 8 rows
+    near the end of a 4096-row cache, against the oracle."""
+    cfg = dict(recipes.DECODE, layers=2, vocab=1000)
+    rng = np.random.default_rng(3)
+    tokens = [int(v) for v in rng.integers(0, cfg["vocab"], 8)]
+    m, tok, pos, logits = _prefill_vs_oracle(q8, cfg, 1, 8, 4000, tokens, 15)
+    m.close()
+
