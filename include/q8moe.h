@@ -216,8 +216,8 @@ Q8_API int decode_step(q8_model *model, q8_stream stream);
 /* The same step as plain launches, without a graph (for tests and graph-capture by the caller). */
 Q8_API int decode_step_launches(q8_model *model, q8_stream stream);
 /* A chunk of `rows` token rows through every layer (the prefill of a prompt chunk): tokens is device int32 [rows]; row
- * r takes position *pos + r.  Each layer: RMSNorm of the rows, the q/k/v projection of all rows, then for each row in
- * turn QK-norm, RoPE, the key/value append at its position and attention over rows 0 .. its position (causal), the O
+ * r takes position *pos + r.  Each layer: RMSNorm of the rows, the q/k/v projection of all rows, QK-norm, RoPE and the
+ * key/value append of every row at its position, then each row's attention over rows 0 .. its position (causal), the O
  * projection onto the residual, RMSNorm, routing with the expert grouping, gate-up and down-and-combine of the chunk
  * (each chosen expert's weights read once for all its rows).  Then the last row's final norm, LM head and greedy token
  * into *tok; *pos advances by `rows`.  The result equals `rows` decode steps fed these tokens (up to the summation

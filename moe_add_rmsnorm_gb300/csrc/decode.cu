@@ -526,6 +526,247 @@ __global__ void __launch_bounds__(256) chunk_setup_kernel(const int32_t* tokens,
     }
 }
 
+// The chunk's rows at their positions: per-head QK-norm and RoPE of every row's queries (into qr) and keys, and the
+// keys and values appended to the caches, before any row attends.  A CTA per row, a warp per head vector, lane l
+// holding dims l, l + 32, l + 64, l + 96 (so the rotation pairs (i, i + 64) sit in one lane).
+__global__ void __launch_bounds__(256) chunk_append_kernel(const float* q, const float* k, const float* v,
+                                                           const float* q_norm, const float* k_norm,
+                                                           const float* cos_t, const float* sin_t, float eps,
+                                                           const int32_t* posr, int heads, int kv, int ctx,
+                                                           float* k_cache, float* v_cache, float* qr) {
+    const int r = blockIdx.x, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int pos = posr[r];
+    if (pos < 0 || pos >= ctx) return;  // flagged by the chunk setup
+    for (int hv = wid; hv < heads + 2 * kv; hv += blockDim.x / 32) {
+        if (hv >= heads + kv) {  // a value row: copied
+            const int g = hv - heads - kv;
+            const float* src = v + ((int64_t)r * kv + g) * ATT_HD;
+            float* dst = v_cache + ((int64_t)g * ctx + pos) * ATT_HD;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[lane + 32 * j] = src[lane + 32 * j];
+            continue;
+        }
+        const bool isq = hv < heads;
+        const float* src = isq ? q + ((int64_t)r * heads + hv) * ATT_HD : k + ((int64_t)r * kv + (hv - heads)) * ATT_HD;
+        const float* w = isq ? q_norm : k_norm;
+        float x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = src[lane + 32 * j];
+        const float ss = group_sum<32>((x[0] * x[0] + x[2] * x[2]) + (x[1] * x[1] + x[3] * x[3]));
+        const float inv = 1.0f / sqrtf(ss / (float)ATT_HD + eps);
+        float y[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) y[j] = x[j] * inv * w[lane + 32 * j];
+        // NeoX rotation of (i, i + 64): dims lane + 32j for j = 0, 1 pair with j = 2, 3
+        float o[4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int i = lane + 32 * j;
+            const float cs = cos_t[(int64_t)pos * (ATT_HD / 2) + i], sn = sin_t[(int64_t)pos * (ATT_HD / 2) + i];
+            o[j] = y[j] * cs - y[j + 2] * sn;
+            o[j + 2] = y[j] * sn + y[j + 2] * cs;
+        }
+        float* dst = isq ? qr + ((int64_t)r * heads + hv) * ATT_HD
+                         : k_cache + ((int64_t)(hv - heads) * ctx + pos) * ATT_HD;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[lane + 32 * j] = o[j];
+    }
+}
+
+// Causal attention of a chunk's rows, split over positions: CTA (key/value head g, position group pg, row block rb)
+// takes rows rb*ACH_RB .. +ACH_RB-1 (every query head of the group: ACH_RB * G query vectors) against positions
+// pg*ACH_GROUP*64 .. +ACH_GROUP*64-1 in chunks of 64, keeping a running (max, sum, weighted values) per query vector
+// (online softmax, chunks in order); row r attends positions 0 .. posr[r].  The group's result (max, sum, 128
+// weighted values) goes to part[r][head][pg] when the row had any position in the group (max > -inf).
+constexpr int ACH_RB = 8;      // rows per CTA
+constexpr int ACH_GROUP = 8;   // 64-position chunks per CTA
+constexpr int ACH_PAIRS = ACH_RB * ATT_MAXG;  // query vectors per CTA
+constexpr int ACH_KP = ATT_HD + 1;             // padded key / query row in shared memory
+constexpr int ACH_PS = ATT_HD + 4;             // a group result: 128 weighted values, max, sum (16-byte rows)
+constexpr size_t ACH_SMEM = (size_t)(64 * ACH_KP + 64 * ATT_HD + ACH_PAIRS * ACH_KP + ACH_PAIRS * 65 + 3 * ACH_PAIRS) *
+                            sizeof(float);
+
+__global__ void __launch_bounds__(256, 1) chunk_attention_kernel(const float* qr, const float* k_cache,
+                                                                 const float* v_cache, const int32_t* posr, int R,
+                                                                 int heads, int kv, int ctx, float scale, float* part,
+                                                                 int ngroups) {
+    extern __shared__ __align__(16) float acs[];
+    float* ks = acs;                           // [64][ACH_KP]
+    float* vs = ks + 64 * ACH_KP;              // [64][128]
+    float* qs = vs + 64 * ATT_HD;              // [pairs][ACH_KP]
+    float* sc = qs + ACH_PAIRS * ACH_KP;       // [pairs][65]
+    float* mrun = sc + ACH_PAIRS * 65;         // [pairs] running max
+    float* lrun = mrun + ACH_PAIRS;            // [pairs] running sum
+    float* fold = lrun + ACH_PAIRS;            // [pairs] rescale of this chunk
+    const int g = blockIdx.x, pg = blockIdx.y, rb = blockIdx.z;
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int G = heads / kv;
+    const int r0 = rb * ACH_RB, nr = min(ACH_RB, R - r0);
+    if (nr <= 0) return;
+    int maxpos = -1;
+    for (int i = 0; i < nr; ++i) maxpos = max(maxpos, min(posr[r0 + i], ctx - 1));
+    const int p_begin = pg * ACH_GROUP * 64;
+    if (p_begin > maxpos) return;  // every row of the block ends before this group
+    // the block's queries: pair = row_in_block * G + head_in_group
+    for (int i = t; i < ACH_PAIRS * ATT_HD; i += blockDim.x) {
+        const int pr = i / ATT_HD, d = i % ATT_HD, rr = pr / ATT_MAXG, hh = pr % ATT_MAXG;
+        const bool ok = rr < nr && hh < G;
+        qs[pr * ACH_KP + d] = ok ? qr[((int64_t)(r0 + rr) * heads + g * G + hh) * ATT_HD + d] : 0.f;
+    }
+    for (int i = t; i < ACH_PAIRS; i += blockDim.x) {
+        mrun[i] = -FLT_MAX;
+        lrun[i] = 0.f;
+    }
+    // values: thread t owns dims 4*lane .. +3 of pairs wid, wid + 8, ... (8 pairs)
+    float4 acc[ACH_PAIRS / 8];
+#pragma unroll
+    for (int i = 0; i < ACH_PAIRS / 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // scores: thread t takes positions 4*(t%16) .. +3 and pairs 4*(t/16) .. +3
+    const int tp = t % 16, tq = t / 16;
+    for (int cc = 0; cc < ACH_GROUP; ++cc) {
+        const int p0 = p_begin + cc * 64;
+        if (p0 > maxpos) break;  // CTA-uniform
+        __syncthreads();  // the previous chunk's rows and weights are no longer read
+        for (int i = t; i < 64 * (ATT_HD / 4); i += blockDim.x) {
+            const int pl = i / (ATT_HD / 4), d4 = i % (ATT_HD / 4);
+            const int p = p0 + pl;
+            float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
+            if (p <= maxpos) {
+                kv4 = __ldcg(reinterpret_cast<const float4*>(k_cache + ((int64_t)g * ctx + p) * ATT_HD) + d4);
+                vv4 = __ldcg(reinterpret_cast<const float4*>(v_cache + ((int64_t)g * ctx + p) * ATT_HD) + d4);
+            }
+            float* kd = ks + pl * ACH_KP + 4 * d4;
+            kd[0] = kv4.x;
+            kd[1] = kv4.y;
+            kd[2] = kv4.z;
+            kd[3] = kv4.w;
+            reinterpret_cast<float4*>(vs + pl * ATT_HD)[d4] = vv4;
+        }
+        __syncthreads();
+        {
+            float a[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) a[i][j] = 0.f;
+            for (int d = 0; d < ATT_HD; ++d) {
+                float kk[4], qq[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) kk[i] = ks[(4 * tp + i) * ACH_KP + d];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) qq[j] = qs[(4 * tq + j) * ACH_KP + d];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) a[i][j] = fmaf(qq[j], kk[i], a[i][j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int pr = 4 * tq + j, rr = pr / ATT_MAXG;
+                const int lim = rr < nr ? min(posr[r0 + rr], ctx - 1) : -1;  // the row's last position
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int p = p0 + 4 * tp + i;
+                    sc[pr * 65 + 4 * tp + i] = p <= lim ? a[i][j] * scale : -FLT_MAX;
+                }
+            }
+        }
+        __syncthreads();
+        // softmax update per pair (warp w takes pairs w, w + 8, ...)
+        for (int pr = wid; pr < ACH_PAIRS; pr += 8) {
+            const float s0 = sc[pr * 65 + lane], s1 = sc[pr * 65 + lane + 32];
+            const float cm = warp_max(fmaxf(s0, s1));
+            const float mo = mrun[pr];
+            const float mn = fmaxf(mo, cm);
+            float e0 = 0.f, e1 = 0.f, f = 1.f;
+            if (mn != -FLT_MAX) {
+                e0 = s0 == -FLT_MAX ? 0.f : expf(s0 - mn);
+                e1 = s1 == -FLT_MAX ? 0.f : expf(s1 - mn);
+                f = mo == -FLT_MAX ? 0.f : expf(mo - mn);
+            }
+            sc[pr * 65 + lane] = e0;
+            sc[pr * 65 + lane + 32] = e1;
+            const float cs = group_sum<32>(e0 + e1);
+            if (lane == 0) {
+                lrun[pr] = lrun[pr] * f + cs;
+                mrun[pr] = mn;
+                fold[pr] = f;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < ACH_PAIRS / 8; ++i) {
+            const int pr = wid + 8 * i;
+            const float f = fold[pr];
+            float4 a4 = acc[i];
+            a4.x *= f;
+            a4.y *= f;
+            a4.z *= f;
+            a4.w *= f;
+            for (int p = 0; p < 64; ++p) {
+                const float e = sc[pr * 65 + p];
+                const float4 v4 = reinterpret_cast<const float4*>(vs + p * ATT_HD)[lane];
+                a4.x = fmaf(e, v4.x, a4.x);
+                a4.y = fmaf(e, v4.y, a4.y);
+                a4.z = fmaf(e, v4.z, a4.z);
+                a4.w = fmaf(e, v4.w, a4.w);
+            }
+            acc[i] = a4;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < ACH_PAIRS / 8; ++i) {
+        const int pr = wid + 8 * i, rr = pr / ATT_MAXG, hh = pr % ATT_MAXG;
+        if (rr >= nr || hh >= G) continue;
+        float* dst = part + (((int64_t)(r0 + rr) * heads + g * G + hh) * ngroups + pg) * ACH_PS;
+        reinterpret_cast<float4*>(dst)[lane] = acc[i];
+        if (lane == 0) {
+            dst[ATT_HD] = mrun[pr];
+            dst[ATT_HD + 1] = lrun[pr];
+        }
+    }
+}
+
+// Row r, head h: the position groups' results folded in group order, out = num / den, and its int8 form.  A warp
+// per (row, head), lane l the dims l, l + 32, l + 64, l + 96.
+__global__ void __launch_bounds__(256) chunk_attn_fold_kernel(const float* part, const int32_t* posr, int R, int heads,
+                                                              int ctx, int ngroups, float* out, int8_t* outq,
+                                                              float* outs) {
+    const int wg = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (wg >= R * heads) return;
+    const int r = wg / heads;
+    const int pos = posr[r];
+    if (pos < 0 || pos >= ctx) return;
+    const int ng = min(ngroups, pos / (ACH_GROUP * 64) + 1);
+    const float* base = part + (int64_t)wg * ngroups * ACH_PS;
+    float M = -FLT_MAX;
+    for (int c = 0; c < ng; ++c) M = fmaxf(M, __ldcg(base + (int64_t)c * ACH_PS + ATT_HD));
+    float num[4] = {0.f, 0.f, 0.f, 0.f}, den = 0.f;
+    for (int c = 0; c < ng; ++c) {
+        const float* b = base + (int64_t)c * ACH_PS;
+        const float mc = __ldcg(b + ATT_HD);
+        if (mc == -FLT_MAX) continue;
+        const float f = expf(mc - M);
+        den = fmaf(f, __ldcg(b + ATT_HD + 1), den);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) num[j] = fmaf(f, __ldcg(b + lane + 32 * j), num[j]);
+    }
+    // the partials' values sit in float4 order (lane l held dims 4l..4l+3): dim d is at index d
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float o = num[j] / den;
+        const int64_t oi = (int64_t)wg * ATT_HD + lane + 32 * j;
+        out[oi] = o;
+        if (outq) {
+            float dsc;
+            const int8_t qv = quantize_lane(o, dsc);
+            outq[oi] = qv;
+            if (lane == 0) outs[oi / 32] = dsc;
+        }
+    }
+}
+
 // *pos += add, unless the step's error word is set.
 __global__ void pos_add_kernel(int32_t* pos, int add, const int* err) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && !(err && *err)) *pos += add;
@@ -621,4 +862,35 @@ cudaError_t launch_pos_add(int32_t* pos, int add, const int* err, cudaStream_t s
     return cudaGetLastError();
 }
 
+int chunk_attn_groups(int ctx) { return (ctx + ACH_GROUP * 64 - 1) / (ACH_GROUP * 64); }
+
+void chunk_attention_scratch(int64_t rows, int heads, int ctx, size_t* bytes) {
+    *bytes = (size_t)rows * heads * chunk_attn_groups(ctx) * ACH_PS * sizeof(float) +
+             (size_t)rows * heads * ATT_HD * sizeof(float);
+}
+
+cudaError_t launch_chunk_attention(const ChunkAttnCall& c, Carve& ws, cudaStream_t st) {
+    if (c.hd != ATT_HD || c.heads % c.kv || c.heads / c.kv > ATT_MAXG || c.rows < 1) return cudaErrorInvalidValue;
+    const int ng = chunk_attn_groups(c.ctx);
+    float* qr = ws.take<float>((size_t)c.rows * c.heads * ATT_HD);
+    float* part = ws.take<float>((size_t)c.rows * c.heads * ng * ACH_PS);
+    if (ws.overflow) return cudaErrorMemoryAllocation;
+    chunk_append_kernel<<<(unsigned)c.rows, 256, 0, st>>>(c.q, c.k, c.v, c.q_norm, c.k_norm, c.cos_t, c.sin_t, c.eps,
+                                                          c.posr, c.heads, c.kv, c.ctx, c.k_cache, c.v_cache, qr);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(chunk_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ACH_SMEM);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)c.kv, (unsigned)ng, (unsigned)((c.rows + ACH_RB - 1) / ACH_RB));
+    chunk_attention_kernel<<<grid, 256, ACH_SMEM, st>>>(qr, c.k_cache, c.v_cache, c.posr, (int)c.rows, c.heads, c.kv,
+                                                       c.ctx, (float)(1.0 / sqrt((double)c.hd)), part, ng);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t warps = c.rows * c.heads;
+    chunk_attn_fold_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(part, c.posr, (int)c.rows, c.heads, c.ctx, ng,
+                                                                       c.out, c.outq, c.outs);
+    return cudaGetLastError();
+}
+
 }  // namespace q8
+

@@ -253,6 +253,29 @@ cudaError_t launch_rope_table(float* cos_t, float* sin_t, int ctx, int half, dou
 // A chunk of token rows: the residual rows gathered from the embedding and each row's position (*pos + r).
 cudaError_t launch_chunk_setup(const int32_t* tokens, int64_t rows, const float* embed, int64_t D, int64_t vocab,
                                const int32_t* pos, int ctx, int32_t* posr, float* h, int* err, cudaStream_t st);
+// Causal attention of a chunk of rows (row r at position posr[r]): QK-norm + RoPE of every row and the cache append
+// first, then the rows attend their positions, split over position groups and folded.
+struct ChunkAttnCall {
+    const float* q = nullptr;       // [rows][heads][hd], before QK-norm and RoPE
+    const float* k = nullptr;       // [rows][kv][hd]
+    const float* v = nullptr;       // [rows][kv][hd]
+    const float* q_norm = nullptr;
+    const float* k_norm = nullptr;
+    const float* cos_t = nullptr;
+    const float* sin_t = nullptr;
+    float eps = 0.f;
+    float* k_cache = nullptr;       // [kv][ctx][hd]
+    float* v_cache = nullptr;
+    const int32_t* posr = nullptr;  // [rows]
+    int64_t rows = 0;
+    int heads = 0, kv = 0, hd = 0, ctx = 0;
+    float* out = nullptr;           // [rows][heads][hd]
+    int8_t* outq = nullptr;         // optional quantized output
+    float* outs = nullptr;
+};
+void chunk_attention_scratch(int64_t rows, int heads, int ctx, size_t* bytes);
+cudaError_t launch_chunk_attention(const ChunkAttnCall& c, Carve& ws, cudaStream_t st);
+
 // *pos += add on the device, unless *err is set.
 cudaError_t launch_pos_add(int32_t* pos, int add, const int* err, cudaStream_t st);
 

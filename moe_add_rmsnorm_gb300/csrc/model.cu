@@ -609,7 +609,7 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
         n.err = m->err;
         return launch_add_rmsnorm(n, st);
     };
-    // Plain launches in order, no programmatic overlap: row r's attention reads the cache row that row r - 1's wrote.
+    // Plain launches in order, no programmatic overlap (each launch reads what the one before it wrote).
     Q8_TRY(launch_chunk_setup(tokens, R, d.embed, D, d.vocab, d.pos, (int)d.ctx, posr, h, m->err, st));
     for (int64_t l = 0; l < d.layers; ++l) {
         Q8_TRY(norm(h, m->attn_norm[l], R));
@@ -629,31 +629,29 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
             Carve cv = cb;
             Q8_TRY_WS(launch_gemv(g, cv, st), cv);
         }
-        for (int64_t r = 0; r < R; ++r) {  // causal: row r attends rows 0 .. *pos + r after appending its own
-            AttnCall a;
-            a.q = q + r * H * HD;
-            a.k = k + r * KV * HD;
-            a.v = v + r * KV * HD;
+        {  // every row's keys and values appended, then each row attends rows 0 .. its position (causal)
+            ChunkAttnCall a;
+            a.q = q;
+            a.k = k;
+            a.v = v;
             a.q_norm = m->q_norm[l];
             a.k_norm = m->k_norm[l];
             a.cos_t = m->cos_t;
             a.sin_t = m->sin_t;
             a.eps = d.eps;
-            a.err = m->err;
             a.k_cache = m->kc[l];
             a.v_cache = m->vc[l];
-            a.pos = posr + r;
+            a.posr = posr;
+            a.rows = R;
             a.heads = (int)H;
             a.kv = (int)KV;
             a.hd = (int)HD;
             a.ctx = (int)d.ctx;
-            a.out = att + r * H * HD;
-            if (mode == 1) {
-                a.outq = attq + r * H * HD;
-                a.outs = atts + r * H * HD / 32;
-            }
+            a.out = att;
+            a.outq = attq;
+            a.outs = atts;
             Carve cv = cb;
-            Q8_TRY_WS(launch_attention(a, cv, st), cv);
+            Q8_TRY_WS(launch_chunk_attention(a, cv, st), cv);
         }
         {
             GemvCall g;
