@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--chunk-only", type=int, default=0, metavar="R",
                     help="only the R-row chunk timing through the mixture block (for a profiler capture of its kernels)")
     ap.add_argument("--correlated", action="store_true", help="with --chunk-only: rows that share their experts")
+    ap.add_argument("--prefill-only", type=int, default=0, metavar="R",
+                    help="only the R-row prefill timing through the model (for a profiler capture of its kernels)")
     return ap.parse_args()
 
 
@@ -334,6 +336,45 @@ def time_chunks(q8, cfg, dev, stream, reps=4, correlated=False, rows=(2, 4, 8, 1
     return out
 
 
+def time_prefill(q8, model, cfg, tok, pos, stream, rows=(16, 64), reps=3):
+    """Prefill chunks of R token rows through the whole model (every layer, the last row's LM head and token),
+    starting at position ctx - 128 - R, timed with CUDA events around `reps` calls (plain launches, no graph); the
+    caches' rows are rewritten each call.  tokens/s = R / time per chunk; weight bytes per chunk count every dense
+    matrix once, the router, and the experts the chunk's routing touched at every layer (estimated from uniform routing
+    as E * (1 - (1 - K/E)^R))."""
+    import torch
+    L, d, E, K, dff = cfg["layers"], cfg["d"], cfg["experts"], cfg["k"], cfg["dff"]
+    H, KV, HD = cfg["heads"], cfg["kv_heads"], cfg["hd"]
+    dense = (H * HD + 2 * KV * HD) * d + d * H * HD + E * d
+    expert = 3 * dff * d
+    ws = q8.Workspace(512 << 20)
+    s = torch.cuda.ExternalStream(stream)
+    out = []
+    with torch.cuda.stream(s):
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(7)
+        for R in rows:
+            toks = torch.randint(0, cfg["vocab"], (R,), dtype=torch.int32, device="cuda", generator=gen)
+            p0 = cfg["ctx"] - 128 - R
+            pos.fill_(p0)
+            model.prefill(toks, ws, stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.synchronize()
+            e0.record(s)
+            for _ in range(reps):
+                pos.fill_(p0)
+                model.prefill(toks, ws, stream)
+            e1.record(s)
+            e1.synchronize()
+            t = e0.elapsed_time(e1) / 1e3 / reps
+            u = E * (1.0 - (1.0 - K / E) ** R)
+            wbytes = L * (dense + u * expert) * 9 // 8 + cfg["vocab"] * d * 9 // 8
+            out.append({"rows": R, "tokens_per_s": R / t, "ms_per_chunk": t * 1e3, "weight_gbs": wbytes / t / 1e9,
+                        "unique_experts_per_layer_est": u})
+    ws.close()
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -369,6 +410,11 @@ def main():
                           "gbs": dom_bytes / dom_sec / 1e9}), flush=True)
         return
     model = q8.Model(cfg, dev, mode, tok, pos, logits)
+    if args.prefill_only:
+        res = time_prefill(q8, model, cfg, tok, pos, sh, rows=(args.prefill_only,), reps=max(1, args.steps))
+        print(json.dumps({"prefill_only": True, **res[0]}), flush=True)
+        model.close()
+        return
 
     def barrier():
         if world > 1:
@@ -479,6 +525,8 @@ def main():
             line["secondary"] = {"mode": "f32-activation/f64-sum" if other == q8.F32ACT_F64SUM else "int8-activation",
                                  "tokens_per_s": args.steps / s2, "weight_stream_gbs": wbytes * args.steps / s2 / 1e9}
             m2.close()
+            line["prefill"] = {"what": "prefill_chunk through all layers (plain launches), positions ctx-128-R ..",
+                               "results": time_prefill(q8, model, cfg, tok, pos, sh)}
             line["chunks"] = {
                 "what": "R-row chunks through the mixture block (int8: quantize, route + grouping, gate-up, "
                         "down-and-combine), another layer's experts per chunk, one CUDA graph of 8 chunks per R",
