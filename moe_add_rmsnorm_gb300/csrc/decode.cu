@@ -577,27 +577,31 @@ __global__ void __launch_bounds__(256) chunk_append_kernel(const float* q, const
 // takes rows rb*ACH_RB .. +ACH_RB-1 (every query head of the group: ACH_RB * G query vectors) against positions
 // pg*ACH_GROUP*64 .. +ACH_GROUP*64-1 in chunks of 64, keeping a running (max, sum, weighted values) per query vector
 // (online softmax, chunks in order); row r attends positions 0 .. posr[r].  The group's result (max, sum, 128
-// weighted values) goes to part[r][head][pg] when the row had any position in the group (max > -inf).
+// weighted values) goes to part[r][head][pg] when the row had any position in the group.
+// Scores as in the one-row attention: warp w takes positions 8w .. 8w+7 of a chunk, four lanes a position (a 32-dim
+// quarter each, the key row in registers, the next chunk's already in flight) against the queries in shared memory.
+// Values: the chunk's value rows arrive in shared memory by cp.async while the scores are formed; thread (w, lane)
+// owns dims 4*lane .. +3 of query vectors w, w + 8, ..., reading each value row once for all of them.
 constexpr int ACH_RB = 8;      // rows per CTA
-constexpr int ACH_GROUP = 8;   // 64-position chunks per CTA
+constexpr int ACH_GROUP = 4;   // 64-position chunks per CTA
 constexpr int ACH_PAIRS = ACH_RB * ATT_MAXG;  // query vectors per CTA
-constexpr int ACH_KP = ATT_HD + 1;             // padded key / query row in shared memory
+constexpr int ACH_QS = 4 * ATT_QP;             // a query vector in shared memory: four padded 32-dim quarters
 constexpr int ACH_PS = ATT_HD + 4;             // a group result: 128 weighted values, max, sum (16-byte rows)
-constexpr size_t ACH_SMEM = (size_t)(64 * ACH_KP + 64 * ATT_HD + ACH_PAIRS * ACH_KP + ACH_PAIRS * 65 + 3 * ACH_PAIRS) *
+constexpr size_t ACH_SMEM = (size_t)(64 * ATT_HD + ACH_PAIRS * ACH_QS + ACH_PAIRS * 65 + 3 * ACH_PAIRS + 16) *
                             sizeof(float);
 
-__global__ void __launch_bounds__(256, 1) chunk_attention_kernel(const float* qr, const float* k_cache,
+__global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr, const float* k_cache,
                                                                  const float* v_cache, const int32_t* posr, int R,
                                                                  int heads, int kv, int ctx, float scale, float* part,
                                                                  int ngroups) {
     extern __shared__ __align__(16) float acs[];
-    float* ks = acs;                           // [64][ACH_KP]
-    float* vs = ks + 64 * ACH_KP;              // [64][128]
-    float* qs = vs + 64 * ATT_HD;              // [pairs][ACH_KP]
-    float* sc = qs + ACH_PAIRS * ACH_KP;       // [pairs][65]
+    float* vs = acs;                           // [64][128]
+    float* qs = vs + 64 * ATT_HD;              // [pairs][4][ATT_QP]
+    float* sc = qs + ACH_PAIRS * ACH_QS;       // [pairs][65]
     float* mrun = sc + ACH_PAIRS * 65;         // [pairs] running max
     float* lrun = mrun + ACH_PAIRS;            // [pairs] running sum
     float* fold = lrun + ACH_PAIRS;            // [pairs] rescale of this chunk
+    int* lim = reinterpret_cast<int*>(fold + ACH_PAIRS);  // [ACH_RB] each row's last position
     const int g = blockIdx.x, pg = blockIdx.y, rb = blockIdx.z;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int G = heads / kv;
@@ -607,72 +611,82 @@ __global__ void __launch_bounds__(256, 1) chunk_attention_kernel(const float* qr
     for (int i = 0; i < nr; ++i) maxpos = max(maxpos, min(posr[r0 + i], ctx - 1));
     const int p_begin = pg * ACH_GROUP * 64;
     if (p_begin > maxpos) return;  // every row of the block ends before this group
-    // the block's queries: pair = row_in_block * G + head_in_group
+    const int nchunk = min(ACH_GROUP, (maxpos - p_begin) / 64 + 1);
+    const int sub = lane & 3, pl = wid * 8 + (lane >> 2);  // score role: position pl of the chunk, dims 32*sub ..
+    auto load_k = [&](int cc, float (&kr)[32]) {
+        const int p = p_begin + cc * 64 + pl;
+        if (cc < nchunk && p <= maxpos) {
+            const float* kp = k_cache + ((int64_t)g * ctx + p) * ATT_HD + sub * 32;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ld_f8_stream(kp + 8 * i, &kr[8 * i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) kr[i] = 0.f;
+        }
+    };
+    auto load_v = [&](int cc) {  // the chunk's value rows into vs by cp.async (rows past maxpos: zeros)
+        for (int i = t; i < 64 * (ATT_HD / 4); i += blockDim.x) {
+            const int row = i / (ATT_HD / 4), d4 = i % (ATT_HD / 4);
+            const int p = p_begin + cc * 64 + row;
+            float* dst = vs + row * ATT_HD + 4 * d4;
+            if (p <= maxpos)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                             "l"(v_cache + ((int64_t)g * ctx + p) * ATT_HD + 4 * d4) : "memory");
+            else
+                *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    float kr[32], krn[32];
+    load_k(0, kr);
+    load_v(0);
+    // the block's queries: pair = row_in_block * ATT_MAXG + head_in_group
     for (int i = t; i < ACH_PAIRS * ATT_HD; i += blockDim.x) {
         const int pr = i / ATT_HD, d = i % ATT_HD, rr = pr / ATT_MAXG, hh = pr % ATT_MAXG;
         const bool ok = rr < nr && hh < G;
-        qs[pr * ACH_KP + d] = ok ? qr[((int64_t)(r0 + rr) * heads + g * G + hh) * ATT_HD + d] : 0.f;
+        qs[pr * ACH_QS + (d >> 5) * ATT_QP + (d & 31)] =
+            ok ? qr[((int64_t)(r0 + rr) * heads + g * G + hh) * ATT_HD + d] : 0.f;
     }
     for (int i = t; i < ACH_PAIRS; i += blockDim.x) {
         mrun[i] = -FLT_MAX;
         lrun[i] = 0.f;
     }
-    // values: thread t owns dims 4*lane .. +3 of pairs wid, wid + 8, ... (8 pairs)
+    if (t < ACH_RB) lim[t] = t < nr ? min(posr[r0 + t], ctx - 1) : -1;
     float4 acc[ACH_PAIRS / 8];
 #pragma unroll
     for (int i = 0; i < ACH_PAIRS / 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    // scores: thread t takes positions 4*(t%16) .. +3 and pairs 4*(t/16) .. +3
-    const int tp = t % 16, tq = t / 16;
-    for (int cc = 0; cc < ACH_GROUP; ++cc) {
+    __syncthreads();
+    for (int cc = 0; cc < nchunk; ++cc) {
         const int p0 = p_begin + cc * 64;
-        if (p0 > maxpos) break;  // CTA-uniform
-        __syncthreads();  // the previous chunk's rows and weights are no longer read
-        for (int i = t; i < 64 * (ATT_HD / 4); i += blockDim.x) {
-            const int pl = i / (ATT_HD / 4), d4 = i % (ATT_HD / 4);
-            const int p = p0 + pl;
-            float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
-            if (p <= maxpos) {
-                kv4 = __ldcg(reinterpret_cast<const float4*>(k_cache + ((int64_t)g * ctx + p) * ATT_HD) + d4);
-                vv4 = __ldcg(reinterpret_cast<const float4*>(v_cache + ((int64_t)g * ctx + p) * ATT_HD) + d4);
-            }
-            float* kd = ks + pl * ACH_KP + 4 * d4;
-            kd[0] = kv4.x;
-            kd[1] = kv4.y;
-            kd[2] = kv4.z;
-            kd[3] = kv4.w;
-            reinterpret_cast<float4*>(vs + pl * ATT_HD)[d4] = vv4;
-        }
-        __syncthreads();
-        {
-            float a[4][4];
+        load_k(cc + 1, krn);  // the next chunk's keys, in flight while this chunk is worked
+        // scores of every query vector against this lane group's position (four vectors at a time: four independent
+        // FMA chains)
+        for (int pr0 = 0; pr0 < ACH_PAIRS; pr0 += 4) {
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) a[i][j] = 0.f;
-            for (int d = 0; d < ATT_HD; ++d) {
-                float kk[4], qq[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) kk[i] = ks[(4 * tp + i) * ACH_KP + d];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) qq[j] = qs[(4 * tq + j) * ACH_KP + d];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) a[i][j] = fmaf(qq[j], kk[i], a[i][j]);
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int pr = 4 * tq + j, rr = pr / ATT_MAXG;
-                const int lim = rr < nr ? min(posr[r0 + rr], ctx - 1) : -1;  // the row's last position
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int p = p0 + 4 * tp + i;
-                    sc[pr * 65 + 4 * tp + i] = p <= lim ? a[i][j] * scale : -FLT_MAX;
+                for (int u = 0; u < 4; ++u) {
+                    const float4 q4 = reinterpret_cast<const float4*>(qs + (pr0 + u) * ACH_QS + sub * ATT_QP)[i];
+                    a[u] = fmaf(q4.x, kr[4 * i], a[u]);
+                    a[u] = fmaf(q4.y, kr[4 * i + 1], a[u]);
+                    a[u] = fmaf(q4.z, kr[4 * i + 2], a[u]);
+                    a[u] = fmaf(q4.w, kr[4 * i + 3], a[u]);
                 }
             }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                a[u] += __shfl_xor_sync(0xffffffffu, a[u], 1);
+                a[u] += __shfl_xor_sync(0xffffffffu, a[u], 2);
+            }
+            if (sub == 0) {
+                const int lm = lim[pr0 / ATT_MAXG];  // the four vectors share a row
+#pragma unroll
+                for (int u = 0; u < 4; ++u) sc[(pr0 + u) * 65 + pl] = p0 + pl <= lm ? a[u] * scale : -FLT_MAX;
+            }
         }
         __syncthreads();
-        // softmax update per pair (warp w takes pairs w, w + 8, ...)
+        // softmax update per query vector (warp w takes vectors w, w + 8, ...)
         for (int pr = wid; pr < ACH_PAIRS; pr += 8) {
             const float s0 = sc[pr * 65 + lane], s1 = sc[pr * 65 + lane + 32];
             const float cm = warp_max(fmaxf(s0, s1));
@@ -693,28 +707,32 @@ __global__ void __launch_bounds__(256, 1) chunk_attention_kernel(const float* qr
                 fold[pr] = f;
             }
         }
-        __syncthreads();
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();  // weights, rescales and the chunk's value rows
 #pragma unroll
         for (int i = 0; i < ACH_PAIRS / 8; ++i) {
-            const int pr = wid + 8 * i;
-            const float f = fold[pr];
-            float4 a4 = acc[i];
-            a4.x *= f;
-            a4.y *= f;
-            a4.z *= f;
-            a4.w *= f;
-            for (int p = 0; p < 64; ++p) {
-                const float e = sc[pr * 65 + p];
-                const float4 v4 = reinterpret_cast<const float4*>(vs + p * ATT_HD)[lane];
-                a4.x = fmaf(e, v4.x, a4.x);
-                a4.y = fmaf(e, v4.y, a4.y);
-                a4.z = fmaf(e, v4.z, a4.z);
-                a4.w = fmaf(e, v4.w, a4.w);
-            }
-            acc[i] = a4;
+            const float f = fold[wid + 8 * i];
+            acc[i].x *= f;
+            acc[i].y *= f;
+            acc[i].z *= f;
+            acc[i].w *= f;
         }
+        for (int p = 0; p < 64; ++p) {
+            const float4 v4 = reinterpret_cast<const float4*>(vs + p * ATT_HD)[lane];
+#pragma unroll
+            for (int i = 0; i < ACH_PAIRS / 8; ++i) {
+                const float e = sc[(wid + 8 * i) * 65 + p];
+                acc[i].x = fmaf(e, v4.x, acc[i].x);
+                acc[i].y = fmaf(e, v4.y, acc[i].y);
+                acc[i].z = fmaf(e, v4.z, acc[i].z);
+                acc[i].w = fmaf(e, v4.w, acc[i].w);
+            }
+        }
+        __syncthreads();  // the weights and value rows are read: the next chunk may overwrite them
+        if (cc + 1 < nchunk) load_v(cc + 1);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) kr[i] = krn[i];
     }
-    __syncthreads();
 #pragma unroll
     for (int i = 0; i < ACH_PAIRS / 8; ++i) {
         const int pr = wid + 8 * i, rr = pr / ATT_MAXG, hh = pr % ATT_MAXG;
