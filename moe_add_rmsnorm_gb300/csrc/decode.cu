@@ -587,7 +587,8 @@ constexpr int ACH_GROUP = 4;   // 64-position chunks per CTA
 constexpr int ACH_PAIRS = ACH_RB * ATT_MAXG;  // query vectors per CTA
 constexpr int ACH_QS = 4 * ATT_QP;             // a query vector in shared memory: four padded 32-dim quarters
 constexpr int ACH_PS = ATT_HD + 4;             // a group result: 128 weighted values, max, sum (16-byte rows)
-constexpr size_t ACH_SMEM = (size_t)(64 * ATT_HD + ACH_PAIRS * ACH_QS + ACH_PAIRS * 65 + 3 * ACH_PAIRS + 16) *
+constexpr int ACH_SS = 68;                     // a query vector's 64 scores (16-byte rows: four read at once)
+constexpr size_t ACH_SMEM = (size_t)(64 * ATT_HD + ACH_PAIRS * ACH_QS + ACH_PAIRS * ACH_SS + 3 * ACH_PAIRS + 16) *
                             sizeof(float);
 
 __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr, const float* k_cache,
@@ -597,8 +598,8 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
     extern __shared__ __align__(16) float acs[];
     float* vs = acs;                           // [64][128]
     float* qs = vs + 64 * ATT_HD;              // [pairs][4][ATT_QP]
-    float* sc = qs + ACH_PAIRS * ACH_QS;       // [pairs][65]
-    float* mrun = sc + ACH_PAIRS * 65;         // [pairs] running max
+    float* sc = qs + ACH_PAIRS * ACH_QS;       // [pairs][ACH_SS]
+    float* mrun = sc + ACH_PAIRS * ACH_SS;     // [pairs] running max
     float* lrun = mrun + ACH_PAIRS;            // [pairs] running sum
     float* fold = lrun + ACH_PAIRS;            // [pairs] rescale of this chunk
     int* lim = reinterpret_cast<int*>(fold + ACH_PAIRS);  // [ACH_RB] each row's last position
@@ -682,13 +683,13 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
             if (sub == 0) {
                 const int lm = lim[pr0 / ATT_MAXG];  // the four vectors share a row
 #pragma unroll
-                for (int u = 0; u < 4; ++u) sc[(pr0 + u) * 65 + pl] = p0 + pl <= lm ? a[u] * scale : -FLT_MAX;
+                for (int u = 0; u < 4; ++u) sc[(pr0 + u) * ACH_SS + pl] = p0 + pl <= lm ? a[u] * scale : -FLT_MAX;
             }
         }
         __syncthreads();
         // softmax update per query vector (warp w takes vectors w, w + 8, ...)
         for (int pr = wid; pr < ACH_PAIRS; pr += 8) {
-            const float s0 = sc[pr * 65 + lane], s1 = sc[pr * 65 + lane + 32];
+            const float s0 = sc[pr * ACH_SS + lane], s1 = sc[pr * ACH_SS + lane + 32];
             const float cm = warp_max(fmaxf(s0, s1));
             const float mo = mrun[pr];
             const float mn = fmaxf(mo, cm);
@@ -698,8 +699,8 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
                 e1 = s1 == -FLT_MAX ? 0.f : expf(s1 - mn);
                 f = mo == -FLT_MAX ? 0.f : expf(mo - mn);
             }
-            sc[pr * 65 + lane] = e0;
-            sc[pr * 65 + lane + 32] = e1;
+            sc[pr * ACH_SS + lane] = e0;
+            sc[pr * ACH_SS + lane + 32] = e1;
             const float cs = group_sum<32>(e0 + e1);
             if (lane == 0) {
                 lrun[pr] = lrun[pr] * f + cs;
@@ -717,15 +718,21 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
             acc[i].z *= f;
             acc[i].w *= f;
         }
-        for (int p = 0; p < 64; ++p) {
-            const float4 v4 = reinterpret_cast<const float4*>(vs + p * ATT_HD)[lane];
+        for (int p = 0; p < 64; p += 4) {  // four value rows, and each vector's four weights in one read
+            float4 v4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v4[j] = reinterpret_cast<const float4*>(vs + (p + j) * ATT_HD)[lane];
 #pragma unroll
             for (int i = 0; i < ACH_PAIRS / 8; ++i) {
-                const float e = sc[(wid + 8 * i) * 65 + p];
-                acc[i].x = fmaf(e, v4.x, acc[i].x);
-                acc[i].y = fmaf(e, v4.y, acc[i].y);
-                acc[i].z = fmaf(e, v4.z, acc[i].z);
-                acc[i].w = fmaf(e, v4.w, acc[i].w);
+                const float4 e4 = *reinterpret_cast<const float4*>(sc + (wid + 8 * i) * ACH_SS + p);
+                const float e[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[i].x = fmaf(e[j], v4[j].x, acc[i].x);
+                    acc[i].y = fmaf(e[j], v4[j].y, acc[i].y);
+                    acc[i].z = fmaf(e[j], v4[j].z, acc[i].z);
+                    acc[i].w = fmaf(e[j], v4[j].w, acc[i].w);
+                }
             }
         }
         __syncthreads();  // the weights and value rows are read: the next chunk may overwrite them
