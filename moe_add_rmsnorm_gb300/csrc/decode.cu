@@ -578,8 +578,8 @@ __global__ void __launch_bounds__(256) chunk_append_kernel(const float* q, const
 // pg*ACH_GROUP*64 .. +ACH_GROUP*64-1 in chunks of 64, keeping a running (max, sum, weighted values) per query vector
 // (online softmax, chunks in order); row r attends positions 0 .. posr[r].  The group's result (max, sum, 128
 // weighted values) goes to part[r][head][pg] when the row had any position in the group.
-// Scores as in the one-row attention: warp w takes positions 8w .. 8w+7 of a chunk, four lanes a position (a 32-dim
-// quarter each, the key row in registers, the next chunk's already in flight) against the queries in shared memory.
+// Scores: four lanes a position pair (a 32-dim quarter each, both key rows in registers, the next chunk's loaded once
+// this chunk's scores are done), each query read from shared memory feeding both positions.
 // Values: the chunk's value rows arrive in shared memory by cp.async while the scores are formed; thread (w, lane)
 // owns dims 4*lane .. +3 of query vectors w, w + 8, ..., reading each value row once for all of them.
 constexpr int ACH_RB = 8;      // rows per CTA
@@ -613,16 +613,21 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
     const int p_begin = pg * ACH_GROUP * 64;
     if (p_begin > maxpos) return;  // every row of the block ends before this group
     const int nchunk = min(ACH_GROUP, (maxpos - p_begin) / 64 + 1);
-    const int sub = lane & 3, pl = wid * 8 + (lane >> 2);  // score role: position pl of the chunk, dims 32*sub ..
-    auto load_k = [&](int cc, float (&kr)[32]) {
-        const int p = p_begin + cc * 64 + pl;
-        if (cc < nchunk && p <= maxpos) {
-            const float* kp = k_cache + ((int64_t)g * ctx + p) * ATT_HD + sub * 32;
+    // score role: warps w and w + 4 share positions 16*(w%4) .. +15 (two a lane group, dims 32*sub ..); warp w takes
+    // query vectors 32*(w/4) .. +31
+    const int sub = lane & 3, pa = 16 * (wid & 3) + 2 * (lane >> 2), pv0 = 32 * (wid >> 2);
+    auto load_k = [&](int cc, float (&kr)[2][32]) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) ld_f8_stream(kp + 8 * i, &kr[8 * i]);
-        } else {
+        for (int j = 0; j < 2; ++j) {
+            const int p = p_begin + cc * 64 + pa + j;
+            if (cc < nchunk && p <= maxpos) {
+                const float* kp = k_cache + ((int64_t)g * ctx + p) * ATT_HD + sub * 32;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) kr[i] = 0.f;
+                for (int i = 0; i < 4; ++i) ld_f8_stream(kp + 8 * i, &kr[j][8 * i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) kr[j][i] = 0.f;
+            }
         }
     };
     auto load_v = [&](int cc) {  // the chunk's value rows into vs by cp.async (rows past maxpos: zeros)
@@ -638,7 +643,7 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    float kr[32], krn[32];
+    float kr[2][32];
     load_k(0, kr);
     load_v(0);
     // the block's queries: pair = row_in_block * ATT_MAXG + head_in_group
@@ -659,34 +664,41 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
     __syncthreads();
     for (int cc = 0; cc < nchunk; ++cc) {
         const int p0 = p_begin + cc * 64;
-        load_k(cc + 1, krn);  // the next chunk's keys, in flight while this chunk is worked
-        // scores of every query vector against this lane group's position (four vectors at a time: four independent
-        // FMA chains)
-        for (int pr0 = 0; pr0 < ACH_PAIRS; pr0 += 4) {
-            float a[4] = {0.f, 0.f, 0.f, 0.f};
+        // scores of this warp's query vectors against the lane group's two positions (two vectors at a time)
+        for (int pr0 = pv0; pr0 < pv0 + 32; pr0 += 2) {
+            float a[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 2; ++u) {
                     const float4 q4 = reinterpret_cast<const float4*>(qs + (pr0 + u) * ACH_QS + sub * ATT_QP)[i];
-                    a[u] = fmaf(q4.x, kr[4 * i], a[u]);
-                    a[u] = fmaf(q4.y, kr[4 * i + 1], a[u]);
-                    a[u] = fmaf(q4.z, kr[4 * i + 2], a[u]);
-                    a[u] = fmaf(q4.w, kr[4 * i + 3], a[u]);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        a[j][u] = fmaf(q4.x, kr[j][4 * i], a[j][u]);
+                        a[j][u] = fmaf(q4.y, kr[j][4 * i + 1], a[j][u]);
+                        a[j][u] = fmaf(q4.z, kr[j][4 * i + 2], a[j][u]);
+                        a[j][u] = fmaf(q4.w, kr[j][4 * i + 3], a[j][u]);
+                    }
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                a[u] += __shfl_xor_sync(0xffffffffu, a[u], 1);
-                a[u] += __shfl_xor_sync(0xffffffffu, a[u], 2);
-            }
-            if (sub == 0) {
-                const int lm = lim[pr0 / ATT_MAXG];  // the four vectors share a row
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int u = 0; u < 4; ++u) sc[(pr0 + u) * ACH_SS + pl] = p0 + pl <= lm ? a[u] * scale : -FLT_MAX;
+                for (int u = 0; u < 2; ++u) {
+                    a[j][u] += __shfl_xor_sync(0xffffffffu, a[j][u], 1);
+                    a[j][u] += __shfl_xor_sync(0xffffffffu, a[j][u], 2);
+                }
+            if (sub == 0) {
+                const int lm = lim[pr0 / ATT_MAXG];  // the two vectors share a row
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        sc[(pr0 + u) * ACH_SS + pa + j] = p0 + pa + j <= lm ? a[j][u] * scale : -FLT_MAX;
             }
         }
         __syncthreads();
+        load_k(cc + 1, kr);  // the next chunk's keys, in flight during this chunk's softmax and values
         // softmax update per query vector (warp w takes vectors w, w + 8, ...)
         for (int pr = wid; pr < ACH_PAIRS; pr += 8) {
             const float s0 = sc[pr * ACH_SS + lane], s1 = sc[pr * ACH_SS + lane + 32];
@@ -737,8 +749,6 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
         }
         __syncthreads();  // the weights and value rows are read: the next chunk may overwrite them
         if (cc + 1 < nchunk) load_v(cc + 1);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) kr[i] = krn[i];
     }
 #pragma unroll
     for (int i = 0; i < ACH_PAIRS / 8; ++i) {
