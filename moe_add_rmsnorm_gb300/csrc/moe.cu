@@ -263,6 +263,7 @@ struct ExpertParams {
     void* partial;          // down over a chunk: [R*K][out_rows] (f64 in mode 0, f32 in mode 1)
     int nrs;                // items per group (row tiles of out_rows)
     int mma_lo, mma_hi;     // groups of mma_lo..mma_hi choices are left to the tensor-core kernel (0: none)
+    int xstage;             // gate-up, int8 mode: bytes of the chunk's activation rows staged in shared memory (0: none)
     L2Prefetch pf;
 };
 
@@ -304,6 +305,21 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gate_up_kernel(const ExpertPara
     issue_l2_prefetch(p.pf);
     griddep_wait();
     griddep_launch();
+    // int8 mode, a chunk whose activation rows fit: they are staged in shared memory once, so a warp's turn to the
+    // next row of its group reads shared memory rather than waiting on L2
+    extern __shared__ __align__(16) unsigned char gsm[];
+    const int8_t* xqb = p.xq;
+    const float* xsb = p.xs;
+    if (MODE == 1 && p.xstage) {
+        const int64_t nq = (int64_t)p.R * p.k;  // a multiple of 32
+        for (int64_t i = threadIdx.x; i < nq / 16; i += blockDim.x)
+            reinterpret_cast<uint4*>(gsm)[i] = __ldcg(reinterpret_cast<const uint4*>(p.xq) + i);
+        float* sxs = reinterpret_cast<float*>(gsm + nq);
+        for (int64_t i = threadIdx.x; i < (int64_t)p.R * p.nb; i += blockDim.x) sxs[i] = __ldcg(p.xs + i);
+        __syncthreads();
+        xqb = reinterpret_cast<const int8_t*>(gsm);
+        xsb = sxs;
+    }
     const int items = n_groups(p) * p.nrs;
     XTile<MODE, BPL> x;
     int loaded = -1;
@@ -323,8 +339,8 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gate_up_kernel(const ExpertPara
             const int c = choice_of(p, g, ci);
             const int xrow = c / p.K;
             if (xrow != loaded) {
-                load_x<MODE, BPL>(x, p.x + (int64_t)xrow * p.k, p.xq + (int64_t)xrow * p.k,
-                                  p.xs + (int64_t)xrow * p.nb, bidx, bval);
+                load_x<MODE, BPL>(x, p.x + (int64_t)xrow * p.k, xqb + (int64_t)xrow * p.k, xsb + (int64_t)xrow * p.nb,
+                                  bidx, bval);
                 loaded = xrow;
             }
 #pragma unroll
@@ -567,7 +583,13 @@ size_t down_one_smem(const ExpertCall& c) {
 #define Q8_EXPERT_ONE(KERNEL, MODE, L, B, R)                                                               \
     if (pl.lpr == L && pl.bpl == B && pl.rt == R) {                                                        \
         auto kern = KERNEL<MODE, L, B, R>;                                                                 \
-        return launch(kern, dim3(persistent_grid(kern, 0, warps)), dim3(Q8_THREADS), 0, st, c.pdl, p);     \
+        if (p.xstage > 48 * 1024) {                                                                        \
+            const cudaError_t ae =                                                                         \
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.xstage);         \
+            if (ae != cudaSuccess) return ae;                                                              \
+        }                                                                                                  \
+        return launch(kern, dim3(persistent_grid(kern, p.xstage, warps)), dim3(Q8_THREADS), (size_t)p.xstage, \
+                      st, c.pdl, p);                                                                       \
     }
 #define Q8_EXPERT_LPR(KERNEL, MODE, L)                                                                     \
     Q8_EXPERT_ONE(KERNEL, MODE, L, 1, 1) Q8_EXPERT_ONE(KERNEL, MODE, L, 1, 2) Q8_EXPERT_ONE(KERNEL, MODE, L, 1, 4) \
@@ -665,6 +687,8 @@ cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
         p.mma_hi = moe_mma_max_rows();
     }
     const int64_t warps = (int64_t)max_groups(c) * p.nrs;
+    const int64_t xbytes = c.R * c.k + c.R * (c.k / 32) * 4;
+    if (c.mode == 1 && c.R > 1 && xbytes <= 96 * 1024 && (uintptr_t)c.xq % 16 == 0) p.xstage = (int)xbytes;
     cudaError_t e = c.mode == 0 ? run_gate_up<0>(c, pl, p, warps, st) : run_gate_up<1>(c, pl, p, warps, st);
     if (e == cudaSuccess && mma) e = launch_moe_mma(c, c.h, max_groups(c), ws, st);  // the groups of >= 16 choices
     return e;
