@@ -51,6 +51,22 @@ def dist_env():
     return world, rank, local
 
 
+def slowest(sec, world, device):
+    """The whole job's time for `world` replicas: the slowest rank's (max over ranks; one rank: its own)."""
+    if world <= 1:
+        return sec
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([sec], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, sec):
+    """Units all ranks processed per second of the job's time."""
+    return world * units_per_rank / sec
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -438,13 +454,9 @@ def main():
         clk = clocks.stop()
         torch.cuda.synchronize()
         barrier()
-    sec = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        t = torch.tensor([sec], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        sec = float(t.item())
+    sec = slowest(e0.elapsed_time(e1) / 1e3, world, "cuda")
     model.check(sh)
-    value = world * args.steps / sec
+    value = job_rate(args.steps, world, sec)
     ms_per_step = sec / args.steps * 1e3
     if args.decode_only:
         if rank == 0:
@@ -470,8 +482,8 @@ def main():
             pin_out.copy_(tok, non_blocking=True)
             stream.synchronize()
             cur = int(pin_out[0])
-        e2e_sec = time.perf_counter() - t0
-    e2e = {"value": world * e2e_steps / e2e_sec, "unit": "tokens/s", "h2d_bytes_per_step": 8,
+        e2e_sec = slowest(time.perf_counter() - t0, world, "cuda")
+    e2e = {"value": job_rate(e2e_steps, world, e2e_sec), "unit": "tokens/s", "h2d_bytes_per_step": 8,
            "d2h_bytes_per_step": 4, "steps": e2e_steps}
 
     wbytes = recipes.weight_bytes_per_token(cfg)

@@ -66,3 +66,39 @@ def test_refusals_before_any_launch(q8):
     h = ctypes.c_void_p()
     assert lib.q8_model_create(ctypes.byref(d), ctypes.byref(h)) == -2
     assert "head_dim" in q8.last_error()
+
+
+_RANK = r"""
+import json, sys
+sys.path.insert(0, {root!r})
+import torch.distributed as dist
+dist.init_process_group("gloo", init_method="tcp://127.0.0.1:{port}", rank={rank}, world_size=2)
+import bench
+s = bench.slowest({sec}, 2, "cpu")
+print(json.dumps({{"rank": {rank}, "sec": s, "rate": bench.job_rate(10, 2, s)}}))
+dist.destroy_process_group()
+"""
+
+
+def test_replicas_report_the_slowest_rank():
+    """Two gloo ranks on the host: the job's time is the slower rank's on both, and the rate counts both ranks' units
+    (the aggregation bench.py applies to its replicas)."""
+    import json
+    import socket
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    procs = [subprocess.Popen([sys.executable, "-c", _RANK.format(root=root, port=port, rank=r, sec=sec)],
+                              stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+             for r, sec in ((0, 0.5), (1, 0.8))]
+    outs = [p.communicate(timeout=120) for p in procs]
+    for p, (o, e) in zip(procs, outs):
+        assert p.returncode == 0, e
+    res = [json.loads(o.strip().splitlines()[-1]) for o, _ in outs]
+    for r in res:
+        assert r["sec"] == 0.8
+        assert abs(r["rate"] - 2 * 10 / 0.8) < 1e-12
+
