@@ -51,6 +51,9 @@ def dist_env():
     return world, rank, local
 
 
+METRIC = "decode tokens/s and Q8_0 weight-stream GB/s (% of GB300 HBM peak), 1 GPU"
+
+
 def slowest(sec, world, device):
     """The whole job's time for `world` replicas: the slowest rank's (max over ranks; one rank: its own)."""
     if world <= 1:
@@ -265,7 +268,7 @@ def run_reference(args):
     per_token = L * float(np.mean(times))
     value = 1.0 / per_token
     line = {
-        "impl": "reference", "metric": "decode tokens/s (Q8_0 MoE, 48 layers) and Q8_0 weight-stream GB/s",
+        "impl": "reference", "metric": METRIC,
         "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_token * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "i8" if mode else "f32", "data": "synthetic",
@@ -493,7 +496,7 @@ def main():
     total_gbs = (wbytes + kv_mean) * args.steps / sec / 1e9
 
     line = {
-        "metric": "decode tokens/s (Q8_0 MoE, 48 layers) and Q8_0 weight-stream GB/s", "value": value,
+        "metric": METRIC, "value": value,
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "i8" if mode == q8.INT8ACT else "f32", "data": "synthetic",
