@@ -66,6 +66,9 @@ def test_refusals_before_any_launch(q8):
     h = ctypes.c_void_p()
     assert lib.q8_model_create(ctypes.byref(d), ctypes.byref(h)) == -2
     assert "head_dim" in q8.last_error()
+    assert lib.prefill_chunk(None, ctypes.c_void_p(256), 4, ctypes.c_void_p(8), None) == -1
+    assert "model" in q8.last_error()
+    assert lib.decode_step(None, None) == -1
 
 
 _RANK = r"""
