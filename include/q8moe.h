@@ -222,7 +222,7 @@ Q8_API int decode_step_launches(q8_model *model, q8_stream stream);
  * (each chosen expert's weights read once for all its rows).  Then the last row's final norm, LM head and greedy token
  * into *tok; *pos advances by `rows`.  The result equals `rows` decode steps fed these tokens (up to the summation
  * order of the multi-row kernels).  The chunk's activations and every launch's scratch come from `ws` (Q8_ENOSPACE if
- * too small; about 0.5 MB a row at d 2048, 32 heads of 128 and a 4096-row cache); plain launches on `stream`, no
+ * too small; about 0.7 MB a row at d 2048, 32 heads of 128 and a 4096-row cache); plain launches on `stream`, no
  * graph.  An id outside [0, vocab) or a row past the cache end sets the
  * model's device error word (q8_model_check). */
 Q8_API int prefill_chunk(q8_model *model, const int32_t *tokens, int64_t rows, q8_ws *ws, q8_stream stream);

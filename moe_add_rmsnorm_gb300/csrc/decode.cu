@@ -583,7 +583,7 @@ __global__ void __launch_bounds__(256) chunk_append_kernel(const float* q, const
 // Values: the chunk's value rows arrive in shared memory by cp.async while the scores are formed; thread (w, lane)
 // owns dims 4*lane .. +3 of query vectors w, w + 8, ..., reading each value row once for all of them.
 constexpr int ACH_RB = 8;      // rows per CTA
-constexpr int ACH_GROUP = 4;   // 64-position chunks per CTA
+constexpr int ACH_GROUP = 2;   // 64-position chunks per CTA
 constexpr int ACH_PAIRS = ACH_RB * ATT_MAXG;  // query vectors per CTA
 constexpr int ACH_QS = 4 * ATT_QP;             // a query vector in shared memory: four padded 32-dim quarters
 constexpr int ACH_PS = ATT_HD + 4;             // a group result: 128 weighted values, max, sum (16-byte rows)
