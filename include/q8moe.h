@@ -27,7 +27,9 @@
  *   - Arguments are checked before any launch.  A bad argument returns Q8_EINVAL (Q8_EUNSUPPORTED for a shape the
  *     kernels refuse, as kernel_refusal does in forward_shim.rs) and launches nothing; q8_last_error() names the
  *     argument.  A CUDA launch error returns Q8_ECUDA.  Errors raised later on the device surface at the caller's next
- *     synchronization as CUDA errors.
+ *     synchronization as CUDA errors.  A bounded device-side wait that gives up (Q8_ETIMEOUT) is reported only for the
+ *     decode model, by q8_model_check; a standalone call whose wait gave up leaves its outputs incomplete and reports
+ *     nothing.
  *   - Calls that take a workspace use its scratch and its arrival counters.  Calls sharing one workspace must be
  *     ordered (one stream, or events); two calls that overlap on the device through one workspace race.
  */
@@ -126,7 +128,8 @@ Q8_API int q8_gemv_blockdots(const q8_mat *W, const q8_act *xq, int64_t rows, in
  * results are those of q8_gemv.  Scratch (the quantized activation when xq is NULL, and the partial sums of a matrix
  * cut along k) comes from a fixed array of Q8_NOALLOC_SCRATCH_BYTES bytes and Q8_NOALLOC_COUNTERS counters that the
  * library holds on every device that loads it, until the process exits; a call that would need more returns
- * Q8_ENOSPACE and launches nothing.  The call allocates nothing and frees nothing.  The first call on each device
+ * Q8_ENOSPACE and launches nothing.  The call allocates nothing and frees nothing.  After its arguments pass their
+ * checks it clears the counters it will use (an asynchronous memset on `stream`) and then launches.  The first call on each device
  * looks up the array's device address (cudaGetSymbolAddress); make that first call before any stream capture.  Every
  * call on a device shares the one array: calls that overlap on the GPU (other streams, other threads) race and must
  * be ordered by the caller. */

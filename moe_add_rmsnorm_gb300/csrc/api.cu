@@ -170,8 +170,9 @@ int add_rmsnorm_q8(const float* a, const float* b, const float* w, int64_t rows,
     return e == cudaSuccess ? Q8_OK : cuda_fail(e, "add_rmsnorm_q8");
 }
 
-static int gemv_common(const q8_mat* W, q8_mode mode, const float* x, const q8_act* xq, int64_t rows, float* y,
-                       int32_t* dots, q8_ws* ws, cudaStream_t st, const char* who) {
+// The projection's argument checks (no launch, no side effect).
+static int gemv_check(const q8_mat* W, q8_mode mode, const float* x, const q8_act* xq, int64_t rows, float* y,
+                      int32_t* dots) {
     if (int r = check_mat(W, "W")) return r;
     if (mode != Q8_F32ACT_F64SUM && mode != Q8_INT8ACT) return fail(Q8_EINVAL, "mode %d", (int)mode);
     if (rows < 0) return fail(Q8_EINVAL, "rows negative");
@@ -183,6 +184,12 @@ static int gemv_common(const q8_mat* W, q8_mode mode, const float* x, const q8_a
     if (xq)
         if (int r = check_act(xq, "xq")) return r;
     if (x && !aligned(x, 16)) return fail(Q8_EINVAL, "x: not 16-byte aligned");
+    return Q8_OK;
+}
+
+static int gemv_common(const q8_mat* W, q8_mode mode, const float* x, const q8_act* xq, int64_t rows, float* y,
+                       int32_t* dots, q8_ws* ws, cudaStream_t st, const char* who) {
+    if (int r = gemv_check(W, mode, x, xq, rows, y, dots)) return r;
     if (rows == 0) return Q8_OK;
     Carve cv;
     if (ws) cv = ws->carve();
@@ -454,13 +461,16 @@ Carve workspace_carve(const q8_ws* ws) { return ws->carve(); }
 // Scratch one q8_gemv call takes (bytes and arrival counters): the quantized activation when x is quantized inside
 // the call, then the partial sums of a projection cut along k; each region rounded up to 256 bytes as a workspace
 // carve rounds it.
-void gemv_call_scratch(const q8_mat* W, q8_mode mode, const q8_act* xq, int64_t rows, size_t* bytes,
+void gemv_call_scratch(const q8_mat* W, q8_mode mode, const float* x, const q8_act* xq, int64_t rows, size_t* bytes,
                        size_t* counters) {
-    GemvCall c;
+    GemvCall c;  // the call q8_gemv would launch, so that the path chosen (bulk-copied rows or not) is the same
     c.mode = (int)mode;
     c.k = W->cols;
     c.nseg = 1;
+    c.seg[0].q = W->q;
+    c.seg[0].s = W->s;
     c.seg[0].n = W->rows;
+    c.x = x;
     c.R = rows;
     size_t b = 0;
     auto region = [&](size_t n) { b = ((b + 255) & ~size_t(255)) + n; };
@@ -475,12 +485,20 @@ void gemv_call_scratch(const q8_mat* W, q8_mode mode, const q8_act* xq, int64_t 
     *counters = pc;
 }
 
-// q8_gemv over scratch memory the caller already holds instead of a workspace.
+// q8_gemv over scratch memory the caller already holds instead of a workspace.  Every argument is checked first; when
+// they pass, the first `zero_counters` counters (those the call will use) are cleared on `st` before the launch, so a
+// call starts from zero even if an earlier one was cut short.
 int gemv_over_scratch(const q8_mat* W, q8_mode mode, const float* x, const q8_act* xq, int64_t rows, float* y,
-                      char* scratch, size_t bytes, int* counters, size_t n_counters, cudaStream_t st,
-                      const char* who) {
+                      char* scratch, size_t bytes, int* counters, size_t n_counters, size_t zero_counters,
+                      cudaStream_t st, const char* who) {
     g_err[0] = 0;
     if (!y) return fail(Q8_EINVAL, "y: null");
+    if (int r = gemv_check(W, mode, x, xq, rows, y, nullptr)) return r;
+    if (rows == 0) return Q8_OK;
+    if (zero_counters) {
+        cudaError_t e = cudaMemsetAsync(counters, 0, zero_counters * sizeof(int), st);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+    }
     q8_ws w;
     w.scratch = scratch;
     w.bytes = bytes;

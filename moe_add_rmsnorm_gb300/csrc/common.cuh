@@ -272,8 +272,10 @@ __device__ __forceinline__ float warp_max(float v) {
 // A warp holds one 32-value block, value `v` in lane `lane`.  d = amax / 127 and q = round-half-away(v / d), both
 // divisions IEEE-rounded f32, q clamped to [-127, 127]; amax = 0 gives d = 0, q = 0.
 //
-// d: the product by fl32(1/127) corrected by one FMA residual step, which equals the IEEE quotient for every
-// non-negative finite float (checked exhaustively on the host over all 2,139,095,040 of them).
+// d: the product by fl32(1/127) corrected by one FMA residual step (Markstein's correction of a quotient by its exact
+// remainder, P. Markstein, "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990), which equals the IEEE quotient for every non-negative finite float (checked exhaustively on the
+// host over all 2,139,095,040 of them).
 __device__ __forceinline__ float div127(float a) {
     const float c = 1.0f / 127.0f;
     const float q = __fmul_rn(a, c);
@@ -327,8 +329,9 @@ __device__ __forceinline__ int8_t quantize_lane(float v, float& d_out) {
 // ---- pairs of f32 carrying about 44 significant bits ------------------------------------------------------------
 // FP64 issues at a small fraction of the f32 rate on this part, so the few quantities that want more than 24 bits
 // (a row's sum of squares, its norm factor, the product s * inv * w before its single rounding) are held as unevaluated
-// sums hi + lo of two floats: Knuth's two-sum and the FMA two-product are exact, Dekker's normalisation keeps
-// |lo| <= ulp(hi) / 2.
+// sums hi + lo of two floats: Knuth's two-sum (TAOCP vol. 2, 4.2.2) and the FMA two-product are error-free
+// transformations, and Dekker's normalisation (T. J. Dekker, "A floating-point technique for extending the available
+// precision", Numer. Math. 18, 1971) keeps |lo| <= ulp(hi) / 2.
 struct F2 {
     float hi, lo;
 };

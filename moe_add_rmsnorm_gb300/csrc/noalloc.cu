@@ -13,11 +13,11 @@
 
 namespace q8 {
 int model_fail(int code, const char* fmt, ...);
-void gemv_call_scratch(const q8_mat* W, q8_mode mode, const q8_act* xq, int64_t rows, size_t* bytes,
-                       size_t* counters);
+void gemv_call_scratch(const q8_mat* W, q8_mode mode, const float* x, const q8_act* xq, int64_t rows,
+                       size_t* bytes, size_t* counters);
 int gemv_over_scratch(const q8_mat* W, q8_mode mode, const float* x, const q8_act* xq, int64_t rows, float* y,
-                      char* scratch, size_t bytes, int* counters, size_t n_counters, cudaStream_t st,
-                      const char* who);
+                      char* scratch, size_t bytes, int* counters, size_t n_counters, size_t zero_counters,
+                      cudaStream_t st, const char* who);
 }  // namespace q8
 
 using namespace q8;
@@ -67,13 +67,12 @@ extern "C" {
 
 int q8_gemv_noalloc(const q8_mat* W, q8_mode mode, const float* x, const q8_act* xq, int64_t rows, float* y,
                     q8_stream stream) {
-    if (!W || !W->q || !W->s || W->rows < 1 || W->cols < 1 || W->cols % 32)
-        return gemv_over_scratch(W, mode, x, xq, rows, y, nullptr, 0, nullptr, 0, (cudaStream_t)stream,
+    if (!W || !W->q || !W->s || W->rows < 1 || W->cols < 1 || W->cols % 32 || rows < 0 || rows > 65536 ||
+        (mode != Q8_F32ACT_F64SUM && mode != Q8_INT8ACT))
+        return gemv_over_scratch(W, mode, x, xq, rows, y, nullptr, 0, nullptr, 0, 0, (cudaStream_t)stream,
                                  "q8_gemv_noalloc");  // the projection's own argument checks name the problem
-    if (mode != Q8_F32ACT_F64SUM && mode != Q8_INT8ACT) return model_fail(Q8_EINVAL, "mode %d", (int)mode);
-    if (rows < 0 || rows > 65536) return model_fail(Q8_EINVAL, "q8_gemv_noalloc: rows %lld", (long long)rows);
     size_t bytes = 0, counters = 0;
-    gemv_call_scratch(W, mode, xq, rows, &bytes, &counters);
+    gemv_call_scratch(W, mode, x, xq, rows, &bytes, &counters);
     if (bytes > Q8_NOALLOC_SCRATCH_BYTES || counters > Q8_NOALLOC_COUNTERS)
         return model_fail(Q8_ENOSPACE,
                           "q8_gemv_noalloc: this call needs %zu bytes and %zu counters of scratch; the library holds "
@@ -81,12 +80,9 @@ int q8_gemv_noalloc(const q8_mat* W, q8_mode mode, const float* x, const q8_act*
                           bytes, counters, (unsigned)Q8_NOALLOC_SCRATCH_BYTES, (unsigned)Q8_NOALLOC_COUNTERS);
     DeviceScratch d;
     if (int r = device_scratch(&d)) return r;
-    if (counters) {  // start from zero even if an earlier call was cut short
-        cudaError_t e = cudaMemsetAsync(d.counters, 0, counters * sizeof(int), (cudaStream_t)stream);
-        if (e != cudaSuccess) return model_fail(Q8_ECUDA, "q8_gemv_noalloc: %s", cudaGetErrorString(e));
-    }
+    // the counters the call uses are cleared after its arguments pass their checks and before its launches
     return gemv_over_scratch(W, mode, x, xq, rows, y, d.scratch, Q8_NOALLOC_SCRATCH_BYTES, d.counters,
-                             Q8_NOALLOC_COUNTERS, (cudaStream_t)stream, "q8_gemv_noalloc");
+                             Q8_NOALLOC_COUNTERS, counters, (cudaStream_t)stream, "q8_gemv_noalloc");
 }
 
 }  // extern "C"

@@ -3,9 +3,10 @@
 Such callers (code inside an allocator's callbacks, loops that forbid allocation after start-up, hosts whose device
 memory another runtime has already handed out) cannot create a workspace.  This entry point takes its scratch from an
 array the library holds on the device, so the test checks it against q8_gemv (which uses a workspace) on shapes that
-do need scratch: a matrix cut along k, and an int8-mode call that quantizes its activation into scratch.  Two calls in
-a row each, so the second call starts from whatever the first left in the shared array.  The file is named to run
-last, so a run that stops at the first failure has already run every other test.
+need scratch: matrices cut along k (one of them because its scales are 4-byte but not 16-byte aligned, which keeps it
+off the bulk-copy path), and int8-mode calls that quantize their activation into scratch.  Two calls in a row each,
+so the second call starts from whatever the first left in the shared array; neither may allocate device memory.  The
+file is named to run last, so a run that stops at the first failure has already run every other test.
 """
 import ctypes
 
@@ -27,13 +28,19 @@ def rel_err(a, b):
     return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
 
 
-@pytest.mark.parametrize("mode,n,k,R,give_xq", [(0, 512, 2048, 1, False), (0, 128, 4096, 3, False),
-                                               (1, 128, 4096, 1, False), (1, 1000, 96, 2, True)])
-def test_noalloc_matches_workspace_projection(q8, mode, n, k, R, give_xq):
+@pytest.mark.parametrize("mode,n,k,R,give_xq,scale_offset", [(0, 512, 2048, 1, False, 1), (0, 128, 4096, 3, False, 0),
+                                                            (1, 128, 4096, 1, False, 0), (1, 1000, 96, 2, True, 0),
+                                                            (1, 512, 2048, 1, False, 1)])
+def test_noalloc_matches_workspace_projection(q8, mode, n, k, R, give_xq, scale_offset):
     import torch
     q, s = synth.q8_matrix(n, k, 7, 300 + n % 5)
     x = synth.normal((R, k), 7, recipes.VEC + 301)
-    tq, ts = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+    tq = torch.from_numpy(q).cuda()
+    # scales placed `scale_offset` floats into their buffer: 4-byte aligned, and with an offset of 1 not 16-byte
+    # aligned, which sends a one-row call to the projection cut along k (arrival counters in the scratch)
+    sbuf = torch.zeros(s.size + 4, dtype=torch.float32, device="cuda")
+    ts = sbuf[scale_offset:scale_offset + s.size].view(n, k // 32)
+    ts.copy_(torch.from_numpy(s))
     tx = torch.from_numpy(x).cuda()
     xq = xs = None
     if give_xq:
@@ -53,15 +60,21 @@ def test_noalloc_matches_workspace_projection(q8, mode, n, k, R, give_xq):
     W = q8.mat(tq, ts)
     qa = ctypes.byref(q8.q8_act(xq.data_ptr(), xs.data_ptr())) if give_xq else None
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    ys = [torch.full((R, n), float("nan"), device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    held = torch.cuda.memory_allocated()
     for call in range(2):
-        y = torch.full((R, n), float("nan"), device="cuda")
+        free_before = torch.cuda.mem_get_info()[0]
         code = q8.lib.q8_gemv_noalloc(ctypes.byref(W), mode, ctypes.c_void_p(tx.data_ptr()), qa, R,
-                                      ctypes.c_void_p(y.data_ptr()), stream)
+                                      ctypes.c_void_p(ys[call].data_ptr()), stream)
         assert code == 0, q8.last_error()
         torch.cuda.synchronize()
-        got = y.cpu().numpy()
+        if call == 1:  # the first call may load the kernels' code; the second allocates nothing at all
+            assert torch.cuda.mem_get_info()[0] == free_before
+        got = ys[call].cpu().numpy()
         assert np.isfinite(got).all()
         assert rel_err(got, ref_h) < TOL[mode], (call, rel_err(got, ref_h))
+    assert torch.cuda.memory_allocated() == held
     ws.close()
 
 
