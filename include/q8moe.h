@@ -218,6 +218,12 @@ Q8_API void q8_model_destroy(q8_model *model);
 Q8_API int decode_step(q8_model *model, q8_stream stream);
 /* The same step as plain launches, without a graph (for tests and graph-capture by the caller). */
 Q8_API int decode_step_launches(q8_model *model, q8_stream stream);
+/* Debug export: decode_step_launches that also copies the residual stream into hidden (device f32 [layers + 1][d]):
+ * row 0 is the stream entering the first layer (the token's embedding row), row l + 1 the stream leaving layer l
+ * (after its attention and mixture sums).  Per layer the step's results are those of decode_step; the copies are
+ * ordinary stream operations between the launches.  For parity checks of each layer against a reference fed the same
+ * input (emit_qwen30b_generate's per-layer order). */
+Q8_API int decode_step_trace(q8_model *model, float *hidden, q8_stream stream);
 /* A chunk of `rows` token rows through every layer (the prefill of a prompt chunk): tokens is device int32 [rows]; row
  * r takes position *pos + r.  Each layer: RMSNorm of the rows, the q/k/v projection of all rows, QK-norm, RoPE and the
  * key/value append of every row at its position, then each row's attention over rows 0 .. its position (causal), the O
@@ -231,9 +237,13 @@ Q8_API int decode_step_launches(q8_model *model, q8_stream stream);
 Q8_API int prefill_chunk(q8_model *model, const int32_t *tokens, int64_t rows, q8_ws *ws, q8_stream stream);
 /* Kernels one step launches: the kernel nodes of the graph the first decode_step captured (0 before it). */
 Q8_API int64_t q8_model_launches_per_step(const q8_model *model);
-/* Reads and clears the model's device error word (synchronizes `stream`): Q8_OK, or Q8_EINVAL when a step met an
- * out-of-range position or token. */
+/* Reads and clears the model's device error word (synchronizes `stream`): Q8_OK, Q8_EINVAL when a step met an
+ * out-of-range position or token, or Q8_ETIMEOUT when a bounded pipeline wait gave up. */
 Q8_API int q8_model_check(q8_model *model, q8_stream stream);
+/* Self-test of the bounded waits: one thread waits on a shared-memory barrier that nothing ever arrives on, giving up
+ * after `polls` polls (1 to 2^20) exactly as the step's pipeline waits give up, and records the timeout in the model's
+ * error word, which the next q8_model_check reports as Q8_ETIMEOUT.  Nothing else is touched. */
+Q8_API int q8_model_wait_selftest(q8_model *model, unsigned polls, q8_stream stream);
 
 /* ---- errors --------------------------------------------------------------------------------------------------- */
 /* The text of the calling thread's last error (empty when none); valid until the thread's next call. */

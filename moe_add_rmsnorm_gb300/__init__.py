@@ -75,8 +75,10 @@ _SIGS = {
     "q8_model_destroy": [_vp],
     "decode_step": [_vp, _vp],
     "decode_step_launches": [_vp, _vp],
+    "decode_step_trace": [_vp, _vp, _vp],
     "prefill_chunk": [_vp, _vp, _i64, _vp, _vp],
     "q8_model_check": [_vp, _vp],
+    "q8_model_wait_selftest": [_vp, ctypes.c_uint, _vp],
     "q8_model_launches_per_step": [_vp],
     "q8_last_error": [],
 }
@@ -260,12 +262,21 @@ class Model:
     def step_launches(self, stream=None):
         _check(lib.decode_step_launches(self.handle, _stream(stream)))
 
+    def step_trace(self, hidden, stream=None):
+        """Plain-launch step that also copies the residual stream entering layer 0 and leaving every layer into
+        hidden (device f32 [layers + 1, d])."""
+        _check(lib.decode_step_trace(self.handle, hidden.data_ptr(), _stream(stream)))
+
     def prefill(self, tokens, ws, stream=None):
         """tokens: device int32 [rows]; the chunk through every layer (plain launches), last row's token into tok."""
         _check(lib.prefill_chunk(self.handle, tokens.data_ptr(), tokens.numel(), ws.handle, _stream(stream)))
 
     def check(self, stream=None):
         _check(lib.q8_model_check(self.handle, _stream(stream)))
+
+    def wait_selftest(self, polls, stream=None):
+        """A bounded wait on a barrier nothing arrives on; the next check() raises Q8_ETIMEOUT."""
+        _check(lib.q8_model_wait_selftest(self.handle, int(polls), _stream(stream)))
 
     def launches_per_step(self):
         """Kernels one step launches (the captured graph's kernel nodes; 0 before the first step)."""

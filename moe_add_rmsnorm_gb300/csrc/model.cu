@@ -21,6 +21,7 @@
 
 #include "kernels.h"
 #include "q8moe.h"
+#include "stream.cuh"
 
 namespace q8 {
 extern int model_fail(int code, const char* fmt, ...);
@@ -79,7 +80,10 @@ Carve fresh_carve(q8_model* m) {
     return c;
 }
 
-cudaError_t step_launches(q8_model* m, cudaStream_t st) {
+// The step's launches in order.  With `trace` (device f32 [layers + 1][d]) the residual stream entering the first layer
+// (the token's embedding row) and leaving each layer is copied out after the launch that completes it (a debug export;
+// the copies are ordinary stream operations between the kernels).
+cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) {
     const q8_model_desc& d = m->d;
     const int mode = (int)d.mode;
     const int64_t D = d.d, H = d.heads, KV = d.kv_heads, HD = d.head_dim;
@@ -141,6 +145,8 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             Carve cv = fresh_carve(m);
             Q8_TRY(launch_gemv(g, cv, st));
         }
+        if (trace && l == 0)
+            Q8_TRY(cudaMemcpyAsync(trace, m->h, (size_t)D * sizeof(float), cudaMemcpyDeviceToDevice, st));
         {
             Carve cv = fresh_carve(m);
             AttnCall a;  // QK-norm, RoPE and the cache append happen inside the attention launch
@@ -296,6 +302,9 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
             c.err = m->err;
             Q8_TRY(launch_down_combine(c, cv, st));
         }
+        if (trace)
+            Q8_TRY(cudaMemcpyAsync(trace + (l + 1) * D, m->h, (size_t)D * sizeof(float), cudaMemcpyDeviceToDevice,
+                                   st));
     }
     // final norm (inside the LM head launch when the shapes allow it), LM head, greedy token
     {
@@ -346,9 +355,27 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st) {
     return cudaSuccess;
 }
 
+// A wait that is bound to give up: one thread waits on a barrier that nothing arrives on, at most `polls` polls, and
+// records the timeout in the error word as every pipeline wait of the step does.
+__global__ void wait_selftest_kernel(int* err, unsigned polls) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    mbar_wait(&bar, 0, err, polls);
+}
+
 }  // namespace
 
 extern "C" {
+
+int q8_model_wait_selftest(q8_model* m, unsigned polls, q8_stream stream) {
+    if (!m) return model_fail(Q8_EINVAL, "model: null");
+    if (polls < 1 || polls > (1u << 20)) return model_fail(Q8_EINVAL, "polls %u: 1 to 2^20", polls);
+    wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(m->err, polls);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? Q8_OK : model_fail(Q8_ECUDA, "q8_model_wait_selftest: %s", cudaGetErrorString(e));
+}
 
 int q8_model_create(const q8_model_desc* desc, q8_model** out) {
     if (!out) return model_fail(Q8_EINVAL, "model: null");
@@ -503,6 +530,13 @@ int decode_step_launches(q8_model* m, q8_stream stream) {
     if (!m) return model_fail(Q8_EINVAL, "model: null");
     cudaError_t e = step_launches(m, (cudaStream_t)stream);
     return e == cudaSuccess ? Q8_OK : model_fail(Q8_ECUDA, "decode_step_launches: %s", cudaGetErrorString(e));
+}
+
+int decode_step_trace(q8_model* m, float* hidden, q8_stream stream) {
+    if (!m) return model_fail(Q8_EINVAL, "model: null");
+    if (!hidden || (uintptr_t)hidden % 4) return model_fail(Q8_EINVAL, "hidden: null or misaligned");
+    cudaError_t e = step_launches(m, (cudaStream_t)stream, hidden);
+    return e == cudaSuccess ? Q8_OK : model_fail(Q8_ECUDA, "decode_step_trace: %s", cudaGetErrorString(e));
 }
 
 int decode_step(q8_model* m, q8_stream stream) {

@@ -40,9 +40,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; false (and `err` |= kErrPipeline) after kWaitLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, int* err) {
-    for (unsigned i = 0; i < kWaitLimit; ++i) {
+// Waits for the phase with the given parity to complete; false (and `err` |= kErrPipeline) after `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, int* err, unsigned limit = kWaitLimit) {
+    for (unsigned i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (i > 64) __nanosleep(32);
     }

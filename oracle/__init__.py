@@ -79,6 +79,8 @@ def lib():
             "ora_argmax": ([vp, i64], i64),
             "ora_decode_step": ([i32, ctypes.POINTER(Model), i64, i64, vp], i64),
             "ora_decode_layers": ([i32, ctypes.POINTER(Model), i64, i64, i64, vp], None),
+            "ora_decode_layer": ([i32, ctypes.POINTER(Model), i64, i64, vp, vp], None),
+            "ora_decode_final": ([i32, ctypes.POINTER(Model), vp, vp], i64),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -336,3 +338,20 @@ def decode_layers(mode, model: ModelArrays, tok, pos, layers):
     out = np.empty(model.cfg["d"], np.float64)
     lib().ora_decode_layers(int(mode), ctypes.byref(model.struct), int(tok), int(pos), int(layers), out.ctypes.data)
     return out
+
+
+def decode_layer(mode, model: ModelArrays, l, pos, h):
+    """Layer ``l`` alone from the residual stream ``h`` (f32 [d]) entering it; writes the layer's key/value rows at
+    ``pos`` into the model's host caches.  Returns (the stream leaving the layer as f32, the router's logits f64)."""
+    h = np.array(h, dtype=np.float32, copy=True)
+    rl = np.empty(model.cfg["experts"], np.float64)
+    lib().ora_decode_layer(int(mode), ctypes.byref(model.struct), int(l), int(pos), h.ctypes.data, rl.ctypes.data)
+    return h, rl
+
+
+def decode_final(mode, model: ModelArrays, h):
+    """The final norm, LM head and greedy token from the residual stream ``h`` leaving the last layer."""
+    h = np.ascontiguousarray(h, np.float32)
+    logits = np.empty(model.cfg["vocab"], np.float64)
+    nxt = lib().ora_decode_final(int(mode), ctypes.byref(model.struct), h.ctypes.data, logits.ctypes.data)
+    return int(nxt), logits

@@ -297,8 +297,13 @@ static void to_f32(const double *x, int64_t n, float *y) {
 /* qwen_emit docs, emit_qwen30b_generate: RMSNorm -> Q/K/V -> per-head QK-norm + RoPE -> attention over the KV cache ->
  * O-proj -> residual -> RMSNorm -> mixture -> residual, per layer; then the LM head and the greedy token.  The
  * residual stream and the caches are f32 (forward_shim.rs, ForwardShim::supports: CompensatedResidual and
- * KvCacheQuant refused); every projection reads an f32 activation (quantized in mode 1). */
-static void run_layers(int mode, const ora_model *m, int64_t tok, int64_t pos, int64_t layers, float *h) {
+ * KvCacheQuant refused); every projection reads an f32 activation (quantized in mode 1).
+ *
+ * One layer: h is the residual stream entering layer l (for the first layer the token's embedding row, which is normed
+ * with no residual added); on return it holds the stream leaving the layer, h + o and then + the mixture, each sum one
+ * f32 add.  The layer's key and value rows are written into the caches at `pos`.  router_logits (NULL or [experts])
+ * receives the router's logits. */
+void ora_decode_layer(int mode, const ora_model *m, int64_t l, int64_t pos, float *h, double *router_logits) {
     const int64_t d = m->d, H = m->heads, KV = m->kv_heads, hd = m->hd, ctx = m->ctx;
     const int64_t group = H / KV;
     double *n64 = (double *)malloc(sizeof(double) * (size_t)d);
@@ -309,55 +314,50 @@ static void run_layers(int mode, const ora_model *m, int64_t tok, int64_t pos, i
     double *att = (double *)malloc(sizeof(double) * (size_t)(H * hd));
     double *o = (double *)malloc(sizeof(double) * (size_t)d);
     double *y = (double *)malloc(sizeof(double) * (size_t)d);
-    float *moe_out = (float *)malloc(sizeof(float) * (size_t)d);
     float *o32 = (float *)malloc(sizeof(float) * (size_t)d);
+    float *moe_out = (float *)malloc(sizeof(float) * (size_t)d);
     int32_t ids[64];
     double gates[64];
 
-    memcpy(h, m->embed + tok * d, sizeof(float) * (size_t)d);
-    for (int64_t l = 0; l < layers; ++l) {
-        /* attention half: the first layer norms the embedding row; later layers add the previous mixture first */
-        ora_add_rmsnorm(h, l == 0 ? NULL : moe_out, m->attn_norm[l], 1, d, m->eps, h, n64);
-        to_f32(n64, d, x32);
-        ora_gemv(mode, m->wq[l].q, m->wq[l].s, H * hd, d, x32, q);
-        ora_gemv(mode, m->wk[l].q, m->wk[l].s, KV * hd, d, x32, k);
-        ora_gemv(mode, m->wv[l].q, m->wv[l].s, KV * hd, d, x32, v);
-        for (int64_t hh = 0; hh < H; ++hh) {
-            ora_rmsnorm_head(q + hh * hd, m->q_norm[l], hd, m->eps, q + hh * hd);
-            ora_rope(q + hh * hd, hd, pos, m->rope_theta);
-        }
-        for (int64_t g = 0; g < KV; ++g) {
-            ora_rmsnorm_head(k + g * hd, m->k_norm[l], hd, m->eps, k + g * hd);
-            ora_rope(k + g * hd, hd, pos, m->rope_theta);
-            float *kr = m->k_cache[l] + (g * ctx + pos) * hd;
-            float *vr = m->v_cache[l] + (g * ctx + pos) * hd;
-            for (int64_t i = 0; i < hd; ++i) {
-                kr[i] = (float)k[g * hd + i];
-                vr[i] = (float)v[g * hd + i];
-            }
-        }
-        for (int64_t hh = 0; hh < H; ++hh) {
-            const int64_t g = hh / group;
-            ora_attention(q + hh * hd, m->k_cache[l] + g * ctx * hd, m->v_cache[l] + g * ctx * hd, pos + 1, hd,
-                          att + hh * hd);
-        }
-        to_f32(att, H * hd, x32);
-        ora_gemv(mode, m->wo[l].q, m->wo[l].s, d, H * hd, x32, o);
-        to_f32(o, d, o32);
-        /* feed-forward half */
-        ora_add_rmsnorm(h, o32, m->ffn_norm[l], 1, d, m->eps, h, n64);
-        to_f32(n64, d, x32);
-        ora_moe mo = m->moe;
-        mo.router = m->router[l];
-        mo.gate = m->gate[l];
-        mo.up = m->up[l];
-        mo.down = m->down[l];
-        ora_moe_row(mode, &mo, x32, NULL, NULL, ids, gates, NULL, NULL, y);
-        to_f32(y, d, moe_out);
+    /* attention half */
+    ora_add_rmsnorm(h, NULL, m->attn_norm[l], 1, d, m->eps, NULL, n64);
+    to_f32(n64, d, x32);
+    ora_gemv(mode, m->wq[l].q, m->wq[l].s, H * hd, d, x32, q);
+    ora_gemv(mode, m->wk[l].q, m->wk[l].s, KV * hd, d, x32, k);
+    ora_gemv(mode, m->wv[l].q, m->wv[l].s, KV * hd, d, x32, v);
+    for (int64_t hh = 0; hh < H; ++hh) {
+        ora_rmsnorm_head(q + hh * hd, m->q_norm[l], hd, m->eps, q + hh * hd);
+        ora_rope(q + hh * hd, hd, pos, m->rope_theta);
     }
-    /* the last mixture's sum into the residual stream */
-    if (layers > 0)
-        for (int64_t i = 0; i < d; ++i) h[i] = h[i] + moe_out[i];
+    for (int64_t g = 0; g < KV; ++g) {
+        ora_rmsnorm_head(k + g * hd, m->k_norm[l], hd, m->eps, k + g * hd);
+        ora_rope(k + g * hd, hd, pos, m->rope_theta);
+        float *kr = m->k_cache[l] + (g * ctx + pos) * hd;
+        float *vr = m->v_cache[l] + (g * ctx + pos) * hd;
+        for (int64_t i = 0; i < hd; ++i) {
+            kr[i] = (float)k[g * hd + i];
+            vr[i] = (float)v[g * hd + i];
+        }
+    }
+    for (int64_t hh = 0; hh < H; ++hh) {
+        const int64_t g = hh / group;
+        ora_attention(q + hh * hd, m->k_cache[l] + g * ctx * hd, m->v_cache[l] + g * ctx * hd, pos + 1, hd,
+                      att + hh * hd);
+    }
+    to_f32(att, H * hd, x32);
+    ora_gemv(mode, m->wo[l].q, m->wo[l].s, d, H * hd, x32, o);
+    to_f32(o, d, o32);
+    /* feed-forward half: the norm of h + o (the sum kept as the residual) feeds the mixture */
+    ora_add_rmsnorm(h, o32, m->ffn_norm[l], 1, d, m->eps, h, n64);
+    to_f32(n64, d, x32);
+    ora_moe mo = m->moe;
+    mo.router = m->router[l];
+    mo.gate = m->gate[l];
+    mo.up = m->up[l];
+    mo.down = m->down[l];
+    ora_moe_row(mode, &mo, x32, NULL, router_logits, ids, gates, NULL, NULL, y);
+    to_f32(y, d, moe_out);
+    for (int64_t i = 0; i < d; ++i) h[i] = h[i] + moe_out[i];
     free(n64);
     free(x32);
     free(q);
@@ -366,23 +366,35 @@ static void run_layers(int mode, const ora_model *m, int64_t tok, int64_t pos, i
     free(att);
     free(o);
     free(y);
-    free(moe_out);
     free(o32);
+    free(moe_out);
 }
 
-int64_t ora_decode_step(int mode, const ora_model *m, int64_t tok, int64_t pos, double *logits) {
+/* The first `layers` layers from the token's embedding row. */
+static void run_layers(int mode, const ora_model *m, int64_t tok, int64_t pos, int64_t layers, float *h) {
+    memcpy(h, m->embed + tok * m->d, sizeof(float) * (size_t)m->d);
+    for (int64_t l = 0; l < layers; ++l) ora_decode_layer(mode, m, l, pos, h, NULL);
+}
+
+/* The step's end (qwen_emit docs, emit_qwen30b_generate): the final RMSNorm of the residual stream h, the LM head and
+ * the greedy token. */
+int64_t ora_decode_final(int mode, const ora_model *m, const float *h, double *logits) {
     const int64_t d = m->d;
-    float *h = (float *)malloc(sizeof(float) * (size_t)d);
     double *n64 = (double *)malloc(sizeof(double) * (size_t)d);
     float *x32 = (float *)malloc(sizeof(float) * (size_t)d);
-    run_layers(mode, m, tok, pos, m->layers, h);
     ora_add_rmsnorm(h, NULL, m->final_norm, 1, d, m->eps, NULL, n64);
     to_f32(n64, d, x32);
     ora_gemv(mode, m->lm_head.q, m->lm_head.s, m->vocab, d, x32, logits);
-    int64_t next = ora_argmax(logits, m->vocab);
-    free(h);
     free(n64);
     free(x32);
+    return ora_argmax(logits, m->vocab);
+}
+
+int64_t ora_decode_step(int mode, const ora_model *m, int64_t tok, int64_t pos, double *logits) {
+    float *h = (float *)malloc(sizeof(float) * (size_t)m->d);
+    run_layers(mode, m, tok, pos, m->layers, h);
+    const int64_t next = ora_decode_final(mode, m, h, logits);
+    free(h);
     return next;
 }
 

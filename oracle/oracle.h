@@ -95,6 +95,11 @@ typedef struct {
 
 /* One token at `pos`: writes the new key/value rows into the caches, fills logits[vocab] and returns the argmax. */
 int64_t ora_decode_step(int mode, const ora_model *m, int64_t tok, int64_t pos, double *logits);
+/* Layer l alone: h [d] is the residual stream entering the layer (the embedding row for the first layer) and holds the
+ * stream leaving it on return; the layer's key/value rows are written at `pos`; router_logits may be NULL. */
+void ora_decode_layer(int mode, const ora_model *m, int64_t l, int64_t pos, float *h, double *router_logits);
+/* The step's end from the residual stream h [d] leaving the last layer: final norm, LM head, greedy token. */
+int64_t ora_decode_final(int mode, const ora_model *m, const float *h, double *logits);
 /* The first `layers` layers of the step only (for a bounded CPU timing sample); returns nothing. */
 void ora_decode_layers(int mode, const ora_model *m, int64_t tok, int64_t pos, int64_t layers, double *hidden_out);
 

@@ -72,8 +72,9 @@ def test_decode_small_matches_oracle_over_steps(q8, mode, cfg, launches):
         assert int(pos.item()) == cur_pos + 1
         # the step wrote its key/value rows at cur_pos
         for l in range(cfg["layers"]):
-            kc = t["k_cache"][l].cpu().numpy()
-            assert rel_err(kc[:, cur_pos], om.k_cache[l][:, cur_pos]) < 10 * TOL[mode]
+            kc, vc = t["k_cache"][l].cpu().numpy(), t["v_cache"][l].cpu().numpy()
+            assert rel_err(kc[:, cur_pos], om.k_cache[l][:, cur_pos]) < TOL[mode]
+            assert rel_err(vc[:, cur_pos], om.v_cache[l][:, cur_pos]) < TOL[mode]
         cur_tok, cur_pos = int(tok.item()), cur_pos + 1
     # fused: per layer q/k/v (+norm), attention (+QK-norm, RoPE, append), O, router (+norm, top-k), gate-up, down;
     # then LM head (+final norm) and arg-max.  Unfused adds the two norms per layer and the final norm.
@@ -117,6 +118,26 @@ def test_decode_bad_position_is_refused_on_device(q8):
     m.close()
 
 
+def test_bounded_wait_gives_up_and_is_reported(q8):
+    """A pipeline wait on a barrier that nothing arrives on gives up after its poll limit instead of hanging, records
+    the timeout in the model's error word, and q8_model_check reports it once (then the word is clear); the model's
+    next step is unaffected."""
+    import torch
+    m, arr, t, tok, pos, logits = build(q8, SMALL, 8, 1)
+    m.wait_selftest(64)
+    torch.cuda.synchronize()
+    with pytest.raises(q8.Q8Error, match="Q8_ETIMEOUT"):
+        m.check()
+    m.check()  # cleared
+    tok.fill_(2)
+    pos.fill_(30)
+    m.step()
+    torch.cuda.synchronize()
+    assert int(pos.item()) == 31
+    m.check()
+    m.close()
+
+
 @pytest.mark.parametrize("mode", [1, 0])
 def test_decode_full_dims_eight_layers(q8, mode):
     """Every dimension of the full configuration (d 2048, 32/4 heads, 128 experts keep 8, vocab 151936, cache 4096)
@@ -137,32 +158,67 @@ def test_decode_full_dims_eight_layers(q8, mode):
     if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
         assert int(tok.item()) == nxt
     for l in range(cfg["layers"]):
-        assert rel_err(t["k_cache"][l].cpu().numpy()[:, -1], om.k_cache[l][:, -1]) < 10 * TOL[mode]
+        assert rel_err(t["k_cache"][l].cpu().numpy()[:, -1], om.k_cache[l][:, -1]) < TOL[mode]
     m.close()
+
+
+def _near_tie(logits, k):
+    """The oracle's K-th and (K+1)-th router logits within 1e-5 of the largest magnitude: an expert choice there may
+    fall either way (flagged, not compared)."""
+    srt = np.sort(np.asarray(logits, np.float64))[::-1]
+    return srt[k - 1] - srt[k] < 1e-5 * np.max(np.abs(srt))
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("mode", [1, 0])
-def test_decode_full_config_one_step(q8, mode):
-    """The full 48-layer configuration as the benchmark runs it (captured graph), one step at the last position.
-    Rounding differences grow through 48 random layers (see the depth note in the design), so the check is: the early
-    layers' new cache rows match the oracle, the token is the arg-max of the step's own logits, the position advanced,
-    and every logit is finite."""
+def test_decode_full_config_layer_by_layer(q8, mode):
+    """The full 48-layer configuration at the last cache position (every cached row attended), teacher-forced: the
+    GPU step exports the residual stream entering every layer, the oracle runs each layer from that same input, and
+    each layer's output (and its increment, the attention and mixture sums), its new key and value rows, then the
+    final norm, LM head and token from the GPU's last stream, are each within the stated tolerance.  The graph replay
+    the benchmark times gives the same logits bit for bit as the traced plain launches."""
     import torch
     cfg = recipes.DECODE
+    L, K = cfg["layers"], cfg["k"]
     m, arr, t, tok, pos, logits = build(q8, cfg, 0, mode)
     om = oracle.ModelArrays(cfg, **arr)
+    P = cfg["ctx"] - 1
     tok.fill_(0)
-    pos.fill_(cfg["ctx"] - 1)
+    pos.fill_(P)
+    hidden = torch.empty(L + 1, cfg["d"], device="cuda")
+    m.step_trace(hidden)
+    torch.cuda.synchronize()
+    hid = hidden.cpu().numpy()
+    gl = logits.cpu().numpy().copy()
+    gtok = int(tok.item())
+    assert int(pos.item()) == cfg["ctx"]
+    np.testing.assert_array_equal(hid[0], arr["embed"][0])
+    flagged, worst = [], 0.0
+    for l in range(L):
+        h_ora, rl = oracle.decode_layer(mode, om, l, P, hid[l])
+        if _near_tie(rl, K):
+            flagged.append(l)
+            continue
+        err_out = rel_err(hid[l + 1], h_ora)
+        err_inc = rel_err(hid[l + 1].astype(np.float64) - hid[l], h_ora.astype(np.float64) - hid[l])
+        kc, vc = t["k_cache"][l][:, P].cpu().numpy(), t["v_cache"][l][:, P].cpu().numpy()
+        err_k, err_v = rel_err(kc, om.k_cache[l][:, P]), rel_err(vc, om.v_cache[l][:, P])
+        worst = max(worst, err_out, err_inc, err_k, err_v)
+        assert max(err_out, err_inc, err_k, err_v) < TOL[mode], (l, err_out, err_inc, err_k, err_v)
+    assert len(flagged) <= 2, flagged
+    nxt, ora_logits = oracle.decode_final(mode, om, hid[L])
+    assert rel_err(gl, ora_logits) < TOL[mode], rel_err(gl, ora_logits)
+    srt = np.sort(ora_logits)[::-1]
+    if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
+        assert gtok == nxt
+    # the captured graph (what the benchmark replays) computes the same step bit for bit
+    tok.fill_(0)
+    pos.fill_(P)
     m.step()
     torch.cuda.synchronize()
-    oracle.decode_step(mode, om, 0, cfg["ctx"] - 1)
-    gl = logits.cpu().numpy()
-    assert np.isfinite(gl).all()
-    assert int(tok.item()) == int(np.argmax(gl)) and int(pos.item()) == cfg["ctx"]
-    for l in range(4):
-        assert rel_err(t["k_cache"][l].cpu().numpy()[:, -1], om.k_cache[l][:, -1]) < 10 * TOL[mode]
-        assert rel_err(t["v_cache"][l].cpu().numpy()[:, -1], om.v_cache[l][:, -1]) < 10 * TOL[mode]
+    np.testing.assert_array_equal(logits.cpu().numpy(), gl)
+    assert int(tok.item()) == gtok
+    print(f"mode {mode}: worst per-layer relative error {worst:.3e}; near-tie layers {flagged}")
     m.close()
 
 
@@ -189,8 +245,8 @@ def _prefill_vs_oracle(q8, cfg, mode, R, pos0, tokens, seed):
     for l in range(cfg["layers"]):  # every row's key and value at its position
         kc, vc = t["k_cache"][l].cpu().numpy(), t["v_cache"][l].cpu().numpy()
         rows = slice(pos0, pos0 + R)
-        assert rel_err(kc[:, rows], om.k_cache[l][:, rows]) < 10 * TOL[mode]
-        assert rel_err(vc[:, rows], om.v_cache[l][:, rows]) < 10 * TOL[mode]
+        assert rel_err(kc[:, rows], om.k_cache[l][:, rows]) < TOL[mode]
+        assert rel_err(vc[:, rows], om.v_cache[l][:, rows]) < TOL[mode]
     m.check()
     ws.close()
     return m, tok, pos, logits

@@ -328,10 +328,16 @@ def _run_moe_gpu(q8, ws, md, mode, x, K, residual=None, expert_out=True, route_p
 
 
 def _compare_moe(out, ref, mode, K):
+    """Row by row against the oracle.  A row whose oracle router logits hold a near tie at the K-th choice (within
+    1e-5 of the largest magnitude) may choose either expert: it is counted, its outputs are still compared when the
+    GPU chose the oracle's experts, and such rows must stay rare."""
     R = out["y"].shape[0]
+    ties = 0
     for r in range(R):
         if _near_tie(ref["logits"][r], K):
-            continue
+            ties += 1
+            if not np.array_equal(out["ids"][r], ref["ids"][r]):
+                continue
         np.testing.assert_array_equal(out["ids"][r], ref["ids"][r])
         assert rel_err(out["gates"][r], ref["gates"][r]) < TOL[mode]
         for j in range(K):  # each expert separately: the gates are nearly one-hot at these router scales
@@ -339,6 +345,7 @@ def _compare_moe(out, ref, mode, K):
             if out["expert_out"] is not None:
                 assert rel_err(out["expert_out"][r, j], ref["expert_out"][r, j]) < TOL[mode]
         assert rel_err(out["y"][r], ref["y"][r]) < TOL[mode]
+    assert ties <= max(1, R // 16), f"{ties} of {R} rows hold a near tie"
     if out["hq"] is not None:  # gate-up's int8 epilogue = the quantizer applied to its own f32 rows, bit for bit
         h = out["h"].reshape(-1, out["h"].shape[-1])
         oq, os_ = oracle.quantize(h)
@@ -382,10 +389,9 @@ def test_moe_one_row_fused_path(q8, ws, moe_host, moe_dev, mode, down_reads_h, s
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("E,K,d", [(4, 4, 64), (16, 3, 1024), (64, 32, 2048), (1000, 8, 4096), (1024, 1, 32)])
 def test_route_one_row_shapes(q8, ws, mode, E, K, d):
-    # the one-cluster router: experts not a multiple of the cluster, K = E, K = 32, the widest rows, one block
+    # the one-cluster router: experts not a multiple of the cluster, K = E, K = 32, the widest rows, one block (the f32
+    # one-row router holds at most 2048 values a row: wider f32 rows take the projection + top-k launches)
     import torch
-    if mode == 0 and d > 2048:
-        pytest.skip("the f32 one-row router holds at most 2048 values a row; wider rows take the two-launch path")
     rq, rs = synth.q8_matrix(E, d, 5, 95)
     x = synth.normal((1, d), 5, recipes.VEC + 96)
     ids = empty((1, K), torch.int32)
@@ -399,12 +405,12 @@ def test_route_one_row_shapes(q8, ws, mode, E, K, d):
     l = oracle.gemv(mode, rq, rs, x[0])
     gl = host(logits)[0]
     assert rel_err(gl, l) < TOL[mode]
-    # ids: the top K of the GPU's own logits, descending, ties to the lower index
-    order = sorted(range(E), key=lambda e: (-gl[e], e))[:K]
-    np.testing.assert_array_equal(host(ids)[0], order)
-    kept = gl[order].astype(np.float64)
-    g = np.exp(kept - kept.max())
-    np.testing.assert_allclose(host(gates)[0], g / g.sum(), rtol=1e-5, atol=1e-7)
+    # ids and gates: the oracle's routing of the oracle's logits (descending, ties to the lower index)
+    ora_ids, ora_g = oracle.route(l, K)
+    if _near_tie(l, K):
+        pytest.skip("the oracle's logits hold a near tie at the K-th choice (flagged)")
+    np.testing.assert_array_equal(host(ids)[0], ora_ids)
+    assert rel_err(host(gates)[0], ora_g) < TOL[mode]
 
 
 @pytest.mark.parametrize("mode", [0, 1])

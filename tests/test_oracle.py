@@ -434,3 +434,116 @@ def test_decode_step_matches_composition_of_pinned_pieces(mode):
     for l in range(cfg["layers"]):
         np.testing.assert_array_equal(model.k_cache[l], kc[l])
         np.testing.assert_array_equal(model.v_cache[l], vc[l])
+
+
+# ---- the whole step's wiring, pinned by a closed form ------------------------------------------------------------
+
+def _select_q8(n, k, cols, coef, scale):
+    """A Q8_0 matrix whose row i has one non-zero weight, coef[i] * scale at column cols[i]: W . x = coef * scale *
+    x[cols], exact in f64."""
+    q = np.zeros((n, k), np.int8)
+    q[np.arange(n), cols] = coef
+    return q, np.full((n, k // 32), scale, np.float32)
+
+
+def test_decode_step_closed_form_with_selection_matrices():
+    """Two layers of a model whose projections each pick one input per output (selection matrices with small integer
+    quants and power-of-two scales, so every product is exact), a one-position cache (position 0: the rotation is the
+    identity and the attention returns the value row itself, for both query heads of the one key/value head), a zero
+    router (all logits 0, so experts 0 and 1 are kept with gates 1/2 each) and SwiGLU experts of selections.  Every
+    value of the step is then fixed by the definitions alone: which norm weight feeds which projection, the first
+    layer's norm of the embedding row with nothing added, the residual sums h + o and h + mixture, the gate/up roles in
+    SwiGLU, the gated combine, the final norm before the LM head and the greedy token."""
+    L, d, H, KV, hd, E, K, dff, V = 2, 64, 2, 1, 32, 4, 2, 32, 8
+    cfg = dict(layers=L, d=d, heads=H, kv_heads=KV, hd=hd, vocab=V, ctx=1, eps=1e-6, rope_theta=1e6, dff=dff,
+               experts=E, k=K)
+    rng = np.random.default_rng(5)
+
+    def coef(n):
+        return rng.choice([-3, -2, -1, 1, 2, 3], n)
+
+    def cols(n, k):
+        return rng.integers(0, k, n)
+
+    sel = dict(wq=[], wk=[], wv=[], wo=[], gate=[], up=[], down=[])
+    spec = []  # per layer: the selections' columns and coefficients
+    for l in range(L):
+        s = {}
+        for name, n, k, sc in (("wq", H * hd, d, 0.5), ("wk", KV * hd, d, 0.5), ("wv", KV * hd, d, 0.5),
+                               ("wo", d, H * hd, 0.25), ("gate", E * dff, d, 1 / 64), ("up", E * dff, d, 0.5),
+                               ("down", E * d, dff, 0.5)):
+            c, f = cols(n, k), coef(n)
+            s[name] = (c, f, sc)
+            sel[name].append(_select_q8(n, k, c, f, sc))
+        spec.append(s)
+    lm_cols, lm_coef = cols(V, d), coef(V)
+    t = iter(range(100))
+
+    def nrm(n):
+        return synth.normal(n, 9, 6000 + next(t), mul=0.1, add=1.0)
+
+    arr = dict(embed=synth.normal((V, d), 9, 6100), attn_norm=[nrm(d) for _ in range(L)],
+               ffn_norm=[nrm(d) for _ in range(L)], q_norm=[nrm(hd) for _ in range(L)],
+               k_norm=[nrm(hd) for _ in range(L)], final_norm=nrm(d), router=[_zeros_q8(E, d) for _ in range(L)],
+               lm_head=_select_q8(V, d, lm_cols, lm_coef, 1.0),
+               k_cache=[np.zeros((KV, 1, hd), np.float32) for _ in range(L)],
+               v_cache=[np.zeros((KV, 1, hd), np.float32) for _ in range(L)], **sel)
+    model = oracle.ModelArrays(cfg, **arr)
+    tok = 3
+    nxt, logits = oracle.decode_step(0, model, tok, 0)
+
+    def f32(v):
+        return np.asarray(v, np.float64).astype(np.float32)
+
+    def rms(h, w):  # s / sqrt(mean(s^2) + eps) * w
+        h = np.asarray(h, np.float64)
+        return h / math.sqrt(math.fsum(h * h) / h.size + 1e-6) * np.asarray(w, np.float64)
+
+    def pick(x, c):
+        col, f, sc = c
+        return f * sc * np.asarray(x, np.float64)[col]
+
+    h = arr["embed"][tok].copy()
+    for l in range(L):
+        s = spec[l]
+        x = f32(rms(h, arr["attn_norm"][l]))
+        k = pick(x, s["wk"])
+        v = f32(pick(x, s["wv"]))
+        k_row = f32(rms(k, arr["k_norm"][l]))  # per-head norm of the one key head; no rotation at position 0
+        np.testing.assert_allclose(model.k_cache[l][0, 0], k_row, rtol=1e-6, atol=1e-7)
+        np.testing.assert_array_equal(model.v_cache[l][0, 0], v)
+        att = f32(np.concatenate([v, v]))  # both query heads read the one key/value head; one position: weight 1
+        o = f32(pick(att, s["wo"]))
+        h = f32(h.astype(np.float64) + o)
+        x2 = f32(rms(h, arr["ffn_norm"][l]))
+        moe = np.zeros(d)
+        for e in range(K):  # the zero router keeps experts 0 and 1, gate 1/2 each
+            sub = lambda c, rows: (c[0][e * rows:(e + 1) * rows], c[1][e * rows:(e + 1) * rows], c[2])
+            g = pick(x2, sub(s["gate"], dff))
+            u = pick(x2, sub(s["up"], dff))
+            hid = f32(g / (1.0 + np.exp(-g)) * u)
+            moe = moe + 0.5 * pick(hid, sub(s["down"], d))
+        h = f32(h.astype(np.float64) + f32(moe))
+    ref = pick(f32(rms(h, arr["final_norm"])), (lm_cols, lm_coef, 1.0))
+    np.testing.assert_allclose(logits, ref, rtol=1e-6, atol=1e-7)
+    assert nxt == int(np.argmax(ref))
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_decode_step_equals_its_layers_then_final(mode):
+    # the per-layer entry points a GPU test teacher-forces compose to the whole step bit for bit
+    cfg, arr = _tiny_model(13)
+    m1 = oracle.ModelArrays(cfg, **{k: ([c.copy() for c in v] if k.endswith("cache") else v) for k, v in arr.items()})
+    m2 = oracle.ModelArrays(cfg, **{k: ([c.copy() for c in v] if k.endswith("cache") else v) for k, v in arr.items()})
+    tok, pos = 9, 4
+    nxt, logits = oracle.decode_step(mode, m1, tok, pos)
+    h = arr["embed"][tok]
+    for l in range(cfg["layers"]):
+        h, rl = oracle.decode_layer(mode, m2, l, pos, h)
+        assert rl.shape == (cfg["experts"],)
+    nxt2, logits2 = oracle.decode_final(mode, m2, h)
+    np.testing.assert_array_equal(logits, logits2)
+    assert nxt == nxt2
+    for l in range(cfg["layers"]):
+        np.testing.assert_array_equal(m1.k_cache[l], m2.k_cache[l])
+        np.testing.assert_array_equal(m1.v_cache[l], m2.v_cache[l])
