@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--correlated", action="store_true", help="with --chunk-only: rows that share their experts")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="R",
                     help="only the R-row prefill timing through the model (for a profiler capture of its kernels)")
+    ap.add_argument("--configs-only", action="store_true",
+                    help="only the single-operation configurations (projection, attention-side projections, mixture)")
     return ap.parse_args()
 
 
@@ -52,6 +54,15 @@ def dist_env():
 
 
 METRIC = "decode tokens/s and Q8_0 weight-stream GB/s (% of GB300 HBM peak), 1 GPU"
+
+
+def workload_config(cfg, mode_int8, world):
+    """The `config` object of both arms' lines (the same workload, whichever implementation runs it)."""
+    return {"workload": f"decode step, {cfg['layers']} layers d=2048 32q/4kv hd128 E=128 K=8 dff=768 vocab=151936 "
+                        "ctx=4096 (full decode configuration), tg-style growing cache",
+            "mode": "int8-activation" if mode_int8 else "f32-activation/f64-sum",
+            "l2": "inputs larger than L2: every step streams 3.42 GB of weights and ~0.8 GB of cache",
+            "parallelism": "replicas" if world > 1 else "1 GPU"}
 
 
 def slowest(sec, world, device):
@@ -212,8 +223,8 @@ def time_dominant_kernel(q8, cfg, dev, mode, reps, stream):
     return sec, K * 2 * dff * d * 9 // 8
 
 
-def cpu_baseline_oracle(cfg, host, mode, tok, pos):
-    """The oracle's whole decode step for one token on this host (single thread), from the same host arrays."""
+def oracle_model(cfg, host):
+    """The oracle's view of the benchmark's host arrays (its own copies of the caches, which a step writes)."""
     import oracle
 
     def np_(v):
@@ -221,65 +232,217 @@ def cpu_baseline_oracle(cfg, host, mode, tok, pos):
             return [np_(e) for e in v]
         if isinstance(v, tuple):
             return tuple(np_(e) for e in v)
-        return v.numpy()
+        return v.numpy() if hasattr(v, "numpy") else v
 
     arr = {k: np_(v) for k, v in host.items()}
     arr["k_cache"] = [c.copy() for c in arr["k_cache"]]
     arr["v_cache"] = [c.copy() for c in arr["v_cache"]]
-    om = oracle.ModelArrays(cfg, **arr)
-    t0 = time.perf_counter()
-    oracle.decode_step(mode, om, tok, pos)
-    dt = time.perf_counter() - t0
-    return 1.0 / dt, dt
+    return oracle.ModelArrays(cfg, **arr)
+
+
+def cpu_baseline_oracle(cfg, host, mode, tok, pos, runs=3):
+    """The oracle's whole decode step for one token on this host: single-threaded, and on every host core (threads
+    over independent rows and heads; the same results).  Median of `runs` steps each; weights generated beforehand."""
+    import oracle
+    om = oracle_model(cfg, host)
+    cores = oracle.host_cores()
+    out = {}
+    for name, threads in (("single_thread", 1), ("all_cores", cores)):
+        used = oracle.set_threads(threads)
+        times = []
+        for _ in range(runs):
+            t0 = time.perf_counter()
+            oracle.decode_step(mode, om, tok, pos)
+            times.append(time.perf_counter() - t0)
+        out[name] = {"tokens_per_s": 1.0 / statistics.median(times), "threads": used,
+                     "median_s": statistics.median(times), "runs": runs}
+    oracle.set_threads(1)
+    return out, cores
 
 
 def run_reference(args):
-    """The reference arm: the CPU oracle (the only other implementation of what the pages define), each step a bounded
-    sample of the decode step — one layer of the 48 (layer = step mod 48) plus 1/48 of the LM head — scaled to
-    tokens/s as 1 / (48 x sample time)."""
+    """The reference arm: the CPU oracle (the only other implementation of what the pages define) on every host core,
+    one whole decode step (48 layers, LM head, greedy token) per step, at the same growing positions as the GPU arm,
+    from the same seeded weights (generated before the timing)."""
     world, rank, local = dist_env()
     if rank != 0:
         return
     import numpy as np
     import oracle
-    import synth
     from synth import recipes
-    cfg = dict(recipes.DECODE)
-    L = cfg["layers"]
-    one = dict(cfg, layers=1, vocab=cfg["vocab"] // L)
+    cfg = dict(recipes.DECODE, layers=args.layers)
     mode = 1 if args.mode == "int8" else 0
-    pos = cfg["ctx"] - 1
-    base = recipes.decode_model(one, seed=0)
+    host = recipes.decode_model(cfg, seed=0)
+    om = oracle_model(cfg, host)
+    threads = oracle.set_threads(oracle.host_cores())
+    total = args.warmup + args.steps
+    start_pos = cfg["ctx"] - total
     times = []
-    for step in range(args.warmup + args.steps):
-        ids = recipes.layer_ids(step % L)
-        arr = dict(base)
-        for key in ("wq", "wk", "wv", "wo", "router", "gate", "up", "down"):
-            n, k = base[key][0][0].shape
-            arr[key] = [synth.q8_matrix(n, k, 0, ids[key])]  # this step's layer (generated outside the timing)
-        arr["k_cache"] = [c.copy() for c in base["k_cache"]]
-        arr["v_cache"] = [c.copy() for c in base["v_cache"]]
-        om = oracle.ModelArrays(one, **arr)
+    tok = 0
+    for step in range(total):
         t0 = time.perf_counter()
-        oracle.decode_step(mode, om, 0, pos)
+        tok, _ = oracle.decode_step(mode, om, tok, start_pos + step)
         dt = time.perf_counter() - t0
         if step >= args.warmup:
             times.append(dt)
-    per_token = L * float(np.mean(times))
-    value = 1.0 / per_token
+    sec = float(np.sum(times))
+    value = args.steps / sec
     line = {
         "impl": "reference", "metric": METRIC,
         "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_token * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "i8" if mode else "f32", "data": "synthetic",
-        "config": {"workload": "decode step, 48 layers d=2048 32q/4kv hd128 E=128 K=8 dff=768 vocab=151936 "
-                               "ctx=4096 (full decode configuration)", "mode": args.mode},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "per step: one decoder layer (layer = step mod 48) plus 1/48 of the LM head rows "
-                                   "at position 4095, single-threaded f64 C oracle, scaled x48 to one token"},
+        "config": workload_config(cfg, mode == 1, 1),
+        "positions": [start_pos + args.warmup, cfg["ctx"] - 1],
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "host_cores": oracle.host_cores(),
+                         "kind": "oracle",
+                         "sample": f"{args.steps} whole decode steps ({cfg['layers']} layers, LM head, greedy token) at "
+                                   f"positions {start_pos + args.warmup}..{cfg['ctx'] - 1}, f64 C oracle on {threads} "
+                                   "threads, each step timed whole"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    oracle.set_threads(1)
     print(json.dumps(line), flush=True)
+
+
+def _graph_time(stream, body, n, reps):
+    """`body(i)` for i < n captured in one CUDA graph, replayed once to warm up and then `reps` times between CUDA events
+    on `stream`; returns seconds per body call."""
+    import torch
+    s = torch.cuda.ExternalStream(stream)
+    with torch.cuda.stream(s):
+        for i in range(min(n, 2)):
+            body(i)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n):
+                body(i)
+        g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.synchronize()
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s)
+        e1.synchronize()
+        del g
+    return e0.elapsed_time(e1) / 1e3 / (reps * n)
+
+
+def time_configs(q8, cfg, dev, stream, peak, reps=4):
+    """The single-operation configurations, each as a user calls it through the C ABI, captured in CUDA graphs and
+    timed with CUDA events; `cold` walks over copies or layers whose weights together exceed L2 several times (each
+    call reads weights no recent call touched), `hot` repeats one call whose weights stay in L2.
+      config 0: one Q8_0 projection 1024 x 1024, batch 1, both numerics (int8 mode: the activation quantized once
+                beforehand, as a producer's epilogue leaves it)
+      config 1: add_rmsnorm_q8 feeding the q, k and v projections (2048 -> 4096, 512, 512), and the o projection
+                (4096 -> 2048) of a fresh activation: the dense attention-side projections of one layer
+      config 2: the mixture block for one token row: moe_route_topk, moe_gate_up, moe_down_combine (router and 8 of 128
+                experts)"""
+    import torch
+    import synth
+    from synth import recipes
+    L, d = cfg["layers"], cfg["d"]
+    s = torch.cuda.ExternalStream(stream)
+    ws = q8.Workspace(64 << 20)
+    out = {}
+
+    def entry(sec, nbytes, **kw):
+        gbs = nbytes / sec / 1e9
+        return dict(us=sec * 1e6, weight_gbs=gbs, frac_of_peak=gbs / peak, **kw)
+
+    with torch.cuda.stream(s):
+        # ---- config 0 ----
+        n = k = 1024
+        q0, s0 = synth.q8_matrix(n, k, 0, recipes.MAT)
+        x0 = torch.from_numpy(recipes.activations(1, k, 0, 0)).cuda()
+        nrep = 448  # 448 x 1.18 MB = 528 MB of copies, over four times the L2
+        qrep = torch.from_numpy(q0).cuda().unsqueeze(0).repeat(nrep, 1, 1)
+        srep = torch.from_numpy(s0).cuda().unsqueeze(0).repeat(nrep, 1, 1)
+        xq0 = torch.empty(1, k, dtype=torch.int8, device="cuda")
+        xs0 = torch.empty(1, k // 32, dtype=torch.float32, device="cuda")
+        q8.q8_quantize(x0, xq0, xs0, stream=stream)
+        y0 = torch.empty(1, n, device="cuda")
+        nbytes0 = n * k * 9 // 8
+        c0 = {}
+        for mode, name in ((q8.F32ACT_F64SUM, "f32-activation/f64-sum"), (q8.INT8ACT, "int8-activation")):
+            def gemv(i, mode=mode):
+                if mode == q8.INT8ACT:
+                    q8.q8_gemv(qrep[i], srep[i], mode, y0, xq=xq0, xs=xs0, ws=ws, stream=stream)
+                else:
+                    q8.q8_gemv(qrep[i], srep[i], mode, y0, x=x0, ws=ws, stream=stream)
+            c0[name] = {"cold": entry(_graph_time(stream, gemv, nrep, reps), nbytes0),
+                        "hot": entry(_graph_time(stream, lambda i: gemv(0), nrep, reps), nbytes0)}
+        out["config0"] = {"what": "Q8_0 projection 1024 x 1024, batch 1 (weights 1,179,648 B)", **c0}
+        del qrep, srep
+        # ---- config 1 ----
+        H, KV, HD = cfg["heads"], cfg["kv_heads"], cfg["hd"]
+        a1 = torch.from_numpy(recipes.activations(1, d, 0, 10)).cuda()
+        b1 = torch.from_numpy(recipes.activations(1, d, 0, 11)).cuda()
+        xo = torch.from_numpy(recipes.activations(1, H * HD, 0, 12)).cuda()
+        sum1 = torch.empty(1, d, device="cuda")
+        x1 = torch.empty(1, d, device="cuda")
+        xq1 = torch.empty(1, d, dtype=torch.int8, device="cuda")
+        xs1 = torch.empty(1, d // 32, dtype=torch.float32, device="cuda")
+        xqo = torch.empty(1, H * HD, dtype=torch.int8, device="cuda")
+        xso = torch.empty(1, H * HD // 32, dtype=torch.float32, device="cuda")
+        q8.q8_quantize(xo, xqo, xso, stream=stream)
+        yq, yk, yv = (torch.empty(1, m, device="cuda") for m in (H * HD, KV * HD, KV * HD))
+        yo = torch.empty(1, d, device="cuda")
+        nbytes1 = ((H * HD + 2 * KV * HD) * d + d * H * HD) * 9 // 8
+        c1 = {}
+        for mode, name in ((q8.INT8ACT, "int8-activation"), (q8.F32ACT_F64SUM, "f32-activation/f64-sum")):
+            def attn_side(l, mode=mode):
+                if mode == q8.INT8ACT:
+                    q8.add_rmsnorm_q8(a1, b1, dev["attn_norm"][l], cfg["eps"], sum_out=sum1, yq=xq1, ys=xs1,
+                                      stream=stream)
+                    for w, y in (("wq", yq), ("wk", yk), ("wv", yv)):
+                        q8.q8_gemv(*dev[w][l], mode, y, xq=xq1, xs=xs1, ws=ws, stream=stream)
+                    q8.q8_gemv(*dev["wo"][l], mode, yo, xq=xqo, xs=xso, ws=ws, stream=stream)
+                else:
+                    q8.add_rmsnorm_q8(a1, b1, dev["attn_norm"][l], cfg["eps"], sum_out=sum1, y_out=x1, stream=stream)
+                    for w, y in (("wq", yq), ("wk", yk), ("wv", yv)):
+                        q8.q8_gemv(*dev[w][l], mode, y, x=x1, ws=ws, stream=stream)
+                    q8.q8_gemv(*dev["wo"][l], mode, yo, x=xo, ws=ws, stream=stream)
+            c1[name] = {"cold": entry(_graph_time(stream, attn_side, L, reps), nbytes1, launches=5),
+                        "hot": entry(_graph_time(stream, lambda i: attn_side(0), L, reps), nbytes1, launches=5)}
+        out["config1"] = {"what": "add_rmsnorm_q8 -> q/k/v projections, o projection at d = 2048 (weights "
+                                  f"{nbytes1:,} B); cold = the 48 layers' matrices in turn", **c1}
+        # ---- config 2 ----
+        E, K, dff = cfg["experts"], cfg["k"], cfg["dff"]
+        x2 = torch.from_numpy(recipes.activations(1, d, 0, 20)).cuda()
+        r2 = torch.from_numpy(recipes.activations(1, d, 0, 21)).cuda()
+        xq2 = torch.empty(1, d, dtype=torch.int8, device="cuda")
+        xs2 = torch.empty(1, d // 32, dtype=torch.float32, device="cuda")
+        q8.q8_quantize(x2, xq2, xs2, stream=stream)
+        ids = torch.empty(1, K, dtype=torch.int32, device="cuda")
+        gates = torch.empty(1, K, device="cuda")
+        h = torch.empty(K, dff, device="cuda")
+        hq = torch.empty(K, dff, dtype=torch.int8, device="cuda")
+        hs = torch.empty(K, dff // 32, device="cuda")
+        y2 = torch.empty(1, d, device="cuda")
+        nbytes2 = (E * d + K * 3 * dff * d) * 9 // 8
+        c2 = {}
+        for mode, name in ((q8.INT8ACT, "int8-activation"), (q8.F32ACT_F64SUM, "f32-activation/f64-sum")):
+            def block(l, mode=mode):
+                if mode == q8.INT8ACT:
+                    q8.moe_route_topk(*dev["router"][l], mode, K, ids, gates, xq=xq2, xs=xs2, ws=ws, stream=stream)
+                    q8.moe_gate_up(*dev["gate"][l], *dev["up"][l], dff, mode, K, ids, h, xq=xq2, xs=xs2, hq=hq, hs=hs,
+                                   ws=ws, stream=stream)
+                    q8.moe_down_combine(*dev["down"][l], d, mode, K, ids, gates, y2, h=h, hq=hq, hs=hs, residual=r2,
+                                        ws=ws, stream=stream)
+                else:
+                    q8.moe_route_topk(*dev["router"][l], mode, K, ids, gates, x=x2, ws=ws, stream=stream)
+                    q8.moe_gate_up(*dev["gate"][l], *dev["up"][l], dff, mode, K, ids, h, x=x2, ws=ws, stream=stream)
+                    q8.moe_down_combine(*dev["down"][l], d, mode, K, ids, gates, y2, h=h, residual=r2, ws=ws,
+                                        stream=stream)
+            c2[name] = {"cold": entry(_graph_time(stream, block, L, reps), nbytes2, launches=3),
+                        "hot": entry(_graph_time(stream, lambda i: block(0), L, reps), nbytes2, launches=3)}
+        out["config2"] = {"what": "mixture block, one token row: route + top-8 of 128, gate-up SwiGLU, down-and-combine "
+                                  f"(weights touched {nbytes2:,} B); cold = the 48 layers' experts in turn", **c2}
+    ws.close()
+    return out
 
 
 def time_chunks(q8, cfg, dev, stream, reps=4, correlated=False, rows=(2, 4, 8, 16, 32, 64)):
@@ -428,6 +591,10 @@ def main():
         print(json.dumps({"roofline_only": True, "us_per_launch": dom_sec * 1e6, "algorithmic_bytes": dom_bytes,
                           "gbs": dom_bytes / dom_sec / 1e9}), flush=True)
         return
+    if args.configs_only:
+        print(json.dumps({"configs_only": True, **time_configs(q8, cfg, dev, sh, peaks()[0],
+                                                                reps=max(1, args.steps))}), flush=True)
+        return
     model = q8.Model(cfg, dev, mode, tok, pos, logits)
     if args.prefill_only:
         res = time_prefill(q8, model, cfg, tok, pos, sh, rows=(args.prefill_only,), reps=max(1, args.steps))
@@ -500,12 +667,8 @@ def main():
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "i8" if mode == q8.INT8ACT else "f32", "data": "synthetic",
-        "config": {"workload": f"decode step, {cfg['layers']} layers d=2048 32q/4kv hd128 E=128 K=8 dff=768 "
-                               "vocab=151936 ctx=4096 (full decode configuration), tg-style growing cache",
-                   "mode": "int8-activation" if mode == q8.INT8ACT else "f32-activation/f64-sum",
-                   "positions": [start_pos + args.warmup, cfg["ctx"] - 1],
-                   "l2": "inputs larger than L2: every step streams 3.42 GB of weights and ~0.8 GB of cache",
-                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "config": workload_config(cfg, mode == q8.INT8ACT, world),
+        "positions": [start_pos + args.warmup, cfg["ctx"] - 1],
         "weight_stream": {"gbs": weight_gbs, "frac_of_peak": weight_gbs / peak, "bytes_per_token": wbytes,
                           "peak_gbs": peak, "peak_kind": peak_kind},
         "hbm_total_gbs": total_gbs,
@@ -548,11 +711,18 @@ def main():
                 "uncorrelated": time_chunks(q8, cfg, dev, sh, reps=max(2, min(args.steps, 8))),
                 "correlated": time_chunks(q8, cfg, dev, sh, reps=max(2, min(args.steps, 8)), correlated=True,
                                           rows=(16, 32, 64))}
+            line["configs"] = time_configs(q8, cfg, dev, sh, peak)
         if not args.no_cpu_baseline:
-            v, dt = cpu_baseline_oracle(cfg, host, 1 if mode == q8.INT8ACT else 0, 0, cfg["ctx"] - 1)
-            line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                    "sample": f"one whole decode step (all {cfg['layers']} layers and the LM head) at "
-                                              f"position 4095, single-threaded f64 C oracle, {dt:.1f} s"}
+            cb, cores = cpu_baseline_oracle(cfg, host, 1 if mode == q8.INT8ACT else 0, 0, cfg["ctx"] - 1)
+            allc, one = cb["all_cores"], cb["single_thread"]
+            line["cpu_baseline"] = {"value": allc["tokens_per_s"], "unit": "tokens/s", "cores": allc["threads"],
+                                    "host_cores": cores, "kind": "oracle",
+                                    "sample": f"one whole decode step (all {cfg['layers']} layers, LM head, greedy "
+                                              f"token) at position 4095, f64 C oracle on {allc['threads']} threads, "
+                                              f"median of {allc['runs']} steps of {allc['median_s']:.2f} s",
+                                    "single_thread": {"value": one["tokens_per_s"], "unit": "tokens/s", "cores": 1,
+                                                      "median_s": one["median_s"], "runs": one["runs"]},
+                                    "weight_gbs_all_cores": wbytes * allc["tokens_per_s"] / 1e9}
         print(json.dumps(line), flush=True)
     model.close()
     if world > 1:

@@ -20,13 +20,15 @@ QBLOCK = 32
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with the host C compiler: IEEE arithmetic, no contraction, no fast-math."""
+    """Compile the oracle with the host C compiler: IEEE arithmetic, no contraction, no fast-math; with OpenMP when the
+    compiler has it (only for the optional all-cores mode), else single-threaded."""
     srcs = [os.path.join(_HERE, "oracle.c")]
     deps = srcs + [os.path.join(_HERE, "oracle.h")]
     if force or not os.path.exists(_LIB_PATH) or any(os.path.getmtime(_LIB_PATH) < os.path.getmtime(p) for p in deps):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-                               *srcs, "-o", tmp, "-lm"])
+        base = ["gcc", "-O2", "-fPIC", "-shared", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", *srcs, "-o", tmp]
+        if subprocess.run(base + ["-fopenmp", "-lm"], capture_output=True).returncode != 0:
+            subprocess.check_call(base + ["-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -59,6 +61,8 @@ def lib():
         L = ctypes.CDLL(_LIB_PATH)
         vp, i64, i32, f32, dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_double
         sig = {
+            "ora_set_threads": ([i32], i32),
+            "ora_host_cores": ([], i32),
             "ora_q8_weight": ([vp, vp, i64, i64, i64], dbl),
             "ora_q8_dequant": ([vp, vp, i64, i64, vp], None),
             "ora_gemv_f32act": ([vp, vp, i64, i64, vp, vp], None),
@@ -66,6 +70,8 @@ def lib():
             "ora_blockdots": ([vp, i64, i64, vp, vp], None),
             "ora_gemv_int8act": ([vp, vp, i64, i64, vp, vp, vp], None),
             "ora_gemv": ([i32, vp, vp, i64, i64, vp, vp], None),
+            "ora_quantize2": ([vp, i64, vp, vp, vp], None),
+            "ora_gemv_int8act2": ([vp, vp, i64, i64, vp, vp, vp, vp], None),
             "ora_add_rmsnorm": ([vp, vp, vp, i64, i64, f32, vp, vp], None),
             "ora_softmax": ([vp, i64, vp], None),
             "ora_topk": ([vp, i64, i32, vp], None),
@@ -88,6 +94,15 @@ def lib():
             fn.restype = res
         _lib = L
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Threads the oracle uses from now on (1 by default; the results do not depend on it); returns the count set."""
+    return int(lib().ora_set_threads(int(n)))
+
+
+def host_cores() -> int:
+    return int(lib().ora_host_cores())
 
 
 def _c(a, dtype):
@@ -121,6 +136,28 @@ def quantize(x):
     return xq, xs
 
 
+def quantize2(x):
+    """Two int8 words per value (high, low in 128ths of the scale) plus an f32 scale per 32-value block."""
+    x, px = _c(x, np.float32)
+    hi = np.empty(x.shape, np.int8)
+    lo = np.empty(x.shape, np.int8)
+    xs = np.empty(x.shape[:-1] + (x.shape[-1] // QBLOCK,), np.float32)
+    lib().ora_quantize2(px, x.size, hi.ctypes.data, lo.ctypes.data, xs.ctypes.data)
+    return hi, lo, xs
+
+
+def gemv_int8act2(q, s, hi, lo, xs):
+    q, pq = _c(q, np.int8)
+    s, ps = _c(s, np.float32)
+    hi, ph = _c(hi, np.int8)
+    lo, pl = _c(lo, np.int8)
+    xs, pxs = _c(xs, np.float32)
+    n, k = q.shape
+    y = np.empty(n, np.float64)
+    lib().ora_gemv_int8act2(pq, ps, n, k, ph, pl, pxs, y.ctypes.data)
+    return y
+
+
 def blockdots(q, xq):
     q, pq = _c(q, np.int8)
     xq, px = _c(xq, np.int8)
@@ -152,7 +189,8 @@ def gemv_int8act(q, s, xq, xs):
 
 
 def gemv(mode, q, s, x):
-    """y = W x for one activation row (mode 0: f32 activations / f64 sums; mode 1: one-word int8 activations)."""
+    """y = W x for one activation row (mode 0: f32 activations / f64 sums; mode 1: one-word int8 activations; mode 2:
+    two-word int8 activations)."""
     q, pq = _c(q, np.int8)
     s, ps = _c(s, np.float32)
     x, px = _c(x, np.float32)

@@ -8,6 +8,30 @@
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#include <unistd.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ==== threads =================================================================================================== */
+
+/* The oracle runs single-threaded unless a caller (the benchmark's all-cores CPU baseline) asks for more.  Threads
+ * only split independent outputs (the rows of a projection, the heads of an attention): every output is computed by
+ * the same loop in the same order whatever the thread count, so the results do not depend on it.  Built without
+ * OpenMP, the pragmas are ignored and the oracle stays single-threaded. */
+static int g_threads = 1;
+
+int ora_set_threads(int n) {
+#ifdef _OPENMP
+    g_threads = n < 1 ? 1 : n;
+#else
+    (void)n;
+    g_threads = 1;
+#endif
+    return g_threads;
+}
+
+int ora_host_cores(void) { return (int)sysconf(_SC_NPROCESSORS_ONLN); }
 
 /* ==== Q8_0 matrices ============================================================================================= */
 
@@ -27,6 +51,7 @@ void ora_q8_dequant(const int8_t *q, const float *s, int64_t n, int64_t k, doubl
  * accumulator; forward_shim.rs, ForwardShim::numerics (Q8MatKind::Dequant: no activation quantized).
  * y[o] = sum_t W[o][t] * x[t], every term and the sum in f64. */
 void ora_gemv_f32act(const int8_t *q, const float *s, int64_t n, int64_t k, const float *x, double *y) {
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1 && n * k >= (1 << 16))
     for (int64_t o = 0; o < n; ++o) {
         double acc = 0.0;
         for (int64_t t = 0; t < k; ++t) acc += ora_q8_weight(q, s, k, o, t) * (double)x[t];
@@ -79,19 +104,88 @@ void ora_blockdots(const int8_t *q, int64_t n, int64_t k, const int8_t *xq, int3
 void ora_gemv_int8act(const int8_t *q, const float *s, int64_t n, int64_t k, const int8_t *xq, const float *xs,
                       double *y) {
     int64_t nb = k / ORA_QBLOCK;
-    int32_t *dots = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nb > 0 ? nb : 1));
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1 && n * k >= (1 << 16))
     for (int64_t o = 0; o < n; ++o) {
-        ora_blockdots(q + o * k, 1, k, xq, dots);
         double acc = 0.0;
-        for (int64_t b = 0; b < nb; ++b) acc += (double)s[o * nb + b] * (double)xs[b] * (double)dots[b];
+        for (int64_t b = 0; b < nb; ++b) {
+            int32_t dot;
+            ora_blockdots(q + o * k + b * ORA_QBLOCK, 1, ORA_QBLOCK, xq + b * ORA_QBLOCK, &dot);
+            acc += (double)s[o * nb + b] * (double)xs[b] * (double)dot;
+        }
         y[o] = acc;
     }
-    free(dots);
+}
+
+/* The two-word activation (lane/mod.rs module docs: "a two-word ~14-bit int8 activation (the default)";
+ * forward_shim.rs, ForwardShim::activation: Q8MatKind::TwoPassInt8 -> QuantFormat::TwoWords; lane/arena.rs,
+ * array_bytes and quant_parts: a quantized array is its words, then its low words under two words, then one f32 scale
+ * a 32-value block).  The pages give the parts, not the rule.  The reading taken: the high word and the scale are the
+ * one-word rule's, and the low word holds what the high word leaves, in 128ths of the scale:
+ *   t = x / d (one f32 division, d = amax/127 as above);  hi = round-half-away(t) clamped to +-127;
+ *   lo = round-half-away(128 (t - hi))   (t - hi and the product by 128 are exact in f32; |lo| <= 64)
+ * so x ~ d (hi + lo/128) = (d/128)(128 hi + lo), a signed integer of 14 magnitude bits (|128 hi + lo| <= 16320)
+ * on the block's one scale. */
+void ora_quantize2(const float *x, int64_t n, int8_t *hi, int8_t *lo, float *xs) {
+    for (int64_t b = 0; b < n / ORA_QBLOCK; ++b) {
+        const float *v = x + b * ORA_QBLOCK;
+        float amax = 0.0f;
+        for (int t = 0; t < ORA_QBLOCK; ++t) {
+            float a = fabsf(v[t]);
+            if (a > amax) amax = a;
+        }
+        float d = amax / 127.0f;
+        xs[b] = d;
+        for (int t = 0; t < ORA_QBLOCK; ++t) {
+            int8_t wh = 0, wl = 0;
+            if (d != 0.0f) {
+                float q = v[t] / d;
+                float r = roundf(q);
+                if (r > 127.0f) r = 127.0f;
+                if (r < -127.0f) r = -127.0f;
+                float f = roundf((q - r) * 128.0f);
+                if (f > 127.0f) f = 127.0f;
+                if (f < -127.0f) f = -127.0f;
+                wh = (int8_t)r;
+                wl = (int8_t)f;
+            }
+            hi[b * ORA_QBLOCK + t] = wh;
+            lo[b * ORA_QBLOCK + t] = wl;
+        }
+    }
+}
+
+/* The two-word product: per block the exact integer 128 D[o,b](hi) + D[o,b](lo) of the two words' int32 dots, so
+ * y[o] = sum_b s_w[o,b] * s_x[b] / 128 * (128 D_hi + D_lo), in f64. */
+void ora_gemv_int8act2(const int8_t *q, const float *s, int64_t n, int64_t k, const int8_t *hi, const int8_t *lo,
+                       const float *xs, double *y) {
+    int64_t nb = k / ORA_QBLOCK;
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1 && n * k >= (1 << 16))
+    for (int64_t o = 0; o < n; ++o) {
+        double acc = 0.0;
+        for (int64_t b = 0; b < nb; ++b) {
+            int32_t dh, dl;
+            ora_blockdots(q + o * k + b * ORA_QBLOCK, 1, ORA_QBLOCK, hi + b * ORA_QBLOCK, &dh);
+            ora_blockdots(q + o * k + b * ORA_QBLOCK, 1, ORA_QBLOCK, lo + b * ORA_QBLOCK, &dl);
+            acc += (double)s[o * nb + b] * (double)xs[b] / 128.0 * (128.0 * (double)dh + (double)dl);
+        }
+        y[o] = acc;
+    }
 }
 
 void ora_gemv(int mode, const int8_t *q, const float *s, int64_t n, int64_t k, const float *x, double *y) {
     if (mode == 0) {
         ora_gemv_f32act(q, s, n, k, x, y);
+        return;
+    }
+    if (mode == 2) {
+        int8_t *hi = (int8_t *)malloc((size_t)(k > 0 ? k : 1));
+        int8_t *lo = (int8_t *)malloc((size_t)(k > 0 ? k : 1));
+        float *xs = (float *)malloc(sizeof(float) * (size_t)(k / ORA_QBLOCK + 1));
+        ora_quantize2(x, k, hi, lo, xs);
+        ora_gemv_int8act2(q, s, n, k, hi, lo, xs, y);
+        free(hi);
+        free(lo);
+        free(xs);
         return;
     }
     int8_t *xq = (int8_t *)malloc((size_t)(k > 0 ? k : 1));
@@ -339,6 +433,7 @@ void ora_decode_layer(int mode, const ora_model *m, int64_t l, int64_t pos, floa
             vr[i] = (float)v[g * hd + i];
         }
     }
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1)
     for (int64_t hh = 0; hh < H; ++hh) {
         const int64_t g = hh / group;
         ora_attention(q + hh * hd, m->k_cache[l] + g * ctx * hd, m->v_cache[l] + g * ctx * hd, pos + 1, hd,

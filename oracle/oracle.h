@@ -2,7 +2,8 @@
  * CPU oracle of the Q8_0 mixture-of-experts decode step — TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT.
  *
  * Only the test suite, the smoke check and the benchmark's CPU-baseline leg may load or call this library.  It shares
- * no code with the CUDA path: it is a plain, slow, single-threaded restatement in C of what the pages define, in f64
+ * no code with the CUDA path: it is a plain, slow restatement in C of what the pages define (single-threaded unless
+ * ora_set_threads asks for more), in f64
  * wherever the pages do not fix another precision.  Each function names the passage it follows.
  *
  * Pages cited (their titles):
@@ -26,6 +27,10 @@ extern "C" {
 
 #define ORA_QBLOCK 32
 
+/* Threads the oracle may use (1 unless set; the results do not depend on it) and the host's online cores. */
+int ora_set_threads(int n);
+int ora_host_cores(void);
+
 /* ---- Q8_0 matrices and projections ---------------------------------------------------------------------------- */
 double ora_q8_weight(const int8_t *q, const float *s, int64_t k, int64_t o, int64_t t);
 void ora_q8_dequant(const int8_t *q, const float *s, int64_t n, int64_t k, double *w);
@@ -34,7 +39,12 @@ void ora_quantize(const float *x, int64_t n, int8_t *xq, float *xs);
 void ora_blockdots(const int8_t *q, int64_t n, int64_t k, const int8_t *xq, int32_t *dots);
 void ora_gemv_int8act(const int8_t *q, const float *s, int64_t n, int64_t k, const int8_t *xq, const float *xs,
                       double *y);
-/* mode 0: f32 activations, f64 sums; mode 1: x quantized to one int8 word per value, then mode-1 sums. */
+/* The two-word activation: high words, low words (128ths of the scale) and one scale per 32-value block. */
+void ora_quantize2(const float *x, int64_t n, int8_t *hi, int8_t *lo, float *xs);
+void ora_gemv_int8act2(const int8_t *q, const float *s, int64_t n, int64_t k, const int8_t *hi, const int8_t *lo,
+                       const float *xs, double *y);
+/* mode 0: f32 activations, f64 sums; mode 1: x quantized to one int8 word per value, then mode-1 sums; mode 2: x
+ * quantized to two words per value, then the two-word sums. */
 void ora_gemv(int mode, const int8_t *q, const float *s, int64_t n, int64_t k, const float *x, double *y);
 
 /* ---- residual add + RMSNorm ----------------------------------------------------------------------------------- */

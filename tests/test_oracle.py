@@ -547,3 +547,103 @@ def test_decode_step_equals_its_layers_then_final(mode):
     for l in range(cfg["layers"]):
         np.testing.assert_array_equal(m1.k_cache[l], m2.k_cache[l])
         np.testing.assert_array_equal(m1.v_cache[l], m2.v_cache[l])
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_threads_do_not_change_results(mode):
+    # the all-cores mode only splits independent outputs (projection rows, attention heads): bit-identical results
+    cfg, arr = _tiny_model(17, d=256, heads=8, kv=2, hd=32, dff=64, E=8, K=2, vocab=300, ctx=16)
+    outs = []
+    for threads in (1, 4):
+        oracle.set_threads(threads)
+        try:
+            model = oracle.ModelArrays(cfg, **{k: ([c.copy() for c in v] if k.endswith("cache") else v)
+                                               for k, v in arr.items()})
+            outs.append(oracle.decode_step(mode, model, 7, 9) + (model.k_cache[1].copy(),))
+        finally:
+            oracle.set_threads(1)
+    assert outs[0][0] == outs[1][0]
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])
+    np.testing.assert_array_equal(outs[0][2], outs[1][2])
+    assert oracle.host_cores() >= 1
+
+
+# ---- the two-word activation ---------------------------------------------------------------------------------------
+
+def test_quantize2_hand_block():
+    g = GOLD["quantize2_hand"]
+    hi, lo, xs = oracle.quantize2(np.array(g["x"], np.float32))
+    assert hi.tolist() == g["hi"] and lo.tolist() == g["lo"] and xs[0] == np.float32(g["d"])
+
+
+def test_quantize2_invariants():
+    x = synth.normal((64, 256), seed=3, tensor=40, mul=3.0)
+    x[5, :32] = 0.0  # an all-zero block: zero words, zero scale
+    hi, lo, xs = oracle.quantize2(x)
+    q1, s1 = oracle.quantize(x)
+    np.testing.assert_array_equal(hi, q1)  # the high word and the scale are the one-word rule's
+    np.testing.assert_array_equal(xs, s1)
+    assert np.abs(lo.astype(np.int32)).max() <= 64
+    assert not hi[5, :32].any() and not lo[5, :32].any() and xs[5, 0] == 0.0
+    blocks = x.reshape(64, 8, 32).astype(np.float64)
+    rec = (hi.reshape(64, 8, 32) + lo.reshape(64, 8, 32) / 128.0) * xs[..., None]
+    # within half a 128th of the scale, plus the one rounding of the f32 quotient (|x/d| <= 128: 2^-17 at most)
+    assert np.all(np.abs(blocks - rec) <= xs[..., None] * (1 / 256 + 2.0 ** -16))
+    # and never worse than the one-word form (up to the quotient's rounding, where the high word alone is exact)
+    rec1 = q1.reshape(64, 8, 32) * xs[..., None]
+    assert np.all(np.abs(blocks - rec) <= np.abs(blocks - rec1) + xs[..., None] * 2.0 ** -16)
+
+
+def test_gemv_int8act2_unit_scales_and_exact_brute_force():
+    q = synth.int8((7, 64), seed=4, tensor=41)
+    hi = synth.int8(64, seed=4, tensor=42)
+    lo = (synth.int8(64, seed=4, tensor=43) // 2).astype(np.int8)
+    ones = np.ones((7, 2), np.float32)
+    ref = q.astype(np.int64) @ (128 * hi.astype(np.int64) + lo.astype(np.int64))
+    np.testing.assert_array_equal(oracle.gemv_int8act2(q, ones, hi, lo, np.ones(2, np.float32)), ref / 128.0)
+    # scaled blocks against exact rationals
+    s = synth.normal((7, 2), seed=4, tensor=44, mul=0.01, absval=True)
+    xs = synth.normal(2, seed=4, tensor=45, absval=True)
+    y = oracle.gemv_int8act2(q, s, hi, lo, xs)
+    for o in range(7):
+        exact = sum(Fraction(float(s[o, t // 32])) * Fraction(float(xs[t // 32])) * int(q[o, t]) *
+                    (Fraction(int(hi[t])) + Fraction(int(lo[t]), 128)) for t in range(64))
+        assert abs(Fraction(y[o]) - exact) <= abs(exact) * Fraction(1, 10 ** 13) + Fraction(1, 10 ** 30)
+
+
+def test_gemv_mode2_is_quantize2_then_two_word_product():
+    q, s = synth.q8_matrix(11, 96, seed=5, tensor=46)
+    x = synth.normal(96, seed=5, tensor=47)
+    hi, lo, xs = oracle.quantize2(x)
+    np.testing.assert_array_equal(oracle.gemv(2, q, s, x), oracle.gemv_int8act2(q, s, hi, lo, xs))
+    # mode 2 differs from the exact f32-activation product by at most 1/256 of a scale per value (plus the quotient's
+    # rounding): 128 times closer than one word's bound
+    y0, y2 = oracle.gemv(0, q, s, x), oracle.gemv(2, q, s, x)
+    w = np.abs(oracle.dequant(q, s))
+    bound = w @ np.repeat(xs, 32).astype(np.float64) * (1 / 256 + 2.0 ** -16)
+    assert np.all(np.abs(y0 - y2) <= bound)
+
+
+def test_moe_and_step_run_in_mode2():
+    # the mixture and the whole step take the two-word numerics through every projection: the mean-expert invariant
+    # holds, and the step stays within the two-word bound's reach of the f32 step on a tiny model
+    d, dff, E = 64, 32, 4
+    router = _zeros_q8(E, d)
+    gate = synth.q8_matrix(E * dff, d, seed=1, tensor=30)
+    up = synth.q8_matrix(E * dff, d, seed=1, tensor=31)
+    down = synth.q8_matrix(E * d, dff, seed=1, tensor=32)
+    w = oracle.MoeWeights(d, dff, E, E, router, gate, up, down)
+    x = synth.normal(d, seed=1, tensor=33)
+    out = oracle.moe_rows(2, w, x)
+    np.testing.assert_allclose(out["gates"][0], np.full(E, 1.0 / E), rtol=1e-15)
+    np.testing.assert_allclose(out["y"][0], out["expert_out"][0].mean(0), rtol=1e-12, atol=1e-12)
+    cfg, arr = _tiny_model(19)
+    m0 = oracle.ModelArrays(cfg, **{k: ([c.copy() for c in v] if k.endswith("cache") else v) for k, v in arr.items()})
+    m2 = oracle.ModelArrays(cfg, **{k: ([c.copy() for c in v] if k.endswith("cache") else v) for k, v in arr.items()})
+    _, l0 = oracle.decode_step(0, m0, 3, 2)
+    _, l2 = oracle.decode_step(2, m2, 3, 2)
+    _, l1 = oracle.decode_step(1, oracle.ModelArrays(cfg, **{k: ([c.copy() for c in v] if k.endswith("cache") else v)
+                                                             for k, v in arr.items()}), 3, 2)
+    e2 = np.max(np.abs(l2 - l0)) / np.max(np.abs(l0))
+    e1 = np.max(np.abs(l1 - l0)) / np.max(np.abs(l0))
+    assert e2 < 1e-3 and e2 < e1 / 8, (e1, e2)
