@@ -21,6 +21,10 @@
  *     "llama.cpp's one int8 word") of R rows x C values is q[R*C] int8 and s[R*(C/32)] f32, q 32-byte aligned.
  *     Quantisation rule: d = max|x|/127 over the block; word = round-half-away-from-zero(x/d) clamped to +-127, both
  *     divisions IEEE f32; a block of zeros has d = 0 and zero words.
+ *   - The two-word form (lane/mod.rs module docs: "a two-word ~14-bit int8 activation"; lane/arena.rs, array_bytes and
+ *     quant_parts: the words, then the low words, then one scale a block) adds low words lo[R*C] int8 (32-byte
+ *     aligned): with t = x/d (IEEE f32) and q the word above, lo = round-half-away-from-zero(128 (t - q)), so
+ *     x ~ d (q + lo/128); together 128 q + lo is a signed integer of 14 magnitude bits on the block's one scale.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream), allocates nothing,
  *     never synchronizes and never reads device memory back to the host, so every call but the first decode_step can
  *     be captured into a CUDA graph.
@@ -64,8 +68,11 @@ typedef enum {
  *   Q8_F32ACT_F64SUM — f32 activations times dequantized int8 weights, each 32-block's f32 partial sum added into an
  *                      f64 accumulator (qwen_emit, emit_moe_forward: "f32 activation x int8 weight, f64 accumulate");
  *   Q8_INT8ACT       — the activation quantized to one int8 word per value; each 32-block's exact int32 dot is
- *                      scaled by both block scales and summed in f32. */
-typedef enum { Q8_F32ACT_F64SUM = 0, Q8_INT8ACT = 1 } q8_mode;
+ *                      scaled by both block scales and summed in f32;
+ *   Q8_INT8ACT2      — the activation in the two-word form (Q8MatKind::TwoPassInt8 -> QuantFormat::TwoWords, the
+ *                      lane's default); each 32-block's exact integer 128 D(words) + D(low words) is scaled by both
+ *                      block scales and 1/128 and summed in f32. */
+typedef enum { Q8_F32ACT_F64SUM = 0, Q8_INT8ACT = 1, Q8_INT8ACT2 = 2 } q8_mode;
 
 /* A device Q8_0 matrix (see the layout above). */
 typedef struct {
@@ -74,10 +81,12 @@ typedef struct {
     int64_t rows, cols;
 } q8_mat;
 
-/* A device quantized activation (see the layout above). */
+/* A device quantized activation (see the layout above): words q, scales s, and the two-word form's low words lo
+ * (read and written only in Q8_INT8ACT2; NULL otherwise). */
 typedef struct {
     int8_t *q;
     float *s;
+    int8_t *lo;
 } q8_act;
 
 /* ---- workspace ------------------------------------------------------------------------------------------------ */
@@ -93,7 +102,7 @@ Q8_API size_t q8_workspace_bytes(const q8_ws *ws);
 /* ---- a1 / K4: quantisation and the residual add + RMSNorm -------------------------------------------------------- */
 
 /* Quantizes x (device f32, rows x cols, cols % 32 == 0) to out (lane_link.rs, Link::prim: the standalone Quant
- * launch). */
+ * launch); when out->lo is not NULL, to the two-word form. */
 Q8_API int q8_quantize(const float *x, int64_t rows, int64_t cols, const q8_act *out, q8_stream stream);
 
 /* Fused residual add + RMSNorm with an int8 epilogue (forward_shim.rs module docs: "a sum and the RMS norm of it ... as
@@ -101,7 +110,8 @@ Q8_API int q8_quantize(const float *x, int64_t rows, int64_t cols, const q8_act 
  * For each of `rows` rows of d values (device f32):
  *     s = a + b (one f32 add; b may be NULL: s = a)           -> sum_out (may be NULL; may alias a)
  *     y = s / sqrt(mean(s^2) + eps) * w   (the norm in f64, y rounded once to f32)  -> y_out (may be NULL)
- *     yq = quantize(y)                                         -> yq (may be NULL; needs d % 32 == 0)
+ *     yq = quantize(y)                                         -> yq (may be NULL; needs d % 32 == 0; the two-word
+ *                                                                 form when yq->lo is not NULL)
  * w is device f32 [d].  At least one output must be given.  eps >= 0. */
 Q8_API int add_rmsnorm_q8(const float *a, const float *b, const float *w, int64_t rows, int64_t d, float eps, float *sum_out,
                    float *y_out, const q8_act *yq, q8_stream stream);
@@ -110,15 +120,17 @@ Q8_API int add_rmsnorm_q8(const float *a, const float *b, const float *w, int64_
 
 /* y[r][o] = sum_t W[o][t] * x[r][t] for r < rows (lane_link.rs, Link::prim: Gemv{x, w, y, k, n, m}; qwen_emit, Q8Ref).
  * mode Q8_F32ACT_F64SUM reads x (device f32 [rows][W.cols]); mode Q8_INT8ACT reads xq ([rows][W.cols] words plus
- * scales) or, when xq is NULL, quantizes x first into workspace scratch.  y is device f32 [rows][W.rows].  Matrices
+ * scales) and mode Q8_INT8ACT2 xq with its low words, or, when xq is NULL, either quantizes x first into workspace
+ * scratch.  y is device f32 [rows][W.rows].  Matrices
  * whose rows under-fill the GPU are cut along k; the partial sums meet in workspace scratch and the last slice to
  * arrive adds them in slice order (lane_link.rs, Link::prim: gemm_blk_tail; lane/arena.rs: the tp/tc scratch). */
 Q8_API int q8_gemv(const q8_mat *W, q8_mode mode, const float *x, const q8_act *xq, int64_t rows, float *y, q8_ws *ws,
             q8_stream stream);
 
-/* Debug export of the int8 path: the q8_gemv call in Q8_INT8ACT mode (y as above) that also writes
- * dots[r][o][b] = the exact int32 dot of weight block (o, b) with activation block (r, b), from the same device code.
- * dots is device int32 [rows][W.rows][W.cols/32]. */
+/* Debug export of the int8 paths: the q8_gemv call (y as above) that also writes dots[r][o][b] = the exact int32 dot
+ * of weight block (o, b) with activation block (r, b), from the same device code; dots is device int32
+ * [rows][W.rows][W.cols/32].  The mode is Q8_INT8ACT, or Q8_INT8ACT2 when xq->lo is not NULL: dots is then
+ * [2][rows][W.rows][W.cols/32], the words' dots followed by the low words' dots. */
 Q8_API int q8_gemv_blockdots(const q8_mat *W, const q8_act *xq, int64_t rows, int32_t *dots, float *y, q8_ws *ws,
                       q8_stream stream);
 
@@ -161,9 +173,9 @@ Q8_API int moe_route_topk(const q8_mat *router, q8_mode mode, const float *x, co
 
 /* Gate-up with SwiGLU (qwen_emit, MoeWeights: gate/up [E*dff, d] stacked, expert e's rows at e*dff; emit_moe_forward:
  * each expert's SwiGLU at an expert-indexed base): h[r][j][i] = silu(Wg[e*dff+i] . x_r) * (Wu[e*dff+i] . x_r) with
- * e = ids[r][j], silu(z) = z/(1+e^-z).  h: device f32 [rows][k][dff].  In Q8_INT8ACT mode hq (device, words
- * [rows*k*dff] + scales [rows*k*dff/32], or NULL) receives quantize(h) (dff % 32 == 0); in the other mode it is
- * ignored.
+ * e = ids[r][j], silu(z) = z/(1+e^-z).  h: device f32 [rows][k][dff].  In the int8 modes hq (device, words
+ * [rows*k*dff] + scales [rows*k*dff/32], in Q8_INT8ACT2 with low words, or NULL) receives quantize(h)
+ * (dff % 32 == 0); in the f32 mode it is ignored.
  * plan (from moe_route_topk) is required when rows > 1: each expert's weights are then read once for all its rows. */
 Q8_API int moe_gate_up(const q8_mat *gate, const q8_mat *up, int64_t dff, q8_mode mode, const float *x, const q8_act *xq,
                 int64_t rows, int k, const int32_t *ids, const q8_moe_plan *plan, float *h, const q8_act *hq,
@@ -171,9 +183,9 @@ Q8_API int moe_gate_up(const q8_mat *gate, const q8_mat *up, int64_t dff, q8_mod
 
 /* Down-and-combine (qwen_emit, MoeWeights: down [E*d, dff] stacked, expert e's rows at e*d; emit_moe_forward: the
  * weighted combine): y[r] = residual[r] + sum_j gates[r][j] * (Wd[e*d .. e*d+d) . h[r][j]), the sum over j in order.
- * Mode Q8_F32ACT_F64SUM reads h; mode Q8_INT8ACT reads hq, or quantizes h when hq is NULL.  residual may be NULL (and
- * may alias y); y is device f32
- * [rows][d]; expert_out (device f32 [rows][k][d] or NULL) receives each expert's unweighted output. */
+ * Mode Q8_F32ACT_F64SUM reads h; the int8 modes read hq (in Q8_INT8ACT2 with its low words), or quantize h when hq
+ * is NULL.  residual may be NULL (and may alias y); y is device f32 [rows][d]; expert_out (device f32 [rows][k][d] or
+ * NULL) receives each expert's unweighted output. */
 Q8_API int moe_down_combine(const q8_mat *down, int64_t d, q8_mode mode, const float *h, const q8_act *hq, int64_t rows,
                      int k, const int32_t *ids, const float *gates, const q8_moe_plan *plan, const float *residual,
                      float *y, float *expert_out, q8_ws *ws, q8_stream stream);

@@ -19,6 +19,7 @@ lib = ctypes.CDLL(LIB_PATH)
 
 F32ACT_F64SUM = 0
 INT8ACT = 1
+INT8ACT2 = 2  # the two-word activation (high words, low words in 128ths of the block scale)
 QBLOCK = 32
 
 STATUS = {0: "Q8_OK", -1: "Q8_EINVAL", -2: "Q8_EUNSUPPORTED", -3: "Q8_ECUDA", -4: "Q8_ETIMEOUT", -5: "Q8_ENOSPACE"}
@@ -35,7 +36,7 @@ class q8_mat(ctypes.Structure):
 
 
 class q8_act(ctypes.Structure):
-    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p)]
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("lo", ctypes.c_void_p)]
 
 
 class q8_moe_plan(ctypes.Structure):
@@ -120,8 +121,12 @@ def mat(q, s) -> q8_mat:
     return q8_mat(q.data_ptr(), s.data_ptr(), q.shape[0], q.shape[1])
 
 
-def act(q, s) -> q8_act:
-    return q8_act(q.data_ptr(), s.data_ptr())
+def act(q, s, lo=None) -> q8_act:
+    return q8_act(q.data_ptr(), s.data_ptr(), lo.data_ptr() if lo is not None else None)
+
+
+def _actref(q, s, lo=None):
+    return ctypes.byref(act(q, s, lo)) if q is not None else None
 
 
 class Workspace:
@@ -146,36 +151,37 @@ class Workspace:
             pass
 
 
-def q8_quantize(x, q, s, stream=None):
+def q8_quantize(x, q, s, stream=None, lo=None):
+    """One word per value, or with `lo` the two-word form."""
     rows = x.shape[0] if x.dim() > 1 else 1
-    a = q8_act(q.data_ptr(), s.data_ptr())
-    _check(lib.q8_quantize(_ptr(x), rows, x.shape[-1], ctypes.byref(a), _stream(stream)))
+    _check(lib.q8_quantize(_ptr(x), rows, x.shape[-1], _actref(q, s, lo), _stream(stream)))
 
 
-def add_rmsnorm_q8(a, b, w, eps, sum_out=None, y_out=None, yq=None, ys=None, stream=None):
+def add_rmsnorm_q8(a, b, w, eps, sum_out=None, y_out=None, yq=None, ys=None, stream=None, yl=None):
     rows = a.shape[0] if a.dim() > 1 else 1
-    qa = ctypes.byref(q8_act(yq.data_ptr(), ys.data_ptr())) if yq is not None else None
+    qa = _actref(yq, ys, yl)
     _check(lib.add_rmsnorm_q8(_ptr(a), _ptr(b), _ptr(w), rows, a.shape[-1], float(eps), _ptr(sum_out), _ptr(y_out),
                               qa, _stream(stream)))
 
 
-def q8_gemv(q, s, mode, y, x=None, xq=None, xs=None, rows=1, ws=None, stream=None):
+def q8_gemv(q, s, mode, y, x=None, xq=None, xs=None, rows=1, ws=None, stream=None, xl=None):
     W = mat(q, s)
-    qa = ctypes.byref(q8_act(xq.data_ptr(), xs.data_ptr())) if xq is not None else None
+    qa = _actref(xq, xs, xl)
     _check(lib.q8_gemv(ctypes.byref(W), int(mode), _ptr(x), qa, rows, _ptr(y), ws.handle if ws else None,
                        _stream(stream)))
 
 
-def q8_gemv_noalloc(q, s, mode, y, x=None, xq=None, xs=None, rows=1, stream=None):
+def q8_gemv_noalloc(q, s, mode, y, x=None, xq=None, xs=None, rows=1, stream=None, xl=None):
     """q8_gemv without a workspace: scratch comes from the library's fixed per-device array (see q8moe.h)."""
     W = mat(q, s)
-    qa = ctypes.byref(q8_act(xq.data_ptr(), xs.data_ptr())) if xq is not None else None
+    qa = _actref(xq, xs, xl)
     _check(lib.q8_gemv_noalloc(ctypes.byref(W), int(mode), _ptr(x), qa, rows, _ptr(y), _stream(stream)))
 
 
-def q8_gemv_blockdots(q, s, xq, xs, dots, y, rows=1, ws=None, stream=None):
+def q8_gemv_blockdots(q, s, xq, xs, dots, y, rows=1, ws=None, stream=None, xl=None):
+    """With xl (two words) dots is [2, rows, n, nb]: the words' dots, then the low words'."""
     W = mat(q, s)
-    qa = q8_act(xq.data_ptr(), xs.data_ptr())
+    qa = act(xq, xs, xl)
     _check(lib.q8_gemv_blockdots(ctypes.byref(W), ctypes.byref(qa), rows, _ptr(dots), _ptr(y),
                                  ws.handle if ws else None, _stream(stream)))
 
@@ -185,28 +191,28 @@ def plan_struct(counts, offsets, lists, active):
 
 
 def moe_route_topk(rq, rs, mode, k, ids, gates, x=None, xq=None, xs=None, rows=1, logits=None, plan=None, ws=None,
-                   stream=None):
+                   stream=None, xl=None):
     R = mat(rq, rs)
-    qa = ctypes.byref(q8_act(xq.data_ptr(), xs.data_ptr())) if xq is not None else None
+    qa = _actref(xq, xs, xl)
     pl = ctypes.byref(plan) if plan is not None else None
     _check(lib.moe_route_topk(ctypes.byref(R), int(mode), _ptr(x), qa, rows, int(k), _ptr(ids), _ptr(gates),
                               _ptr(logits), pl, ws.handle if ws else None, _stream(stream)))
 
 
 def moe_gate_up(gq, gs, uq, us, dff, mode, k, ids, h, x=None, xq=None, xs=None, hq=None, hs=None, rows=1, plan=None,
-                ws=None, stream=None):
+                ws=None, stream=None, xl=None, hl=None):
     G, U = mat(gq, gs), mat(uq, us)
-    qa = ctypes.byref(q8_act(xq.data_ptr(), xs.data_ptr())) if xq is not None else None
-    ha = ctypes.byref(q8_act(hq.data_ptr(), hs.data_ptr())) if hq is not None else None
+    qa = _actref(xq, xs, xl)
+    ha = _actref(hq, hs, hl)
     pl = ctypes.byref(plan) if plan is not None else None
     _check(lib.moe_gate_up(ctypes.byref(G), ctypes.byref(U), int(dff), int(mode), _ptr(x), qa, rows, int(k),
                            _ptr(ids), pl, _ptr(h), ha, ws.handle if ws else None, _stream(stream)))
 
 
 def moe_down_combine(dq, ds, d, mode, k, ids, gates, y, h=None, hq=None, hs=None, rows=1, plan=None, residual=None,
-                     expert_out=None, ws=None, stream=None):
+                     expert_out=None, ws=None, stream=None, hl=None):
     Dm = mat(dq, ds)
-    ha = ctypes.byref(q8_act(hq.data_ptr(), hs.data_ptr())) if hq is not None else None
+    ha = _actref(hq, hs, hl)
     pl = ctypes.byref(plan) if plan is not None else None
     _check(lib.moe_down_combine(ctypes.byref(Dm), int(d), int(mode), _ptr(h), ha, rows, int(k), _ptr(ids),
                                 _ptr(gates), pl, _ptr(residual), _ptr(y), _ptr(expert_out),

@@ -58,12 +58,17 @@ static int check_mat(const q8_mat* W, const char* name) {
     return Q8_OK;
 }
 
-static int check_act(const q8_act* a, const char* name) {
+// A quantized activation; `two`: the two-word form, whose low words must be given too.
+static int check_act(const q8_act* a, const char* name, bool two = false) {
     if (!a || !a->q || !a->s) return fail(Q8_EINVAL, "%s: null quantized activation", name);
     if (!aligned(a->q, 32)) return fail(Q8_EINVAL, "%s: words not 32-byte aligned", name);
     if (!aligned(a->s, 4)) return fail(Q8_EINVAL, "%s: scales not 4-byte aligned", name);
+    if (two && !a->lo) return fail(Q8_EINVAL, "%s: null low words (the two-word mode)", name);
+    if (a->lo && !aligned(a->lo, 32)) return fail(Q8_EINVAL, "%s: low words not 32-byte aligned", name);
     return Q8_OK;
 }
+
+static bool valid_mode(q8_mode mode) { return mode == Q8_F32ACT_F64SUM || mode == Q8_INT8ACT || mode == Q8_INT8ACT2; }
 
 // The same error reporting for the decode model (model.cu).
 int model_fail(int code, const char* fmt, ...) {
@@ -137,7 +142,7 @@ int q8_quantize(const float* x, int64_t rows, int64_t cols, const q8_act* out, q
     if (cols % 32) return fail(Q8_EUNSUPPORTED, "cols %lld: not whole 32-value blocks", (long long)cols);
     if (int r = check_act(out, "out")) return r;
     if (rows * cols == 0) return Q8_OK;
-    cudaError_t e = launch_quantize(x, rows * cols, out->q, out->s, (cudaStream_t)stream);
+    cudaError_t e = launch_quantize(x, rows * cols, out->q, out->s, (cudaStream_t)stream, out->lo);
     return e == cudaSuccess ? Q8_OK : cuda_fail(e, "q8_quantize");
 }
 
@@ -165,6 +170,7 @@ int add_rmsnorm_q8(const float* a, const float* b, const float* w, int64_t rows,
     c.sum = sum_out;
     c.y = y_out;
     c.yq = yq ? yq->q : nullptr;
+    c.yl = yq ? yq->lo : nullptr;
     c.ys = yq ? yq->s : nullptr;
     cudaError_t e = launch_add_rmsnorm(c, (cudaStream_t)stream);
     return e == cudaSuccess ? Q8_OK : cuda_fail(e, "add_rmsnorm_q8");
@@ -174,15 +180,15 @@ int add_rmsnorm_q8(const float* a, const float* b, const float* w, int64_t rows,
 static int gemv_check(const q8_mat* W, q8_mode mode, const float* x, const q8_act* xq, int64_t rows, float* y,
                       int32_t* dots) {
     if (int r = check_mat(W, "W")) return r;
-    if (mode != Q8_F32ACT_F64SUM && mode != Q8_INT8ACT) return fail(Q8_EINVAL, "mode %d", (int)mode);
+    if (!valid_mode(mode)) return fail(Q8_EINVAL, "mode %d", (int)mode);
     if (rows < 0) return fail(Q8_EINVAL, "rows negative");
     if (rows > 65536) return fail(Q8_EUNSUPPORTED, "rows %lld: more activation rows than the kernel loops over",
                                   (long long)rows);
     if (!y && !dots) return fail(Q8_EINVAL, "y: null");
     if (mode == Q8_F32ACT_F64SUM && !x) return fail(Q8_EINVAL, "x: null (f32 mode reads x)");
-    if (mode == Q8_INT8ACT && !xq && !x) return fail(Q8_EINVAL, "xq and x: both null");
-    if (xq)
-        if (int r = check_act(xq, "xq")) return r;
+    if (mode != Q8_F32ACT_F64SUM && !xq && !x) return fail(Q8_EINVAL, "xq and x: both null");
+    if (xq && mode != Q8_F32ACT_F64SUM)
+        if (int r = check_act(xq, "xq", mode == Q8_INT8ACT2)) return r;
     if (x && !aligned(x, 16)) return fail(Q8_EINVAL, "x: not 16-byte aligned");
     return Q8_OK;
 }
@@ -204,18 +210,22 @@ static int gemv_common(const q8_mat* W, q8_mode mode, const float* x, const q8_a
     c.x = x;
     c.R = rows;
     c.dots = dots;
-    if (mode == Q8_INT8ACT) {
+    if (dots && mode == Q8_INT8ACT2) c.dots_lo = dots + rows * W->rows * (W->cols / 32);
+    if (mode != Q8_F32ACT_F64SUM) {
         if (xq) {
             c.xq = xq->q;
+            c.xl = mode == Q8_INT8ACT2 ? xq->lo : nullptr;
             c.xs = xq->s;
         } else {
             if (!ws) return fail(Q8_EINVAL, "ws: null (x is quantized into workspace scratch)");
             int8_t* q = cv.take<int8_t>((size_t)(rows * W->cols));
             float* s = cv.take<float>((size_t)(rows * W->cols / 32));
+            int8_t* l = mode == Q8_INT8ACT2 ? cv.take<int8_t>((size_t)(rows * W->cols)) : nullptr;
             if (cv.overflow) return fail(Q8_ENOSPACE, "%s: workspace too small for the quantized activation", who);
-            cudaError_t e = launch_quantize(x, rows * W->cols, q, s, st);
+            cudaError_t e = launch_quantize(x, rows * W->cols, q, s, st, l);
             if (e != cudaSuccess) return cuda_fail(e, who);
             c.xq = q;
+            c.xl = l;
             c.xs = s;
         }
     }
@@ -239,7 +249,8 @@ int q8_gemv_blockdots(const q8_mat* W, const q8_act* xq, int64_t rows, int32_t* 
     g_err[0] = 0;
     if (!dots || !y) return fail(Q8_EINVAL, "dots or y: null");
     if (!xq) return fail(Q8_EINVAL, "xq: null");
-    return gemv_common(W, Q8_INT8ACT, nullptr, xq, rows, y, dots, ws, (cudaStream_t)stream, "q8_gemv_blockdots");
+    return gemv_common(W, xq->lo ? Q8_INT8ACT2 : Q8_INT8ACT, nullptr, xq, rows, y, dots, ws, (cudaStream_t)stream,
+                       "q8_gemv_blockdots");
 }
 
 static int check_plan(const q8_moe_plan* plan) {
@@ -264,7 +275,9 @@ int moe_route_topk(const q8_mat* router, q8_mode mode, const float* x, const q8_
         if (int r = check_plan(plan)) return r;
     if (rows == 0) return Q8_OK;
     cudaStream_t st = (cudaStream_t)stream;
-    const bool act = mode == Q8_INT8ACT ? (xq && !check_act(xq, "xq")) : (x && aligned(x, 16));
+    if (!valid_mode(mode)) return fail(Q8_EINVAL, "mode %d", (int)mode);
+    const bool act = mode != Q8_F32ACT_F64SUM ? (xq && !check_act(xq, "xq", mode == Q8_INT8ACT2))
+                                              : (x && aligned(x, 16));
     if (rows == 1 && !plan && act && route_row_supported((int)mode, E, router->cols, k)) {
         // one row: the projection and the top-k in one cluster launch
         RouteRowCall c;
@@ -275,8 +288,9 @@ int moe_route_topk(const q8_mat* router, q8_mode mode, const float* x, const q8_
         c.d = router->cols;
         c.K = k;
         c.x = x;
-        c.xq = mode == Q8_INT8ACT ? xq->q : nullptr;
-        c.xs = mode == Q8_INT8ACT ? xq->s : nullptr;
+        c.xq = mode != Q8_F32ACT_F64SUM ? xq->q : nullptr;
+        c.xl = mode == Q8_INT8ACT2 ? xq->lo : nullptr;
+        c.xs = mode != Q8_F32ACT_F64SUM ? xq->s : nullptr;
         c.logits = logits;
         c.ids = ids;
         c.gates = gates;
@@ -330,16 +344,16 @@ int moe_gate_up(const q8_mat* gate, const q8_mat* up, int64_t dff, q8_mode mode,
     if (gate->rows != up->rows || gate->cols != up->cols) return fail(Q8_EINVAL, "gate and up differ in shape");
     if (dff < 1 || gate->rows % dff) return fail(Q8_EINVAL, "dff %lld does not divide the %lld stacked rows",
                                                 (long long)dff, (long long)gate->rows);
-    if (mode != Q8_F32ACT_F64SUM && mode != Q8_INT8ACT) return fail(Q8_EINVAL, "mode %d", (int)mode);
+    if (!valid_mode(mode)) return fail(Q8_EINVAL, "mode %d", (int)mode);
     if (k < 1 || k > 32) return fail(Q8_EUNSUPPORTED, "k %d: 1 to 32 experts a row", k);
     if (!ids || !h || !ws) return fail(Q8_EINVAL, "ids, h or ws: null");
     if (rows < 0) return fail(Q8_EINVAL, "rows negative");
     if (rows > 1 && !plan) return fail(Q8_EINVAL, "plan: null (a chunk of %lld rows is grouped by expert)", (long long)rows);
     if (mode == Q8_F32ACT_F64SUM && (!x || !aligned(x, 16))) return fail(Q8_EINVAL, "x: null or not 16-byte aligned");
-    if (mode == Q8_INT8ACT) {
-        if (int r = check_act(xq, "xq")) return r;
+    if (mode != Q8_F32ACT_F64SUM) {
+        if (int r = check_act(xq, "xq", mode == Q8_INT8ACT2)) return r;
         if (hq)
-            if (int r = check_act(hq, "hq")) return r;
+            if (int r = check_act(hq, "hq", mode == Q8_INT8ACT2)) return r;
         if (dff % 32) return fail(Q8_EUNSUPPORTED, "dff %lld: the int8 epilogue needs whole 32-row blocks", (long long)dff);
     }
     if (!experts_supported((int)mode, gate->cols))
@@ -361,8 +375,9 @@ int moe_gate_up(const q8_mat* gate, const q8_mat* up, int64_t dff, q8_mode mode,
     c.K = k;
     c.ids = ids;
     c.x = x;
-    c.xq = mode == Q8_INT8ACT ? xq->q : nullptr;
-    c.xs = mode == Q8_INT8ACT ? xq->s : nullptr;
+    c.xq = mode != Q8_F32ACT_F64SUM ? xq->q : nullptr;
+    c.xl = mode == Q8_INT8ACT2 ? xq->lo : nullptr;
+    c.xs = mode != Q8_F32ACT_F64SUM ? xq->s : nullptr;
     c.h = h;
     if (plan) {
         c.plan.counts = plan->counts;
@@ -370,15 +385,16 @@ int moe_gate_up(const q8_mat* gate, const q8_mat* up, int64_t dff, q8_mode mode,
         c.plan.lists = plan->lists;
         c.plan.active = plan->active;
     }
-    if (mode == Q8_INT8ACT && hq && gate_row_supported(c)) {  // one row: the kernel quantizes each 32-row block
+    if (mode != Q8_F32ACT_F64SUM && hq && gate_row_supported(c)) {  // one row: the kernel quantizes each 32-row block
         c.hq_out = hq->q;
+        c.hl_out = mode == Q8_INT8ACT2 ? hq->lo : nullptr;
         c.hs_out = hq->s;
     }
     Carve cv = ws->carve();
     cudaError_t e = launch_gate_up(c, cv, st);
     if (cv.overflow) return fail(Q8_ENOSPACE, "moe_gate_up: workspace too small for the int8 epilogue's counters");
-    if (e == cudaSuccess && mode == Q8_INT8ACT && hq && !c.hq_out)
-        e = launch_quantize(h, rows * k * dff, hq->q, hq->s, st);
+    if (e == cudaSuccess && mode != Q8_F32ACT_F64SUM && hq && !c.hq_out)
+        e = launch_quantize(h, rows * k * dff, hq->q, hq->s, st, mode == Q8_INT8ACT2 ? hq->lo : nullptr);
     return e == cudaSuccess ? Q8_OK : cuda_fail(e, "moe_gate_up");
 }
 
@@ -389,15 +405,15 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
     if (int r = check_mat(down, "down")) return r;
     if (d < 1 || down->rows % d) return fail(Q8_EINVAL, "d %lld does not divide the %lld stacked rows", (long long)d,
                                             (long long)down->rows);
-    if (mode != Q8_F32ACT_F64SUM && mode != Q8_INT8ACT) return fail(Q8_EINVAL, "mode %d", (int)mode);
+    if (!valid_mode(mode)) return fail(Q8_EINVAL, "mode %d", (int)mode);
     if (k < 1 || k > 32) return fail(Q8_EUNSUPPORTED, "k %d: 1 to 32 experts a row", k);
     if (!ids || !gates || !y || !ws) return fail(Q8_EINVAL, "ids, gates, y or ws: null");
     if (rows < 0) return fail(Q8_EINVAL, "rows negative");
     if (rows > 1 && !plan) return fail(Q8_EINVAL, "plan: null (a chunk of %lld rows is grouped by expert)", (long long)rows);
     if (mode == Q8_F32ACT_F64SUM && (!h || !aligned(h, 16))) return fail(Q8_EINVAL, "h: null or not 16-byte aligned");
-    if (mode == Q8_INT8ACT) {
+    if (mode != Q8_F32ACT_F64SUM) {
         if (hq) {
-            if (int r = check_act(hq, "hq")) return r;
+            if (int r = check_act(hq, "hq", mode == Q8_INT8ACT2)) return r;
         } else if (!h || !aligned(h, 16)) {
             return fail(Q8_EINVAL, "hq and h: both null (or h not 16-byte aligned)");
         }
@@ -420,9 +436,10 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
     c.ids = ids;
     c.gates = gates;
     c.x = h;
-    if (mode == Q8_INT8ACT && hq) {
+    if (mode != Q8_F32ACT_F64SUM && hq) {
         c.x = nullptr;
         c.xq = hq->q;
+        c.xl = mode == Q8_INT8ACT2 ? hq->lo : nullptr;
         c.xs = hq->s;
     }
     c.residual = residual;
@@ -435,14 +452,16 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
         c.plan.active = plan->active;
     }
     Carve cv = ws->carve();
-    if (mode == Q8_INT8ACT && !hq && (rows > 1 || plan)) {  // a chunk reads its hidden rows quantized
+    if (mode != Q8_F32ACT_F64SUM && !hq && (rows > 1 || plan)) {  // a chunk reads its hidden rows quantized
         int8_t* q = cv.take<int8_t>((size_t)(rows * k * down->cols));
         float* s = cv.take<float>((size_t)(rows * k * down->cols / 32));
+        int8_t* l = mode == Q8_INT8ACT2 ? cv.take<int8_t>((size_t)(rows * k * down->cols)) : nullptr;
         if (cv.overflow) return fail(Q8_ENOSPACE, "moe_down_combine: workspace too small for the quantized rows");
-        cudaError_t qe = launch_quantize(h, rows * k * down->cols, q, s, st);
+        cudaError_t qe = launch_quantize(h, rows * k * down->cols, q, s, st, l);
         if (qe != cudaSuccess) return cuda_fail(qe, "moe_down_combine");
         c.x = nullptr;
         c.xq = q;
+        c.xl = l;
         c.xs = s;
     }
     size_t need = 0, cnt = 0;
@@ -474,9 +493,10 @@ void gemv_call_scratch(const q8_mat* W, q8_mode mode, const float* x, const q8_a
     c.R = rows;
     size_t b = 0;
     auto region = [&](size_t n) { b = ((b + 255) & ~size_t(255)) + n; };
-    if (mode == Q8_INT8ACT && !xq) {
+    if (mode != Q8_F32ACT_F64SUM && !xq) {  // the quantized activation: words, scales (and low words)
         region((size_t)(rows * W->cols));
         region((size_t)(rows * W->cols / 32) * sizeof(float));
+        if (mode == Q8_INT8ACT2) region((size_t)(rows * W->cols));
     }
     size_t pb = 0, pc = 0;
     gemv_scratch(c, &pb, &pc);

@@ -112,18 +112,25 @@ __device__ __forceinline__ void load_tile(WTile<BPL, RT>& t, const int8_t* __res
         }
 }
 
-// The activation blocks a lane multiplies: f32 values (mode 0) or int8 words and their scales (mode 1).  The pointers
-// may be global or shared memory.
+// The activation blocks a lane multiplies: f32 values (mode 0), int8 words and their scales (mode 1), or high and low
+// words and their scales (mode 2).  The pointers may be global or shared memory.
 template <int MODE, int BPL>
 struct XTile {
     float f[MODE == 0 ? BPL : 1][MODE == 0 ? 32 : 1];
-    uint32_t w[MODE == 1 ? BPL : 1][8];
+    uint32_t w[MODE >= 1 ? BPL : 1][8];
+    uint32_t l[MODE == 2 ? BPL : 1][8];
     float s[BPL];
 };
 
+__device__ __forceinline__ void load_words32(const int8_t* p, uint32_t (&w)[8]) {
+    const uint4 a = reinterpret_cast<const uint4*>(p)[0], b = reinterpret_cast<const uint4*>(p)[1];
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
 template <int MODE, int BPL>
-__device__ __forceinline__ void load_x(XTile<MODE, BPL>& x, const float* xf, const int8_t* xq, const float* xs,
-                                       const int (&bidx)[BPL], const bool (&bval)[BPL]) {
+__device__ __forceinline__ void load_x(XTile<MODE, BPL>& x, const float* xf, const int8_t* xq, const int8_t* xl,
+                                       const float* xs, const int (&bidx)[BPL], const bool (&bval)[BPL]) {
 #pragma unroll
     for (int j = 0; j < BPL; ++j) {
         if (MODE == 0) {
@@ -139,14 +146,15 @@ __device__ __forceinline__ void load_x(XTile<MODE, BPL>& x, const float* xf, con
             x.s[j] = 0.f;
         } else {
             if (bval[j]) {
-                const uint4* p = reinterpret_cast<const uint4*>(xq + bidx[j] * 32);
-                const uint4 a = p[0], b = p[1];
-                x.w[j][0] = a.x; x.w[j][1] = a.y; x.w[j][2] = a.z; x.w[j][3] = a.w;
-                x.w[j][4] = b.x; x.w[j][5] = b.y; x.w[j][6] = b.z; x.w[j][7] = b.w;
+                load_words32(xq + bidx[j] * 32, x.w[j]);
+                if (MODE == 2) load_words32(xl + bidx[j] * 32, x.l[MODE == 2 ? j : 0]);
                 x.s[j] = xs[bidx[j]];
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x.w[j][e] = 0u;
+                for (int e = 0; e < 8; ++e) {
+                    x.w[j][e] = 0u;
+                    x.l[MODE == 2 ? j : 0][e] = 0u;
+                }
                 x.s[j] = 0.f;
             }
         }
@@ -163,9 +171,20 @@ template <>
 struct AccType<1> {
     using T = float;
 };
+template <>
+struct AccType<2> {
+    using T = float;
+};
+
+// The two-word block dot: the exact integer 128 D(high words) + D(low words) (|.| < 2^27), which multiplies the block's
+// scales and 1/128.
+__device__ __forceinline__ int block_dot_i8x2(const uint32_t (&w)[8], const uint32_t (&xh)[8], const uint32_t (&xl)[8]) {
+    return block_dot_i8(w, xh) * 128 + block_dot_i8(w, xl);
+}
 
 // This lane's share of row i of the tile: mode 0 adds each block's f32 partial, scaled, into f64; mode 1 scales each
-// block's exact int32 dot by both block scales and adds in f32.
+// block's exact int32 dot by both block scales and adds in f32; mode 2 does the same with the two-word block dot and
+// the scales times 1/128.
 template <int MODE, int BPL, int RT>
 __device__ __forceinline__ typename AccType<MODE>::T tile_row_dot(const WTile<BPL, RT>& t, int i,
                                                                   const XTile<MODE, BPL>& x) {
@@ -175,79 +194,12 @@ __device__ __forceinline__ typename AccType<MODE>::T tile_row_dot(const WTile<BP
         if (MODE == 0) {
             const float ps = block_dot_f32(t.w[i][j], x.f[j]);
             acc = fma((double)t.s[i][j], (double)ps, (double)acc);
-        } else {
+        } else if (MODE == 1) {
             const int D = block_dot_i8(t.w[i][j], x.w[j]);
             acc = fmaf(t.s[i][j] * x.s[j], (float)D, (float)acc);
-        }
-    }
-    return acc;
-}
-
-// ---- a lane's half-block view of a row held in shared memory -----------------------------------------------------
-// Lane l reads the 16 bytes at columns 16l + 512j (j < KCH) of a row: conflict-free 128-bit shared loads.  Lanes 2m and
-// 2m+1 hold the two halves of block m + 16j, so a block's dot is the sum of the pair's halves (one shuffle).
-template <int MODE, int KCH>
-struct XHalf {
-    uint32_t w[MODE == 1 ? KCH : 1][4];
-    float f[MODE == 0 ? KCH : 1][MODE == 0 ? 16 : 1];
-    float s[KCH];
-};
-
-// Loads this lane's columns of an activation row (global or shared): f32 values, or words and their block scales.
-template <int MODE, int KCH>
-__device__ __forceinline__ void load_xhalf(XHalf<MODE, KCH>& x, const float* xf, const int8_t* xq, const float* xs,
-                                           int k, int lane) {
-#pragma unroll
-    for (int j = 0; j < KCH; ++j) {
-        const int col = 16 * lane + 512 * j;
-        const bool ok = col < k;
-        if (MODE == 1) {
-            const uint4 v = ok ? *reinterpret_cast<const uint4*>(xq + col) : make_uint4(0, 0, 0, 0);
-            x.w[j][0] = v.x; x.w[j][1] = v.y; x.w[j][2] = v.z; x.w[j][3] = v.w;
-            x.s[j] = ok ? xs[col / 32] : 0.f;
         } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 v = ok ? *reinterpret_cast<const float4*>(xf + col + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
-                x.f[j][4 * e] = v.x; x.f[j][4 * e + 1] = v.y; x.f[j][4 * e + 2] = v.z; x.f[j][4 * e + 3] = v.w;
-            }
-            x.s[j] = 0.f;
-        }
-    }
-}
-
-// This lane's share of (row . x) for a Q8_0 row in shared memory (quants q_row[k], scales s_row[k/32]); summed over the
-// warp it is the row's dot (blocks scaled, f64 sums in mode 0, f32 in mode 1).  Every lane must call it.
-template <int MODE, int KCH>
-__device__ __forceinline__ typename AccType<MODE>::T smem_row_dot(const int8_t* q_row, const float* s_row, int k,
-                                                                  const XHalf<MODE, KCH>& x, int lane) {
-    typename AccType<MODE>::T acc = 0;
-#pragma unroll
-    for (int j = 0; j < KCH; ++j) {
-        const int col = 16 * lane + 512 * j;
-        const bool ok = col < k;
-        const uint4 w = ok ? *reinterpret_cast<const uint4*>(q_row + col) : make_uint4(0, 0, 0, 0);
-        const float sc = ok ? s_row[col / 32] : 0.f;
-        if (MODE == 1) {
-            int d = __dp4a((int)w.x, (int)x.w[j][0], 0);
-            d = __dp4a((int)w.y, (int)x.w[j][1], d);
-            d = __dp4a((int)w.z, (int)x.w[j][2], d);
-            d = __dp4a((int)w.w, (int)x.w[j][3], d);
-            d += __shfl_xor_sync(0xffffffffu, d, 1);
-            if (!(lane & 1)) acc = fmaf(sc * x.s[j], (float)d, (float)acc);
-        } else {
-            const uint32_t wv[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
-            float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                p0 = fmaf(i8_to_f32<0>(wv[e]), x.f[j][4 * e + 0], p0);
-                p1 = fmaf(i8_to_f32<1>(wv[e]), x.f[j][4 * e + 1], p1);
-                p0 = fmaf(i8_to_f32<2>(wv[e]), x.f[j][4 * e + 2], p0);
-                p1 = fmaf(i8_to_f32<3>(wv[e]), x.f[j][4 * e + 3], p1);
-            }
-            float ps = p0 + p1;
-            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-            if (!(lane & 1)) acc = fma((double)sc, (double)ps, (double)acc);
+            const int D = block_dot_i8x2(t.w[i][j], x.w[j], x.l[MODE == 2 ? j : 0]);
+            acc = fmaf(t.s[i][j] * x.s[j] * 0.0078125f, (float)D, (float)acc);
         }
     }
     return acc;
@@ -315,6 +267,44 @@ __device__ __forceinline__ void quantize_lanes(const float (&v)[N], int8_t (&q)[
     }
 #pragma unroll
     for (int i = 0; i < N; ++i) q[i] = d[i] == 0.0f ? (int8_t)0 : (int8_t)(int)fminf(fmaxf(roundf(t[i]), -127.0f), 127.0f);
+}
+
+// The two-word form of N independent blocks (lane/mod.rs: the two-word activation): the one-word scale d and high word,
+// and the low word = round-half-away(128 (t - hi)) of the IEEE quotient t = v / d itself (t - hi and the product by
+// 128 are exact), so both words follow the correctly rounded quotient.
+template <int N>
+__device__ __forceinline__ void quantize2_lanes(const float (&v)[N], int8_t (&hi)[N], int8_t (&lo)[N], float (&d)[N]) {
+    float m[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) m[i] = fabsf(v[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < N; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        d[i] = div127(m[i]);
+        if (d[i] == 0.0f) {
+            hi[i] = 0;
+            lo[i] = 0;
+            continue;
+        }
+        const float t = __fdiv_rn(v[i], d[i]);
+        const float r = fminf(fmaxf(roundf(t), -127.0f), 127.0f);
+        const float f = fminf(fmaxf(roundf(__fmul_rn(__fsub_rn(t, r), 128.0f)), -127.0f), 127.0f);
+        hi[i] = (int8_t)(int)r;
+        lo[i] = (int8_t)(int)f;
+    }
+}
+
+__device__ __forceinline__ int8_t quantize2_lane(float v, float& d_out, int8_t& lo_out) {
+    const float vv[1] = {v};
+    int8_t h[1], l[1];
+    float d[1];
+    quantize2_lanes<1>(vv, h, l, d);
+    d_out = d[0];
+    lo_out = l[0];
+    return h[0];
 }
 
 __device__ __forceinline__ int8_t quantize_lane(float v, float& d_out) {

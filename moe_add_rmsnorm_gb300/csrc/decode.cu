@@ -58,6 +58,7 @@ struct AttnParams {
     float scale;
     float* out;
     int8_t* outq;
+    int8_t* outl;  // with outq: the two-word form's low words
     float* outs;
     float* part;   // [kv][G][ncl_max][ATT_HD + 2]: each cluster's fold
     int* cnt;      // [kv * G]
@@ -165,8 +166,13 @@ __device__ void fold_cluster(const AttnParams& p, int g, int chunk, int G, int t
         p.out[oi] = o;
         if (p.outq) {  // the slot's four warps hold the head's four 32-value blocks
             float dsc;
-            const int8_t qv = quantize_lane(o, dsc);
-            p.outq[oi] = qv;
+            if (p.outl) {
+                int8_t lv;
+                p.outq[oi] = quantize2_lane(o, dsc, lv);
+                p.outl[oi] = lv;
+            } else {
+                p.outq[oi] = quantize_lane(o, dsc);
+            }
             if (lane == 0) p.outs[oi / 32] = dsc;
         }
         if (d == 0) p.cnt[g * G + hh] = 0;
@@ -767,7 +773,7 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
 // per (row, head), lane l the dims l, l + 32, l + 64, l + 96.
 __global__ void __launch_bounds__(256) chunk_attn_fold_kernel(const float* part, const int32_t* posr, int R, int heads,
                                                               int ctx, int ngroups, float* out, int8_t* outq,
-                                                              float* outs) {
+                                                              int8_t* outl, float* outs) {
     const int wg = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (wg >= R * heads) return;
     const int r = wg / heads;
@@ -795,8 +801,13 @@ __global__ void __launch_bounds__(256) chunk_attn_fold_kernel(const float* part,
         out[oi] = o;
         if (outq) {
             float dsc;
-            const int8_t qv = quantize_lane(o, dsc);
-            outq[oi] = qv;
+            if (outl) {
+                int8_t lv;
+                outq[oi] = quantize2_lane(o, dsc, lv);
+                outl[oi] = lv;
+            } else {
+                outq[oi] = quantize_lane(o, dsc);
+            }
             if (lane == 0) outs[oi / 32] = dsc;
         }
     }
@@ -836,6 +847,7 @@ cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
     p.scale = (float)(1.0 / sqrt((double)c.hd));
     p.out = c.out;
     p.outq = c.outq;
+    p.outl = c.outl;
     p.outs = c.outs;
     p.nch_max = attn_chunks(c.ctx);
     p.ncl_max = p.nch_max / ATT_CLUSTER;
@@ -923,7 +935,7 @@ cudaError_t launch_chunk_attention(const ChunkAttnCall& c, Carve& ws, cudaStream
     if (e != cudaSuccess) return e;
     const int64_t warps = c.rows * c.heads;
     chunk_attn_fold_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(part, c.posr, (int)c.rows, c.heads, c.ctx, ng,
-                                                                       c.out, c.outq, c.outs);
+                                                                       c.out, c.outq, c.outl, c.outs);
     return cudaGetLastError();
 }
 

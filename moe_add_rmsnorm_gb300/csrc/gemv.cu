@@ -32,6 +32,7 @@ struct GemvParams {
     int k, nb;
     const float* x;
     const int8_t* xq;
+    const int8_t* xl;  // mode 2: the low words
     const float* xs;
     int R;
     int RG;          // activation row groups: warp w takes rows w % RG, w % RG + RG, ... (RG <= warps)
@@ -39,6 +40,7 @@ struct GemvParams {
     void* partial;   // [R][S][ntot] (f64 in mode 0, f32 in mode 1)
     int* counters;   // [R][items]
     int32_t* dots;
+    int32_t* dots_lo;  // mode 2: the low words' block dots
     L2Prefetch pf;
 };
 
@@ -90,15 +92,19 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gemv_kernel(const GemvParams p)
         if (it != first) load_tile<BPL, RT>(t, p.q[sg], p.s[sg], row0, nvalid, p.k, p.nb, bidx, bval);
         for (int r = rg; r < p.R; r += RG) {
             XTile<MODE, BPL> x;
-            load_x<MODE, BPL>(x, p.x + (int64_t)r * p.k, p.xq + (int64_t)r * p.k, p.xs + (int64_t)r * p.nb, bidx, bval);
+            load_x<MODE, BPL>(x, p.x + (int64_t)r * p.k, p.xq + (int64_t)r * p.k, p.xl + (int64_t)r * p.k,
+                              p.xs + (int64_t)r * p.nb, bidx, bval);
             T acc[RT];
 #pragma unroll
             for (int i = 0; i < RT; ++i) {
                 if (DOTS) {
 #pragma unroll
                     for (int j = 0; j < BPL; ++j)
-                        if (i < nvalid && bval[j])
-                            p.dots[((int64_t)r * p.ntot + row0 + i) * p.nb + bidx[j]] = block_dot_i8(t.w[i][j], x.w[j]);
+                        if (i < nvalid && bval[j]) {
+                            const int64_t at = ((int64_t)r * p.ntot + row0 + i) * p.nb + bidx[j];
+                            p.dots[at] = block_dot_i8(t.w[i][j], x.w[j]);
+                            if (MODE == 2) p.dots_lo[at] = block_dot_i8(t.w[i][j], x.l[MODE == 2 ? j : 0]);
+                        }
                 }
                 acc[i] = group_sum<LPR>(tile_row_dot<MODE, BPL, RT>(t, i, x));
             }
@@ -239,6 +245,7 @@ __global__ void __launch_bounds__(TMA_THREADS, 1) gemv_tma_kernel(const TmaParam
     griddep_launch();
     const float* xfp = p.x;
     const int8_t* xqp = p.xq;
+    const int8_t* xlp = p.xl;
     const float* xsp = p.xs;
     if (norm) {
         // RMSNorm prologue, the same order in every CTA: squares summed as f32 pairs, each y rounded once
@@ -289,7 +296,7 @@ __global__ void __launch_bounds__(TMA_THREADS, 1) gemv_tma_kernel(const TmaParam
                 const int i = threadIdx.x + TMA_CONSUMERS * 32 * j;
                 if (i < k) xbuf[i] = y[j];
             }
-        } else {
+        } else if (MODE == 1) {
             int8_t qv[NP];
             float dsc[NP];
             quantize_lanes<NP>(y, qv, dsc);  // round j: warp w holds block w + 8 j
@@ -301,23 +308,43 @@ __global__ void __launch_bounds__(TMA_THREADS, 1) gemv_tma_kernel(const TmaParam
                     if (lane == 0) xsbuf[i / 32] = dsc[j];
                 }
             }
+        } else {
+            int8_t qv[NP], lv[NP];
+            float dsc[NP];
+            quantize2_lanes<NP>(y, qv, lv, dsc);  // the high words, then the low words k bytes on
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int i = threadIdx.x + TMA_CONSUMERS * 32 * j;
+                if (i < k) {
+                    reinterpret_cast<int8_t*>(xbuf)[i] = qv[j];
+                    reinterpret_cast<int8_t*>(xbuf)[k + i] = lv[j];
+                    if (lane == 0) xsbuf[i / 32] = dsc[j];
+                }
+            }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(TMA_CONSUMERS * 32));
         xfp = xbuf;
         xqp = reinterpret_cast<const int8_t*>(xbuf);
+        xlp = reinterpret_cast<const int8_t*>(xbuf) + k;
         xsp = xsbuf;
     }
     // this lane's activation values: columns 16*lane + 512*j
-    uint32_t xw[MODE == 1 ? KCH : 1][4];
+    uint32_t xw[MODE >= 1 ? KCH : 1][4];
+    uint32_t xwl[MODE == 2 ? KCH : 1][4];
     float xsc[KCH];
     float xf[MODE == 0 ? KCH : 1][MODE == 0 ? 16 : 1];
 #pragma unroll
     for (int j = 0; j < KCH; ++j) {
         const int col = 16 * lane + 512 * j;
         const bool ok = col < k;
-        if (MODE == 1) {
+        if (MODE >= 1) {
             const uint4 v = ok ? *reinterpret_cast<const uint4*>(xqp + col) : make_uint4(0, 0, 0, 0);
             xw[j][0] = v.x; xw[j][1] = v.y; xw[j][2] = v.z; xw[j][3] = v.w;
+            if (MODE == 2) {
+                const uint4 u = ok ? *reinterpret_cast<const uint4*>(xlp + col) : make_uint4(0, 0, 0, 0);
+                const int jj = MODE == 2 ? j : 0;
+                xwl[jj][0] = u.x; xwl[jj][1] = u.y; xwl[jj][2] = u.z; xwl[jj][3] = u.w;
+            }
             xsc[j] = ok ? xsp[col / 32] : 0.f;
         } else {
 #pragma unroll
@@ -354,6 +381,19 @@ __global__ void __launch_bounds__(TMA_THREADS, 1) gemv_tma_kernel(const TmaParam
                     d = __dp4a((int)w.w, (int)xw[j][3], d);
                     d += __shfl_xor_sync(0xffffffffu, d, 1);  // the block's exact dot: both halves
                     if (!(lane & 1)) acc = fmaf(sc * xsc[j], (float)d, (float)acc);
+                } else if (MODE == 2) {
+                    const int jj = MODE == 2 ? j : 0;
+                    int d = __dp4a((int)w.x, (int)xw[j][0], 0);
+                    d = __dp4a((int)w.y, (int)xw[j][1], d);
+                    d = __dp4a((int)w.z, (int)xw[j][2], d);
+                    d = __dp4a((int)w.w, (int)xw[j][3], d);
+                    int e = __dp4a((int)w.x, (int)xwl[jj][0], 0);
+                    e = __dp4a((int)w.y, (int)xwl[jj][1], e);
+                    e = __dp4a((int)w.z, (int)xwl[jj][2], e);
+                    e = __dp4a((int)w.w, (int)xwl[jj][3], e);
+                    d = d * 128 + e;
+                    d += __shfl_xor_sync(0xffffffffu, d, 1);  // the block's exact two-word dot: both halves
+                    if (!(lane & 1)) acc = fmaf(sc * xsc[j] * 0.0078125f, (float)d, (float)acc);
                 } else {
                     const uint32_t wv[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u,
                                             w.w ^ 0x80808080u};
@@ -408,7 +448,7 @@ int items_of(const GemvCall& c, const Plan& pl) {
 
 Plan plan_for(const GemvCall& c) {
     const int nb = (int)(c.k / 32);
-    const int bpl_max = (c.mode == 0) ? 3 : 4;
+    const int bpl_max = (c.mode == 0) ? 3 : 4;  // the int8 modes hold more blocks a lane
     // lanes per row and blocks per lane: the fewest slices, then every lane busy
     Plan best{32, 1, 1, 1 << 30};
     double best_util = -1.0;
@@ -461,8 +501,8 @@ cudaError_t dispatch_lpr(const Plan& pl, const GemvParams& p, int64_t grid, cuda
     if (pl.bpl == 2 && pl.rt == 4) return run<MODE, LPR, 2, 4, DOTS>(p, grid, st, pdl);
     if (pl.bpl == 3 && pl.rt == 1) return run<MODE, LPR, 3, 1, DOTS>(p, grid, st, pdl);
     if (pl.bpl == 3 && pl.rt == 2) return run<MODE, LPR, 3, 2, DOTS>(p, grid, st, pdl);
-    if (MODE == 1 && pl.bpl == 4 && pl.rt == 1) return run<MODE, LPR, 4, 1, DOTS>(p, grid, st, pdl);
-    if (MODE == 1 && pl.bpl == 4 && pl.rt == 2) return run<MODE, LPR, 4, 2, DOTS>(p, grid, st, pdl);
+    if (MODE >= 1 && pl.bpl == 4 && pl.rt == 1) return run<MODE, LPR, 4, 1, DOTS>(p, grid, st, pdl);
+    if (MODE >= 1 && pl.bpl == 4 && pl.rt == 2) return run<MODE, LPR, 4, 2, DOTS>(p, grid, st, pdl);
     return cudaErrorInvalidConfiguration;
 }
 
@@ -512,6 +552,7 @@ cudaError_t launch_gemv_tma(const GemvCall& c, int* err, cudaStream_t st) {
     p.nb = (int)(c.k / 32);
     p.x = c.x;
     p.xq = c.xq;
+    p.xl = c.xl;
     p.xs = c.xs;
     p.R = 1;
     p.S = 1;
@@ -544,11 +585,18 @@ cudaError_t launch_gemv_tma(const GemvCall& c, int* err, cudaStream_t st) {
     if (ns < 2) return cudaErrorInvalidConfiguration;
     tp.ns = ns;
     tp.err = err;
-    // the normed activation after the ring: k values (f32) or words, k/32 scales, the reduction's pairs
+    // the normed activation after the ring: k values (f32) or words (two words: 2k bytes), k/32 scales, the
+    // reduction's pairs
     const size_t nbytes = c.norm_a ? (size_t)c.k * 4 + (size_t)(c.k / 32) * 4 + (TMA_CONSUMERS + 1) * sizeof(F2) : 0;
     const size_t smem = TMA_HDR + (size_t)ns * tp.stage + nbytes;
     const int grid = tiles < sms ? tiles : sms;
     const int kch = (int)((c.k + 511) / 512);
+    if (c.mode == 2) {
+        if (kch <= 1) return run_tma<2, 1>(tp, grid, smem, st, c.pdl);
+        if (kch <= 2) return run_tma<2, 2>(tp, grid, smem, st, c.pdl);
+        if (kch <= 4) return run_tma<2, 4>(tp, grid, smem, st, c.pdl);
+        return run_tma<2, 8>(tp, grid, smem, st, c.pdl);
+    }
     if (c.mode == 1) {
         if (kch <= 1) return run_tma<1, 1>(tp, grid, smem, st, c.pdl);
         if (kch <= 2) return run_tma<1, 2>(tp, grid, smem, st, c.pdl);
@@ -591,10 +639,12 @@ cudaError_t launch_gemv(const GemvCall& c, Carve& ws, cudaStream_t st) {
     p.nb = nb;
     p.x = c.x;
     p.xq = c.xq;
+    p.xl = c.xl;
     p.xs = c.xs;
     p.R = (int)c.R;
     p.S = pl.S;
     p.dots = c.dots;
+    p.dots_lo = c.dots_lo;
     p.pf = c.pf;
     if (pl.S > 1) {
         size_t bytes = 0, cnt = 0;
@@ -607,6 +657,7 @@ cudaError_t launch_gemv(const GemvCall& c, Carve& ws, cudaStream_t st) {
     p.RG = pl.RG;
     const int64_t grid = (int64_t)it * pl.S * pl.RG;
     if (c.mode == 0) return dispatch<0, false>(pl, p, grid, st, c.pdl);
+    if (c.mode == 2) return c.dots ? dispatch<2, true>(pl, p, grid, st, c.pdl) : dispatch<2, false>(pl, p, grid, st, c.pdl);
     if (c.dots) return dispatch<1, true>(pl, p, grid, st, c.pdl);
     return dispatch<1, false>(pl, p, grid, st, c.pdl);
 }

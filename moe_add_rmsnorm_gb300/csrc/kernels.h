@@ -61,10 +61,12 @@ struct GemvCall {
     int nseg = 1;
     GemvSeg seg[3];
     const float* x = nullptr;            // [R][k] (mode 0)
-    const int8_t* xq = nullptr;          // [R][k] (mode 1)
+    const int8_t* xq = nullptr;          // [R][k] (modes 1 and 2: the words; in mode 2 the high words)
+    const int8_t* xl = nullptr;          // [R][k] (mode 2: the low words)
     const float* xs = nullptr;           // [R][k/32]
     int64_t R = 1;
-    int32_t* dots = nullptr;             // mode 1 debug export [R][n][k/32] (single segment)
+    int32_t* dots = nullptr;             // modes 1, 2 debug export [R][n][k/32] (single segment; mode 2: high words)
+    int32_t* dots_lo = nullptr;          // mode 2 debug export of the low words' dots
     int* err = nullptr;                  // device error word for a pipeline wait that gave up
     L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;                         // launch with programmatic dependent launch allowed
@@ -96,13 +98,15 @@ struct NormCall {
     float* sum = nullptr;
     float* y = nullptr;
     int8_t* yq = nullptr;
+    int8_t* yl = nullptr;                // with yq: the two-word form's low words
     float* ys = nullptr;
     int* err = nullptr;                  // device error word for a gathered row out of range
     L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };
 cudaError_t launch_add_rmsnorm(const NormCall& c, cudaStream_t st);
-cudaError_t launch_quantize(const float* x, int64_t n, int8_t* q, float* s, cudaStream_t st);
+// One word per value, or with l the two-word form (high words to q, low words to l).
+cudaError_t launch_quantize(const float* x, int64_t n, int8_t* q, float* s, cudaStream_t st, int8_t* l = nullptr);
 
 // ---- mixture ----------------------------------------------------------------------------------------------------
 struct PlanPtrs {
@@ -152,10 +156,12 @@ struct ExpertCall {
     PlanPtrs plan;                       // used when plan.active != nullptr, else choice j is group j (R == 1)
     const float* x = nullptr;            // gate-up: x [R][k]; down: h [R*K][k] (f32; for one row in mode 1 the kernel
                                          // quantizes it as it stages it)
-    const int8_t* xq = nullptr;          // mode 1: gate-up xq [R][k]; down hq [R*K][k]
+    const int8_t* xq = nullptr;          // modes 1, 2: gate-up xq [R][k]; down hq [R*K][k]
+    const int8_t* xl = nullptr;          // mode 2: the low words beside xq
     const float* xs = nullptr;
     float* h = nullptr;                  // gate-up out [R*K][dff]
-    int8_t* hq_out = nullptr;            // gate-up, one row, int8 mode: h quantized per 32 rows (dff % 32 == 0)
+    int8_t* hq_out = nullptr;            // gate-up, one row, int8 modes: h quantized per 32 rows (dff % 32 == 0)
+    int8_t* hl_out = nullptr;            //   (mode 2: its low words)
     float* hs_out = nullptr;             //   and its scales [K][dff/32]
     const float* residual = nullptr;     // down
     float* y = nullptr;                  // down out [R][d]
@@ -180,7 +186,8 @@ struct RouteRowCall {
     int64_t E = 0, d = 0;
     int K = 0;
     const float* x = nullptr;   // f32 mode
-    const int8_t* xq = nullptr; // int8 mode
+    const int8_t* xq = nullptr; // int8 modes
+    const int8_t* xl = nullptr; // mode 2: the low words
     const float* xs = nullptr;
     float* logits = nullptr;    // optional [E]
     int32_t* ids = nullptr;
@@ -192,6 +199,7 @@ struct RouteRowCall {
     float eps = 0.f;
     float* x_out = nullptr;
     int8_t* xq_out = nullptr;
+    int8_t* xl_out = nullptr;   // mode 2
     float* xs_out = nullptr;
     L2Prefetch pf;
     int pdl = 0;
@@ -227,6 +235,7 @@ struct AttnCall {
     int heads = 0, kv = 0, hd = 0, ctx = 0;
     float* out = nullptr;           // [heads][hd]
     int8_t* outq = nullptr;         // optional quantized output
+    int8_t* outl = nullptr;         // with outq: the two-word form's low words
     float* outs = nullptr;
     int* err = nullptr;             // bit 2 set for a position outside [0, ctx)
     L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
@@ -271,6 +280,7 @@ struct ChunkAttnCall {
     int heads = 0, kv = 0, hd = 0, ctx = 0;
     float* out = nullptr;           // [rows][heads][hd]
     int8_t* outq = nullptr;         // optional quantized output
+    int8_t* outl = nullptr;         // with outq: the two-word form's low words
     float* outs = nullptr;
 };
 void chunk_attention_scratch(int64_t rows, int heads, int ctx, size_t* bytes);

@@ -39,6 +39,7 @@ struct q8_model {
     float *h = nullptr, *x = nullptr, *q = nullptr, *k = nullptr, *v = nullptr, *att = nullptr, *logits = nullptr;
     float *cos_t = nullptr, *sin_t = nullptr, *hbuf = nullptr, *gates = nullptr, *rlog = nullptr;
     int8_t *xq = nullptr, *attq = nullptr, *hq = nullptr;
+    int8_t *xl = nullptr, *attl = nullptr, *hl = nullptr;  // the two-word mode's low words
     float *xs = nullptr, *atts = nullptr, *hs = nullptr;
     int32_t* ids = nullptr;
     int* err = nullptr;
@@ -106,6 +107,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
         g.seg[2] = GemvSeg{m->wv[l].q, m->wv[l].s, KV * HD, m->v, nullptr};
         g.x = m->x;
         g.xq = m->xq;
+        g.xl = m->xl;
         g.xs = m->xs;
         g.pdl = pdl;
         g.err = m->err;
@@ -135,6 +137,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             if (mode == 0) n.y = m->x;
             else {
                 n.yq = m->xq;
+                n.yl = m->xl;
                 n.ys = m->xs;
             }
             n.err = m->err;
@@ -167,8 +170,9 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             a.hd = (int)HD;
             a.ctx = (int)d.ctx;
             a.out = m->att;
-            if (mode == 1) {
+            if (mode >= 1) {
                 a.outq = m->attq;
+                a.outl = m->attl;
                 a.outs = m->atts;
             }
             a.pdl = pdl;
@@ -182,6 +186,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             g.seg[0] = GemvSeg{m->wo[l].q, m->wo[l].s, D, m->h, m->h};  // h = h + o
             g.x = m->att;
             g.xq = m->attq;
+            g.xl = m->attl;
             g.xs = m->atts;
             g.pdl = pdl;
             g.err = m->err;
@@ -199,6 +204,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             if (mode == 0) n2.y = m->x;
             else {
                 n2.yq = m->xq;
+                n2.yl = m->xl;
                 n2.ys = m->xs;
             }
             n2.pdl = pdl;
@@ -215,6 +221,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             r.K = (int)d.k;
             r.x = m->x;
             r.xq = m->xq;
+            r.xl = m->xl;
             r.xs = m->xs;
             r.ids = m->ids;
             r.gates = m->gates;
@@ -224,6 +231,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
                 r.eps = d.eps;
                 r.x_out = mode == 0 ? m->x : nullptr;
                 r.xq_out = m->xq;
+                r.xl_out = m->xl;
                 r.xs_out = m->xs;
             }
             r.pdl = pdl;
@@ -236,6 +244,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             g.seg[0] = GemvSeg{m->router[l].q, m->router[l].s, d.experts, m->rlog, nullptr};
             g.x = m->x;
             g.xq = m->xq;
+            g.xl = m->xl;
             g.xs = m->xs;
             g.pdl = pdl;
             g.err = m->err;
@@ -267,10 +276,12 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             c.ids = m->ids;
             c.x = m->x;
             c.xq = m->xq;
+            c.xl = m->xl;
             c.xs = m->xs;
             c.h = m->hbuf;
-            if (mode == 1 && gate_row_supported(c)) {  // the hidden rows quantized once, by the kernel that forms them
+            if (mode >= 1 && gate_row_supported(c)) {  // the hidden rows quantized once, by the kernel that forms them
                 c.hq_out = m->hq;
+                c.hl_out = m->hl;
                 c.hs_out = m->hs;
                 hq_by_gate = true;
             }
@@ -294,6 +305,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             c.x = m->hbuf;  // f32 hidden rows
             if (hq_by_gate) {  // and their int8 form, written by gate-up
                 c.xq = m->hq;
+                c.xl = m->hl;
                 c.xs = m->hs;
             }
             c.residual = m->h;  // h = h + mixture
@@ -314,6 +326,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
         g.seg[0] = GemvSeg{d.lm_head.q, d.lm_head.s, d.vocab, m->logits, nullptr};
         g.x = m->x;
         g.xq = m->xq;
+        g.xl = m->xl;
         g.xs = m->xs;
         g.pdl = pdl;
         g.err = m->err;
@@ -331,6 +344,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             if (mode == 0) nf.y = m->x;
             else {
                 nf.yq = m->xq;
+                nf.yl = m->xl;
                 nf.ys = m->xs;
             }
             nf.pdl = pdl;
@@ -382,7 +396,8 @@ int q8_model_create(const q8_model_desc* desc, q8_model** out) {
     *out = nullptr;
     if (!desc) return model_fail(Q8_EINVAL, "desc: null");
     const q8_model_desc& d = *desc;
-    if (d.mode != Q8_F32ACT_F64SUM && d.mode != Q8_INT8ACT) return model_fail(Q8_EINVAL, "mode %d", (int)d.mode);
+    if (d.mode != Q8_F32ACT_F64SUM && d.mode != Q8_INT8ACT && d.mode != Q8_INT8ACT2)
+        return model_fail(Q8_EINVAL, "mode %d", (int)d.mode);
     if (d.layers < 1 || d.d < 32 || d.heads < 1 || d.kv_heads < 1 || d.vocab < 1 || d.ctx < 1 || d.experts < 1 ||
         d.dff < 32)
         return model_fail(Q8_EINVAL, "a size below its minimum (layers, d, heads, kv_heads, vocab, ctx, experts, dff)");
@@ -461,6 +476,9 @@ int q8_model_create(const q8_model_desc* desc, q8_model** out) {
     add(QD / 32 * 4);    // atts
     add(KF);             // hq
     add(KF / 32 * 4);    // hs
+    add(D);              // xl
+    add(QD);             // attl
+    add(KF);             // hl
     add(d.k * 4);        // ids
     add(256);            // err
     need += 4096;
@@ -489,6 +507,9 @@ int q8_model_create(const q8_model_desc* desc, q8_model** out) {
     m->atts = carve_arena<float>(at, QD / 32);
     m->hq = carve_arena<int8_t>(at, KF);
     m->hs = carve_arena<float>(at, KF / 32);
+    m->xl = carve_arena<int8_t>(at, D);
+    m->attl = carve_arena<int8_t>(at, QD);
+    m->hl = carve_arena<int8_t>(at, KF);
     m->ids = carve_arena<int32_t>(at, d.k);
     m->err = carve_arena<int>(at, 64);
     if (d.mode == Q8_F32ACT_F64SUM) {
@@ -498,6 +519,11 @@ int q8_model_create(const q8_model_desc* desc, q8_model** out) {
         m->atts = nullptr;
         m->hq = nullptr;
         m->hs = nullptr;
+    }
+    if (d.mode != Q8_INT8ACT2) {
+        m->xl = nullptr;
+        m->attl = nullptr;
+        m->hl = nullptr;
     }
     // workspace: the largest single launch's scratch (launches of a step run one after another)
     m->ws_bytes = size_t(64) << 20;
@@ -593,14 +619,16 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
     Carve cb = workspace_carve(ws);
     float* h = cb.take<float>((size_t)(R * D));
     float* x = mode == 0 ? cb.take<float>((size_t)(R * D)) : nullptr;
-    int8_t* xq = mode == 1 ? cb.take<int8_t>((size_t)(R * D)) : nullptr;
-    float* xs = mode == 1 ? cb.take<float>((size_t)(R * D / 32)) : nullptr;
+    int8_t* xq = mode >= 1 ? cb.take<int8_t>((size_t)(R * D)) : nullptr;
+    int8_t* xl = mode == 2 ? cb.take<int8_t>((size_t)(R * D)) : nullptr;
+    float* xs = mode >= 1 ? cb.take<float>((size_t)(R * D / 32)) : nullptr;
     float* q = cb.take<float>((size_t)(R * H * HD));
     float* k = cb.take<float>((size_t)(R * KV * HD));
     float* v = cb.take<float>((size_t)(R * KV * HD));
     float* att = cb.take<float>((size_t)(R * H * HD));
-    int8_t* attq = mode == 1 ? cb.take<int8_t>((size_t)(R * H * HD)) : nullptr;
-    float* atts = mode == 1 ? cb.take<float>((size_t)(R * H * HD / 32)) : nullptr;
+    int8_t* attq = mode >= 1 ? cb.take<int8_t>((size_t)(R * H * HD)) : nullptr;
+    int8_t* attl = mode == 2 ? cb.take<int8_t>((size_t)(R * H * HD)) : nullptr;
+    float* atts = mode >= 1 ? cb.take<float>((size_t)(R * H * HD / 32)) : nullptr;
     float* rlog = cb.take<float>((size_t)(R * E));
     int32_t* ids = cb.take<int32_t>((size_t)(R * K));
     float* gates = cb.take<float>((size_t)(R * K));
@@ -610,8 +638,9 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
     plan.lists = cb.take<int32_t>((size_t)(R * K));
     plan.active = cb.take<int32_t>((size_t)E + 1);
     float* hm = cb.take<float>((size_t)(R * K * F));
-    int8_t* hmq = mode == 1 ? cb.take<int8_t>((size_t)(R * K * F)) : nullptr;
-    float* hms = mode == 1 ? cb.take<float>((size_t)(R * K * F / 32)) : nullptr;
+    int8_t* hmq = mode >= 1 ? cb.take<int8_t>((size_t)(R * K * F)) : nullptr;
+    int8_t* hml = mode == 2 ? cb.take<int8_t>((size_t)(R * K * F)) : nullptr;
+    float* hms = mode >= 1 ? cb.take<float>((size_t)(R * K * F / 32)) : nullptr;
     int32_t* posr = cb.take<int32_t>((size_t)R);
     int* done = cb.take_counters(1);
     if (cb.overflow) return model_fail(Q8_ENOSPACE, "prefill_chunk: workspace too small for %lld rows", (long long)R);
@@ -638,6 +667,7 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
         if (mode == 0) n.y = x;
         else {
             n.yq = xq;
+            n.yl = xl;
             n.ys = xs;
         }
         n.err = m->err;
@@ -658,6 +688,7 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
             g.seg[2] = GemvSeg{m->wv[l].q, m->wv[l].s, KV * HD, v, nullptr};
             g.x = x;
             g.xq = xq;
+            g.xl = xl;
             g.xs = xs;
             g.err = m->err;
             Carve cv = cb;
@@ -683,6 +714,7 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
             a.ctx = (int)d.ctx;
             a.out = att;
             a.outq = attq;
+            a.outl = attl;
             a.outs = atts;
             Carve cv = cb;
             Q8_TRY_WS(launch_chunk_attention(a, cv, st), cv);
@@ -695,6 +727,7 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
             g.seg[0] = GemvSeg{m->wo[l].q, m->wo[l].s, D, h, h};  // h = h + o
             g.x = att;
             g.xq = attq;
+            g.xl = attl;
             g.xs = atts;
             g.err = m->err;
             Carve cv = cb;
@@ -709,6 +742,7 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
             g.seg[0] = GemvSeg{m->router[l].q, m->router[l].s, E, rlog, nullptr};
             g.x = x;
             g.xq = xq;
+            g.xl = xl;
             g.xs = xs;
             g.err = m->err;
             Carve cv = cb;
@@ -739,13 +773,14 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
             c.ids = ids;
             c.x = x;
             c.xq = xq;
+            c.xl = xl;
             c.xs = xs;
             c.h = hm;
             c.plan = plan;
             c.err = m->err;
             Carve cv = cb;
             Q8_TRY_WS(launch_gate_up(c, cv, st), cv);
-            if (mode == 1) Q8_TRY(launch_quantize(hm, R * K * F, hmq, hms, st));
+            if (mode >= 1) Q8_TRY(launch_quantize(hm, R * K * F, hmq, hms, st, hml));
         }
         {
             ExpertCall c;
@@ -759,8 +794,9 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
             c.K = (int)K;
             c.ids = ids;
             c.gates = gates;
-            c.x = mode == 1 ? nullptr : hm;
+            c.x = mode >= 1 ? nullptr : hm;
             c.xq = hmq;
+            c.xl = hml;
             c.xs = hms;
             c.plan = plan;
             c.residual = h;  // h = h + mixture
@@ -782,6 +818,7 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
         if (mode == 0) nf.y = m->x;
         else {
             nf.yq = m->xq;
+            nf.yl = m->xl;
             nf.ys = m->xs;
         }
         Q8_TRY(launch_add_rmsnorm(nf, st));
@@ -791,6 +828,7 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
         g.seg[0] = GemvSeg{d.lm_head.q, d.lm_head.s, d.vocab, m->logits, nullptr};
         g.x = m->x;
         g.xq = m->xq;
+        g.xl = m->xl;
         g.xs = m->xs;
         g.err = m->err;
         Carve cv = cb;

@@ -255,6 +255,7 @@ struct ExpertParams {
     const int32_t* active;
     const float* x;         // gate-up: [R][k]; down: h [R*K][k] f32
     const int8_t* xq;       // gate-up: [R][k]; down: hq [R*K][k]
+    const int8_t* xl;       // mode 2: the low words beside xq
     const float* xs;
     float* h;               // gate-up out [R*K][out_rows]
     const float* residual;  // down
@@ -263,7 +264,7 @@ struct ExpertParams {
     void* partial;          // down over a chunk: [R*K][out_rows] (f64 in mode 0, f32 in mode 1)
     int nrs;                // items per group (row tiles of out_rows)
     int mma_lo, mma_hi;     // groups of mma_lo..mma_hi choices are left to the tensor-core kernel (0: none)
-    int xstage;             // gate-up, int8 mode: bytes of the chunk's activation rows staged in shared memory (0: none)
+    int xstage;             // gate-up, int8 modes: bytes of the chunk's activation rows staged in shared memory (0: none)
     L2Prefetch pf;
 };
 
@@ -309,15 +310,20 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gate_up_kernel(const ExpertPara
     // next row of its group reads shared memory rather than waiting on L2
     extern __shared__ __align__(16) unsigned char gsm[];
     const int8_t* xqb = p.xq;
+    const int8_t* xlb = p.xl;
     const float* xsb = p.xs;
-    if (MODE == 1 && p.xstage) {
+    if (MODE >= 1 && p.xstage) {
         const int64_t nq = (int64_t)p.R * p.k;  // a multiple of 32
         for (int64_t i = threadIdx.x; i < nq / 16; i += blockDim.x)
             reinterpret_cast<uint4*>(gsm)[i] = __ldcg(reinterpret_cast<const uint4*>(p.xq) + i);
-        float* sxs = reinterpret_cast<float*>(gsm + nq);
+        if (MODE == 2)  // the low words after the high words
+            for (int64_t i = threadIdx.x; i < nq / 16; i += blockDim.x)
+                reinterpret_cast<uint4*>(gsm + nq)[i] = __ldcg(reinterpret_cast<const uint4*>(p.xl) + i);
+        float* sxs = reinterpret_cast<float*>(gsm + nq * (MODE == 2 ? 2 : 1));
         for (int64_t i = threadIdx.x; i < (int64_t)p.R * p.nb; i += blockDim.x) sxs[i] = __ldcg(p.xs + i);
         __syncthreads();
         xqb = reinterpret_cast<const int8_t*>(gsm);
+        xlb = reinterpret_cast<const int8_t*>(gsm + nq);
         xsb = sxs;
     }
     const int items = n_groups(p) * p.nrs;
@@ -339,8 +345,8 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) gate_up_kernel(const ExpertPara
             const int c = choice_of(p, g, ci);
             const int xrow = c / p.K;
             if (xrow != loaded) {
-                load_x<MODE, BPL>(x, p.x + (int64_t)xrow * p.k, xqb + (int64_t)xrow * p.k, xsb + (int64_t)xrow * p.nb,
-                                  bidx, bval);
+                load_x<MODE, BPL>(x, p.x + (int64_t)xrow * p.k, xqb + (int64_t)xrow * p.k, xlb + (int64_t)xrow * p.k,
+                                  xsb + (int64_t)xrow * p.nb, bidx, bval);
                 loaded = xrow;
             }
 #pragma unroll
@@ -381,22 +387,31 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) down_one_kernel(const ExpertPar
     griddep_wait();
     griddep_launch();
     float* hf = reinterpret_cast<float*>(dsm);                              // [K][kk] f32 staging
-    int8_t* hq = reinterpret_cast<int8_t*>(dsm + (size_t)K * kk * 4);       // [K][kk] words (int8 mode)
-    float* hs = reinterpret_cast<float*>(dsm + (size_t)K * kk * 5);         // [K][kk/32] scales
+    int8_t* hq = reinterpret_cast<int8_t*>(dsm + (size_t)K * kk * 4);       // [K][kk] words (int8 modes)
+    int8_t* hl = reinterpret_cast<int8_t*>(dsm + (size_t)K * kk * 5);       // [K][kk] low words (mode 2)
+    float* hs = reinterpret_cast<float*>(dsm + (size_t)K * kk * (MODE == 2 ? 6 : 5));  // [K][kk/32] scales
     if (MODE == 0 || p.x) {
         for (int i = threadIdx.x; i < K * kk / 4; i += Q8_THREADS)
             reinterpret_cast<float4*>(hf)[i] = __ldcg(reinterpret_cast<const float4*>(p.x) + i);
         __syncthreads();
-        if (MODE == 1)
+        if (MODE >= 1)
             for (int b = wid; b < K * kk / 32; b += Q8_WARPS) {
                 float dsc;
-                const int8_t v = quantize_lane(hf[b * 32 + lane], dsc);
-                hq[b * 32 + lane] = v;
+                if (MODE == 2) {
+                    int8_t lv;
+                    hq[b * 32 + lane] = quantize2_lane(hf[b * 32 + lane], dsc, lv);
+                    hl[b * 32 + lane] = lv;
+                } else {
+                    hq[b * 32 + lane] = quantize_lane(hf[b * 32 + lane], dsc);
+                }
                 if (lane == 0) hs[b] = dsc;
             }
     } else {
         for (int i = threadIdx.x; i < K * kk / 16; i += Q8_THREADS)
             reinterpret_cast<uint4*>(hq)[i] = __ldcg(reinterpret_cast<const uint4*>(p.xq) + i);
+        if (MODE == 2)
+            for (int i = threadIdx.x; i < K * kk / 16; i += Q8_THREADS)
+                reinterpret_cast<uint4*>(hl)[i] = __ldcg(reinterpret_cast<const uint4*>(p.xl) + i);
         for (int i = threadIdx.x; i < K * kk / 32; i += Q8_THREADS) hs[i] = __ldcg(p.xs + i);
     }
     __syncthreads();
@@ -420,7 +435,8 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) down_one_kernel(const ExpertPar
                 const int j = m * NG + gi;
                 const int jj = j < K ? j : 0;
                 XTile<MODE, BPL> x;
-                load_x<MODE, BPL>(x, hf + (int64_t)jj * kk, hq + (int64_t)jj * kk, hs + (int64_t)jj * p.nb, bidx, bval);
+                load_x<MODE, BPL>(x, hf + (int64_t)jj * kk, hq + (int64_t)jj * kk, hl + (int64_t)jj * kk,
+                                  hs + (int64_t)jj * p.nb, bidx, bval);
                 const T mine = group_sum<LPR>(tile_row_dot<MODE, BPL, 1>(t[u], 0, x));
                 // lane 0 adds this pass's experts in choice order
                 for (int g = 0; g < NG; ++g) {
@@ -477,7 +493,8 @@ __global__ void __launch_bounds__(Q8_THREADS, 1) down_group_kernel(const ExpertP
         for (int ci = 0; ci < g.nc; ++ci) {
             const int c = choice_of(p, g, ci);
             XTile<MODE, BPL> x;
-            load_x<MODE, BPL>(x, p.x + (int64_t)c * p.k, p.xq + (int64_t)c * p.k, p.xs + (int64_t)c * p.nb, bidx, bval);
+            load_x<MODE, BPL>(x, p.x + (int64_t)c * p.k, p.xq + (int64_t)c * p.k, p.xl + (int64_t)c * p.k,
+                              p.xs + (int64_t)c * p.nb, bidx, bval);
 #pragma unroll
             for (int i = 0; i < RT; ++i) {
                 const T e = group_sum<LPR>(tile_row_dot<MODE, BPL, RT>(t, i, x));
@@ -560,6 +577,7 @@ ExpertParams make_params(const ExpertCall& c, const EPlan& pl) {
     p.active = c.plan.active;
     p.x = c.x;
     p.xq = c.xq;
+    p.xl = c.xl;
     p.xs = c.xs;
     p.h = c.h;
     p.residual = c.residual;
@@ -577,7 +595,7 @@ int max_groups(const ExpertCall& c) {
 }
 
 size_t down_one_smem(const ExpertCall& c) {
-    return (size_t)c.K * c.k * 4 + (c.mode == 1 ? (size_t)c.K * c.k + (size_t)c.K * c.k / 32 * 4 : 0);
+    return (size_t)c.K * c.k * 4 + (c.mode >= 1 ? (size_t)c.K * c.k * c.mode + (size_t)c.K * c.k / 32 * 4 : 0);
 }
 
 #define Q8_EXPERT_ONE(KERNEL, MODE, L, B, R)                                                               \
@@ -594,9 +612,9 @@ size_t down_one_smem(const ExpertCall& c) {
 #define Q8_EXPERT_LPR(KERNEL, MODE, L)                                                                     \
     Q8_EXPERT_ONE(KERNEL, MODE, L, 1, 1) Q8_EXPERT_ONE(KERNEL, MODE, L, 1, 2) Q8_EXPERT_ONE(KERNEL, MODE, L, 1, 4) \
     Q8_EXPERT_ONE(KERNEL, MODE, L, 2, 1) Q8_EXPERT_ONE(KERNEL, MODE, L, 2, 2) Q8_EXPERT_ONE(KERNEL, MODE, L, 3, 1) \
-    if (MODE == 1) {                                                                                       \
-        Q8_EXPERT_ONE(KERNEL, 1, L, 2, 4) Q8_EXPERT_ONE(KERNEL, 1, L, 3, 2) Q8_EXPERT_ONE(KERNEL, 1, L, 4, 1) \
-        Q8_EXPERT_ONE(KERNEL, 1, L, 4, 2)                                                                  \
+    if (MODE >= 1) {                                                                                       \
+        Q8_EXPERT_ONE(KERNEL, MODE, L, 2, 4) Q8_EXPERT_ONE(KERNEL, MODE, L, 3, 2)                          \
+        Q8_EXPERT_ONE(KERNEL, MODE, L, 4, 1) Q8_EXPERT_ONE(KERNEL, MODE, L, 4, 2)                          \
     }
 #define Q8_EXPERT_DISPATCH(KERNEL, MODE)                                                                   \
     do {                                                                                                   \
@@ -634,10 +652,10 @@ cudaError_t dispatch_down_one(const EPlan& pl, const ExpertParams& p, int64_t gr
     if (pl.lpr == 8 && pl.bpl == 1) return run_down_one<MODE, 8, 1>(p, grid, smem, st, pdl);
     if (pl.lpr == 8 && pl.bpl == 2) return run_down_one<MODE, 8, 2>(p, grid, smem, st, pdl);
     if (pl.lpr == 8 && pl.bpl == 3) return run_down_one<MODE, 8, 3>(p, grid, smem, st, pdl);
-    if (MODE == 1) {
-        if (pl.lpr == 32 && pl.bpl == 4) return run_down_one<1, 32, 4>(p, grid, smem, st, pdl);
-        if (pl.lpr == 16 && pl.bpl == 4) return run_down_one<1, 16, 4>(p, grid, smem, st, pdl);
-        if (pl.lpr == 8 && pl.bpl == 4) return run_down_one<1, 8, 4>(p, grid, smem, st, pdl);
+    if (MODE >= 1) {
+        if (pl.lpr == 32 && pl.bpl == 4) return run_down_one<MODE, 32, 4>(p, grid, smem, st, pdl);
+        if (pl.lpr == 16 && pl.bpl == 4) return run_down_one<MODE, 16, 4>(p, grid, smem, st, pdl);
+        if (pl.lpr == 8 && pl.bpl == 4) return run_down_one<MODE, 8, 4>(p, grid, smem, st, pdl);
     }
     return cudaErrorInvalidConfiguration;
 }
@@ -687,9 +705,12 @@ cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
         p.mma_hi = moe_mma_max_rows();
     }
     const int64_t warps = (int64_t)max_groups(c) * p.nrs;
-    const int64_t xbytes = c.R * c.k + c.R * (c.k / 32) * 4;
-    if (c.mode == 1 && c.R > 1 && xbytes <= 96 * 1024 && (uintptr_t)c.xq % 16 == 0) p.xstage = (int)xbytes;
-    cudaError_t e = c.mode == 0 ? run_gate_up<0>(c, pl, p, warps, st) : run_gate_up<1>(c, pl, p, warps, st);
+    const int64_t xbytes = c.R * c.k * c.mode + c.R * (c.k / 32) * 4;
+    if (c.mode >= 1 && c.R > 1 && xbytes <= 96 * 1024 && (uintptr_t)c.xq % 16 == 0 &&
+        (c.mode == 1 || (uintptr_t)c.xl % 16 == 0))
+        p.xstage = (int)xbytes;
+    cudaError_t e = c.mode == 0 ? run_gate_up<0>(c, pl, p, warps, st)
+                  : c.mode == 1 ? run_gate_up<1>(c, pl, p, warps, st) : run_gate_up<2>(c, pl, p, warps, st);
     if (e == cudaSuccess && mma) e = launch_moe_mma(c, c.h, max_groups(c), ws, st);  // the groups of >= 16 choices
     return e;
 }
@@ -705,7 +726,8 @@ cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st)
         const int64_t grid = c.out_rows;
         const size_t smem = down_one_smem(c);
         return c.mode == 0 ? dispatch_down_one<0>(pl, p, grid, smem, st, c.pdl)
-                           : dispatch_down_one<1>(pl, p, grid, smem, st, c.pdl);
+             : c.mode == 1 ? dispatch_down_one<1>(pl, p, grid, smem, st, c.pdl)
+                           : dispatch_down_one<2>(pl, p, grid, smem, st, c.pdl);
     }
     // a chunk (or one row through a plan): grouped product into scratch, then the ordered combine
     const EPlan pl = eplan(c.mode, nb, c.mode == 0 ? 4 : 8);
@@ -718,14 +740,15 @@ cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st)
         p.mma_hi = moe_mma_max_rows();
     }
     const int64_t warps = (int64_t)max_groups(c) * p.nrs;
-    cudaError_t e = c.mode == 0 ? run_down_group<0>(c, pl, p, warps, st) : run_down_group<1>(c, pl, p, warps, st);
+    cudaError_t e = c.mode == 0 ? run_down_group<0>(c, pl, p, warps, st)
+                  : c.mode == 1 ? run_down_group<1>(c, pl, p, warps, st) : run_down_group<2>(c, pl, p, warps, st);
     if (e == cudaSuccess && mma) e = launch_moe_mma(c, reinterpret_cast<float*>(p.partial), max_groups(c), ws, st);
     if (e != cudaSuccess) return e;
     const int64_t n = c.R * c.out_rows;
     int cg = (int)((n + 255) / 256);
     if (cg > device_info().sms * 4) cg = device_info().sms * 4;
     return c.mode == 0 ? launch(combine_kernel<0>, dim3(cg), dim3(256), 0, st, c.pdl, p)
-                       : launch(combine_kernel<1>, dim3(cg), dim3(256), 0, st, c.pdl, p);
+                       : launch(combine_kernel<1>, dim3(cg), dim3(256), 0, st, c.pdl, p);  // f32 sums in modes 1, 2
 }
 
 }  // namespace q8

@@ -43,6 +43,7 @@ struct RouteRowParams {
     int E, d, nb, K;
     const float* x;
     const int8_t* xq;
+    const int8_t* xl;
     const float* xs;
     float* logits;
     int32_t* ids;
@@ -54,6 +55,7 @@ struct RouteRowParams {
     float eps;
     float* x_out;
     int8_t* xq_out;
+    int8_t* xl_out;
     float* xs_out;
     L2Prefetch pf;
 };
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(RR_THREADS) route_row_kernel(const RouteRowPar
     griddep_launch();
     const float* xf = p.x;
     const int8_t* xq = p.xq;
+    const int8_t* xl = p.xl;
     const float* xsc = p.xs;
     if (norm) {
         // RMSNorm of the residual row, every CTA of the cluster in the same order (so all hold the same x): the sum
@@ -150,17 +153,20 @@ __global__ void __launch_bounds__(RR_THREADS) route_row_kernel(const RouteRowPar
                 }
             }
         } else {
-            int8_t qv[NP];
+            int8_t qv[NP], lv[NP];
             float dsc[NP];
-            quantize_lanes<NP>(y, qv, dsc);  // round j: warp w holds block w + 8 j
+            if (MODE == 2) quantize2_lanes<NP>(y, qv, lv, dsc);  // round j: warp w holds block w + 8 j
+            else quantize_lanes<NP>(y, qv, dsc);
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
                 const int i = threadIdx.x + RR_THREADS * j;
                 if (i < p.d) {
                     reinterpret_cast<int8_t*>(xbuf)[i] = qv[j];
+                    if (MODE == 2) reinterpret_cast<int8_t*>(xbuf)[p.d + i] = lv[j];  // the low words d bytes on
                     if (lane == 0) xsbuf[i / 32] = dsc[j];
                     if (j % RR_CL == rank) {  // CTA r writes rounds j = r, r + 8, ...
                         p.xq_out[i] = qv[j];
+                        if (MODE == 2) p.xl_out[i] = lv[j];
                         if (lane == 0) p.xs_out[i / 32] = dsc[j];
                     }
                 }
@@ -169,10 +175,11 @@ __global__ void __launch_bounds__(RR_THREADS) route_row_kernel(const RouteRowPar
         __syncthreads();
         xf = xbuf;
         xq = reinterpret_cast<const int8_t*>(xbuf);
+        xl = reinterpret_cast<const int8_t*>(xbuf) + p.d;
         xsc = xsbuf;
     }
     XTile<MODE, BPL> x;
-    load_x<MODE, BPL>(x, xf, xq, xsc, bidx, bval);
+    load_x<MODE, BPL>(x, xf, xq, xl, xsc, bidx, bval);
 #pragma unroll
     for (int u = 0; u < RR_RW; ++u) {
         const int lr = wid + RR_WARPS * u;
@@ -276,10 +283,12 @@ struct GateRowParams {
     const float* us;
     int E, dff, d, nb, K;
     const int32_t* ids;
-    const int8_t* xq;  // int8 mode: the normed activation [d] and its scales
+    const int8_t* xq;  // int8 modes: the normed activation [d] (mode 2: high words), its low words, its scales
+    const int8_t* xl;
     const float* xs;
     float* h;          // [K][dff]
-    int8_t* hq;        // optional: h quantized per 32 rows [K][dff] and its scales [K][dff/32] (dff % 32 == 0)
+    int8_t* hq;        // optional: h quantized per 32 rows [K][dff] (mode 2: with low words hl) and its scales
+    int8_t* hl;        // [K][dff/32] (dff % 32 == 0)
     float* hs;
     int* qcnt;         // [K*dff/32] arrivals per 32-row block (left zero)
     L2Prefetch pf;
@@ -289,7 +298,7 @@ struct GateRowParams {
 // matrices; warp w takes items w*IPW .. w*IPW + IPW - 1 (consecutive rows, so each warp reads contiguous weights) and
 // issues all of their loads before it multiplies any, so a whole launch's weights are in flight at once.  The expert
 // ids and the activation are read after the wait.
-template <int BPL, int IPW>
+template <int MODE, int BPL, int IPW>
 __global__ void __launch_bounds__(GR_WPC * 32, 1) gate_row_kernel(const GateRowParams p) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int warp = blockIdx.x * GR_WPC + wid;
@@ -305,8 +314,8 @@ __global__ void __launch_bounds__(GR_WPC * 32, 1) gate_row_kernel(const GateRowP
     issue_l2_prefetch(p.pf);
     griddep_wait();  // the expert ids (and, when the router launch norms it, the activation) come from the previous launch
     griddep_launch();
-    XTile<1, BPL> x;
-    load_x<1, BPL>(x, nullptr, p.xq, p.xs, bidx, bval);
+    XTile<MODE, BPL> x;
+    load_x<MODE, BPL>(x, nullptr, p.xq, p.xl, p.xs, bidx, bval);
     for (int it0 = warp * IPW; it0 < n; it0 += W * IPW) {
         WTile<BPL, 1> tg[IPW], tu[IPW];
         int eid[IPW];  // every item's expert id read before any weight address depends on one
@@ -324,8 +333,8 @@ __global__ void __launch_bounds__(GR_WPC * 32, 1) gate_row_kernel(const GateRowP
         }
 #pragma unroll
         for (int u = 0; u < IPW; ++u) {
-            const float gv = group_sum<32>(tile_row_dot<1, BPL, 1>(tg[u], 0, x));
-            const float uv = group_sum<32>(tile_row_dot<1, BPL, 1>(tu[u], 0, x));
+            const float gv = group_sum<32>(tile_row_dot<MODE, BPL, 1>(tg[u], 0, x));
+            const float uv = group_sum<32>(tile_row_dot<MODE, BPL, 1>(tu[u], 0, x));
             if (lane == 0 && it0 + u < n) p.h[it0 + u] = silu_f32(gv) * uv;
         }
         if (p.hq) {
@@ -342,8 +351,14 @@ __global__ void __launch_bounds__(GR_WPC * 32, 1) gate_row_kernel(const GateRowP
                 if (old + (hi - lo + 1) == 32) {  // warp-uniform
                     __syncwarp();
                     float dsc;
-                    const int8_t qv = quantize_lane(__ldcg(p.h + (int64_t)b * 32 + lane), dsc);
-                    p.hq[(int64_t)b * 32 + lane] = qv;
+                    const float hv = __ldcg(p.h + (int64_t)b * 32 + lane);
+                    if (MODE == 2) {
+                        int8_t lv;
+                        p.hq[(int64_t)b * 32 + lane] = quantize2_lane(hv, dsc, lv);
+                        p.hl[(int64_t)b * 32 + lane] = lv;
+                    } else {
+                        p.hq[(int64_t)b * 32 + lane] = quantize_lane(hv, dsc);
+                    }
                     if (lane == 0) {
                         p.hs[b] = dsc;
                         p.qcnt[b] = 0;
@@ -354,13 +369,22 @@ __global__ void __launch_bounds__(GR_WPC * 32, 1) gate_row_kernel(const GateRowP
     }
 }
 
-template <int BPL, int IPW>
+template <int MODE, int BPL, int IPW>
 cudaError_t run_gate_row(const GateRowParams& p, cudaStream_t st, int pdl) {
     const int n = p.K * p.dff;
     int grid = (n + GR_WPC * IPW - 1) / (GR_WPC * IPW);
     const int cap = device_info().sms;
     if (grid > cap) grid = cap;
-    return launch(gate_row_kernel<BPL, IPW>, dim3(grid), dim3(GR_WPC * 32), 0, st, pdl, p);
+    return launch(gate_row_kernel<MODE, BPL, IPW>, dim3(grid), dim3(GR_WPC * 32), 0, st, pdl, p);
+}
+
+template <int MODE>
+cudaError_t dispatch_gate_row(const GateRowParams& p, int bpl, int ipw, cudaStream_t st, int pdl) {
+    if (bpl == 1) return ipw == 1 ? run_gate_row<MODE, 1, 1>(p, st, pdl) : ipw == 2 ? run_gate_row<MODE, 1, 2>(p, st, pdl)
+                                                                             : run_gate_row<MODE, 1, 3>(p, st, pdl);
+    if (bpl == 2) return ipw == 1 ? run_gate_row<MODE, 2, 1>(p, st, pdl) : ipw == 2 ? run_gate_row<MODE, 2, 2>(p, st, pdl)
+                                                                             : run_gate_row<MODE, 2, 3>(p, st, pdl);
+    return run_gate_row<MODE, 4, 1>(p, st, pdl);
 }
 
 // ==== down-and-combine ==============================================================================================
@@ -376,7 +400,8 @@ struct DownRowParams {
     const int32_t* ids;
     const float* gates;
     const float* h;    // the K hidden rows [K][k], f32
-    const int8_t* hq;  // int8 mode: their words [K][k] and scales [K][nb]; when null the CTA quantizes h itself
+    const int8_t* hq;  // int8 modes: their words [K][k] (mode 2: high words, with the low words hl) and scales [K][nb];
+    const int8_t* hl;  // when null the CTA quantizes h itself
     const float* hs;
     const float* residual;
     float* y;
@@ -423,6 +448,7 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
     griddep_wait();  // the hidden rows come from the previous launch
     griddep_launch();
     const int8_t* hq = p.hq;
+    const int8_t* hl = p.hl;
     const float* hs = p.hs;
     if (MODE == 0) {
         for (int i = threadIdx.x; i < p.K * p.k / 4; i += blockDim.x)
@@ -432,7 +458,8 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
         // the CTA quantizes the f32 hidden rows into shared memory: warp w takes blocks w, w + W, ..., up to
         // DR_QB of them with every load in flight before the first is quantized
         int8_t* sq = reinterpret_cast<int8_t*>(hsm);
-        float* ss = hsm + P * 8;  // after the P * 32 words
+        int8_t* sl = sq + P * 32;                         // mode 2: the low words after the high words
+        float* ss = hsm + P * 8 * (MODE == 2 ? 2 : 1);    // then the scales
         const int W = blockDim.x >> 5;
         for (int b0 = wid; b0 < P; b0 += DR_QB * W) {
             float v[DR_QB];
@@ -441,41 +468,47 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
                 const int b = b0 + u * W;
                 v[u] = b < P ? __ldcg(p.h + (int64_t)b * 32 + lane) : 0.f;
             }
-            int8_t qv[DR_QB];
+            int8_t qv[DR_QB], lv[DR_QB];
             float dsc[DR_QB];
-            quantize_lanes<DR_QB>(v, qv, dsc);  // the blocks' warp reductions interleaved
+            if (MODE == 2) quantize2_lanes<DR_QB>(v, qv, lv, dsc);  // the blocks' warp reductions interleaved
+            else quantize_lanes<DR_QB>(v, qv, dsc);
 #pragma unroll
             for (int u = 0; u < DR_QB; ++u) {
                 const int b = b0 + u * W;
                 if (b < P) {
                     sq[b * 32 + lane] = qv[u];
+                    if (MODE == 2) sl[b * 32 + lane] = lv[u];
                     if (lane == 0) ss[b] = dsc[u];
                 }
             }
         }
         __syncthreads();
         hq = sq;
+        hl = sl;
         hs = ss;
     }
     typename AccType<MODE>::T acc = 0;
 #pragma unroll
     for (int i = 0; i < PPL; ++i) {
         const bool in = orow && lane + 32 * i < P;
-        if (MODE == 1) {
-            uint32_t xw[8];
+        if (MODE >= 1) {
+            uint32_t xw[8], xl[8];
             float xs = 0.f;
             if (in) {  // global (written by the previous launch) or this CTA's shared memory
-                const uint4 a = reinterpret_cast<const uint4*>(hq + xo[i])[0];
-                const uint4 b = reinterpret_cast<const uint4*>(hq + xo[i])[1];
-                xw[0] = a.x; xw[1] = a.y; xw[2] = a.z; xw[3] = a.w;
-                xw[4] = b.x; xw[5] = b.y; xw[6] = b.z; xw[7] = b.w;
+                load_words32(hq + xo[i], xw);
+                if (MODE == 2) load_words32(hl + xo[i], xl);
                 xs = hs[xo[i] / 32];
             } else {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) xw[c] = 0u;
+                for (int c = 0; c < 8; ++c) xw[c] = xl[c] = 0u;
             }
-            const int D = block_dot_i8(w[i], xw);
-            acc = fmaf(g[i] * (sw[i] * xs), (float)D, (float)acc);
+            if (MODE == 2) {
+                const int D = block_dot_i8x2(w[i], xw, xl);
+                acc = fmaf(g[i] * (sw[i] * xs * 0.0078125f), (float)D, (float)acc);
+            } else {
+                const int D = block_dot_i8(w[i], xw);
+                acc = fmaf(g[i] * (sw[i] * xs), (float)D, (float)acc);
+            }
         } else {
             float xf[32];
             const float4* src = reinterpret_cast<const float4*>(hsm + xo[i]);
@@ -502,7 +535,8 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
 template <int MODE, int PPL>
 cudaError_t run_down_row(const DownRowParams& p, int wpc, cudaStream_t st, int pdl) {
     auto kern = down_row_kernel<MODE, PPL>;
-    const size_t smem = MODE == 0 ? (size_t)p.K * p.k * sizeof(float) : p.hq ? 0 : (size_t)p.K * p.k * 5 / 4 + 16;
+    const size_t smem = MODE == 0 ? (size_t)p.K * p.k * sizeof(float)
+                        : p.hq ? 0 : (size_t)p.K * p.k * (MODE == 2 ? 2 : 1) + (size_t)p.K * p.k / 32 * 4 + 16;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -541,34 +575,40 @@ bool route_row_supported(int mode, int64_t E, int64_t d, int K) {
 cudaError_t launch_route_row(const RouteRowCall& c, cudaStream_t st) {
     if (!route_row_supported(c.mode, c.E, c.d, c.K)) return cudaErrorInvalidConfiguration;
     if (c.norm_a && (c.d % RR_THREADS || c.d > RR_THREADS * RR_NPER || !c.norm_w ||
-                     (c.mode == 0 ? !c.x_out : (!c.xq_out || !c.xs_out))))
+                     (c.mode == 0 ? !c.x_out : (!c.xq_out || !c.xs_out || (c.mode == 2 && !c.xl_out)))))
         return cudaErrorInvalidValue;
-    RouteRowParams p = {c.q, c.s, (int)c.E, (int)c.d, (int)(c.d / 32), c.K, c.x, c.xq, c.xs, c.logits, c.ids, c.gates,
-                        c.norm_a, c.norm_w, c.eps, c.x_out, c.xq_out, c.xs_out, c.pf};
+    RouteRowParams p = {c.q, c.s, (int)c.E, (int)c.d, (int)(c.d / 32), c.K, c.x, c.xq, c.xl, c.xs, c.logits, c.ids,
+                        c.gates, c.norm_a, c.norm_w, c.eps, c.x_out, c.xq_out, c.xl_out, c.xs_out, c.pf};
     const int bpl = route_bpl(c.mode, c.d);
     if (c.mode == 0) {
         if (bpl == 1) return run_route_row<0, 1>(p, st, c.pdl);
         if (bpl == 2) return run_route_row<0, 2>(p, st, c.pdl);
-    } else {
+    } else if (c.mode == 1) {
         if (bpl == 1) return run_route_row<1, 1>(p, st, c.pdl);
         if (bpl == 2) return run_route_row<1, 2>(p, st, c.pdl);
         if (bpl == 4) return run_route_row<1, 4>(p, st, c.pdl);
+    } else {
+        if (bpl == 1) return run_route_row<2, 1>(p, st, c.pdl);
+        if (bpl == 2) return run_route_row<2, 2>(p, st, c.pdl);
+        if (bpl == 4) return run_route_row<2, 4>(p, st, c.pdl);
     }
     return cudaErrorInvalidConfiguration;
 }
 
 bool gate_row_supported(const ExpertCall& c) {
-    return c.mode == 1 && c.R == 1 && !c.plan.active && c.xq && c.xs && c.k % 32 == 0 && c.k / 32 <= 128 &&
+    return c.mode >= 1 && c.R == 1 && !c.plan.active && c.xq && c.xs && (c.mode == 1 || c.xl) && c.k % 32 == 0 &&
+           c.k / 32 <= 128 &&
            c.K >= 1 && c.out_rows >= 1 && c.E * c.out_rows < (int64_t(1) << 31);
 }
 
 cudaError_t launch_gate_row(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     if (!gate_row_supported(c)) return cudaErrorInvalidConfiguration;
     GateRowParams p = {c.q0, c.s0, c.q1, c.s1, (int)c.E, (int)c.out_rows, (int)c.k, (int)(c.k / 32), c.K, c.ids,
-                       c.xq, c.xs, c.h, nullptr, nullptr, nullptr, c.pf};
+                       c.xq, c.xl, c.xs, c.h, nullptr, nullptr, nullptr, nullptr, c.pf};
     if (c.hq_out) {
-        if (c.out_rows % 32) return cudaErrorInvalidValue;
+        if (c.out_rows % 32 || (c.mode == 2 && !c.hl_out)) return cudaErrorInvalidValue;
         p.hq = c.hq_out;
+        p.hl = c.hl_out;
         p.hs = c.hs_out;
         p.qcnt = ws.take_counters((size_t)(c.K * c.out_rows / 32));
         if (ws.overflow) return cudaErrorMemoryAllocation;
@@ -581,16 +621,12 @@ cudaError_t launch_gate_row(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     int ipw = (int)((n + slots - 1) / slots);
     const int ipw_max = bpl == 4 ? 1 : 3;
     if (ipw > ipw_max) ipw = ipw_max;
-    if (bpl == 1) return ipw == 1 ? run_gate_row<1, 1>(p, st, c.pdl) : ipw == 2 ? run_gate_row<1, 2>(p, st, c.pdl)
-                                                                            : run_gate_row<1, 3>(p, st, c.pdl);
-    if (bpl == 2) return ipw == 1 ? run_gate_row<2, 1>(p, st, c.pdl) : ipw == 2 ? run_gate_row<2, 2>(p, st, c.pdl)
-                                                                            : run_gate_row<2, 3>(p, st, c.pdl);
-    return run_gate_row<4, 1>(p, st, c.pdl);
+    return c.mode == 2 ? dispatch_gate_row<2>(p, bpl, ipw, st, c.pdl) : dispatch_gate_row<1>(p, bpl, ipw, st, c.pdl);
 }
 
 bool down_row_supported(const ExpertCall& c) {
     const bool act = c.mode == 0 ? (c.x != nullptr && (size_t)c.K * c.k * 4 <= 96 * 1024)
-                                 : (c.xq != nullptr || c.x != nullptr);
+                                 : ((c.xq != nullptr && (c.mode == 1 || c.xl != nullptr)) || c.x != nullptr);
     return c.R == 1 && !c.plan.active && !c.expert_out && act && c.k % 32 == 0 && c.K >= 1 &&
            (int64_t)c.K * (c.k / 32) <= 32 * DR_MAXP;
 }
@@ -598,13 +634,14 @@ bool down_row_supported(const ExpertCall& c) {
 cudaError_t launch_down_row(const ExpertCall& c, cudaStream_t st) {
     if (!down_row_supported(c)) return cudaErrorInvalidConfiguration;
     DownRowParams p = {c.q0, c.s0, (int)c.E, (int)c.out_rows, (int)c.k, (int)(c.k / 32), c.K, c.ids, c.gates,
-                       c.x, c.xq, c.xs, c.residual, c.y, c.pf};
+                       c.x, c.xq, c.xl, c.xs, c.residual, c.y, c.pf};
     const int ppl = (int)((c.K * (c.k / 32) + 31) / 32);
     // one output row per warp, the rows spread over every SM
     const int sms = device_info().sms;
     int wpc = (int)((c.out_rows + sms - 1) / sms);
     if (wpc < 4) wpc = 4;
     if (wpc > DR_MAXW) wpc = DR_MAXW;
+    if (c.mode == 2) return dispatch_down_row<2>(p, ppl, wpc, st, c.pdl);
     return c.mode == 0 ? dispatch_down_row<0>(p, ppl, wpc, st, c.pdl) : dispatch_down_row<1>(p, ppl, wpc, st, c.pdl);
 }
 

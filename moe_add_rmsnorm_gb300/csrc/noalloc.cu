@@ -68,7 +68,7 @@ extern "C" {
 int q8_gemv_noalloc(const q8_mat* W, q8_mode mode, const float* x, const q8_act* xq, int64_t rows, float* y,
                     q8_stream stream) {
     if (!W || !W->q || !W->s || W->rows < 1 || W->cols < 1 || W->cols % 32 || rows < 0 || rows > 65536 ||
-        (mode != Q8_F32ACT_F64SUM && mode != Q8_INT8ACT))
+        (mode != Q8_F32ACT_F64SUM && mode != Q8_INT8ACT && mode != Q8_INT8ACT2))
         return gemv_over_scratch(W, mode, x, xq, rows, y, nullptr, 0, nullptr, 0, 0, (cudaStream_t)stream,
                                  "q8_gemv_noalloc");  // the projection's own argument checks name the problem
     size_t bytes = 0, counters = 0;

@@ -34,6 +34,7 @@ struct NormParams {
     float* sum;
     float* y;
     int8_t* yq;
+    int8_t* yl;  // with yq: the low words of the two-word form
     float* ys;
     int* err;
     L2Prefetch pf;
@@ -126,8 +127,12 @@ __global__ void __launch_bounds__(NORM_THREADS) add_rmsnorm_kernel(const NormPar
             // The block of 32 values lies in this warp's lanes (the slice is whole 32-value blocks when quantizing).
             if (p.yq && (j * NORM_THREADS + wid * 32) < dl) {
                 float dsc;
-                const int8_t qv = quantize_lane(y, dsc);
-                if (in) p.yq[gi] = qv;
+                int8_t lv = 0;
+                const int8_t qv = p.yl ? quantize2_lane(y, dsc, lv) : quantize_lane(y, dsc);
+                if (in) {
+                    p.yq[gi] = qv;
+                    if (p.yl) p.yl[gi] = lv;
+                }
                 if (lane == 0) p.ys[gi / 32] = dsc;
             }
         }
@@ -135,16 +140,23 @@ __global__ void __launch_bounds__(NORM_THREADS) add_rmsnorm_kernel(const NormPar
     cluster_wait();  // no CTA leaves while another may still read its shared memory
 }
 
+// One word per value, or with `l` the two-word form (high words to q, low words to l).
 __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ x, int64_t nblocks,
-                                                       int8_t* __restrict__ q, float* __restrict__ s) {
+                                                       int8_t* __restrict__ q, int8_t* __restrict__ l,
+                                                       float* __restrict__ s) {
     griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int64_t stride = (int64_t)gridDim.x * 8;
     for (int64_t b = warp; b < nblocks; b += stride) {
         float d;
-        const int8_t v = quantize_lane(x[b * 32 + lane], d);
-        q[b * 32 + lane] = v;
+        if (l) {
+            int8_t lv;
+            q[b * 32 + lane] = quantize2_lane(x[b * 32 + lane], d, lv);
+            l[b * 32 + lane] = lv;
+        } else {
+            q[b * 32 + lane] = quantize_lane(x[b * 32 + lane], d);
+        }
         if (lane == 0) s[b] = d;
     }
     griddep_launch();
@@ -175,7 +187,7 @@ cudaError_t launch_norm(const NormParams& p, int64_t rows, cudaStream_t st, int 
 }
 
 cudaError_t launch_add_rmsnorm(const NormCall& c, cudaStream_t st) {
-    NormParams p = {c.a, c.a_row, c.a_rows, c.b, c.w, (int)c.d, c.eps, c.sum, c.y, c.yq, c.ys, c.err, c.pf};
+    NormParams p = {c.a, c.a_row, c.a_rows, c.b, c.w, (int)c.d, c.eps, c.sum, c.y, c.yq, c.yl, c.ys, c.err, c.pf};
     // cluster size: up to 8 CTAs of at least 256 values each, each slice whole 32-value blocks
     int cl = 1;
     while (cl < 8 && c.d % (cl * 2 * 32) == 0 && c.d / (cl * 2) >= NORM_THREADS) cl *= 2;
@@ -198,13 +210,13 @@ cudaError_t launch_add_rmsnorm(const NormCall& c, cudaStream_t st) {
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_quantize(const float* x, int64_t n, int8_t* q, float* s, cudaStream_t st) {
+cudaError_t launch_quantize(const float* x, int64_t n, int8_t* q, float* s, cudaStream_t st, int8_t* l) {
     const int64_t nblocks = n / 32;
     int64_t grid = (nblocks + 7) / 8;
     const int64_t cap = (int64_t)device_info().sms * 8;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    return launch(quantize_kernel, dim3((unsigned)grid), dim3(256), 0, st, 0, x, nblocks, q, s);
+    return launch(quantize_kernel, dim3((unsigned)grid), dim3(256), 0, st, 0, x, nblocks, q, l, s);
 }
 
 }  // namespace q8

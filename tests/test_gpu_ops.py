@@ -13,7 +13,7 @@ from synth import recipes
 
 pytestmark = pytest.mark.gpu
 
-TOL = {0: 1e-4, 1: 2e-3}
+TOL = {0: 1e-4, 1: 2e-3, 2: 2e-3}  # mode 2 (two words) is an int8-activation mode
 
 
 def rel_err(gpu, ora):
@@ -306,25 +306,29 @@ def _run_moe_gpu(q8, ws, md, mode, x, K, residual=None, expert_out=True, route_p
     pt = _plan_tensors(E, R * K)
     plan = q8.plan_struct(*pt) if R > 1 else None
     h = empty((R * K, dff), torch.float32)
-    hq = empty((R * K, dff), torch.int8) if mode == 1 else None
-    hs = empty((R * K, dff // 32), torch.float32) if mode == 1 else None
+    hq = empty((R * K, dff), torch.int8) if mode >= 1 else None
+    hl = empty((R * K, dff), torch.int8) if mode == 2 else None
+    hs = empty((R * K, dff // 32), torch.float32) if mode >= 1 else None
     y = empty((R, d), torch.float32)
     eo = empty((R, K, d), torch.float32) if expert_out else None
     tx = dev(x)
-    xq = xs = None
+    xq = xs = xl = None
     if mode == 1:
         oq, os_ = oracle.quantize(x)
         xq, xs = dev(oq), dev(os_)
-    q8.moe_route_topk(*md["router"], mode, K, ids, gates, x=tx, xq=xq, xs=xs, rows=R, logits=logits,
+    elif mode == 2:
+        oq, ol, os_ = oracle.quantize2(x)
+        xq, xl, xs = dev(oq), dev(ol), dev(os_)
+    q8.moe_route_topk(*md["router"], mode, K, ids, gates, x=tx, xq=xq, xs=xs, xl=xl, rows=R, logits=logits,
                       plan=q8.plan_struct(*pt) if route_plan else None, ws=ws)
-    q8.moe_gate_up(*md["gate"], *md["up"], dff, mode, K, ids, h, x=tx, xq=xq, xs=xs, hq=hq, hs=hs, rows=R, plan=plan,
-                   ws=ws)
+    q8.moe_gate_up(*md["gate"], *md["up"], dff, mode, K, ids, h, x=tx, xq=xq, xs=xs, xl=xl, hq=hq, hs=hs, hl=hl,
+                   rows=R, plan=plan, ws=ws)
     q8.moe_down_combine(*md["down"], d, mode, K, ids, gates, y, h=h if (down_reads_h or mode == 0) else None,
-                        hq=hq, hs=hs, rows=R, plan=plan,
+                        hq=hq, hs=hs, hl=hl, rows=R, plan=plan,
                         residual=dev(residual) if residual is not None else None, expert_out=eo, ws=ws)
     return dict(ids=host(ids), gates=host(gates), logits=host(logits), h=host(h).reshape(R, K, dff),
                 y=host(y), expert_out=host(eo) if expert_out else None, hq=host(hq) if hq is not None else None,
-                hs=host(hs) if hs is not None else None)
+                hs=host(hs) if hs is not None else None, hl=host(hl) if hl is not None else None)
 
 
 def _compare_moe(out, ref, mode, K):
@@ -348,12 +352,16 @@ def _compare_moe(out, ref, mode, K):
     assert ties <= max(1, R // 16), f"{ties} of {R} rows hold a near tie"
     if out["hq"] is not None:  # gate-up's int8 epilogue = the quantizer applied to its own f32 rows, bit for bit
         h = out["h"].reshape(-1, out["h"].shape[-1])
-        oq, os_ = oracle.quantize(h)
+        if mode == 2:
+            oq, ol, os_ = oracle.quantize2(h)
+            np.testing.assert_array_equal(out["hl"], ol)
+        else:
+            oq, os_ = oracle.quantize(h)
         np.testing.assert_array_equal(out["hq"], oq)
         np.testing.assert_array_equal(out["hs"].reshape(os_.shape), os_)
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_moe_block_batch1(q8, ws, moe_host, moe_dev, mode):
     x = synth.normal((1, 2048), 0, recipes.VEC + 70)
     res = synth.normal((1, 2048), 0, recipes.VEC + 71)
@@ -363,7 +371,7 @@ def test_moe_block_batch1(q8, ws, moe_host, moe_dev, mode):
     _compare_moe(out, ref, mode, 8)
 
 
-@pytest.mark.parametrize("mode,down_reads_h", [(0, True), (1, True), (1, False)])
+@pytest.mark.parametrize("mode,down_reads_h", [(0, True), (1, True), (1, False), (2, True), (2, False)])
 @pytest.mark.parametrize("spread", [False, True])
 def test_moe_one_row_fused_path(q8, ws, moe_host, moe_dev, mode, down_reads_h, spread):
     # one row, no plan, no per-expert outputs: the router and its top-k in one cluster launch, gate-up quantizing its
@@ -386,7 +394,7 @@ def test_moe_one_row_fused_path(q8, ws, moe_host, moe_dev, mode, down_reads_h, s
         assert abs(out["gates"][0].sum() - 1.0) < 1e-5
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("E,K,d", [(4, 4, 64), (16, 3, 1024), (64, 32, 2048), (1000, 8, 4096), (1024, 1, 32)])
 def test_route_one_row_shapes(q8, ws, mode, E, K, d):
     # the one-cluster router: experts not a multiple of the cluster, K = E, K = 32, the widest rows, one block (the f32
@@ -399,9 +407,13 @@ def test_route_one_row_shapes(q8, ws, mode, E, K, d):
     logits = empty((1, E), torch.float32)
     if mode == 0:
         q8.moe_route_topk(dev(rq), dev(rs), 0, K, ids, gates, x=dev(x), rows=1, logits=logits, ws=ws)
-    else:
+    elif mode == 1:
         xq, xs = oracle.quantize(x)
         q8.moe_route_topk(dev(rq), dev(rs), 1, K, ids, gates, xq=dev(xq), xs=dev(xs), rows=1, logits=logits, ws=ws)
+    else:
+        xq, xl, xs = oracle.quantize2(x)
+        q8.moe_route_topk(dev(rq), dev(rs), 2, K, ids, gates, xq=dev(xq), xs=dev(xs), xl=dev(xl), rows=1,
+                          logits=logits, ws=ws)
     l = oracle.gemv(mode, rq, rs, x[0])
     gl = host(logits)[0]
     assert rel_err(gl, l) < TOL[mode]
@@ -413,7 +425,7 @@ def test_route_one_row_shapes(q8, ws, mode, E, K, d):
     assert rel_err(host(gates)[0], ora_g) < TOL[mode]
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_moe_block_spread_gates(q8, ws, moe_host, mode):
     # router scales x1e-3: logits of std ~0.03, so all eight gates carry weight in the combine
     mh = dict(moe_host)
@@ -427,7 +439,7 @@ def test_moe_block_spread_gates(q8, ws, moe_host, mode):
     _compare_moe(out, ref, mode, 8)
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("R", [2, 4, 8, 16, 32, 64])
 def test_moe_chunk(q8, ws, moe_host, moe_dev, mode, R):
     x = synth.normal((R, 2048), 1, recipes.VEC + 80)
@@ -437,7 +449,7 @@ def test_moe_chunk(q8, ws, moe_host, moe_dev, mode, R):
     _compare_moe(out, ref, mode, 8)
 
 
-@pytest.mark.parametrize("mode,R", [(0, 32), (1, 16), (1, 32), (1, 64)])
+@pytest.mark.parametrize("mode,R", [(0, 32), (1, 16), (1, 32), (1, 64), (2, 64)])
 def test_moe_chunk_correlated_rows(q8, ws, moe_host, moe_dev, mode, R):
     # every row near one x0: the rows share their experts, so each expert's group holds all R rows (int8 mode: the
     # tensor-core products, groups of 16 to 64 rows)
@@ -480,7 +492,7 @@ def test_moe_small_shapes_and_k_equals_e(q8, ws):
               gate=synth.q8_matrix(E * dff, d, 4, 90), up=synth.q8_matrix(E * dff, d, 4, 91),
               down=synth.q8_matrix(E * d, dff, 4, 92))
     md = {k: (dev(v[0]), dev(v[1])) for k, v in mh.items()}
-    for mode in (0, 1):
+    for mode in (0, 1, 2):
         x = synth.normal((3, d), 4, recipes.VEC + 93)
         ref = oracle.moe_rows(mode, oracle.MoeWeights(d, dff, E, E, **mh), x)
         out = _run_moe_gpu(q8, ws, md, mode, x, E)
