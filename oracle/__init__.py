@@ -39,7 +39,8 @@ class Q8(ctypes.Structure):
 
 class Moe(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int64), ("dff", ctypes.c_int64), ("experts", ctypes.c_int64), ("k", ctypes.c_int),
-                ("router", Q8), ("gate", Q8), ("up", Q8), ("down", Q8)]
+                ("router", Q8), ("gate", Q8), ("up", Q8), ("down", Q8), ("router_f32", ctypes.c_void_p),
+                ("sdff", ctypes.c_int64), ("sgate", Q8), ("sup", Q8), ("sdown", Q8)]
 
 
 class Model(ctypes.Structure):
@@ -50,7 +51,8 @@ class Model(ctypes.Structure):
                 ("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
                 ("wq", ctypes.c_void_p), ("wk", ctypes.c_void_p), ("wv", ctypes.c_void_p), ("wo", ctypes.c_void_p),
                 ("router", ctypes.c_void_p), ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p),
-                ("down", ctypes.c_void_p), ("lm_head", Q8), ("k_cache", ctypes.c_void_p),
+                ("down", ctypes.c_void_p), ("router_f32", ctypes.c_void_p), ("sgate", ctypes.c_void_p),
+                ("sup", ctypes.c_void_p), ("sdown", ctypes.c_void_p), ("lm_head", Q8), ("k_cache", ctypes.c_void_p),
                 ("v_cache", ctypes.c_void_p)]
 
 
@@ -77,7 +79,8 @@ def lib():
             "ora_topk": ([vp, i64, i32, vp], None),
             "ora_route": ([vp, i64, i32, vp, vp], None),
             "ora_silu": ([dbl], dbl),
-            "ora_moe_row": ([i32, ctypes.POINTER(Moe), vp, vp, vp, vp, vp, vp, vp, vp], None),
+            "ora_moe_row": ([i32, ctypes.POINTER(Moe), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp], None),
+            "ora_gemv_f32w": ([vp, i64, i64, vp, vp], None),
             "ora_group": ([vp, i64, i32, i64, vp, vp, vp], None),
             "ora_rmsnorm_head": ([vp, vp, i64, f32, vp], None),
             "ora_rope": ([vp, i64, i64, dbl], None),
@@ -247,16 +250,27 @@ def silu(z):
 
 
 class MoeWeights:
-    """Host arrays of one mixture: router [E,d], stacked gate/up [E*dff,d], stacked down [E*d,dff] (Q8_0 each)."""
+    """Host arrays of one mixture: router [E,d], stacked gate/up [E*dff,d], stacked down [E*d,dff] (Q8_0 each);
+    optionally a router of f32 values [E,d] used in place of the Q8_0 router, and a shared expert (gate/up [sdff,d],
+    down [d,sdff], Q8_0)."""
 
-    def __init__(self, d, dff, experts, k, router, gate, up, down):
+    def __init__(self, d, dff, experts, k, router, gate, up, down, router_f32=None, shared=None):
         self.d, self.dff, self.experts, self.k = d, dff, experts, k
         self.arrays = [np.ascontiguousarray(a[0], np.int8) for a in (router, gate, up, down)]
         self.scales = [np.ascontiguousarray(a[1], np.float32) for a in (router, gate, up, down)]
+        self.router_f32 = None if router_f32 is None else np.ascontiguousarray(router_f32, np.float32)
+        self.shared = None
+        self.sdff = 0
+        if shared is not None:
+            self.shared = [(np.ascontiguousarray(q, np.int8), np.ascontiguousarray(s, np.float32))
+                           for q, s in (shared["gate"], shared["up"], shared["down"])]
+            self.sdff = self.shared[0][0].shape[0]
 
     def struct(self):
         q8 = [Q8(q.ctypes.data, s.ctypes.data) for q, s in zip(self.arrays, self.scales)]
-        return Moe(self.d, self.dff, self.experts, self.k, *q8)
+        sh = [Q8(q.ctypes.data, s.ctypes.data) for q, s in self.shared] if self.shared else [Q8(), Q8(), Q8()]
+        rf = None if self.router_f32 is None else self.router_f32.ctypes.data
+        return Moe(self.d, self.dff, self.experts, self.k, *q8, rf, self.sdff, *sh)
 
 
 def moe_rows(mode, w: MoeWeights, x, residual=None):
@@ -267,14 +281,28 @@ def moe_rows(mode, w: MoeWeights, x, residual=None):
     out = {
         "logits": np.empty((R, w.experts)), "ids": np.empty((R, w.k), np.int32), "gates": np.empty((R, w.k)),
         "hidden": np.empty((R, w.k, w.dff)), "expert_out": np.empty((R, w.k, w.d)), "y": np.empty((R, w.d)),
+        "shared_hidden": np.empty((R, max(w.sdff, 1))), "shared_out": np.empty((R, w.d)),
     }
     res = None if residual is None else np.ascontiguousarray(np.reshape(residual, (R, w.d)), np.float32)
     for r in range(R):
         lib().ora_moe_row(int(mode), ctypes.byref(st), x[r].ctypes.data,
                           None if res is None else res[r].ctypes.data,
                           out["logits"][r].ctypes.data, out["ids"][r].ctypes.data, out["gates"][r].ctypes.data,
-                          out["hidden"][r].ctypes.data, out["expert_out"][r].ctypes.data, out["y"][r].ctypes.data)
+                          out["hidden"][r].ctypes.data, out["expert_out"][r].ctypes.data, out["y"][r].ctypes.data,
+                          out["shared_hidden"][r].ctypes.data, out["shared_out"][r].ctypes.data)
+    if not w.sdff:
+        del out["shared_hidden"], out["shared_out"]
     return out
+
+
+def gemv_f32w(w, x):
+    """y = W x for a matrix of f32 values (an f32 router), f64 sums."""
+    w, pw = _c(w, np.float32)
+    x, px = _c(x, np.float32)
+    n, k = w.shape
+    y = np.empty(n, np.float64)
+    lib().ora_gemv_f32w(pw, n, k, px, y.ctypes.data)
+    return y
 
 
 def group(ids, experts):
@@ -322,7 +350,8 @@ class ModelArrays:
     """Host arrays of a whole model (per-layer lists); keeps every array alive while the C struct points at it."""
 
     def __init__(self, cfg, embed, attn_norm, ffn_norm, q_norm, k_norm, final_norm, wq, wk, wv, wo, router, gate, up,
-                 down, lm_head, k_cache, v_cache):
+                 down, lm_head, k_cache, v_cache, router_f32=None, shared_gate=None, shared_up=None,
+                 shared_down=None):
         self.cfg = cfg
         keep = []
 
@@ -357,11 +386,17 @@ class ModelArrays:
         p_kc, self.k_cache = ptrs(k_cache, np.float32)
         p_vc, self.v_cache = ptrs(v_cache, np.float32)
         lq, ls = arr(lm_head[0], np.int8), arr(lm_head[1], np.float32)
-        moe = Moe(cfg["d"], cfg["dff"], cfg["experts"], cfg["k"], Q8(), Q8(), Q8(), Q8())
+        sdff = shared_gate[0][0].shape[0] if shared_gate is not None else 0
+        moe = Moe(cfg["d"], cfg["dff"], cfg["experts"], cfg["k"], Q8(), Q8(), Q8(), Q8(), None, sdff, Q8(), Q8(),
+                  Q8())
+        p_rf = ptrs(router_f32, np.float32)[0] if router_f32 is not None else None
         self.struct = Model(L, cfg["d"], cfg["heads"], cfg["kv_heads"], cfg["hd"], cfg["vocab"], cfg["ctx"],
                             cfg["eps"], cfg["rope_theta"], moe, self.embed.ctypes.data, p_attn, p_ffn, p_qn, p_kn,
                             self.final_norm.ctypes.data, q8s(wq), q8s(wk), q8s(wv), q8s(wo), q8s(router), q8s(gate),
-                            q8s(up), q8s(down), Q8(lq.ctypes.data, ls.ctypes.data), p_kc, p_vc)
+                            q8s(up), q8s(down), p_rf,
+                            q8s(shared_gate) if sdff else None, q8s(shared_up) if sdff else None,
+                            q8s(shared_down) if sdff else None,
+                            Q8(lq.ctypes.data, ls.ctypes.data), p_kc, p_vc)
         self._keep = keep
 
 

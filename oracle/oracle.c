@@ -267,17 +267,37 @@ void ora_route(const double *logits, int64_t experts, int k, int32_t *ids, doubl
  * silu(gate . x) * (up . x). */
 double ora_silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* lane_link.rs, Link::prim (Moe: Router::F32, a router whose operand is values rather than quantized checkpoint rows):
+ * the router's logits as a product of f32 values by the f32 activation.  Every term and the sum in f64. */
+void ora_gemv_f32w(const float *w, int64_t n, int64_t k, const float *x, double *y) {
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1 && n * k >= (1 << 16))
+    for (int64_t o = 0; o < n; ++o) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < k; ++t) acc += (double)w[o * k + t] * (double)x[t];
+        y[o] = acc;
+    }
+}
+
 /* qwen_emit docs, MoeWeights (router [E,d]; gate/up [E*dff,d] with expert e at row e*dff; down [E*d,dff] with expert e
  * at row e*d) and emit_moe_forward (router product, softmax top-K renormalized, each expert's SwiGLU at an
- * expert-indexed base, weighted combine).  In mode 1 every projection reads its activation quantized
+ * expert-indexed base, weighted combine).  In the int8 modes every Q8_0 projection reads its activation quantized
  * (forward_shim.rs, ForwardShim::activation: operand 0 of a Q8_0 product or a mixture); the hidden row is held in f32
- * before the down product reads it. */
+ * before the down product reads it.
+ * An f32 router (lane_link.rs, Link::prim: Router::F32) is a product of values, not of quantized rows: it reads the
+ * f32 activation in every mode.
+ * A shared expert (lane_link.rs, Link::class_launch: SharedExpertFusion, the mixture with the shared expert's gated pair
+ * and down product in one launch; SharedExperts {wg, wu, wd, dff}) is a SwiGLU feed-forward every row passes through,
+ * unweighted: its output is added to the weighted sum of the kept experts, after them. */
 void ora_moe_row(int mode, const ora_moe *m, const float *x, const float *residual, double *logits, int32_t *ids,
-                 double *gates, double *hidden, double *expert_out, double *y) {
+                 double *gates, double *hidden, double *expert_out, double *y, double *shared_hidden,
+                 double *shared_out) {
     const int64_t d = m->d, dff = m->dff, E = m->experts;
     const int K = m->k;
     double *l = (double *)malloc(sizeof(double) * (size_t)E);
-    ora_gemv(mode, m->router.q, m->router.s, E, d, x, l);
+    if (m->router_f32)
+        ora_gemv_f32w(m->router_f32, E, d, x, l);
+    else
+        ora_gemv(mode, m->router.q, m->router.s, E, d, x, l);
     if (logits) memcpy(logits, l, sizeof(double) * (size_t)E);
     double g[64];
     int32_t id[64];
@@ -302,6 +322,27 @@ void ora_moe_row(int mode, const ora_moe *m, const float *x, const float *residu
             if (expert_out) expert_out[j * d + o] = yj[o];
             acc[o] += g[j] * yj[o];
         }
+    }
+    if (m->sdff > 0) {  /* the shared expert, after the kept experts */
+        const int64_t sdff = m->sdff;
+        double *sg = (double *)malloc(sizeof(double) * (size_t)sdff);
+        double *su = (double *)malloc(sizeof(double) * (size_t)sdff);
+        float *sh32 = (float *)malloc(sizeof(float) * (size_t)sdff);
+        ora_gemv(mode, m->sgate.q, m->sgate.s, sdff, d, x, sg);
+        ora_gemv(mode, m->sup.q, m->sup.s, sdff, d, x, su);
+        for (int64_t i = 0; i < sdff; ++i) {
+            double h = ora_silu(sg[i]) * su[i];
+            if (shared_hidden) shared_hidden[i] = h;
+            sh32[i] = (float)h;
+        }
+        ora_gemv(mode, m->sdown.q, m->sdown.s, d, sdff, sh32, yj);
+        for (int64_t o = 0; o < d; ++o) {
+            if (shared_out) shared_out[o] = yj[o];
+            acc[o] += yj[o];
+        }
+        free(sg);
+        free(su);
+        free(sh32);
     }
     for (int64_t o = 0; o < d; ++o) y[o] = (residual ? (double)residual[o] : 0.0) + acc[o];
     for (int j = 0; j < K; ++j) {
@@ -450,7 +491,15 @@ void ora_decode_layer(int mode, const ora_model *m, int64_t l, int64_t pos, floa
     mo.gate = m->gate[l];
     mo.up = m->up[l];
     mo.down = m->down[l];
-    ora_moe_row(mode, &mo, x32, NULL, router_logits, ids, gates, NULL, NULL, y);
+    mo.router_f32 = m->router_f32 ? m->router_f32[l] : NULL;
+    if (m->sgate && mo.sdff > 0) {
+        mo.sgate = m->sgate[l];
+        mo.sup = m->sup[l];
+        mo.sdown = m->sdown[l];
+    } else {
+        mo.sdff = 0;
+    }
+    ora_moe_row(mode, &mo, x32, NULL, router_logits, ids, gates, NULL, NULL, y, NULL, NULL);
     to_f32(y, d, moe_out);
     for (int64_t i = 0; i < d; ++i) h[i] = h[i] + moe_out[i];
     free(n64);

@@ -69,11 +69,19 @@ typedef struct {
     ora_q8 gate;   /* [experts*dff, d], expert e at row e*dff */
     ora_q8 up;     /* [experts*dff, d] */
     ora_q8 down;   /* [experts*d, dff], expert e at row e*d */
+    const float *router_f32; /* NULL, or a router of f32 values [experts, d] used in place of `router` */
+    int64_t sdff;            /* 0, or the shared expert's hidden width */
+    ora_q8 sgate, sup;       /* the shared expert: [sdff, d] each */
+    ora_q8 sdown;            /* [d, sdff] */
 } ora_moe;
 
-/* One row through the mixture; every output pointer but ids/gates/y may be NULL. */
+/* y[o] = sum_t w[o][t] * x[t] for a matrix of f32 values, every term and the sum in f64. */
+void ora_gemv_f32w(const float *w, int64_t n, int64_t k, const float *x, double *y);
+/* One row through the mixture; every output pointer but ids/gates/y may be NULL.  With a shared expert, shared_hidden
+ * [sdff] and shared_out [d] receive its hidden row and its output. */
 void ora_moe_row(int mode, const ora_moe *m, const float *x, const float *residual, double *logits, int32_t *ids,
-                 double *gates, double *hidden, double *expert_out, double *y);
+                 double *gates, double *hidden, double *expert_out, double *y, double *shared_hidden,
+                 double *shared_out);
 /* Choices of a chunk grouped by expert: counts[e], offsets[e] (offsets[experts] = rows*k) and the choice indices
  * r*k+j of each expert in ascending order. */
 void ora_group(const int32_t *ids, int64_t rows, int k, int64_t experts, int32_t *counts, int32_t *offsets,
@@ -98,6 +106,8 @@ typedef struct {
     const float *final_norm;               /* [d] */
     const ora_q8 *wq, *wk, *wv, *wo;       /* [layers] */
     const ora_q8 *router, *gate, *up, *down; /* [layers] */
+    const float *const *router_f32;        /* NULL, or [layers] -> f32 router values [experts, d] */
+    const ora_q8 *sgate, *sup, *sdown;     /* NULL, or [layers]: the shared expert (moe.sdff wide) */
     ora_q8 lm_head;                        /* [vocab, d] */
     float *const *k_cache;                 /* [layers] -> [kv_heads, ctx, hd] */
     float *const *v_cache;                 /* [layers] -> [kv_heads, ctx, hd] */

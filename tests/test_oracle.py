@@ -647,3 +647,133 @@ def test_moe_and_step_run_in_mode2():
     e2 = np.max(np.abs(l2 - l0)) / np.max(np.abs(l0))
     e1 = np.max(np.abs(l1 - l0)) / np.max(np.abs(l0))
     assert e2 < 1e-3 and e2 < e1 / 8, (e1, e2)
+
+
+# ---- the f32 router and the shared expert ----------------------------------------------------------------------------
+
+def test_gemv_f32w_closed_form_and_exact():
+    # unit-vector rows pick single inputs exactly; random rows against exact rationals
+    x = synth.normal(64, seed=6, tensor=50)
+    w = np.zeros((5, 64), np.float32)
+    cols = [3, 0, 63, 17, 3]
+    for o, c in enumerate(cols):
+        w[o, c] = [1.0, -2.0, 0.5, 4.0, -0.25][o]
+    np.testing.assert_array_equal(oracle.gemv_f32w(w, x), w[np.arange(5), cols].astype(np.float64) * x[cols])
+    w = synth.normal((7, 64), seed=6, tensor=51)
+    y = oracle.gemv_f32w(w, x)
+    for o in range(7):
+        exact = sum(Fraction(float(w[o, t])) * Fraction(float(x[t])) for t in range(64))
+        assert abs(Fraction(y[o]) - exact) <= abs(exact) * Fraction(1, 10 ** 13) + Fraction(1, 10 ** 30)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_f32_router_reads_the_f32_activation(mode):
+    # an f32 router is a product of values: its logits are the f32 product of x in every mode (no quantized activation)
+    d, dff, E, K = 64, 32, 6, 2
+    gate = synth.q8_matrix(E * dff, d, seed=7, tensor=52)
+    up = synth.q8_matrix(E * dff, d, seed=7, tensor=53)
+    down = synth.q8_matrix(E * d, dff, seed=7, tensor=54)
+    rf = synth.normal((E, d), seed=7, tensor=55, mul=0.1)
+    x = synth.normal((3, d), seed=7, tensor=56)
+    w = oracle.MoeWeights(d, dff, E, K, _zeros_q8(E, d), gate, up, down, router_f32=rf)
+    out = oracle.moe_rows(mode, w, x)
+    for r in range(3):
+        np.testing.assert_array_equal(out["logits"][r], oracle.gemv_f32w(rf, x[r]))
+        ids, g = oracle.route(oracle.gemv_f32w(rf, x[r]), K)
+        np.testing.assert_array_equal(out["ids"][r], ids)
+        np.testing.assert_array_equal(out["gates"][r], g)
+
+
+def test_f32_router_with_a_q8_routers_exact_values_gives_the_same_step():
+    # router scales of powers of two make q * s exact in f32: the f32 router then holds the Q8_0 router's exact
+    # values, and the f32-activation step is the same bit for bit
+    cfg, arr = _tiny_model(21)
+    arr = dict(arr)
+    arr["router"] = [(q, np.full_like(s, 2.0 ** -6)) for q, s in arr["router"]]
+    rf = [(q.astype(np.float32) * s.repeat(32, 1)).astype(np.float32) for q, s in arr["router"]]
+
+    def fresh(**extra):
+        return oracle.ModelArrays(cfg, **{k: ([c.copy() for c in v] if k.endswith("cache") else v)
+                                          for k, v in arr.items()}, **extra)
+
+    n0, l0 = oracle.decode_step(0, fresh(), 4, 3)
+    n1, l1 = oracle.decode_step(0, fresh(router_f32=rf), 4, 3)
+    np.testing.assert_array_equal(l0, l1)
+    assert n0 == n1
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_shared_expert_identity_closed_form(mode):
+    # every routed expert has zero scales, so the mixture is the shared expert alone: gate = 127 * 0.01 * I,
+    # up = I, down = I gives y = residual + silu(1.27 x) * x (mode 0; in mode 1 on the quantized x and hidden row)
+    d, dff, E, K = 32, 32, 3, 2
+    router = synth.q8_matrix(E, d, seed=8, tensor=57)
+    zq, zs = np.zeros((E * dff, d), np.int8), np.zeros((E * dff, 1), np.float32)
+    dq, ds = np.zeros((E * d, dff), np.int8), np.zeros((E * d, 1), np.float32)
+    shared = dict(gate=_ident_q8(32, 127, 0.01), up=_ident_q8(32), down=_ident_q8(32))
+    w = oracle.MoeWeights(d, dff, E, K, router, (zq, zs), (zq, zs), (dq, ds), shared=shared)
+    x = np.abs(synth.normal(d, seed=8, tensor=58)) + 0.1
+    res = synth.normal(d, seed=8, tensor=59)
+    out = oracle.moe_rows(mode, w, x, residual=res)
+    if mode == 0:
+        xv = x.astype(np.float64)
+    else:
+        xq, xs = oracle.quantize(x)
+        xv = xq.astype(np.float64) * np.float64(xs[0])
+    gv = np.float64(np.float32(0.01)) * 127 * xv
+    h = gv / (1 + np.exp(-gv)) * xv
+    np.testing.assert_allclose(out["shared_hidden"][0], h, rtol=1e-14)
+    if mode == 0:
+        so = h.astype(np.float32).astype(np.float64)
+    else:
+        hq, hs = oracle.quantize(h.astype(np.float32))
+        so = hq.astype(np.float64) * np.float64(hs[0])
+    np.testing.assert_allclose(out["shared_out"][0], so, rtol=1e-14)
+    np.testing.assert_allclose(out["y"][0], res.astype(np.float64) + so, rtol=1e-14, atol=1e-14)
+    assert not out["expert_out"].any()
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+def test_shared_expert_adds_unweighted_to_the_mean_expert(mode):
+    # K = E with a zero router: y = mean of the routed experts' outputs + the shared expert's output (sdff != dff)
+    d, dff, sdff, E = 64, 32, 96, 4
+    gate = synth.q8_matrix(E * dff, d, seed=9, tensor=60)
+    up = synth.q8_matrix(E * dff, d, seed=9, tensor=61)
+    down = synth.q8_matrix(E * d, dff, seed=9, tensor=62)
+    shared = dict(gate=synth.q8_matrix(sdff, d, seed=9, tensor=63), up=synth.q8_matrix(sdff, d, seed=9, tensor=64),
+                  down=synth.q8_matrix(d, sdff, seed=9, tensor=65))
+    w = oracle.MoeWeights(d, dff, E, E, _zeros_q8(E, d), gate, up, down, shared=shared)
+    x = synth.normal(d, seed=9, tensor=66)
+    out = oracle.moe_rows(mode, w, x)
+    np.testing.assert_allclose(out["y"][0], out["expert_out"][0].mean(0) + out["shared_out"][0], rtol=1e-12,
+                               atol=1e-12)
+    # the shared expert's output is its own SwiGLU feed-forward of x, whatever the routing
+    hid = out["shared_hidden"][0]
+    g = oracle.gemv(mode, *shared["gate"], x)
+    u = oracle.gemv(mode, *shared["up"], x)
+    np.testing.assert_allclose(hid, g / (1 + np.exp(-g)) * u, rtol=1e-13)
+    np.testing.assert_allclose(out["shared_out"][0], oracle.gemv(mode, *shared["down"], hid.astype(np.float32)),
+                               rtol=1e-13)
+
+
+def test_step_with_a_zero_shared_expert_equals_the_step_without():
+    cfg, arr = _tiny_model(23)
+    L, d = cfg["layers"], cfg["d"]
+    zero = lambda n, k: (np.zeros((n, k), np.int8), np.zeros((n, k // 32), np.float32))
+
+    def fresh(**extra):
+        return oracle.ModelArrays(cfg, **{k: ([c.copy() for c in v] if k.endswith("cache") else v)
+                                          for k, v in arr.items()}, **extra)
+
+    for mode in (0, 1, 2):
+        n0, l0 = oracle.decode_step(mode, fresh(), 5, 6)
+        n1, l1 = oracle.decode_step(mode, fresh(shared_gate=[zero(64, d)] * L, shared_up=[zero(64, d)] * L,
+                                                shared_down=[zero(d, 64)] * L), 5, 6)
+        np.testing.assert_array_equal(l0, l1)
+        assert n0 == n1
+        # and a live one changes the step
+        n2, l2 = oracle.decode_step(mode, fresh(shared_gate=[synth.q8_matrix(64, d, 3, 70 + l) for l in range(L)],
+                                                shared_up=[synth.q8_matrix(64, d, 3, 80 + l) for l in range(L)],
+                                                shared_down=[synth.q8_matrix(d, 64, 3, 90 + l) for l in range(L)]),
+                                    5, 6)
+        assert np.max(np.abs(l2 - l0)) > 1e-3 * np.max(np.abs(l0))
