@@ -171,24 +171,44 @@ typedef struct {
 Q8_API int moe_route_topk(const q8_mat *router, q8_mode mode, const float *x, const q8_act *xq, int64_t rows, int k,
                    int32_t *ids, float *gates, float *logits, const q8_moe_plan *plan, q8_ws *ws, q8_stream stream);
 
+/* A shared expert (lane_link.rs, Link::class_launch: SharedExpertFusion, the mixture with the shared expert's gated
+ * pair and down product in one launch; SharedExperts {wg, wu, wd, dff}): a SwiGLU feed-forward every row passes
+ * through, its output added unweighted to the kept experts' weighted sum.  gate and up are [sdff, d], down [d, sdff]
+ * (Q8_0, sdff % 32 == 0).  Where a call takes one, its hidden rows follow the routed ones in h (and hq): h is
+ * [rows*k*dff + rows*sdff]. */
+typedef struct {
+    q8_mat gate, up, down;
+} q8_shared_expert;
+
+/* Router and top-k over a router of f32 values (lane_link.rs, Link::prim Moe: Router::F32, a router that is values
+ * rather than quantized checkpoint rows): l = router . x_r with router device f32 [experts][d] (16-byte aligned,
+ * d % 32 == 0) and x the f32 activation (in every mode: the router reads no quantized form), products summed in f32
+ * per 128 values and then in f64; then top-k, gates and the grouping as moe_route_topk. */
+Q8_API int moe_route_topk_f32(const float *router, int64_t experts, int64_t d, const float *x, int64_t rows, int k,
+                              int32_t *ids, float *gates, float *logits, const q8_moe_plan *plan, q8_ws *ws,
+                              q8_stream stream);
+
 /* Gate-up with SwiGLU (qwen_emit, MoeWeights: gate/up [E*dff, d] stacked, expert e's rows at e*dff; emit_moe_forward:
  * each expert's SwiGLU at an expert-indexed base): h[r][j][i] = silu(Wg[e*dff+i] . x_r) * (Wu[e*dff+i] . x_r) with
  * e = ids[r][j], silu(z) = z/(1+e^-z).  h: device f32 [rows][k][dff].  In the int8 modes hq (device, words
  * [rows*k*dff] + scales [rows*k*dff/32], in Q8_INT8ACT2 with low words, or NULL) receives quantize(h)
  * (dff % 32 == 0); in the f32 mode it is ignored.
- * plan (from moe_route_topk) is required when rows > 1: each expert's weights are then read once for all its rows. */
+ * plan (from moe_route_topk) is required when rows > 1: each expert's weights are then read once for all its rows.
+ * shared (or NULL): a shared expert whose hidden rows are written after the routed ones (one row: rows of the same
+ * launch; a chunk: a projection of every row and a SwiGLU pass after the routed launches). */
 Q8_API int moe_gate_up(const q8_mat *gate, const q8_mat *up, int64_t dff, q8_mode mode, const float *x, const q8_act *xq,
                 int64_t rows, int k, const int32_t *ids, const q8_moe_plan *plan, float *h, const q8_act *hq,
-                q8_ws *ws, q8_stream stream);
+                const q8_shared_expert *shared, q8_ws *ws, q8_stream stream);
 
 /* Down-and-combine (qwen_emit, MoeWeights: down [E*d, dff] stacked, expert e's rows at e*d; emit_moe_forward: the
  * weighted combine): y[r] = residual[r] + sum_j gates[r][j] * (Wd[e*d .. e*d+d) . h[r][j]), the sum over j in order.
  * Mode Q8_F32ACT_F64SUM reads h; the int8 modes read hq (in Q8_INT8ACT2 with its low words), or quantize h when hq
  * is NULL.  residual may be NULL (and may alias y); y is device f32 [rows][d]; expert_out (device f32 [rows][k][d] or
- * NULL) receives each expert's unweighted output. */
+ * NULL) receives each expert's unweighted output.  shared (or NULL): the shared expert of moe_gate_up, whose output is
+ * added after the kept experts' (one row: blocks of the same launch; a chunk: a projection onto y after the combine). */
 Q8_API int moe_down_combine(const q8_mat *down, int64_t d, q8_mode mode, const float *h, const q8_act *hq, int64_t rows,
                      int k, const int32_t *ids, const float *gates, const q8_moe_plan *plan, const float *residual,
-                     float *y, float *expert_out, q8_ws *ws, q8_stream stream);
+                     float *y, float *expert_out, const q8_shared_expert *shared, q8_ws *ws, q8_stream stream);
 
 /* ---- a10-a11: the decode step ----------------------------------------------------------------------------------- */
 
@@ -212,6 +232,10 @@ typedef struct {
     int32_t *tok;               /* device int32 [1]: the token the step reads; the step writes the next token here */
     int32_t *pos;               /* device int32 [1]: the position the step writes; the step adds 1 */
     float *logits;              /* device f32 [vocab] or NULL */
+    /* Optional variants of the mixture (NULL / 0 when absent): */
+    const float *const *router_f32;  /* [layers] -> device f32 [E][d] routers of values used in place of `router` */
+    const q8_mat *shared_gate, *shared_up, *shared_down;  /* [layers]: a shared expert, [shared_dff, d] x 2, [d, shared_dff] */
+    int64_t shared_dff;
 } q8_model_desc;
 
 typedef struct q8_model q8_model;

@@ -39,6 +39,10 @@ class q8_act(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("lo", ctypes.c_void_p)]
 
 
+class q8_shared_expert(ctypes.Structure):
+    _fields_ = [("gate", q8_mat), ("up", q8_mat), ("down", q8_mat)]
+
+
 class q8_moe_plan(ctypes.Structure):
     _fields_ = [("counts", ctypes.c_void_p), ("offsets", ctypes.c_void_p), ("lists", ctypes.c_void_p),
                 ("active", ctypes.c_void_p)]
@@ -53,7 +57,9 @@ class q8_model_desc(ctypes.Structure):
         ("wq", ctypes.c_void_p), ("wk", ctypes.c_void_p), ("wv", ctypes.c_void_p), ("wo", ctypes.c_void_p),
         ("router", ctypes.c_void_p), ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("down", ctypes.c_void_p),
         ("lm_head", q8_mat), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
-        ("tok", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("logits", ctypes.c_void_p)]
+        ("tok", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("logits", ctypes.c_void_p),
+        ("router_f32", ctypes.c_void_p), ("shared_gate", ctypes.c_void_p), ("shared_up", ctypes.c_void_p),
+        ("shared_down", ctypes.c_void_p), ("shared_dff", ctypes.c_int64)]
 
 
 _vp, _i64, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -68,10 +74,11 @@ _SIGS = {
     "q8_gemv_blockdots": [_P(q8_mat), _P(q8_act), _i64, _vp, _vp, _vp, _vp],
     "q8_gemv_noalloc": [_P(q8_mat), _i32, _vp, _P(q8_act), _i64, _vp, _vp],
     "moe_route_topk": [_P(q8_mat), _i32, _vp, _P(q8_act), _i64, _i32, _vp, _vp, _vp, _P(q8_moe_plan), _vp, _vp],
+    "moe_route_topk_f32": [_vp, _i64, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _P(q8_moe_plan), _vp, _vp],
     "moe_gate_up": [_P(q8_mat), _P(q8_mat), _i64, _i32, _vp, _P(q8_act), _i64, _i32, _vp, _P(q8_moe_plan), _vp,
-                    _P(q8_act), _vp, _vp],
+                    _P(q8_act), _P(q8_shared_expert), _vp, _vp],
     "moe_down_combine": [_P(q8_mat), _i64, _i32, _vp, _P(q8_act), _i64, _i32, _vp, _vp, _P(q8_moe_plan), _vp, _vp,
-                         _vp, _vp, _vp],
+                         _vp, _P(q8_shared_expert), _vp, _vp],
     "q8_model_create": [_P(q8_model_desc), _P(_vp)],
     "q8_model_destroy": [_vp],
     "decode_step": [_vp, _vp],
@@ -199,23 +206,37 @@ def moe_route_topk(rq, rs, mode, k, ids, gates, x=None, xq=None, xs=None, rows=1
                               _ptr(logits), pl, ws.handle if ws else None, _stream(stream)))
 
 
+def shared_expert(gate, up, down) -> q8_shared_expert:
+    """A shared expert over (q, s) device tensor pairs: gate and up [sdff, d], down [d, sdff]."""
+    return q8_shared_expert(mat(*gate), mat(*up), mat(*down))
+
+
+def moe_route_topk_f32(router, k, ids, gates, x, rows=1, logits=None, plan=None, ws=None, stream=None):
+    """The router of f32 values (device f32 [E, d]) over the f32 rows x, then top-k as moe_route_topk."""
+    pl = ctypes.byref(plan) if plan is not None else None
+    _check(lib.moe_route_topk_f32(_ptr(router), router.shape[0], router.shape[1], _ptr(x), rows, int(k), _ptr(ids),
+                                  _ptr(gates), _ptr(logits), pl, ws.handle if ws else None, _stream(stream)))
+
+
 def moe_gate_up(gq, gs, uq, us, dff, mode, k, ids, h, x=None, xq=None, xs=None, hq=None, hs=None, rows=1, plan=None,
-                ws=None, stream=None, xl=None, hl=None):
+                ws=None, stream=None, xl=None, hl=None, shared=None):
     G, U = mat(gq, gs), mat(uq, us)
     qa = _actref(xq, xs, xl)
     ha = _actref(hq, hs, hl)
     pl = ctypes.byref(plan) if plan is not None else None
+    sh = ctypes.byref(shared) if shared is not None else None
     _check(lib.moe_gate_up(ctypes.byref(G), ctypes.byref(U), int(dff), int(mode), _ptr(x), qa, rows, int(k),
-                           _ptr(ids), pl, _ptr(h), ha, ws.handle if ws else None, _stream(stream)))
+                           _ptr(ids), pl, _ptr(h), ha, sh, ws.handle if ws else None, _stream(stream)))
 
 
 def moe_down_combine(dq, ds, d, mode, k, ids, gates, y, h=None, hq=None, hs=None, rows=1, plan=None, residual=None,
-                     expert_out=None, ws=None, stream=None, hl=None):
+                     expert_out=None, ws=None, stream=None, hl=None, shared=None):
     Dm = mat(dq, ds)
     ha = _actref(hq, hs, hl)
     pl = ctypes.byref(plan) if plan is not None else None
+    sh = ctypes.byref(shared) if shared is not None else None
     _check(lib.moe_down_combine(ctypes.byref(Dm), int(d), int(mode), _ptr(h), ha, rows, int(k), _ptr(ids),
-                                _ptr(gates), pl, _ptr(residual), _ptr(y), _ptr(expert_out),
+                                _ptr(gates), pl, _ptr(residual), _ptr(y), _ptr(expert_out), sh,
                                 ws.handle if ws else None, _stream(stream)))
 
 
@@ -257,6 +278,12 @@ class Model:
         d.tok = tok.data_ptr()
         d.pos = pos.data_ptr()
         d.logits = logits.data_ptr() if logits is not None else None
+        if t.get("router_f32") is not None:  # optional: routers of f32 values
+            d.router_f32 = ptr_array(t["router_f32"])
+        if t.get("shared_gate") is not None:  # optional: a shared expert per layer
+            for key in ("shared_gate", "shared_up", "shared_down"):
+                setattr(d, key, mat_array(t[key]))
+            d.shared_dff = int(t["shared_gate"][0][0].shape[0])
         h = ctypes.c_void_p()
         _check(lib.q8_model_create(ctypes.byref(d), ctypes.byref(h)))
         self.handle = h

@@ -335,9 +335,23 @@ int moe_route_topk(const q8_mat* router, q8_mode mode, const float* x, const q8_
 
 extern "C" {
 
+// A shared expert's shapes: gate and up [sdff][d], down [d][sdff], whole 32-value blocks.
+static int check_shared(const q8_shared_expert* sh, int64_t d, int64_t* sdff) {
+    *sdff = 0;
+    if (!sh) return Q8_OK;
+    if (int r = check_mat(&sh->gate, "shared.gate")) return r;
+    if (int r = check_mat(&sh->up, "shared.up")) return r;
+    if (int r = check_mat(&sh->down, "shared.down")) return r;
+    const int64_t f = sh->gate.rows;
+    if (sh->up.rows != f || sh->gate.cols != d || sh->up.cols != d || sh->down.rows != d || sh->down.cols != f)
+        return fail(Q8_EINVAL, "shared: gate/up must be [sdff, %lld] and down [%lld, sdff]", (long long)d, (long long)d);
+    *sdff = f;
+    return Q8_OK;
+}
+
 int moe_gate_up(const q8_mat* gate, const q8_mat* up, int64_t dff, q8_mode mode, const float* x, const q8_act* xq,
                 int64_t rows, int k, const int32_t* ids, const q8_moe_plan* plan, float* h, const q8_act* hq,
-                q8_ws* ws, q8_stream stream) {
+                const q8_shared_expert* shared, q8_ws* ws, q8_stream stream) {
     g_err[0] = 0;
     if (int r = check_mat(gate, "gate")) return r;
     if (int r = check_mat(up, "up")) return r;
@@ -360,6 +374,8 @@ int moe_gate_up(const q8_mat* gate, const q8_mat* up, int64_t dff, q8_mode mode,
         return fail(Q8_EUNSUPPORTED, "d %lld: an expert row wider than one pass of the kernel", (long long)gate->cols);
     if (plan)
         if (int r = check_plan(plan)) return r;
+    int64_t sdff = 0;
+    if (int r = check_shared(shared, gate->cols, &sdff)) return r;
     if (rows == 0) return Q8_OK;
     cudaStream_t st = (cudaStream_t)stream;
     ExpertCall c;
@@ -368,6 +384,13 @@ int moe_gate_up(const q8_mat* gate, const q8_mat* up, int64_t dff, q8_mode mode,
     c.s0 = gate->s;
     c.q1 = up->q;
     c.s1 = up->s;
+    if (shared) {
+        c.sq0 = shared->gate.q;
+        c.ss0 = shared->gate.s;
+        c.sq1 = shared->up.q;
+        c.ss1 = shared->up.s;
+        c.sdff = sdff;
+    }
     c.E = gate->rows / dff;
     c.out_rows = dff;
     c.k = gate->cols;
@@ -394,13 +417,13 @@ int moe_gate_up(const q8_mat* gate, const q8_mat* up, int64_t dff, q8_mode mode,
     cudaError_t e = launch_gate_up(c, cv, st);
     if (cv.overflow) return fail(Q8_ENOSPACE, "moe_gate_up: workspace too small for the int8 epilogue's counters");
     if (e == cudaSuccess && mode != Q8_F32ACT_F64SUM && hq && !c.hq_out)
-        e = launch_quantize(h, rows * k * dff, hq->q, hq->s, st, mode == Q8_INT8ACT2 ? hq->lo : nullptr);
+        e = launch_quantize(h, rows * k * dff + rows * sdff, hq->q, hq->s, st, mode == Q8_INT8ACT2 ? hq->lo : nullptr);
     return e == cudaSuccess ? Q8_OK : cuda_fail(e, "moe_gate_up");
 }
 
 int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h, const q8_act* hq, int64_t rows,
                      int k, const int32_t* ids, const float* gates, const q8_moe_plan* plan, const float* residual,
-                     float* y, float* expert_out, q8_ws* ws, q8_stream stream) {
+                     float* y, float* expert_out, const q8_shared_expert* shared, q8_ws* ws, q8_stream stream) {
     g_err[0] = 0;
     if (int r = check_mat(down, "down")) return r;
     if (d < 1 || down->rows % d) return fail(Q8_EINVAL, "d %lld does not divide the %lld stacked rows", (long long)d,
@@ -422,12 +445,19 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
         return fail(Q8_EUNSUPPORTED, "dff %lld: an expert row wider than one pass of the kernel", (long long)down->cols);
     if (plan)
         if (int r = check_plan(plan)) return r;
+    int64_t sdff = 0;
+    if (int r = check_shared(shared, d, &sdff)) return r;
     if (rows == 0) return Q8_OK;
     cudaStream_t st = (cudaStream_t)stream;
     ExpertCall c;
     c.mode = (int)mode;
     c.q0 = down->q;
     c.s0 = down->s;
+    if (shared) {
+        c.sq0 = shared->down.q;
+        c.ss0 = shared->down.s;
+        c.sdff = sdff;
+    }
     c.E = down->rows / d;
     c.out_rows = d;
     c.k = down->cols;
@@ -453,11 +483,12 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
     }
     Carve cv = ws->carve();
     if (mode != Q8_F32ACT_F64SUM && !hq && (rows > 1 || plan)) {  // a chunk reads its hidden rows quantized
-        int8_t* q = cv.take<int8_t>((size_t)(rows * k * down->cols));
-        float* s = cv.take<float>((size_t)(rows * k * down->cols / 32));
-        int8_t* l = mode == Q8_INT8ACT2 ? cv.take<int8_t>((size_t)(rows * k * down->cols)) : nullptr;
+        const int64_t nh = rows * k * down->cols + rows * sdff;  // the routed hidden rows, then the shared expert's
+        int8_t* q = cv.take<int8_t>((size_t)nh);
+        float* s = cv.take<float>((size_t)(nh / 32));
+        int8_t* l = mode == Q8_INT8ACT2 ? cv.take<int8_t>((size_t)nh) : nullptr;
         if (cv.overflow) return fail(Q8_ENOSPACE, "moe_down_combine: workspace too small for the quantized rows");
-        cudaError_t qe = launch_quantize(h, rows * k * down->cols, q, s, st, l);
+        cudaError_t qe = launch_quantize(h, nh, q, s, st, l);
         if (qe != cudaSuccess) return cuda_fail(qe, "moe_down_combine");
         c.x = nullptr;
         c.xq = q;
@@ -469,6 +500,47 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
     cudaError_t e = launch_down_combine(c, cv, st);
     if (cv.overflow) return fail(Q8_ENOSPACE, "moe_down_combine: workspace too small (%zu bytes, %zu counters)", need, cnt);
     return e == cudaSuccess ? Q8_OK : cuda_fail(e, "moe_down_combine");
+}
+
+int moe_route_topk_f32(const float* router, int64_t E, int64_t d, const float* x, int64_t rows, int k, int32_t* ids,
+                       float* gates, float* logits, const q8_moe_plan* plan, q8_ws* ws, q8_stream stream) {
+    g_err[0] = 0;
+    if (!router || !x) return fail(Q8_EINVAL, "router or x: null");
+    if (!aligned(router, 16) || !aligned(x, 16)) return fail(Q8_EINVAL, "router or x: not 16-byte aligned");
+    if (E < 1 || d < 1) return fail(Q8_EINVAL, "experts %lld, d %lld", (long long)E, (long long)d);
+    if (d % 32) return fail(Q8_EUNSUPPORTED, "d %lld: not whole 32-value blocks", (long long)d);
+    if (k < 1 || k > 32) return fail(Q8_EUNSUPPORTED, "k %d: the router keeps 1 to 32 experts", k);
+    if (E > 8192) return fail(Q8_EUNSUPPORTED, "%lld experts: at most 8192", (long long)E);
+    if (k > E) return fail(Q8_EINVAL, "k %d above the %lld experts", k, (long long)E);
+    if (!ids || !gates || !ws) return fail(Q8_EINVAL, "ids, gates or ws: null");
+    if (rows < 0) return fail(Q8_EINVAL, "rows negative");
+    if (rows * k > 65536) return fail(Q8_EUNSUPPORTED, "rows*k %lld: the grouping handles at most 65536 choices",
+                                      (long long)(rows * k));
+    if (plan)
+        if (int r = check_plan(plan)) return r;
+    if (rows == 0) return Q8_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    Carve cv = ws->carve();
+    float* l = logits ? logits : cv.take<float>((size_t)(rows * E));
+    if (cv.overflow) return fail(Q8_ENOSPACE, "moe_route_topk_f32: workspace too small for the logits");
+    cudaError_t e = launch_router_f32(router, E, d, x, rows, l, 0, st);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_route_topk_f32");
+    TopkCall t;
+    t.done = plan && ws->n_counters > 0 ? ws->counters + ws->n_counters - 1 : nullptr;
+    t.logits = l;
+    t.R = rows;
+    t.E = E;
+    t.K = k;
+    t.ids = ids;
+    t.gates = gates;
+    if (plan) {
+        t.plan.counts = plan->counts;
+        t.plan.offsets = plan->offsets;
+        t.plan.lists = plan->lists;
+        t.plan.active = plan->active;
+    }
+    e = launch_topk(t, st);
+    return e == cudaSuccess ? Q8_OK : cuda_fail(e, "moe_route_topk_f32");
 }
 
 }  // extern "C"

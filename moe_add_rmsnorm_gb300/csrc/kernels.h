@@ -141,6 +141,11 @@ struct TopkCall {
 };
 cudaError_t launch_topk(const TopkCall& c, cudaStream_t st);
 
+// A router of f32 values (lane_link.rs, Link::prim: Router::F32): logits[r][e] = w[e] . x[r], f32 products summed per
+// 32 values and then in f64.
+cudaError_t launch_router_f32(const float* w, int64_t E, int64_t d, const float* x, int64_t R, float* logits,
+                              int pdl, cudaStream_t st);
+
 struct ExpertCall {
     int mode = 0;
     // gate-up: w0 = gate, w1 = up (rows E*dff, cols d); down: w0 = down (rows E*d, cols dff)
@@ -166,6 +171,14 @@ struct ExpertCall {
     const float* residual = nullptr;     // down
     float* y = nullptr;                  // down out [R][d]
     float* expert_out = nullptr;         // down out [R][K][d]
+    // a shared expert every row passes through, unweighted (sdff > 0): gate-up takes sq0/ss0 = its gate and sq1/ss1 =
+    // its up [sdff][k], and writes its hidden rows after the routed ones (h + R*K*out_rows, [R][sdff]; the int8 forms
+    // likewise); down takes sq0/ss0 = its down [out_rows][sdff] and reads those hidden rows
+    const int8_t* sq0 = nullptr;
+    const float* ss0 = nullptr;
+    const int8_t* sq1 = nullptr;
+    const float* ss1 = nullptr;
+    int64_t sdff = 0;
     int* err = nullptr;                  // device error word for a pipeline wait that gave up
     L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;

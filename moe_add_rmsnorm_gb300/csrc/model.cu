@@ -33,6 +33,8 @@ struct q8_model {
     q8_model_desc d;
     std::vector<const float*> attn_norm, ffn_norm, q_norm, k_norm;
     std::vector<q8_mat> wq, wk, wv, wo, router, gate, up, down;
+    std::vector<q8_mat> sgate, sup, sdown;  // the shared expert per layer (empty when there is none)
+    std::vector<const float*> router_f32;   // f32 routers per layer (empty when the routers are Q8_0)
     std::vector<float*> kc, vc;
     char* arena = nullptr;
     size_t arena_bytes = 0;
@@ -192,8 +194,11 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             g.err = m->err;
             Q8_TRY(launch_gemv(g, cv, st));
         }
-        // feed-forward half: the norm happens inside the router launch when the shapes allow it
-        const bool fused_norm2 = route_row_supported(mode, d.experts, D, (int)d.k) && D % 256 == 0 && D <= 4096;
+        // feed-forward half: the norm happens inside the router launch when the shapes allow it (a router of f32
+        // values reads the f32 activation: a norm launch writes it, and the int8 form the experts read)
+        const bool rf = !m->router_f32.empty();
+        const bool fused_norm2 =
+            !rf && route_row_supported(mode, d.experts, D, (int)d.k) && D % 256 == 0 && D <= 4096;
         if (!fused_norm2) {
             NormCall n2;
             n2.a = m->h;
@@ -201,8 +206,8 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             n2.rows = 1;
             n2.d = D;
             n2.eps = d.eps;
-            if (mode == 0) n2.y = m->x;
-            else {
+            if (mode == 0 || rf) n2.y = m->x;
+            if (mode != 0) {
                 n2.yq = m->xq;
                 n2.yl = m->xl;
                 n2.ys = m->xs;
@@ -210,7 +215,18 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             n2.pdl = pdl;
             Q8_TRY(launch_add_rmsnorm(n2, st));
         }
-        if (route_row_supported(mode, d.experts, D, (int)d.k)) {
+        if (rf) {  // the f32 router's projection, then its top-k
+            Q8_TRY(launch_router_f32(m->router_f32[l], d.experts, D, m->x, 1, m->rlog, pdl, st));
+            TopkCall t;
+            t.logits = m->rlog;
+            t.R = 1;
+            t.E = d.experts;
+            t.K = (int)d.k;
+            t.ids = m->ids;
+            t.gates = m->gates;
+            t.pdl = pdl;
+            Q8_TRY(launch_topk(t, st));
+        } else if (route_row_supported(mode, d.experts, D, (int)d.k)) {
             // the router projection and its top-k in one cluster launch
             RouteRowCall r;
             r.mode = mode;
@@ -279,6 +295,13 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
             c.xl = m->xl;
             c.xs = m->xs;
             c.h = m->hbuf;
+            if (!m->sgate.empty()) {  // the shared expert's rows follow the routed ones
+                c.sq0 = m->sgate[l].q;
+                c.ss0 = m->sgate[l].s;
+                c.sq1 = m->sup[l].q;
+                c.ss1 = m->sup[l].s;
+                c.sdff = d.shared_dff;
+            }
             if (mode >= 1 && gate_row_supported(c)) {  // the hidden rows quantized once, by the kernel that forms them
                 c.hq_out = m->hq;
                 c.hl_out = m->hl;
@@ -307,6 +330,11 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
                 c.xq = m->hq;
                 c.xl = m->hl;
                 c.xs = m->hs;
+            }
+            if (!m->sdown.empty()) {
+                c.sq0 = m->sdown[l].q;
+                c.ss0 = m->sdown[l].s;
+                c.sdff = d.shared_dff;
             }
             c.residual = m->h;  // h = h + mixture
             c.y = m->h;
@@ -431,6 +459,24 @@ int q8_model_create(const q8_model_desc* desc, q8_model** out) {
             return r;
     }
     if (int r = check_mat_shape(d.lm_head, d.vocab, D, "lm_head", 0)) return r;
+    const bool has_shared = d.shared_gate || d.shared_up || d.shared_down || d.shared_dff;
+    if (has_shared) {
+        if (!d.shared_gate || !d.shared_up || !d.shared_down || d.shared_dff < 32)
+            return model_fail(Q8_EINVAL, "shared expert: all of shared_gate, shared_up, shared_down and shared_dff");
+        if (d.shared_dff % 32) return model_fail(Q8_EUNSUPPORTED, "shared_dff %lld: whole 32-value blocks",
+                                                 (long long)d.shared_dff);
+        for (int64_t l = 0; l < d.layers; ++l) {
+            int r;
+            if ((r = check_mat_shape(d.shared_gate[l], d.shared_dff, D, "shared_gate", l)) ||
+                (r = check_mat_shape(d.shared_up[l], d.shared_dff, D, "shared_up", l)) ||
+                (r = check_mat_shape(d.shared_down[l], D, d.shared_dff, "shared_down", l)))
+                return r;
+        }
+    }
+    if (d.router_f32)
+        for (int64_t l = 0; l < d.layers; ++l)
+            if (!d.router_f32[l] || (uintptr_t)d.router_f32[l] % 16)
+                return model_fail(Q8_EINVAL, "router_f32[%lld]: null or not 16-byte aligned", (long long)l);
 
     q8_model* m = new q8_model();
     m->d = d;
@@ -448,13 +494,24 @@ int q8_model_create(const q8_model_desc* desc, q8_model** out) {
     m->down.assign(d.down, d.down + d.layers);
     m->kc.assign(d.k_cache, d.k_cache + d.layers);
     m->vc.assign(d.v_cache, d.v_cache + d.layers);
+    if (has_shared) {
+        m->sgate.assign(d.shared_gate, d.shared_gate + d.layers);
+        m->sup.assign(d.shared_up, d.shared_up + d.layers);
+        m->sdown.assign(d.shared_down, d.shared_down + d.layers);
+    } else {
+        m->d.shared_dff = 0;
+    }
+    if (d.router_f32) m->router_f32.assign(d.router_f32, d.router_f32 + d.layers);
+    m->d.router_f32 = nullptr;
+    m->d.shared_gate = m->d.shared_up = m->d.shared_down = nullptr;
     // pointers into the caller's arrays are not kept
     m->d.attn_norm = m->d.ffn_norm = m->d.q_norm = m->d.k_norm = nullptr;
     m->d.wq = m->d.wk = m->d.wv = m->d.wo = m->d.router = m->d.gate = m->d.up = m->d.down = nullptr;
     m->d.k_cache = m->d.v_cache = nullptr;
 
-    // one arena for the step's activations (sizes rounded to 256 B each)
-    const int64_t KF = d.k * d.dff;
+    // one arena for the step's activations (sizes rounded to 256 B each); the hidden rows hold the routed experts'
+    // rows and then the shared expert's
+    const int64_t KF = d.k * d.dff + (has_shared ? d.shared_dff : 0);
     const size_t half = (size_t)d.head_dim / 2;
     size_t need = 0;
     auto add = [&](size_t bytes) { need += (bytes + 255) & ~size_t(255); };
@@ -617,8 +674,10 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
     cudaStream_t st = (cudaStream_t)stream;
     // the chunk's rows, carved from the caller's workspace; every launch's own scratch comes after them
     Carve cb = workspace_carve(ws);
+    const bool rf = !m->router_f32.empty();
+    const int64_t SF = m->sgate.empty() ? 0 : d.shared_dff;  // the shared expert's hidden width (0: none)
     float* h = cb.take<float>((size_t)(R * D));
-    float* x = mode == 0 ? cb.take<float>((size_t)(R * D)) : nullptr;
+    float* x = (mode == 0 || rf) ? cb.take<float>((size_t)(R * D)) : nullptr;  // the f32 router reads f32 rows
     int8_t* xq = mode >= 1 ? cb.take<int8_t>((size_t)(R * D)) : nullptr;
     int8_t* xl = mode == 2 ? cb.take<int8_t>((size_t)(R * D)) : nullptr;
     float* xs = mode >= 1 ? cb.take<float>((size_t)(R * D / 32)) : nullptr;
@@ -637,10 +696,11 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
     plan.offsets = cb.take<int32_t>((size_t)E + 1);
     plan.lists = cb.take<int32_t>((size_t)(R * K));
     plan.active = cb.take<int32_t>((size_t)E + 1);
-    float* hm = cb.take<float>((size_t)(R * K * F));
-    int8_t* hmq = mode >= 1 ? cb.take<int8_t>((size_t)(R * K * F)) : nullptr;
-    int8_t* hml = mode == 2 ? cb.take<int8_t>((size_t)(R * K * F)) : nullptr;
-    float* hms = mode >= 1 ? cb.take<float>((size_t)(R * K * F / 32)) : nullptr;
+    const int64_t NH = R * K * F + R * SF;  // the routed hidden rows, then the shared expert's
+    float* hm = cb.take<float>((size_t)NH);
+    int8_t* hmq = mode >= 1 ? cb.take<int8_t>((size_t)NH) : nullptr;
+    int8_t* hml = mode == 2 ? cb.take<int8_t>((size_t)NH) : nullptr;
+    float* hms = mode >= 1 ? cb.take<float>((size_t)(NH / 32)) : nullptr;
     int32_t* posr = cb.take<int32_t>((size_t)R);
     int* done = cb.take_counters(1);
     if (cb.overflow) return model_fail(Q8_ENOSPACE, "prefill_chunk: workspace too small for %lld rows", (long long)R);
@@ -664,8 +724,8 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
         n.rows = rows;
         n.d = D;
         n.eps = d.eps;
-        if (mode == 0) n.y = x;
-        else {
+        n.y = x;  // f32 rows when the f32 mode or an f32 router reads them
+        if (mode != 0) {
             n.yq = xq;
             n.yl = xl;
             n.ys = xs;
@@ -735,18 +795,22 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
         }
         Q8_TRY(norm(h, m->ffn_norm[l], R));
         {
-            GemvCall g;
-            g.mode = mode;
-            g.k = D;
-            g.R = R;
-            g.seg[0] = GemvSeg{m->router[l].q, m->router[l].s, E, rlog, nullptr};
-            g.x = x;
-            g.xq = xq;
-            g.xl = xl;
-            g.xs = xs;
-            g.err = m->err;
-            Carve cv = cb;
-            Q8_TRY_WS(launch_gemv(g, cv, st), cv);
+            if (rf) {
+                Q8_TRY(launch_router_f32(m->router_f32[l], E, D, x, R, rlog, 0, st));
+            } else {
+                GemvCall g;
+                g.mode = mode;
+                g.k = D;
+                g.R = R;
+                g.seg[0] = GemvSeg{m->router[l].q, m->router[l].s, E, rlog, nullptr};
+                g.x = x;
+                g.xq = xq;
+                g.xl = xl;
+                g.xs = xs;
+                g.err = m->err;
+                Carve cv = cb;
+                Q8_TRY_WS(launch_gemv(g, cv, st), cv);
+            }
             TopkCall t;
             t.logits = rlog;
             t.R = R;
@@ -778,9 +842,16 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
             c.h = hm;
             c.plan = plan;
             c.err = m->err;
+            if (SF) {
+                c.sq0 = m->sgate[l].q;
+                c.ss0 = m->sgate[l].s;
+                c.sq1 = m->sup[l].q;
+                c.ss1 = m->sup[l].s;
+                c.sdff = SF;
+            }
             Carve cv = cb;
             Q8_TRY_WS(launch_gate_up(c, cv, st), cv);
-            if (mode >= 1) Q8_TRY(launch_quantize(hm, R * K * F, hmq, hms, st, hml));
+            if (mode >= 1) Q8_TRY(launch_quantize(hm, NH, hmq, hms, st, hml));
         }
         {
             ExpertCall c;
@@ -802,6 +873,11 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
             c.residual = h;  // h = h + mixture
             c.y = h;
             c.err = m->err;
+            if (SF) {
+                c.sq0 = m->sdown[l].q;
+                c.ss0 = m->sdown[l].s;
+                c.sdff = SF;
+            }
             Carve cv = cb;
             Q8_TRY_WS(launch_down_combine(c, cv, st), cv);
         }

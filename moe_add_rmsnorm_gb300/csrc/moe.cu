@@ -238,6 +238,42 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(const TopkParams p) 
     }
 }
 
+// ==== the f32 router ================================================================================================
+
+// A router of f32 values (lane_link.rs, Link::prim: Router::F32).  Warp e owns router row e and every activation row r:
+// lane l multiplies columns 4l .. 4l+3 of each 128-column stripe in f32 and adds the stripe's partial into an f64
+// accumulator; the warp's lanes are summed in f64.
+__global__ void __launch_bounds__(256) router_f32_kernel(const float* __restrict__ w, int E, int d,
+                                                         const float* __restrict__ x, int R, float* logits) {
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+    griddep_wait();
+    griddep_launch();
+    if (e >= E) return;
+    const float* wr = w + (int64_t)e * d;
+    for (int r = 0; r < R; ++r) {
+        const float* xr = x + (int64_t)r * d;
+        double acc = 0.0;
+        for (int c = 4 * lane; c < d; c += 128) {
+            const float4 wv = *reinterpret_cast<const float4*>(wr + c);
+            const float4 xv = *reinterpret_cast<const float4*>(xr + c);
+            const float part = fmaf(wv.w, xv.w, fmaf(wv.z, xv.z, fmaf(wv.y, xv.y, wv.x * xv.x)));
+            acc += (double)part;
+        }
+        acc = group_sum<32>(acc);
+        if (lane == 0) logits[(int64_t)r * E + e] = (float)acc;
+    }
+}
+
+// h[i] = silu(g[i]) * u[i] (the shared expert's gated pair, as the expert kernels form it).
+__global__ void __launch_bounds__(256) swiglu_kernel(const float* __restrict__ g, const float* __restrict__ u,
+                                                     float* __restrict__ h, int64_t n) {
+    griddep_wait();
+    griddep_launch();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        h[i] = silu_f32(g[i]) * u[i];
+}
+
 // ==== expert products =============================================================================================
 
 struct ExpertParams {
@@ -686,6 +722,8 @@ void gate_up_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
     *counters = c.hq_out ? (size_t)(c.R * c.K * (c.out_rows / 32)) : 0;
 }
 
+cudaError_t launch_down_routed(const ExpertCall& c, Carve& ws, cudaStream_t st);
+
 void down_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
     const bool one = down_row_supported(c) ||
                      (c.R == 1 && !c.plan.active && c.K <= 32 && down_one_smem(c) <= (size_t)DOWN_SMEM_MAX);
@@ -693,8 +731,78 @@ void down_scratch(const ExpertCall& c, size_t* bytes, size_t* counters) {
     *counters = 0;
 }
 
+cudaError_t launch_router_f32(const float* w, int64_t E, int64_t d, const float* x, int64_t R, float* logits,
+                              int pdl, cudaStream_t st) {
+    return launch(router_f32_kernel, dim3((unsigned)((E + 7) / 8)), dim3(256), 0, st, pdl, w, (int)E, (int)d, x,
+                  (int)R, logits);
+}
+
+namespace {
+
+// The shared expert's gated pair for the forms that do not fuse it: one two-segment projection (gate and up rows of
+// every activation row), then h = silu(g) * u into the hidden rows after the routed ones.
+cudaError_t shared_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
+    const int64_t n = c.R * c.sdff;
+    float* g = ws.take<float>((size_t)n);
+    float* u = ws.take<float>((size_t)n);
+    if (ws.overflow) return cudaErrorMemoryAllocation;
+    GemvCall pc;
+    pc.mode = c.mode;
+    pc.k = c.k;
+    pc.nseg = 2;
+    pc.seg[0] = GemvSeg{c.sq0, c.ss0, c.sdff, g, nullptr};
+    pc.seg[1] = GemvSeg{c.sq1, c.ss1, c.sdff, u, nullptr};
+    pc.x = c.x;
+    pc.xq = c.xq;
+    pc.xl = c.xl;
+    pc.xs = c.xs;
+    pc.R = c.R;
+    pc.err = c.err;
+    pc.pdl = c.pdl;
+    cudaError_t e = launch_gemv(pc, ws, st);
+    if (e != cudaSuccess) return e;
+    int grid = (int)((n + 255) / 256);
+    if (grid > device_info().sms * 4) grid = device_info().sms * 4;
+    return launch(swiglu_kernel, dim3(grid), dim3(256), 0, st, c.pdl, (const float*)g, (const float*)u,
+                  c.h + c.R * c.K * c.out_rows, n);
+}
+
+// The shared expert's down product for the forms that do not fuse it, added onto y (which already holds the residual
+// and the routed experts' weighted sum): y = y + Wd_s . h_s.
+cudaError_t shared_down(const ExpertCall& c, Carve& ws, cudaStream_t st) {
+    const int64_t off = c.R * c.K * c.k;  // the shared hidden rows follow the routed ones
+    GemvCall pc;
+    pc.mode = c.mode;
+    pc.k = c.sdff;
+    pc.seg[0] = GemvSeg{c.sq0, c.ss0, c.out_rows, c.y, c.y};
+    pc.R = c.R;
+    pc.err = c.err;
+    pc.pdl = c.pdl;
+    if (c.mode == 0) {
+        pc.x = c.x + off;
+    } else if (c.xq) {
+        pc.xq = c.xq + off;
+        pc.xl = c.xl ? c.xl + off : nullptr;
+        pc.xs = c.xs + off / 32;
+    } else {  // f32 hidden rows in an int8 mode: the shared rows quantized here
+        const int64_t n = c.R * c.sdff;
+        int8_t* q = ws.take<int8_t>((size_t)n);
+        int8_t* l = c.mode == 2 ? ws.take<int8_t>((size_t)n) : nullptr;
+        float* s = ws.take<float>((size_t)(n / 32));
+        if (ws.overflow) return cudaErrorMemoryAllocation;
+        cudaError_t e = launch_quantize(c.x + off, n, q, s, st, l);
+        if (e != cudaSuccess) return e;
+        pc.xq = q;
+        pc.xl = l;
+        pc.xs = s;
+    }
+    return launch_gemv(pc, ws, st);
+}
+
+}  // namespace
+
 cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
-    if (gate_row_supported(c)) return launch_gate_row(c, ws, st);
+    if (gate_row_supported(c)) return launch_gate_row(c, ws, st);  // the shared expert's rows are items of the kernel
     if (c.hq_out) return cudaErrorInvalidConfiguration;  // the int8 epilogue exists in the one-row kernel only
     // gate and up tiles are both in flight: about four (f32) or eight (int8) 32-byte loads per lane in all
     const EPlan pl = eplan(c.mode, (int)(c.k / 32), c.mode == 0 ? 2 : 4);
@@ -712,12 +820,19 @@ cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     cudaError_t e = c.mode == 0 ? run_gate_up<0>(c, pl, p, warps, st)
                   : c.mode == 1 ? run_gate_up<1>(c, pl, p, warps, st) : run_gate_up<2>(c, pl, p, warps, st);
     if (e == cudaSuccess && mma) e = launch_moe_mma(c, c.h, max_groups(c), ws, st);  // the groups of >= 16 choices
+    if (e == cudaSuccess && c.sdff) e = shared_gate_up(c, ws, st);
     return e;
 }
 
 cudaError_t launch_down_combine(const ExpertCall& c, Carve& ws, cudaStream_t st) {
+    if (down_row_supported(c)) return launch_down_row(c, st);  // the shared expert's blocks are pairs of the kernel
+    cudaError_t e = launch_down_routed(c, ws, st);
+    if (e == cudaSuccess && c.sdff) e = shared_down(c, ws, st);
+    return e;
+}
+
+cudaError_t launch_down_routed(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     const int nb = (int)(c.k / 32);
-    if (down_row_supported(c)) return launch_down_row(c, st);
     if (c.R == 1 && !c.plan.active && c.K <= 32 && down_one_smem(c) <= (size_t)DOWN_SMEM_MAX) {
         // one token: a warp per output row, its lane groups over the kept experts
         EPlan pl = eplan(c.mode, nb, 4);

@@ -290,7 +290,12 @@ struct GateRowParams {
     int8_t* hq;        // optional: h quantized per 32 rows [K][dff] (mode 2: with low words hl) and its scales
     int8_t* hl;        // [K][dff/32] (dff % 32 == 0)
     float* hs;
-    int* qcnt;         // [K*dff/32] arrivals per 32-row block (left zero)
+    int* qcnt;         // [(K*dff + sdff)/32] arrivals per 32-row block (left zero)
+    const int8_t* sgq; // a shared expert's gate and up [sdff][d] (sdff > 0): its rows are items K*dff.., its hidden
+    const float* sgs;  // rows follow the routed ones in h (and in the int8 forms)
+    const int8_t* suq;
+    const float* sus;
+    int sdff;
     L2Prefetch pf;
 };
 
@@ -303,7 +308,8 @@ __global__ void __launch_bounds__(GR_WPC * 32, 1) gate_row_kernel(const GateRowP
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int warp = blockIdx.x * GR_WPC + wid;
     const int W = gridDim.x * GR_WPC;
-    const int n = p.K * p.dff;
+    const int nk = p.K * p.dff;  // routed items; the shared expert's rows follow
+    const int n = nk + p.sdff;
     int bidx[BPL];
     bool bval[BPL];
 #pragma unroll
@@ -320,16 +326,19 @@ __global__ void __launch_bounds__(GR_WPC * 32, 1) gate_row_kernel(const GateRowP
         WTile<BPL, 1> tg[IPW], tu[IPW];
         int eid[IPW];  // every item's expert id read before any weight address depends on one
 #pragma unroll
-        for (int u = 0; u < IPW; ++u) eid[u] = it0 + u < n ? __ldcg(p.ids + (it0 + u) / p.dff) : -1;
+        for (int u = 0; u < IPW; ++u) eid[u] = it0 + u < nk ? __ldcg(p.ids + (it0 + u) / p.dff) : -1;
 #pragma unroll
         for (int u = 0; u < IPW; ++u) {
             const int it = it0 + u;
+            const bool sh = it >= nk && it < n;  // a row of the shared expert
             const int j = it / p.dff, i = it - j * p.dff;
             const int e = eid[u];
             const bool ev = e >= 0 && e < p.E;  // an id outside [0, E) counts as an expert of zero weights
-            const int64_t wrow = (int64_t)(ev ? e : 0) * p.dff + i;
-            load_tile<BPL, 1>(tg[u], p.gq, p.gs, wrow, ev ? 1 : 0, p.d, p.nb, bidx, bval);
-            load_tile<BPL, 1>(tu[u], p.uq, p.us, wrow, ev ? 1 : 0, p.d, p.nb, bidx, bval);
+            const int64_t wrow = sh ? (int64_t)(it - nk) : (int64_t)(ev ? e : 0) * p.dff + i;
+            load_tile<BPL, 1>(tg[u], sh ? p.sgq : p.gq, sh ? p.sgs : p.gs, wrow, (ev || sh) ? 1 : 0, p.d, p.nb, bidx,
+                              bval);
+            load_tile<BPL, 1>(tu[u], sh ? p.suq : p.uq, sh ? p.sus : p.us, wrow, (ev || sh) ? 1 : 0, p.d, p.nb, bidx,
+                              bval);
         }
 #pragma unroll
         for (int u = 0; u < IPW; ++u) {
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(GR_WPC * 32, 1) gate_row_kernel(const GateRowP
 
 template <int MODE, int BPL, int IPW>
 cudaError_t run_gate_row(const GateRowParams& p, cudaStream_t st, int pdl) {
-    const int n = p.K * p.dff;
+    const int n = p.K * p.dff + p.sdff;
     int grid = (n + GR_WPC * IPW - 1) / (GR_WPC * IPW);
     const int cap = device_info().sms;
     if (grid > cap) grid = cap;
@@ -405,6 +414,9 @@ struct DownRowParams {
     const float* hs;
     const float* residual;
     float* y;
+    const int8_t* sq;  // a shared expert's down [rows][sk] (sk > 0): its blocks are pairs K*nb.., gate 1, its hidden
+    const float* ss;   // row after the routed ones (value K*k + 32 b)
+    int sk;
     L2Prefetch pf;
 };
 
@@ -417,7 +429,8 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int o = blockIdx.x * (blockDim.x >> 5) + wid;
     const bool orow = o < p.rows;
-    const int P = p.K * p.nb;
+    const int PK = p.K * p.nb;     // routed pairs
+    const int P = PK + p.sk / 32;  // and the shared expert's blocks
     uint32_t w[PPL][8];
     float sw[PPL], g[PPL];
     int xo[PPL];  // the pair's first value in the hidden rows: j*k + 32*b
@@ -429,13 +442,18 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
 #pragma unroll
     for (int i = 0; i < PPL; ++i) {
         const int pi = lane + 32 * i;
-        const bool in = orow && pi < P;
+        const bool in = orow && pi < PK;
+        const bool sh = orow && pi >= PK && pi < P;  // a block of the shared expert
         const int j = in ? pi / p.nb : 0;
         const int b = in ? pi - j * p.nb : 0;
         const int e = in ? __ldg(p.ids + j) : -1;
-        xo[i] = j * p.k + 32 * b;
-        g[i] = in ? __ldg(p.gates + j) : 0.f;
-        if (e >= 0 && e < p.E) {  // an id outside [0, E) counts as an expert of zero weights
+        xo[i] = 32 * pi;  // = j*k + 32*b for a routed pair, K*k + 32*(pi - PK) for a shared block
+        g[i] = in ? __ldg(p.gates + j) : sh ? 1.f : 0.f;
+        if (sh) {
+            const int bs = pi - PK;
+            ld_block_stream(p.sq + (int64_t)o * p.sk + 32 * bs, w[i]);
+            sw[i] = ld_scale_stream(p.ss + (int64_t)o * (p.sk / 32) + bs);
+        } else if (e >= 0 && e < p.E) {  // an id outside [0, E) counts as an expert of zero weights
             const int64_t row = (int64_t)e * p.rows + o;
             ld_block_stream(p.q + row * p.k + 32 * b, w[i]);
             sw[i] = ld_scale_stream(p.s + row * p.nb + b);
@@ -451,7 +469,7 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
     const int8_t* hl = p.hl;
     const float* hs = p.hs;
     if (MODE == 0) {
-        for (int i = threadIdx.x; i < p.K * p.k / 4; i += blockDim.x)
+        for (int i = threadIdx.x; i < P * 8; i += blockDim.x)
             reinterpret_cast<float4*>(hsm)[i] = __ldcg(reinterpret_cast<const float4*>(p.h) + i);
         __syncthreads();
     } else if (!hq) {
@@ -491,7 +509,7 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
 #pragma unroll
     for (int i = 0; i < PPL; ++i) {
         const bool in = orow && lane + 32 * i < P;
-        if (MODE >= 1) {
+        if (MODE >= 1) {  // P words and scales: the routed pairs' hidden blocks, then the shared expert's
             uint32_t xw[8], xl[8];
             float xs = 0.f;
             if (in) {  // global (written by the previous launch) or this CTA's shared memory
@@ -535,8 +553,8 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
 template <int MODE, int PPL>
 cudaError_t run_down_row(const DownRowParams& p, int wpc, cudaStream_t st, int pdl) {
     auto kern = down_row_kernel<MODE, PPL>;
-    const size_t smem = MODE == 0 ? (size_t)p.K * p.k * sizeof(float)
-                        : p.hq ? 0 : (size_t)p.K * p.k * (MODE == 2 ? 2 : 1) + (size_t)p.K * p.k / 32 * 4 + 16;
+    const size_t vals = (size_t)p.K * p.k + p.sk;  // the hidden values the kernel reads
+    const size_t smem = MODE == 0 ? vals * sizeof(float) : p.hq ? 0 : vals * (MODE == 2 ? 2 : 1) + vals / 32 * 4 + 16;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -597,26 +615,27 @@ cudaError_t launch_route_row(const RouteRowCall& c, cudaStream_t st) {
 
 bool gate_row_supported(const ExpertCall& c) {
     return c.mode >= 1 && c.R == 1 && !c.plan.active && c.xq && c.xs && (c.mode == 1 || c.xl) && c.k % 32 == 0 &&
-           c.k / 32 <= 128 &&
+           c.k / 32 <= 128 && c.sdff % 32 == 0 && c.K * c.out_rows + c.sdff < (int64_t(1) << 31) &&
            c.K >= 1 && c.out_rows >= 1 && c.E * c.out_rows < (int64_t(1) << 31);
 }
 
 cudaError_t launch_gate_row(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     if (!gate_row_supported(c)) return cudaErrorInvalidConfiguration;
     GateRowParams p = {c.q0, c.s0, c.q1, c.s1, (int)c.E, (int)c.out_rows, (int)c.k, (int)(c.k / 32), c.K, c.ids,
-                       c.xq, c.xl, c.xs, c.h, nullptr, nullptr, nullptr, nullptr, c.pf};
+                       c.xq, c.xl, c.xs, c.h, nullptr, nullptr, nullptr, nullptr, c.sq0, c.ss0, c.sq1, c.ss1,
+                       (int)c.sdff, c.pf};
     if (c.hq_out) {
         if (c.out_rows % 32 || (c.mode == 2 && !c.hl_out)) return cudaErrorInvalidValue;
         p.hq = c.hq_out;
         p.hl = c.hl_out;
         p.hs = c.hs_out;
-        p.qcnt = ws.take_counters((size_t)(c.K * c.out_rows / 32));
+        p.qcnt = ws.take_counters((size_t)((c.K * c.out_rows + c.sdff) / 32));
         if (ws.overflow) return cudaErrorMemoryAllocation;
     }
     const int nb = (int)(c.k / 32);
     const int bpl = nb <= 32 ? 1 : nb <= 64 ? 2 : 4;
     // items per warp: enough that one pass covers every item on a grid of one CTA per SM, at most 6 blocks per lane
-    const int64_t n = (int64_t)c.K * c.out_rows;
+    const int64_t n = (int64_t)c.K * c.out_rows + c.sdff;
     const int64_t slots = (int64_t)device_info().sms * GR_WPC;
     int ipw = (int)((n + slots - 1) / slots);
     const int ipw_max = bpl == 4 ? 1 : 3;
@@ -625,17 +644,17 @@ cudaError_t launch_gate_row(const ExpertCall& c, Carve& ws, cudaStream_t st) {
 }
 
 bool down_row_supported(const ExpertCall& c) {
-    const bool act = c.mode == 0 ? (c.x != nullptr && (size_t)c.K * c.k * 4 <= 96 * 1024)
+    const bool act = c.mode == 0 ? (c.x != nullptr && (size_t)(c.K * c.k + c.sdff) * 4 <= 96 * 1024)
                                  : ((c.xq != nullptr && (c.mode == 1 || c.xl != nullptr)) || c.x != nullptr);
-    return c.R == 1 && !c.plan.active && !c.expert_out && act && c.k % 32 == 0 && c.K >= 1 &&
-           (int64_t)c.K * (c.k / 32) <= 32 * DR_MAXP;
+    return c.R == 1 && !c.plan.active && !c.expert_out && act && c.k % 32 == 0 && c.K >= 1 && c.sdff % 32 == 0 &&
+           (int64_t)c.K * (c.k / 32) + c.sdff / 32 <= 32 * DR_MAXP;
 }
 
 cudaError_t launch_down_row(const ExpertCall& c, cudaStream_t st) {
     if (!down_row_supported(c)) return cudaErrorInvalidConfiguration;
     DownRowParams p = {c.q0, c.s0, (int)c.E, (int)c.out_rows, (int)c.k, (int)(c.k / 32), c.K, c.ids, c.gates,
-                       c.x, c.xq, c.xl, c.xs, c.residual, c.y, c.pf};
-    const int ppl = (int)((c.K * (c.k / 32) + 31) / 32);
+                       c.x, c.xq, c.xl, c.xs, c.residual, c.y, c.sq0, c.ss0, (int)c.sdff, c.pf};
+    const int ppl = (int)((c.K * (c.k / 32) + c.sdff / 32 + 31) / 32);
     // one output row per warp, the rows spread over every SM
     const int sms = device_info().sms;
     int wpc = (int)((c.out_rows + sms - 1) / sms);

@@ -21,7 +21,8 @@ def layer_ids(l: int) -> dict:
     b = 1000 + 32 * l
     return dict(wq=b, wk=b + 1, wv=b + 2, wo=b + 3, router=b + 4, gate=b + 5, up=b + 6, down=b + 7,
                 attn_norm=VEC + b + 8, ffn_norm=VEC + b + 9, q_norm=VEC + b + 10, k_norm=VEC + b + 11,
-                k_cache=VEC + b + 12, v_cache=VEC + b + 13)
+                k_cache=VEC + b + 12, v_cache=VEC + b + 13, shared_gate=b + 14, shared_up=b + 15,
+                shared_down=b + 16, router_f32=VEC + b + 17)
 
 
 EMBED = VEC + 1
@@ -88,6 +89,22 @@ def decode_model(cfg: dict, seed: int = 0, alloc=_alloc_np, ptr=lambda a: a.ctyp
         out["down"].append(mat(E * d, dff, ids["down"]))
         out["k_cache"].append(vec((KV, ctx, hd), ids["k_cache"]))
         out["v_cache"].append(vec((KV, ctx, hd), ids["v_cache"]))
+    return out
+
+
+def mixture_variants(cfg: dict, seed: int = 0, shared_dff: int = 0, router_f32: bool = False, layers=None) -> dict:
+    """The optional mixture variants of a model, per layer: a shared expert of width ``shared_dff`` (gate/up
+    [shared_dff, d], down [d, shared_dff], Q8_0 as the experts) and routers of f32 values N(0,1) * 0.02 [E, d] (logits
+    of about unit spread at d = 2048)."""
+    L, d, E = cfg["layers"], cfg["d"], cfg["experts"]
+    out = {}
+    rng = range(L) if layers is None else layers
+    if shared_dff:
+        out["shared_gate"] = [q8_matrix(shared_dff, d, seed, layer_ids(l)["shared_gate"]) for l in rng]
+        out["shared_up"] = [q8_matrix(shared_dff, d, seed, layer_ids(l)["shared_up"]) for l in rng]
+        out["shared_down"] = [q8_matrix(d, shared_dff, seed, layer_ids(l)["shared_down"]) for l in rng]
+    if router_f32:
+        out["router_f32"] = [normal((E, d), seed, layer_ids(l)["router_f32"], mul=0.02) for l in rng]
     return out
 
 
