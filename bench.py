@@ -28,7 +28,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=128)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--mode", default="int8", choices=["int8", "f32"])
+    ap.add_argument("--mode", default="int8", choices=["int8", "f32", "int8x2"])
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
@@ -56,11 +56,14 @@ def dist_env():
 METRIC = "decode tokens/s and Q8_0 weight-stream GB/s (% of GB300 HBM peak), 1 GPU"
 
 
-def workload_config(cfg, mode_int8, world):
+MODE_NAMES = {0: "f32-activation/f64-sum", 1: "int8-activation", 2: "two-word int8-activation"}
+
+
+def workload_config(cfg, mode, world):
     """The `config` object of both arms' lines (the same workload, whichever implementation runs it)."""
     return {"workload": f"decode step, {cfg['layers']} layers d=2048 32q/4kv hd128 E=128 K=8 dff=768 vocab=151936 "
                         "ctx=4096 (full decode configuration), tg-style growing cache",
-            "mode": "int8-activation" if mode_int8 else "f32-activation/f64-sum",
+            "mode": MODE_NAMES[int(mode)],
             "l2": "inputs larger than L2: every step streams 3.42 GB of weights and ~0.8 GB of cache",
             "parallelism": "replicas" if world > 1 else "1 GPU"}
 
@@ -271,7 +274,7 @@ def run_reference(args):
     import oracle
     from synth import recipes
     cfg = dict(recipes.DECODE, layers=args.layers)
-    mode = 1 if args.mode == "int8" else 0
+    mode = {"int8": 1, "f32": 0, "int8x2": 2}[args.mode]
     host = recipes.decode_model(cfg, seed=0)
     om = oracle_model(cfg, host)
     threads = oracle.set_threads(oracle.host_cores())
@@ -292,7 +295,7 @@ def run_reference(args):
         "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "i8" if mode else "f32", "data": "synthetic",
-        "config": workload_config(cfg, mode == 1, 1),
+        "config": workload_config(cfg, mode, 1),
         "positions": [start_pos + args.warmup, cfg["ctx"] - 1],
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "host_cores": oracle.host_cores(),
                          "kind": "oracle",
@@ -557,6 +560,50 @@ def time_prefill(q8, model, cfg, tok, pos, stream, rows=(16, 64), reps=3):
     return out
 
 
+def time_batch(q8, cfg, dev, stream, mode, batches=(2, 4, 8), steps=8, warmup=3):
+    """The batch form: B sequences per step through the whole model (one captured graph), each with its own f32 cache
+    of the full length (seeded N(0,1), generated on the device) at positions ctx - steps - warmup .. ctx - 1.
+    tokens/s = B / time per step; weight bytes per step count every dense matrix and the LM head once and the experts
+    the sequences' routing touched at every layer (estimated from uniform routing as E (1 - (1 - K/E)^B))."""
+    import torch
+    L, d, E, K, dff = cfg["layers"], cfg["d"], cfg["experts"], cfg["k"], cfg["dff"]
+    H, KV, HD, ctx = cfg["heads"], cfg["kv_heads"], cfg["hd"], cfg["ctx"]
+    dense = (H * HD + 2 * KV * HD) * d + d * H * HD + E * d
+    expert = 3 * dff * d
+    s = torch.cuda.ExternalStream(stream)
+    out = []
+    for B in batches:
+        with torch.cuda.stream(s):
+            gen = torch.Generator(device="cuda")
+            gen.manual_seed(100 + B)
+            t = dict(dev)
+            t["k_cache"] = [torch.randn(B, KV, ctx, HD, device="cuda", generator=gen) for _ in range(L)]
+            t["v_cache"] = [torch.randn(B, KV, ctx, HD, device="cuda", generator=gen) for _ in range(L)]
+            tok = torch.randint(0, cfg["vocab"], (B,), dtype=torch.int32, device="cuda", generator=gen)
+            pos = torch.full((B,), ctx - steps - warmup, dtype=torch.int32, device="cuda")
+            logits = torch.empty(B, cfg["vocab"], device="cuda")
+            m = q8.Model(dict(cfg, batch=B), t, mode, tok, pos, logits)
+            for _ in range(warmup):
+                m.step(stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.synchronize()
+            e0.record(s)
+            for _ in range(steps):
+                m.step(stream)
+            e1.record(s)
+            e1.synchronize()
+            m.check(stream)
+            sec = e0.elapsed_time(e1) / 1e3 / steps
+            u = E * (1.0 - (1.0 - K / E) ** B)
+            wbytes = (L * (dense + u * expert) + cfg["vocab"] * d) * 9 // 8
+            out.append({"batch": B, "tokens_per_s": B / sec, "ms_per_step": sec * 1e3, "weight_gbs": wbytes / sec / 1e9,
+                        "unique_experts_per_layer_est": u, "launches_per_step": m.launches_per_step()})
+            m.close()
+            del t, m
+            torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -572,7 +619,7 @@ def main():
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     cfg = dict(recipes.DECODE, layers=args.layers)
-    mode = q8.INT8ACT if args.mode == "int8" else q8.F32ACT_F64SUM
+    mode = {"int8": q8.INT8ACT, "f32": q8.F32ACT_F64SUM, "int8x2": q8.INT8ACT2}[args.mode]
     host, dev = make_model_tensors(cfg, seed=0)
     total = args.warmup + args.steps
     start_pos = cfg["ctx"] - total
@@ -666,8 +713,8 @@ def main():
         "metric": METRIC, "value": value,
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "i8" if mode == q8.INT8ACT else "f32", "data": "synthetic",
-        "config": workload_config(cfg, mode == q8.INT8ACT, world),
+        "dtype": "f32" if mode == q8.F32ACT_F64SUM else "i8", "data": "synthetic",
+        "config": workload_config(cfg, mode, world),
         "positions": [start_pos + args.warmup, cfg["ctx"] - 1],
         "weight_stream": {"gbs": weight_gbs, "frac_of_peak": weight_gbs / peak, "bytes_per_token": wbytes,
                           "peak_gbs": peak, "peak_kind": peak_kind},
@@ -687,22 +734,31 @@ def main():
                             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
                             "us_per_launch": dom_sec * 1e6, "algorithmic_bytes_per_launch": dom_bytes}
         if not args.no_secondary:
-            other = q8.F32ACT_F64SUM if mode == q8.INT8ACT else q8.INT8ACT
-            m2 = q8.Model(cfg, dev, other, tok, pos, logits)
-            pos.fill_(cfg["ctx"] - total)
-            with torch.cuda.stream(stream):
-                for _ in range(args.warmup):
-                    m2.step(sh)
-                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a0.record(stream)
-                for _ in range(args.steps):
-                    m2.step(sh)
-                a1.record(stream)
-                a1.synchronize()
-            s2 = a0.elapsed_time(a1) / 1e3
-            line["secondary"] = {"mode": "f32-activation/f64-sum" if other == q8.F32ACT_F64SUM else "int8-activation",
-                                 "tokens_per_s": args.steps / s2, "weight_stream_gbs": wbytes * args.steps / s2 / 1e9}
-            m2.close()
+            names = {q8.F32ACT_F64SUM: "f32-activation/f64-sum", q8.INT8ACT: "int8-activation",
+                     q8.INT8ACT2: "two-word int8-activation"}
+            line["secondary"] = []
+            for other in (q8.INT8ACT2, q8.F32ACT_F64SUM, q8.INT8ACT):
+                if other == mode:
+                    continue
+                m2 = q8.Model(cfg, dev, other, tok, pos, logits)
+                pos.fill_(cfg["ctx"] - total)
+                with torch.cuda.stream(stream):
+                    for _ in range(args.warmup):
+                        m2.step(sh)
+                    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a0.record(stream)
+                    for _ in range(args.steps):
+                        m2.step(sh)
+                    a1.record(stream)
+                    a1.synchronize()
+                s2 = a0.elapsed_time(a1) / 1e3
+                line["secondary"].append({"mode": names[other], "tokens_per_s": args.steps / s2,
+                                          "weight_stream_gbs": wbytes * args.steps / s2 / 1e9,
+                                          "frac_of_peak": wbytes * args.steps / s2 / 1e9 / peak})
+                m2.check(sh)
+                m2.close()
+            line["batch"] = {"what": "the batch form: B sequences per step, every weight read once for all of them, "
+                                     "one CUDA graph per step, int8 mode", "results": time_batch(q8, cfg, dev, sh, mode)}
             line["prefill"] = {"what": "prefill_chunk through all layers (plain launches), positions ctx-128-R ..",
                                "results": time_prefill(q8, model, cfg, tok, pos, sh)}
             line["chunks"] = {
@@ -713,7 +769,7 @@ def main():
                                           rows=(16, 32, 64))}
             line["configs"] = time_configs(q8, cfg, dev, sh, peak)
         if not args.no_cpu_baseline:
-            cb, cores = cpu_baseline_oracle(cfg, host, 1 if mode == q8.INT8ACT else 0, 0, cfg["ctx"] - 1)
+            cb, cores = cpu_baseline_oracle(cfg, host, int(mode), 0, cfg["ctx"] - 1)
             allc, one = cb["all_cores"], cb["single_thread"]
             line["cpu_baseline"] = {"value": allc["tokens_per_s"], "unit": "tokens/s", "cores": allc["threads"],
                                     "host_cores": cores, "kind": "oracle",

@@ -236,6 +236,10 @@ typedef struct {
     const float *const *router_f32;  /* [layers] -> device f32 [E][d] routers of values used in place of `router` */
     const q8_mat *shared_gate, *shared_up, *shared_down;  /* [layers]: a shared expert, [shared_dff, d] x 2, [d, shared_dff] */
     int64_t shared_dff;
+    /* The batch form (lane/mod.rs: Form / FormKind::Batch, batch_io): `batch` sequences (0 or 1: one) step together,
+     * every weight read once for all of them.  Then tok and pos are device int32 [batch], logits [batch][vocab], and
+     * each layer's cache holds the sequences' caches one after another: [batch][kv_heads][ctx][head_dim]. */
+    int64_t batch;
 } q8_model_desc;
 
 typedef struct q8_model q8_model;
@@ -245,8 +249,11 @@ typedef struct q8_model q8_model;
 Q8_API int q8_model_create(const q8_model_desc *desc, q8_model **model);
 Q8_API void q8_model_destroy(q8_model *model);
 
-/* One token: reads *tok and *pos on the device, writes the new key/value rows at *pos, the logits (if requested) and the
- * next token into *tok, and advances *pos.  The first call on a model captures the whole step as one CUDA graph on a
+/* One token (one per sequence in the batch form): reads *tok and *pos on the device, writes the new key/value rows at
+ * *pos, the logits (if requested) and the next token into *tok, and advances *pos.  In the batch form sequence b reads
+ * tok[b] and pos[b] and attends its own cache; its norms, projections, routing and experts run as rows of one chunk
+ * (each expert's weights read once for every sequence that chose it), and a bad position anywhere leaves every
+ * sequence's token and position unchanged.  The first call on a model captures the whole step as one CUDA graph on a
  * private capture of `stream`; every call then replays it on `stream` (qwen_emit docs: one captured graph replayed per
  * token, position and token in device memory).  The first call must not be made while `stream` is capturing.  A step
  * whose *pos is outside [0, ctx) writes nothing and leaves *tok and *pos unchanged (the error is counted in the
@@ -254,7 +261,8 @@ Q8_API void q8_model_destroy(q8_model *model);
 Q8_API int decode_step(q8_model *model, q8_stream stream);
 /* The same step as plain launches, without a graph (for tests and graph-capture by the caller). */
 Q8_API int decode_step_launches(q8_model *model, q8_stream stream);
-/* Debug export: decode_step_launches that also copies the residual stream into hidden (device f32 [layers + 1][d]):
+/* Debug export (one sequence only): decode_step_launches that also copies the residual stream into hidden (device f32
+ * [layers + 1][d]):
  * row 0 is the stream entering the first layer (the token's embedding row), row l + 1 the stream leaving layer l
  * (after its attention and mixture sums).  Per layer the step's results are those of decode_step; the copies are
  * ordinary stream operations between the launches.  For parity checks of each layer against a reference fed the same
@@ -269,7 +277,7 @@ Q8_API int decode_step_trace(q8_model *model, float *hidden, q8_stream stream);
  * order of the multi-row kernels).  The chunk's activations and every launch's scratch come from `ws` (Q8_ENOSPACE if
  * too small; about 0.7 MB a row at d 2048, 32 heads of 128 and a 4096-row cache); plain launches on `stream`, no
  * graph.  An id outside [0, vocab) or a row past the cache end sets the
- * model's device error word (q8_model_check). */
+ * model's device error word (q8_model_check).  Not for the batch form. */
 Q8_API int prefill_chunk(q8_model *model, const int32_t *tokens, int64_t rows, q8_ws *ws, q8_stream stream);
 /* Kernels one step launches: the kernel nodes of the graph the first decode_step captured (0 before it). */
 Q8_API int64_t q8_model_launches_per_step(const q8_model *model);

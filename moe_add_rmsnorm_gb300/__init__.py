@@ -59,7 +59,7 @@ class q8_model_desc(ctypes.Structure):
         ("lm_head", q8_mat), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
         ("tok", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("logits", ctypes.c_void_p),
         ("router_f32", ctypes.c_void_p), ("shared_gate", ctypes.c_void_p), ("shared_up", ctypes.c_void_p),
-        ("shared_down", ctypes.c_void_p), ("shared_dff", ctypes.c_int64)]
+        ("shared_down", ctypes.c_void_p), ("shared_dff", ctypes.c_int64), ("batch", ctypes.c_int64)]
 
 
 _vp, _i64, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -261,6 +261,8 @@ class Model:
         for key in ("layers", "d", "heads", "kv_heads", "experts", "k", "dff", "vocab", "ctx"):
             setattr(d, key, int(cfg[key]))
         d.head_dim = int(cfg["hd"])
+        d.batch = int(cfg.get("batch", 0))  # the batch form: tok, pos [batch], logits [batch, vocab], caches per layer
+                                            # [batch, kv, ctx, hd]
         d.eps = float(cfg["eps"])
         d.rope_theta = float(cfg["rope_theta"])
         d.mode = int(mode)

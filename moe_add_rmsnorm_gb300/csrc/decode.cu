@@ -64,8 +64,28 @@ struct AttnParams {
     int* cnt;      // [kv * G]
     int nch_max;
     int ncl_max;
+    int64_t cache_stride;  // batch form: the next sequence's caches (its q/k/v/out rows, position, scratch follow theirs)
     L2Prefetch pf;
 };
+
+// The batch form's sequence b (blockIdx.z): its rows, caches, position, outputs and fold scratch.
+__device__ __forceinline__ AttnParams attn_for_sequence(const AttnParams& p0, int b) {
+    AttnParams p = p0;
+    const int64_t qd = (int64_t)p0.heads * ATT_HD, kd = (int64_t)p0.kv * ATT_HD;
+    p.q += b * qd;
+    p.k += b * kd;
+    p.v += b * kd;
+    p.k_cache += b * p0.cache_stride;
+    p.v_cache += b * p0.cache_stride;
+    p.pos += b;
+    p.out += b * qd;
+    if (p.outq) p.outq += b * qd;
+    if (p.outl) p.outl += b * qd;
+    if (p.outs) p.outs += b * qd / 32;
+    p.part += (int64_t)b * p0.heads * p0.ncl_max * (ATT_HD + 2);
+    p.cnt += (int64_t)b * p0.heads;
+    return p;
+}
 
 // A chunk's partial: per query head its weighted values (ATT_HD), its max score and its sum of exponentials.
 __shared__ __align__(16) float att_partial[ATT_MAXG][ATT_HD + 2];
@@ -184,7 +204,9 @@ __device__ void fold_cluster(const AttnParams& p, int g, int chunk, int G, int t
 // each), each warp 8 positions.  Values: warp w takes positions w, w+8, ... (8 rows), lane l the dims 4l..4l+3; every
 // key and value row is loaded before any is used; the 8 warps' sums meet in shared memory.  A chunk's partial
 // is then folded with the rest of its cluster and across clusters (fold_cluster), always in chunk order.
-__global__ void __launch_bounds__(ATT_THREADS, 2) attention_kernel(const AttnParams p) {
+template <bool BATCH>
+__global__ void __launch_bounds__(ATT_THREADS, 2) attention_kernel(const AttnParams pk) {
+    const AttnParams p = BATCH ? attn_for_sequence(pk, blockIdx.z) : pk;
     __shared__ __align__(16) float qs[ATT_MAXG][4 * ATT_QP];
     __shared__ __align__(16) float sc[ATT_MAXG][ATT_CHUNK];
     __shared__ __align__(16) float red[ATT_THREADS / 32][ATT_MAXG][ATT_HD];  // [warp][g][dim]; float4 stores
@@ -822,8 +844,9 @@ __global__ void pos_add_kernel(int32_t* pos, int add, const int* err) {
 
 void attention_scratch(const AttnCall& c, size_t* bytes, size_t* counters) {
     const int G = c.heads / c.kv;
-    *bytes = (size_t)c.kv * G * (attn_chunks(c.ctx) / ATT_CLUSTER) * (ATT_HD + 2) * sizeof(float);
-    *counters = (size_t)c.kv * G;
+    const int B = c.batch > 1 ? c.batch : 1;
+    *bytes = (size_t)B * c.kv * G * (attn_chunks(c.ctx) / ATT_CLUSTER) * (ATT_HD + 2) * sizeof(float);
+    *counters = (size_t)B * c.kv * G;
 }
 
 cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
@@ -851,14 +874,16 @@ cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
     p.outs = c.outs;
     p.nch_max = attn_chunks(c.ctx);
     p.ncl_max = p.nch_max / ATT_CLUSTER;
+    p.cache_stride = c.cache_stride;
     p.pf = c.pf;
     size_t bytes = 0, cnt = 0;
     attention_scratch(c, &bytes, &cnt);
     p.part = ws.take<float>(bytes / sizeof(float));
     p.cnt = ws.take_counters(cnt);
     if (ws.overflow) return cudaErrorMemoryAllocation;
+    const int B = c.batch > 1 ? c.batch : 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(c.kv, p.nch_max);
+    cfg.gridDim = dim3(c.kv, p.nch_max, B);
     cfg.blockDim = dim3(ATT_THREADS);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -874,7 +899,7 @@ cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, attention_kernel, p);
+    return B > 1 ? cudaLaunchKernelEx(&cfg, attention_kernel<true>, p) : cudaLaunchKernelEx(&cfg, attention_kernel<false>, p);
 }
 
 void argmax_scratch(const ArgmaxCall& c, size_t* bytes, size_t* counters) {

@@ -251,6 +251,10 @@ struct AttnCall {
     int8_t* outl = nullptr;         // with outq: the two-word form's low words
     float* outs = nullptr;
     int* err = nullptr;             // bit 2 set for a position outside [0, ctx)
+    // batch form: `batch` sequences, sequence b's rows at b * (heads or kv) * hd, caches at b * cache_stride, position
+    // pos[b], outputs at b * heads * hd
+    int batch = 1;
+    int64_t cache_stride = 0;
     L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };

@@ -44,6 +44,8 @@ struct q8_model {
     int8_t *xl = nullptr, *attl = nullptr, *hl = nullptr;  // the two-word mode's low words
     float *xs = nullptr, *atts = nullptr, *hs = nullptr;
     int32_t* ids = nullptr;
+    PlanPtrs plan;                 // batch form: the sequences' choices grouped by expert
+    int64_t B = 1;                 // sequences per step
     int* err = nullptr;
     char* ws = nullptr;
     size_t ws_bytes = 0;
@@ -397,6 +399,224 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
     return cudaSuccess;
 }
 
+// The batch form's step (lane/mod.rs: FormKind::Batch): the sequences are the rows of one chunk for every norm,
+// projection and the mixture (each weight read once for all of them, each chosen expert once for the sequences that
+// chose it), and each attends its own cache at its own position.  Plain launches in order.
+cudaError_t batch_step_launches(q8_model* m, cudaStream_t st) {
+    const q8_model_desc& d = m->d;
+    const int mode = (int)d.mode;
+    const int64_t B = m->B, D = d.d, H = d.heads, KV = d.kv_heads, HD = d.head_dim, E = d.experts, K = d.k, F = d.dff;
+    const bool rf = !m->router_f32.empty();
+    const int64_t SF = m->sgate.empty() ? 0 : d.shared_dff;
+    cudaError_t e = cudaSuccess;
+#define Q8_TRY(x)                       \
+    do {                                \
+        e = (x);                        \
+        if (e != cudaSuccess) return e; \
+    } while (0)
+    auto norm = [&](const float* a, const int32_t* a_row, const float* w, float* sum) {
+        NormCall n;
+        n.a = a;
+        n.a_row = a_row;
+        n.a_rows = d.vocab;
+        n.w = w;
+        n.rows = B;
+        n.d = D;
+        n.eps = d.eps;
+        n.sum = sum;
+        if (mode == 0 || rf) n.y = m->x;
+        if (mode != 0) {
+            n.yq = m->xq;
+            n.yl = m->xl;
+            n.ys = m->xs;
+        }
+        n.err = m->err;
+        return launch_add_rmsnorm(n, st);
+    };
+    for (int64_t l = 0; l < d.layers; ++l) {
+        // the first layer gathers each sequence's embedding row into its residual row
+        Q8_TRY(norm(l == 0 ? d.embed : m->h, l == 0 ? d.tok : nullptr, m->attn_norm[l], l == 0 ? m->h : nullptr));
+        {
+            GemvCall g;
+            g.mode = mode;
+            g.k = D;
+            g.R = B;
+            g.nseg = 3;
+            g.seg[0] = GemvSeg{m->wq[l].q, m->wq[l].s, H * HD, m->q, nullptr};
+            g.seg[1] = GemvSeg{m->wk[l].q, m->wk[l].s, KV * HD, m->k, nullptr};
+            g.seg[2] = GemvSeg{m->wv[l].q, m->wv[l].s, KV * HD, m->v, nullptr};
+            g.x = m->x;
+            g.xq = m->xq;
+            g.xl = m->xl;
+            g.xs = m->xs;
+            g.err = m->err;
+            Carve cv = fresh_carve(m);
+            Q8_TRY(launch_gemv(g, cv, st));
+        }
+        {
+            AttnCall a;
+            a.q = m->q;
+            a.k = m->k;
+            a.v = m->v;
+            a.q_norm = m->q_norm[l];
+            a.k_norm = m->k_norm[l];
+            a.cos_t = m->cos_t;
+            a.sin_t = m->sin_t;
+            a.eps = d.eps;
+            a.err = m->err;
+            a.k_cache = m->kc[l];
+            a.v_cache = m->vc[l];
+            a.pos = d.pos;
+            a.heads = (int)H;
+            a.kv = (int)KV;
+            a.hd = (int)HD;
+            a.ctx = (int)d.ctx;
+            a.out = m->att;
+            if (mode >= 1) {
+                a.outq = m->attq;
+                a.outl = m->attl;
+                a.outs = m->atts;
+            }
+            a.batch = (int)B;
+            a.cache_stride = KV * d.ctx * HD;
+            Carve cv = fresh_carve(m);
+            Q8_TRY(launch_attention(a, cv, st));
+        }
+        {
+            GemvCall g;
+            g.mode = mode;
+            g.k = H * HD;
+            g.R = B;
+            g.seg[0] = GemvSeg{m->wo[l].q, m->wo[l].s, D, m->h, m->h};  // h = h + o
+            g.x = m->att;
+            g.xq = m->attq;
+            g.xl = m->attl;
+            g.xs = m->atts;
+            g.err = m->err;
+            Carve cv = fresh_carve(m);
+            Q8_TRY(launch_gemv(g, cv, st));
+        }
+        Q8_TRY(norm(m->h, nullptr, m->ffn_norm[l], nullptr));
+        if (rf) {
+            Q8_TRY(launch_router_f32(m->router_f32[l], E, D, m->x, B, m->rlog, 0, st));
+        } else {
+            GemvCall g;
+            g.mode = mode;
+            g.k = D;
+            g.R = B;
+            g.seg[0] = GemvSeg{m->router[l].q, m->router[l].s, E, m->rlog, nullptr};
+            g.x = m->x;
+            g.xq = m->xq;
+            g.xl = m->xl;
+            g.xs = m->xs;
+            g.err = m->err;
+            Carve cv = fresh_carve(m);
+            Q8_TRY(launch_gemv(g, cv, st));
+        }
+        {
+            Carve cv = fresh_carve(m);
+            TopkCall t;
+            t.logits = m->rlog;
+            t.R = B;
+            t.E = E;
+            t.K = (int)K;
+            t.ids = m->ids;
+            t.gates = m->gates;
+            t.plan = m->plan;
+            t.done = cv.take_counters(1);
+            Q8_TRY(launch_topk(t, st));
+        }
+        {
+            ExpertCall c;
+            c.mode = mode;
+            c.q0 = m->gate[l].q;
+            c.s0 = m->gate[l].s;
+            c.q1 = m->up[l].q;
+            c.s1 = m->up[l].s;
+            c.E = E;
+            c.out_rows = F;
+            c.k = D;
+            c.R = B;
+            c.K = (int)K;
+            c.ids = m->ids;
+            c.x = m->x;
+            c.xq = m->xq;
+            c.xl = m->xl;
+            c.xs = m->xs;
+            c.h = m->hbuf;
+            c.plan = m->plan;
+            c.err = m->err;
+            if (SF) {
+                c.sq0 = m->sgate[l].q;
+                c.ss0 = m->sgate[l].s;
+                c.sq1 = m->sup[l].q;
+                c.ss1 = m->sup[l].s;
+                c.sdff = SF;
+            }
+            Carve cv = fresh_carve(m);
+            Q8_TRY(launch_gate_up(c, cv, st));
+            if (mode >= 1) Q8_TRY(launch_quantize(m->hbuf, B * (K * F + SF), m->hq, m->hs, st, m->hl));
+        }
+        {
+            ExpertCall c;
+            c.mode = mode;
+            c.q0 = m->down[l].q;
+            c.s0 = m->down[l].s;
+            c.E = E;
+            c.out_rows = D;
+            c.k = F;
+            c.R = B;
+            c.K = (int)K;
+            c.ids = m->ids;
+            c.gates = m->gates;
+            c.x = mode >= 1 ? nullptr : m->hbuf;
+            c.xq = m->hq;
+            c.xl = m->hl;
+            c.xs = m->hs;
+            c.plan = m->plan;
+            c.err = m->err;
+            if (SF) {
+                c.sq0 = m->sdown[l].q;
+                c.ss0 = m->sdown[l].s;
+                c.sdff = SF;
+            }
+            c.residual = m->h;  // h = h + mixture
+            c.y = m->h;
+            Carve cv = fresh_carve(m);
+            Q8_TRY(launch_down_combine(c, cv, st));
+        }
+    }
+    // each sequence's final norm, LM head row and greedy token
+    Q8_TRY(norm(m->h, nullptr, d.final_norm, nullptr));
+    {
+        GemvCall g;
+        g.mode = mode;
+        g.k = D;
+        g.R = B;
+        g.seg[0] = GemvSeg{d.lm_head.q, d.lm_head.s, d.vocab, m->logits, nullptr};
+        g.x = m->x;
+        g.xq = m->xq;
+        g.xl = m->xl;
+        g.xs = m->xs;
+        g.err = m->err;
+        Carve cv = fresh_carve(m);
+        Q8_TRY(launch_gemv(g, cv, st));
+    }
+    for (int64_t b = 0; b < B; ++b) {
+        ArgmaxCall a;
+        a.x = m->logits + b * d.vocab;
+        a.n = d.vocab;
+        a.tok = d.tok + b;
+        a.pos = d.pos + b;
+        a.err = m->err;
+        a.ctx = (int)d.ctx;
+        Carve cv = fresh_carve(m);
+        Q8_TRY(launch_argmax(a, cv, st));
+    }
+#undef Q8_TRY
+    return cudaSuccess;
+}
+
 // A wait that is bound to give up: one thread waits on a barrier that nothing arrives on, at most `polls` polls, and
 // records the timeout in the error word as every pipeline wait of the step does.
 __global__ void wait_selftest_kernel(int* err, unsigned polls) {
@@ -439,6 +659,8 @@ int q8_model_create(const q8_model_desc* desc, q8_model** out) {
     if (d.experts > 8192) return model_fail(Q8_EUNSUPPORTED, "%lld experts: at most 8192", (long long)d.experts);
     if (d.ctx > (1 << 24) || d.vocab > (1 << 30)) return model_fail(Q8_EUNSUPPORTED, "ctx or vocab past the index range");
     if (!(d.eps >= 0.f) || !(d.rope_theta > 0.0)) return model_fail(Q8_EINVAL, "eps or rope_theta out of range");
+    if (d.batch < 0 || d.batch > 64) return model_fail(Q8_EUNSUPPORTED, "batch %lld: 1 to 64 sequences", (long long)d.batch);
+    if (d.batch > 1 && d.batch * d.k > 65536) return model_fail(Q8_EUNSUPPORTED, "batch * k: too many choices");
     if (!d.embed || !d.final_norm || !d.tok || !d.pos) return model_fail(Q8_EINVAL, "embed, final_norm, tok or pos: null");
     if (!d.attn_norm || !d.ffn_norm || !d.q_norm || !d.k_norm || !d.wq || !d.wk || !d.wv || !d.wo || !d.router ||
         !d.gate || !d.up || !d.down || !d.k_cache || !d.v_cache)
@@ -509,34 +731,36 @@ int q8_model_create(const q8_model_desc* desc, q8_model** out) {
     m->d.wq = m->d.wk = m->d.wv = m->d.wo = m->d.router = m->d.gate = m->d.up = m->d.down = nullptr;
     m->d.k_cache = m->d.v_cache = nullptr;
 
-    // one arena for the step's activations (sizes rounded to 256 B each); the hidden rows hold the routed experts'
-    // rows and then the shared expert's
-    const int64_t KF = d.k * d.dff + (has_shared ? d.shared_dff : 0);
+    // one arena for the step's activations, a row each per sequence (sizes rounded to 256 B each); the hidden rows
+    // hold the routed experts' rows and then the shared expert's
+    const int64_t B = d.batch > 1 ? d.batch : 1;
+    const int64_t KF = B * (d.k * d.dff + (has_shared ? d.shared_dff : 0));
     const size_t half = (size_t)d.head_dim / 2;
     size_t need = 0;
     auto add = [&](size_t bytes) { need += (bytes + 255) & ~size_t(255); };
-    add(D * 4);          // h
-    add(D * 4);          // x
-    add(QD * 4);         // q
-    add(KD * 4);         // k
-    add(KD * 4);         // v
-    add(QD * 4);         // att
-    add(d.logits ? 0 : d.vocab * 4);
+    add(B * D * 4);          // h
+    add(B * D * 4);          // x
+    add(B * QD * 4);         // q
+    add(B * KD * 4);         // k
+    add(B * KD * 4);         // v
+    add(B * QD * 4);         // att
+    add(d.logits ? 0 : B * d.vocab * 4);
     add(d.ctx * half * 4);  // cos
     add(d.ctx * half * 4);  // sin
     add(KF * 4);         // hbuf
-    add(d.k * 4);        // gates
-    add(d.experts * 4);  // router logits
-    add(D);              // xq
-    add(D / 32 * 4);     // xs
-    add(QD);             // attq
-    add(QD / 32 * 4);    // atts
+    add(B * d.k * 4);        // gates
+    add(B * d.experts * 4);  // router logits
+    add(B * D);              // xq
+    add(B * D / 32 * 4);     // xs
+    add(B * QD);             // attq
+    add(B * QD / 32 * 4);    // atts
     add(KF);             // hq
     add(KF / 32 * 4);    // hs
-    add(D);              // xl
-    add(QD);             // attl
+    add(B * D);              // xl
+    add(B * QD);             // attl
     add(KF);             // hl
-    add(d.k * 4);        // ids
+    add(B * d.k * 4);        // ids
+    add(d.experts * 4 + (d.experts + 1) * 4 * 2 + B * d.k * 4 + 1024);  // the batch form's grouping
     add(256);            // err
     need += 4096;
     cudaError_t e = cudaMalloc(&m->arena, need);
@@ -546,28 +770,33 @@ int q8_model_create(const q8_model_desc* desc, q8_model** out) {
     }
     m->arena_bytes = need;
     char* at = m->arena;
-    m->h = carve_arena<float>(at, D);
-    m->x = carve_arena<float>(at, D);
-    m->q = carve_arena<float>(at, QD);
-    m->k = carve_arena<float>(at, KD);
-    m->v = carve_arena<float>(at, KD);
-    m->att = carve_arena<float>(at, QD);
-    m->logits = d.logits ? d.logits : carve_arena<float>(at, d.vocab);
+    m->B = B;
+    m->h = carve_arena<float>(at, B * D);
+    m->x = carve_arena<float>(at, B * D);
+    m->q = carve_arena<float>(at, B * QD);
+    m->k = carve_arena<float>(at, B * KD);
+    m->v = carve_arena<float>(at, B * KD);
+    m->att = carve_arena<float>(at, B * QD);
+    m->logits = d.logits ? d.logits : carve_arena<float>(at, B * d.vocab);
     m->cos_t = carve_arena<float>(at, d.ctx * half);
     m->sin_t = carve_arena<float>(at, d.ctx * half);
     m->hbuf = carve_arena<float>(at, KF);
-    m->gates = carve_arena<float>(at, d.k);
-    m->rlog = carve_arena<float>(at, d.experts);
-    m->xq = carve_arena<int8_t>(at, D);
-    m->xs = carve_arena<float>(at, D / 32);
-    m->attq = carve_arena<int8_t>(at, QD);
-    m->atts = carve_arena<float>(at, QD / 32);
+    m->gates = carve_arena<float>(at, B * d.k);
+    m->rlog = carve_arena<float>(at, B * d.experts);
+    m->xq = carve_arena<int8_t>(at, B * D);
+    m->xs = carve_arena<float>(at, B * D / 32);
+    m->attq = carve_arena<int8_t>(at, B * QD);
+    m->atts = carve_arena<float>(at, B * QD / 32);
     m->hq = carve_arena<int8_t>(at, KF);
     m->hs = carve_arena<float>(at, KF / 32);
-    m->xl = carve_arena<int8_t>(at, D);
-    m->attl = carve_arena<int8_t>(at, QD);
+    m->xl = carve_arena<int8_t>(at, B * D);
+    m->attl = carve_arena<int8_t>(at, B * QD);
     m->hl = carve_arena<int8_t>(at, KF);
-    m->ids = carve_arena<int32_t>(at, d.k);
+    m->ids = carve_arena<int32_t>(at, B * d.k);
+    m->plan.counts = carve_arena<int32_t>(at, d.experts);
+    m->plan.offsets = carve_arena<int32_t>(at, d.experts + 1);
+    m->plan.lists = carve_arena<int32_t>(at, B * d.k);
+    m->plan.active = carve_arena<int32_t>(at, d.experts + 1);
     m->err = carve_arena<int>(at, 64);
     if (d.mode == Q8_F32ACT_F64SUM) {
         m->xq = nullptr;
@@ -609,15 +838,21 @@ void q8_model_destroy(q8_model* m) {
     delete m;
 }
 
+// The step's launches of either form.
+static cudaError_t any_step_launches(q8_model* m, cudaStream_t st) {
+    return m->B > 1 ? batch_step_launches(m, st) : step_launches(m, st);
+}
+
 int decode_step_launches(q8_model* m, q8_stream stream) {
     if (!m) return model_fail(Q8_EINVAL, "model: null");
-    cudaError_t e = step_launches(m, (cudaStream_t)stream);
+    cudaError_t e = any_step_launches(m, (cudaStream_t)stream);
     return e == cudaSuccess ? Q8_OK : model_fail(Q8_ECUDA, "decode_step_launches: %s", cudaGetErrorString(e));
 }
 
 int decode_step_trace(q8_model* m, float* hidden, q8_stream stream) {
     if (!m) return model_fail(Q8_EINVAL, "model: null");
     if (!hidden || (uintptr_t)hidden % 4) return model_fail(Q8_EINVAL, "hidden: null or misaligned");
+    if (m->B > 1) return model_fail(Q8_EUNSUPPORTED, "decode_step_trace: one sequence only");
     cudaError_t e = step_launches(m, (cudaStream_t)stream, hidden);
     return e == cudaSuccess ? Q8_OK : model_fail(Q8_ECUDA, "decode_step_trace: %s", cudaGetErrorString(e));
 }
@@ -636,7 +871,7 @@ int decode_step(q8_model* m, q8_stream stream) {
         cudaGraph_t graph = nullptr;
         e = cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal);
         if (e == cudaSuccess) {
-            cudaError_t le = step_launches(m, m->cap);
+            cudaError_t le = any_step_launches(m, m->cap);
             e = cudaStreamEndCapture(m->cap, &graph);
             if (le != cudaSuccess) e = le;
         }
@@ -668,6 +903,7 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
     if (!m) return model_fail(Q8_EINVAL, "model: null");
     if (!tokens || !ws) return model_fail(Q8_EINVAL, "prefill_chunk: tokens or ws null");
     if (R < 1 || R > (1 << 20)) return model_fail(Q8_EINVAL, "prefill_chunk: %lld rows", (long long)R);
+    if (m->B > 1) return model_fail(Q8_EUNSUPPORTED, "prefill_chunk: one sequence only (the model is a batch form)");
     const q8_model_desc& d = m->d;
     const int mode = (int)d.mode;
     const int64_t D = d.d, H = d.heads, KV = d.kv_heads, HD = d.head_dim, E = d.experts, K = d.k, F = d.dff;

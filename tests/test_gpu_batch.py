@@ -1,0 +1,142 @@
+"""The batch form (lane/mod.rs: Form / FormKind::Batch, batch_io): B sequences step together, every weight read once
+for all of them, each sequence attending its own cache at its own position.  Each sequence's logits, token, position
+and new cache rows equal the oracle's decode step of that sequence alone (same weights, its own caches)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth import recipes
+
+pytestmark = pytest.mark.gpu
+
+TOL = {0: 1e-4, 1: 2e-3, 2: 2e-3}
+
+
+def rel_err(gpu, ora):
+    gpu = np.asarray(gpu, np.float64)
+    ora = np.asarray(ora, np.float64)
+    return float(np.max(np.abs(gpu - ora)) / max(np.max(np.abs(ora)), 1e-300))
+
+
+SMALL = dict(layers=2, d=256, heads=8, kv_heads=2, hd=128, experts=16, k=4, dff=64, vocab=1000, ctx=96, eps=1e-6,
+             rope_theta=1e6)
+
+
+def _batch_model(q8, cfg, B, seed, mode, variants=None):
+    import torch
+    arr = recipes.decode_model(cfg, seed)
+    if variants:
+        arr.update(recipes.mixture_variants(cfg, seed, **variants))
+    L, KV, ctx, hd = cfg["layers"], cfg["kv_heads"], cfg["ctx"], cfg["hd"]
+    # sequence b's caches: its own seeded values (sequence 0 keeps the model's)
+    kc = [[arr["k_cache"][l]] + [synth.normal((KV, ctx, hd), seed + b, 9000 + l) for b in range(1, B)] for l in range(L)]
+    vc = [[arr["v_cache"][l]] + [synth.normal((KV, ctx, hd), seed + b, 9100 + l) for b in range(1, B)] for l in range(L)]
+
+    def dv(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    t = {}
+    for key, v in arr.items():
+        if key in ("k_cache", "v_cache"):
+            continue
+        if isinstance(v, list):
+            t[key] = [tuple(dv(x) for x in e) if isinstance(e, tuple) else dv(e) for e in v]
+        elif isinstance(v, tuple):
+            t[key] = tuple(dv(x) for x in v)
+        else:
+            t[key] = dv(v)
+    t["k_cache"] = [dv(np.stack(kc[l])) for l in range(L)]
+    t["v_cache"] = [dv(np.stack(vc[l])) for l in range(L)]
+    tok = torch.zeros(B, dtype=torch.int32, device="cuda")
+    pos = torch.zeros(B, dtype=torch.int32, device="cuda")
+    logits = torch.empty(B, cfg["vocab"], dtype=torch.float32, device="cuda")
+    m = q8.Model(dict(cfg, batch=B), t, mode, tok, pos, logits)
+    oms = []
+    for b in range(B):
+        ab = dict(arr)
+        ab["k_cache"] = [kc[l][b].copy() for l in range(L)]
+        ab["v_cache"] = [vc[l][b].copy() for l in range(L)]
+        oms.append(oracle.ModelArrays(cfg, **ab))
+    return m, oms, t, tok, pos, logits
+
+
+def _steps_vs_oracle(q8, cfg, B, mode, toks, poss, steps, seed, variants=None):
+    import torch
+    m, oms, t, tok, pos, logits = _batch_model(q8, cfg, B, seed, mode, variants)
+    tok.copy_(torch.tensor(toks, dtype=torch.int32))
+    pos.copy_(torch.tensor(poss, dtype=torch.int32))
+    cur_t, cur_p = list(toks), list(poss)
+    for step in range(steps):
+        (m.step if step % 2 == 0 else m.step_launches)()
+        torch.cuda.synchronize()
+        gl = logits.cpu().numpy()
+        gt, gp = tok.cpu().numpy(), pos.cpu().numpy()
+        for b in range(B):
+            nxt, ora = oracle.decode_step(mode, oms[b], cur_t[b], cur_p[b])
+            assert rel_err(gl[b], ora) < TOL[mode], (step, b, rel_err(gl[b], ora))
+            srt = np.sort(ora)[::-1]
+            if srt[0] - srt[1] > 1e-5 * abs(srt[0]):
+                assert gt[b] == nxt
+            assert gp[b] == cur_p[b] + 1
+            for l in range(cfg["layers"]):
+                kcb = t["k_cache"][l][b].cpu().numpy()
+                vcb = t["v_cache"][l][b].cpu().numpy()
+                assert rel_err(kcb[:, cur_p[b]], oms[b].k_cache[l][:, cur_p[b]]) < TOL[mode]
+                assert rel_err(vcb[:, cur_p[b]], oms[b].v_cache[l][:, cur_p[b]]) < TOL[mode]
+            cur_t[b], cur_p[b] = int(gt[b]), cur_p[b] + 1
+    m.check()
+    return m
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("B", [2, 5])
+def test_batch_step_equals_independent_steps(q8, mode, B):
+    toks = [3, 500, 77, 999, 12][:B]
+    poss = [10, 63, 0, 94, 40][:B]  # different lengths, from one row to the cache's end
+    m = _steps_vs_oracle(q8, SMALL, B, mode, toks, poss, 2 if max(poss) >= 94 else 3, 41)
+    m.close()
+
+
+def test_batch_step_with_mixture_variants(q8):
+    m = _steps_vs_oracle(q8, SMALL, 3, 1, [1, 2, 3], [20, 30, 40], 2, 42,
+                         variants=dict(shared_dff=64, router_f32=True))
+    m.close()
+
+
+def test_batch_full_width_two_layers(q8):
+    """The full layer width (d 2048, 32 q / 4 kv heads, 128 experts, top-8, dff 768), 4 sequences near the end of
+    4096-row caches, two steps, int8 mode."""
+    cfg = dict(recipes.DECODE, layers=2, vocab=1000)
+    m = _steps_vs_oracle(q8, cfg, 4, 1, [5, 6, 7, 8], [4000, 4050, 3000, 4093], 2, 43)
+    assert m.launches_per_step() > 0
+    m.close()
+
+
+def test_batch_graph_equals_launches_bitwise(q8):
+    import torch
+    outs = []
+    for use_graph in (True, False):
+        m, oms, t, tok, pos, logits = _batch_model(q8, SMALL, 3, 44, 2)
+        tok.copy_(torch.tensor([4, 5, 6], dtype=torch.int32))
+        pos.copy_(torch.tensor([7, 8, 9], dtype=torch.int32))
+        for _ in range(3):
+            (m.step if use_graph else m.step_launches)()
+        torch.cuda.synchronize()
+        outs.append((logits.cpu().numpy().copy(), tok.cpu().numpy().copy(), t["k_cache"][1].cpu().numpy().copy()))
+        m.close()
+    for a, b in zip(outs[0], outs[1]):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_batch_bad_position_is_flagged_and_nothing_advances(q8):
+    import torch
+    m, oms, t, tok, pos, logits = _batch_model(q8, SMALL, 3, 45, 0)
+    tok.copy_(torch.tensor([1, 2, 3], dtype=torch.int32))
+    pos.copy_(torch.tensor([5, SMALL["ctx"], 7], dtype=torch.int32))  # sequence 1 is past its cache
+    m.step()
+    torch.cuda.synchronize()
+    assert pos.cpu().tolist() == [5, SMALL["ctx"], 7] and tok.cpu().tolist() == [1, 2, 3]
+    with pytest.raises(q8.Q8Error, match="position"):
+        m.check()
+    m.close()
