@@ -261,8 +261,8 @@ Q8_API void q8_model_destroy(q8_model *model);
 Q8_API int decode_step(q8_model *model, q8_stream stream);
 /* The same step as plain launches, without a graph (for tests and graph-capture by the caller). */
 Q8_API int decode_step_launches(q8_model *model, q8_stream stream);
-/* Debug export (one sequence only): decode_step_launches that also copies the residual stream into hidden (device f32
- * [layers + 1][d]):
+/* Debug export: decode_step_launches that also copies the residual stream into hidden (device f32 [layers + 1][d]; in
+ * the batch form [layers + 1][batch][d]):
  * row 0 is the stream entering the first layer (the token's embedding row), row l + 1 the stream leaving layer l
  * (after its attention and mixture sums).  Per layer the step's results are those of decode_step; the copies are
  * ordinary stream operations between the launches.  For parity checks of each layer against a reference fed the same

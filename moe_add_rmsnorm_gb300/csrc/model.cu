@@ -402,7 +402,7 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
 // The batch form's step (lane/mod.rs: FormKind::Batch): the sequences are the rows of one chunk for every norm,
 // projection and the mixture (each weight read once for all of them, each chosen expert once for the sequences that
 // chose it), and each attends its own cache at its own position.  Plain launches in order.
-cudaError_t batch_step_launches(q8_model* m, cudaStream_t st) {
+cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) {
     const q8_model_desc& d = m->d;
     const int mode = (int)d.mode;
     const int64_t B = m->B, D = d.d, H = d.heads, KV = d.kv_heads, HD = d.head_dim, E = d.experts, K = d.k, F = d.dff;
@@ -436,6 +436,8 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st) {
     for (int64_t l = 0; l < d.layers; ++l) {
         // the first layer gathers each sequence's embedding row into its residual row
         Q8_TRY(norm(l == 0 ? d.embed : m->h, l == 0 ? d.tok : nullptr, m->attn_norm[l], l == 0 ? m->h : nullptr));
+        if (trace && l == 0)
+            Q8_TRY(cudaMemcpyAsync(trace, m->h, (size_t)(B * D) * sizeof(float), cudaMemcpyDeviceToDevice, st));
         {
             GemvCall g;
             g.mode = mode;
@@ -585,6 +587,9 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st) {
             Carve cv = fresh_carve(m);
             Q8_TRY(launch_down_combine(c, cv, st));
         }
+        if (trace)
+            Q8_TRY(cudaMemcpyAsync(trace + (l + 1) * B * D, m->h, (size_t)(B * D) * sizeof(float),
+                                   cudaMemcpyDeviceToDevice, st));
     }
     // each sequence's final norm, LM head row and greedy token
     Q8_TRY(norm(m->h, nullptr, d.final_norm, nullptr));
@@ -852,8 +857,8 @@ int decode_step_launches(q8_model* m, q8_stream stream) {
 int decode_step_trace(q8_model* m, float* hidden, q8_stream stream) {
     if (!m) return model_fail(Q8_EINVAL, "model: null");
     if (!hidden || (uintptr_t)hidden % 4) return model_fail(Q8_EINVAL, "hidden: null or misaligned");
-    if (m->B > 1) return model_fail(Q8_EUNSUPPORTED, "decode_step_trace: one sequence only");
-    cudaError_t e = step_launches(m, (cudaStream_t)stream, hidden);
+    cudaError_t e = m->B > 1 ? batch_step_launches(m, (cudaStream_t)stream, hidden)
+                             : step_launches(m, (cudaStream_t)stream, hidden);
     return e == cudaSuccess ? Q8_OK : model_fail(Q8_ECUDA, "decode_step_trace: %s", cudaGetErrorString(e));
 }
 
@@ -869,7 +874,9 @@ int decode_step(q8_model* m, q8_stream stream) {
             if (e != cudaSuccess) return model_fail(Q8_ECUDA, "decode_step: %s", cudaGetErrorString(e));
         }
         cudaGraph_t graph = nullptr;
-        e = cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal);
+        // relaxed: calls other code makes on this thread while the step is captured (a profiler's own synchronizing
+        // calls around each launch it intercepts) do not invalidate the capture
+        e = cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeRelaxed);
         if (e == cudaSuccess) {
             cudaError_t le = any_step_launches(m, m->cap);
             e = cudaStreamEndCapture(m->cap, &graph);

@@ -447,7 +447,9 @@ __global__ void __launch_bounds__(DR_MAXW * 32, 1) down_row_kernel(const DownRow
         const int j = in ? pi / p.nb : 0;
         const int b = in ? pi - j * p.nb : 0;
         const int e = in ? __ldg(p.ids + j) : -1;
-        xo[i] = 32 * pi;  // = j*k + 32*b for a routed pair, K*k + 32*(pi - PK) for a shared block
+        // = j*k + 32*b for a routed pair, K*k + 32*(pi - PK) for a shared block; 0 for a lane past the pairs, whose
+        // (zero-weight) block is still read in the f32 mode: it must stay inside the staged rows
+        xo[i] = (in || sh) ? 32 * pi : 0;
         g[i] = in ? __ldg(p.gates + j) : sh ? 1.f : 0.f;
         if (sh) {
             const int bs = pi - PK;

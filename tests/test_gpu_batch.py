@@ -104,12 +104,59 @@ def test_batch_step_with_mixture_variants(q8):
     m.close()
 
 
-def test_batch_full_width_two_layers(q8):
-    """The full layer width (d 2048, 32 q / 4 kv heads, 128 experts, top-8, dff 768), 4 sequences near the end of
-    4096-row caches, two steps, int8 mode."""
+def test_batch_full_width_two_layers_two_steps(q8):
+    """The full layer width (d 2048, 32 q / 4 kv heads, 128 experts, top-8, dff 768), 4 sequences at different cache
+    lengths of 4096-row caches, two steps end to end, f32-activation mode."""
     cfg = dict(recipes.DECODE, layers=2, vocab=1000)
-    m = _steps_vs_oracle(q8, cfg, 4, 1, [5, 6, 7, 8], [4000, 4050, 3000, 4093], 2, 43)
+    m = _steps_vs_oracle(q8, cfg, 4, 0, [5, 6, 7, 8], [4000, 4050, 3000, 4093], 2, 43)
     assert m.launches_per_step() > 0
+    m.close()
+
+
+def _near_tie(logits, k):
+    srt = np.sort(np.asarray(logits, np.float64))[::-1]
+    return srt[k - 1] - srt[k] < 1e-5 * np.max(np.abs(srt))
+
+
+@pytest.mark.parametrize("mode", [1, 0, 2])
+def test_batch_full_width_layer_by_layer(q8, mode):
+    """Teacher-forced, as the single-sequence full-configuration test: the batch step exports every sequence's
+    residual stream entering each layer; the oracle runs each layer of each sequence from that same input (its own
+    cache), and each layer's output and increment, its new key and value rows, and the final norm / LM head from the
+    last stream are within the mode's tolerance."""
+    import torch
+    cfg = dict(recipes.DECODE, layers=4, vocab=1000)
+    L, K, d = cfg["layers"], cfg["k"], cfg["d"]
+    toks, poss = [5, 6, 7, 8], [4000, 4050, 3000, 4093]
+    B = len(toks)
+    m, oms, t, tok, pos, logits = _batch_model(q8, cfg, B, 46, mode)
+    tok.copy_(torch.tensor(toks, dtype=torch.int32))
+    pos.copy_(torch.tensor(poss, dtype=torch.int32))
+    hidden = torch.empty(L + 1, B, d, device="cuda")
+    m.step_trace(hidden)
+    torch.cuda.synchronize()
+    hid = hidden.cpu().numpy()
+    gl = logits.cpu().numpy()
+    arr_embed = recipes.decode_model(dict(cfg, layers=1), 46)["embed"]
+    flagged = []
+    for b in range(B):
+        np.testing.assert_array_equal(hid[0, b], arr_embed[toks[b]])
+        for l in range(L):
+            h_ora, rl = oracle.decode_layer(mode, oms[b], l, poss[b], hid[l, b])
+            if _near_tie(rl, K):
+                flagged.append((b, l))
+                continue
+            err_out = rel_err(hid[l + 1, b], h_ora)
+            err_inc = rel_err(hid[l + 1, b].astype(np.float64) - hid[l, b], h_ora.astype(np.float64) - hid[l, b])
+            kcb = t["k_cache"][l][b].cpu().numpy()[:, poss[b]]
+            vcb = t["v_cache"][l][b].cpu().numpy()[:, poss[b]]
+            err_k = rel_err(kcb, oms[b].k_cache[l][:, poss[b]])
+            err_v = rel_err(vcb, oms[b].v_cache[l][:, poss[b]])
+            assert max(err_out, err_inc, err_k, err_v) < TOL[mode], (b, l, err_out, err_inc, err_k, err_v)
+        _, ora_logits = oracle.decode_final(mode, oms[b], hid[L, b])
+        assert rel_err(gl[b], ora_logits) < TOL[mode], (b, rel_err(gl[b], ora_logits))
+    assert len(flagged) <= 1, flagged
+    assert pos.cpu().tolist() == [p + 1 for p in poss]
     m.close()
 
 
