@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--correlated", action="store_true", help="with --chunk-only: rows that share their experts")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="R",
                     help="only the R-row prefill timing through the model (for a profiler capture of its kernels)")
+    ap.add_argument("--batch-only", type=int, default=0, metavar="B",
+                    help="only the batch form's timing with B sequences (for a profiler capture of its kernels)")
     ap.add_argument("--configs-only", action="store_true",
                     help="only the single-operation configurations (projection, attention-side projections, mixture)")
     return ap.parse_args()
@@ -637,6 +639,11 @@ def main():
         dom_sec, dom_bytes = time_dominant_kernel(q8, cfg, dev, mode, reps=args.steps, stream=sh)
         print(json.dumps({"roofline_only": True, "us_per_launch": dom_sec * 1e6, "algorithmic_bytes": dom_bytes,
                           "gbs": dom_bytes / dom_sec / 1e9}), flush=True)
+        return
+    if args.batch_only:
+        res = time_batch(q8, cfg, dev, sh, mode, batches=(args.batch_only,), steps=max(1, args.steps),
+                         warmup=max(1, args.warmup))
+        print(json.dumps({"batch_only": True, **res[0]}), flush=True)
         return
     if args.configs_only:
         print(json.dumps({"configs_only": True, **time_configs(q8, cfg, dev, sh, peaks()[0],

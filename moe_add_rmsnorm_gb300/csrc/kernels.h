@@ -224,7 +224,12 @@ cudaError_t launch_route_row(const RouteRowCall& c, cudaStream_t st);
 bool moe_mma_supported(const ExpertCall& c);
 int moe_mma_min_rows();
 int moe_mma_max_rows();
-cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carve& ws, cudaStream_t st);
+cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carve& ws, cudaStream_t st,
+                           const float* res = nullptr);
+// A dense int8-mode projection of 16..64 activation rows on the tensor cores (the grouped product with one group of
+// every row; each segment's rows a multiple of 128, k a multiple of 64).
+bool dense_mma_supported(const GemvCall& g);
+cudaError_t launch_dense_mma(const GemvCall& g, Carve& ws, cudaStream_t st);
 bool gate_row_supported(const ExpertCall& c);
 cudaError_t launch_gate_row(const ExpertCall& c, Carve& ws, cudaStream_t st);
 bool down_row_supported(const ExpertCall& c);

@@ -79,6 +79,7 @@ struct MmaParams {
     const int8_t* xq;    // gate-up: token rows [R][k] (choice c reads row c / K); down: hidden rows [R*K][k]
     const float* xs;
     float* out;          // gate-up: h [R*K][out_rows]; down: part [R*K][out_rows]
+    const float* res;    // down only, or null: out = res + the product (same index; may alias out)
     int tiles;           // out_rows / 128
     int S;               // k slices per (group, tile) at most (scratch holds that many); 1: no split
     float* part;         // S > 1: [slots][tiles][S][2][64][128] scaled partial sums
@@ -465,7 +466,8 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams 
                     const int col = col0 + c;
                     if (col >= n) break;
                     const float v = p.gate_up ? silu_f32(acc0[c]) * acc1[c] : acc0[c];
-                    p.out[(int64_t)choice_d[col] * p.out_rows + orow] = v;
+                    const int64_t oi = (int64_t)choice_d[col] * p.out_rows + orow;
+                    p.out[oi] = p.res ? p.res[oi] + v : v;
                 }
             } else if (S > 1) {
                 // K split: this slice's scaled sums to scratch; the last slice to arrive adds the slices in order
@@ -495,7 +497,8 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams 
                             gsum += __ldcg(base + (size_t)sl2 * slab + (size_t)col * MM_M + r);
                             if (p.gate_up) usum += __ldcg(base + (size_t)sl2 * slab + (size_t)(MM_NMAX + col) * MM_M + r);
                         }
-                        p.out[(int64_t)choice_d[col] * p.out_rows + orow] = p.gate_up ? silu_f32(gsum) * usum : gsum;
+                        const int64_t oi = (int64_t)choice_d[col] * p.out_rows + orow;
+                        p.out[oi] = p.gate_up ? silu_f32(gsum) * usum : (p.res ? p.res[oi] + gsum : gsum);
                     }
                     if (dt == 0) p.cnt[pt] = 0;
                 }
@@ -520,7 +523,8 @@ bool moe_mma_supported(const ExpertCall& c) {
 int moe_mma_min_rows() { return MM_MIN; }
 int moe_mma_max_rows() { return MM_NMAX; }
 
-cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carve& ws, cudaStream_t st) {
+cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carve& ws, cudaStream_t st,
+                           const float* res) {
     if (!moe_mma_supported(c)) return cudaErrorInvalidConfiguration;
     MmaParams p = {};
     // K split: up to MM_SMAX slices of at least 4 stages, when the workspace holds their partial sums (the kernel picks
@@ -557,6 +561,7 @@ cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carv
     p.xq = c.xq;
     p.xs = c.xs;
     p.out = out;
+    p.res = res;
     p.tiles = (int)(c.out_rows / MM_M);
     p.err = c.err;
     cudaError_t e = cudaFuncSetAttribute(moe_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MM_SMEM);
@@ -565,6 +570,64 @@ cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carv
     if (grid > device_info().sms) grid = device_info().sms;
     if (grid < 1) grid = 1;
     return launch(moe_mma_kernel, dim3((unsigned)grid), dim3(MM_THREADS), MM_SMEM, st, c.pdl, p);
+}
+
+namespace {
+
+// The one group of a dense projection: every activation row, in order (group 0 of "expert" 0).
+__global__ void dense_plan_kernel(int32_t* active, int32_t* offsets, int32_t* lists, int R) {
+    griddep_wait();
+    griddep_launch();
+    if (threadIdx.x == 0) {
+        active[0] = 1;
+        active[1] = 0;
+        offsets[0] = 0;
+        offsets[1] = R;
+    }
+    for (int i = threadIdx.x; i < R; i += blockDim.x) lists[i] = i;
+}
+
+}  // namespace
+
+bool dense_mma_supported(const GemvCall& g) {
+    if (g.mode != 1 || g.R < MM_MIN || g.R > MM_NMAX || g.dots || g.norm_a || g.k % (32 * MM_BPS)) return false;
+    if ((uintptr_t)g.xq % 16 || (uintptr_t)g.xs % 8) return false;
+    for (int i = 0; i < g.nseg; ++i)
+        if (g.seg[i].n % MM_M || (uintptr_t)g.seg[i].q % 16 || (uintptr_t)g.seg[i].s % 8) return false;
+    return true;
+}
+
+// A dense projection of 16..64 activation rows (a prefill chunk's q/k/v or O) on the tensor cores: the grouped
+// product's kernel with one group holding every row, each segment's matrix as the group's expert, the residual (when
+// given) added in its epilogue.
+cudaError_t launch_dense_mma(const GemvCall& g, Carve& ws, cudaStream_t st) {
+    if (!dense_mma_supported(g)) return cudaErrorInvalidConfiguration;
+    int32_t* active = ws.take<int32_t>(2);
+    int32_t* offsets = ws.take<int32_t>(2);
+    int32_t* lists = ws.take<int32_t>((size_t)g.R);
+    if (ws.overflow) return cudaErrorMemoryAllocation;
+    cudaError_t e = launch(dense_plan_kernel, dim3(1), dim3(64), 0, st, g.pdl, active, offsets, lists, (int)g.R);
+    for (int i = 0; i < g.nseg && e == cudaSuccess; ++i) {
+        ExpertCall c;
+        c.mode = 1;
+        c.q0 = g.seg[i].q;
+        c.s0 = g.seg[i].s;
+        c.E = 1;
+        c.out_rows = g.seg[i].n;
+        c.k = g.k;
+        c.R = g.R;
+        c.K = 1;
+        c.plan.active = active;
+        c.plan.offsets = offsets;
+        c.plan.lists = lists;
+        c.xq = g.xq;
+        c.xs = g.xs;
+        c.err = g.err;
+        c.pdl = g.pdl;
+        Carve cv = ws;  // each segment's launch may reuse the same scratch after the one before it
+        e = launch_moe_mma(c, g.seg[i].y, 1, cv, st, g.seg[i].residual);
+    }
+    return e;
 }
 
 }  // namespace q8

@@ -306,6 +306,17 @@ def test_prefill_past_the_cache_is_flagged(q8):
     m.close()
 
 
+@pytest.mark.parametrize("mode,R", [(1, 32), (2, 32), (0, 32)])
+def test_prefill_full_width_tensor_core_rows(q8, mode, R):
+    """A 32-row chunk at full layer width: in the int8 mode the dense projections (q/k/v and O with its residual)
+    run on the tensor cores; every mode against the oracle's decode steps."""
+    cfg = dict(recipes.DECODE, layers=2, vocab=1000)
+    rng = np.random.default_rng(R)
+    tokens = [int(v) for v in rng.integers(0, cfg["vocab"], R)]
+    m, tok, pos, logits = _prefill_vs_oracle(q8, cfg, mode, R, 4000, tokens, 16)
+    m.close()
+
+
 def test_prefill_full_width_two_layers(q8):
     """The full layer width (d 2048, 32 q / 4 kv heads, 128 experts, top-8, dff 768) on two layers, a chunk of 8 rows
     near the end of a 4096-row cache, against the oracle."""

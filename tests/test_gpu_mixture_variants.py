@@ -145,7 +145,7 @@ def test_shared_expert_of_the_experts_width_one_row(q8, ws, mix_host, mode):
     import torch
     v = recipes.mixture_variants(dict(layers=1, d=D, experts=E), seed=1, shared_dff=DFF)
     shared = dict(gate=v["shared_gate"][0], up=v["shared_up"][0], down=v["shared_down"][0])
-    md = {k: (dev(a), dev(b)) for k, (a, b) in mix_host.items() if k in ("router", "gate", "up", "down")}
+    md = {k: (dev(mix_host[k][0]), dev(mix_host[k][1])) for k in ("router", "gate", "up", "down")}
     md["shared"] = {k: (dev(a), dev(b)) for k, (a, b) in shared.items()}
     x = synth.normal((1, D), 4, recipes.VEC + 122)
     res = synth.normal((1, D), 4, recipes.VEC + 123)
