@@ -23,6 +23,11 @@ SMALL = dict(layers=2, d=256, heads=8, kv_heads=2, hd=128, experts=16, k=4, dff=
              rope_theta=1e6)
 
 
+def _near_tie(logits, k):
+    srt = np.sort(np.asarray(logits, np.float64))[::-1]
+    return srt[k - 1] - srt[k] < 1e-5 * np.max(np.abs(srt))
+
+
 def _batch_model(q8, cfg, B, seed, mode, variants=None):
     import torch
     arr = recipes.decode_model(cfg, seed)
@@ -61,30 +66,51 @@ def _batch_model(q8, cfg, B, seed, mode, variants=None):
     return m, oms, t, tok, pos, logits
 
 
+def _oracle_step(mode, om, cfg, tok, pos):
+    """The oracle's decode step layer by layer, with whether any layer's router held a near tie on the way (the
+    K-th and (K+1)-th logits within 1e-5 of the largest: a choice last-bit differences may flip)."""
+    h = om.embed[tok]
+    tie = False
+    for l in range(cfg["layers"]):
+        h, rl = oracle.decode_layer(mode, om, l, pos, h)
+        tie = tie or _near_tie(rl, cfg["k"])
+    nxt, logits = oracle.decode_final(mode, om, h)
+    return nxt, logits, tie
+
+
 def _steps_vs_oracle(q8, cfg, B, mode, toks, poss, steps, seed, variants=None):
+    """B sequences stepped together, each against its own oracle decode steps.  A sequence whose oracle path met a
+    router near tie is flagged and left out from then on (its path may fork from the GPU's there); such forks must
+    stay rare."""
     import torch
     m, oms, t, tok, pos, logits = _batch_model(q8, cfg, B, seed, mode, variants)
     tok.copy_(torch.tensor(toks, dtype=torch.int32))
     pos.copy_(torch.tensor(poss, dtype=torch.int32))
     cur_t, cur_p = list(toks), list(poss)
+    forked = set()
     for step in range(steps):
         (m.step if step % 2 == 0 else m.step_launches)()
         torch.cuda.synchronize()
         gl = logits.cpu().numpy()
         gt, gp = tok.cpu().numpy(), pos.cpu().numpy()
         for b in range(B):
-            nxt, ora = oracle.decode_step(mode, oms[b], cur_t[b], cur_p[b])
-            assert rel_err(gl[b], ora) < TOL[mode], (step, b, rel_err(gl[b], ora))
-            srt = np.sort(ora)[::-1]
-            if srt[0] - srt[1] > 1e-5 * abs(srt[0]):
-                assert gt[b] == nxt
             assert gp[b] == cur_p[b] + 1
-            for l in range(cfg["layers"]):
-                kcb = t["k_cache"][l][b].cpu().numpy()
-                vcb = t["v_cache"][l][b].cpu().numpy()
-                assert rel_err(kcb[:, cur_p[b]], oms[b].k_cache[l][:, cur_p[b]]) < TOL[mode]
-                assert rel_err(vcb[:, cur_p[b]], oms[b].v_cache[l][:, cur_p[b]]) < TOL[mode]
+            if b not in forked:
+                nxt, ora, tie = _oracle_step(mode, oms[b], cfg, cur_t[b], cur_p[b])
+                if tie:
+                    forked.add(b)
+                else:
+                    assert rel_err(gl[b], ora) < TOL[mode], (step, b, rel_err(gl[b], ora))
+                    srt = np.sort(ora)[::-1]
+                    if srt[0] - srt[1] > 1e-5 * abs(srt[0]):
+                        assert gt[b] == nxt
+                    for l in range(cfg["layers"]):
+                        kcb = t["k_cache"][l][b].cpu().numpy()
+                        vcb = t["v_cache"][l][b].cpu().numpy()
+                        assert rel_err(kcb[:, cur_p[b]], oms[b].k_cache[l][:, cur_p[b]]) < TOL[mode]
+                        assert rel_err(vcb[:, cur_p[b]], oms[b].v_cache[l][:, cur_p[b]]) < TOL[mode]
             cur_t[b], cur_p[b] = int(gt[b]), cur_p[b] + 1
+    assert len(forked) <= max(1, B // 4), forked
     m.check()
     return m
 
@@ -104,26 +130,15 @@ def test_batch_step_with_mixture_variants(q8):
     m.close()
 
 
-def test_batch_full_width_two_layers_two_steps(q8):
-    """The full layer width (d 2048, 32 q / 4 kv heads, 128 experts, top-8, dff 768), 4 sequences at different cache
-    lengths of 4096-row caches, two steps end to end, f32-activation mode."""
-    cfg = dict(recipes.DECODE, layers=2, vocab=1000)
-    m = _steps_vs_oracle(q8, cfg, 4, 0, [5, 6, 7, 8], [4000, 4050, 3000, 4093], 2, 43)
-    assert m.launches_per_step() > 0
-    m.close()
-
-
-def _near_tie(logits, k):
-    srt = np.sort(np.asarray(logits, np.float64))[::-1]
-    return srt[k - 1] - srt[k] < 1e-5 * np.max(np.abs(srt))
-
-
 @pytest.mark.parametrize("mode", [1, 0, 2])
 def test_batch_full_width_layer_by_layer(q8, mode):
-    """Teacher-forced, as the single-sequence full-configuration test: the batch step exports every sequence's
-    residual stream entering each layer; the oracle runs each layer of each sequence from that same input (its own
-    cache), and each layer's output and increment, its new key and value rows, and the final norm / LM head from the
-    last stream are within the mode's tolerance."""
+    """Teacher-forced over two steps, as the single-sequence full-configuration test: each batch step exports every
+    sequence's residual stream entering each layer; the oracle runs each layer of each sequence from that same input
+    (its own cache, which it appends to as the GPU does), and each layer's output and increment, its new key and value
+    rows, and the final norm / LM head from the last stream are within the mode's tolerance.  The second step reads the
+    cache rows the first wrote.  (End to end, untethered, two correctly rounding implementations drift apart through
+    the layers at a rate set by the random weights' conditioning; the per-layer comparison is the one a kernel fault
+    cannot hide from.)"""
     import torch
     cfg = dict(recipes.DECODE, layers=4, vocab=1000)
     L, K, d = cfg["layers"], cfg["k"], cfg["d"]
@@ -132,35 +147,40 @@ def test_batch_full_width_layer_by_layer(q8, mode):
     m, oms, t, tok, pos, logits = _batch_model(q8, cfg, B, 46, mode)
     tok.copy_(torch.tensor(toks, dtype=torch.int32))
     pos.copy_(torch.tensor(poss, dtype=torch.int32))
-    hidden = torch.empty(L + 1, B, d, device="cuda")
-    m.step_trace(hidden)
-    torch.cuda.synchronize()
-    hid = hidden.cpu().numpy()
-    gl = logits.cpu().numpy()
     arr_embed = recipes.decode_model(dict(cfg, layers=1), 46)["embed"]
     flagged, worst = [], {}
-    for b in range(B):
-        np.testing.assert_array_equal(hid[0, b], arr_embed[toks[b]])
-        for l in range(L):
-            h_ora, rl = oracle.decode_layer(mode, oms[b], l, poss[b], hid[l, b])
-            if _near_tie(rl, K):
-                flagged.append((b, l))
-                continue
-            err_out = rel_err(hid[l + 1, b], h_ora)
-            err_inc = rel_err(hid[l + 1, b].astype(np.float64) - hid[l, b], h_ora.astype(np.float64) - hid[l, b])
-            kcb = t["k_cache"][l][b].cpu().numpy()[:, poss[b]]
-            vcb = t["v_cache"][l][b].cpu().numpy()[:, poss[b]]
-            err_k = rel_err(kcb, oms[b].k_cache[l][:, poss[b]])
-            err_v = rel_err(vcb, oms[b].v_cache[l][:, poss[b]])
-            for name, e in (("out", err_out), ("inc", err_inc), ("k", err_k), ("v", err_v)):
-                worst[name] = max(worst.get(name, 0.0), e)
-            assert max(err_out, err_inc, err_k, err_v) < TOL[mode], (b, l, err_out, err_inc, err_k, err_v)
-        _, ora_logits = oracle.decode_final(mode, oms[b], hid[L, b])
-        worst["logits"] = max(worst.get("logits", 0.0), rel_err(gl[b], ora_logits))
-        assert rel_err(gl[b], ora_logits) < TOL[mode], (b, rel_err(gl[b], ora_logits))
+    cur_t, cur_p = list(toks), list(poss)
+    hidden = torch.empty(L + 1, B, d, device="cuda")
+    for step in range(2):
+        m.step_trace(hidden)
+        torch.cuda.synchronize()
+        hid = hidden.cpu().numpy()
+        gl = logits.cpu().numpy()
+        for b in range(B):
+            np.testing.assert_array_equal(hid[0, b], arr_embed[cur_t[b]])
+            for l in range(L):
+                h_ora, rl = oracle.decode_layer(mode, oms[b], l, cur_p[b], hid[l, b])
+                if _near_tie(rl, K):
+                    flagged.append((step, b, l))
+                    continue
+                err_out = rel_err(hid[l + 1, b], h_ora)
+                err_inc = rel_err(hid[l + 1, b].astype(np.float64) - hid[l, b],
+                                  h_ora.astype(np.float64) - hid[l, b])
+                kcb = t["k_cache"][l][b].cpu().numpy()[:, cur_p[b]]
+                vcb = t["v_cache"][l][b].cpu().numpy()[:, cur_p[b]]
+                err_k = rel_err(kcb, oms[b].k_cache[l][:, cur_p[b]])
+                err_v = rel_err(vcb, oms[b].v_cache[l][:, cur_p[b]])
+                for name, e in (("out", err_out), ("inc", err_inc), ("k", err_k), ("v", err_v)):
+                    worst[name] = max(worst.get(name, 0.0), e)
+                assert max(err_out, err_inc, err_k, err_v) < TOL[mode], (step, b, l, err_out, err_inc, err_k, err_v)
+            _, ora_logits = oracle.decode_final(mode, oms[b], hid[L, b])
+            worst["logits"] = max(worst.get("logits", 0.0), rel_err(gl[b], ora_logits))
+            assert rel_err(gl[b], ora_logits) < TOL[mode], (step, b, rel_err(gl[b], ora_logits))
+        nt, np_ = tok.cpu().tolist(), pos.cpu().tolist()
+        assert np_ == [p + 1 for p in cur_p]
+        cur_t, cur_p = nt, np_
     print(f"batch mode {mode}: worst per-layer relative errors {worst}; near-tie layers {flagged}")
-    assert len(flagged) <= 1, flagged
-    assert pos.cpu().tolist() == [p + 1 for p in poss]
+    assert len(flagged) <= 2, flagged
     m.close()
 
 
@@ -190,35 +210,4 @@ def test_batch_bad_position_is_flagged_and_nothing_advances(q8):
     assert pos.cpu().tolist() == [5, SMALL["ctx"], 7] and tok.cpu().tolist() == [1, 2, 3]
     with pytest.raises(q8.Q8Error, match="position"):
         m.check()
-    m.close()
-
-
-def test_batch_untethered_error_growth_f32(q8):
-    """Diagnostic of the f32 mode's end-to-end error: the batch step's residual streams (traced) against the oracle's
-    own untethered streams, layer by layer, for every sequence; the per-layer growth is printed and the first
-    layer's output must be within the tolerance."""
-    import torch
-    cfg = dict(recipes.DECODE, layers=2, vocab=1000)
-    toks, poss = [5, 6, 7, 8], [4000, 4050, 3000, 4093]
-    B = len(toks)
-    m, oms, t, tok, pos, logits = _batch_model(q8, cfg, B, 43, 0)
-    tok.copy_(torch.tensor(toks, dtype=torch.int32))
-    pos.copy_(torch.tensor(poss, dtype=torch.int32))
-    hidden = torch.empty(cfg["layers"] + 1, B, cfg["d"], device="cuda")
-    m.step_trace(hidden)
-    torch.cuda.synchronize()
-    hid = hidden.cpu().numpy()
-    gl = logits.cpu().numpy()
-    report = []
-    for b in range(B):
-        h = hid[0, b]
-        errs = []
-        for l in range(cfg["layers"]):
-            h, _ = oracle.decode_layer(0, oms[b], l, poss[b], h)
-            errs.append(rel_err(hid[l + 1, b], h))
-        _, ora = oracle.decode_final(0, oms[b], h)
-        errs.append(rel_err(gl[b], ora))
-        report.append(errs)
-        assert errs[0] < TOL[0], errs
-    print("batch f32 untethered errors per layer (last: logits):", report)
     m.close()

@@ -224,7 +224,7 @@ def test_decode_full_config_layer_by_layer(q8, mode):
 
 # ---- prefill chunks: R token rows through every layer ---------------------------------------------------------------
 
-def _prefill_vs_oracle(q8, cfg, mode, R, pos0, tokens, seed):
+def _prefill_vs_oracle(q8, cfg, mode, R, pos0, tokens, seed, cache_layers=None):
     import torch
     m, arr, t, tok, pos, logits = build(q8, cfg, seed, mode)
     om = oracle.ModelArrays(cfg, **arr)
@@ -242,7 +242,7 @@ def _prefill_vs_oracle(q8, cfg, mode, R, pos0, tokens, seed):
     if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
         assert int(tok.item()) == nxt
     assert int(pos.item()) == pos0 + R
-    for l in range(cfg["layers"]):  # every row's key and value at its position
+    for l in (range(cfg["layers"]) if cache_layers is None else cache_layers):  # every row's key and value
         kc, vc = t["k_cache"][l].cpu().numpy(), t["v_cache"][l].cpu().numpy()
         rows = slice(pos0, pos0 + R)
         assert rel_err(kc[:, rows], om.k_cache[l][:, rows]) < TOL[mode]
@@ -309,11 +309,15 @@ def test_prefill_past_the_cache_is_flagged(q8):
 @pytest.mark.parametrize("mode,R", [(1, 32), (2, 32), (0, 32)])
 def test_prefill_full_width_tensor_core_rows(q8, mode, R):
     """A 32-row chunk at full layer width: in the int8 mode the dense projections (q/k/v and O with its residual)
-    run on the tensor cores; every mode against the oracle's decode steps."""
+    run on the tensor cores; every mode against the oracle's decode steps.  The first layer's key/value rows depend
+    only on the embedding, the norm and the q/k/v projection: strict in every mode.  Later layers are compared end to
+    end (the oracle's 32 sequential steps against one chunk); in the one-word mode an input differing in its last bits
+    can flip a word of 127 steps, so there the end-to-end check is the last row's logits."""
     cfg = dict(recipes.DECODE, layers=2, vocab=1000)
     rng = np.random.default_rng(R)
     tokens = [int(v) for v in rng.integers(0, cfg["vocab"], R)]
-    m, tok, pos, logits = _prefill_vs_oracle(q8, cfg, mode, R, 4000, tokens, 16)
+    m, tok, pos, logits = _prefill_vs_oracle(q8, cfg, mode, R, 4000, tokens, 16,
+                                             cache_layers=[0] if mode == 1 else None)
     m.close()
 
 
