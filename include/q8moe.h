@@ -127,6 +127,13 @@ Q8_API int add_rmsnorm_q8(const float *a, const float *b, const float *w, int64_
 Q8_API int q8_gemv(const q8_mat *W, q8_mode mode, const float *x, const q8_act *xq, int64_t rows, float *y, q8_ws *ws,
             q8_stream stream);
 
+/* Dense int8-mode projections of 16 to 64 activation rows (a prefill chunk's, a batch's, or q8_gemv's with that many
+ * rows) can run on the tensor cores — the grouped tensor-core product of the mixture with one group holding every row
+ * — instead of the CUDA cores.  rows: the fewest activation rows that take the tensor cores (16 to 64), or 0 for the
+ * CUDA cores always (the default: on this part the tensor-core form is measured slower at these row counts).
+ * Process-wide; set it before the calls (and the decode model's first step) it should affect. */
+Q8_API int q8_set_tensor_core_rows(int rows);
+
 /* Debug export of the int8 paths: the q8_gemv call (y as above) that also writes dots[r][o][b] = the exact int32 dot
  * of weight block (o, b) with activation block (r, b), from the same device code; dots is device int32
  * [rows][W.rows][W.cols/32].  The mode is Q8_INT8ACT, or Q8_INT8ACT2 when xq->lo is not NULL: dots is then

@@ -13,6 +13,8 @@
 
 namespace q8 {
 
+extern int kDenseMmaMinRows;  // gemv.cu
+
 static thread_local char g_err[512];
 
 static int fail(int code, const char* fmt, ...) {
@@ -500,6 +502,13 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
     cudaError_t e = launch_down_combine(c, cv, st);
     if (cv.overflow) return fail(Q8_ENOSPACE, "moe_down_combine: workspace too small (%zu bytes, %zu counters)", need, cnt);
     return e == cudaSuccess ? Q8_OK : cuda_fail(e, "moe_down_combine");
+}
+
+int q8_set_tensor_core_rows(int rows) {
+    g_err[0] = 0;
+    if (rows != 0 && (rows < 16 || rows > 64)) return fail(Q8_EINVAL, "rows %d: 0 (off) or 16 to 64", rows);
+    kDenseMmaMinRows = rows ? rows : (1 << 30);
+    return Q8_OK;
 }
 
 int moe_route_topk_f32(const float* router, int64_t E, int64_t d, const float* x, int64_t rows, int k, int32_t* ids,

@@ -613,11 +613,16 @@ cudaError_t launch_gemv_tma(const GemvCall& c, int* err, cudaStream_t st) {
 
 bool gemv_norm_supported(const GemvCall& c) { return tma_eligible(c); }
 
+// Activation rows from which a dense int8 projection takes the tensor cores (q8_set_tensor_core_rows; off by default).
+int kDenseMmaMinRows = 1 << 30;
+
 cudaError_t launch_gemv(const GemvCall& c, Carve& ws, cudaStream_t st) {
-    // 16..64 rows of int8 activations (a prefill chunk, a batch of sequences): the weight tiles go to the tensor cores
-    // once for all rows, when the workspace holds the group's lists (the CUDA-core form needs no more than before)
+    // 16..64 rows of int8 activations (a prefill chunk, a batch of sequences) can go to the tensor cores, the weight
+    // tiles read once for all rows, when the workspace holds the group's lists (the CUDA-core form needs no more than
+    // before); taken from kDenseMmaMinRows rows on (q8_set_tensor_core_rows)
     const size_t at = (ws.used + 255) & ~size_t(255);
-    if (dense_mma_supported(c) && ws.base && at + 4096 + 4 * (size_t)c.R <= ws.size) return launch_dense_mma(c, ws, st);
+    if (c.R >= kDenseMmaMinRows && dense_mma_supported(c) && ws.base && at + 4096 + 4 * (size_t)c.R <= ws.size)
+        return launch_dense_mma(c, ws, st);
     if (tma_eligible(c))
         return launch_gemv_tma(c, c.err ? c.err : (ws.counters ? ws.counters + ws.n_counters - 1 : nullptr), st);
     if (c.norm_a) return cudaErrorInvalidConfiguration;  // the norm prologue exists in the TMA projection only

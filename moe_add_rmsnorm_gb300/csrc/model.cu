@@ -431,6 +431,7 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nul
             n.ys = m->xs;
         }
         n.err = m->err;
+        n.pdl = m->pdl;
         return launch_add_rmsnorm(n, st);
     };
     for (int64_t l = 0; l < d.layers; ++l) {
@@ -452,6 +453,7 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nul
             g.xl = m->xl;
             g.xs = m->xs;
             g.err = m->err;
+            g.pdl = m->pdl;
             Carve cv = fresh_carve(m);
             Q8_TRY(launch_gemv(g, cv, st));
         }
@@ -481,6 +483,7 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nul
             }
             a.batch = (int)B;
             a.cache_stride = KV * d.ctx * HD;
+            a.pdl = m->pdl;
             Carve cv = fresh_carve(m);
             Q8_TRY(launch_attention(a, cv, st));
         }
@@ -495,6 +498,7 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nul
             g.xl = m->attl;
             g.xs = m->atts;
             g.err = m->err;
+            g.pdl = m->pdl;
             Carve cv = fresh_carve(m);
             Q8_TRY(launch_gemv(g, cv, st));
         }
@@ -512,6 +516,7 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nul
             g.xl = m->xl;
             g.xs = m->xs;
             g.err = m->err;
+            g.pdl = m->pdl;
             Carve cv = fresh_carve(m);
             Q8_TRY(launch_gemv(g, cv, st));
         }
@@ -526,6 +531,7 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nul
             t.gates = m->gates;
             t.plan = m->plan;
             t.done = cv.take_counters(1);
+            t.pdl = m->pdl;
             Q8_TRY(launch_topk(t, st));
         }
         {
@@ -548,6 +554,7 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nul
             c.h = m->hbuf;
             c.plan = m->plan;
             c.err = m->err;
+            c.pdl = m->pdl;
             if (SF) {
                 c.sq0 = m->sgate[l].q;
                 c.ss0 = m->sgate[l].s;
@@ -577,6 +584,7 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nul
             c.xs = m->hs;
             c.plan = m->plan;
             c.err = m->err;
+            c.pdl = m->pdl;
             if (SF) {
                 c.sq0 = m->sdown[l].q;
                 c.ss0 = m->sdown[l].s;
@@ -604,6 +612,7 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nul
         g.xl = m->xl;
         g.xs = m->xs;
         g.err = m->err;
+        g.pdl = m->pdl;
         Carve cv = fresh_carve(m);
         Q8_TRY(launch_gemv(g, cv, st));
     }
@@ -615,6 +624,7 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nul
         a.pos = d.pos + b;
         a.err = m->err;
         a.ctx = (int)d.ctx;
+        a.pdl = m->pdl;
         Carve cv = fresh_carve(m);
         Q8_TRY(launch_argmax(a, cv, st));
     }

@@ -261,6 +261,19 @@ def test_prefill_chunk_matches_oracle(q8, mode, cfg, R):
     m.close()
 
 
+def test_prefill_chunk_tensor_core_projections_small(q8):
+    """The 17-row chunk of the small model with its dense int8 projections (q/k/v and O with its residual) on the
+    tensor cores: every layer's cache rows and the logits against the oracle."""
+    rng = np.random.default_rng(17)
+    tokens = [int(v) for v in rng.integers(0, SMALL["vocab"], 17)]
+    q8.set_tensor_core_rows(16)
+    try:
+        m, tok, pos, logits = _prefill_vs_oracle(q8, SMALL, 1, 17, 40, tokens, 11)
+    finally:
+        q8.set_tensor_core_rows(0)
+    m.close()
+
+
 def test_prefill_chunk_same_token_rows_group_experts(q8):
     """Eight copies of one token: every row routes alike at the first layer, so the chunk's expert groups hold all
     rows (the grouped products with their largest groups)."""
@@ -316,8 +329,12 @@ def test_prefill_full_width_tensor_core_rows(q8, mode, R):
     cfg = dict(recipes.DECODE, layers=2, vocab=1000)
     rng = np.random.default_rng(R)
     tokens = [int(v) for v in rng.integers(0, cfg["vocab"], R)]
-    m, tok, pos, logits = _prefill_vs_oracle(q8, cfg, mode, R, 4000, tokens, 16,
-                                             cache_layers=[0] if mode == 1 else None)
+    q8.set_tensor_core_rows(16)
+    try:
+        m, tok, pos, logits = _prefill_vs_oracle(q8, cfg, mode, R, 4000, tokens, 16,
+                                                 cache_layers=[0] if mode == 1 else None)
+    finally:
+        q8.set_tensor_core_rows(0)
     m.close()
 
 

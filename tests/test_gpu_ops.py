@@ -516,8 +516,12 @@ def test_q8_gemv_rows_on_tensor_cores(q8, n, k, R):
     ref = np.stack([oracle.gemv_int8act(q, s, xq[r], xs[r]) for r in range(R)])
     big = q8.Workspace(64 << 20)
     y = empty((R, n), torch.float32)
-    q8.q8_gemv(dev(q), dev(s), 1, y, xq=dev(xq), xs=dev(xs), rows=R, ws=big)
-    gy = host(y)
+    q8.set_tensor_core_rows(16)
+    try:
+        q8.q8_gemv(dev(q), dev(s), 1, y, xq=dev(xq), xs=dev(xs), rows=R, ws=big)
+        gy = host(y)
+    finally:
+        q8.set_tensor_core_rows(0)
     assert rel_err(gy, ref) < TOL[1], rel_err(gy, ref)
     small = q8.Workspace(1024)
     y2 = empty((R, n), torch.float32)
