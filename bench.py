@@ -165,9 +165,9 @@ def make_model_tensors(cfg, seed=0):
 
 # DRAM traffic per launch of the roofline kernel (gate_row_kernel through moe_gate_up, int8 mode), from the ncu capture
 # summarised in profiles/moe_gate_up_roofline_kernel_int8.md; valid only while the kernel's sources are the captured ones.
-ROOFLINE_TRAFFIC = {"bytes": 28339200, "sources": ["moe_add_rmsnorm_gb300/csrc/moe_row.cu",
+ROOFLINE_TRAFFIC = {"bytes": 28344491, "sources": ["moe_add_rmsnorm_gb300/csrc/moe_row.cu",
                                                    "moe_add_rmsnorm_gb300/csrc/common.cuh"],
-                    "sha256_16": "1039cc4ba97c0c71", "profile": "profiles/moe_gate_up_roofline_kernel_int8.md"}
+                    "sha256_16": "565a6e58b25e8cbb", "profile": "profiles/moe_gate_up_roofline_kernel_int8.md"}
 
 
 def roofline_traffic(mode_int8):
