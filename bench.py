@@ -43,6 +43,10 @@ def parse():
                     help="only the R-row prefill timing through the model (for a profiler capture of its kernels)")
     ap.add_argument("--batch-only", type=int, default=0, metavar="B",
                     help="only the batch form's timing with B sequences (for a profiler capture of its kernels)")
+    ap.add_argument("--tensor-core-rows", type=int, default=None, metavar="N",
+                    help="dense int8 projections of N..64 rows on the tensor cores (0: off; the library's default)")
+    ap.add_argument("--grouped-tensor-core-rows", type=int, default=None, metavar="N",
+                    help="int8 expert groups of N..64 rows on the tensor cores (0: off; the library's default is 32)")
     ap.add_argument("--configs-only", action="store_true",
                     help="only the single-operation configurations (projection, attention-side projections, mixture)")
     return ap.parse_args()
@@ -630,6 +634,10 @@ def main():
     logits = torch.empty(cfg["vocab"], device="cuda")
     stream = torch.cuda.Stream()
     sh = stream.cuda_stream
+    if args.tensor_core_rows is not None:
+        q8.set_tensor_core_rows(args.tensor_core_rows)
+    if args.grouped_tensor_core_rows is not None:
+        q8.set_grouped_tensor_core_rows(args.grouped_tensor_core_rows)
     if args.chunk_only:
         res = time_chunks(q8, cfg, dev, sh, reps=max(1, args.steps), correlated=args.correlated,
                           rows=(args.chunk_only,))

@@ -134,6 +134,13 @@ Q8_API int q8_gemv(const q8_mat *W, q8_mode mode, const float *x, const q8_act *
  * Process-wide; set it before the calls (and the decode model's first step) it should affect. */
 Q8_API int q8_set_tensor_core_rows(int rows);
 
+/* The fewest rows an expert group of a chunk's int8-mode mixture (moe_gate_up, moe_down_combine over rows > 1) needs
+ * to take the grouped tensor-core product instead of the CUDA-core kernels: 16 to 64, or 0 for the CUDA cores always.
+ * The default is 32 (on this part 16-row groups are measured faster on the CUDA cores, 32-row groups even, 64-row
+ * groups faster on the tensor cores).  Groups of more than 64 rows stay on the CUDA cores.  Process-wide; set it before the calls (and
+ * the prefill chunks or batch steps) it should affect. */
+Q8_API int q8_set_grouped_tensor_core_rows(int rows);
+
 /* Debug export of the int8 paths: the q8_gemv call (y as above) that also writes dots[r][o][b] = the exact int32 dot
  * of weight block (o, b) with activation block (r, b), from the same device code; dots is device int32
  * [rows][W.rows][W.cols/32].  The mode is Q8_INT8ACT, or Q8_INT8ACT2 when xq->lo is not NULL: dots is then

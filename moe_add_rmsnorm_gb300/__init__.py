@@ -74,6 +74,7 @@ _SIGS = {
     "q8_gemv_blockdots": [_P(q8_mat), _P(q8_act), _i64, _vp, _vp, _vp, _vp],
     "q8_gemv_noalloc": [_P(q8_mat), _i32, _vp, _P(q8_act), _i64, _vp, _vp],
     "q8_set_tensor_core_rows": [_i32],
+    "q8_set_grouped_tensor_core_rows": [_i32],
     "moe_route_topk": [_P(q8_mat), _i32, _vp, _P(q8_act), _i64, _i32, _vp, _vp, _vp, _P(q8_moe_plan), _vp, _vp],
     "moe_route_topk_f32": [_vp, _i64, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _P(q8_moe_plan), _vp, _vp],
     "moe_gate_up": [_P(q8_mat), _P(q8_mat), _i64, _i32, _vp, _P(q8_act), _i64, _i32, _vp, _P(q8_moe_plan), _vp,
@@ -197,6 +198,11 @@ def q8_gemv_blockdots(q, s, xq, xs, dots, y, rows=1, ws=None, stream=None, xl=No
 def set_tensor_core_rows(rows: int):
     """The fewest int8 activation rows (16..64) a dense projection takes to the tensor cores; 0: never (default)."""
     _check(lib.q8_set_tensor_core_rows(int(rows)))
+
+
+def set_grouped_tensor_core_rows(rows: int):
+    """The fewest rows (16..64) an int8 expert group of a chunk needs to take the tensor cores; 0: never (default 32)."""
+    _check(lib.q8_set_grouped_tensor_core_rows(int(rows)))
 
 
 def plan_struct(counts, offsets, lists, active):

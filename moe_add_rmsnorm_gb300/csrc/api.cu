@@ -13,7 +13,8 @@
 
 namespace q8 {
 
-extern int kDenseMmaMinRows;  // gemv.cu
+extern int kDenseMmaMinRows;    // gemv.cu
+extern int kGroupedMmaMinRows;  // moe_mma.cu
 
 static thread_local char g_err[512];
 
@@ -508,6 +509,13 @@ int q8_set_tensor_core_rows(int rows) {
     g_err[0] = 0;
     if (rows != 0 && (rows < 16 || rows > 64)) return fail(Q8_EINVAL, "rows %d: 0 (off) or 16 to 64", rows);
     kDenseMmaMinRows = rows ? rows : (1 << 30);
+    return Q8_OK;
+}
+
+int q8_set_grouped_tensor_core_rows(int rows) {
+    g_err[0] = 0;
+    if (rows != 0 && (rows < 16 || rows > 64)) return fail(Q8_EINVAL, "rows %d: 0 (off) or 16 to 64", rows);
+    kGroupedMmaMinRows = rows;
     return Q8_OK;
 }
 

@@ -807,7 +807,7 @@ cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     // gate and up tiles are both in flight: about four (f32) or eight (int8) 32-byte loads per lane in all
     const EPlan pl = eplan(c.mode, (int)(c.k / 32), c.mode == 0 ? 2 : 4);
     ExpertParams p = make_params(c, pl);
-    const bool mma = moe_mma_supported(c);
+    const bool mma = moe_mma_grouped(c);
     if (mma) {
         p.mma_lo = moe_mma_min_rows();
         p.mma_hi = moe_mma_max_rows();
@@ -849,7 +849,7 @@ cudaError_t launch_down_routed(const ExpertCall& c, Carve& ws, cudaStream_t st) 
     ExpertParams p = make_params(c, pl);
     p.partial = ws.take<char>((size_t)c.R * c.K * c.out_rows * (c.mode == 0 ? 8 : 4));
     if (ws.overflow) return cudaErrorMemoryAllocation;
-    const bool mma = moe_mma_supported(c);
+    const bool mma = moe_mma_grouped(c);
     if (mma) {
         p.mma_lo = moe_mma_min_rows();
         p.mma_hi = moe_mma_max_rows();

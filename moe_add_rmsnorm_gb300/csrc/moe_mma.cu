@@ -19,6 +19,7 @@
 // matrices.  One CTA per SM walks the items (group, 128-row tile, k slice) of the groups it takes; the k split is
 // chosen per call from the number of such groups, and the last slice of a tile to finish adds the slices' partial sums
 // in slice order.
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -31,33 +32,40 @@ namespace q8 {
 namespace {
 
 constexpr int MM_M = 128;        // weight rows per tile: the MMA's M, one TMEM lane per thread
-constexpr int MM_THREADS = 896;  // 28 warps in three roles (below)
+constexpr int MM_THREADS = 896;  // 28 warps in four roles (below)
 constexpr int MM_NMAX = 64;      // group rows the kernel takes
 constexpr int MM_MIN = 16;       // smaller groups stay on the CUDA cores
 constexpr int MM_CORE = 128;     // bytes of one core matrix (8 rows x 16 bytes)
 constexpr int MM_BPS = 2;        // 32-value blocks per pipeline stage (K = 64)
-constexpr int MM_RING = 5;       // raw stages in the ring (cp.async, MM_RING - 1 ahead)
+constexpr int MM_RING = 6;       // raw stages in the ring, filled by the tensor-copy producer
 constexpr int MM_SMAX = 4;       // k slices per (group, tile) at most
 constexpr int MM_GCAP = 256;     // eligible groups listed in shared memory (beyond: found by a scan)
 constexpr int MM_ROWB = MM_BPS * 32;                 // bytes of one raw row of a stage (int8)
 constexpr int MM_KG = MM_BPS * 4;                    // f16 k-groups (core matrices) along K per stage
 constexpr int MM_SBO = MM_KG * MM_CORE;              // bytes between row groups of an operand tile
-// raw stage: weights [mat][128][64 B], activation rows [64][64 B], weight scales [mat][128][2], row scales [64][2]
+constexpr int MM_SCB = 4;        // scale columns a tensor copy brings per row (16 bytes: the copy's minimum width)
+// raw stage, as the tensor copies lay it out (every copy's destination 128-byte aligned): weights [mat][128][64 B]
+// and weight scales [mat][128][4] (the 4-block column group holding the stage's 2 blocks)
 constexpr int MM_RAW_W = 2 * MM_M * MM_ROWB;
-constexpr int MM_RAW_X = MM_NMAX * MM_ROWB;
-constexpr int MM_RAW_SW = 2 * MM_M * MM_BPS * 4;
-constexpr int MM_RAW_SX = MM_BPS * MM_NMAX * 4;  // block-major: [block][row]
-constexpr int MM_RAW = MM_RAW_W + MM_RAW_X + MM_RAW_SW + MM_RAW_SX;
+constexpr int MM_RAW_SW = 2 * MM_M * MM_SCB * 4;
+constexpr int MM_RAW = MM_RAW_W + MM_RAW_SW;
+static_assert(MM_RAW % 128 == 0 && MM_RAW_W % 128 == 0, "tensor-copy destinations 128-byte aligned");
 // operand buffer (f16, core-matrix layout): A per matrix [128 x 64], B [64 x 64]
 constexpr int MM_OPA = MM_M * MM_ROWB * 2;
 constexpr int MM_OPB = MM_NMAX * MM_ROWB * 2;
 constexpr int MM_OP = 2 * MM_OPA + MM_OPB;
 constexpr int MM_TCOLS = 512;    // TMEM: 2 buffers x 2 blocks x 2 matrices x 64 columns
-constexpr int MM_SQ = 4;         // scale slots between the converters and the read-back
-constexpr int MM_SCL = 2 * 2 * MM_M + MM_BPS * MM_NMAX;  // floats of a slot: sw [2][128][2], sx [2][64]
+constexpr int MM_SQ = 4;         // row-scale slots between the converters and the read-back
+constexpr int MM_SCL = MM_BPS * MM_NMAX;  // floats of a slot: sx [2][64]
 constexpr size_t MM_SMEM = (size_t)MM_RING * MM_RAW + 2 * MM_OP + (size_t)MM_SQ * MM_SCL * sizeof(float);
-constexpr int MM_CONV_WARPS = 11;                  // warps 0..10 fetch and convert
+static_assert(MM_SMEM + 2048 <= 232448, "dynamic plus static shared memory within the 227 KB a CTA may hold");
+constexpr int MM_CONV_WARPS = 10;                  // warps 0..9 convert
 constexpr int MM_CONV_T = MM_CONV_WARPS * 32;
+constexpr int MM_XT0 = MM_CONV_T - 4 * MM_NMAX;    // converter threads MM_XT0.. each own a quarter of a group row
+constexpr int MM_WPT = 4;                          // weight row quarters a converter thread takes per stage, at most
+constexpr int MM_XPD = 3;                          // stages the group-row loads run ahead of the conversion
+static_assert(MM_XT0 >= 0 && MM_WPT * MM_CONV_T >= 2 * MM_M * 4, "converters cover a stage");
+constexpr int MM_PROD_WARP = 10;                   // issues the tensor copies
 constexpr int MM_ISSUE_WARP = 11;                  // lane 0 issues the MMAs
 constexpr int MM_DRAIN_W0 = 12;                    // warps 12..27 read back: lanes 32*(w%4).., 16 columns each
 constexpr int MM_DRAIN_WARPS = 16;
@@ -67,11 +75,10 @@ static_assert(MM_DRAIN_W0 + MM_DRAIN_WARPS == MM_THREADS / 32, "roles cover the 
 static_assert(MM_DRAIN_W0 % 4 == 0 && MM_DRAIN_WARPS * MM_DCOLS == 4 * MM_NMAX, "read-back warps cover lanes and columns");
 
 struct MmaParams {
+    CUtensorMap tw0, tw1;  // weights [E*out_rows][k] int8, box 64 bytes x 128 rows (tw1: up, gate-up only)
+    CUtensorMap ts0, ts1;  // weight scales [E*out_rows][nb] f32, box 4 x 128
     int gate_up;         // 1: gate and up (SiLU product to h); 0: down (per-choice outputs to part)
-    const int8_t* q0;    // gate (or down) [E*out_rows][k]
-    const float* s0;
-    const int8_t* q1;    // up
-    const float* s1;
+    int nmin;            // the fewest rows of a group this kernel takes (MM_MIN..MM_NMAX)
     int E, out_rows, k, nb, K;
     const int32_t* offsets;
     const int32_t* lists;
@@ -116,19 +123,31 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
                  : "r"(taddr));
 }
 
-__device__ __forceinline__ void cp16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+// Two f32 lanes at once (sm_100+ packed f32 arithmetic; each lane rounds as the scalar instruction does).
+__device__ __forceinline__ uint64_t pk2(float2 a) { return (uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32); }
+__device__ __forceinline__ float2 upk2(uint64_t r) {
+    return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
 }
-__device__ __forceinline__ void cp4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)));
+    return upk2(r);
 }
-__device__ __forceinline__ void cp8(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)), "l"(pk2(c)));
+    return upk2(r);
 }
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// 16 bytes of read-only global memory (16-byte aligned).
+__device__ __forceinline__ uint4 ldg_nc_v4(const int8_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+// A tensor copy (TMA) of the 2-D tile at (x, y) into shared memory, counted on an mbarrier's transaction bytes.
+__device__ __forceinline__ void tma_tile(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+                 : "memory");
+}
 // Four int8 (one 32-bit word) to four exact f16: 0x6400 | (v + 128) is the f16 1024 + v + 128, minus 1152.
 __device__ __forceinline__ void i8x4_to_h(uint32_t w, uint32_t& lo, uint32_t& hi) {
     const uint32_t u = w ^ 0x80808080u;
@@ -139,11 +158,10 @@ __device__ __forceinline__ void i8x4_to_h(uint32_t w, uint32_t& lo, uint32_t& hi
     hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
-// 16 int8 (quarter q of a raw row of a stage) into f16 operand row r, k-groups 2q and 2q+1: row r lives in core
+// 16 int8 (quarter q of a row of a stage) into f16 operand row r, k-groups 2q and 2q+1: row r lives in core
 // row-group r/8, row r%8; its k-group g (values 8g..8g+7) at (r/8) * MM_SBO + g * 128 + (r%8) * 16.
-__device__ __forceinline__ void convert_quarter(unsigned char* op, int r, int q, const unsigned char* raw) {
+__device__ __forceinline__ void convert_quarter(unsigned char* op, int r, int q, const uint4 v) {
     unsigned char* base = op + (size_t)(r >> 3) * MM_SBO + (r & 7) * 16 + 2 * q * MM_CORE;
-    const uint4 v = *reinterpret_cast<const uint4*>(raw);
     uint4 o0, o1;
     i8x4_to_h(v.x, o0.x, o0.y);
     i8x4_to_h(v.y, o0.z, o0.w);
@@ -164,7 +182,7 @@ __device__ __forceinline__ bool mm_eligible(const MmaParams& p, int a) {
     const int e = __ldg(p.active + 1 + a);
     if (e < 0 || e >= p.E) return false;
     const int n = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
-    return n >= MM_MIN && n <= MM_NMAX;
+    return n >= p.nmin && n <= MM_NMAX;
 }
 
 // Warp-wide scan of the active groups in order: returns how many are eligible; the first MM_GCAP go to list (when
@@ -191,6 +209,13 @@ __device__ int mm_scan(const MmaParams& p, int nact, int* list, int target, int*
     return count;
 }
 
+// The same for one thread alone: the index of the g-th eligible group by a serial scan (groups past the list only).
+__device__ int mm_group_scan_one(const MmaParams& p, int nact, int g) {
+    for (int a = 0, c = 0; a < nact; ++a)
+        if (mm_eligible(p, a) && c++ == g) return a;
+    return 0;
+}
+
 // The eligible group at position g of the order (warp-wide; the first MM_GCAP come from the list).
 __device__ __forceinline__ int mm_group_at(const MmaParams& p, int nact, const int* glist, int g) {
     if (g < MM_GCAP) return glist[g];
@@ -202,25 +227,29 @@ __device__ __forceinline__ int mm_group_at(const MmaParams& p, int nact, const i
 // Persistent: the work is the items (eligible group g, tile, k slice) in that order, CTA b taking items b,
 // b + gridDim.x, ...; an item covers weight rows tile*128 .. tile*128+127 of group g's expert against the group's n rows
 // (16 <= n <= 64), k stages [slice*nst/S, (slice+1)*nst/S), S chosen per call from the number of eligible groups.
-// Stage i covers blocks 2i, 2i+1.  The warps have three roles, handing stages on through mbarriers:
-//  - warps 0..6 fetch raw stages by cp.async up to MM_RING - 1 ahead, convert each to f16 operands (two buffers, each
-//    reused once the MMAs that read it completed) and copy its scales into one of MM_SQ scale slots (reused once the
-//    read-back released it);
-//  - warp 7 (one lane) issues the stage's MMAs, two per block and matrix (K = 16 each), into one of two TMEM buffers
+// Stage i covers blocks 2i, 2i+1.  The warps have four roles, handing stages on through mbarriers:
+//  - warp 10 (the producer, one lane) brings each stage's weight tiles and their scales into one of MM_RING ring slots
+//    with 2-D tensor copies; the slot's "full" barrier counts the bytes, and the slot is refilled once the converters
+//    released it;
+//  - warps 0..9 convert each raw stage to f16 operands (two buffers, each reused once the MMAs that read it completed),
+//    together with the stage's slice of the group's rows, which they load from global memory a few stages ahead
+//    (the rows are few and stay in L2), and copy the scales into one of MM_SQ scale slots (reused once the read-back
+//    released it);
+//  - warp 11 (one lane) issues the stage's MMAs, two per block and matrix (K = 16 each), into one of two TMEM buffers
 //    (reused once the read-back released it) and commits them to the operand buffer's and the TMEM buffer's barriers;
-//  - warps 8..15 read the TMEM buffer back (warp w: lanes 32*(w%4).., columns 32*((w-8)/4)..+31), add
-//    s_w * s_x * D into registers in block order, and after an item's last stage store its outputs (or its k slice's
-//    partial sums, the last slice of a tile adding them in slice order).
-// TMEM, buffers and barriers carry on from item to item: a running stage count gives buffers and phases, so the
-// three roles run several stages apart.
-__global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams p) {
+//  - warps 12..27 read the TMEM buffer back (warp w: lanes 32*(w%4).., 16 columns), add s_w * s_x * D into registers
+//    in block order, and after an item's last stage store its outputs (or its k slice's partial sums, the last slice
+//    of a tile adding them in slice order).
+// TMEM, buffers and barriers carry on from item to item: a running stage count gives slots, buffers and phases, so the
+// roles run several stages apart.
+__global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_constant__ MmaParams p) {
     extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) uint64_t raw_full[MM_RING], raw_empty[MM_RING];
     __shared__ __align__(8) uint64_t op_full[2], op_empty[2], tm_full[2], tm_empty[2], sc_full[MM_SQ], sc_empty[MM_SQ];
     __shared__ uint32_t tmem_base;
-    __shared__ int rows_c[MM_NMAX];    // converters: each group row's activation row
     __shared__ int choice_d[MM_NMAX];  // read-back: each group row's choice
     __shared__ int glist[MM_GCAP];     // the first eligible groups' indices in the active list
-    __shared__ int nelig_s, a_c, a_d, last_d;
+    __shared__ int nelig_s, a_d, last_d;
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     griddep_wait();
     griddep_launch();
@@ -245,6 +274,10 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams 
     const int items = nelig * p.tiles * S;
     if ((int)blockIdx.x >= items) return;
     if (t == 0) {
+        for (int i = 0; i < MM_RING; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], MM_CONV_WARPS + MM_DRAIN_WARPS);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&op_full[i], MM_CONV_WARPS);
             mbar_init(&op_empty[i], 1);
@@ -269,98 +302,128 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams 
     const int mats = p.gate_up ? 2 : 1;
     unsigned char* raw = smem;
     unsigned char* ops = smem + (size_t)MM_RING * MM_RAW;
-    float* scl = reinterpret_cast<float*>(ops + 2 * (size_t)MM_OP);  // [MM_SQ] slots: sw [2][128][2], sx [2][64]
+    float* scl = reinterpret_cast<float*>(ops + 2 * (size_t)MM_OP);  // [MM_SQ] slots: sx [2][64]
     uint32_t gs = 0;  // stages this CTA has run (every role counts the same)
     bool ok = true;
 
-    if (w < MM_CONV_WARPS) {
-        // ---- fetch and convert ------------------------------------------------------------------------------------
+    if (w == MM_PROD_WARP) {
+        // ---- tensor-copy producer: weight tiles and their scales ---------------------------------------------------
+        uint32_t issued = 0;  // stages whose copies were issued (the drain below waits for the last of them)
+        if (lane == 0) {
+            const unsigned bytes = (unsigned)(mats * (MM_M * MM_ROWB + MM_M * MM_SCB * 4));
+            for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+                const int g = item / (p.tiles * S), tile = (item / S) % p.tiles, slice = item % S;
+                const int a = g < MM_GCAP ? glist[g] : -1;
+                const int e = __ldg(p.active + 1 + (a >= 0 ? a : mm_group_scan_one(p, nact, g)));
+                const int wrow = e * p.out_rows + tile * MM_M;
+                const int st0 = slice * nst_all / S, nst = (slice + 1) * nst_all / S - st0;
+                for (int i = 0; i < nst && ok; ++i) {
+                    const uint32_t gi = gs + i;
+                    const int slot = gi % MM_RING;
+                    if (gi >= MM_RING) ok = mbar_wait(&raw_empty[slot], ((gi / MM_RING) - 1) & 1, p.err);
+                    if (!ok) break;
+                    unsigned char* st = raw + (size_t)slot * MM_RAW;
+                    const int b0 = (st0 + i) * MM_BPS;
+                    mbar_arrive_expect_tx(&raw_full[slot], bytes);
+                    tma_tile(st, &p.tw0, 32 * b0, wrow, &raw_full[slot]);
+                    tma_tile(st + MM_RAW_W, &p.ts0, b0 & ~(MM_SCB - 1), wrow, &raw_full[slot]);
+                    if (mats == 2) {
+                        tma_tile(st + MM_M * MM_ROWB, &p.tw1, 32 * b0, wrow, &raw_full[slot]);
+                        tma_tile(st + MM_RAW_W + MM_M * MM_SCB * 4, &p.ts1, b0 & ~(MM_SCB - 1), wrow, &raw_full[slot]);
+                    }
+                    ++issued;
+                }
+                gs += nst;
+            }
+            // every copy issued has landed before the CTA may end (bounded: a stalled pipeline already set the error)
+            for (uint32_t gi = issued > MM_RING ? issued - MM_RING : 0; gi < issued; ++gi)
+                mbar_wait(&raw_full[gi % MM_RING], (gi / MM_RING) & 1, p.err);
+        }
+        __syncwarp();
+    } else if (w < MM_CONV_WARPS) {
+        // ---- convert ----------------------------------------------------------------------------------------------
+        // Per stage thread ct converts weight row quarters ct, ct + MM_CONV_T, ... from the raw stage, and threads
+        // MM_XT0.. each one quarter (16 bytes) of a group row, loaded from global memory MM_XPD stages ahead into
+        // registers; the threads holding quarter 0 of a row also load its two block scales.
         const int ct = t;  // 0 .. MM_CONV_T - 1
-        for (int item = blockIdx.x; item < items; item += gridDim.x) {  // (no early exit: named barriers below)
-            const int g = item / (p.tiles * S), tile = (item / S) % p.tiles, slice = item % S;
-            if (w == 0) {
-                const int a = mm_group_at(p, nact, glist, g);
-                if (lane == 0) a_c = a;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(MM_CONV_T));
-            const int e = __ldg(p.active + 1 + a_c);
+        const int xt = ct - MM_XT0, xr = xt >> 2, xqq = xt & 3;
+        for (int item = blockIdx.x; item < items; item += gridDim.x) {
+            const int g = item / (p.tiles * S), slice = item % S;
+            const int a = mm_group_at(p, nact, glist, g);
+            const int e = __ldg(p.active + 1 + a);
             const int c0 = __ldg(p.offsets + e), n = __ldg(p.offsets + e + 1) - c0;
-            if (ct < n) {
-                const int c = __ldg(p.lists + c0 + ct);
-                rows_c[ct] = p.gate_up ? c / p.K : c;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(MM_CONV_T));
             const int N = (n + 15) & ~15;
-            const int64_t wbase = (int64_t)e * p.out_rows + (int64_t)tile * MM_M;
             const int st0 = slice * nst_all / S, nst = (slice + 1) * nst_all / S - st0;
-            auto fetch = [&](int i) {
-                unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
-                const int b0 = (st0 + i) * MM_BPS;
-                for (int task = ct; task < mats * MM_M * 4; task += MM_CONV_T) {  // weight row quarters
-                    const int m = task / (MM_M * 4), wr = (task >> 2) & (MM_M - 1), q = task & 3;
-                    cp16(st + (size_t)(m * MM_M + wr) * MM_ROWB + 16 * q,
-                         (m == 0 ? p.q0 : p.q1) + (wbase + wr) * p.k + 32 * b0 + 16 * q);
+            const bool xown = xt >= 0 && xr < n;  // this thread brings a real row quarter
+            int64_t xrow = 0;
+            if (xown) {
+                const int c = __ldg(p.lists + c0 + xr);
+                xrow = p.gate_up ? c / p.K : c;
+            }
+            const int8_t* xsrc = p.xq + xrow * p.k + 16 * xqq;
+            const float* ssrc = p.xs + xrow * p.nb;
+            uint4 xb[MM_XPD];
+            float2 sb[MM_XPD];
+#pragma unroll
+            for (int d = 0; d < MM_XPD; ++d) {
+                xb[d] = make_uint4(0, 0, 0, 0);
+                sb[d] = make_float2(0.f, 0.f);
+                if (xown && d < nst) {
+                    xb[d] = ldg_nc_v4(xsrc + 64 * (st0 + d));
+                    if (xqq == 0) sb[d] = __ldg(reinterpret_cast<const float2*>(ssrc + MM_BPS * (st0 + d)));
                 }
-                for (int task = ct; task < mats * MM_M; task += MM_CONV_T) {  // weight scales
-                    const int m = task / MM_M, wr = task & (MM_M - 1);
-                    cp8(st + MM_RAW_W + MM_RAW_X + (size_t)(m * MM_M + wr) * MM_BPS * 4,
-                        (m == 0 ? p.s0 : p.s1) + (wbase + wr) * p.nb + b0);
-                }
-                for (int task = ct; task < 4 * n; task += MM_CONV_T) {  // group row quarters
-                    const int xr = task >> 2, q = task & 3;
-                    cp16(st + MM_RAW_W + (size_t)xr * MM_ROWB + 16 * q,
-                         p.xq + (int64_t)rows_c[xr] * p.k + 32 * b0 + 16 * q);
-                }
-                for (int task = ct; task < MM_BPS * n; task += MM_CONV_T) {  // group row scales, [block][row]
-                    const int j = task / n, xr = task - j * n;
-                    float* sxr = reinterpret_cast<float*>(st + MM_RAW_W + MM_RAW_X + MM_RAW_SW);
-                    cp4(sxr + j * MM_NMAX + xr, p.xs + (int64_t)rows_c[xr] * p.nb + b0 + j);
-                }
-            };
-            for (int i = 0; i < MM_RING - 1; ++i) {
-                if (i < nst) fetch(i);
-                cp_commit();
             }
             for (int i = 0; i < nst; ++i) {
                 const uint32_t gi = gs + i;
-                const int b = gi & 1, q = gi % MM_SQ;
-                cp_wait<MM_RING - 2>();
-                asm volatile("bar.sync 1, %0;" ::"n"(MM_CONV_T));  // raw stage i landed (every converter's copies)
-                // the ring slot of stage i-1 (converted, its scales copied) takes stage i + MM_RING - 1
-                if (i + MM_RING - 1 < nst) fetch(i + MM_RING - 1);
-                cp_commit();
-                const unsigned char* st = raw + (size_t)(i % MM_RING) * MM_RAW;
+                const int b = gi & 1, q = gi % MM_SQ, slot = gi % MM_RING;
+                const int jo = ((st0 + i) * MM_BPS) & (MM_SCB - 1);  // the stage's blocks inside the copied scale columns
+                const uint4 xc = xb[0];
+                const float2 sc = sb[0];
+#pragma unroll
+                for (int d = 0; d + 1 < MM_XPD; ++d) xb[d] = xb[d + 1], sb[d] = sb[d + 1];
+                if (xown && i + MM_XPD < nst) {
+                    xb[MM_XPD - 1] = ldg_nc_v4(xsrc + 64 * (st0 + i + MM_XPD));
+                    if (xqq == 0) sb[MM_XPD - 1] = __ldg(reinterpret_cast<const float2*>(ssrc + MM_BPS * (st0 + i + MM_XPD)));
+                }
+                if (ok) ok = mbar_wait(&raw_full[slot], (gi / MM_RING) & 1, p.err);
+                const unsigned char* st = raw + (size_t)slot * MM_RAW;
                 if (ok && gi >= 2) ok = mbar_wait(&op_empty[b], ((gi >> 1) - 1) & 1, p.err);
                 unsigned char* op = ops + (size_t)b * MM_OP;
-                for (int task = ct; task < (mats * MM_M + N) * 4; task += MM_CONV_T) {
-                    const int row = task >> 2, qq = task & 3;
-                    if (row < mats * MM_M) {
-                        const int m = row / MM_M;
-                        convert_quarter(op + m * MM_OPA, row - m * MM_M, qq, st + (size_t)row * MM_ROWB + 16 * qq);
-                    } else {
-                        const int xr = row - mats * MM_M;
-                        if (xr < n) convert_quarter(op + 2 * MM_OPA, xr, qq, st + MM_RAW_W + (size_t)xr * MM_ROWB + 16 * qq);
-                        else zero_quarter(op + 2 * MM_OPA, xr, qq);
+                {  // weight row quarters: every load first, then the conversions
+                    uint4 wv[MM_WPT];
+#pragma unroll
+                    for (int u = 0; u < MM_WPT; ++u) {
+                        const int task = ct + u * MM_CONV_T;
+                        if (task < mats * MM_M * 4) wv[u] = *reinterpret_cast<const uint4*>(st + (size_t)task * 16);
+                    }
+#pragma unroll
+                    for (int u = 0; u < MM_WPT; ++u) {
+                        const int task = ct + u * MM_CONV_T;
+                        if (task < mats * MM_M * 4) {
+                            const int row = task >> 2, m = row / MM_M;
+                            convert_quarter(op + m * MM_OPA, row - m * MM_M, task & 3, wv[u]);
+                        }
                     }
                 }
+                if (xown) convert_quarter(op + 2 * MM_OPA, xr, xqq, xc);
+                else if (xt >= 0 && xr < N) zero_quarter(op + 2 * MM_OPA, xr, xqq);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the operands, to the tensor cores
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&op_full[b]);
                 if (ok && gi >= MM_SQ) ok = mbar_wait(&sc_empty[q], ((gi / MM_SQ) - 1) & 1, p.err);
-                {  // the stage's scales into slot q
+                if (xt >= 0 && xqq == 0) {  // the stage's row scales into slot q (the weight scales stay in the raw slot)
                     float* sl = scl + (size_t)q * MM_SCL;
-                    const float2* sw = reinterpret_cast<const float2*>(st + MM_RAW_W + MM_RAW_X);
-                    const float* sx = reinterpret_cast<const float*>(st + MM_RAW_W + MM_RAW_X + MM_RAW_SW);
-                    for (int task = ct; task < mats * MM_M; task += MM_CONV_T) reinterpret_cast<float2*>(sl)[task] = sw[task];
-                    for (int task = ct; task < MM_BPS * MM_NMAX; task += MM_CONV_T) sl[2 * 2 * MM_M + task] = sx[task];
+                    sl[xr] = sc.x;
+                    sl[MM_NMAX + xr] = sc.y;
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sc_full[q]);
+                if (lane == 0) {
+                    mbar_arrive(&sc_full[q]);
+                    mbar_arrive(&raw_empty[slot]);  // this warp is done with the raw stage
+                }
             }
-            cp_wait<0>();
             gs += nst;
         }
-        cp_wait<0>();
     } else if (w == MM_ISSUE_WARP) {
         // ---- MMA issue --------------------------------------------------------------------------------------------
         for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
@@ -415,47 +478,59 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams 
             if (dt < n) choice_d[dt] = __ldg(p.lists + c0 + dt);
             asm volatile("bar.sync 2, %0;" ::"n"(MM_DRAIN_T));
             const int N = (n + 15) & ~15;
-            const int nst = (slice + 1) * nst_all / S - slice * nst_all / S;
+            const int st0 = slice * nst_all / S, nst = (slice + 1) * nst_all / S - st0;
             float acc0[MM_DCOLS], acc1[MM_DCOLS];
 #pragma unroll
             for (int c = 0; c < MM_DCOLS; ++c) acc0[c] = acc1[c] = 0.f;
             const uint32_t lane_base = tmem + ((uint32_t)(32 * (w & 3)) << 16);
             for (int i = 0; i < nst; ++i) {
                 const uint32_t gi = gs + i;
-                const int b = gi & 1, q = gi % MM_SQ;
+                const int b = gi & 1, q = gi % MM_SQ, slot = gi % MM_RING;
+                const int jo = ((st0 + i) * MM_BPS) & (MM_SCB - 1);  // the stage's blocks inside the copied scale columns
                 if (ok) ok = mbar_wait(&tm_full[b], (gi >> 1) & 1, p.err);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 if (ok) ok = mbar_wait(&sc_full[q], (gi / MM_SQ) & 1, p.err);
+                if (ok) ok = mbar_wait(&raw_full[slot], (gi / MM_RING) & 1, p.err);  // (complete: the weight scales)
                 const float* sl = scl + (size_t)q * MM_SCL;
+                const float* swr = reinterpret_cast<const float*>(raw + (size_t)slot * MM_RAW + MM_RAW_W) + r * MM_SCB + jo;
                 if (ok && col0 < N) {  // warp-uniform
 #pragma unroll
-                    for (int j = 0; j < MM_BPS; ++j)
+                    for (int j = 0; j < MM_BPS; ++j) {
+                        const float4* sxj = reinterpret_cast<const float4*>(sl + j * MM_NMAX + col0);
 #pragma unroll
                         for (int m = 0; m < 2; ++m) {
                             if (m == 1 && !p.gate_up) break;
                             uint32_t v[16];
                             tmem_ld16(lane_base + (uint32_t)(b * 256 + j * 128 + m * 64 + col0), v);
+                            // the scales load while the accumulator values travel
+                            const float swv = swr[m * MM_M * MM_SCB + j];
+                            float4 x4[4];  // the block's row scales for this warp's columns
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) x4[q4] = sxj[q4];
                             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                            const float swv = sl[(m * MM_M + r) * MM_BPS + j];
-                            const float* sxj = sl + 2 * 2 * MM_M + j * MM_NMAX + col0;
+                            float* acc = m == 0 ? acc0 : acc1;
 #pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                const float4 x4 = *reinterpret_cast<const float4*>(sxj + 4 * q4);
-                                const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const int c = 4 * q4 + u;
-                                    if (m == 0) acc0[c] = fmaf(swv * xv[u], __uint_as_float(v[c]), acc0[c]);
-                                    else acc1[c] = fmaf(swv * xv[u], __uint_as_float(v[c]), acc1[c]);
-                                }
+                            for (int q4 = 0; q4 < 4; ++q4) {  // s_w * s_x, then + (s_w * s_x) * D, two columns an instruction
+                                const float2 s01 = mul2(make_float2(swv, swv), make_float2(x4[q4].x, x4[q4].y));
+                                const float2 s23 = mul2(make_float2(swv, swv), make_float2(x4[q4].z, x4[q4].w));
+                                float2 a01 = make_float2(acc[4 * q4], acc[4 * q4 + 1]);
+                                float2 a23 = make_float2(acc[4 * q4 + 2], acc[4 * q4 + 3]);
+                                a01 = fma2(s01, make_float2(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1])), a01);
+                                a23 = fma2(s23, make_float2(__uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])), a23);
+                                acc[4 * q4] = a01.x;
+                                acc[4 * q4 + 1] = a01.y;
+                                acc[4 * q4 + 2] = a23.x;
+                                acc[4 * q4 + 3] = a23.y;
                             }
                         }
+                    }
                 }
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&tm_empty[b]);
                     mbar_arrive(&sc_empty[q]);
+                    mbar_arrive(&raw_empty[slot]);
                 }
             }
             gs += nst;
@@ -513,18 +588,66 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const MmaParams 
 
 }  // namespace
 
-bool moe_mma_supported(const ExpertCall& c) {
-    return c.mode == 1 && c.plan.active && c.R >= MM_MIN && c.out_rows % MM_M == 0 && c.k % (32 * MM_BPS) == 0 &&
-           c.xq && c.xs && (uintptr_t)c.q0 % 16 == 0 && (!c.q1 || (uintptr_t)c.q1 % 16 == 0) &&
-           (uintptr_t)c.xq % 16 == 0 && (uintptr_t)c.s0 % 8 == 0 && (!c.s1 || (uintptr_t)c.s1 % 8 == 0) &&
-           (uintptr_t)c.xs % 8 == 0;
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, found once through the runtime (no link against the driver library).
+EncodeTiled encode_tiled() {
+    static const EncodeTiled fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (EncodeTiled) nullptr;
+        return reinterpret_cast<EncodeTiled>(f);
+    }();
+    return fn;
 }
 
-int moe_mma_min_rows() { return MM_MIN; }
+// A 2-D row-major tensor [rows][cols] of u8 or f32 elements (row stride `stride` bytes) read in boxes of
+// box_cols x box_rows; no swizzle, zero fill outside.
+bool map_2d(CUtensorMap* m, bool f32, const void* base, uint64_t cols, uint64_t rows, uint64_t stride,
+            uint32_t box_cols, uint32_t box_rows) {
+    const EncodeTiled enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {stride};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base),
+               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool moe_mma_supported(const ExpertCall& c) {
+    // tensor copies: 16-byte aligned bases, row strides (k bytes, nb scales) multiples of 16 bytes, 4-column scale
+    // boxes inside the rows, row coordinates that fit an int
+    return c.mode == 1 && c.plan.active && c.R >= MM_MIN && c.out_rows % MM_M == 0 && c.k % (32 * MM_SCB) == 0 &&
+           c.xq && c.xs && (uintptr_t)c.q0 % 16 == 0 && (!c.q1 || (uintptr_t)c.q1 % 16 == 0) &&
+           (uintptr_t)c.xq % 16 == 0 && (uintptr_t)c.s0 % 16 == 0 && (!c.s1 || (uintptr_t)c.s1 % 16 == 0) &&
+           (uintptr_t)c.xs % 16 == 0 && c.E * c.out_rows < ((int64_t)1 << 31) && c.R * c.K < ((int64_t)1 << 31) &&
+           encode_tiled() != nullptr;
+}
+
+// The fewest rows of a group that takes the tensor cores (q8_set_grouped_tensor_core_rows); 0: none does.  Measured
+// on correlated chunks (every group the chunk's rows): 16-row groups 89 us a chunk against 63 on the CUDA cores,
+// 32-row groups 99 against 101, 64-row groups 99 against 176.
+int kGroupedMmaMinRows = 32;
+
+int moe_mma_min_rows() { return kGroupedMmaMinRows ? kGroupedMmaMinRows : MM_NMAX + 1; }
+
+bool moe_mma_grouped(const ExpertCall& c) {
+    return kGroupedMmaMinRows && c.R >= kGroupedMmaMinRows && moe_mma_supported(c);
+}
 int moe_mma_max_rows() { return MM_NMAX; }
 
 cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carve& ws, cudaStream_t st,
-                           const float* res) {
+                           const float* res, int nmin) {
     if (!moe_mma_supported(c)) return cudaErrorInvalidConfiguration;
     MmaParams p = {};
     // K split: up to MM_SMAX slices of at least 4 stages, when the workspace holds their partial sums (the kernel picks
@@ -533,7 +656,8 @@ cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carv
     int S = nst_all / 4;
     S = S < 1 ? 1 : (S > MM_SMAX ? MM_SMAX : S);
     const int tiles = (int)(c.out_rows / MM_M);
-    const int64_t slots = std::min<int64_t>(max_groups, c.R * c.K / MM_MIN);  // eligible groups at most
+    if (nmin < MM_MIN || nmin > MM_NMAX) return cudaErrorInvalidValue;
+    const int64_t slots = std::min<int64_t>(max_groups, c.R * c.K / nmin);  // eligible groups at most
     if (S > 1) {
         const size_t bytes = (size_t)slots * tiles * S * 2 * MM_NMAX * MM_M * sizeof(float);
         const size_t at = (ws.used + 255) & ~size_t(255);
@@ -544,12 +668,16 @@ cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carv
             S = 1;
         }
     }
+    const uint64_t nb = (uint64_t)(c.k / 32), wrows = (uint64_t)(c.E * c.out_rows);
+    bool maps = map_2d(&p.tw0, false, c.q0, (uint64_t)c.k, wrows, (uint64_t)c.k, MM_ROWB, MM_M) &&
+                map_2d(&p.ts0, true, c.s0, nb, wrows, nb * 4, MM_SCB, MM_M);
+    if (maps && c.q1)
+        maps = map_2d(&p.tw1, false, c.q1, (uint64_t)c.k, wrows, (uint64_t)c.k, MM_ROWB, MM_M) &&
+               map_2d(&p.ts1, true, c.s1, nb, wrows, nb * 4, MM_SCB, MM_M);
+    if (!maps) return cudaErrorInvalidValue;
     p.S = S;
     p.gate_up = c.q1 != nullptr;
-    p.q0 = c.q0;
-    p.s0 = c.s0;
-    p.q1 = c.q1;
-    p.s1 = c.s1;
+    p.nmin = nmin;
     p.E = (int)c.E;
     p.out_rows = (int)c.out_rows;
     p.k = (int)c.k;
@@ -590,10 +718,10 @@ __global__ void dense_plan_kernel(int32_t* active, int32_t* offsets, int32_t* li
 }  // namespace
 
 bool dense_mma_supported(const GemvCall& g) {
-    if (g.mode != 1 || g.R < MM_MIN || g.R > MM_NMAX || g.dots || g.norm_a || g.k % (32 * MM_BPS)) return false;
-    if ((uintptr_t)g.xq % 16 || (uintptr_t)g.xs % 8) return false;
+    if (g.mode != 1 || g.R < MM_MIN || g.R > MM_NMAX || g.dots || g.norm_a || g.k % (32 * MM_SCB)) return false;
+    if ((uintptr_t)g.xq % 16 || (uintptr_t)g.xs % 16 || !encode_tiled()) return false;
     for (int i = 0; i < g.nseg; ++i)
-        if (g.seg[i].n % MM_M || (uintptr_t)g.seg[i].q % 16 || (uintptr_t)g.seg[i].s % 8) return false;
+        if (g.seg[i].n % MM_M || (uintptr_t)g.seg[i].q % 16 || (uintptr_t)g.seg[i].s % 16) return false;
     return true;
 }
 
@@ -625,7 +753,7 @@ cudaError_t launch_dense_mma(const GemvCall& g, Carve& ws, cudaStream_t st) {
         c.err = g.err;
         c.pdl = g.pdl;
         Carve cv = ws;  // each segment's launch may reuse the same scratch after the one before it
-        e = launch_moe_mma(c, g.seg[i].y, 1, cv, st, g.seg[i].residual);
+        e = launch_moe_mma(c, g.seg[i].y, 1, cv, st, g.seg[i].residual, MM_MIN);
     }
     return e;
 }

@@ -449,15 +449,21 @@ def test_moe_chunk(q8, ws, moe_host, moe_dev, mode, R):
     _compare_moe(out, ref, mode, 8)
 
 
-@pytest.mark.parametrize("mode,R", [(0, 32), (1, 16), (1, 32), (1, 64), (2, 64)])
-def test_moe_chunk_correlated_rows(q8, ws, moe_host, moe_dev, mode, R):
-    # every row near one x0: the rows share their experts, so each expert's group holds all R rows (int8 mode: the
-    # tensor-core products, groups of 16 to 64 rows)
+@pytest.mark.parametrize("mode,R,grouped", [(0, 32, None), (1, 16, 16), (1, 16, 0), (1, 32, 16), (1, 32, None),
+                                            (1, 64, None), (1, 64, 0), (2, 64, None)])
+def test_moe_chunk_correlated_rows(q8, ws, moe_host, moe_dev, mode, R, grouped):
+    # every row near one x0: the rows share their experts, so each expert's group holds all R rows.  Int8 mode: groups
+    # of `grouped`..64 rows take the tensor-core products (None: the library's default of 32; 0: the CUDA cores only)
     x0 = synth.normal((1, 2048), 2, recipes.VEC + 81)
     x = (x0 + 0.01 * synth.normal((R, 2048), 2, recipes.VEC + 82)).astype(np.float32)
     w = oracle.MoeWeights(2048, 768, 128, 8, **moe_host)
     ref = oracle.moe_rows(mode, w, x)
-    out = _run_moe_gpu(q8, ws, moe_dev, mode, x, 8)
+    if grouped is not None:
+        q8.set_grouped_tensor_core_rows(grouped)
+    try:
+        out = _run_moe_gpu(q8, ws, moe_dev, mode, x, 8)
+    finally:
+        q8.set_grouped_tensor_core_rows(32)
     _compare_moe(out, ref, mode, 8)
 
 

@@ -71,6 +71,17 @@ def test_refusals_before_any_launch(q8):
     assert lib.decode_step(None, None) == -1
 
 
+def test_tensor_core_thresholds_refuse_bad_row_counts(q8):
+    lib = q8.lib
+    for setter in (lib.q8_set_tensor_core_rows, lib.q8_set_grouped_tensor_core_rows):
+        for bad in (1, 15, 65, -16):
+            assert setter(bad) == -1
+            assert "0 (off) or 16 to 64" in q8.last_error()
+    assert lib.q8_set_grouped_tensor_core_rows(16) == 0
+    assert lib.q8_set_grouped_tensor_core_rows(32) == 0  # the default again
+    assert lib.q8_set_tensor_core_rows(0) == 0
+
+
 _RANK = r"""
 import json, sys
 sys.path.insert(0, {root!r})
