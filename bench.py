@@ -47,6 +47,8 @@ def parse():
                     help="dense int8 projections of N..64 rows on the tensor cores (0: off; the library's default)")
     ap.add_argument("--grouped-tensor-core-rows", type=int, default=None, metavar="N",
                     help="int8 expert groups of N..64 rows on the tensor cores (0: off; the library's default is 32)")
+    ap.add_argument("--tensor-core-attention", type=int, default=None, choices=[0, 1],
+                    help="prefill chunks' attention on the tensor cores (1, the library's default) or CUDA cores (0)")
     ap.add_argument("--configs-only", action="store_true",
                     help="only the single-operation configurations (projection, attention-side projections, mixture)")
     return ap.parse_args()
@@ -638,6 +640,8 @@ def main():
         q8.set_tensor_core_rows(args.tensor_core_rows)
     if args.grouped_tensor_core_rows is not None:
         q8.set_grouped_tensor_core_rows(args.grouped_tensor_core_rows)
+    if args.tensor_core_attention is not None:
+        q8.set_tensor_core_attention(bool(args.tensor_core_attention))
     if args.chunk_only:
         res = time_chunks(q8, cfg, dev, sh, reps=max(1, args.steps), correlated=args.correlated,
                           rows=(args.chunk_only,))

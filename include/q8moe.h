@@ -141,6 +141,13 @@ Q8_API int q8_set_tensor_core_rows(int rows);
  * the prefill chunks or batch steps) it should affect. */
 Q8_API int q8_set_grouped_tensor_core_rows(int rows);
 
+/* Whether prefill_chunk's causal attention runs on the tensor cores (1, the default) or the CUDA cores (0).  The
+ * tensor-core form scales each tile of queries, keys, values and weights by a power of two, splits every f32 value
+ * into two f16 parts and accumulates the three significant products in f32 (about 2^-22 relative per product); a
+ * tile holding an infinity or a NaN cannot be split, and q8_model_check then reports Q8_EUNSUPPORTED.
+ * Process-wide. */
+Q8_API int q8_set_tensor_core_attention(int on);
+
 /* Debug export of the int8 paths: the q8_gemv call (y as above) that also writes dots[r][o][b] = the exact int32 dot
  * of weight block (o, b) with activation block (r, b), from the same device code; dots is device int32
  * [rows][W.rows][W.cols/32].  The mode is Q8_INT8ACT, or Q8_INT8ACT2 when xq->lo is not NULL: dots is then
@@ -293,6 +300,10 @@ Q8_API int decode_step_trace(q8_model *model, float *hidden, q8_stream stream);
  * graph.  An id outside [0, vocab) or a row past the cache end sets the
  * model's device error word (q8_model_check).  Not for the batch form. */
 Q8_API int prefill_chunk(q8_model *model, const int32_t *tokens, int64_t rows, q8_ws *ws, q8_stream stream);
+/* prefill_chunk that also exports, for per-layer parity checks, the residual rows entering every layer and the final
+ * ones (the input of the final norm): hidden is device f32 [layers + 1][rows][d]. */
+Q8_API int prefill_chunk_trace(q8_model *model, const int32_t *tokens, int64_t rows, q8_ws *ws, float *hidden,
+                               q8_stream stream);
 /* Kernels one step launches: the kernel nodes of the graph the first decode_step captured (0 before it). */
 Q8_API int64_t q8_model_launches_per_step(const q8_model *model);
 /* Reads and clears the model's device error word (synchronizes `stream`): Q8_OK, Q8_EINVAL when a step met an

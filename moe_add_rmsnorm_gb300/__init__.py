@@ -75,6 +75,7 @@ _SIGS = {
     "q8_gemv_noalloc": [_P(q8_mat), _i32, _vp, _P(q8_act), _i64, _vp, _vp],
     "q8_set_tensor_core_rows": [_i32],
     "q8_set_grouped_tensor_core_rows": [_i32],
+    "q8_set_tensor_core_attention": [_i32],
     "moe_route_topk": [_P(q8_mat), _i32, _vp, _P(q8_act), _i64, _i32, _vp, _vp, _vp, _P(q8_moe_plan), _vp, _vp],
     "moe_route_topk_f32": [_vp, _i64, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _P(q8_moe_plan), _vp, _vp],
     "moe_gate_up": [_P(q8_mat), _P(q8_mat), _i64, _i32, _vp, _P(q8_act), _i64, _i32, _vp, _P(q8_moe_plan), _vp,
@@ -87,6 +88,7 @@ _SIGS = {
     "decode_step_launches": [_vp, _vp],
     "decode_step_trace": [_vp, _vp, _vp],
     "prefill_chunk": [_vp, _vp, _i64, _vp, _vp],
+    "prefill_chunk_trace": [_vp, _vp, _i64, _vp, _vp, _vp],
     "q8_model_check": [_vp, _vp],
     "q8_model_wait_selftest": [_vp, ctypes.c_uint, _vp],
     "q8_model_launches_per_step": [_vp],
@@ -205,6 +207,11 @@ def set_grouped_tensor_core_rows(rows: int):
     _check(lib.q8_set_grouped_tensor_core_rows(int(rows)))
 
 
+def set_tensor_core_attention(on: bool):
+    """Prefill chunks' causal attention on the tensor cores (default) or, with False, the CUDA cores."""
+    _check(lib.q8_set_tensor_core_attention(1 if on else 0))
+
+
 def plan_struct(counts, offsets, lists, active):
     return q8_moe_plan(counts.data_ptr(), offsets.data_ptr(), lists.data_ptr(), active.data_ptr())
 
@@ -317,6 +324,12 @@ class Model:
     def prefill(self, tokens, ws, stream=None):
         """tokens: device int32 [rows]; the chunk through every layer (plain launches), last row's token into tok."""
         _check(lib.prefill_chunk(self.handle, tokens.data_ptr(), tokens.numel(), ws.handle, _stream(stream)))
+
+    def prefill_trace(self, tokens, ws, hidden, stream=None):
+        """prefill() that also copies the residual rows entering every layer and the final ones into hidden (device
+        f32 [layers + 1, rows, d])."""
+        _check(lib.prefill_chunk_trace(self.handle, tokens.data_ptr(), tokens.numel(), ws.handle, hidden.data_ptr(),
+                                       _stream(stream)))
 
     def check(self, stream=None):
         _check(lib.q8_model_check(self.handle, _stream(stream)))

@@ -15,6 +15,7 @@ namespace q8 {
 
 extern int kDenseMmaMinRows;    // gemv.cu
 extern int kGroupedMmaMinRows;  // moe_mma.cu
+extern int kChunkAttnTensorCores;  // decode.cu
 
 static thread_local char g_err[512];
 
@@ -516,6 +517,13 @@ int q8_set_grouped_tensor_core_rows(int rows) {
     g_err[0] = 0;
     if (rows != 0 && (rows < 16 || rows > 64)) return fail(Q8_EINVAL, "rows %d: 0 (off) or 16 to 64", rows);
     kGroupedMmaMinRows = rows;
+    return Q8_OK;
+}
+
+int q8_set_tensor_core_attention(int on) {
+    g_err[0] = 0;
+    if (on != 0 && on != 1) return fail(Q8_EINVAL, "on %d: 0 or 1", on);
+    kChunkAttnTensorCores = on;
     return Q8_OK;
 }
 

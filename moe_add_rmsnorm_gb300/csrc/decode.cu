@@ -24,6 +24,8 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "stream.cuh"
+#include "tcgen05.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -791,6 +793,316 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
     }
 }
 
+// The same partials on the tensor cores.  CTA (key/value head g, position group pg, row block rb) takes query vectors
+// m = 8 * (row in block) + (head in group) of rows rb*TCA_ROWS .. +TCA_ROWS-1 (128 vectors: the MMA's M) against the
+// group's 128 positions, in one pass (no running rescale: the group is the unit the fold combines).  Every f32
+// operand is split into two f16 parts, x = hi + lo (hi = x rounded to f16, lo = the remainder rounded to f16: the
+// pair holds x to about 2^-22 relative), and the three products hi*hi + hi*lo + lo*hi are accumulated in f32 in
+// tensor memory; the lo*lo term (about 2^-22 relative) is left out.
+//  - S = Q K^T: 3 x 8 MMAs (M 128 query vectors, N 128 positions, K 16 dims each), the hi*hi products into TMEM
+//    columns 0..127 and the cross products into 128..255, added in f32 when read (the tensor cores' accumulation
+//    rounds each step; keeping the large terms apart from the small halves the steps that round them).
+//  - Thread (vector m = 32 * (w % 4) + lane, positions 32 * (w / 4) ..) scales and masks its 32 scores (row r
+//    attends positions 0 .. posr[r]), and with its vector's three other threads takes the max and the sum of the
+//    weights e = exp(s - max); the weights go back, split the same way, as the A operand of the second product
+//    (positions along K) over the queries' buffers.
+//  - O = E V: 3 x 8 MMAs (N 128 dims, K 16 positions each), hi*hi into columns 256..383 and the cross products into
+//    384..511; the value rows were transposed when converted (dims as B's rows, positions along K).
+// Before the split each operand tile is scaled by a power of two (the weights by 2^14; queries, keys and values so
+// that the tile's largest magnitude lies in [2^14, 2^15)), which keeps the lo parts normal f16 numbers; the results
+// are scaled back exactly.  The partial (128 weighted values, max, sum) goes to part[r][head][pg] as
+// chunk_attention_kernel writes it.  A tile holding an infinity or a NaN sets kErrHalfRange in the error word.
+constexpr int TCA_ROWS = 16;                       // rows per CTA
+constexpr int TCA_M = TCA_ROWS * ATT_MAXG;         // query vectors per CTA: the MMA's M
+constexpr int TCA_P = ACH_GROUP * 64;              // positions per CTA: the partials' position group
+constexpr int TCA_THREADS = 512;
+constexpr int TCA_TILE = 128 * ATT_HD * 2;         // bytes of an f16 operand tile of 128 rows x 128
+constexpr uint32_t TCA_SBO = (ATT_HD / 8) * 128;   // bytes between its 8-row groups
+constexpr size_t TCA_SMEM = 6 * (size_t)TCA_TILE + 2 * (size_t)TCA_M * 4 * sizeof(float);
+constexpr int kErrHalfRange = 8;                   // error bit: a tensor-core attention tile that is not finite
+static_assert(TCA_M == 128 && TCA_P == 128 && ATT_HD == 128, "one 128 x 128 tile each way");
+
+__device__ __forceinline__ uint32_t tca_off(int r, int k8) {  // bytes of (row r, halves 8 * k8 .. 8 * k8 + 7)
+    return (uint32_t)(r >> 3) * TCA_SBO + (uint32_t)k8 * 128 + (uint32_t)(r & 7) * 16;
+}
+
+__device__ __forceinline__ uint32_t half2_bits(__half a, __half b) {
+    return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+}
+
+constexpr int TCA_PEXP = 14;  // the weights e (at most 1) are split as e * 2^14
+
+// 2^e as a float, e in [-126, 127].
+__device__ __forceinline__ float exp2_int(int e) { return __int_as_float((127 + e) << 23); }
+
+// max(a, b), not a number when b is not one (so an operand's NaN reaches the tile maximum).
+__device__ __forceinline__ float fmax_nan(float a, float b) { return b != b ? b : fmaxf(a, b); }
+
+// Copies eight values to v and returns their largest magnitude.
+__device__ __forceinline__ float load8_amax(const float (&x)[8], float (&v)[8]) {
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[i] = x[i];
+        m = fmax_nan(m, fabsf(x[i]));
+    }
+    return m;
+}
+
+// The CTA's largest magnitude over the first n of every thread's xa (all threads call it; bits of non-negative
+// floats order as unsigned integers, and a NaN's above every finite value's).
+__device__ __forceinline__ float block_amax(const float (&xa)[4], int n, unsigned int* slot) {
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (i < n) m = fmax_nan(m, xa[i]);
+    unsigned int b = __float_as_uint(m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(slot, b);
+    __syncthreads();
+    return __uint_as_float(*slot);
+}
+
+// The power of two that brings a tile's largest magnitude into [2^14, 2^15) (0 for an all-zero tile); a maximum that
+// is not finite sets kErrHalfRange in the error word.
+__device__ __forceinline__ int tile_exponent(float amax, int* err) {
+    if (!(amax <= FLT_MAX)) {
+        if (err && threadIdx.x == 0) atomicOr(err, kErrHalfRange);
+        return 0;
+    }
+    if (amax == 0.f) return 0;
+    const int e = 14 - ilogbf(amax);
+    return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+
+// Eight f32 values times 2^e (exact) into f16 hi and lo parts: hi = the value rounded to f16, lo = the remainder
+// rounded to f16 (one 16-byte core-matrix row each).
+__device__ __forceinline__ void split8_scaled(const float (&x)[8], int e, uint4& hi, uint4& lo) {
+    const float f = exp2_int(e);
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float a = x[2 * i] * f, b = x[2 * i + 1] * f;
+        const __half h0 = __float2half_rn(a), h1 = __float2half_rn(b);
+        const __half l0 = __float2half_rn(a - __half2float(h0)), l1 = __float2half_rn(b - __half2float(h1));
+        h[i] = half2_bits(h0, h1);
+        l[i] = half2_bits(l0, l1);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__global__ void __launch_bounds__(TCA_THREADS, 1) chunk_attention_tc_kernel(const float* qr, const float* k_cache,
+                                                                            const float* v_cache,
+                                                                            const int32_t* posr, int R, int heads,
+                                                                            int kv, int ctx, float scale, float* part,
+                                                                            int ngroups, int* err) {
+    extern __shared__ __align__(1024) unsigned char tsm[];
+    unsigned char* qh = tsm;                  // queries, then the weights E (hi parts)
+    unsigned char* ql = tsm + TCA_TILE;       // (lo parts)
+    unsigned char* kh = tsm + 2 * TCA_TILE;   // key rows
+    unsigned char* kl = tsm + 3 * TCA_TILE;
+    unsigned char* vh = tsm + 4 * TCA_TILE;   // value rows, transposed
+    unsigned char* vl = tsm + 5 * TCA_TILE;
+    float* pmax = reinterpret_cast<float*>(tsm + 6 * TCA_TILE);  // [vector][4] partial maxima
+    float* psum = pmax + TCA_M * 4;                                // [vector][4] partial sums
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    __shared__ int lim[TCA_ROWS];
+    __shared__ unsigned int amax[3];  // the query, key and value tiles' largest magnitudes (f32 bits)
+    const int g = blockIdx.x, pg = blockIdx.y, rb = blockIdx.z;
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    const int G = heads / kv;
+    const int r0 = rb * TCA_ROWS, nr = min(TCA_ROWS, R - r0);
+    if (nr <= 0) return;
+    int maxpos = -1;
+    for (int i = 0; i < nr; ++i) maxpos = max(maxpos, min(posr[r0 + i], ctx - 1));
+    const int p_begin = pg * TCA_P;
+    if (p_begin > maxpos) return;  // every row of the block ends before this group
+    if (t < TCA_ROWS) lim[t] = t < nr ? min(posr[r0 + t], ctx - 1) : -1;
+    if (t == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    if (t < 3) amax[t] = 0u;
+    if (w == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tc_smem(&tmem_base)),
+                     "r"(512));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    __syncthreads();  // the tile maxima start at zero
+    float xv[4][8];   // a thread's operand values between the tile's max and its split
+    float xa[4];      // their largest magnitudes
+    int evs = 0;
+    // Each operand tile is scaled by a power of two before the split, so that its largest magnitude lies in
+    // [2^14, 2^15): the lo parts of all but the tile's tiniest values stay normal f16 numbers.  The products are
+    // scaled back exactly.
+#pragma unroll
+    for (int u = 0; u < TCA_M * 16 / TCA_THREADS; ++u) {  // queries: vector m, dims 8 * k8 ..
+        const int task = t + u * TCA_THREADS, m = task >> 4, k8 = task & 15, rr = m >> 3, hh = m & 7;
+        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (rr < nr && hh < G) {
+            const float4* src = reinterpret_cast<const float4*>(qr + ((int64_t)(r0 + rr) * heads + g * G + hh) * ATT_HD) + 2 * k8;
+            const float4 a = src[0], b = src[1];
+            x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+        }
+        xa[u] = load8_amax(x, xv[u]);
+    }
+    const int eq = tile_exponent(block_amax(xa, TCA_M * 16 / TCA_THREADS, &amax[0]), err);
+#pragma unroll
+    for (int u = 0; u < TCA_M * 16 / TCA_THREADS; ++u) {
+        const int task = t + u * TCA_THREADS, m = task >> 4, k8 = task & 15;
+        uint4 hi, lo;
+        split8_scaled(xv[u], eq, hi, lo);
+        *reinterpret_cast<uint4*>(qh + tca_off(m, k8)) = hi;
+        *reinterpret_cast<uint4*>(ql + tca_off(m, k8)) = lo;
+    }
+#pragma unroll
+    for (int u = 0; u < TCA_P * 16 / TCA_THREADS; ++u) {  // key rows: position n, dims 8 * k8 ..
+        const int task = t + u * TCA_THREADS, n = task >> 4, k8 = task & 15, p = p_begin + n;
+        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (p <= maxpos) {
+            const float4* src = reinterpret_cast<const float4*>(k_cache + ((int64_t)g * ctx + p) * ATT_HD) + 2 * k8;
+            const float4 a = __ldg(src), b = __ldg(src + 1);
+            x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+        }
+        xa[u] = load8_amax(x, xv[u]);
+    }
+    const int ek = tile_exponent(block_amax(xa, TCA_P * 16 / TCA_THREADS, &amax[1]), err);
+#pragma unroll
+    for (int u = 0; u < TCA_P * 16 / TCA_THREADS; ++u) {
+        const int task = t + u * TCA_THREADS, n = task >> 4, k8 = task & 15;
+        uint4 hi, lo;
+        split8_scaled(xv[u], ek, hi, lo);
+        *reinterpret_cast<uint4*>(kh + tca_off(n, k8)) = hi;
+        *reinterpret_cast<uint4*>(kl + tca_off(n, k8)) = lo;
+    }
+    static_assert((ATT_HD / 4) * (TCA_P / 8) == TCA_THREADS, "one value task a thread");
+    {  // values: dims 4 * d4 .. +3, positions 8 * p8 .. +7 (transposed: dims as B's rows)
+        const int d4 = t & (ATT_HD / 4 - 1), p8 = t / (ATT_HD / 4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int p = p_begin + 8 * p8 + i;
+            const float4 v4 = p <= maxpos ? __ldg(reinterpret_cast<const float4*>(v_cache + ((int64_t)g * ctx + p) * ATT_HD) + d4)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            xv[0][i] = v4.x, xv[1][i] = v4.y, xv[2][i] = v4.z, xv[3][i] = v4.w;
+        }
+        float mv = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mv = fmax_nan(mv, fabsf(xv[j][i]));
+        xa[0] = mv;
+        const int ev = tile_exponent(block_amax(xa, 1, &amax[2]), err);
+        evs = ev;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 hi, lo;
+            split8_scaled(xv[j], ev, hi, lo);
+            *reinterpret_cast<uint4*>(vh + tca_off(4 * d4 + j, p8)) = hi;
+            *reinterpret_cast<uint4*>(vl + tca_off(4 * d4 + j, p8)) = lo;
+        }
+    }
+    const float s_back = exp2_int(-eq) * exp2_int(-ek) * scale;  // scores: D * 2^-(eq + ek), then the 1/sqrt(hd) scale
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the operands, to the tensor cores
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = tmem_base;
+    const uint32_t idesc = tc_idesc_f16(128, 128);
+    if (t == 0) {
+#pragma unroll 1
+        for (int j = 0; j < ATT_HD / 16; ++j) {  // K = 16 dims: two core matrices along K
+            const int o = j * 256;
+            tc_mma_f16(tmem, tc_desc(qh + o, TCA_SBO), tc_desc(kh + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
+            tc_mma_f16(tmem + 128, tc_desc(qh + o, TCA_SBO), tc_desc(kl + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
+            tc_mma_f16(tmem + 128, tc_desc(ql + o, TCA_SBO), tc_desc(kh + o, TCA_SBO), idesc, 1u);
+        }
+        tc_commit(&bar);
+    }
+    bool ok = __syncthreads_and(mbar_wait(&bar, 0, err) ? 1 : 0) != 0;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const int lq = w & 3, cq = w >> 2, m = 32 * lq + lane, rr = m >> 3, hh = m & 7;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
+    const int lm = lim[rr];
+    float s[32];
+    {
+        uint32_t sv[32], sx[32];
+        tc_ld32(lane_base + 32 * cq, sv);        // hi * hi
+        tc_ld32(lane_base + 128 + 32 * cq, sx);  // hi * lo + lo * hi
+        tc_wait_ld();
+        float mx = -FLT_MAX;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float d = __uint_as_float(sv[i]) + __uint_as_float(sx[i]);
+            s[i] = p_begin + 32 * cq + i <= lm ? d * s_back : -FLT_MAX;
+            mx = fmaxf(mx, s[i]);
+        }
+        pmax[m * 4 + cq] = mx;
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();  // every partial max; the first product is read (its operands may be overwritten)
+    const float M = fmaxf(fmaxf(pmax[m * 4], pmax[m * 4 + 1]), fmaxf(pmax[m * 4 + 2], pmax[m * 4 + 3]));
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        s[i] = (M == -FLT_MAX || s[i] == -FLT_MAX) ? 0.f : expf(s[i] - M);
+        sum += s[i];
+    }
+    psum[m * 4 + cq] = sum;
+#pragma unroll
+    for (int k8 = 0; k8 < 4; ++k8) {  // the weights (at most 1) times 2^14, positions 32 * cq + 8 * k8 .., as A
+        uint4 hi, lo;
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = s[8 * k8 + i];
+        split8_scaled(x, TCA_PEXP, hi, lo);
+        *reinterpret_cast<uint4*>(qh + tca_off(m, 4 * cq + k8)) = hi;
+        *reinterpret_cast<uint4*>(ql + tca_off(m, 4 * cq + k8)) = lo;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (t == 0 && ok) {
+#pragma unroll 1
+        for (int j = 0; j < TCA_P / 16; ++j) {  // K = 16 positions
+            const int o = j * 256;
+            tc_mma_f16(tmem + 256, tc_desc(qh + o, TCA_SBO), tc_desc(vh + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
+            tc_mma_f16(tmem + 384, tc_desc(qh + o, TCA_SBO), tc_desc(vl + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
+            tc_mma_f16(tmem + 384, tc_desc(ql + o, TCA_SBO), tc_desc(vh + o, TCA_SBO), idesc, 1u);
+        }
+        tc_commit(&bar);
+    }
+    if (ok) ok = __syncthreads_and(mbar_wait(&bar, 1, err) ? 1 : 0) != 0;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (ok) {
+        uint32_t ov[32], ox[32];
+        tc_ld32(lane_base + 256 + 32 * cq, ov);  // hi * hi
+        tc_ld32(lane_base + 384 + 32 * cq, ox);  // hi * lo + lo * hi
+        tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) + __uint_as_float(ox[i]));
+        if (rr < nr && hh < G) {
+            float* dst = part + (((int64_t)(r0 + rr) * heads + g * G + hh) * ngroups + pg) * ACH_PS;
+            const float o_back = exp2_int(-TCA_PEXP) * exp2_int(-evs);  // exact
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                reinterpret_cast<float4*>(dst + 32 * cq)[i] =
+                    make_float4(__uint_as_float(ov[4 * i]) * o_back, __uint_as_float(ov[4 * i + 1]) * o_back,
+                                __uint_as_float(ov[4 * i + 2]) * o_back, __uint_as_float(ov[4 * i + 3]) * o_back);
+            if (cq == 0) {
+                dst[ATT_HD] = M;
+                dst[ATT_HD + 1] = ((psum[m * 4] + psum[m * 4 + 1]) + psum[m * 4 + 2]) + psum[m * 4 + 3];
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (w == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+}
+
 // Row r, head h: the position groups' results folded in group order, out = num / den, and its int8 form.  A warp
 // per (row, head), lane l the dims l, l + 32, l + 64, l + 96.
 __global__ void __launch_bounds__(256) chunk_attn_fold_kernel(const float* part, const int32_t* posr, int R, int heads,
@@ -934,6 +1246,9 @@ cudaError_t launch_pos_add(int32_t* pos, int add, const int* err, cudaStream_t s
     return cudaGetLastError();
 }
 
+// Whether a prefill chunk's attention runs on the tensor cores (q8_set_tensor_core_attention).
+int kChunkAttnTensorCores = 1;
+
 int chunk_attn_groups(int ctx) { return (ctx + ACH_GROUP * 64 - 1) / (ACH_GROUP * 64); }
 
 void chunk_attention_scratch(int64_t rows, int heads, int ctx, size_t* bytes) {
@@ -951,11 +1266,20 @@ cudaError_t launch_chunk_attention(const ChunkAttnCall& c, Carve& ws, cudaStream
                                                           c.posr, c.heads, c.kv, c.ctx, c.k_cache, c.v_cache, qr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chunk_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ACH_SMEM);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)c.kv, (unsigned)ng, (unsigned)((c.rows + ACH_RB - 1) / ACH_RB));
-    chunk_attention_kernel<<<grid, 256, ACH_SMEM, st>>>(qr, c.k_cache, c.v_cache, c.posr, (int)c.rows, c.heads, c.kv,
-                                                       c.ctx, (float)(1.0 / sqrt((double)c.hd)), part, ng);
+    const float scale = (float)(1.0 / sqrt((double)c.hd));
+    if (kChunkAttnTensorCores) {
+        e = cudaFuncSetAttribute(chunk_attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TCA_SMEM);
+        if (e != cudaSuccess) return e;
+        const dim3 grid((unsigned)c.kv, (unsigned)ng, (unsigned)((c.rows + TCA_ROWS - 1) / TCA_ROWS));
+        chunk_attention_tc_kernel<<<grid, TCA_THREADS, TCA_SMEM, st>>>(qr, c.k_cache, c.v_cache, c.posr, (int)c.rows,
+                                                                       c.heads, c.kv, c.ctx, scale, part, ng, c.err);
+    } else {
+        e = cudaFuncSetAttribute(chunk_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ACH_SMEM);
+        if (e != cudaSuccess) return e;
+        const dim3 grid((unsigned)c.kv, (unsigned)ng, (unsigned)((c.rows + ACH_RB - 1) / ACH_RB));
+        chunk_attention_kernel<<<grid, 256, ACH_SMEM, st>>>(qr, c.k_cache, c.v_cache, c.posr, (int)c.rows, c.heads,
+                                                           c.kv, c.ctx, scale, part, ng);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t warps = c.rows * c.heads;

@@ -307,6 +307,7 @@ struct ChunkAttnCall {
     int8_t* outq = nullptr;         // optional quantized output
     int8_t* outl = nullptr;         // with outq: the two-word form's low words
     float* outs = nullptr;
+    int* err = nullptr;             // error word: bit 8 when the tensor-core form meets a value that is not finite
 };
 void chunk_attention_scratch(int64_t rows, int heads, int ctx, size_t* bytes);
 cudaError_t launch_chunk_attention(const ChunkAttnCall& c, Carve& ws, cudaStream_t st);

@@ -916,7 +916,20 @@ int decode_step(q8_model* m, q8_stream stream) {
     return e == cudaSuccess ? Q8_OK : model_fail(Q8_ECUDA, "decode_step: %s", cudaGetErrorString(e));
 }
 
+// The prefill launches; with `trace`, the residual rows entering every layer, and the final ones, are copied to
+// trace[l][R][d] (l = 0 .. layers).
+static int prefill_launches(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_stream stream, float* trace);
+
 int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_stream stream) {
+    return prefill_launches(m, tokens, R, ws, stream, nullptr);
+}
+
+int prefill_chunk_trace(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, float* hidden, q8_stream stream) {
+    if (!hidden) return model_fail(Q8_EINVAL, "prefill_chunk_trace: hidden null");
+    return prefill_launches(m, tokens, R, ws, stream, hidden);
+}
+
+static int prefill_launches(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_stream stream, float* trace) {
     if (!m) return model_fail(Q8_EINVAL, "model: null");
     if (!tokens || !ws) return model_fail(Q8_EINVAL, "prefill_chunk: tokens or ws null");
     if (R < 1 || R > (1 << 20)) return model_fail(Q8_EINVAL, "prefill_chunk: %lld rows", (long long)R);
@@ -989,6 +1002,8 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
     // Plain launches in order, no programmatic overlap (each launch reads what the one before it wrote).
     Q8_TRY(launch_chunk_setup(tokens, R, d.embed, D, d.vocab, d.pos, (int)d.ctx, posr, h, m->err, st));
     for (int64_t l = 0; l < d.layers; ++l) {
+        if (trace)
+            Q8_TRY(cudaMemcpyAsync(trace + l * R * D, h, (size_t)(R * D) * sizeof(float), cudaMemcpyDeviceToDevice, st));
         Q8_TRY(norm(h, m->attn_norm[l], R));
         {
             GemvCall g;
@@ -1029,6 +1044,7 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
             a.outq = attq;
             a.outl = attl;
             a.outs = atts;
+            a.err = m->err;
             Carve cv = cb;
             Q8_TRY_WS(launch_chunk_attention(a, cv, st), cv);
         }
@@ -1135,6 +1151,9 @@ int prefill_chunk(q8_model* m, const int32_t* tokens, int64_t R, q8_ws* ws, q8_s
             Q8_TRY_WS(launch_down_combine(c, cv, st), cv);
         }
     }
+    if (trace)
+        Q8_TRY(cudaMemcpyAsync(trace + d.layers * R * D, h, (size_t)(R * D) * sizeof(float), cudaMemcpyDeviceToDevice,
+                               st));
     // the last row's logits and greedy token; the position ends R rows on
     Q8_TRY(launch_pos_add(d.pos, (int)(R - 1), m->err, st));
     {
@@ -1192,6 +1211,9 @@ int q8_model_check(q8_model* m, q8_stream stream) {
     if (v & 1) return model_fail(Q8_EINVAL, "a step read a token outside [0, vocab)");
     if (v & 2) return model_fail(Q8_EINVAL, "a step met a position outside [0, ctx)");
     if (v & 4) return model_fail(Q8_ETIMEOUT, "a weight pipeline wait gave up (the step's results are not valid)");
+    if (v & 8)
+        return model_fail(Q8_EUNSUPPORTED, "a prefill chunk's tensor-core attention met a query, key or value that is "
+                                           "not finite");
     return Q8_OK;
 }
 

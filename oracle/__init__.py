@@ -89,6 +89,7 @@ def lib():
             "ora_decode_step": ([i32, ctypes.POINTER(Model), i64, i64, vp], i64),
             "ora_decode_layers": ([i32, ctypes.POINTER(Model), i64, i64, i64, vp], None),
             "ora_decode_layer": ([i32, ctypes.POINTER(Model), i64, i64, vp, vp], None),
+            "ora_probe_arm": ([i32, vp, vp, vp, i32], None),
             "ora_decode_final": ([i32, ctypes.POINTER(Model), vp, vp], i64),
         }
         for name, (args, res) in sig.items():
@@ -273,6 +274,30 @@ class MoeWeights:
         return Moe(self.d, self.dff, self.experts, self.k, *q8, rf, self.sdff, *sh)
 
 
+PROBE_MOE_INPUT, PROBE_ATTN_OUT = 0, 1  # the probe's sites (oracle.h)
+
+
+def _arm_probe(site, n, probe, flips):
+    """Arms the rounding-boundary probe for the site's next activation row (see oracle.h, ora_probe_arm); returns the
+    margins array it fills (0.5 wherever no one-word quantization of the row records one)."""
+    margins = np.full(n, 0.5) if probe else None
+    idx = np.array([int(i) for i, _ in flips] or [0], np.int64)
+    dl = np.array([int(v) for _, v in flips] or [0], np.int32)
+    lib().ora_probe_arm(int(site), None if margins is None else margins.ctypes.data, idx.ctypes.data, dl.ctypes.data,
+                        len(flips))
+    return margins
+
+
+def moe_row_probed(mode, w: MoeWeights, x, flips=()):
+    """One mixture row with the rounding-boundary probe (test support): returns (the row's outputs as moe_rows gives
+    them for one row, the input's margins: per value the signed distance of x/d from the nearest rounding boundary
+    in steps).  flips: (index, delta) pairs added to the input's one-word words before every product reads them."""
+    x = np.ascontiguousarray(np.reshape(x, (1, w.d)), np.float32)
+    margins = _arm_probe(PROBE_MOE_INPUT, w.d, True, flips)
+    out = moe_rows(mode, w, x)
+    return {k: v[0] for k, v in out.items()}, margins
+
+
 def moe_rows(mode, w: MoeWeights, x, residual=None):
     """The mixture over each row of x [R, d]; returns dict of logits, ids, gates, hidden, expert_out, y."""
     x = np.ascontiguousarray(np.atleast_2d(x), np.float32)
@@ -413,13 +438,18 @@ def decode_layers(mode, model: ModelArrays, tok, pos, layers):
     return out
 
 
-def decode_layer(mode, model: ModelArrays, l, pos, h):
+def decode_layer(mode, model: ModelArrays, l, pos, h, probe=False, flips=(), site=PROBE_MOE_INPUT):
     """Layer ``l`` alone from the residual stream ``h`` (f32 [d]) entering it; writes the layer's key/value rows at
-    ``pos`` into the model's host caches.  Returns (the stream leaving the layer as f32, the router's logits f64)."""
+    ``pos`` into the model's host caches.  Returns (the stream leaving the layer as f32, the router's logits f64), and
+    with ``probe`` also the rounding margins (f64, see moe_row_probed) of the probe site's row: the mixture input
+    (PROBE_MOE_INPUT, [d]) or the attention output the O projection reads (PROBE_ATTN_OUT, [heads * hd]); ``flips``
+    adds (index, delta) pairs to that row's one-word words."""
     h = np.array(h, dtype=np.float32, copy=True)
     rl = np.empty(model.cfg["experts"], np.float64)
+    n = model.cfg["d"] if site == PROBE_MOE_INPUT else model.cfg["heads"] * model.cfg["hd"]
+    margins = _arm_probe(site, n, probe, flips) if (probe or flips) else None
     lib().ora_decode_layer(int(mode), ctypes.byref(model.struct), int(l), int(pos), h.ctypes.data, rl.ctypes.data)
-    return h, rl
+    return (h, rl, margins) if probe else (h, rl)
 
 
 def decode_final(mode, model: ModelArrays, h):

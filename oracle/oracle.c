@@ -59,6 +59,36 @@ void ora_gemv_f32act(const int8_t *q, const float *s, int64_t n, int64_t k, cons
     }
 }
 
+/* ==== rounding-boundary probe (test support) ====================================================================
+ * The one-word rule decides each word by rounding x/d; when a value lies within an f32 rounding error of a half-step
+ * boundary, a computation that reaches the same value by another summation order may round it the other way, and
+ * both words are results of the rule.  The probe lets a test see those decisions and take the other one: armed for a
+ * site, it follows that site's next activation row through every one-word quantization of it, records for each value
+ * the signed distance of x/d from the nearest rounding boundary in steps (sign = the direction of that boundary), and
+ * adds the requested deltas to chosen words.  Sites: ORA_PROBE_MOE_INPUT, the input row of the next ora_moe_row call
+ * (which the router and every expert read); ORA_PROBE_ATTN_OUT, the attention output row that the next
+ * ora_decode_layer's O projection reads.  Unarmed (the default) it changes nothing. */
+static int g_probe_armed, g_probe_site;
+static const float *g_probe_src;
+static double *g_probe_margin;
+static int g_probe_recorded;
+static int64_t g_flip_idx[ORA_MAX_FLIPS];
+static int g_flip_delta[ORA_MAX_FLIPS];
+static int g_nflip;
+
+void ora_probe_arm(int site, double *margins, const int64_t *flip_idx, const int32_t *flip_delta, int nflip) {
+    g_probe_armed = 1;
+    g_probe_site = site;
+    g_probe_src = NULL;
+    g_probe_margin = margins;
+    g_probe_recorded = 0;
+    g_nflip = nflip < 0 ? 0 : (nflip > ORA_MAX_FLIPS ? ORA_MAX_FLIPS : nflip);
+    for (int i = 0; i < g_nflip; ++i) {
+        g_flip_idx[i] = flip_idx[i];
+        g_flip_delta[i] = flip_delta[i];
+    }
+}
+
 /* lane/mod.rs module docs ("llama.cpp's one int8 word") and forward_shim.rs, ForwardShim::activation
  * (QuantFormat::OneWord): an activation read by a Q8_0 product is one int8 word per value plus one f32 scale per
  * 32-value block.  The pages do not print the rule; the reading taken (the usual one for that format):
@@ -76,14 +106,27 @@ void ora_quantize(const float *x, int64_t n, int8_t *xq, float *xs) {
         xs[b] = d;
         for (int t = 0; t < ORA_QBLOCK; ++t) {
             int8_t w = 0;
+            double margin = 0.5;
             if (d != 0.0f) {
-                float r = roundf(v[t] / d);
+                float qv = v[t] / d;
+                float r = roundf(qv);
+                double off = (double)qv - (double)r;
+                margin = off >= 0.0 ? 0.5 - off : -(0.5 + off);
                 if (r > 127.0f) r = 127.0f;
                 if (r < -127.0f) r = -127.0f;
                 w = (int8_t)r;
             }
             xq[b * ORA_QBLOCK + t] = w;
+            if (x == g_probe_src && g_probe_margin && !g_probe_recorded) g_probe_margin[b * ORA_QBLOCK + t] = margin;
         }
+    }
+    if (x == g_probe_src) {
+        g_probe_recorded = 1;
+        for (int i = 0; i < g_nflip; ++i)
+            if (g_flip_idx[i] >= 0 && g_flip_idx[i] < n) {
+                int w = xq[g_flip_idx[i]] + g_flip_delta[i];
+                xq[g_flip_idx[i]] = (int8_t)(w > 127 ? 127 : (w < -127 ? -127 : w));
+            }
     }
 }
 
@@ -293,6 +336,10 @@ void ora_moe_row(int mode, const ora_moe *m, const float *x, const float *residu
                  double *shared_out) {
     const int64_t d = m->d, dff = m->dff, E = m->experts;
     const int K = m->k;
+    if (g_probe_armed && g_probe_site == ORA_PROBE_MOE_INPUT) {  /* this row's input takes the probe (test support) */
+        g_probe_armed = 0;
+        g_probe_src = x;
+    }
     double *l = (double *)malloc(sizeof(double) * (size_t)E);
     if (m->router_f32)
         ora_gemv_f32w(m->router_f32, E, d, x, l);
@@ -355,6 +402,7 @@ void ora_moe_row(int mode, const ora_moe *m, const float *x, const float *residu
     free(h32);
     free(yj);
     free(acc);
+    if (g_probe_src == x) g_probe_src = NULL;
 }
 
 /* lane_link.rs, Link::class_launch (MoeTokenSort) and lane/arena.rs, scratch (a chunk's choices counted per expert,
@@ -481,7 +529,12 @@ void ora_decode_layer(int mode, const ora_model *m, int64_t l, int64_t pos, floa
                       att + hh * hd);
     }
     to_f32(att, H * hd, x32);
+    if (g_probe_armed && g_probe_site == ORA_PROBE_ATTN_OUT) {  /* the O projection's input takes the probe */
+        g_probe_armed = 0;
+        g_probe_src = x32;
+    }
     ora_gemv(mode, m->wo[l].q, m->wo[l].s, d, H * hd, x32, o);
+    if (g_probe_src == x32) g_probe_src = NULL;
     to_f32(o, d, o32);
     /* feed-forward half: the norm of h + o (the sum kept as the residual) feeds the mixture */
     ora_add_rmsnorm(h, o32, m->ffn_norm[l], 1, d, m->eps, h, n64);

@@ -82,6 +82,15 @@ void ora_gemv_f32w(const float *w, int64_t n, int64_t k, const float *x, double 
 void ora_moe_row(int mode, const ora_moe *m, const float *x, const float *residual, double *logits, int32_t *ids,
                  double *gates, double *hidden, double *expert_out, double *y, double *shared_hidden,
                  double *shared_out);
+/* Test support: the next activation row of `site` is probed through every one-word quantization of it — margins (may
+ * be NULL) receives, per value, the signed distance of x/d from the nearest rounding boundary in steps (sign = that
+ * boundary's direction, a signed zero for an exact tie; 0.5 for a value of an all-zero block), and each word flip_idx[i] gets flip_delta[i] added
+ * (clamped to +-127).  Sites: the next ora_moe_row call's input row, or the attention output row that the next
+ * ora_decode_layer's O projection reads.  One-shot; unarmed, nothing changes. */
+#define ORA_MAX_FLIPS 8
+#define ORA_PROBE_MOE_INPUT 0
+#define ORA_PROBE_ATTN_OUT 1
+void ora_probe_arm(int site, double *margins, const int64_t *flip_idx, const int32_t *flip_delta, int nflip);
 /* Choices of a chunk grouped by expert: counts[e], offsets[e] (offsets[experts] = rows*k) and the choice indices
  * r*k+j of each expert in ascending order. */
 void ora_group(const int32_t *ids, int64_t rows, int k, int64_t experts, int32_t *counts, int32_t *offsets,

@@ -224,6 +224,32 @@ def test_decode_full_config_layer_by_layer(q8, mode):
 
 # ---- prefill chunks: R token rows through every layer ---------------------------------------------------------------
 
+def _layer_vs_oracle(mode, om, l, pos, h_in, h_out):
+    """Layer l of the oracle from the GPU's input row h_in, against the GPU's output row h_out (the row and its
+    increment).  In the one-word mode each word of an activation decides by rounding x/d; where that value lies within
+    1e-4 of a step of a rounding boundary, the GPU (whose input to the rule differs from the oracle's in its last bits)
+    may round it the other way, and both words are results of the rule.  When the oracle's own result misses the
+    tolerance, the results with such words rounded the other way (one or two of the four nearest a boundary) are tried:
+    the words of the attention output the O projection reads, then those of the mixture's input.
+    Returns (router logits, error of the matching result, (site, word) rounded the other way or None)."""
+    def err(h_ora):
+        return max(rel_err(h_out, h_ora), rel_err(h_out.astype(np.float64) - h_in, h_ora.astype(np.float64) - h_in))
+    h_ora, rl = oracle.decode_layer(mode, om, l, pos, h_in)
+    e = err(h_ora)
+    if e < TOL[mode] or mode != 1:
+        return rl, e, None
+    for site in (oracle.PROBE_ATTN_OUT, oracle.PROBE_MOE_INPUT):
+        _, _, mg = oracle.decode_layer(mode, om, l, pos, h_in, probe=True, site=site)
+        # the other rounding of each word on a boundary (an exact tie's margin is a signed zero: its sign still
+        # points to the other rounding), alone and in pairs
+        near = [(int(i), -1 if np.signbit(mg[i]) else 1) for i in np.argsort(np.abs(mg))[:4] if abs(mg[i]) < 1e-4]
+        for flips in [[f] for f in near] + [[a, b] for j, a in enumerate(near) for b in near[j + 1:]]:
+            h_alt, _ = oracle.decode_layer(mode, om, l, pos, h_in, flips=flips, site=site)
+            if err(h_alt) < TOL[mode]:
+                return rl, err(h_alt), (site, [i for i, _ in flips])
+    return rl, e, None
+
+
 def _prefill_vs_oracle(q8, cfg, mode, R, pos0, tokens, seed, cache_layers=None):
     import torch
     m, arr, t, tok, pos, logits = build(q8, cfg, seed, mode)
@@ -252,12 +278,18 @@ def _prefill_vs_oracle(q8, cfg, mode, R, pos0, tokens, seed, cache_layers=None):
     return m, tok, pos, logits
 
 
+@pytest.mark.parametrize("attention", ["tensor", "cuda"])
 @pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("cfg,R", [(SMALL, 1), (SMALL, 5), (SMALL, 17), (UNFUSED, 6)], ids=["s1", "s5", "s17", "u6"])
-def test_prefill_chunk_matches_oracle(q8, mode, cfg, R):
+def test_prefill_chunk_matches_oracle(q8, mode, cfg, R, attention):
+    """Both forms of the chunk attention (tensor cores with split f16 operands; CUDA cores in f32)."""
     rng = np.random.default_rng(R)
     tokens = [int(v) for v in rng.integers(0, cfg["vocab"], R)]
-    m, tok, pos, logits = _prefill_vs_oracle(q8, cfg, mode, R, 40 if cfg is SMALL else 30, tokens, 11)
+    q8.set_tensor_core_attention(attention == "tensor")
+    try:
+        m, tok, pos, logits = _prefill_vs_oracle(q8, cfg, mode, R, 40 if cfg is SMALL else 30, tokens, 11)
+    finally:
+        q8.set_tensor_core_attention(True)
     m.close()
 
 
@@ -338,12 +370,109 @@ def test_prefill_full_width_tensor_core_rows(q8, mode, R):
     m.close()
 
 
-def test_prefill_full_width_two_layers(q8):
+@pytest.mark.parametrize("attention", ["tensor", "cuda"])
+def test_prefill_full_width_two_layers(q8, attention):
     """The full layer width (d 2048, 32 q / 4 kv heads, 128 experts, top-8, dff 768) on two layers, a chunk of 8 rows
-    near the end of a 4096-row cache, against the oracle."""
+    near the end of a 4096-row cache, against the oracle end to end in the f32 mode, with either form of the chunk
+    attention (the int8 modes at this width are checked layer by layer below: an activation word decided by the last
+    bits of an input can differ from the oracle's, and downstream layers then follow another, equally valid path)."""
     cfg = dict(recipes.DECODE, layers=2, vocab=1000)
     rng = np.random.default_rng(3)
     tokens = [int(v) for v in rng.integers(0, cfg["vocab"], 8)]
-    m, tok, pos, logits = _prefill_vs_oracle(q8, cfg, 1, 8, 4000, tokens, 15)
+    q8.set_tensor_core_attention(attention == "tensor")
+    try:
+        m, tok, pos, logits = _prefill_vs_oracle(q8, cfg, 0, 8, 4000, tokens, 15)
+    finally:
+        q8.set_tensor_core_attention(True)
     m.close()
+
+
+@pytest.mark.parametrize("attention", ["tensor", "cuda"])
+@pytest.mark.parametrize("mode", [1, 0, 2])
+def test_prefill_per_layer_teacher_forced(q8, mode, attention):
+    """A 20-row chunk at full width on two layers (a full and a partial block of 16 rows; positions 4000..4019 of a
+    4096-row cache), teacher forced: the chunk exports the residual rows entering every layer, and the oracle runs each
+    layer for rows 0..19 in order from the GPU's own inputs (its cache rows for the chunk come from those inputs too).
+    Every layer's output rows, their increments and the key/value rows it wrote are within the mode's tolerance, the
+    oracle's result or, in the one-word mode, the result with one mixture-input word on a rounding boundary rounded
+    the other way (_layer_vs_oracle); a row whose oracle router held a near tie (the K-th and (K+1)-th logits within
+    1e-5 of the largest) is left out.
+    The last row's logits follow from the GPU's final residual row."""
+    import torch
+    cfg = dict(recipes.DECODE, layers=2, vocab=1000)
+    L, R, P, D, K = cfg["layers"], 20, 4000, cfg["d"], cfg["k"]
+    rng = np.random.default_rng(20)
+    tokens = [int(v) for v in rng.integers(0, cfg["vocab"], R)]
+    q8.set_tensor_core_attention(attention == "tensor")
+    try:
+        m, arr, t, tok, pos, logits = build(q8, cfg, 18, mode)
+        ws = q8.Workspace(128 << 20)
+        hidden = torch.empty((L + 1, R, D), dtype=torch.float32, device="cuda")
+        pos.fill_(P)
+        m.prefill_trace(torch.tensor(tokens, dtype=torch.int32, device="cuda"), ws, hidden)
+        torch.cuda.synchronize()
+        m.check()
+    finally:
+        q8.set_tensor_core_attention(True)
+    hid = hidden.cpu().numpy()
+    gl = logits.cpu().numpy()
+    om = oracle.ModelArrays(cfg, **arr)
+    for r in range(R):
+        np.testing.assert_array_equal(hid[0][r], arr["embed"][tokens[r]])
+    flagged, rounded, worst = [], [], 0.0
+    for l in range(L):
+        kc, vc = t["k_cache"][l].cpu().numpy(), t["v_cache"][l].cpu().numpy()
+        for r in range(R):
+            rl, err, word = _layer_vs_oracle(mode, om, l, P + r, hid[l][r], hid[l + 1][r])
+            err_k = rel_err(kc[:, P + r], om.k_cache[l][:, P + r])
+            err_v = rel_err(vc[:, P + r], om.v_cache[l][:, P + r])
+            assert max(err_k, err_v) < TOL[mode], (l, r, err_k, err_v)
+            if _near_tie(rl, K):
+                flagged.append((l, r))
+                continue
+            if word is not None:
+                rounded.append((l, r, word))
+            worst = max(worst, err, err_k, err_v)
+            assert err < TOL[mode], (l, r, err)
+    assert len(flagged) <= 2, flagged
+    assert len(rounded) <= 4, rounded
+    nxt, ora_logits = oracle.decode_final(mode, om, hid[L][R - 1])
+    assert rel_err(gl, ora_logits) < TOL[mode], rel_err(gl, ora_logits)
+    print(f"mode {mode}, {attention} attention: worst per-layer relative error {worst:.3e}; near-tie rows {flagged}; "
+          f"input words rounded the other way {rounded}")
+    ws.close()
+    m.close()
+
+
+def test_prefill_attention_forms_agree_full_width(q8):
+    """One 64-row chunk at full width (every row block of 16 and every position group of the 4096-row cache in use),
+    f32 mode, run with the tensor-core attention and with the CUDA-core attention from the same state: the logits and
+    the second layer's cache rows (which depend on the first layer's attention) agree to 1e-5, and the tensor-core
+    form's result matches the oracle's decode steps."""
+    import torch
+    cfg = dict(recipes.DECODE, layers=2, vocab=1000)
+    rng = np.random.default_rng(64)
+    tokens = [int(v) for v in rng.integers(0, cfg["vocab"], 64)]
+    out = {}
+    for form in ("tensor", "cuda"):
+        q8.set_tensor_core_attention(form == "tensor")
+        try:
+            m, arr, t, tok, pos, logits = build(q8, cfg, 17, 0)
+            ws = q8.Workspace(256 << 20)
+            pos.fill_(3000)
+            m.prefill(torch.tensor(tokens, dtype=torch.int32, device="cuda"), ws)
+            torch.cuda.synchronize()
+            m.check()
+            out[form] = (logits.cpu().numpy(), t["k_cache"][1][:, 3000:3064].cpu().numpy(),
+                         t["v_cache"][1][:, 3000:3064].cpu().numpy())
+            ws.close()
+            m.close()
+        finally:
+            q8.set_tensor_core_attention(True)
+    for a, b in zip(out["tensor"], out["cuda"]):
+        assert rel_err(a, b) < 1e-5, rel_err(a, b)
+    om = oracle.ModelArrays(cfg, **arr)
+    for r, tk in enumerate(tokens):
+        _, ora_logits = oracle.decode_step(0, om, tk, 3000 + r)
+    assert rel_err(out["tensor"][0], ora_logits) < TOL[0]
 

@@ -14,6 +14,7 @@ import pytest
 
 import oracle
 import synth
+from synth import recipes
 
 pytestmark = pytest.mark.filterwarnings("ignore")
 
@@ -777,3 +778,50 @@ def test_step_with_a_zero_shared_expert_equals_the_step_without():
                                                 shared_down=[synth.q8_matrix(d, 64, 3, 90 + l) for l in range(L)]),
                                     5, 6)
         assert np.max(np.abs(l2 - l0)) > 1e-3 * np.max(np.abs(l0))
+
+
+# ---- the rounding-boundary probe (test support for the GPU comparisons) --------------------------------------------
+
+def _probe_case():
+    m = recipes.moe_block(seed=0)
+    w = oracle.MoeWeights(2048, 768, 128, 8, **m)
+    x = synth.normal((1, 2048), 7, recipes.VEC + 300)[0]
+    return m, w, x
+
+
+def test_probe_margins_are_the_one_word_rules_distances():
+    """Per value: t = x / d in f32 (d = amax / 127 in f32), the distance of t from the nearest half-step boundary
+    with that boundary's sign, recomputed here from the rule's definition."""
+    m, w, x = _probe_case()
+    _, mg = oracle.moe_row_probed(1, w, x)
+    xb = x.reshape(-1, 32).astype(np.float32)
+    d = (np.abs(xb).max(1) / np.float32(127)).astype(np.float32)
+    t = (xb / d[:, None]).astype(np.float32).astype(np.float64).ravel()
+    r = np.sign(t) * np.floor(np.abs(t) + 0.5)  # round half away from zero
+    off = t - r
+    want = np.where(off >= 0, 0.5 - off, -(0.5 + off))
+    np.testing.assert_array_equal(mg, want)
+    assert np.all(np.abs(mg) <= 0.5)
+
+
+def test_probe_unarmed_and_empty_change_nothing():
+    m, w, x = _probe_case()
+    plain = oracle.moe_rows(1, w, x.reshape(1, -1))
+    probed, _ = oracle.moe_row_probed(1, w, x)
+    for key in ("logits", "gates", "y"):
+        np.testing.assert_array_equal(probed[key], plain[key][0])
+
+
+def test_probe_flip_moves_the_router_by_one_words_product():
+    """Word i one step up (or down): every router logit moves by s_r[e, i/32] * s_x[i/32] * q_r[e, i] * delta, the
+    block product's change, in f64."""
+    m, w, x = _probe_case()
+    out0, mg = oracle.moe_row_probed(1, w, x)
+    i = int(np.argmin(np.abs(mg)))
+    delta = 1 if mg[i] > 0 else -1
+    out1, _ = oracle.moe_row_probed(1, w, x, flips=[(i, delta)])
+    xq, xs = oracle.quantize(x.reshape(1, -1))
+    rq, rs = m["router"]
+    want = rs[:, i // 32].astype(np.float64) * np.float64(xs[0, i // 32]) * rq[:, i].astype(np.float64) * delta
+    assert np.abs((out1["logits"] - out0["logits"]) - want).max() < 1e-12 * np.abs(out0["logits"]).max()
+    assert np.abs(want).max() > 0
