@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--batch-only", type=int, default=0, metavar="B",
                     help="only the batch form's timing with B sequences (for a profiler capture of its kernels)")
     ap.add_argument("--tensor-core-rows", type=int, default=None, metavar="N",
-                    help="dense int8 projections of N..64 rows on the tensor cores (0: off; the library's default)")
+                    help="dense int8 projections of N..64 rows on the tensor cores (-1: automatic, the library default; 0: off)")
     ap.add_argument("--grouped-tensor-core-rows", type=int, default=None, metavar="N",
                     help="int8 expert groups of N..64 rows on the tensor cores (0: off; the library's default is 32)")
     ap.add_argument("--tensor-core-attention", type=int, default=None, choices=[0, 1],

@@ -129,9 +129,10 @@ Q8_API int q8_gemv(const q8_mat *W, q8_mode mode, const float *x, const q8_act *
 
 /* Dense int8-mode projections of 16 to 64 activation rows (a prefill chunk's, a batch's, or q8_gemv's with that many
  * rows) can run on the tensor cores — the grouped tensor-core product of the mixture with one group holding every row
- * — instead of the CUDA cores.  rows: the fewest activation rows that take the tensor cores (16 to 64), or 0 for the
- * CUDA cores always (the default: on this part the tensor-core form is measured slower at these row counts).
- * Process-wide; set it before the calls (and the decode model's first step) it should affect. */
+ * — instead of the CUDA cores.  rows: -1 (automatic, the default): a call of one matrix of at least 2048 x 2048 takes
+ * the tensor cores from 32 rows on, where they are measured faster (a prefill chunk's O projection); 0: the CUDA cores
+ * always; 16 to 64: every call from that many rows on.  Process-wide; set it before the calls (and the decode model's
+ * first step) it should affect. */
 Q8_API int q8_set_tensor_core_rows(int rows);
 
 /* The fewest rows an expert group of a chunk's int8-mode mixture (moe_gate_up, moe_down_combine over rows > 1) needs

@@ -198,7 +198,8 @@ def q8_gemv_blockdots(q, s, xq, xs, dots, y, rows=1, ws=None, stream=None, xl=No
 
 
 def set_tensor_core_rows(rows: int):
-    """The fewest int8 activation rows (16..64) a dense projection takes to the tensor cores; 0: never (default)."""
+    """The fewest int8 activation rows (16..64) a dense projection takes to the tensor cores; 0: never; -1 (the
+    default): one matrix of at least 2048 x 2048 from 32 rows on."""
     _check(lib.q8_set_tensor_core_rows(int(rows)))
 
 

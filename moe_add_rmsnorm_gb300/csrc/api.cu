@@ -508,8 +508,9 @@ int moe_down_combine(const q8_mat* down, int64_t d, q8_mode mode, const float* h
 
 int q8_set_tensor_core_rows(int rows) {
     g_err[0] = 0;
-    if (rows != 0 && (rows < 16 || rows > 64)) return fail(Q8_EINVAL, "rows %d: 0 (off) or 16 to 64", rows);
-    kDenseMmaMinRows = rows ? rows : (1 << 30);
+    if (rows != 0 && rows != -1 && (rows < 16 || rows > 64))
+        return fail(Q8_EINVAL, "rows %d: -1 (automatic), 0 (off) or 16 to 64", rows);
+    kDenseMmaMinRows = rows;
     return Q8_OK;
 }
 

@@ -1104,7 +1104,9 @@ __global__ void __launch_bounds__(TCA_THREADS, 1) chunk_attention_tc_kernel(cons
 }
 
 // Row r, head h: the position groups' results folded in group order, out = num / den, and its int8 form.  A warp
-// per (row, head), lane l the dims l, l + 32, l + 64, l + 96.
+// per (row, head), lane l the dims l, l + 32, l + 64, l + 96.  The groups' maxima and sums are read a group a lane
+// (32 at a time) and passed along by shuffles; each group's values are then added in group order, four groups'
+// loads in flight at once.
 __global__ void __launch_bounds__(256) chunk_attn_fold_kernel(const float* part, const int32_t* posr, int R, int heads,
                                                               int ctx, int ngroups, float* out, int8_t* outq,
                                                               int8_t* outl, float* outs) {
@@ -1116,16 +1118,42 @@ __global__ void __launch_bounds__(256) chunk_attn_fold_kernel(const float* part,
     const int ng = min(ngroups, pos / (ACH_GROUP * 64) + 1);
     const float* base = part + (int64_t)wg * ngroups * ACH_PS;
     float M = -FLT_MAX;
-    for (int c = 0; c < ng; ++c) M = fmaxf(M, __ldcg(base + (int64_t)c * ACH_PS + ATT_HD));
+    for (int c = lane; c < ng; c += 32) M = fmaxf(M, __ldcg(base + (int64_t)c * ACH_PS + ATT_HD));
+    M = warp_max(M);
     float num[4] = {0.f, 0.f, 0.f, 0.f}, den = 0.f;
-    for (int c = 0; c < ng; ++c) {
-        const float* b = base + (int64_t)c * ACH_PS;
-        const float mc = __ldcg(b + ATT_HD);
-        if (mc == -FLT_MAX) continue;
-        const float f = expf(mc - M);
-        den = fmaf(f, __ldcg(b + ATT_HD + 1), den);
+    for (int c0 = 0; c0 < ng; c0 += 32) {
+        const int nb = min(32, ng - c0);
+        float f = 0.f, l = 0.f;
+        int live = 0;
+        if (lane < nb) {
+            const float* b = base + (int64_t)(c0 + lane) * ACH_PS;
+            const float mc = __ldcg(b + ATT_HD);
+            if (mc != -FLT_MAX) {
+                live = 1;
+                f = expf(mc - M);
+                l = __ldcg(b + ATT_HD + 1);
+            }
+        }
+        for (int cc = 0; cc < nb; cc += 4) {
+            float v[4][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) num[j] = fmaf(f, __ldcg(b + lane + 32 * j), num[j]);
+            for (int u = 0; u < 4; ++u) {
+                const float* b = base + (int64_t)(c0 + cc + u) * ACH_PS;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[u][j] = cc + u < nb ? __ldcg(b + lane + 32 * j) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int src = (cc + u) & 31;
+                const float fu = __shfl_sync(0xffffffffu, f, src), lu = __shfl_sync(0xffffffffu, l, src);
+                const int lv = __shfl_sync(0xffffffffu, live, src);
+                if (cc + u < nb && lv) {  // warp-uniform
+                    den = fmaf(fu, lu, den);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) num[j] = fmaf(fu, v[u][j], num[j]);
+                }
+            }
+        }
     }
     // the partials' values sit in float4 order (lane l held dims 4l..4l+3): dim d is at index d
 #pragma unroll

@@ -613,15 +613,25 @@ cudaError_t launch_gemv_tma(const GemvCall& c, int* err, cudaStream_t st) {
 
 bool gemv_norm_supported(const GemvCall& c) { return tma_eligible(c); }
 
-// Activation rows from which a dense int8 projection takes the tensor cores (q8_set_tensor_core_rows; off by default).
-int kDenseMmaMinRows = 1 << 30;
+// Activation rows from which a dense int8 projection takes the tensor cores (q8_set_tensor_core_rows): -1, the
+// default, lets one matrix of at least 2048 x 2048 take them from 32 rows on (measured faster there: 64 rows of a
+// 2048 x 4096 projection 32.8 us against 45.2 on the CUDA cores, of 4096 x 2048 30.8 against 51.3; smaller matrices,
+// fewer rows and several segments in one call stay faster on the CUDA cores, whose time grows with the rows while the
+// tensor-core kernel's has a floor of about 25 us); 0: never; 16..64: every shape from that many rows.
+int kDenseMmaMinRows = -1;
+
+static bool dense_on_tensor_cores(const GemvCall& c) {
+    if (kDenseMmaMinRows < 0)
+        return c.R >= 32 && c.nseg == 1 && c.seg[0].n >= 2048 && c.k >= 2048;
+    return kDenseMmaMinRows > 0 && c.R >= kDenseMmaMinRows;
+}
 
 cudaError_t launch_gemv(const GemvCall& c, Carve& ws, cudaStream_t st) {
     // 16..64 rows of int8 activations (a prefill chunk, a batch of sequences) can go to the tensor cores, the weight
-    // tiles read once for all rows, when the workspace holds the group's lists (the CUDA-core form needs no more than
-    // before); taken from kDenseMmaMinRows rows on (q8_set_tensor_core_rows)
+    // tiles read once for all rows (dense_on_tensor_cores); a workspace without room for the kernel's scratch keeps the
+    // CUDA-core form
     const size_t at = (ws.used + 255) & ~size_t(255);
-    if (c.R >= kDenseMmaMinRows && dense_mma_supported(c) && ws.base && at + 4096 + 4 * (size_t)c.R <= ws.size)
+    if (dense_on_tensor_cores(c) && dense_mma_supported(c) && ws.base && at + 4096 + 4 * (size_t)c.R <= ws.size)
         return launch_dense_mma(c, ws, st);
     if (tma_eligible(c))
         return launch_gemv_tma(c, c.err ? c.err : (ws.counters ? ws.counters + ws.n_counters - 1 : nullptr), st);

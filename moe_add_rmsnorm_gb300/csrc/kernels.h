@@ -223,12 +223,13 @@ cudaError_t launch_route_row(const RouteRowCall& c, cudaStream_t st);
 // gate-up (q1 set) writes h, down writes the per-choice outputs to `out`; other groups are left alone.  A chunk's
 // groups take them from moe_mma_min_rows() rows on (q8_set_grouped_tensor_core_rows; moe_mma_grouped says whether a
 // call has any to give), the CUDA-core kernels skipping those groups.
-bool moe_mma_supported(const ExpertCall& c);
+bool moe_mma_supported(const ExpertCall& c, bool dense = false);
 bool moe_mma_grouped(const ExpertCall& c);
 int moe_mma_min_rows();
 int moe_mma_max_rows();
+// dense_rows > 0: a dense projection of that many rows (E = K = 1, no plan: the rows are the one group)
 cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carve& ws, cudaStream_t st,
-                           const float* res = nullptr, int nmin = moe_mma_min_rows());
+                           const float* res = nullptr, int nmin = moe_mma_min_rows(), int dense_rows = 0);
 // A dense int8-mode projection of 16..64 activation rows on the tensor cores (the grouped product with one group of
 // every row; each segment's rows a multiple of 128, k a multiple of 128).
 bool dense_mma_supported(const GemvCall& g);

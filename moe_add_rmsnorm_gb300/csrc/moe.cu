@@ -801,6 +801,65 @@ cudaError_t shared_down(const ExpertCall& c, Carve& ws, cudaStream_t st) {
 
 }  // namespace
 
+namespace {
+
+// The grouped tensor-core launch and the CUDA-core launch of a chunk read the same routing and write disjoint rows, so
+// with plain launches the former runs on a side stream beside the latter: forked from `st` by an event, joined back
+// by another.  One side stream and two events per thread and device, made on first use and kept for the thread's
+// life.
+struct Side {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+Side* side_stream() {
+    constexpr int kDevices = 16;
+    thread_local Side sides[kDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return nullptr;
+    Side& sd = sides[dev];
+    if (!sd.s) {
+        if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            sd = Side{};
+            return nullptr;
+        }
+    }
+    return &sd;
+}
+
+// Forks the side stream off `st`: work launched on the returned stream starts after what `st` holds so far.  Without
+// a side stream (or if the fork fails), and while `st` is being captured into a graph, the work goes on `st` itself:
+// measured in a replayed graph of eight uncorrelated 64-row chunks, the forked branches made a chunk 279 us against
+// 207 us in order, while plain launches gain (a 64-row prefill chunk 21.1 ms against 23.2 ms).
+cudaStream_t fork_side(cudaStream_t st, Side** used) {
+    *used = nullptr;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return st;
+    }
+    Side* sd = side_stream();
+    if (!sd || cudaEventRecord(sd->fork, st) != cudaSuccess || cudaStreamWaitEvent(sd->s, sd->fork, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return st;
+    }
+    *used = sd;
+    return sd->s;
+}
+
+// Joins the side stream back into `st`: what `st` runs next waits for the side stream's work.
+cudaError_t join_side(cudaStream_t st, Side* sd) {
+    if (!sd) return cudaSuccess;
+    cudaError_t e = cudaEventRecord(sd->join, sd->s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, sd->join, 0);
+    return e;
+}
+
+}  // namespace
+
 cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     if (gate_row_supported(c)) return launch_gate_row(c, ws, st);  // the shared expert's rows are items of the kernel
     if (c.hq_out) return cudaErrorInvalidConfiguration;  // the int8 epilogue exists in the one-row kernel only
@@ -817,9 +876,18 @@ cudaError_t launch_gate_up(const ExpertCall& c, Carve& ws, cudaStream_t st) {
     if (c.mode >= 1 && c.R > 1 && xbytes <= 96 * 1024 && (uintptr_t)c.xq % 16 == 0 &&
         (c.mode == 1 || (uintptr_t)c.xl % 16 == 0))
         p.xstage = (int)xbytes;
-    cudaError_t e = c.mode == 0 ? run_gate_up<0>(c, pl, p, warps, st)
-                  : c.mode == 1 ? run_gate_up<1>(c, pl, p, warps, st) : run_gate_up<2>(c, pl, p, warps, st);
-    if (e == cudaSuccess && mma) e = launch_moe_mma(c, c.h, max_groups(c), ws, st);  // the groups of >= 16 choices
+    Side* sd = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (mma) {  // the groups of moe_mma_min_rows() choices or more, beside the CUDA-core launch
+        ExpertCall cm = c;
+        cm.pdl = 0;
+        e = launch_moe_mma(cm, c.h, max_groups(c), ws, fork_side(st, &sd));
+    }
+    if (e == cudaSuccess)
+        e = c.mode == 0 ? run_gate_up<0>(c, pl, p, warps, st)
+          : c.mode == 1 ? run_gate_up<1>(c, pl, p, warps, st) : run_gate_up<2>(c, pl, p, warps, st);
+    const cudaError_t ej = join_side(st, sd);
+    if (e == cudaSuccess) e = ej;
     if (e == cudaSuccess && c.sdff) e = shared_gate_up(c, ws, st);
     return e;
 }
@@ -855,9 +923,18 @@ cudaError_t launch_down_routed(const ExpertCall& c, Carve& ws, cudaStream_t st) 
         p.mma_hi = moe_mma_max_rows();
     }
     const int64_t warps = (int64_t)max_groups(c) * p.nrs;
-    cudaError_t e = c.mode == 0 ? run_down_group<0>(c, pl, p, warps, st)
-                  : c.mode == 1 ? run_down_group<1>(c, pl, p, warps, st) : run_down_group<2>(c, pl, p, warps, st);
-    if (e == cudaSuccess && mma) e = launch_moe_mma(c, reinterpret_cast<float*>(p.partial), max_groups(c), ws, st);
+    Side* sd = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (mma) {  // the groups of moe_mma_min_rows() choices or more, beside the CUDA-core launch
+        ExpertCall cm = c;
+        cm.pdl = 0;
+        e = launch_moe_mma(cm, reinterpret_cast<float*>(p.partial), max_groups(c), ws, fork_side(st, &sd));
+    }
+    if (e == cudaSuccess)
+        e = c.mode == 0 ? run_down_group<0>(c, pl, p, warps, st)
+          : c.mode == 1 ? run_down_group<1>(c, pl, p, warps, st) : run_down_group<2>(c, pl, p, warps, st);
+    const cudaError_t ej = join_side(st, sd);
+    if (e == cudaSuccess) e = ej;
     if (e != cudaSuccess) return e;
     const int64_t n = c.R * c.out_rows;
     int cg = (int)((n + 255) / 256);

@@ -38,7 +38,7 @@ constexpr int MM_MIN = 16;       // smaller groups stay on the CUDA cores
 constexpr int MM_CORE = 128;     // bytes of one core matrix (8 rows x 16 bytes)
 constexpr int MM_BPS = 2;        // 32-value blocks per pipeline stage (K = 64)
 constexpr int MM_RING = 6;       // raw stages in the ring, filled by the tensor-copy producer
-constexpr int MM_SMAX = 4;       // k slices per (group, tile) at most
+constexpr int MM_SMAX = 16;      // k slices per (group, tile) at most
 constexpr int MM_GCAP = 256;     // eligible groups listed in shared memory (beyond: found by a scan)
 constexpr int MM_ROWB = MM_BPS * 32;                 // bytes of one raw row of a stage (int8)
 constexpr int MM_KG = MM_BPS * 4;                    // f16 k-groups (core matrices) along K per stage
@@ -79,6 +79,7 @@ struct MmaParams {
     CUtensorMap ts0, ts1;  // weight scales [E*out_rows][nb] f32, box 4 x 128
     int gate_up;         // 1: gate and up (SiLU product to h); 0: down (per-choice outputs to part)
     int nmin;            // the fewest rows of a group this kernel takes (MM_MIN..MM_NMAX)
+    int dense_rows;      // > 0: a dense projection: one group, matrix 0, rows 0 .. dense_rows - 1 (no plan lists)
     int E, out_rows, k, nb, K;
     const int32_t* offsets;
     const int32_t* lists;
@@ -216,12 +217,30 @@ __device__ int mm_group_scan_one(const MmaParams& p, int nact, int g) {
     return 0;
 }
 
+// A group: its expert (matrix) e, first choice c0 and rows n.
+struct MmGroup {
+    int e, c0, n;
+};
+
+// Choice i of a group starting at c0 (a dense projection's rows are its choices).
+__device__ __forceinline__ int mm_choice(const MmaParams& p, int c0, int i) {
+    return p.dense_rows ? i : __ldg(p.lists + c0 + i);
+}
+
 // The eligible group at position g of the order (warp-wide; the first MM_GCAP come from the list).
 __device__ __forceinline__ int mm_group_at(const MmaParams& p, int nact, const int* glist, int g) {
     if (g < MM_GCAP) return glist[g];
     int found = 0;
     mm_scan(p, nact, nullptr, g, &found);
     return __reduce_max_sync(0xffffffffu, found);
+}
+
+// Group position g (warp-wide); a dense projection's one group needs no lookup.
+__device__ __forceinline__ MmGroup mm_group(const MmaParams& p, int nact, const int* glist, int g) {
+    if (p.dense_rows) return MmGroup{0, 0, p.dense_rows};
+    const int e = __ldg(p.active + 1 + mm_group_at(p, nact, glist, g));
+    const int c0 = __ldg(p.offsets + e);
+    return MmGroup{e, c0, __ldg(p.offsets + e + 1) - c0};
 }
 
 // Persistent: the work is the items (eligible group g, tile, k slice) in that order, CTA b taking items b,
@@ -253,13 +272,13 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     griddep_wait();
     griddep_launch();
-    const int nact = __ldg(p.active);
-    if (w == 0) {
+    const int nact = p.dense_rows ? 0 : __ldg(p.active);
+    if (w == 0 && !p.dense_rows) {
         const int c = mm_scan(p, nact, glist, -1, nullptr);
         if (lane == 0) nelig_s = c;
     }
     __syncthreads();
-    const int nelig = nelig_s;
+    const int nelig = p.dense_rows ? 1 : nelig_s;
     const int nst_all = p.nb / MM_BPS;
     // k slices: the fewest rounds of items over the grid times the stages per item (plus two for fill and epilogue)
     int S = 1;
@@ -313,8 +332,8 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
             const unsigned bytes = (unsigned)(mats * (MM_M * MM_ROWB + MM_M * MM_SCB * 4));
             for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
                 const int g = item / (p.tiles * S), tile = (item / S) % p.tiles, slice = item % S;
-                const int a = g < MM_GCAP ? glist[g] : -1;
-                const int e = __ldg(p.active + 1 + (a >= 0 ? a : mm_group_scan_one(p, nact, g)));
+                const int a = p.dense_rows ? 0 : (g < MM_GCAP ? glist[g] : mm_group_scan_one(p, nact, g));
+                const int e = p.dense_rows ? 0 : __ldg(p.active + 1 + a);
                 const int wrow = e * p.out_rows + tile * MM_M;
                 const int st0 = slice * nst_all / S, nst = (slice + 1) * nst_all / S - st0;
                 for (int i = 0; i < nst && ok; ++i) {
@@ -349,15 +368,14 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
         const int xt = ct - MM_XT0, xr = xt >> 2, xqq = xt & 3;
         for (int item = blockIdx.x; item < items; item += gridDim.x) {
             const int g = item / (p.tiles * S), slice = item % S;
-            const int a = mm_group_at(p, nact, glist, g);
-            const int e = __ldg(p.active + 1 + a);
-            const int c0 = __ldg(p.offsets + e), n = __ldg(p.offsets + e + 1) - c0;
+            const MmGroup grp = mm_group(p, nact, glist, g);
+            const int c0 = grp.c0, n = grp.n;
             const int N = (n + 15) & ~15;
             const int st0 = slice * nst_all / S, nst = (slice + 1) * nst_all / S - st0;
             const bool xown = xt >= 0 && xr < n;  // this thread brings a real row quarter
             int64_t xrow = 0;
             if (xown) {
-                const int c = __ldg(p.lists + c0 + xr);
+                const int c = mm_choice(p, c0, xr);
                 xrow = p.gate_up ? c / p.K : c;
             }
             const int8_t* xsrc = p.xq + xrow * p.k + 16 * xqq;
@@ -376,7 +394,6 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
             for (int i = 0; i < nst; ++i) {
                 const uint32_t gi = gs + i;
                 const int b = gi & 1, q = gi % MM_SQ, slot = gi % MM_RING;
-                const int jo = ((st0 + i) * MM_BPS) & (MM_SCB - 1);  // the stage's blocks inside the copied scale columns
                 const uint4 xc = xb[0];
                 const float2 sc = sb[0];
 #pragma unroll
@@ -428,9 +445,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
         // ---- MMA issue --------------------------------------------------------------------------------------------
         for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
             const int g = item / (p.tiles * S), slice = item % S;
-            const int a = mm_group_at(p, nact, glist, g);
-            const int e = __ldg(p.active + 1 + a);
-            const int n = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+            const int n = mm_group(p, nact, glist, g).n;
             const int N = (n + 15) & ~15;
             const uint32_t idesc = mm_idesc(N);
             const int nst = (slice + 1) * nst_all / S - slice * nst_all / S;
@@ -468,14 +483,18 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
         const int dt = t - MM_DRAIN_W0 * 32;            // 0 .. MM_DRAIN_T - 1
         for (int item = blockIdx.x; item < items; item += gridDim.x) {  // (no early exit: named barriers below)
             const int g = item / (p.tiles * S), tile = (item / S) % p.tiles, slice = item % S;
-            if (dw == 0) {
+            if (dw == 0 && !p.dense_rows) {
                 const int a = mm_group_at(p, nact, glist, g);
                 if (lane == 0) a_d = a;
             }
             asm volatile("bar.sync 2, %0;" ::"n"(MM_DRAIN_T));
-            const int e = __ldg(p.active + 1 + a_d);
-            const int c0 = __ldg(p.offsets + e), n = __ldg(p.offsets + e + 1) - c0;
-            if (dt < n) choice_d[dt] = __ldg(p.lists + c0 + dt);
+            int c0 = 0, n = p.dense_rows;
+            if (!p.dense_rows) {
+                const int e = __ldg(p.active + 1 + a_d);
+                c0 = __ldg(p.offsets + e);
+                n = __ldg(p.offsets + e + 1) - c0;
+            }
+            if (dt < n) choice_d[dt] = mm_choice(p, c0, dt);
             asm volatile("bar.sync 2, %0;" ::"n"(MM_DRAIN_T));
             const int N = (n + 15) & ~15;
             const int st0 = slice * nst_all / S, nst = (slice + 1) * nst_all / S - st0;
@@ -624,10 +643,10 @@ bool map_2d(CUtensorMap* m, bool f32, const void* base, uint64_t cols, uint64_t 
 
 }  // namespace
 
-bool moe_mma_supported(const ExpertCall& c) {
+bool moe_mma_supported(const ExpertCall& c, bool dense) {
     // tensor copies: 16-byte aligned bases, row strides (k bytes, nb scales) multiples of 16 bytes, 4-column scale
-    // boxes inside the rows, row coordinates that fit an int
-    return c.mode == 1 && c.plan.active && c.R >= MM_MIN && c.out_rows % MM_M == 0 && c.k % (32 * MM_SCB) == 0 &&
+    // boxes inside the rows, row coordinates that fit an int; a chunk's groups come from a plan
+    return c.mode == 1 && (dense || c.plan.active) && c.R >= MM_MIN && c.out_rows % MM_M == 0 && c.k % (32 * MM_SCB) == 0 &&
            c.xq && c.xs && (uintptr_t)c.q0 % 16 == 0 && (!c.q1 || (uintptr_t)c.q1 % 16 == 0) &&
            (uintptr_t)c.xq % 16 == 0 && (uintptr_t)c.s0 % 16 == 0 && (!c.s1 || (uintptr_t)c.s1 % 16 == 0) &&
            (uintptr_t)c.xs % 16 == 0 && c.E * c.out_rows < ((int64_t)1 << 31) && c.R * c.K < ((int64_t)1 << 31) &&
@@ -647,25 +666,24 @@ bool moe_mma_grouped(const ExpertCall& c) {
 int moe_mma_max_rows() { return MM_NMAX; }
 
 cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carve& ws, cudaStream_t st,
-                           const float* res, int nmin) {
-    if (!moe_mma_supported(c)) return cudaErrorInvalidConfiguration;
+                           const float* res, int nmin, int dense_rows) {
+    if (!moe_mma_supported(c, dense_rows > 0)) return cudaErrorInvalidConfiguration;
     MmaParams p = {};
-    // K split: up to MM_SMAX slices of at least 4 stages, when the workspace holds their partial sums (the kernel picks
-    // the number per call from the groups it finds)
+    // K split: up to MM_SMAX slices of at least 2 stages, as many as the workspace holds the partial sums of (the
+    // kernel picks the number per call from the groups it finds; few groups, a dense projection's one, want many)
     const int nst_all = (int)(c.k / 32) / MM_BPS;
-    int S = nst_all / 4;
+    int S = nst_all / 2;
     S = S < 1 ? 1 : (S > MM_SMAX ? MM_SMAX : S);
     const int tiles = (int)(c.out_rows / MM_M);
     if (nmin < MM_MIN || nmin > MM_NMAX) return cudaErrorInvalidValue;
     const int64_t slots = std::min<int64_t>(max_groups, c.R * c.K / nmin);  // eligible groups at most
-    if (S > 1) {
+    for (; S > 1; S = S > 4 ? S / 2 : S - 1) {
         const size_t bytes = (size_t)slots * tiles * S * 2 * MM_NMAX * MM_M * sizeof(float);
         const size_t at = (ws.used + 255) & ~size_t(255);
         if (at + bytes <= ws.size && ws.used_counters + (size_t)slots * tiles <= ws.n_counters) {
             p.part = ws.take<float>(bytes / sizeof(float));
             p.cnt = ws.take_counters((size_t)slots * tiles);
-        } else {
-            S = 1;
+            break;
         }
     }
     const uint64_t nb = (uint64_t)(c.k / 32), wrows = (uint64_t)(c.E * c.out_rows);
@@ -678,6 +696,8 @@ cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carv
     p.S = S;
     p.gate_up = c.q1 != nullptr;
     p.nmin = nmin;
+    p.dense_rows = dense_rows;
+    if (dense_rows && (c.E != 1 || c.K != 1 || c.R != dense_rows || dense_rows > MM_NMAX)) return cudaErrorInvalidValue;
     p.E = (int)c.E;
     p.out_rows = (int)c.out_rows;
     p.k = (int)c.k;
@@ -700,23 +720,6 @@ cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carv
     return launch(moe_mma_kernel, dim3((unsigned)grid), dim3(MM_THREADS), MM_SMEM, st, c.pdl, p);
 }
 
-namespace {
-
-// The one group of a dense projection: every activation row, in order (group 0 of "expert" 0).
-__global__ void dense_plan_kernel(int32_t* active, int32_t* offsets, int32_t* lists, int R) {
-    griddep_wait();
-    griddep_launch();
-    if (threadIdx.x == 0) {
-        active[0] = 1;
-        active[1] = 0;
-        offsets[0] = 0;
-        offsets[1] = R;
-    }
-    for (int i = threadIdx.x; i < R; i += blockDim.x) lists[i] = i;
-}
-
-}  // namespace
-
 bool dense_mma_supported(const GemvCall& g) {
     if (g.mode != 1 || g.R < MM_MIN || g.R > MM_NMAX || g.dots || g.norm_a || g.k % (32 * MM_SCB)) return false;
     if ((uintptr_t)g.xq % 16 || (uintptr_t)g.xs % 16 || !encode_tiled()) return false;
@@ -726,15 +729,11 @@ bool dense_mma_supported(const GemvCall& g) {
 }
 
 // A dense projection of 16..64 activation rows (a prefill chunk's q/k/v or O) on the tensor cores: the grouped
-// product's kernel with one group holding every row, each segment's matrix as the group's expert, the residual (when
-// given) added in its epilogue.
+// product's kernel with one group holding every row (known to the kernel: no plan lists, no group scan), each
+// segment's matrix as the group's expert, the residual (when given) added in its epilogue.
 cudaError_t launch_dense_mma(const GemvCall& g, Carve& ws, cudaStream_t st) {
     if (!dense_mma_supported(g)) return cudaErrorInvalidConfiguration;
-    int32_t* active = ws.take<int32_t>(2);
-    int32_t* offsets = ws.take<int32_t>(2);
-    int32_t* lists = ws.take<int32_t>((size_t)g.R);
-    if (ws.overflow) return cudaErrorMemoryAllocation;
-    cudaError_t e = launch(dense_plan_kernel, dim3(1), dim3(64), 0, st, g.pdl, active, offsets, lists, (int)g.R);
+    cudaError_t e = cudaSuccess;
     for (int i = 0; i < g.nseg && e == cudaSuccess; ++i) {
         ExpertCall c;
         c.mode = 1;
@@ -745,15 +744,12 @@ cudaError_t launch_dense_mma(const GemvCall& g, Carve& ws, cudaStream_t st) {
         c.k = g.k;
         c.R = g.R;
         c.K = 1;
-        c.plan.active = active;
-        c.plan.offsets = offsets;
-        c.plan.lists = lists;
         c.xq = g.xq;
         c.xs = g.xs;
         c.err = g.err;
         c.pdl = g.pdl;
         Carve cv = ws;  // each segment's launch may reuse the same scratch after the one before it
-        e = launch_moe_mma(c, g.seg[i].y, 1, cv, st, g.seg[i].residual, MM_MIN);
+        e = launch_moe_mma(c, g.seg[i].y, 1, cv, st, g.seg[i].residual, MM_MIN, (int)g.R);
     }
     return e;
 }

@@ -527,7 +527,7 @@ def test_q8_gemv_rows_on_tensor_cores(q8, n, k, R):
         q8.q8_gemv(dev(q), dev(s), 1, y, xq=dev(xq), xs=dev(xs), rows=R, ws=big)
         gy = host(y)
     finally:
-        q8.set_tensor_core_rows(0)
+        q8.set_tensor_core_rows(-1)
     assert rel_err(gy, ref) < TOL[1], rel_err(gy, ref)
     small = q8.Workspace(1024)
     y2 = empty((R, n), torch.float32)

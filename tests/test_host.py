@@ -80,6 +80,7 @@ def test_tensor_core_thresholds_refuse_bad_row_counts(q8):
     assert lib.q8_set_grouped_tensor_core_rows(16) == 0
     assert lib.q8_set_grouped_tensor_core_rows(32) == 0  # the default again
     assert lib.q8_set_tensor_core_rows(0) == 0
+    assert lib.q8_set_tensor_core_rows(-1) == 0  # the default again
 
 
 _RANK = r"""
