@@ -793,9 +793,10 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
     }
 }
 
-// The same partials on the tensor cores.  CTA (key/value head g, position group pg, row block rb) takes query vectors
-// m = 8 * (row in block) + (head in group) of rows rb*TCA_ROWS .. +TCA_ROWS-1 (128 vectors: the MMA's M) against the
-// group's 128 positions, in one pass (no running rescale: the group is the unit the fold combines).  Every f32
+// The same partials on the tensor cores.  CTA (key/value head g, position group pg, rows z*64 .. z*64+63) converts
+// the group's 128 key and value rows once and then takes its row blocks of TCA_ROWS rows in turn: query vectors
+// m = 8 * (row in block) + (head in group) (128 vectors: the MMA's M) against the group's positions, one pass each
+// (no running rescale: the group is the unit the fold combines).  Every f32
 // operand is split into two f16 parts, x = hi + lo (hi = x rounded to f16, lo = the remainder rounded to f16: the
 // pair holds x to about 2^-22 relative), and the three products hi*hi + hi*lo + lo*hi are accumulated in f32 in
 // tensor memory; the lo*lo term (about 2^-22 relative) is left out.
@@ -812,7 +813,8 @@ __global__ void __launch_bounds__(256, 2) chunk_attention_kernel(const float* qr
 // that the tile's largest magnitude lies in [2^14, 2^15)), which keeps the lo parts normal f16 numbers; the results
 // are scaled back exactly.  The partial (128 weighted values, max, sum) goes to part[r][head][pg] as
 // chunk_attention_kernel writes it.  A tile holding an infinity or a NaN sets kErrHalfRange in the error word.
-constexpr int TCA_ROWS = 16;                       // rows per CTA
+constexpr int TCA_ROWS = 16;                       // rows per row block
+constexpr int TCA_BLOCKS = 4;                      // row blocks per CTA (keys and values converted once for them)
 constexpr int TCA_M = TCA_ROWS * ATT_MAXG;         // query vectors per CTA: the MMA's M
 constexpr int TCA_P = ACH_GROUP * 64;              // positions per CTA: the partials' position group
 constexpr int TCA_THREADS = 512;
@@ -911,16 +913,15 @@ __global__ void __launch_bounds__(TCA_THREADS, 1) chunk_attention_tc_kernel(cons
     __shared__ uint32_t tmem_base;
     __shared__ int lim[TCA_ROWS];
     __shared__ unsigned int amax[3];  // the query, key and value tiles' largest magnitudes (f32 bits)
-    const int g = blockIdx.x, pg = blockIdx.y, rb = blockIdx.z;
+    const int g = blockIdx.x, pg = blockIdx.y;
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     const int G = heads / kv;
-    const int r0 = rb * TCA_ROWS, nr = min(TCA_ROWS, R - r0);
-    if (nr <= 0) return;
-    int maxpos = -1;
-    for (int i = 0; i < nr; ++i) maxpos = max(maxpos, min(posr[r0 + i], ctx - 1));
+    const int rbeg = blockIdx.z * TCA_ROWS * TCA_BLOCKS, rend = min(R, rbeg + TCA_ROWS * TCA_BLOCKS);
+    if (rend <= rbeg) return;
+    int maxpos = -1;  // the last position any of the CTA's rows attends
+    for (int i = rbeg; i < rend; ++i) maxpos = max(maxpos, min(posr[i], ctx - 1));
     const int p_begin = pg * TCA_P;
-    if (p_begin > maxpos) return;  // every row of the block ends before this group
-    if (t < TCA_ROWS) lim[t] = t < nr ? min(posr[r0 + t], ctx - 1) : -1;
+    if (p_begin > maxpos) return;  // every row ends before this group
     if (t == 0) {
         mbar_init(&bar, 1);
         fence_barrier_init();
@@ -938,26 +939,6 @@ __global__ void __launch_bounds__(TCA_THREADS, 1) chunk_attention_tc_kernel(cons
     // Each operand tile is scaled by a power of two before the split, so that its largest magnitude lies in
     // [2^14, 2^15): the lo parts of all but the tile's tiniest values stay normal f16 numbers.  The products are
     // scaled back exactly.
-#pragma unroll
-    for (int u = 0; u < TCA_M * 16 / TCA_THREADS; ++u) {  // queries: vector m, dims 8 * k8 ..
-        const int task = t + u * TCA_THREADS, m = task >> 4, k8 = task & 15, rr = m >> 3, hh = m & 7;
-        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (rr < nr && hh < G) {
-            const float4* src = reinterpret_cast<const float4*>(qr + ((int64_t)(r0 + rr) * heads + g * G + hh) * ATT_HD) + 2 * k8;
-            const float4 a = src[0], b = src[1];
-            x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
-        }
-        xa[u] = load8_amax(x, xv[u]);
-    }
-    const int eq = tile_exponent(block_amax(xa, TCA_M * 16 / TCA_THREADS, &amax[0]), err);
-#pragma unroll
-    for (int u = 0; u < TCA_M * 16 / TCA_THREADS; ++u) {
-        const int task = t + u * TCA_THREADS, m = task >> 4, k8 = task & 15;
-        uint4 hi, lo;
-        split8_scaled(xv[u], eq, hi, lo);
-        *reinterpret_cast<uint4*>(qh + tca_off(m, k8)) = hi;
-        *reinterpret_cast<uint4*>(ql + tca_off(m, k8)) = lo;
-    }
 #pragma unroll
     for (int u = 0; u < TCA_P * 16 / TCA_THREADS; ++u) {  // key rows: position n, dims 8 * k8 ..
         const int task = t + u * TCA_THREADS, n = task >> 4, k8 = task & 15, p = p_begin + n;
@@ -1004,99 +985,132 @@ __global__ void __launch_bounds__(TCA_THREADS, 1) chunk_attention_tc_kernel(cons
             *reinterpret_cast<uint4*>(vl + tca_off(4 * d4 + j, p8)) = lo;
         }
     }
-    const float s_back = exp2_int(-eq) * exp2_int(-ek) * scale;  // scores: D * 2^-(eq + ek), then the 1/sqrt(hd) scale
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the operands, to the tensor cores
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base;
     const uint32_t idesc = tc_idesc_f16(128, 128);
-    if (t == 0) {
-#pragma unroll 1
-        for (int j = 0; j < ATT_HD / 16; ++j) {  // K = 16 dims: two core matrices along K
-            const int o = j * 256;
-            tc_mma_f16(tmem, tc_desc(qh + o, TCA_SBO), tc_desc(kh + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
-            tc_mma_f16(tmem + 128, tc_desc(qh + o, TCA_SBO), tc_desc(kl + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
-            tc_mma_f16(tmem + 128, tc_desc(ql + o, TCA_SBO), tc_desc(kh + o, TCA_SBO), idesc, 1u);
+    bool ok = true;
+    for (int r0 = rbeg; r0 < rend; r0 += TCA_ROWS) {  // the row blocks: the keys and values stay converted
+        const int nr = min(TCA_ROWS, rend - r0);
+        int bmax = -1;
+        for (int i = 0; i < nr; ++i) bmax = max(bmax, min(posr[r0 + i], ctx - 1));
+        if (p_begin > bmax) continue;  // every row of the block ends before this group (CTA-uniform)
+        if (t < TCA_ROWS) lim[t] = t < nr ? min(posr[r0 + t], ctx - 1) : -1;
+        if (t == 0) amax[0] = 0u;
+        __syncthreads();  // the block's limits and its tile maximum; the previous block's products are read
+#pragma unroll
+        for (int u = 0; u < TCA_M * 16 / TCA_THREADS; ++u) {  // queries: vector m, dims 8 * k8 ..
+            const int task = t + u * TCA_THREADS, m = task >> 4, k8 = task & 15, rr = m >> 3, hh = m & 7;
+            float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (rr < nr && hh < G) {
+                const float4* src = reinterpret_cast<const float4*>(qr + ((int64_t)(r0 + rr) * heads + g * G + hh) * ATT_HD) + 2 * k8;
+                const float4 a = src[0], b = src[1];
+                x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+            }
+            xa[u] = load8_amax(x, xv[u]);
         }
-        tc_commit(&bar);
-    }
-    bool ok = __syncthreads_and(mbar_wait(&bar, 0, err) ? 1 : 0) != 0;
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const int lq = w & 3, cq = w >> 2, m = 32 * lq + lane, rr = m >> 3, hh = m & 7;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
-    const int lm = lim[rr];
-    float s[32];
-    {
-        uint32_t sv[32], sx[32];
-        tc_ld32(lane_base + 32 * cq, sv);        // hi * hi
-        tc_ld32(lane_base + 128 + 32 * cq, sx);  // hi * lo + lo * hi
-        tc_wait_ld();
-        float mx = -FLT_MAX;
+        const int eq = tile_exponent(block_amax(xa, TCA_M * 16 / TCA_THREADS, &amax[0]), err);
+#pragma unroll
+        for (int u = 0; u < TCA_M * 16 / TCA_THREADS; ++u) {
+            const int task = t + u * TCA_THREADS, m = task >> 4, k8 = task & 15;
+            uint4 hi, lo;
+            split8_scaled(xv[u], eq, hi, lo);
+            *reinterpret_cast<uint4*>(qh + tca_off(m, k8)) = hi;
+            *reinterpret_cast<uint4*>(ql + tca_off(m, k8)) = lo;
+        }
+        const float s_back = exp2_int(-eq) * exp2_int(-ek) * scale;  // scores: D * 2^-(eq + ek), then the 1/sqrt(hd) scale
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the operands, to the tensor cores
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (t == 0 && ok) {
+#pragma unroll 1
+            for (int j = 0; j < ATT_HD / 16; ++j) {  // K = 16 dims: two core matrices along K
+                const int o = j * 256;
+                tc_mma_f16(tmem, tc_desc(qh + o, TCA_SBO), tc_desc(kh + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
+                tc_mma_f16(tmem + 128, tc_desc(qh + o, TCA_SBO), tc_desc(kl + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
+                tc_mma_f16(tmem + 128, tc_desc(ql + o, TCA_SBO), tc_desc(kh + o, TCA_SBO), idesc, 1u);
+            }
+            tc_commit(&bar);
+        }
+        if (ok) ok = __syncthreads_and(mbar_wait(&bar, 0, err) ? 1 : 0) != 0;  // (each block completes two phases)
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const int lq = w & 3, cq = w >> 2, m = 32 * lq + lane, rr = m >> 3, hh = m & 7;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
+        const int lm = lim[rr];
+        float s[32];
+        {
+            uint32_t sv[32], sx[32];
+            tc_ld32(lane_base + 32 * cq, sv);        // hi * hi
+            tc_ld32(lane_base + 128 + 32 * cq, sx);  // hi * lo + lo * hi
+            tc_wait_ld();
+            float mx = -FLT_MAX;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float d = __uint_as_float(sv[i]) + __uint_as_float(sx[i]);
+                s[i] = p_begin + 32 * cq + i <= lm ? d * s_back : -FLT_MAX;
+                mx = fmaxf(mx, s[i]);
+            }
+            pmax[m * 4 + cq] = mx;
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();  // every partial max; the first product is read (its operands may be overwritten)
+        const float M = fmaxf(fmaxf(pmax[m * 4], pmax[m * 4 + 1]), fmaxf(pmax[m * 4 + 2], pmax[m * 4 + 3]));
+        float sum = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const float d = __uint_as_float(sv[i]) + __uint_as_float(sx[i]);
-            s[i] = p_begin + 32 * cq + i <= lm ? d * s_back : -FLT_MAX;
-            mx = fmaxf(mx, s[i]);
+            s[i] = (M == -FLT_MAX || s[i] == -FLT_MAX) ? 0.f : expf(s[i] - M);
+            sum += s[i];
         }
-        pmax[m * 4 + cq] = mx;
-    }
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();  // every partial max; the first product is read (its operands may be overwritten)
-    const float M = fmaxf(fmaxf(pmax[m * 4], pmax[m * 4 + 1]), fmaxf(pmax[m * 4 + 2], pmax[m * 4 + 3]));
-    float sum = 0.f;
+        psum[m * 4 + cq] = sum;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        s[i] = (M == -FLT_MAX || s[i] == -FLT_MAX) ? 0.f : expf(s[i] - M);
-        sum += s[i];
-    }
-    psum[m * 4 + cq] = sum;
+        for (int k8 = 0; k8 < 4; ++k8) {  // the weights (at most 1) times 2^14, positions 32 * cq + 8 * k8 .., as A
+            uint4 hi, lo;
+            float x[8];
 #pragma unroll
-    for (int k8 = 0; k8 < 4; ++k8) {  // the weights (at most 1) times 2^14, positions 32 * cq + 8 * k8 .., as A
-        uint4 hi, lo;
-        float x[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = s[8 * k8 + i];
-        split8_scaled(x, TCA_PEXP, hi, lo);
-        *reinterpret_cast<uint4*>(qh + tca_off(m, 4 * cq + k8)) = hi;
-        *reinterpret_cast<uint4*>(ql + tca_off(m, 4 * cq + k8)) = lo;
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (t == 0 && ok) {
+            for (int i = 0; i < 8; ++i) x[i] = s[8 * k8 + i];
+            split8_scaled(x, TCA_PEXP, hi, lo);
+            *reinterpret_cast<uint4*>(qh + tca_off(m, 4 * cq + k8)) = hi;
+            *reinterpret_cast<uint4*>(ql + tca_off(m, 4 * cq + k8)) = lo;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (t == 0 && ok) {
 #pragma unroll 1
-        for (int j = 0; j < TCA_P / 16; ++j) {  // K = 16 positions
-            const int o = j * 256;
-            tc_mma_f16(tmem + 256, tc_desc(qh + o, TCA_SBO), tc_desc(vh + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
-            tc_mma_f16(tmem + 384, tc_desc(qh + o, TCA_SBO), tc_desc(vl + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
-            tc_mma_f16(tmem + 384, tc_desc(ql + o, TCA_SBO), tc_desc(vh + o, TCA_SBO), idesc, 1u);
+            for (int j = 0; j < TCA_P / 16; ++j) {  // K = 16 positions
+                const int o = j * 256;
+                tc_mma_f16(tmem + 256, tc_desc(qh + o, TCA_SBO), tc_desc(vh + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
+                tc_mma_f16(tmem + 384, tc_desc(qh + o, TCA_SBO), tc_desc(vl + o, TCA_SBO), idesc, j > 0 ? 1u : 0u);
+                tc_mma_f16(tmem + 384, tc_desc(ql + o, TCA_SBO), tc_desc(vh + o, TCA_SBO), idesc, 1u);
+            }
+            tc_commit(&bar);
         }
-        tc_commit(&bar);
-    }
-    if (ok) ok = __syncthreads_and(mbar_wait(&bar, 1, err) ? 1 : 0) != 0;
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (ok) {
-        uint32_t ov[32], ox[32];
-        tc_ld32(lane_base + 256 + 32 * cq, ov);  // hi * hi
-        tc_ld32(lane_base + 384 + 32 * cq, ox);  // hi * lo + lo * hi
-        tc_wait_ld();
+        if (ok) ok = __syncthreads_and(mbar_wait(&bar, 1, err) ? 1 : 0) != 0;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (ok) {
+            uint32_t ov[32], ox[32];
+            tc_ld32(lane_base + 256 + 32 * cq, ov);  // hi * hi
+            tc_ld32(lane_base + 384 + 32 * cq, ox);  // hi * lo + lo * hi
+            tc_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) + __uint_as_float(ox[i]));
-        if (rr < nr && hh < G) {
-            float* dst = part + (((int64_t)(r0 + rr) * heads + g * G + hh) * ngroups + pg) * ACH_PS;
-            const float o_back = exp2_int(-TCA_PEXP) * exp2_int(-evs);  // exact
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) + __uint_as_float(ox[i]));
+            if (rr < nr && hh < G) {
+                float* dst = part + (((int64_t)(r0 + rr) * heads + g * G + hh) * ngroups + pg) * ACH_PS;
+                const float o_back = exp2_int(-TCA_PEXP) * exp2_int(-evs);  // exact
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                reinterpret_cast<float4*>(dst + 32 * cq)[i] =
-                    make_float4(__uint_as_float(ov[4 * i]) * o_back, __uint_as_float(ov[4 * i + 1]) * o_back,
-                                __uint_as_float(ov[4 * i + 2]) * o_back, __uint_as_float(ov[4 * i + 3]) * o_back);
-            if (cq == 0) {
-                dst[ATT_HD] = M;
-                dst[ATT_HD + 1] = ((psum[m * 4] + psum[m * 4 + 1]) + psum[m * 4 + 2]) + psum[m * 4 + 3];
+                for (int i = 0; i < 8; ++i)
+                    reinterpret_cast<float4*>(dst + 32 * cq)[i] =
+                        make_float4(__uint_as_float(ov[4 * i]) * o_back, __uint_as_float(ov[4 * i + 1]) * o_back,
+                                    __uint_as_float(ov[4 * i + 2]) * o_back, __uint_as_float(ov[4 * i + 3]) * o_back);
+                if (cq == 0) {
+                    dst[ATT_HD] = M;
+                    dst[ATT_HD + 1] = ((psum[m * 4] + psum[m * 4 + 1]) + psum[m * 4 + 2]) + psum[m * 4 + 3];
+                }
             }
         }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();  // every thread has read the block's results: the next block may overwrite them
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -1298,7 +1312,8 @@ cudaError_t launch_chunk_attention(const ChunkAttnCall& c, Carve& ws, cudaStream
     if (kChunkAttnTensorCores) {
         e = cudaFuncSetAttribute(chunk_attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TCA_SMEM);
         if (e != cudaSuccess) return e;
-        const dim3 grid((unsigned)c.kv, (unsigned)ng, (unsigned)((c.rows + TCA_ROWS - 1) / TCA_ROWS));
+        const int rows_per_cta = TCA_ROWS * TCA_BLOCKS;
+        const dim3 grid((unsigned)c.kv, (unsigned)ng, (unsigned)((c.rows + rows_per_cta - 1) / rows_per_cta));
         chunk_attention_tc_kernel<<<grid, TCA_THREADS, TCA_SMEM, st>>>(qr, c.k_cache, c.v_cache, c.posr, (int)c.rows,
                                                                        c.heads, c.kv, c.ctx, scale, part, ng, c.err);
     } else {
