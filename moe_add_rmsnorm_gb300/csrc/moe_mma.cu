@@ -39,6 +39,7 @@ constexpr int MM_CORE = 128;     // bytes of one core matrix (8 rows x 16 bytes)
 constexpr int MM_BPS = 2;        // 32-value blocks per pipeline stage (K = 64)
 constexpr int MM_RING = 6;       // raw stages in the ring, filled by the tensor-copy producer
 constexpr int MM_SMAX = 16;      // k slices per (group, tile) at most
+constexpr int MM_SFOR = 130;     // eligible-group counts the host tabulates the k split for (the last for any more)
 constexpr int MM_GCAP = 256;     // eligible groups listed in shared memory (beyond: found by a scan)
 constexpr int MM_ROWB = MM_BPS * 32;                 // bytes of one raw row of a stage (int8)
 constexpr int MM_KG = MM_BPS * 4;                    // f16 k-groups (core matrices) along K per stage
@@ -90,6 +91,7 @@ struct MmaParams {
     const float* res;    // down only, or null: out = res + the product (same index; may alias out)
     int tiles;           // out_rows / 128
     int S;               // k slices per (group, tile) at most (scratch holds that many); 1: no split
+    unsigned char s_for[MM_SFOR];  // the k slices to take for n eligible groups (n >= MM_SFOR - 1: the last)
     float* part;         // S > 1: [slots][tiles][S][2][64][128] scaled partial sums
     int* cnt;            // S > 1: [slots][tiles] arrivals (left zero)
     int* err;
@@ -265,6 +267,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t raw_full[MM_RING], raw_empty[MM_RING];
     __shared__ __align__(8) uint64_t op_full[2], op_empty[2], tm_full[2], tm_empty[2], sc_full[MM_SQ], sc_empty[MM_SQ];
+    __shared__ __align__(8) uint64_t tm_ready;  // the tensor memory is allocated
     __shared__ uint32_t tmem_base;
     __shared__ int choice_d[MM_NMAX];  // read-back: each group row's choice
     __shared__ int glist[MM_GCAP];     // the first eligible groups' indices in the active list
@@ -280,16 +283,9 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
     __syncthreads();
     const int nelig = p.dense_rows ? 1 : nelig_s;
     const int nst_all = p.nb / MM_BPS;
-    // k slices: the fewest rounds of items over the grid times the stages per item (plus two for fill and epilogue)
-    int S = 1;
-    {
-        int64_t best = -1;
-        for (int s = 1; s <= p.S; ++s) {
-            const int64_t its = (int64_t)nelig * p.tiles * s;
-            const int64_t cost = ((its + gridDim.x - 1) / gridDim.x) * ((nst_all + s - 1) / s + 2);
-            if (best < 0 || cost < best) best = cost, S = s;
-        }
-    }
+    // k slices for this many eligible groups, chosen on the host (a loop of divisions here cost microseconds of
+    // every launch's start)
+    const int S = p.s_for[nelig < MM_SFOR ? nelig : MM_SFOR - 1];
     const int items = nelig * p.tiles * S;
     if ((int)blockIdx.x >= items) return;
     if (t == 0) {
@@ -307,17 +303,13 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
             mbar_init(&sc_full[i], MM_CONV_WARPS);
             mbar_init(&sc_empty[i], MM_DRAIN_WARPS);
         }
+        mbar_init(&tm_ready, 1);
         fence_barrier_init();
     }
-    if (w == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
-                     "r"(MM_TCOLS));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t tmem = tmem_base;
+    // The tensor memory is allocated by the MMA-issue warp, which then releases the read-back warps through tm_ready;
+    // the allocation takes microseconds, and the producer and the converters start their stages meanwhile.
+    uint32_t tmem = 0;
     const int mats = p.gate_up ? 2 : 1;
     unsigned char* raw = smem;
     unsigned char* ops = smem + (size_t)MM_RING * MM_RAW;
@@ -443,6 +435,14 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
         }
     } else if (w == MM_ISSUE_WARP) {
         // ---- MMA issue --------------------------------------------------------------------------------------------
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                     "r"(MM_TCOLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        tmem = tmem_base;
+        if (lane == 0) mbar_arrive(&tm_ready);
         for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
             const int g = item / (p.tiles * S), slice = item % S;
             const int n = mm_group(p, nact, glist, g).n;
@@ -481,6 +481,9 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
         const int r = 32 * (w & 3) + lane;              // tile row = TMEM lane
         const int col0 = MM_DCOLS * (dw >> 2);          // this warp's columns
         const int dt = t - MM_DRAIN_W0 * 32;            // 0 .. MM_DRAIN_T - 1
+        if (ok) ok = mbar_wait(&tm_ready, 0, p.err);    // the tensor memory is allocated
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        tmem = tmem_base;
         for (int item = blockIdx.x; item < items; item += gridDim.x) {  // (no early exit: named barriers below)
             const int g = item / (p.tiles * S), tile = (item / S) % p.tiles, slice = item % S;
             if (dw == 0 && !p.dense_rows) {
@@ -602,7 +605,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) moe_mma_kernel(const __grid_con
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (w == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(MM_TCOLS));
+    if (w == MM_ISSUE_WARP) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(MM_TCOLS));
 }
 
 }  // namespace
@@ -717,6 +720,17 @@ cudaError_t launch_moe_mma(const ExpertCall& c, float* out, int max_groups, Carv
     int64_t grid = slots * p.tiles * p.S;  // persistent: one CTA per SM at most
     if (grid > device_info().sms) grid = device_info().sms;
     if (grid < 1) grid = 1;
+    // for each possible number of eligible groups, the k slices giving the fewest rounds of items over the grid times
+    // the stages per item (plus two for fill and epilogue)
+    for (int n = 0; n < MM_SFOR; ++n) {
+        int64_t best = -1;
+        p.s_for[n] = 1;
+        for (int sl = 1; sl <= p.S; ++sl) {
+            const int64_t its = (int64_t)n * p.tiles * sl;
+            const int64_t cost = ((its + grid - 1) / grid) * ((nst_all + sl - 1) / sl + 2);
+            if (best < 0 || cost < best) best = cost, p.s_for[n] = (unsigned char)sl;
+        }
+    }
     return launch(moe_mma_kernel, dim3((unsigned)grid), dim3(MM_THREADS), MM_SMEM, st, c.pdl, p);
 }
 
