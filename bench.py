@@ -568,7 +568,7 @@ def time_prefill(q8, model, cfg, tok, pos, stream, rows=(16, 64), reps=3):
     return out
 
 
-def time_batch(q8, cfg, dev, stream, mode, batches=(2, 4, 8), steps=8, warmup=3):
+def time_batch(q8, cfg, dev, stream, mode, batches=(2, 4, 8, 16, 32, 64), steps=8, warmup=3):
     """The batch form: B sequences per step through the whole model (one captured graph), each with its own f32 cache
     of the full length (seeded N(0,1), generated on the device) at positions ctx - steps - warmup .. ctx - 1.
     tokens/s = B / time per step; weight bytes per step count every dense matrix and the LM head once and the experts

@@ -6,6 +6,7 @@ import pytest
 
 import oracle
 import synth
+from layer_parity import layer_vs_oracle
 from synth import recipes
 
 pytestmark = pytest.mark.gpu
@@ -181,6 +182,53 @@ def test_batch_full_width_layer_by_layer(q8, mode):
         cur_t, cur_p = nt, np_
     print(f"batch mode {mode}: worst per-layer relative errors {worst}; near-tie layers {flagged}")
     assert len(flagged) <= 2, flagged
+    m.close()
+
+
+def test_batch_32_sequences_layer_by_layer(q8):
+    """32 sequences at full width (two layers, one graph step, int8 mode): the step's projections and mixture have 32
+    rows, so the O projection and the expert groups that 16 or more sequences share reach the tensor cores inside the
+    captured graph.  Teacher forced: every sequence's layers against the oracle from the GPU's own inputs, a word on a
+    rounding boundary rounded either way (layer_vs_oracle); its key and value rows and logits within the tolerance."""
+    import torch
+    cfg = dict(recipes.DECODE, layers=2, vocab=1000)
+    L, K, d, B = cfg["layers"], cfg["k"], cfg["d"], 32
+    rng = np.random.default_rng(32)
+    toks = [int(v) for v in rng.integers(0, cfg["vocab"], B)]
+    poss = [int(v) for v in rng.integers(3500, 4095, B)]
+    q8.set_grouped_tensor_core_rows(16)
+    try:
+        m, oms, t, tok, pos, logits = _batch_model(q8, cfg, B, 47, 1)
+        tok.copy_(torch.tensor(toks, dtype=torch.int32))
+        pos.copy_(torch.tensor(poss, dtype=torch.int32))
+        hidden = torch.empty(L + 1, B, d, device="cuda")
+        m.step_trace(hidden)
+        torch.cuda.synchronize()
+        m.check()
+    finally:
+        q8.set_grouped_tensor_core_rows(32)
+    hid = hidden.cpu().numpy()
+    gl = logits.cpu().numpy()
+    flagged, rounded, worst = [], [], 0.0
+    for b in range(B):
+        for l in range(L):
+            rl, err, word = layer_vs_oracle(1, oms[b], l, poss[b], hid[l, b], hid[l + 1, b], TOL[1])
+            kcb = t["k_cache"][l][b].cpu().numpy()[:, poss[b]]
+            vcb = t["v_cache"][l][b].cpu().numpy()[:, poss[b]]
+            err_kv = max(rel_err(kcb, oms[b].k_cache[l][:, poss[b]]), rel_err(vcb, oms[b].v_cache[l][:, poss[b]]))
+            assert err_kv < TOL[1], (b, l, err_kv)
+            if _near_tie(rl, K):
+                flagged.append((b, l))
+                continue
+            if word is not None:
+                rounded.append((b, l, word))
+            worst = max(worst, err, err_kv)
+            assert err < TOL[1], (b, l, err)
+        _, ora_logits = oracle.decode_final(1, oms[b], hid[L, b])
+        assert rel_err(gl[b], ora_logits) < TOL[1], (b, rel_err(gl[b], ora_logits))
+    assert len(flagged) <= 3, flagged
+    assert len(rounded) <= 6, rounded
+    print(f"32 sequences: worst per-layer relative error {worst:.3e}; near ties {flagged}; rounded {rounded}")
     m.close()
 
 
