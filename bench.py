@@ -47,6 +47,9 @@ def parse():
                     help="dense int8 projections of N..64 rows on the tensor cores (-1: automatic, the library default; 0: off)")
     ap.add_argument("--grouped-tensor-core-rows", type=int, default=None, metavar="N",
                     help="int8 expert groups of N..64 rows on the tensor cores (0: off; the library's default is 32)")
+    ap.add_argument("--persistent", type=int, default=None, choices=[0, 1],
+                    help="one-sequence int8 decode steps as one persistent launch for all layers (1) or six launches "
+                         "a layer (0, the library's default)")
     ap.add_argument("--tensor-core-attention", type=int, default=None, choices=[0, 1],
                     help="prefill chunks' attention on the tensor cores (1, the library's default) or CUDA cores (0)")
     ap.add_argument("--configs-only", action="store_true",
@@ -642,6 +645,8 @@ def main():
         q8.set_grouped_tensor_core_rows(args.grouped_tensor_core_rows)
     if args.tensor_core_attention is not None:
         q8.set_tensor_core_attention(bool(args.tensor_core_attention))
+    if args.persistent is not None:
+        q8.set_persistent_decode(bool(args.persistent))
     if args.chunk_only:
         res = time_chunks(q8, cfg, dev, sh, reps=max(1, args.steps), correlated=args.correlated,
                           rows=(args.chunk_only,))

@@ -149,6 +149,18 @@ Q8_API int q8_set_grouped_tensor_core_rows(int rows);
  * Process-wide. */
 Q8_API int q8_set_tensor_core_attention(int on);
 
+/* Whether a one-sequence decode step in an int8 activation mode runs its layers as one persistent launch (1) or as six
+ * launches a layer (0, the default: on this part the persistent form measured a few percent slower).  The persistent launch keeps one CTA on every SM for the whole step (a
+ * cooperative launch), separates a layer's stages (the norm and q/k/v, the attention, its fold, O, the norm and router,
+ * gate-up, down-and-combine) by grid-wide barriers, and copies the weights and cache rows that do not depend on the
+ * token into shared memory while the stage before them runs.  Its results equal the launch-per-stage step's up to the
+ * summation order of the attention (qwen_emit docs, emit_qwen30b_generate: the same layer).  A model takes it when
+ * its shapes fit (d and dff multiples of 128, d at most 4096, a CTA's share of the cache and of each stage's rows
+ * within shared memory), its routers are Q8_0, it has no shared expert, and every block-scale array starts on a
+ * 16-byte boundary; q8_model_persistent says whether it does.  Read when a step is launched or captured (a model's
+ * first decode_step captures its graph).  Process-wide. */
+Q8_API int q8_set_persistent_decode(int on);
+
 /* Debug export of the int8 paths: the q8_gemv call (y as above) that also writes dots[r][o][b] = the exact int32 dot
  * of weight block (o, b) with activation block (r, b), from the same device code; dots is device int32
  * [rows][W.rows][W.cols/32].  The mode is Q8_INT8ACT, or Q8_INT8ACT2 when xq->lo is not NULL: dots is then
@@ -307,6 +319,8 @@ Q8_API int prefill_chunk_trace(q8_model *model, const int32_t *tokens, int64_t r
                                q8_stream stream);
 /* Kernels one step launches: the kernel nodes of the graph the first decode_step captured (0 before it). */
 Q8_API int64_t q8_model_launches_per_step(const q8_model *model);
+/* 1 when the model's decode steps run their layers as one persistent launch (q8_set_persistent_decode), else 0. */
+Q8_API int q8_model_persistent(const q8_model *model);
 /* Reads and clears the model's device error word (synchronizes `stream`): Q8_OK, Q8_EINVAL when a step met an
  * out-of-range position or token, or Q8_ETIMEOUT when a bounded pipeline wait gave up. */
 Q8_API int q8_model_check(q8_model *model, q8_stream stream);

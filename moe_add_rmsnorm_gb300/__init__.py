@@ -76,6 +76,8 @@ _SIGS = {
     "q8_set_tensor_core_rows": [_i32],
     "q8_set_grouped_tensor_core_rows": [_i32],
     "q8_set_tensor_core_attention": [_i32],
+    "q8_set_persistent_decode": [_i32],
+    "q8_model_persistent": [_vp],
     "moe_route_topk": [_P(q8_mat), _i32, _vp, _P(q8_act), _i64, _i32, _vp, _vp, _vp, _P(q8_moe_plan), _vp, _vp],
     "moe_route_topk_f32": [_vp, _i64, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _P(q8_moe_plan), _vp, _vp],
     "moe_gate_up": [_P(q8_mat), _P(q8_mat), _i64, _i32, _vp, _P(q8_act), _i64, _i32, _vp, _P(q8_moe_plan), _vp,
@@ -213,6 +215,11 @@ def set_tensor_core_attention(on: bool):
     _check(lib.q8_set_tensor_core_attention(1 if on else 0))
 
 
+def set_persistent_decode(on: bool):
+    """One-sequence int8 decode steps as one persistent launch, or (False, the default) six launches a layer."""
+    _check(lib.q8_set_persistent_decode(1 if on else 0))
+
+
 def plan_struct(counts, offsets, lists, active):
     return q8_moe_plan(counts.data_ptr(), offsets.data_ptr(), lists.data_ptr(), active.data_ptr())
 
@@ -342,6 +349,10 @@ class Model:
     def launches_per_step(self):
         """Kernels one step launches (the captured graph's kernel nodes; 0 before the first step)."""
         return int(lib.q8_model_launches_per_step(self.handle))
+
+    def persistent(self):
+        """Whether the model's decode steps run their layers as one persistent launch."""
+        return bool(lib.q8_model_persistent(self.handle))
 
     def close(self):
         if self.handle:

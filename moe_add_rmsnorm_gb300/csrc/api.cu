@@ -521,6 +521,13 @@ int q8_set_grouped_tensor_core_rows(int rows) {
     return Q8_OK;
 }
 
+int q8_set_persistent_decode(int on) {
+    g_err[0] = 0;
+    if (on != 0 && on != 1) return fail(Q8_EINVAL, "on %d: 0 or 1", on);
+    kPersistentDecode = on;
+    return Q8_OK;
+}
+
 int q8_set_tensor_core_attention(int on) {
     g_err[0] = 0;
     if (on != 0 && on != 1) return fail(Q8_EINVAL, "on %d: 0 or 1", on);

@@ -321,6 +321,77 @@ Carve workspace_carve(const q8_ws* ws);
 
 // A persistent grid for `kernel`: enough CTAs of Q8_THREADS threads for `warps` warps, at most the CTAs that fit on
 // the device at once (occupancy times SMs).
+// ---- the decode step's layers in one persistent launch (decode_persistent.cu) ----------------------------------
+// One layer's matrices and vectors, as the persistent kernel reads them (a device array of these, one per layer).
+struct PersistLayer {
+    const int8_t *wq_q, *wk_q, *wv_q, *wo_q, *wr_q, *wg_q, *wu_q, *wd_q;  // quants
+    const float *wq_s, *wk_s, *wv_s, *wo_s, *wr_s, *wg_s, *wu_s, *wd_s;   // block scales
+    const float *attn_norm, *ffn_norm, *q_norm, *k_norm;
+    float *kc, *vc;  // this layer's caches [kv][ctx][hd]
+};
+
+// The shapes the kernel is sized for, and how it deals each phase's work to the CTAs (one CTA per SM).
+struct PersistDims {
+    int L = 0, D = 0, H = 0, KV = 0, E = 0, K = 0, F = 0, ctx = 0, mode = 0;
+};
+// Byte offsets in a CTA's shared memory (computed on the host; the kernel reads them from its parameters).
+struct PersistLayout {
+    uint32_t xq = 0, xl = 0, xs = 0;     // the normed activation's words (and low words) and scales
+    uint32_t u = 0;                      // per-stage scratch (a union over the stages)
+    uint32_t w = 0, c = 0, r = 0;        // the weight regions
+    uint32_t total = 0;
+    // inside u
+    uint32_t b_qs = 0, b_kn = 0, b_vn = 0, b_sc = 0, b_red = 0;  // attention
+    uint32_t f_m = 0, f_red = 0;                               // fold
+    uint32_t o_q = 0, o_l = 0, o_s = 0;                        // O: the attention output's words and scales
+    uint32_t e_key = 0, e_val = 0;                             // routing
+    uint32_t d_q = 0, d_l = 0, d_s = 0;                        // down: the hidden rows' words and scales
+    uint32_t red_in_c = 0;  // the attention's value sums meet at b_red in the C region (else in u)
+};
+struct PersistPlan {
+    int ok = 0;          // 0: the shapes do not fit the kernel (why: in `why`)
+    const char* why = "";
+    int nb = 0;          // CTAs (one per SM)
+    int rq = 0, ro = 0, rr = 0, rd = 0;  // q/k/v, O, router and down rows per CTA
+    int ppg = 0;         // attention CTAs per key/value head
+    int capr = 0;        // cache positions a CTA stages (its share at the longest cache)
+    int gu = 0;          // gate-up items (row pairs) per CTA
+    size_t smem = 0;     // dynamic shared memory per CTA
+    PersistLayout lay;
+};
+PersistPlan persist_plan(const PersistDims& d);
+
+struct PersistCall {
+    PersistDims dims;
+    PersistPlan plan;
+    const PersistLayer* layers = nullptr;  // device [L]
+    float eps = 0.f, scale = 0.f;
+    const float* embed = nullptr;
+    int64_t vocab = 0;
+    const int32_t* tok = nullptr;
+    const int32_t* pos = nullptr;
+    const float *cos_t = nullptr, *sin_t = nullptr;
+    float *h = nullptr, *q = nullptr, *k = nullptr, *v = nullptr;
+    float* part = nullptr;                 // [H][ppg][hd + 2] attention partials
+    float* att = nullptr;
+    int8_t *attq = nullptr, *attl = nullptr;
+    float* atts = nullptr;
+    float* logits = nullptr;               // [E]
+    int32_t* ids = nullptr;
+    float* gates = nullptr;
+    float* hbuf = nullptr;                 // [K * F]
+    int8_t *hq = nullptr, *hl = nullptr;   // the hidden rows' words (and low words) [K * F] and scales [K * F / 32]
+    float* hs = nullptr;
+    int* qcnt = nullptr;                   // [K * F / 32] arrivals per 32-row block (left zero)
+    float* trace = nullptr;                // optional [L + 1][D]
+    unsigned* bar = nullptr;               // kPersistBarBytes: grid-barrier arrival and exit counters, zero between
+                                           // launches
+    int* err = nullptr;
+};
+cudaError_t launch_persist(const PersistCall& c, cudaStream_t st);
+constexpr size_t kPersistBarBytes = 2048;  // the grid barrier's counters, each on a 128-byte line of its own
+extern int kPersistentDecode;  // q8_set_persistent_decode
+
 template <typename Kern>
 int persistent_grid(Kern kernel, size_t smem, int64_t warps) {
     int occ = 1;

@@ -55,6 +55,14 @@ struct q8_model {
     cudaGraphExec_t exec = nullptr;
     int64_t kernels_per_step = 0;  // kernel nodes of the captured step
     int pdl = 1;       // programmatic dependent launch between the step's kernels
+    // the step's layers as one persistent launch (when the shapes fit it): its plan, layer table, attention partials
+    // and grid-barrier counters, in one allocation
+    PersistPlan pplan;
+    char* pstate = nullptr;
+    PersistLayer* players = nullptr;
+    float* ppart = nullptr;
+    unsigned* pbar = nullptr;
+    int* pqcnt = nullptr;
 };
 
 namespace {
@@ -99,7 +107,51 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
         e = (x);                     \
         if (e != cudaSuccess) return e; \
     } while (0)
-    for (int64_t l = 0; l < d.layers; ++l) {
+    const bool persistent = kPersistentDecode && m->pplan.ok;
+    if (persistent) {
+        PersistCall c;
+        c.dims.L = (int)d.layers;
+        c.dims.D = (int)D;
+        c.dims.H = (int)H;
+        c.dims.KV = (int)KV;
+        c.dims.E = (int)d.experts;
+        c.dims.K = (int)d.k;
+        c.dims.F = (int)d.dff;
+        c.dims.ctx = (int)d.ctx;
+        c.dims.mode = mode;
+        c.plan = m->pplan;
+        c.layers = m->players;
+        c.eps = d.eps;
+        c.scale = (float)(1.0 / sqrt((double)HD));
+        c.embed = d.embed;
+        c.vocab = d.vocab;
+        c.tok = d.tok;
+        c.pos = d.pos;
+        c.cos_t = m->cos_t;
+        c.sin_t = m->sin_t;
+        c.h = m->h;
+        c.q = m->q;
+        c.k = m->k;
+        c.v = m->v;
+        c.part = m->ppart;
+        c.att = m->att;
+        c.attq = m->attq;
+        c.attl = m->attl;
+        c.atts = m->atts;
+        c.logits = m->rlog;
+        c.ids = m->ids;
+        c.gates = m->gates;
+        c.hbuf = m->hbuf;
+        c.hq = m->hq;
+        c.hl = m->hl;
+        c.hs = m->hs;
+        c.qcnt = m->pqcnt;
+        c.trace = trace;
+        c.bar = m->pbar;
+        c.err = m->err;
+        Q8_TRY(launch_persist(c, st));
+    }
+    for (int64_t l = 0; !persistent && l < d.layers; ++l) {
         // attention half: norm (the first layer gathers the token's embedding row into the residual stream), then q,
         // k and v in one projection launch; the norm runs inside the projection launch when the shapes allow it
         GemvCall g;
@@ -358,7 +410,9 @@ cudaError_t step_launches(q8_model* m, cudaStream_t st, float* trace = nullptr) 
         g.xq = m->xq;
         g.xl = m->xl;
         g.xs = m->xs;
-        g.pdl = pdl;
+        // after the persistent launch the LM head waits for it to end: programmatic dependent launch is not relied on
+        // behind a cooperative launch (logits read part of a residual row the layers were still writing)
+        g.pdl = persistent ? 0 : pdl;
         g.err = m->err;
         g.norm_a = m->h;
         g.norm_w = d.final_norm;
@@ -834,6 +888,66 @@ int q8_model_create(const q8_model_desc* desc, q8_model** out) {
     if (e == cudaSuccess) e = cudaMemset(m->counters, 0, m->n_counters * sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(m->err, 0, 256);
     if (e == cudaSuccess) e = launch_rope_table(m->cos_t, m->sin_t, (int)d.ctx, (int)half, d.rope_theta, 0);
+    // the persistent step: one sequence in an int8 mode, Q8_0 routers, no shared expert, block scales on 16-byte
+    // boundaries (the kernel bulk-copies whole rows of them), shapes it fits
+    bool scales16 = true;
+    for (int64_t l = 0; l < d.layers; ++l)
+        for (const q8_mat* w : {&m->wq[l], &m->wk[l], &m->wv[l], &m->wo[l], &m->router[l], &m->gate[l], &m->up[l],
+                                &m->down[l]})
+            scales16 = scales16 && (uintptr_t)w->s % 16 == 0;
+    if (e == cudaSuccess && B == 1 && !has_shared && !d.router_f32 && scales16) {
+        PersistDims pd;
+        pd.L = (int)d.layers;
+        pd.D = (int)D;
+        pd.H = (int)d.heads;
+        pd.KV = (int)d.kv_heads;
+        pd.E = (int)d.experts;
+        pd.K = (int)d.k;
+        pd.F = (int)d.dff;
+        pd.ctx = (int)d.ctx;
+        pd.mode = (int)d.mode;
+        m->pplan = persist_plan(pd);
+        if (m->pplan.ok) {
+            const size_t lt = ((size_t)d.layers * sizeof(PersistLayer) + 255) & ~size_t(255);
+            const size_t pb = ((size_t)d.heads * m->pplan.ppg * (d.head_dim + 2) * 4 + 255) & ~size_t(255);
+            const size_t qc = ((size_t)d.k * d.dff / 32 * 4 + 255) & ~size_t(255);
+            e = cudaMalloc(&m->pstate, lt + pb + kPersistBarBytes + qc);
+            if (e == cudaSuccess) {
+                m->players = reinterpret_cast<PersistLayer*>(m->pstate);
+                m->ppart = reinterpret_cast<float*>(m->pstate + lt);
+                m->pbar = reinterpret_cast<unsigned*>(m->pstate + lt + pb);
+                m->pqcnt = reinterpret_cast<int*>(m->pstate + lt + pb + kPersistBarBytes);
+                std::vector<PersistLayer> t((size_t)d.layers);
+                for (int64_t l = 0; l < d.layers; ++l) {
+                    PersistLayer& y = t[(size_t)l];
+                    y.wq_q = m->wq[l].q;
+                    y.wq_s = m->wq[l].s;
+                    y.wk_q = m->wk[l].q;
+                    y.wk_s = m->wk[l].s;
+                    y.wv_q = m->wv[l].q;
+                    y.wv_s = m->wv[l].s;
+                    y.wo_q = m->wo[l].q;
+                    y.wo_s = m->wo[l].s;
+                    y.wr_q = m->router[l].q;
+                    y.wr_s = m->router[l].s;
+                    y.wg_q = m->gate[l].q;
+                    y.wg_s = m->gate[l].s;
+                    y.wu_q = m->up[l].q;
+                    y.wu_s = m->up[l].s;
+                    y.wd_q = m->down[l].q;
+                    y.wd_s = m->down[l].s;
+                    y.attn_norm = m->attn_norm[l];
+                    y.ffn_norm = m->ffn_norm[l];
+                    y.q_norm = m->q_norm[l];
+                    y.k_norm = m->k_norm[l];
+                    y.kc = m->kc[l];
+                    y.vc = m->vc[l];
+                }
+                e = cudaMemcpy(m->players, t.data(), t.size() * sizeof(PersistLayer), cudaMemcpyHostToDevice);
+                if (e == cudaSuccess) e = cudaMemset(m->pbar, 0, kPersistBarBytes + qc);
+            }
+        }
+    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         q8_model_destroy(m);
@@ -850,6 +964,7 @@ void q8_model_destroy(q8_model* m) {
     cudaFree(m->arena);
     cudaFree(m->ws);
     cudaFree(m->counters);
+    cudaFree(m->pstate);
     delete m;
 }
 
@@ -1200,12 +1315,18 @@ static int prefill_launches(q8_model* m, const int32_t* tokens, int64_t R, q8_ws
 
 int64_t q8_model_launches_per_step(const q8_model* m) { return m ? m->kernels_per_step : 0; }
 
+int q8_model_persistent(const q8_model* m) { return m && kPersistentDecode && m->pplan.ok ? 1 : 0; }
+
 int q8_model_check(q8_model* m, q8_stream stream) {
     if (!m) return model_fail(Q8_EINVAL, "model: null");
     int v = 0;
     cudaError_t e = cudaMemcpyAsync(&v, m->err, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->err, 0, sizeof(int), (cudaStream_t)stream);
+    // a persistent step whose wait gave up may have left its grid-barrier counters part-way
+    if (e == cudaSuccess && (v & 4) && m->pbar)
+        e = cudaMemsetAsync(m->pbar, 0, kPersistBarBytes + ((size_t)m->d.k * m->d.dff / 32 * 4 + 255) / 256 * 256,
+                            (cudaStream_t)stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return model_fail(Q8_ECUDA, "q8_model_check: %s", cudaGetErrorString(e));
     if (v & 1) return model_fail(Q8_EINVAL, "a step read a token outside [0, vocab)");

@@ -84,6 +84,200 @@ def test_decode_small_matches_oracle_over_steps(q8, mode, cfg, launches):
     m.close()
 
 
+# dff a multiple of 128 and 4 key/value heads (38 attention CTAs a head on 152 SMs, as in the full configuration): the
+# int8 modes can run the layers as one persistent launch (q8_set_persistent_decode)
+PERSIST = dict(SMALL, dff=128, heads=16, kv_heads=4)
+
+
+@pytest.fixture
+def persistent(q8):
+    """The persistent step switched on for one test (the library's default is six launches a layer)."""
+    q8.set_persistent_decode(True)
+    yield
+    q8.set_persistent_decode(False)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_decode_persistent_matches_oracle_over_steps(q8, persistent, mode):
+    """The persistent step (one launch for all layers, then LM head and arg-max) over four steps, teacher forced: each
+    step exports the residual stream entering every layer, every layer's output (and its increment) is within the
+    mode's tolerance of the oracle's layer run from the GPU's own input (a word on a rounding boundary may be rounded
+    the other way, _layer_vs_oracle), the oracle's cache rows at the step's position come from those same inputs, and
+    the logits and token follow from the GPU's final residual row.  (End to end, an activation word or a router choice
+    decided by the last bits of an input can send the GPU and the oracle down two equally valid paths.)"""
+    import torch
+    m, arr, t, tok, pos, logits = build(q8, PERSIST, 5, mode)
+    assert m.persistent()
+    om = oracle.ModelArrays(PERSIST, **arr)
+    L = PERSIST["layers"]
+    cur_tok, cur_pos = 7, 60
+    tok.fill_(cur_tok)
+    pos.fill_(cur_pos)
+    for step in range(4):
+        hidden = torch.empty(L + 1, PERSIST["d"], device="cuda")
+        m.step_trace(hidden)
+        torch.cuda.synchronize()
+        hid = hidden.cpu().numpy()
+        np.testing.assert_array_equal(hid[0], arr["embed"][cur_tok])
+        for l in range(L):
+            _, e, _ = _layer_vs_oracle(mode, om, l, cur_pos, hid[l], hid[l + 1])
+            assert e < TOL[mode], (step, l, e)
+            kc, vc = t["k_cache"][l][:, cur_pos].cpu().numpy(), t["v_cache"][l][:, cur_pos].cpu().numpy()
+            assert rel_err(kc, om.k_cache[l][:, cur_pos]) < TOL[mode]
+            assert rel_err(vc, om.v_cache[l][:, cur_pos]) < TOL[mode]
+        nxt, ora_logits = oracle.decode_final(mode, om, hid[L])
+        gl = logits.cpu().numpy()
+        assert rel_err(gl, ora_logits) < TOL[mode], (step, rel_err(gl, ora_logits))
+        srt = np.sort(ora_logits)[::-1]
+        if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
+            assert int(tok.item()) == nxt
+        assert int(pos.item()) == cur_pos + 1
+        cur_tok, cur_pos = int(tok.item()), cur_pos + 1
+    m.step()  # the captured graph: the layers, the LM head (+final norm), the arg-max
+    torch.cuda.synchronize()
+    assert m.launches_per_step() == 3
+    m.check()
+    m.close()
+
+
+@pytest.mark.parametrize("pos0", [0, 1, 75, 95], ids=["first", "second", "mid", "last"])
+def test_decode_persistent_equals_launch_per_stage(q8, pos0):
+    """The persistent step and the six-launches-a-layer step on the same model and cache: every layer's residual
+    stream and the logits agree to the attention's summation order (the other stages' arithmetic is the same), and both
+    write the same new key and value rows; at every cache length, the shortest ones included (most attention CTAs then
+    hold no position)."""
+    import torch
+    outs = []
+    for on in (True, False):
+        q8.set_persistent_decode(on)
+        try:
+            m, arr, t, tok, pos, logits = build(q8, PERSIST, 9, 1)
+            assert m.persistent() == on
+            tok.fill_(11)
+            pos.fill_(pos0)
+            hidden = torch.empty(PERSIST["layers"] + 1, PERSIST["d"], device="cuda")
+            m.step_trace(hidden)
+            torch.cuda.synchronize()
+            outs.append((hidden.cpu().numpy(), logits.cpu().numpy().copy(),
+                         [c[:, pos0].cpu().numpy() for c in t["k_cache"]],
+                         [c[:, pos0].cpu().numpy() for c in t["v_cache"]]))
+            m.check()
+            m.close()
+        finally:
+            q8.set_persistent_decode(False)
+    (h1, l1, k1, v1), (h0, l0, k0, v0) = outs
+    np.testing.assert_array_equal(h1[0], h0[0])
+    for l in range(1, PERSIST["layers"] + 1):
+        assert rel_err(h1[l], h0[l]) < 1e-4, (l, rel_err(h1[l], h0[l]))
+    assert rel_err(l1, l0) < 1e-4
+    for a, b in zip(k1 + v1, k0 + v0):
+        assert rel_err(a, b) < 1e-5
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_decode_persistent_full_dims_layer_by_layer(q8, persistent, mode):
+    """Every dimension of the full configuration with 8 layers, at the last cache position, through the persistent step
+    (152 CTAs: 34 q/k/v rows, 38 attention CTAs a key/value head of 108 positions each, 14 O and down rows, 41 gate-up
+    row pairs a CTA), teacher forced layer by layer as in the 48-layer test, then the final norm, LM head and token."""
+    import torch
+    cfg = dict(recipes.DECODE, layers=8)
+    L = cfg["layers"]
+    m, arr, t, tok, pos, logits = build(q8, cfg, 0, mode)
+    if not m.persistent():
+        pytest.skip("the persistent step does not fit this device")
+    om = oracle.ModelArrays(cfg, **arr)
+    P = cfg["ctx"] - 1
+    tok.fill_(0)
+    pos.fill_(P)
+    hidden = torch.empty(L + 1, cfg["d"], device="cuda")
+    m.step_trace(hidden)
+    torch.cuda.synchronize()
+    hid = hidden.cpu().numpy()
+    np.testing.assert_array_equal(hid[0], arr["embed"][0])
+    flagged = []
+    for l in range(L):
+        rl, e, _ = _layer_vs_oracle(mode, om, l, P, hid[l], hid[l + 1])
+        if _near_tie(rl, cfg["k"]):
+            flagged.append(l)
+            continue
+        assert e < TOL[mode], (l, e)
+        kc, vc = t["k_cache"][l][:, P].cpu().numpy(), t["v_cache"][l][:, P].cpu().numpy()
+        assert rel_err(kc, om.k_cache[l][:, P]) < TOL[mode]
+        assert rel_err(vc, om.v_cache[l][:, P]) < TOL[mode]
+    assert len(flagged) <= 1, flagged
+    nxt, ora_logits = oracle.decode_final(mode, om, hid[L])
+    assert rel_err(logits.cpu().numpy(), ora_logits) < TOL[mode]
+    m.check()
+    m.close()
+
+
+def test_decode_persistent_graph_equals_launches_bitwise(q8, persistent):
+    import torch
+    outs = []
+    for use_graph in (True, False):
+        m, arr, t, tok, pos, logits = build(q8, PERSIST, 6, 1)
+        assert m.persistent()
+        tok.fill_(3)
+        pos.fill_(10)
+        for _ in range(3):
+            (m.step if use_graph else m.step_launches)()
+        torch.cuda.synchronize()
+        outs.append((logits.cpu().numpy().copy(), int(tok.item()), int(pos.item()),
+                     t["k_cache"][1].cpu().numpy().copy()))
+        m.close()
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    assert outs[0][1:3] == outs[1][1:3]
+    np.testing.assert_array_equal(outs[0][3], outs[1][3])
+
+
+def test_decode_persistent_bad_position_is_refused_on_device(q8, persistent):
+    import torch
+    m, arr, t, tok, pos, logits = build(q8, PERSIST, 7, 1)
+    assert m.persistent()
+    tok.fill_(1)
+    pos.fill_(PERSIST["ctx"])  # one past the cache
+    before = [c.clone() for c in t["k_cache"] + t["v_cache"]]
+    m.step()
+    torch.cuda.synchronize()
+    assert int(pos.item()) == PERSIST["ctx"] and int(tok.item()) == 1
+    for a, b in zip(before, t["k_cache"] + t["v_cache"]):
+        assert torch.equal(a, b)
+    with pytest.raises(q8.Q8Error, match="position"):
+        m.check()
+    m.close()
+
+
+def test_decode_persistent_step_after_a_timeout_waits_for_nothing(q8, persistent):
+    """With a timeout on record (the bounded-wait self-test leaves one), a persistent step skips every wait, grid and
+    copy alike, and runs to its end instead of waiting on CTAs that may have given up; q8_model_check reports the
+    timeout and resets the grid-barrier counters, and the next step is valid again."""
+    import torch
+    m, arr, t, tok, pos, logits = build(q8, PERSIST, 8, 1)
+    assert m.persistent()
+    om = oracle.ModelArrays(PERSIST, **arr)
+    m.wait_selftest(64)
+    tok.fill_(2)
+    pos.fill_(30)
+    m.step()
+    torch.cuda.synchronize()
+    with pytest.raises(q8.Q8Error, match="Q8_ETIMEOUT"):
+        m.check()
+    m.check()  # cleared
+    # the cache row at 30 may hold anything now: rerun from the oracle's row 30 onwards on a clean cache copy
+    for l in range(PERSIST["layers"]):
+        t["k_cache"][l].copy_(torch.from_numpy(arr["k_cache"][l]))
+        t["v_cache"][l].copy_(torch.from_numpy(arr["v_cache"][l]))
+    tok.fill_(2)
+    pos.fill_(30)
+    m.step()
+    torch.cuda.synchronize()
+    nxt, ora_logits = oracle.decode_step(1, om, 2, 30)
+    assert rel_err(logits.cpu().numpy(), ora_logits) < TOL[1]
+    assert int(pos.item()) == 31
+    m.check()
+    m.close()
+
+
 def test_decode_graph_equals_launches_bitwise(q8):
     import torch
     cfg = SMALL
