@@ -781,6 +781,32 @@ def main():
                                           "frac_of_peak": wbytes * args.steps / s2 / 1e9 / peak})
                 m2.check(sh)
                 m2.close()
+            # the same step as one persistent launch for all layers (opt-in in the library; int8 modes)
+            if mode != q8.F32ACT_F64SUM:
+                q8.set_persistent_decode(True)
+                try:
+                    m3 = q8.Model(cfg, dev, mode, tok, pos, logits)
+                    if m3.persistent():
+                        pos.fill_(cfg["ctx"] - total)
+                        with torch.cuda.stream(stream):
+                            for _ in range(args.warmup):
+                                m3.step(sh)
+                            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                            a0.record(stream)
+                            for _ in range(args.steps):
+                                m3.step(sh)
+                            a1.record(stream)
+                            a1.synchronize()
+                        s3 = a0.elapsed_time(a1) / 1e3
+                        line["secondary"].append({
+                            "mode": names[mode] + ", all layers as one persistent launch",
+                            "tokens_per_s": args.steps / s3, "weight_stream_gbs": wbytes * args.steps / s3 / 1e9,
+                            "frac_of_peak": wbytes * args.steps / s3 / 1e9 / peak,
+                            "launches_per_step": m3.launches_per_step()})
+                        m3.check(sh)
+                    m3.close()
+                finally:
+                    q8.set_persistent_decode(bool(args.persistent))
             line["batch"] = {"what": "the batch form: B sequences per step, every weight read once for all of them, "
                                      "one CUDA graph per step, int8 mode", "results": time_batch(q8, cfg, dev, sh, mode)}
             line["prefill"] = {"what": "prefill_chunk through all layers (plain launches), positions ctx-128-R ..",
