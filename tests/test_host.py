@@ -83,6 +83,17 @@ def test_tensor_core_thresholds_refuse_bad_row_counts(q8):
     assert lib.q8_set_tensor_core_rows(-1) == 0  # the default again
 
 
+def test_on_off_switches_refuse_other_values(q8):
+    lib = q8.lib
+    for setter in (lib.q8_set_persistent_decode, lib.q8_set_tensor_core_attention):
+        for bad in (-1, 2, 7):
+            assert setter(bad) == -1
+            assert "0 or 1" in q8.last_error()
+    assert lib.q8_set_persistent_decode(0) == 0  # the default again
+    assert lib.q8_set_tensor_core_attention(1) == 0  # the default again
+    assert lib.q8_model_persistent(None) == 0
+
+
 _RANK = r"""
 import json, sys
 sys.path.insert(0, {root!r})
