@@ -24,8 +24,9 @@
 // Stages (B = grid barrier):
 //   A  every CTA norms the residual row and quantizes it; its share of the q/k/v rows      B
 //   P  attention: CTA (g, j) takes positions [j c, (j+1) c) of key/value head g for the group's query heads; the
-//      CTA holding the new position norms, turns and appends the new key and value rows; partial max, sum, values  B
-//   C  fold: (query head, 32-dim quarter) per CTA, the partials in order; the output quantized per 32-value block  B
+//      CTA holding the new position norms, turns and appends the new key and value rows; partial max, sum, values;
+//      then the head's last CTAs to finish fold its partials, a (query head, 32-dim quarter) each, in partial order,
+//      the output quantized per 32-value block                                                 B
 //   O  its share of the O rows with the residual add                                          B
 //   R  every CTA norms and quantizes the residual row; its share of the router rows           B
 //   E  every CTA ranks the logits (top-k, renormalized gates); its share of the gate-up row pairs   B
@@ -75,6 +76,7 @@ struct PsSmall {
     float kval[PS_MAXK];
     float gate[PS_MAXK];
     float den;                     // fold: the sum of weighted partial sums
+    int ticket;                    // fold: this CTA's arrival rank among its key/value head's CTAs
 };
 
 inline size_t ps_align(size_t v) { return (v + 127) & ~size_t(127); }
@@ -192,8 +194,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.p
 // lines of their own, summed by each waiter, measured slower: the waiters' eight loads a poll cost more than the
 // atomics' queueing on one line.)
 constexpr int PS_BARS = 1;
+constexpr int PS_GROUP_BAR = 128;  // unsigned ints: the attention's per-head arrival counters start 512 bytes in
+constexpr int PS_MAXKV = 12;       // key/value heads with a counter of their own
 constexpr int PS_BAR_STRIDE = 32;  // unsigned ints: 128 bytes
-static_assert((PS_BARS + 1) * PS_BAR_STRIDE * 4 <= kPersistBarBytes, "barrier counters");
+static_assert((PS_BARS + 1) * PS_BAR_STRIDE <= PS_GROUP_BAR, "barrier counters");
+static_assert((PS_GROUP_BAR + PS_MAXKV * PS_BAR_STRIDE) * 4 <= kPersistBarBytes, "barrier counters");
 
 __device__ __forceinline__ unsigned grid_arrivals(const unsigned* bar) {
     unsigned v[PS_BARS];
@@ -574,6 +579,103 @@ __device__ __forceinline__ void row_dots(const int8_t* wq, int qstride, const fl
 // Ranking key: a NaN logit ranks below every number (and ties with -inf, broken by index).
 __device__ __forceinline__ float ps_rank_key(float v) { return v != v ? -INFINITY : v; }
 
+// The fold of one item (query head h, 32-dim quarter qd) of the attention partials: out = sum_j f_j o_j / sum_j f_j l_j
+// with f_j = exp(m_j - max m).  Every warp holds the partials' maxima in its lanes (partial j in lane j % 32) and forms
+// the max by shuffles; lane d of warp w sums f_j o_j[d] over the partials j = w, w + 11, ... in order, and the warps'
+// sums meet in shared memory; warp 0 forms the denominator the same way.  The quarter is one 32-value block of the O
+// projection's activation, quantized by warp 0.
+template <int MODE>
+__device__ void fold_item(const PersistCall& p, unsigned char* sm, PsSmall& s, int h, int qd) {
+    constexpr int NU = (PS_MAXPPG + PS_CW - 1) / PS_CW;
+    const PersistLayout& L = p.plan.lay;
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int ppg = p.plan.ppg;
+    float* fr = smp<float>(sm, (uint32_t)(L.u + L.f_red));
+    const float* base = p.part + (int64_t)h * ppg * (PS_HD + 2);
+    float ov[NU];
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+        const int jj = wid + PS_CW * u;
+        ov[u] = jj < ppg ? __ldcg(base + (int64_t)jj * (PS_HD + 2) + qd * 32 + lane) : 0.f;
+    }
+    const float m0 = lane < ppg ? __ldcg(base + (int64_t)lane * (PS_HD + 2) + PS_HD) : -FLT_MAX;
+    const float m1 = lane + 32 < ppg ? __ldcg(base + (int64_t)(lane + 32) * (PS_HD + 2) + PS_HD) : -FLT_MAX;
+    float l0 = 0.f, l1 = 0.f;
+    if (wid == 0) {
+        l0 = lane < ppg ? __ldcg(base + (int64_t)lane * (PS_HD + 2) + PS_HD + 1) : 0.f;
+        l1 = lane + 32 < ppg ? __ldcg(base + (int64_t)(lane + 32) * (PS_HD + 2) + PS_HD + 1) : 0.f;
+    }
+    const float M = warp_max(fmaxf(m0, m1));
+    float num = 0.f;
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+        const int jj = wid + PS_CW * u;  // warp-uniform
+        const float mj = __shfl_sync(0xffffffffu, jj < 32 ? m0 : m1, jj & 31);
+        if (jj < ppg) num = fmaf(mj == -FLT_MAX ? 0.f : expf(mj - M), ov[u], num);
+    }
+    fr[wid * 32 + lane] = num;
+    if (wid == 0) {
+        float den = (m0 == -FLT_MAX ? 0.f : expf(m0 - M)) * l0;
+        den = fmaf(m1 == -FLT_MAX ? 0.f : expf(m1 - M), l1, den);
+        den = group_sum<32>(den);
+        if (lane == 0) s.den = den;
+    }
+    cbar();
+    if (wid == 0) {
+        float o = 0.f;
+#pragma unroll
+        for (int v = 0; v < PS_CW; ++v) o += fr[v * 32 + lane];
+        const float den = s.den;
+        o = den > 0.f ? o / den : 0.f;
+        const int64_t oi = (int64_t)h * PS_HD + qd * 32 + lane;
+        p.att[oi] = o;
+        float dsc;
+        if (MODE == 2) {
+            int8_t lv;
+            p.attq[oi] = quantize2_lane(o, dsc, lv);
+            p.attl[oi] = lv;
+        } else {
+            const float ov1[1] = {o};
+            int8_t q1[1];
+            float d1[1];
+            ps_quantize<1>(ov1, q1, d1);
+            p.attq[oi] = q1[0];
+            dsc = d1[0];
+        }
+        if (lane == 0) p.atts[oi / 32] = dsc;
+    }
+    cbar();
+}
+
+// The fold of a key/value head's partials inside the attention stage, by the last CTAs of the head to finish: each CTA
+// of head g takes a ticket when its partials are written (an arrival counter per head that only grows within a launch);
+// ticket t of the layer folds the items i = ppg - 1 - t, + ppg, ... (the last arriver item 0), once every CTA of the head
+// has arrived (a bounded wait).  Items: (query head of the group, 32-dim quarter).
+template <int MODE>
+__device__ void fold_tail(const PersistCall& p, unsigned char* sm, PsSmall& s, int l, int g) {
+    const PersistDims& d = p.dims;
+    const int G = d.H / d.KV, ppg = p.plan.ppg, nit = G * 4;
+    unsigned* cnt = p.bar + PS_GROUP_BAR + g * PS_BAR_STRIDE;
+    cbar();  // this CTA's partials are written
+    if (threadIdx.x == 0) s.ticket = (int)(atom_add_acq_rel_u32(cnt, 1u) - (unsigned)l * ppg);
+    cbar();
+    const int first = ppg - 1 - s.ticket;
+    if (first < 0 || first >= nit) return;  // CTA-uniform
+    if (threadIdx.x == 0 && !s.dead) {
+        const unsigned target = (unsigned)(l + 1) * ppg;
+        const long long t0 = clock64();
+        while ((int)(ld_acquire_gpu(cnt) - target) < 0) {
+            if (clock64() - t0 > kGridWaitCycles || (*(volatile int*)p.err & kErrPipeline)) {
+                atomicOr(p.err, kErrPipeline);
+                s.dead = 1;
+                break;
+            }
+        }
+    }
+    cbar();
+    for (int i = first; i < nit; i += ppg) fold_item<MODE>(p, sm, s, g * G + i / 4, i % 4);
+}
+
 // ---- the stages (compute warps) -------------------------------------------------------------------------------------
 
 // A: the attention norm (layer 0: of the token's embedding row, which becomes the residual) and this CTA's q/k/v rows:
@@ -628,8 +730,8 @@ __device__ void stage_qkv(const PersistCall& p, const PersistLayer& ly, int l, u
 //   Values: warp w takes the same positions, lane l the dims 4 l .. 4 l + 3 of every head (32 sums in registers); the
 //   15 warps' sums meet in shared memory in a fixed order (warp w + 8 into warp w, then warps 0..7 in order).
 template <int MODE>
-__device__ void stage_attention(const PersistCall& p, const PersistLayer& ly, int len, unsigned char* sm, PsSmall& s,
-                                unsigned& nc) {
+__device__ void stage_attention(const PersistCall& p, const PersistLayer& ly, int l, int len, unsigned char* sm,
+                                PsSmall& s, unsigned& nc) {
     const PersistDims& d = p.dims;
     const PersistLayout& L = p.plan.lay;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
@@ -818,78 +920,7 @@ __device__ void stage_attention(const PersistCall& p, const PersistLayer& ly, in
             b[PS_HD] = np > 0 ? s.stat[t][0] : -FLT_MAX;
             b[PS_HD + 1] = np > 0 ? s.stat[t][1] : 0.f;
         }
-    }
-}
-
-// C: fold of the attention partials, item (query head h, 32-dim quarter) per CTA: out = sum_j f_j o_j / sum_j f_j l_j
-// with f_j = exp(m_j - max m).  Every warp holds the partials' maxima in its lanes (partial j in lane j % 32) and forms
-// the max by shuffles; lane d of warp w sums f_j o_j[d] over the partials j = w, w + 11, ... in order, and the warps'
-// sums meet in shared memory; warp 0 forms the denominator the same way.  The quarter is one 32-value block of the O
-// projection's activation, quantized by warp 0.
-template <int MODE>
-__device__ void stage_fold(const PersistCall& p, unsigned char* sm, PsSmall& s) {
-    constexpr int NU = (PS_MAXPPG + PS_CW - 1) / PS_CW;
-    const PersistDims& d = p.dims;
-    const PersistLayout& L = p.plan.lay;
-    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
-    const int ppg = p.plan.ppg;
-    float* fr = smp<float>(sm, (uint32_t)(L.u + L.f_red));
-    for (int it = blockIdx.x; it < d.H * 4; it += gridDim.x) {
-        const int h = it >> 2, qd = it & 3;
-        const float* base = p.part + (int64_t)h * ppg * (PS_HD + 2);
-        float ov[NU];
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            const int jj = wid + PS_CW * u;
-            ov[u] = jj < ppg ? __ldcg(base + (int64_t)jj * (PS_HD + 2) + qd * 32 + lane) : 0.f;
-        }
-        const float m0 = lane < ppg ? __ldcg(base + (int64_t)lane * (PS_HD + 2) + PS_HD) : -FLT_MAX;
-        const float m1 = lane + 32 < ppg ? __ldcg(base + (int64_t)(lane + 32) * (PS_HD + 2) + PS_HD) : -FLT_MAX;
-        float l0 = 0.f, l1 = 0.f;
-        if (wid == 0) {
-            l0 = lane < ppg ? __ldcg(base + (int64_t)lane * (PS_HD + 2) + PS_HD + 1) : 0.f;
-            l1 = lane + 32 < ppg ? __ldcg(base + (int64_t)(lane + 32) * (PS_HD + 2) + PS_HD + 1) : 0.f;
-        }
-        const float M = warp_max(fmaxf(m0, m1));
-        float num = 0.f;
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            const int jj = wid + PS_CW * u;  // warp-uniform
-            const float mj = __shfl_sync(0xffffffffu, jj < 32 ? m0 : m1, jj & 31);
-            if (jj < ppg) num = fmaf(mj == -FLT_MAX ? 0.f : expf(mj - M), ov[u], num);
-        }
-        fr[wid * 32 + lane] = num;
-        if (wid == 0) {
-            float den = (m0 == -FLT_MAX ? 0.f : expf(m0 - M)) * l0;
-            den = fmaf(m1 == -FLT_MAX ? 0.f : expf(m1 - M), l1, den);
-            den = group_sum<32>(den);
-            if (lane == 0) s.den = den;
-        }
-        cbar();
-        if (wid == 0) {
-            float o = 0.f;
-#pragma unroll
-            for (int v = 0; v < PS_CW; ++v) o += fr[v * 32 + lane];
-            const float den = s.den;
-            o = den > 0.f ? o / den : 0.f;
-            const int64_t oi = (int64_t)h * PS_HD + qd * 32 + lane;
-            p.att[oi] = o;
-            float dsc;
-            if (MODE == 2) {
-                int8_t lv;
-                p.attq[oi] = quantize2_lane(o, dsc, lv);
-                p.attl[oi] = lv;
-            } else {
-                const float ov1[1] = {o};
-                int8_t q1[1];
-                float d1[1];
-                ps_quantize<1>(ov1, q1, d1);
-                p.attq[oi] = q1[0];
-                dsc = d1[0];
-            }
-            if (lane == 0) p.atts[oi / 32] = dsc;
-        }
-        cbar();
+        fold_tail<MODE>(p, sm, s, l, g);
     }
 }
 
@@ -1164,9 +1195,7 @@ __global__ void __maxnreg__(168) decode_persistent_kernel(const __grid_constant_
         cbar();
         signal(&s.ev_w, 2u * l + 1u);  // the W region's q/k/v rows are used: O may come
         grid_barrier(p.bar, kb++, p.err, s);
-        stage_attention<MODE>(p, ly, len, sm, s, nc);
-        grid_barrier(p.bar, kb++, p.err, s);
-        stage_fold<MODE>(p, sm, s);
+        stage_attention<MODE>(p, ly, l, len, sm, s, nc);
         grid_barrier(p.bar, kb++, p.err, s);
         stage_o<MODE>(p, sm, s, nw);
         cbar();
@@ -1192,6 +1221,7 @@ __global__ void __maxnreg__(168) decode_persistent_kernel(const __grid_constant_
         const unsigned old = atom_add_acq_rel_u32(exits, 1u);
         if (old == gridDim.x - 1) {
             for (int i = 0; i < PS_BARS; ++i) atomicExch(p.bar + i * PS_BAR_STRIDE, 0u);
+            for (int g = 0; g < p.dims.KV; ++g) atomicExch(p.bar + PS_GROUP_BAR + g * PS_BAR_STRIDE, 0u);
             atomicExch(exits, 0u);
         }
     }
@@ -1232,6 +1262,7 @@ PersistPlan persist_plan(const PersistDims& d) {
     if (d.L < 1 || d.D < 128 || d.D % 128 || d.D > 4096) return no("d is not a multiple of 128 up to 4096");
     if (d.KV < 1 || d.H < 1 || d.H % d.KV || d.H / d.KV > PS_MAXG) return no("more than 8 query heads a key/value head");
     if (d.H * PS_HD > PS_MAXHHD) return no("more than 32 query heads");
+    if (d.KV > PS_MAXKV) return no("more than 12 key/value heads");
     if (d.F < 128 || d.F % 128) return no("dff is not a multiple of 128");
     if (d.K < 1 || d.K > PS_MAXK || d.K > d.E || d.E > PS_MAXE) return no("top-k or expert count out of range");
     if (d.ctx < 1) return no("no cache");
