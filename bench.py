@@ -781,12 +781,13 @@ def main():
                                           "frac_of_peak": wbytes * args.steps / s2 / 1e9 / peak})
                 m2.check(sh)
                 m2.close()
-            # the same step as one persistent launch for all layers (opt-in in the library; int8 modes)
+            # the same step in the other form (as one persistent launch for all layers, or as six launches a layer)
             if mode != q8.F32ACT_F64SUM:
-                q8.set_persistent_decode(True)
+                other_form = not model.persistent()
+                q8.set_persistent_decode(other_form)
                 try:
                     m3 = q8.Model(cfg, dev, mode, tok, pos, logits)
-                    if m3.persistent():
+                    if m3.persistent() == other_form:
                         pos.fill_(cfg["ctx"] - total)
                         with torch.cuda.stream(stream):
                             for _ in range(args.warmup):
@@ -799,7 +800,8 @@ def main():
                             a1.synchronize()
                         s3 = a0.elapsed_time(a1) / 1e3
                         line["secondary"].append({
-                            "mode": names[mode] + ", all layers as one persistent launch",
+                            "mode": names[mode] + (", all layers as one persistent launch" if other_form
+                                                   else ", six launches a layer"),
                             "tokens_per_s": args.steps / s3, "weight_stream_gbs": wbytes * args.steps / s3 / 1e9,
                             "frac_of_peak": wbytes * args.steps / s3 / 1e9 / peak,
                             "launches_per_step": m3.launches_per_step()})

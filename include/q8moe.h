@@ -150,7 +150,7 @@ Q8_API int q8_set_grouped_tensor_core_rows(int rows);
 Q8_API int q8_set_tensor_core_attention(int on);
 
 /* Whether a one-sequence decode step in an int8 activation mode runs its layers as one persistent launch (1) or as six
- * launches a layer (0, the default: on this part the persistent form measured a few percent slower).  The persistent launch keeps one CTA on every SM for the whole step (a
+ * launches a layer (0, the default).  The persistent launch keeps one CTA on every SM for the whole step (a
  * cooperative launch), separates a layer's stages (the norm and q/k/v, the attention, its fold, O, the norm and router,
  * gate-up, down-and-combine) by grid-wide barriers, and copies the weights and cache rows that do not depend on the
  * token into shared memory while the stage before them runs.  Its results equal the launch-per-stage step's up to the

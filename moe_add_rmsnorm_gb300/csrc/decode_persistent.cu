@@ -371,7 +371,8 @@ __device__ void producer(const PersistCall& p, int len, unsigned char* sm, PsSma
         fill_o(p, p.layers[l], sm + L.w, &s.bw);
         ++iw;
         // the down rows first: the down-and-combine waits for them right after gate-up, while the next layer's
-        // q/k/v and router rows are not needed before the next layer begins
+        // q/k/v and router rows are not needed before the next layer begins (issued before, they slowed the router
+        // stage they ran beside)
         if (!producer_wait(&s.ev_route, l + 1u, p.err, s)) break;  // routing of layer l known (the cache rows used)
         fill_down(p, p.layers[l], s.kid, sm + L.c, &s.bc);
         ++ic;
@@ -1191,27 +1192,25 @@ __global__ void __maxnreg__(168) decode_persistent_kernel(const __grid_constant_
         asm volatile("mov.u32 %0, %1;" : "=r"(l) : "r"(li));
         const PersistLayer& ly = p.layers[l];
         const bool more = l + 1 < p.dims.L;
+        // a region's next fill is released after the grid barrier that follows its last use: copies started just
+        // before a barrier slow the barrier (the release and the arrivals queue behind them)
         stage_qkv<MODE, BPL, NP>(p, ly, l, sm, s, nw);
-        cbar();
-        signal(&s.ev_w, 2u * l + 1u);  // the W region's q/k/v rows are used: O may come
         grid_barrier(p.bar, kb++, p.err, s);
+        signal(&s.ev_w, 2u * l + 1u);  // the W region's q/k/v rows are used: O may come
         stage_attention<MODE>(p, ly, l, len, sm, s, nc);
         grid_barrier(p.bar, kb++, p.err, s);
         stage_o<MODE>(p, sm, s, nw);
-        cbar();
+        grid_barrier(p.bar, kb++, p.err, s);
         signal(&s.ev_w, 2u * l + 2u);  // O's rows are used: the next layer's q/k/v may come
-        grid_barrier(p.bar, kb++, p.err, s);
         stage_router<MODE, BPL, NP>(p, ly, sm, s, nr);
-        cbar();
-        signal(&s.ev_r, l + 1u);
         grid_barrier(p.bar, kb++, p.err, s);
+        signal(&s.ev_r, l + 1u);
         stage_gate_up<MODE, BPL>(p, ly, l, sm, s);
         grid_barrier(p.bar, kb++, p.err, s);
         stage_down<MODE>(p, l, sm, s, nc);
         if (more) {
-            cbar();
-            signal(&s.ev_c, l + 1u);  // the down rows are used: the next layer's cache rows may come
             grid_barrier(p.bar, kb++, p.err, s);
+            signal(&s.ev_c, l + 1u);  // the down rows are used: the next layer's cache rows may come
         }
     }
     cbar();
@@ -1249,6 +1248,20 @@ cudaError_t run_persist(const PersistCall& c, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, kern, c);
 }
 
+// Whether one CTA of the instance for these shapes fits an SM with `smem` bytes of shared memory.
+template <int MODE, int BPL>
+bool fits(size_t smem) {
+    auto kern = decode_persistent_kernel<MODE, BPL>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return false;
+    int occ = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, PS_THREADS, smem) == cudaSuccess && occ >= 1;
+}
+
+bool persist_fits(const PersistDims& d, size_t smem) {
+    if (d.mode == 2) return d.D <= 1024 ? fits<2, 1>(smem) : d.D <= 2048 ? fits<2, 2>(smem) : fits<2, 4>(smem);
+    return d.D <= 1024 ? fits<1, 1>(smem) : d.D <= 2048 ? fits<1, 2>(smem) : fits<1, 4>(smem);
+}
+
 }  // namespace
 
 PersistPlan persist_plan(const PersistDims& d) {
@@ -1284,6 +1297,7 @@ PersistPlan persist_plan(const PersistDims& d) {
     pl.lay = ps_layout(d, pl);
     pl.smem = pl.lay.total;
     if ((int64_t)pl.smem > di.smem_optin) return no("the stages' shared memory does not fit (cache or rows per CTA)");
+    if (!persist_fits(d, pl.smem)) return no("a CTA of the kernel does not fit an SM");
     pl.ok = 1;
     return pl;
 }
