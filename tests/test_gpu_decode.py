@@ -365,17 +365,29 @@ def _near_tie(logits, k):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("mode", [1, 0, 2])
-def test_decode_full_config_layer_by_layer(q8, mode):
+@pytest.mark.parametrize("mode,form", [(1, "launches"), (0, "launches"), (2, "launches"), (1, "persistent"),
+                                       (2, "persistent")])
+def test_decode_full_config_layer_by_layer(q8, mode, form):
     """The full 48-layer configuration at the last cache position (every cached row attended), teacher-forced: the
     GPU step exports the residual stream entering every layer, the oracle runs each layer from that same input, and
     each layer's output (and its increment, the attention and mixture sums), its new key and value rows, then the
     final norm, LM head and token from the GPU's last stream, are each within the stated tolerance.  The graph replay
-    the benchmark times gives the same logits bit for bit as the traced plain launches."""
+    the benchmark times gives the same logits bit for bit as the traced plain launches.  Both forms of the step: six
+    launches a layer and (the int8 modes) all layers as one persistent launch."""
+    q8.set_persistent_decode(form == "persistent")
+    try:
+        _full_config_layer_by_layer(q8, mode, form)
+    finally:
+        q8.set_persistent_decode(False)
+
+
+def _full_config_layer_by_layer(q8, mode, form):
     import torch
     cfg = recipes.DECODE
     L, K = cfg["layers"], cfg["k"]
     m, arr, t, tok, pos, logits = build(q8, cfg, 0, mode)
+    if form == "persistent" and not m.persistent():
+        pytest.skip("the persistent step does not fit this device")
     om = oracle.ModelArrays(cfg, **arr)
     P = cfg["ctx"] - 1
     tok.fill_(0)
@@ -413,7 +425,7 @@ def test_decode_full_config_layer_by_layer(q8, mode):
     torch.cuda.synchronize()
     np.testing.assert_array_equal(logits.cpu().numpy(), gl)
     assert int(tok.item()) == gtok
-    print(f"mode {mode}: worst per-layer relative error {worst:.3e}; near-tie layers {flagged}")
+    print(f"mode {mode} ({form}): worst per-layer relative error {worst:.3e}; near-tie layers {flagged}")
     m.close()
 
 
