@@ -12,7 +12,7 @@
 // starts its weight stream only once its CTAs find room.  Here the weights and cache rows that do not depend on the
 // token are copied into shared memory ahead of the stage that uses them by bulk copies (`cp.async.bulk`, completion
 // counted on an mbarrier per region).  Issuing a bulk copy holds the issuing thread until the copy engine has taken
-// most of its bytes, so one warp of the CTA (the producer) does nothing else; the other 15 (the compute warps) run the
+// most of its bytes, so one warp of the CTA (the producer) does nothing else; the other 11 (the compute warps) run the
 // stages and tell the producer, through counters in shared memory, when a region is free again:
 //   - q/k/v rows of layer l+1 as soon as O of layer l is done with the region, its router rows after the router,
 //   - the cache rows of layer l+1 after the down-and-combine of layer l,
@@ -123,8 +123,6 @@ PersistLayout ps_layout(const PersistDims& d, const PersistPlan& pl) {
     b = ps_align(b + (red_in_c ? 0 : red));
     // fold scratch
     size_t f = 0;
-    L.f_m = (uint32_t)f;
-    f = ps_align(f + (size_t)PS_MAXPPG * 8);
     L.f_red = (uint32_t)f;
     f = ps_align(f + (size_t)PS_CW * 32 * 4);
     // O scratch
@@ -428,7 +426,7 @@ __device__ __forceinline__ void ps_quantize(const float (&v)[N], int8_t (&q)[N],
 
 // RMSNorm of the row a (written by other CTAs: read through L2) times w, quantized per 32-value block into the
 // activation words (and low words) and scales in shared memory; every CTA forms the same values in the same order.
-// Compute thread t holds values t + 480 j (a warp holds whole blocks); the squares are summed as f32 pairs and each y
+// Compute thread t holds values t + 352 j (a warp holds whole blocks); the squares are summed as f32 pairs and each y
 // is rounded once.  With `copy`, CTA 0 also writes the row there (and to `copy2`).
 template <int MODE, int NP>
 __device__ __noinline__ void norm_quant(const float* a, const float* w, int D, float eps, int8_t* xq, int8_t* xl, float* xs,
@@ -680,7 +678,7 @@ __device__ void fold_tail(const PersistCall& p, unsigned char* sm, PsSmall& s, i
 // ---- the stages (compute warps) -------------------------------------------------------------------------------------
 
 // A: the attention norm (layer 0: of the token's embedding row, which becomes the residual) and this CTA's q/k/v rows:
-// warp w takes rows w, w + 15, w + 30, ... three at a time, the activation blocks in registers.
+// warp w takes rows w, w + 11, w + 22, ... three at a time, the activation blocks in registers.
 template <int MODE, int BPL, int NP>
 __device__ void stage_qkv(const PersistCall& p, const PersistLayer& ly, int l, unsigned char* sm, PsSmall& s,
                           unsigned& nw) {
@@ -725,11 +723,11 @@ __device__ void stage_qkv(const PersistCall& p, const PersistLayer& ly, int l, u
 // P: this CTA's positions of its key/value head for every query head of the group.
 //   QK-norm + RoPE: warp h < G turns query head h, warp G the new key and warp G + 1 takes the new value (the CTA that
 //   holds the new position); lane l the pairs (l, l + 64) and (l + 32, l + 96).
-//   Scores: warp w takes positions w, w + 15, ...; lane (head pair l >> 3, dim group l & 7) holds its two heads' dims
+//   Scores: warp w takes positions w, w + 11, ...; lane (head pair l >> 3, dim group l & 7) holds its two heads' dims
 //   4 (l & 7) + 32 i .. + 3 (i < 4) in registers, so a key row is read once per warp, each 16-byte piece by the four
 //   lanes of a group at once; the dim groups' sums meet by shuffles.
 //   Values: warp w takes the same positions, lane l the dims 4 l .. 4 l + 3 of every head (32 sums in registers); the
-//   15 warps' sums meet in shared memory in a fixed order (warp w + 8 into warp w, then warps 0..7 in order).
+//   11 warps' sums meet in shared memory in a fixed order (warp w + 8 into warp w, then warps 0..7 in order).
 template <int MODE>
 __device__ void stage_attention(const PersistCall& p, const PersistLayer& ly, int l, int len, unsigned char* sm,
                                 PsSmall& s, unsigned& nc) {
@@ -925,7 +923,7 @@ __device__ void stage_attention(const PersistCall& p, const PersistLayer& ly, in
     }
 }
 
-// O: the attention output's words staged in shared memory, then this CTA's O rows (warp w: row w, w + 15, ...) with
+// O: the attention output's words staged in shared memory, then this CTA's O rows (warp w: row w, w + 11, ...) with
 // the residual add (in place: every CTA read the residual row before the first barrier of the layer).
 template <int MODE>
 __device__ void stage_o(const PersistCall& p, unsigned char* sm, PsSmall& s, unsigned& nw) {
@@ -1158,8 +1156,8 @@ __device__ void stage_down(const PersistCall& p, int l, unsigned char* sm, PsSma
 
 // ---- the kernel -------------------------------------------------------------------------------------------------------
 
-// grid = one CTA per SM (cooperative launch), 512 threads: warps 0..14 compute, warp 15 the producer.  BPL = 32-value
-// blocks of a d-wide row per lane (d <= 1024 BPL); NP = 480-value rounds of the residual row per compute thread.
+// grid = one CTA per SM (cooperative launch), 384 threads: warps 0..10 compute, warp 11 the producer.  BPL = 32-value
+// blocks of a d-wide row per lane (d <= 1024 BPL); NP = 352-value rounds of the residual row per compute thread.
 template <int MODE, int BPL>
 __global__ void __maxnreg__(168) decode_persistent_kernel(const __grid_constant__ PersistCall p) {
     extern __shared__ __align__(128) unsigned char sm[];

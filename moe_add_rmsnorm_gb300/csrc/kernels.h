@@ -342,7 +342,7 @@ struct PersistLayout {
     uint32_t total = 0;
     // inside u
     uint32_t b_qs = 0, b_kn = 0, b_vn = 0, b_sc = 0, b_red = 0;  // attention
-    uint32_t f_m = 0, f_red = 0;                               // fold
+    uint32_t f_red = 0;                                        // fold: the warps' sums
     uint32_t o_q = 0, o_l = 0, o_s = 0;                        // O: the attention output's words and scales
     uint32_t e_key = 0, e_val = 0;                             // routing
     uint32_t d_q = 0, d_l = 0, d_s = 0;                        // down: the hidden rows' words and scales
