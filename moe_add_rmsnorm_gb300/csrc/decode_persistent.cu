@@ -813,6 +813,7 @@ __device__ void stage_attention(const PersistCall& p, const PersistLayer& ly, in
                 q1[4 * i + 2] = b.z;
                 q1[4 * i + 3] = b.w;
             }
+#pragma unroll 2
             for (int pl = wid; pl < np; pl += PS_CW) {
                 const float* krow = (has_new && pl == np - 1) ? kn : Kc + (size_t)pl * PS_HD;
                 float s0a = 0.f, s0b = 0.f, s1a = 0.f, s1b = 0.f;
@@ -864,6 +865,7 @@ __device__ void stage_attention(const PersistCall& p, const PersistLayer& ly, in
         float4 acc[PS_MAXG];
 #pragma unroll
         for (int h = 0; h < PS_MAXG; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
         for (int pl = wid; pl < np; pl += PS_CW) {
             const float4 v4 = (has_new && pl == np - 1) ? reinterpret_cast<const float4*>(vn)[lane]
                                                         : reinterpret_cast<const float4*>(Vc + (size_t)pl * PS_HD)[lane];
