@@ -616,7 +616,8 @@ using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, 
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// The driver's tensor-map encoder, found once through the runtime (no link against the driver library).
+// The CUDA driver API's tensor-map encoder (cuTensorMapEncodeTiled), found once through the runtime's entry-point
+// lookup, so the library does not link against libcuda.
 EncodeTiled encode_tiled() {
     static const EncodeTiled fn = [] {
         void* f = nullptr;
