@@ -211,6 +211,32 @@ def test_decode_persistent_full_dims_layer_by_layer(q8, persistent, mode):
     m.close()
 
 
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("cfg", [dict(PERSIST, d=1024), dict(PERSIST, d=4096, heads=8)], ids=["d1024", "d4096"])
+def test_decode_persistent_other_widths_layer_by_layer(q8, persistent, mode, cfg):
+    """The persistent step's other row widths (the kernel's instances for d up to 1024 and up to 4096), teacher forced
+    layer by layer against the oracle, then the final norm and LM head."""
+    import torch
+    m, arr, t, tok, pos, logits = build(q8, cfg, 21, mode)
+    assert m.persistent()
+    om = oracle.ModelArrays(cfg, **arr)
+    L, P = cfg["layers"], 50
+    tok.fill_(9)
+    pos.fill_(P)
+    hidden = torch.empty(L + 1, cfg["d"], device="cuda")
+    m.step_trace(hidden)
+    torch.cuda.synchronize()
+    hid = hidden.cpu().numpy()
+    for l in range(L):
+        _, e, _ = _layer_vs_oracle(mode, om, l, P, hid[l], hid[l + 1])
+        assert e < TOL[mode], (l, e)
+        assert rel_err(t["k_cache"][l][:, P].cpu().numpy(), om.k_cache[l][:, P]) < TOL[mode]
+    nxt, ora_logits = oracle.decode_final(mode, om, hid[L])
+    assert rel_err(logits.cpu().numpy(), ora_logits) < TOL[mode]
+    m.check()
+    m.close()
+
+
 def test_decode_persistent_graph_equals_launches_bitwise(q8, persistent):
     import torch
     outs = []
