@@ -52,6 +52,9 @@ def parse():
                          "a layer (0, the library's default)")
     ap.add_argument("--tensor-core-attention", type=int, default=None, choices=[0, 1],
                     help="prefill chunks' attention on the tensor cores (1, the library's default) or CUDA cores (0)")
+    ap.add_argument("--streamed-batch-attention", type=int, default=None, metavar="B",
+                    help="batch steps of B or more sequences attend in the streamed form (0: never; the library's "
+                         "default is 8)")
     ap.add_argument("--configs-only", action="store_true",
                     help="only the single-operation configurations (projection, attention-side projections, mixture)")
     return ap.parse_args()
@@ -607,7 +610,10 @@ def time_batch(q8, cfg, dev, stream, mode, batches=(2, 4, 8, 16, 32, 64), steps=
             sec = e0.elapsed_time(e1) / 1e3 / steps
             u = E * (1.0 - (1.0 - K / E) ** B)
             wbytes = (L * (dense + u * expert) + cfg["vocab"] * d) * 9 // 8
+            # every sequence reads its key and value rows 0..pos at every layer (f32), the timed steps' mean length
+            cbytes = B * L * KV * 2 * HD * 4 * (ctx - (steps - 1) / 2)
             out.append({"batch": B, "tokens_per_s": B / sec, "ms_per_step": sec * 1e3, "weight_gbs": wbytes / sec / 1e9,
+                        "cache_gbs": cbytes / sec / 1e9, "hbm_gbs": (wbytes + cbytes) / sec / 1e9,
                         "unique_experts_per_layer_est": u, "launches_per_step": m.launches_per_step()})
             m.close()
             del t, m
@@ -647,6 +653,8 @@ def main():
         q8.set_tensor_core_attention(bool(args.tensor_core_attention))
     if args.persistent is not None:
         q8.set_persistent_decode(bool(args.persistent))
+    if args.streamed_batch_attention is not None:
+        q8.set_streamed_batch_attention(args.streamed_batch_attention)
     if args.chunk_only:
         res = time_chunks(q8, cfg, dev, sh, reps=max(1, args.steps), correlated=args.correlated,
                           rows=(args.chunk_only,))

@@ -149,6 +149,15 @@ Q8_API int q8_set_grouped_tensor_core_rows(int rows);
  * Process-wide. */
 Q8_API int q8_set_tensor_core_attention(int on);
 
+/* The fewest sequences of a batch decode step (q8_model_desc.batch) whose attention runs in the streamed form: one
+ * CTA per (split of 8 position chunks, key/value head, sequence) with a copy warp bringing its key and value rows
+ * into a ring of shared-memory stages by bulk copies while eight warps fold each stage into a running softmax; the
+ * splits of a (sequence, head) are folded in split order by the last to arrive.  Smaller batches keep the chunked form
+ * (a CTA per 64 positions, folded in clusters of 8).  Both compute qwen_emit's attention (emit_qwen30b_generate);
+ * their results differ only in summation order.  min_batch: 0 for never, else at least 2 (the default is 8).  Read
+ * when a step is launched or captured.  Process-wide. */
+Q8_API int q8_set_streamed_batch_attention(int min_batch);
+
 /* Whether a one-sequence decode step in an int8 activation mode runs its layers as one persistent launch (1) or as six
  * launches a layer (0, the default).  The persistent launch keeps one CTA on every SM for the whole step (a
  * cooperative launch), separates a layer's stages (the norm and q/k/v, the attention, its fold, O, the norm and router,

@@ -77,6 +77,7 @@ _SIGS = {
     "q8_set_grouped_tensor_core_rows": [_i32],
     "q8_set_tensor_core_attention": [_i32],
     "q8_set_persistent_decode": [_i32],
+    "q8_set_streamed_batch_attention": [_i32],
     "q8_model_persistent": [_vp],
     "moe_route_topk": [_P(q8_mat), _i32, _vp, _P(q8_act), _i64, _i32, _vp, _vp, _vp, _P(q8_moe_plan), _vp, _vp],
     "moe_route_topk_f32": [_vp, _i64, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _P(q8_moe_plan), _vp, _vp],
@@ -218,6 +219,11 @@ def set_tensor_core_attention(on: bool):
 def set_persistent_decode(on: bool):
     """One-sequence int8 decode steps as one persistent launch, or (False, the default) six launches a layer."""
     _check(lib.q8_set_persistent_decode(1 if on else 0))
+
+
+def set_streamed_batch_attention(min_batch: int):
+    """Batch decode steps of at least min_batch sequences (default 8) attend in the streamed form; 0: never."""
+    _check(lib.q8_set_streamed_batch_attention(int(min_batch)))
 
 
 def plan_struct(counts, offsets, lists, active):

@@ -16,6 +16,7 @@ namespace q8 {
 extern int kDenseMmaMinRows;    // gemv.cu
 extern int kGroupedMmaMinRows;  // moe_mma.cu
 extern int kChunkAttnTensorCores;  // decode.cu
+extern int kStreamedBatchAttention;  // decode.cu
 
 static thread_local char g_err[512];
 
@@ -525,6 +526,13 @@ int q8_set_persistent_decode(int on) {
     g_err[0] = 0;
     if (on != 0 && on != 1) return fail(Q8_EINVAL, "on %d: 0 or 1", on);
     kPersistentDecode = on;
+    return Q8_OK;
+}
+
+int q8_set_streamed_batch_attention(int min_batch) {
+    g_err[0] = 0;
+    if (min_batch != 0 && min_batch < 2) return fail(Q8_EINVAL, "min_batch %d: 0 or at least 2", min_batch);
+    kStreamedBatchAttention = min_batch;
     return Q8_OK;
 }
 

@@ -430,6 +430,328 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attention_kernel(const AttnPar
     fold_cluster(p, g, chunk, G, t);
 }
 
+// ==== the batch form's streamed attention ========================================================================
+// Many sequences, each one query row against its own cache: the (sequence, key/value head) pairs already fill the GPU,
+// so a CTA takes a long run of positions instead of one chunk and keeps the copy engine busy on it: one lane of the
+// copy warp brings each 64-position stage (its key rows, then its value rows: two contiguous bulk copies) into a ring
+// of AS_STAGES stages while the eight compute warps work on an earlier one with a running (online) softmax.  The
+// splits of a (sequence, key/value head) meet through global scratch: the last to arrive folds them in split order.
+
+constexpr int AS_CW = 8;                      // compute warps
+constexpr int AS_THREADS = (AS_CW + 1) * 32;  // + the copy warp
+constexpr int AS_SUB = 64;                    // positions per stage
+constexpr int AS_STAGES = 3;
+constexpr size_t AS_STAGE = 2 * (size_t)AS_SUB * ATT_HD * sizeof(float);  // keys, then values
+constexpr size_t AS_SMEM = AS_STAGES * AS_STAGE;
+static_assert(AS_SMEM + 12 * 1024 <= 232448, "the ring and the static arrays within a CTA's shared memory");
+static_assert((size_t)AS_CW * ATT_MAXG * ATT_HD * sizeof(float) <= AS_STAGE, "the warps' sums fit in a stage");
+
+// grid (split, key/value head, sequence).  Split j of S takes the 64-position stages [j * nch / S, (j+1) * nch / S) of
+// its sequence's nch = ceil(len / 64).  Scores: 4 lanes a position (8 float4 of the key row each, rotated by the
+// position's parity so that the 8 lanes of a shared-memory phase read 8 different bank groups), a warp 8 positions.
+// Values: warp w takes positions 8w .. 8w + 7, lane l the dimensions 4l..4l+3, the running sums rescaled by each
+// stage's change of the running maximum.
+__global__ void __launch_bounds__(AS_THREADS, 1) attention_stream_kernel(const AttnParams pk) {
+    extern __shared__ __align__(128) unsigned char as_ring[];
+    __shared__ __align__(16) float qs[ATT_MAXG][ATT_HD];
+    __shared__ __align__(16) float sc[2][ATT_MAXG][AS_SUB];
+    __shared__ float rfac[2][ATT_MAXG];
+    __shared__ float run_m[ATT_MAXG], run_l[ATT_MAXG];
+    __shared__ __align__(16) float knew[ATT_HD];
+    __shared__ __align__(16) float vnew[ATT_HD];
+    __shared__ float nred[ATT_MAXG + 1][2];
+    __shared__ __align__(8) uint64_t full[AS_STAGES], empty[AS_STAGES];
+    __shared__ int last_s;
+    const AttnParams p = attn_for_sequence(pk, blockIdx.z);
+    const int split = blockIdx.x, S = gridDim.x, g = blockIdx.y;
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int G = p.G;
+    const int len = *p.pos + 1;
+    if (len < 1 || len > p.ctx) {  // a bad position: nothing is read or written
+        griddep_wait();
+        griddep_launch();
+        if (split == 0 && g == 0 && t == 0 && p.err) atomicOr(p.err, 2);
+        return;
+    }
+    const int nch = (len + AS_SUB - 1) / AS_SUB;
+    const int c0 = split * nch / S, nst = (split + 1) * nch / S - c0;
+    const int pos = len - 1;
+    const bool has_new = nst > 0 && c0 + nst == nch;  // this split holds the last stage, whose last row is new
+    if (t == 0) {
+        for (int i = 0; i < AS_STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], AS_CW);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const float* kb = p.k_cache + (int64_t)g * p.ctx * ATT_HD;
+    const float* vb = p.v_cache + (int64_t)g * p.ctx * ATT_HD;
+    if (wid == AS_CW) {
+        // ---- the copy warp: stage i = positions 64 (c0 + i) .. of the cached rows (the new row is not read) --------
+        // The cached rows were written by earlier steps, so the first stages go out before the wait for this step's
+        // kernels.
+        if (lane == 0) {
+            bool ok = true;
+            for (int i = 0; i < nst && ok; ++i) {
+                const int slot = i % AS_STAGES;
+                if (i >= AS_STAGES) ok = mbar_wait(&empty[slot], ((i / AS_STAGES) - 1) & 1, p.err);
+                if (!ok) break;
+                const int p0 = (c0 + i) * AS_SUB;
+                int rows = min(AS_SUB, len - p0);
+                if (c0 + i == nch - 1) --rows;  // the new position is the last row
+                unsigned char* st = as_ring + (size_t)slot * AS_STAGE;
+                const unsigned rb = (unsigned)rows * ATT_HD * sizeof(float);
+                mbar_arrive_expect_tx(&full[slot], 2u * rb);
+                if (rows > 0) {
+                    bulk_g2s(st, kb + (int64_t)p0 * ATT_HD, rb, &full[slot]);
+                    bulk_g2s(st + AS_STAGE / 2, vb + (int64_t)p0 * ATT_HD, rb, &full[slot]);
+                }
+            }
+            // every copy issued has landed before the CTA may end (bounded: a stalled pipeline already set the error)
+            for (int i = max(0, nst - AS_STAGES); i < nst && ok; ++i)
+                mbar_wait(&full[i % AS_STAGES], (i / AS_STAGES) & 1, p.err);
+        }
+        griddep_wait();
+        griddep_launch();
+        __syncwarp();
+    } else {
+        griddep_wait();
+        griddep_launch();
+        // ---- QK-norm and RoPE of the group's queries (and of the new key row, in the split that holds it) ----------
+        // thread t (< 256) takes the pair (i, i + 64) of query heads t/64 and t/64 + 4, and of the key head when t < 64
+        const int hsub = t >> 6, pi = t & 63;
+        const float cs = __ldg(p.cos_t + (int64_t)pos * (ATT_HD / 2) + pi);
+        const float sn = __ldg(p.sin_t + (int64_t)pos * (ATT_HD / 2) + pi);
+        float qa[2], qb[2], ka = 0.f, kb2 = 0.f, va = 0.f, vb2 = 0.f;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int hh = hsub + 4 * u;
+            const float* src = p.q + ((int64_t)g * G + (hh < G ? hh : 0)) * ATT_HD;
+            qa[u] = hh < G ? __ldcg(src + pi) : 0.f;
+            qb[u] = hh < G ? __ldcg(src + pi + ATT_HD / 2) : 0.f;
+        }
+        if (has_new && t < 64) {
+            ka = __ldcg(p.k + (int64_t)g * ATT_HD + pi);
+            kb2 = __ldcg(p.k + (int64_t)g * ATT_HD + pi + ATT_HD / 2);
+        } else if (has_new && t < 128) {
+            va = __ldcg(p.v + (int64_t)g * ATT_HD + pi);
+            vb2 = __ldcg(p.v + (int64_t)g * ATT_HD + pi + ATT_HD / 2);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float ss = group_sum<32>(qa[u] * qa[u] + qb[u] * qb[u]);
+            if (lane == 0) nred[hsub + 4 * u][wid & 1] = ss;
+        }
+        {
+            const float ss = group_sum<32>(ka * ka + kb2 * kb2);
+            if (lane == 0 && t < 64) nred[ATT_MAXG][wid & 1] = ss;
+        }
+        if (t < ATT_MAXG) {
+            run_m[t] = -FLT_MAX;
+            run_l[t] = 0.f;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(AS_CW * 32));
+        const float qw0 = __ldg(p.q_norm + pi), qw1 = __ldg(p.q_norm + pi + ATT_HD / 2);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int hh = hsub + 4 * u;
+            if (hh < G) {
+                const float tot = (0.f + nred[hh][0]) + nred[hh][1];
+                const float inv = 1.0f / sqrtf(tot / (float)ATT_HD + p.eps);
+                const float a = qa[u] * inv * qw0, b = qb[u] * inv * qw1;
+                qs[hh][pi] = a * cs - b * sn;
+                qs[hh][pi + ATT_HD / 2] = a * sn + b * cs;
+            }
+        }
+        if (has_new) {
+            if (t < 64) {
+                const float kw0 = __ldg(p.k_norm + pi), kw1 = __ldg(p.k_norm + pi + ATT_HD / 2);
+                const float tot = (0.f + nred[ATT_MAXG][0]) + nred[ATT_MAXG][1];
+                const float inv = 1.0f / sqrtf(tot / (float)ATT_HD + p.eps);
+                const float a = ka * inv * kw0, b = kb2 * inv * kw1;
+                const float ra = a * cs - b * sn, rb = a * sn + b * cs;
+                knew[pi] = ra;
+                knew[pi + ATT_HD / 2] = rb;
+                float* kr_out = p.k_cache + ((int64_t)g * p.ctx + pos) * ATT_HD;
+                kr_out[pi] = ra;
+                kr_out[pi + ATT_HD / 2] = rb;
+            } else if (t < 128) {
+                vnew[pi] = va;
+                vnew[pi + ATT_HD / 2] = vb2;
+                float* vr_out = p.v_cache + ((int64_t)g * p.ctx + pos) * ATT_HD;
+                vr_out[pi] = va;
+                vr_out[pi + ATT_HD / 2] = vb2;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(AS_CW * 32));
+        // ---- the stages -----------------------------------------------------------------------------------------------
+        float4 acc[ATT_MAXG];
+#pragma unroll
+        for (int hh = 0; hh < ATT_MAXG; ++hh) acc[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+        bool ok = true;
+        const int sub = lane & 3;
+        for (int i = 0; i < nst; ++i) {
+            const int slot = i % AS_STAGES, b = i & 1;
+            if (ok) ok = mbar_wait(&full[slot], (i / AS_STAGES) & 1, p.err);
+            float* K = reinterpret_cast<float*>(as_ring + (size_t)slot * AS_STAGE);
+            float* V = K + AS_SUB * ATT_HD;
+            const int p0 = (c0 + i) * AS_SUB;
+            const int np = min(AS_SUB, len - p0);
+            if (c0 + i == nch - 1) {  // the new row, from this CTA's own norm and rotation
+                if (t < ATT_HD) K[(np - 1) * ATT_HD + t] = knew[t];
+                else V[(np - 1) * ATT_HD + t - ATT_HD] = vnew[t - ATT_HD];
+                asm volatile("bar.sync 1, %0;" ::"n"(AS_CW * 32));
+            }
+            // scores
+            {
+                const int pl = wid * 8 + (lane >> 2);
+                const int rot = 4 * (pl & 1);
+                float4 k4[8];
+                const float4* kr = reinterpret_cast<const float4*>(K + pl * ATT_HD);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) k4[j] = kr[(4 * j + sub + rot) & 31];
+                for (int hh = 0; hh < G; ++hh) {
+                    const float4* qv = reinterpret_cast<const float4*>(qs[hh]);
+                    float a = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 q4 = qv[(4 * j + sub + rot) & 31];
+                        a = fmaf(q4.x, k4[j].x, a);
+                        a = fmaf(q4.y, k4[j].y, a);
+                        a = fmaf(q4.z, k4[j].z, a);
+                        a = fmaf(q4.w, k4[j].w, a);
+                    }
+                    a += __shfl_xor_sync(0xffffffffu, a, 1);
+                    a += __shfl_xor_sync(0xffffffffu, a, 2);
+                    if (sub == 0 && pl < np) sc[b][hh][pl] = a * p.scale;
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(AS_CW * 32));
+            // the running softmax: warp hh takes head hh
+            if (wid < G) {
+                float m = -FLT_MAX;
+                for (int r = lane; r < np; r += 32) m = fmaxf(m, sc[b][wid][r]);
+                m = warp_max(m);
+                const float mo = run_m[wid];
+                const float mn = fmaxf(mo, m);
+                float l = 0.f;
+                for (int r = lane; r < np; r += 32) {
+                    const float e = expf(sc[b][wid][r] - mn);
+                    sc[b][wid][r] = e;
+                    l += e;
+                }
+                l = group_sum<32>(l);
+                if (lane == 0) {
+                    const float f = mo == -FLT_MAX ? 0.f : expf(mo - mn);
+                    rfac[b][wid] = f;
+                    run_l[wid] = run_l[wid] * f + l;
+                    run_m[wid] = mn;
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(AS_CW * 32));
+            // weighted values: warp w takes the 8 consecutive positions 8w.., so a head's 8 weights are two float4
+            {
+                constexpr int PW = AS_SUB / AS_CW;
+                float4 v4[PW];
+#pragma unroll
+                for (int u = 0; u < PW; ++u) {
+                    const int pl = PW * wid + u;
+                    v4[u] = pl < np ? reinterpret_cast<const float4*>(V + pl * ATT_HD)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int hh = 0; hh < ATT_MAXG; ++hh) {
+                    if (hh < G) {
+                        const float f = rfac[b][hh];
+                        float4 a = make_float4(acc[hh].x * f, acc[hh].y * f, acc[hh].z * f, acc[hh].w * f);
+                        const float4 w0 = *reinterpret_cast<const float4*>(&sc[b][hh][PW * wid]);
+                        const float4 w1 = *reinterpret_cast<const float4*>(&sc[b][hh][PW * wid + 4]);
+                        const float wv[PW] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                        for (int u = 0; u < PW; ++u) {
+                            const int pl = PW * wid + u;
+                            if (pl < np) {  // warp-uniform (a weight past np was never written)
+                                const float w = wv[u];
+                                a.x = fmaf(w, v4[u].x, a.x);
+                                a.y = fmaf(w, v4[u].y, a.y);
+                                a.z = fmaf(w, v4[u].z, a.z);
+                                a.w = fmaf(w, v4[u].w, a.w);
+                            }
+                        }
+                        acc[hh] = a;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+        // ---- this split's partial: the warps' sums meet in the first stage of the ring (every copy has been used) ----
+        asm volatile("bar.sync 1, %0;" ::"n"(AS_CW * 32));
+        float* red = reinterpret_cast<float*>(as_ring);  // [warp][head][dim]
+#pragma unroll
+        for (int hh = 0; hh < ATT_MAXG; ++hh)
+            if (hh < G) *reinterpret_cast<float4*>(red + ((size_t)wid * ATT_MAXG + hh) * ATT_HD + 4 * lane) = acc[hh];
+        asm volatile("bar.sync 1, %0;" ::"n"(AS_CW * 32));
+        const int ncl = p.ncl_max;
+        for (int i = t; i < G * ATT_HD; i += AS_CW * 32) {
+            const int hh = i / ATT_HD, dd = i % ATT_HD;
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < AS_CW; ++w) s += red[((size_t)w * ATT_MAXG + hh) * ATT_HD + dd];
+            p.part[(((int64_t)g * G + hh) * ncl + split) * (ATT_HD + 2) + dd] = s;
+        }
+        if (t < G) {
+            float* o = p.part + (((int64_t)g * G + t) * ncl + split) * (ATT_HD + 2);
+            o[ATT_HD] = nst > 0 ? run_m[t] : -FLT_MAX;
+            o[ATT_HD + 1] = run_l[t];
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(AS_CW * 32));
+        if (t == 0) last_s = atomic_add_acq_rel_gpu(p.cnt + g * G, 1) == S - 1;  // releases the partial, acquires the others'
+        asm volatile("bar.sync 1, %0;" ::"n"(AS_CW * 32));
+        if (last_s) {
+            // the fold, in split order: warp hh takes head hh, lane the dimensions lane + 32 k (k = 0..3: one 32-value
+            // block each, quantized by the warp)
+            if (wid < G) {
+                const float* base = p.part + ((int64_t)g * G + wid) * ncl * (ATT_HD + 2);
+                float M = -FLT_MAX, den = 0.f, num[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int c = 0; c < S; ++c) {
+                    const float* src = base + (int64_t)c * (ATT_HD + 2);
+                    const float mc = __ldcg(src + ATT_HD);
+                    if (mc == -FLT_MAX) continue;  // an empty split
+                    const float lc = __ldcg(src + ATT_HD + 1);
+                    float vc[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) vc[k] = __ldcg(src + lane + 32 * k);
+                    const float Mn = fmaxf(M, mc);
+                    const float r = M == -FLT_MAX ? 0.f : expf(M - Mn), f = expf(mc - Mn);
+                    den = den * r + f * lc;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) num[k] = fmaf(f, vc[k], num[k] * r);
+                    M = Mn;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float o = num[k] / den;
+                    const int64_t oi = ((int64_t)g * G + wid) * ATT_HD + lane + 32 * k;
+                    p.out[oi] = o;
+                    if (p.outq) {
+                        float dsc;
+                        if (p.outl) {
+                            int8_t lv;
+                            p.outq[oi] = quantize2_lane(o, dsc, lv);
+                            p.outl[oi] = lv;
+                        } else {
+                            p.outq[oi] = quantize_lane(o, dsc);
+                        }
+                        if (lane == 0) p.outs[oi / 32] = dsc;
+                    }
+                }
+            }
+            if (t == 0) p.cnt[g * G] = 0;
+        }
+    }
+}
+
 // ==== arg-max and advance ========================================================================================
 
 constexpr int AM_THREADS = 512;
@@ -1196,6 +1518,8 @@ __global__ void pos_add_kernel(int32_t* pos, int add, const int* err) {
 
 }  // namespace
 
+int kStreamedBatchAttention = 8;
+
 void attention_scratch(const AttnCall& c, size_t* bytes, size_t* counters) {
     const int G = c.heads / c.kv;
     const int B = c.batch > 1 ? c.batch : 1;
@@ -1253,6 +1577,18 @@ cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
+    if (B > 1 && kStreamedBatchAttention && B >= kStreamedBatchAttention) {
+        // the streamed form: splits of 8 chunks (one scratch slot each), no clusters
+        static const cudaError_t set = cudaFuncSetAttribute(attention_stream_kernel,
+                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AS_SMEM);
+        if (set != cudaSuccess) return set;
+        cfg.gridDim = dim3(p.ncl_max, c.kv, B);
+        cfg.blockDim = dim3(AS_THREADS);
+        cfg.dynamicSmemBytes = AS_SMEM;
+        cfg.attrs = attr + 1;
+        cfg.numAttrs = na - 1;
+        return cudaLaunchKernelEx(&cfg, attention_stream_kernel, p);
+    }
     return B > 1 ? cudaLaunchKernelEx(&cfg, attention_kernel<true>, p) : cudaLaunchKernelEx(&cfg, attention_kernel<false>, p);
 }
 

@@ -10,6 +10,20 @@ def rel_err(gpu, ora):
     return float(np.max(np.abs(gpu - ora)) / max(np.max(np.abs(ora)), 1e-300))
 
 
+def check_token(gpu_tok, ora_logits, tol):
+    """The greedy token against the oracle's logits.  Logits within the mode's tolerance (relative to the largest
+    magnitude) fix the arg-max only when the oracle's top two differ by more than twice that bound; inside the band
+    either of the close candidates is a correct result, so the GPU's token must then be one of them (its oracle logit
+    within the band of the top)."""
+    ora_logits = np.asarray(ora_logits, np.float64)
+    band = 2.0 * tol * float(np.max(np.abs(ora_logits)))
+    srt = np.sort(ora_logits)[::-1]
+    if srt[0] - srt[1] > band:
+        assert int(gpu_tok) == int(np.argmax(ora_logits)), (int(gpu_tok), int(np.argmax(ora_logits)))
+    else:
+        assert ora_logits[int(gpu_tok)] >= srt[0] - band, (int(gpu_tok), ora_logits[int(gpu_tok)], srt[0], band)
+
+
 def layer_vs_oracle(mode, om, l, pos, h_in, h_out, tol):
     """Layer l of the oracle from the GPU's input row h_in, against the GPU's output row h_out (the row and its
     increment).  In the one-word mode each word of an activation decides by rounding x/d; where that value lies within

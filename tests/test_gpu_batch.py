@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synth
-from layer_parity import layer_vs_oracle
+from layer_parity import check_token, layer_vs_oracle
 from synth import recipes
 
 pytestmark = pytest.mark.gpu
@@ -102,9 +102,7 @@ def _steps_vs_oracle(q8, cfg, B, mode, toks, poss, steps, seed, variants=None):
                     forked.add(b)
                 else:
                     assert rel_err(gl[b], ora) < TOL[mode], (step, b, rel_err(gl[b], ora))
-                    srt = np.sort(ora)[::-1]
-                    if srt[0] - srt[1] > 1e-5 * abs(srt[0]):
-                        assert gt[b] == nxt
+                    check_token(gt[b], ora, TOL[mode])
                     for l in range(cfg["layers"]):
                         kcb = t["k_cache"][l][b].cpu().numpy()
                         vcb = t["v_cache"][l][b].cpu().numpy()
@@ -116,12 +114,31 @@ def _steps_vs_oracle(q8, cfg, B, mode, toks, poss, steps, seed, variants=None):
     return m
 
 
+@pytest.fixture(params=["chunked", "streamed"])
+def attn_form(q8, request):
+    """The batch attention's two forms: chunks folded in clusters, or splits streamed through a copy ring (forced for
+    every batch size here)."""
+    q8.set_streamed_batch_attention(0 if request.param == "chunked" else 2)
+    yield request.param
+    q8.set_streamed_batch_attention(8)
+
+
 @pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("B", [2, 5])
-def test_batch_step_equals_independent_steps(q8, mode, B):
+def test_batch_step_equals_independent_steps(q8, mode, B, attn_form):
     toks = [3, 500, 77, 999, 12][:B]
     poss = [10, 63, 0, 94, 40][:B]  # different lengths, from one row to the cache's end
     m = _steps_vs_oracle(q8, SMALL, B, mode, toks, poss, 2 if max(poss) >= 94 else 3, 41)
+    m.close()
+
+
+@pytest.mark.parametrize("mode", [1, 0])
+def test_batch_long_caches_split_over_positions(q8, mode, attn_form):
+    """Caches of 1536 rows: the streamed form cuts each (sequence, head) into three splits of eight 64-position stages,
+    so one row, a stage exactly, a stage boundary, several splits (some empty at short lengths) and the cache's
+    last rows all occur; the chunked form folds up to three clusters."""
+    cfg = dict(SMALL, ctx=1536)
+    m = _steps_vs_oracle(q8, cfg, 5, mode, [3, 500, 77, 999, 12], [0, 63, 64, 700, 1534], 2, 48)
     m.close()
 
 
@@ -232,7 +249,7 @@ def test_batch_32_sequences_layer_by_layer(q8):
     m.close()
 
 
-def test_batch_graph_equals_launches_bitwise(q8):
+def test_batch_graph_equals_launches_bitwise(q8, attn_form):
     import torch
     outs = []
     for use_graph in (True, False):
@@ -248,7 +265,7 @@ def test_batch_graph_equals_launches_bitwise(q8):
         np.testing.assert_array_equal(a, b)
 
 
-def test_batch_bad_position_is_flagged_and_nothing_advances(q8):
+def test_batch_bad_position_is_flagged_and_nothing_advances(q8, attn_form):
     import torch
     m, oms, t, tok, pos, logits = _batch_model(q8, SMALL, 3, 45, 0)
     tok.copy_(torch.tensor([1, 2, 3], dtype=torch.int32))

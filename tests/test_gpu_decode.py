@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 import oracle
-from layer_parity import layer_vs_oracle
+from layer_parity import check_token, layer_vs_oracle
 from synth import recipes
 
 pytestmark = pytest.mark.gpu
@@ -67,9 +67,7 @@ def test_decode_small_matches_oracle_over_steps(q8, mode, cfg, launches):
         torch.cuda.synchronize()
         gl = logits.cpu().numpy()
         assert rel_err(gl, ora_logits) < TOL[mode], (step, rel_err(gl, ora_logits))
-        srt = np.sort(ora_logits)[::-1]
-        if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
-            assert int(tok.item()) == nxt
+        check_token(int(tok.item()), ora_logits, TOL[mode])
         assert int(pos.item()) == cur_pos + 1
         # the step wrote its key/value rows at cur_pos
         for l in range(cfg["layers"]):
@@ -128,9 +126,7 @@ def test_decode_persistent_matches_oracle_over_steps(q8, persistent, mode):
         nxt, ora_logits = oracle.decode_final(mode, om, hid[L])
         gl = logits.cpu().numpy()
         assert rel_err(gl, ora_logits) < TOL[mode], (step, rel_err(gl, ora_logits))
-        srt = np.sort(ora_logits)[::-1]
-        if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
-            assert int(tok.item()) == nxt
+        check_token(int(tok.item()), ora_logits, TOL[mode])
         assert int(pos.item()) == cur_pos + 1
         cur_tok, cur_pos = int(tok.item()), cur_pos + 1
     m.step()  # the captured graph: the layers, the LM head (+final norm), the arg-max
@@ -375,9 +371,7 @@ def test_decode_full_dims_eight_layers(q8, mode):
     gl = logits.cpu().numpy()
     err = rel_err(gl, ora_logits)
     assert err < TOL[mode], err
-    srt = np.sort(ora_logits)[::-1]
-    if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
-        assert int(tok.item()) == nxt
+    check_token(int(tok.item()), ora_logits, TOL[mode])
     for l in range(cfg["layers"]):
         assert rel_err(t["k_cache"][l].cpu().numpy()[:, -1], om.k_cache[l][:, -1]) < TOL[mode]
     m.close()
@@ -441,9 +435,7 @@ def _full_config_layer_by_layer(q8, mode, form):
     assert len(flagged) <= 2, flagged
     nxt, ora_logits = oracle.decode_final(mode, om, hid[L])
     assert rel_err(gl, ora_logits) < TOL[mode], rel_err(gl, ora_logits)
-    srt = np.sort(ora_logits)[::-1]
-    if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
-        assert gtok == nxt
+    check_token(gtok, ora_logits, TOL[mode])
     # the captured graph (what the benchmark replays) computes the same step bit for bit
     tok.fill_(0)
     pos.fill_(P)
@@ -475,9 +467,7 @@ def _prefill_vs_oracle(q8, cfg, mode, R, pos0, tokens, seed, cache_layers=None):
         nxt, ora_logits = oracle.decode_step(mode, om, tk, pos0 + r)
     gl = logits.cpu().numpy()
     assert rel_err(gl, ora_logits) < TOL[mode], rel_err(gl, ora_logits)
-    srt = np.sort(ora_logits)[::-1]
-    if srt[0] - srt[1] > 1e-5 * np.abs(srt[0]):
-        assert int(tok.item()) == nxt
+    check_token(int(tok.item()), ora_logits, TOL[mode])
     assert int(pos.item()) == pos0 + R
     for l in (range(cfg["layers"]) if cache_layers is None else cache_layers):  # every row's key and value
         kc, vc = t["k_cache"][l].cpu().numpy(), t["v_cache"][l].cpu().numpy()

@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -92,6 +93,10 @@ def test_on_off_switches_refuse_other_values(q8):
     assert lib.q8_set_persistent_decode(0) == 0  # the default again
     assert lib.q8_set_tensor_core_attention(1) == 0  # the default again
     assert lib.q8_model_persistent(None) == 0
+    for bad in (-1, 1):
+        assert lib.q8_set_streamed_batch_attention(bad) == -1
+        assert "0 or at least 2" in q8.last_error()
+    assert lib.q8_set_streamed_batch_attention(8) == 0  # the default again
 
 
 _RANK = r"""
@@ -127,4 +132,19 @@ def test_replicas_report_the_slowest_rank():
     for r in res:
         assert r["sec"] == 0.8
         assert abs(r["rate"] - 2 * 10 / 0.8) < 1e-12
+
+
+def test_token_check_follows_the_tolerance():
+    """The GPU tests' greedy-token check: outside the tolerance band the token must be the oracle's arg-max; inside it
+    (the top two closer than the logits' error bound allows to separate) either close candidate passes, and nothing
+    else does."""
+    from layer_parity import check_token
+    lg = np.array([10.0, 9.99, 0.0, -3.0])  # top two 0.01 apart; the band at 2e-3 is 2 * 2e-3 * 10 = 0.04
+    check_token(0, lg, 2e-3)
+    check_token(1, lg, 2e-3)
+    with pytest.raises(AssertionError):
+        check_token(2, lg, 2e-3)
+    with pytest.raises(AssertionError):
+        check_token(1, lg, 1e-4)  # band 2e-3 < 0.01: the gap decides
+    check_token(0, lg, 1e-4)
 
