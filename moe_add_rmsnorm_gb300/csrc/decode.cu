@@ -433,25 +433,29 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attention_kernel(const AttnPar
 // ==== the batch form's streamed attention ========================================================================
 // Many sequences, each one query row against its own cache: the (sequence, key/value head) pairs already fill the GPU,
 // so a CTA takes a long run of positions instead of one chunk and keeps the copy engine busy on it: one lane of the
-// copy warp brings each 64-position stage (its key rows, then its value rows: two contiguous bulk copies) into a ring
-// of AS_STAGES stages while the eight compute warps work on an earlier one with a running (online) softmax.  The
+// copy warp brings each stage of AS_SUB positions (its key rows, then its value rows: two contiguous bulk copies) into
+// a ring of AS_STAGES stages while the eight compute warps work on an earlier one with a running (online) softmax.  The
 // splits of a (sequence, key/value head) meet through global scratch: the last to arrive folds them in split order.
 
 constexpr int AS_CW = 8;                      // compute warps
 constexpr int AS_THREADS = (AS_CW + 1) * 32;  // + the copy warp
-constexpr int AS_SUB = 64;                    // positions per stage
-constexpr int AS_STAGES = 3;
+constexpr int AS_SUB = 32;                    // positions per stage
+constexpr int AS_STAGES = 3;                  // (two CTAs an SM: one's start and end overlap the other's stream)
+constexpr int AS_PPW = AS_SUB / AS_CW;        // positions a warp takes in a stage
+constexpr int AS_LP = 32 / AS_PPW;            // lanes a position's score takes
+constexpr int AS_FL = ATT_HD / 4 / AS_LP;     // float4 of the key row a lane takes
+static_assert(AS_PPW % 4 == 0 && AS_LP <= 8, "whole float4 of weights; 8 lanes at most per position");
 constexpr size_t AS_STAGE = 2 * (size_t)AS_SUB * ATT_HD * sizeof(float);  // keys, then values
 constexpr size_t AS_SMEM = AS_STAGES * AS_STAGE;
-static_assert(AS_SMEM + 12 * 1024 <= 232448, "the ring and the static arrays within a CTA's shared memory");
+static_assert(2 * (AS_SMEM + 12 * 1024) <= 232448, "two CTAs' rings and static arrays within an SM's shared memory");
 static_assert((size_t)AS_CW * ATT_MAXG * ATT_HD * sizeof(float) <= AS_STAGE, "the warps' sums fit in a stage");
 
-// grid (split, key/value head, sequence).  Split j of S takes the 64-position stages [j * nch / S, (j+1) * nch / S) of
-// its sequence's nch = ceil(len / 64).  Scores: 4 lanes a position (8 float4 of the key row each, rotated by the
-// position's parity so that the 8 lanes of a shared-memory phase read 8 different bank groups), a warp 8 positions.
-// Values: warp w takes positions 8w .. 8w + 7, lane l the dimensions 4l..4l+3, the running sums rescaled by each
-// stage's change of the running maximum.
-__global__ void __launch_bounds__(AS_THREADS, 1) attention_stream_kernel(const AttnParams pk) {
+// grid (split, key/value head, sequence).  Split j of S takes the stages [j * nch / S, (j+1) * nch / S) of its
+// sequence's nch = ceil(len / AS_SUB).  Scores: AS_LP lanes a position, lane s of them the float4 s, s + AS_LP, ... of
+// the key row (with 4 lanes a position rotated by the position's parity), so that the 8 lanes of a shared-memory phase
+// read 8 different bank groups; a warp AS_PPW positions.  Values: warp w takes positions AS_PPW w .., lane l the
+// dimensions 4l..4l+3, the running sums rescaled by each stage's change of the running maximum.
+__global__ void __launch_bounds__(AS_THREADS, 2) attention_stream_kernel(const AttnParams pk) {
     extern __shared__ __align__(128) unsigned char as_ring[];
     __shared__ __align__(16) float qs[ATT_MAXG][ATT_HD];
     __shared__ __align__(16) float sc[2][ATT_MAXG][AS_SUB];
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(AS_THREADS, 1) attention_stream_kernel(const A
 #pragma unroll
         for (int hh = 0; hh < ATT_MAXG; ++hh) acc[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
         bool ok = true;
-        const int sub = lane & 3;
+        const int sub = lane & (AS_LP - 1);
         for (int i = 0; i < nst; ++i) {
             const int slot = i % AS_STAGES, b = i & 1;
             if (ok) ok = mbar_wait(&full[slot], (i / AS_STAGES) & 1, p.err);
@@ -605,25 +609,25 @@ __global__ void __launch_bounds__(AS_THREADS, 1) attention_stream_kernel(const A
             }
             // scores
             {
-                const int pl = wid * 8 + (lane >> 2);
-                const int rot = 4 * (pl & 1);
-                float4 k4[8];
+                const int pl = wid * AS_PPW + lane / AS_LP;
+                const int rot = AS_LP < 8 ? AS_LP * (pl & 1) : 0;
+                float4 k4[AS_FL];
                 const float4* kr = reinterpret_cast<const float4*>(K + pl * ATT_HD);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) k4[j] = kr[(4 * j + sub + rot) & 31];
+                for (int j = 0; j < AS_FL; ++j) k4[j] = kr[(AS_LP * j + sub + rot) & 31];
                 for (int hh = 0; hh < G; ++hh) {
                     const float4* qv = reinterpret_cast<const float4*>(qs[hh]);
                     float a = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float4 q4 = qv[(4 * j + sub + rot) & 31];
+                    for (int j = 0; j < AS_FL; ++j) {
+                        const float4 q4 = qv[(AS_LP * j + sub + rot) & 31];
                         a = fmaf(q4.x, k4[j].x, a);
                         a = fmaf(q4.y, k4[j].y, a);
                         a = fmaf(q4.z, k4[j].z, a);
                         a = fmaf(q4.w, k4[j].w, a);
                     }
-                    a += __shfl_xor_sync(0xffffffffu, a, 1);
-                    a += __shfl_xor_sync(0xffffffffu, a, 2);
+#pragma unroll
+                    for (int o = 1; o < AS_LP; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
                     if (sub == 0 && pl < np) sc[b][hh][pl] = a * p.scale;
                 }
             }
@@ -650,9 +654,9 @@ __global__ void __launch_bounds__(AS_THREADS, 1) attention_stream_kernel(const A
                 }
             }
             asm volatile("bar.sync 1, %0;" ::"n"(AS_CW * 32));
-            // weighted values: warp w takes the 8 consecutive positions 8w.., so a head's 8 weights are two float4
+            // weighted values: warp w takes the consecutive positions AS_PPW w .., so a head's weights are whole float4
             {
-                constexpr int PW = AS_SUB / AS_CW;
+                constexpr int PW = AS_PPW;
                 float4 v4[PW];
 #pragma unroll
                 for (int u = 0; u < PW; ++u) {
@@ -664,9 +668,15 @@ __global__ void __launch_bounds__(AS_THREADS, 1) attention_stream_kernel(const A
                     if (hh < G) {
                         const float f = rfac[b][hh];
                         float4 a = make_float4(acc[hh].x * f, acc[hh].y * f, acc[hh].z * f, acc[hh].w * f);
-                        const float4 w0 = *reinterpret_cast<const float4*>(&sc[b][hh][PW * wid]);
-                        const float4 w1 = *reinterpret_cast<const float4*>(&sc[b][hh][PW * wid + 4]);
-                        const float wv[PW] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        float wv[PW];
+#pragma unroll
+                        for (int f4 = 0; f4 < PW / 4; ++f4) {
+                            const float4 w4 = *reinterpret_cast<const float4*>(&sc[b][hh][PW * wid + 4 * f4]);
+                            wv[4 * f4] = w4.x;
+                            wv[4 * f4 + 1] = w4.y;
+                            wv[4 * f4 + 2] = w4.z;
+                            wv[4 * f4 + 3] = w4.w;
+                        }
 #pragma unroll
                         for (int u = 0; u < PW; ++u) {
                             const int pl = PW * wid + u;
