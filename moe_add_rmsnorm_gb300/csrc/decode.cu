@@ -615,21 +615,31 @@ __global__ void __launch_bounds__(AS_THREADS, 2) attention_stream_kernel(const A
                 const float4* kr = reinterpret_cast<const float4*>(K + pl * ATT_HD);
 #pragma unroll
                 for (int j = 0; j < AS_FL; ++j) k4[j] = kr[(AS_LP * j + sub + rot) & 31];
-                for (int hh = 0; hh < G; ++hh) {
-                    const float4* qv = reinterpret_cast<const float4*>(qs[hh]);
-                    float a = 0.f;
+                // every head's partial dot first, then their lane sums side by side (independent chains)
+                float a[ATT_MAXG];
 #pragma unroll
-                    for (int j = 0; j < AS_FL; ++j) {
-                        const float4 q4 = qv[(AS_LP * j + sub + rot) & 31];
-                        a = fmaf(q4.x, k4[j].x, a);
-                        a = fmaf(q4.y, k4[j].y, a);
-                        a = fmaf(q4.z, k4[j].z, a);
-                        a = fmaf(q4.w, k4[j].w, a);
+                for (int hh = 0; hh < ATT_MAXG; ++hh) {
+                    a[hh] = 0.f;
+                    if (hh < G) {  // uniform
+                        const float4* qv = reinterpret_cast<const float4*>(qs[hh]);
+#pragma unroll
+                        for (int j = 0; j < AS_FL; ++j) {
+                            const float4 q4 = qv[(AS_LP * j + sub + rot) & 31];
+                            a[hh] = fmaf(q4.x, k4[j].x, a[hh]);
+                            a[hh] = fmaf(q4.y, k4[j].y, a[hh]);
+                            a[hh] = fmaf(q4.z, k4[j].z, a[hh]);
+                            a[hh] = fmaf(q4.w, k4[j].w, a[hh]);
+                        }
                     }
-#pragma unroll
-                    for (int o = 1; o < AS_LP; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-                    if (sub == 0 && pl < np) sc[b][hh][pl] = a * p.scale;
                 }
+#pragma unroll
+                for (int o = 1; o < AS_LP; o <<= 1)
+#pragma unroll
+                    for (int hh = 0; hh < ATT_MAXG; ++hh) a[hh] += __shfl_xor_sync(0xffffffffu, a[hh], o);
+                if (sub == 0 && pl < np)
+#pragma unroll
+                    for (int hh = 0; hh < ATT_MAXG; ++hh)
+                        if (hh < G) sc[b][hh][pl] = a[hh] * p.scale;
             }
             asm volatile("bar.sync 1, %0;" ::"n"(AS_CW * 32));
             // the running softmax: warp hh takes head hh
