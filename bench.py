@@ -818,7 +818,7 @@ def main():
                 finally:
                     q8.set_persistent_decode(bool(args.persistent))
             line["batch"] = {"what": "the batch form: B sequences per step, every weight read once for all of them, "
-                                     "one CUDA graph per step, int8 mode", "results": time_batch(q8, cfg, dev, sh, mode)}
+                                     "one CUDA graph per step, int8 mode; the attention streamed from 8 sequences", "results": time_batch(q8, cfg, dev, sh, mode)}
             line["prefill"] = {"what": "prefill_chunk through all layers (plain launches), positions ctx-128-R ..",
                                "results": time_prefill(q8, model, cfg, tok, pos, sh)}
             line["chunks"] = {

@@ -17,7 +17,9 @@
 // 48 KiB static score row of the pages' design is not needed: a chunk's scores live in shared memory and any cache
 // length works.  Every CTA norms and turns its group's query heads itself (a few hundred values), so no launch sits
 // between the projection and the attention; the CTA whose chunk holds the new position also norms and turns the new
-// key row and writes it and the value row to the caches.
+// key row and writes it and the value row to the caches.  Batches of many sequences attend in a streamed form instead
+// (attention_stream_kernel): a CTA takes a long run of one sequence's positions and streams its rows through a ring of
+// bulk copies with a running softmax, since the (sequence, head) pairs already fill the GPU.
 #include <float.h>
 
 #include <cooperative_groups.h>
