@@ -494,12 +494,13 @@ __global__ void __launch_bounds__(AS_THREADS, 2) attention_stream_kernel(const A
     const float* kb = p.k_cache + (int64_t)g * p.ctx * ATT_HD;
     const float* vb = p.v_cache + (int64_t)g * p.ctx * ATT_HD;
     if (wid == AS_CW) {
-        // ---- the copy warp: stage i = positions 64 (c0 + i) .. of the cached rows (the new row is not read) --------
+        // ---- the copy warp: stage i = positions AS_SUB (c0 + i) .. of the cached rows (the new row is not read) ----
         // The cached rows were written by earlier steps, so the first stages go out before the wait for this step's
         // kernels.
         if (lane == 0) {
             bool ok = true;
-            for (int i = 0; i < nst && ok; ++i) {
+            int issued = 0;
+            for (int i = 0; i < nst && ok; ++i, ++issued) {
                 const int slot = i % AS_STAGES;
                 if (i >= AS_STAGES) ok = mbar_wait(&empty[slot], ((i / AS_STAGES) - 1) & 1, p.err);
                 if (!ok) break;
@@ -514,8 +515,8 @@ __global__ void __launch_bounds__(AS_THREADS, 2) attention_stream_kernel(const A
                     bulk_g2s(st + AS_STAGE / 2, vb + (int64_t)p0 * ATT_HD, rb, &full[slot]);
                 }
             }
-            // every copy issued has landed before the CTA may end (bounded: a stalled pipeline already set the error)
-            for (int i = max(0, nst - AS_STAGES); i < nst && ok; ++i)
+            // every copy issued has landed before the CTA may end, after a timed-out wait too (each wait bounded)
+            for (int i = max(0, issued - AS_STAGES); i < issued; ++i)
                 mbar_wait(&full[i % AS_STAGES], (i / AS_STAGES) & 1, p.err);
         }
         griddep_wait();
