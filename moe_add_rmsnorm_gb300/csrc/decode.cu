@@ -791,6 +791,15 @@ __global__ void __launch_bounds__(AM_THREADS) argmax_kernel(const float* __restr
     __shared__ int last;
     issue_l2_prefetch(pf);
     griddep_wait();
+    {  // row blockIdx.y of a batch: its logits, scratch, counter, token and position
+        const int row = blockIdx.y;
+        x += (int64_t)row * n;
+        bv_out += (int64_t)row * gridDim.x;
+        bi_out += (int64_t)row * gridDim.x;
+        cnt += row;
+        tok += row;
+        if (pos) pos += row;
+    }
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     float bv = -FLT_MAX;
     int bi = -1;
@@ -1616,18 +1625,21 @@ cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
 }
 
 void argmax_scratch(const ArgmaxCall& c, size_t* bytes, size_t* counters) {
-    *bytes = (size_t)argmax_blocks(c.n) * 8 + 256;
-    *counters = 1;
+    const int rows = c.rows > 1 ? c.rows : 1;
+    *bytes = (size_t)argmax_blocks(c.n) * 8 * rows + 256;
+    *counters = rows;
 }
 
 cudaError_t launch_argmax(const ArgmaxCall& c, Carve& ws, cudaStream_t st) {
     const int blocks = argmax_blocks(c.n);
-    float* bv = ws.take<float>(blocks);
-    int* bi = ws.take<int>(blocks);
-    int* cnt = ws.take_counters(1);
+    const int rows = c.rows > 1 ? c.rows : 1;
+    if (rows > 65535) return cudaErrorInvalidValue;
+    float* bv = ws.take<float>((size_t)blocks * rows);
+    int* bi = ws.take<int>((size_t)blocks * rows);
+    int* cnt = ws.take_counters(rows);
     if (ws.overflow) return cudaErrorMemoryAllocation;
-    return launch(argmax_kernel, dim3(blocks), dim3(AM_THREADS), 0, st, c.pdl, c.x, c.n, bv, bi, cnt, c.tok, c.pos,
-                  c.err, c.ctx, c.pf);
+    return launch(argmax_kernel, dim3(blocks, rows), dim3(AM_THREADS), 0, st, c.pdl, c.x, c.n, bv, bi, cnt, c.tok,
+                  c.pos, c.err, c.ctx, c.pf);
 }
 
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int ctx, int half, double theta, cudaStream_t st) {

@@ -277,6 +277,7 @@ struct ArgmaxCall {
     int32_t* pos = nullptr;     // incremented (when not null)
     const int* err = nullptr;   // when set and non-zero, tok and pos are left unchanged
     int ctx = 0;                // with pos: a position outside [0, ctx) leaves tok and pos unchanged
+    int rows = 1;               // a batch: rows of n logits (row r at x + r * n), each with its own tok[r] and pos[r]
     L2Prefetch pf;                       // weights of later launches to fetch into L2 at the start
     int pdl = 0;
 };

@@ -670,14 +670,15 @@ cudaError_t batch_step_launches(q8_model* m, cudaStream_t st, float* trace = nul
         Carve cv = fresh_carve(m);
         Q8_TRY(launch_gemv(g, cv, st));
     }
-    for (int64_t b = 0; b < B; ++b) {
+    {  // every sequence's arg-max in one launch (a row of CTAs per sequence)
         ArgmaxCall a;
-        a.x = m->logits + b * d.vocab;
+        a.x = m->logits;
         a.n = d.vocab;
-        a.tok = d.tok + b;
-        a.pos = d.pos + b;
+        a.tok = d.tok;
+        a.pos = d.pos;
         a.err = m->err;
         a.ctx = (int)d.ctx;
+        a.rows = (int)B;
         a.pdl = m->pdl;
         Carve cv = fresh_carve(m);
         Q8_TRY(launch_argmax(a, cv, st));
