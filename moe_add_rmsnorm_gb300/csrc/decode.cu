@@ -1610,7 +1610,8 @@ cudaError_t launch_attention(const AttnCall& c, Carve& ws, cudaStream_t st) {
     cfg.attrs = attr;
     cfg.numAttrs = na;
     if (B > 1 && kStreamedBatchAttention && B >= kStreamedBatchAttention) {
-        // the streamed form: splits of 8 chunks (one scratch slot each), no clusters
+        // the streamed form: as many splits of the positions as the chunked form has clusters of 8 chunks (one scratch
+        // slot each), no clusters
         static const cudaError_t set = cudaFuncSetAttribute(attention_stream_kernel,
                                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AS_SMEM);
         if (set != cudaSuccess) return set;
